@@ -1,0 +1,467 @@
+/*
+ * qd_oracle.c — the plain, slow CPU oracle for the quantized decode path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this code.  It shares no code, header,
+ * table or constant with the CUDA library: it is written from the pages'
+ * statement of each operation, and computes the plain definition of each one:
+ * every block is dequantised to f32, and every dot product, norm, softmax and
+ * weighted sum is accumulated in double, in index order.  The only
+ * parallelism is OpenMP over independent outputs (matrix rows, attention
+ * heads), which does not change any output's summation order.
+ *
+ * Sources (the five pages on quantized decode GEMV):
+ *  [llmoxide]  "Running an LLM, then forgetting it" (llmoxide blog):
+ *              s1 "A neuron is a dot product", s2 "Layers, and the bend
+ *              between them", s3 "Text in, vectors out", s4 "Keeping the numbers
+ *              in range", s5 "Attention", s6 "Where things are: RoPE", s7 "The
+ *              block, and the residual stream", s10 "Loading weights", s12 "The
+ *              KV cache".
+ *  [go-llm]    "llm" Go package documentation (go-wasmcontainers/llm v0.1.0):
+ *              "Design points", "Oracle tolerances", index entries Argmax,
+ *              F16ToF32.
+ *  [llamini]   "Building llamini.cpp: a from-scratch llama.cpp core in C99",
+ *              section "What I reimplemented" (the Q4_K 6-bit scale unpacker).
+ *  [dasLLAMA]  "dasLLAMA-00 - The Problem Statement", 8.7.1.4 "Five small
+ *              functions", 8.7.1.6.2 "Attention", 8.7.1.6.3 "Feed-forward",
+ *              8.7.1.6.4 "Logits", 8.7.1.7 "Prompting is repeated forward".
+ *  [minillm]   minillm-cpp README: "Loader" (BF16 zero-extension), "NEON
+ *              kernels" and "Quantization" (per-row symmetric INT8).
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - Q4_0 block: f16 d at byte 0, then 16 code bytes; element j (0..15) is the
+ *    low nibble of code byte j and element j+16 its high nibble; value (q-8)*d.
+ *  - Q4_K super-block: d, dmin (f16), 12 scale bytes, 128 code bytes; code
+ *    chunk c (0..3) is bytes 32c..32c+31, whose low nibbles are sub-block 2c
+ *    (elements 64c..64c+31) and high nibbles sub-block 2c+1 (elements
+ *    64c+32..64c+63); value d*sc*q - dmin*m.
+ *  - per-row INT8 tensor bytes: int8 codes [rows][cols], then f32 scale[rows].
+ *  - RoPE angle for pair i at position p: p * theta^(-2i/hd), in double.
+ *
+ * Portable C99 + optional OpenMP; no architecture intrinsics.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_Q4_0 = 0, OR_Q8_0 = 1, OR_Q4_K = 2, OR_I8_ROW = 3 };
+enum { OR_ROPE_ADJACENT = 0, OR_ROPE_HALF = 1 };
+
+/* ------------------------------------------------------------------------- */
+/* Scalar formats                                                             */
+/* ------------------------------------------------------------------------- */
+
+/* IEEE 754 binary16 -> double, exactly ([go-llm] index, F16ToF32: "converts an
+ * IEEE binary16 value, exactly").  Written from the format's definition:
+ * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double or_f16_to_f64(uint16_t h) {
+    const int sign = (h >> 15) & 1;
+    const int e = (h >> 10) & 0x1F;
+    const int f = h & 0x3FF;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24); /* zero or subnormal: f * 2^-14 / 1024 */
+    } else if (e == 31) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp(1.0 + (double)f / 1024.0, e - 15);
+    }
+    return sign ? -v : v;
+}
+
+/* BF16 -> f32 by zero-extension of the bit pattern ([minillm] "Loader"). */
+float or_bf16_to_f32(uint16_t b) {
+    uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return f;
+}
+
+/* Array form of the two conversions, writing f32 bit patterns (keeps NaN payloads). */
+void or_bf16_to_f32_array(const uint16_t* in, int64_t n, float* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = or_bf16_to_f32(in[i]);
+}
+
+void or_f16_to_f32_array(const uint16_t* in, int64_t n, float* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = (float)or_f16_to_f64(in[i]);
+}
+
+static double f16_at(const uint8_t* p) { return or_f16_to_f64((uint16_t)(p[0] | (p[1] << 8))); }
+
+/* ------------------------------------------------------------------------- */
+/* Block dequantisation ([llmoxide] s10 "Loading weights"; [llamini])         */
+/* ------------------------------------------------------------------------- */
+
+/* The Q4_K 12-byte field holds eight 6-bit (scale, min) pairs.  Sub-blocks 0-3
+ * keep theirs in the low six bits of bytes j and j+4; sub-blocks 4-7 take their
+ * low four bits from byte j+4 (scale: low nibble, min: high nibble) and their
+ * top two bits from the spare top bits of bytes j-4 (scale) and j (min).
+ * ([llamini] "What I reimplemented", the get_scale_min_k4 unpacker.) */
+void or_get_scale_min_k4(int j, const uint8_t* q, uint8_t* sc, uint8_t* m) {
+    if (j < 4) {
+        *sc = q[j] & 63;
+        *m = q[j + 4] & 63;
+    } else {
+        *sc = (uint8_t)((q[j + 4] & 0x0F) | ((q[j - 4] >> 6) << 4));
+        *m = (uint8_t)((q[j + 4] >> 4) | ((q[j] >> 6) << 4));
+    }
+}
+
+static int64_t row_bytes(int fmt, int64_t cols) {
+    switch (fmt) {
+        case OR_Q4_0: return (cols / 32) * 18;
+        case OR_Q8_0: return (cols / 32) * 34;
+        case OR_Q4_K: return (cols / 256) * 144;
+        case OR_I8_ROW: return cols;
+        default: return -1;
+    }
+}
+
+int or_shape_ok(int fmt, int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0) return 0;
+    switch (fmt) {
+        case OR_Q4_0:
+        case OR_Q8_0: return cols % 32 == 0;
+        case OR_Q4_K: return cols % 256 == 0;
+        case OR_I8_ROW: return 1;
+        default: return 0;
+    }
+}
+
+/* Dequantise row r of a rows x cols tensor (model-file layout) into out[cols],
+ * each value rounded once to f32. */
+static void dequant_row(int fmt, const uint8_t* w, int64_t rows, int64_t cols, int64_t r, float* out) {
+    const uint8_t* row = w + r * row_bytes(fmt, cols);
+    if (fmt == OR_Q4_0) {
+        for (int64_t b = 0; b < cols / 32; ++b) {
+            const uint8_t* blk = row + b * 18;
+            const double d = f16_at(blk);
+            for (int j = 0; j < 16; ++j) {
+                const int lo = blk[2 + j] & 0x0F, hi = blk[2 + j] >> 4;
+                out[b * 32 + j] = (float)((lo - 8) * d);
+                out[b * 32 + j + 16] = (float)((hi - 8) * d);
+            }
+        }
+    } else if (fmt == OR_Q8_0) {
+        /* [llmoxide] s10: d = f16 at byte 0, 32 signed bytes follow. */
+        for (int64_t b = 0; b < cols / 32; ++b) {
+            const uint8_t* blk = row + b * 34;
+            const double d = f16_at(blk);
+            for (int j = 0; j < 32; ++j) out[b * 32 + j] = (float)((int8_t)blk[2 + j] * d);
+        }
+    } else if (fmt == OR_Q4_K) {
+        for (int64_t s = 0; s < cols / 256; ++s) {
+            const uint8_t* blk = row + s * 144;
+            const double d = f16_at(blk), dmin = f16_at(blk + 2);
+            const uint8_t* scales = blk + 4;
+            const uint8_t* qs = blk + 16;
+            for (int c = 0; c < 4; ++c) {
+                uint8_t sc0, m0, sc1, m1;
+                or_get_scale_min_k4(2 * c, scales, &sc0, &m0);
+                or_get_scale_min_k4(2 * c + 1, scales, &sc1, &m1);
+                for (int l = 0; l < 32; ++l) {
+                    const int lo = qs[32 * c + l] & 0x0F, hi = qs[32 * c + l] >> 4;
+                    out[s * 256 + 64 * c + l] = (float)(d * sc0 * lo - dmin * m0);
+                    out[s * 256 + 64 * c + 32 + l] = (float)(d * sc1 * hi - dmin * m1);
+                }
+            }
+        }
+    } else { /* OR_I8_ROW ([minillm] "Quantization": one scale per output row) */
+        float s;
+        memcpy(&s, w + rows * cols + 4 * r, sizeof s);
+        const int8_t* q = (const int8_t*)row;
+        for (int64_t c = 0; c < cols; ++c) out[c] = (float)((double)s * q[c]);
+    }
+}
+
+/* Dequantise rows [row0, row0+nrows) into out[nrows][cols]. */
+int or_dequant(int fmt, const uint8_t* w, int64_t rows, int64_t cols, int64_t row0, int64_t nrows, float* out) {
+    if (!or_shape_ok(fmt, rows, cols) || row0 < 0 || nrows < 0 || row0 + nrows > rows) return -1;
+#pragma omp parallel for schedule(static) if (nrows * cols > 262144)
+    for (int64_t r = 0; r < nrows; ++r) dequant_row(fmt, w, rows, cols, row0 + r, out + r * cols);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Matrix-vector product ([llmoxide] s1; [dasLLAMA] 8.7.1.4 matmul)          */
+/* y[b][r] = sum_c deq(W)[r][c] * x[b][c], W row-major [out][in].             */
+/* ------------------------------------------------------------------------- */
+
+static void gemv_rows_d(int fmt, const uint8_t* w, int64_t rows, int64_t cols, const double* x, int batch,
+                        int64_t x_stride, double* y, int64_t y_stride, int64_t row0, int64_t nrows) {
+#pragma omp parallel if (nrows * cols > 65536)
+    {
+        float* deq = (float*)malloc(sizeof(float) * (size_t)cols);
+#pragma omp for schedule(static)
+        for (int64_t i = 0; i < nrows; ++i) {
+            const int64_t r = row0 + i;
+            dequant_row(fmt, w, rows, cols, r, deq);
+            for (int b = 0; b < batch; ++b) {
+                double acc = 0.0;
+                const double* xb = x + (int64_t)b * x_stride;
+                for (int64_t c = 0; c < cols; ++c) acc += (double)deq[c] * xb[c];
+                y[(int64_t)b * y_stride + i] = acc;
+            }
+        }
+        free(deq);
+    }
+}
+
+/* Public GEMV over f32 activations: x[batch][cols] (f32), y[batch][nrows]
+ * (double) for rows [row0, row0+nrows). */
+int or_gemv(int fmt, const uint8_t* w, int64_t rows, int64_t cols, const float* x, int batch, int64_t row0,
+            int64_t nrows, double* y) {
+    if (!or_shape_ok(fmt, rows, cols) || batch <= 0 || row0 < 0 || nrows < 0 || row0 + nrows > rows) return -1;
+    double* xd = (double*)malloc(sizeof(double) * (size_t)(cols * batch));
+    if (!xd) return -2;
+    for (int64_t i = 0; i < cols * batch; ++i) xd[i] = x[i];
+    gemv_rows_d(fmt, w, rows, cols, xd, batch, cols, y, nrows, row0, nrows);
+    free(xd);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* RMSNorm ([llmoxide] s4 rms_norm_mul; [dasLLAMA] 8.7.1.6.2 rmsnorm):        */
+/* out = x * g / sqrt(mean(x^2) + eps), eps inside the root.                  */
+/* ------------------------------------------------------------------------- */
+
+void or_rmsnorm_d(const double* x, const float* g, int n, double eps, double* out) {
+    double ss = 0.0;
+    for (int i = 0; i < n; ++i) ss += x[i] * x[i];
+    const double scale = 1.0 / sqrt(ss / n + eps);
+    for (int i = 0; i < n; ++i) out[i] = x[i] * scale * (double)g[i];
+}
+
+int or_rmsnorm(const float* x, const float* g, int n, int batch, double eps, double* out) {
+    if (n <= 0 || batch <= 0) return -1;
+    double* xd = (double*)malloc(sizeof(double) * (size_t)n);
+    if (!xd) return -2;
+    for (int b = 0; b < batch; ++b) {
+        for (int i = 0; i < n; ++i) xd[i] = x[(int64_t)b * n + i];
+        or_rmsnorm_d(xd, g, n, eps, out + (int64_t)b * n);
+    }
+    free(xd);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* RoPE ([llmoxide] s6 rope; [dasLLAMA] 8.7.1.6.2 rope)                      */
+/* Pair i of a head of width hd turns by pos * theta^(-2i/hd).  Pairs are     */
+/* (2i, 2i+1) ("adjacent", llama files) or (i, i+hd/2) ("half", NeoX/Qwen).   */
+/* ------------------------------------------------------------------------- */
+
+static double rope_angle(int pos, int i, int hd, double theta) {
+    return (double)pos * pow(theta, -2.0 * (double)i / (double)hd);
+}
+
+void or_rope_head_d(double* v, int hd, int pos, int pairing, double theta) {
+    const int half = hd / 2;
+    for (int i = 0; i < half; ++i) {
+        const double a = rope_angle(pos, i, hd, theta);
+        const double c = cos(a), s = sin(a);
+        const int ia = (pairing == OR_ROPE_ADJACENT) ? 2 * i : i;
+        const int ib = (pairing == OR_ROPE_ADJACENT) ? 2 * i + 1 : i + half;
+        const double x0 = v[ia], x1 = v[ib];
+        v[ia] = x0 * c - x1 * s;
+        v[ib] = x0 * s + x1 * c;
+    }
+}
+
+/* Rotate n_heads heads of v (f32 in, double out) at position pos. */
+int or_rope(const float* v, int n_heads, int hd, int pos, int pairing, double theta, double* out) {
+    if (n_heads <= 0 || hd <= 0 || (hd & 1) || pos < 0) return -1;
+    for (int64_t i = 0; i < (int64_t)n_heads * hd; ++i) out[i] = v[i];
+    for (int h = 0; h < n_heads; ++h) or_rope_head_d(out + (int64_t)h * hd, hd, pos, pairing, theta);
+    return 0;
+}
+
+/* cos/sin table [ctx][hd/2][2] rounded to f32 ([go-llm] "Design points": RoPE
+ * angles computed on the CPU in double precision). */
+int or_rope_table(double theta, int hd, int ctx, float* out) {
+    if (hd <= 0 || (hd & 1) || ctx <= 0) return -1;
+    for (int p = 0; p < ctx; ++p)
+        for (int i = 0; i < hd / 2; ++i) {
+            const double a = rope_angle(p, i, hd, theta);
+            out[((int64_t)p * (hd / 2) + i) * 2 + 0] = (float)cos(a);
+            out[((int64_t)p * (hd / 2) + i) * 2 + 1] = (float)sin(a);
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Causal GQA decode attention ([llmoxide] s5; [dasLLAMA] 8.7.1.6.2)          */
+/* For q head h: kvh = h / (hq/hk); score[p] = q.k_p / sqrt(hd), p=0..n_pos-1;*/
+/* softmax with the max subtracted; out = sum_p w_p v_p.                      */
+/* Cache for one layer and one sequence: k[kvh][ctx][hd], v likewise (f32).   */
+/* ------------------------------------------------------------------------- */
+
+void or_attention_d(const double* q, const float* k, const float* v, int hq, int hk, int hd, int n_pos,
+                    int64_t ctx, double* out) {
+    const int group = hq / hk;
+#pragma omp parallel if ((int64_t)hq * n_pos * hd > 262144)
+    {
+        double* sc = (double*)malloc(sizeof(double) * (size_t)n_pos);
+#pragma omp for schedule(static)
+        for (int h = 0; h < hq; ++h) {
+            const int kvh = h / group;
+            const double* qh = q + (int64_t)h * hd;
+            const float* kb = k + (int64_t)kvh * ctx * hd;
+            const float* vb = v + (int64_t)kvh * ctx * hd;
+            for (int p = 0; p < n_pos; ++p) {
+                double dot = 0.0;
+                for (int i = 0; i < hd; ++i) dot += qh[i] * (double)kb[(int64_t)p * hd + i];
+                sc[p] = dot / sqrt((double)hd);
+            }
+            /* softmax: [dasLLAMA] 8.7.1.6.2 softmax */
+            double mx = sc[0];
+            for (int p = 1; p < n_pos; ++p) mx = sc[p] > mx ? sc[p] : mx;
+            double sum = 0.0;
+            for (int p = 0; p < n_pos; ++p) {
+                sc[p] = exp(sc[p] - mx);
+                sum += sc[p];
+            }
+            for (int p = 0; p < n_pos; ++p) sc[p] /= sum;
+            double* oh = out + (int64_t)h * hd;
+            for (int i = 0; i < hd; ++i) oh[i] = 0.0;
+            for (int p = 0; p < n_pos; ++p)
+                for (int i = 0; i < hd; ++i) oh[i] += sc[p] * (double)vb[(int64_t)p * hd + i];
+        }
+        free(sc);
+    }
+}
+
+int or_attention(const float* q, const float* k, const float* v, int hq, int hk, int hd, int n_pos, int64_t ctx,
+                 double* out) {
+    if (hq <= 0 || hk <= 0 || hq % hk || hd <= 0 || n_pos <= 0 || n_pos > ctx) return -1;
+    double* qd = (double*)malloc(sizeof(double) * (size_t)hq * hd);
+    if (!qd) return -2;
+    for (int64_t i = 0; i < (int64_t)hq * hd; ++i) qd[i] = q[i];
+    or_attention_d(qd, k, v, hq, hk, hd, n_pos, ctx, out);
+    free(qd);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* SwiGLU ([llmoxide] s2; [dasLLAMA] 8.7.1.6.3): silu(g) * u with              */
+/* silu(z) = z / (1 + exp(-z)).                                               */
+/* ------------------------------------------------------------------------- */
+
+double or_silu(double z) { return z / (1.0 + exp(-z)); }
+
+int or_swiglu(const float* g, const float* u, int64_t n, double* out) {
+    if (n <= 0) return -1;
+    for (int64_t i = 0; i < n; ++i) out[i] = or_silu((double)g[i]) * (double)u[i];
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Greedy argmax: the largest value, the first index on ties ([go-llm] index, */
+/* Argmax; [dasLLAMA] 8.7.1.6.4 most_likely: strict '>' from index 0).        */
+/* ------------------------------------------------------------------------- */
+
+int64_t or_argmax_f32(const float* v, int64_t n) {
+    int64_t best = 0;
+    for (int64_t i = 1; i < n; ++i)
+        if (v[i] > v[best]) best = i;
+    return best;
+}
+
+int64_t or_argmax_f64(const double* v, int64_t n) {
+    int64_t best = 0;
+    for (int64_t i = 1; i < n; ++i)
+        if (v[i] > v[best]) best = i;
+    return best;
+}
+
+/* ------------------------------------------------------------------------- */
+/* One decode step of a llama-style model for one sequence                    */
+/* ([llmoxide] s7 "The block, and the residual stream"; [dasLLAMA] 8.7.1.6    */
+/* forward):                                                                  */
+/*   x = embed(token)                                                         */
+/*   per layer: x += Wo . attn(rope(Wq xn), rope(Wk xn), Wv xn),              */
+/*              xn = rmsnorm(x) * attn_norm;                                  */
+/*              x += Wd . (silu(Wg xn) * (Wu xn)), xn = rmsnorm(x) * ffn_norm */
+/*   logits = W_out . (rmsnorm(x) * out_norm); next = argmax(logits)           */
+/* The new k, v are appended to the f32 cache at pos before attending over    */
+/* positions 0..pos ([llmoxide] s12; [dasLLAMA] 8.7.1.6.2).                   */
+/*                                                                            */
+/* tensors[] (host pointers, model-file layouts):                             */
+/*   [0] token embedding (emb_fmt, vocab x dim)  [1] out_norm f32[dim]        */
+/*   [2] output head (emb_fmt, vocab x dim) or NULL when tied to [0]          */
+/*   then for each layer l, at 3 + 9l: attn_norm, wq, wk, wv, wo, ffn_norm,   */
+/*   wg, wu, wd.                                                              */
+/* k_cache, v_cache: this sequence's cache, element (l, kvh, p, i) at         */
+/*   l*layer_stride + (kvh*max_ctx + p)*hd + i.                               */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    int layers, dim, ffn, n_heads, n_kv_heads, head_dim, vocab, max_ctx;
+    double rope_theta, eps;
+    int pairing, w_fmt, emb_fmt;
+} or_config;
+
+int or_decode_step(const or_config* c, const void* const* tensors, float* k_cache, float* v_cache,
+                   int64_t layer_stride, int pos, int token, double* logits, int64_t* next_token) {
+    if (!c || pos < 0 || pos >= c->max_ctx || token < 0 || token >= c->vocab) return -1;
+    if (c->n_heads % c->n_kv_heads) return -1;
+    const int D = c->dim, F = c->ffn, hd = c->head_dim, hq = c->n_heads, hk = c->n_kv_heads;
+    const int QD = hq * hd, KD = hk * hd;
+    double* x = (double*)calloc((size_t)D, sizeof(double));
+    double* xn = (double*)calloc((size_t)D, sizeof(double));
+    double* q = (double*)calloc((size_t)QD, sizeof(double));
+    double* k = (double*)calloc((size_t)KD, sizeof(double));
+    double* v = (double*)calloc((size_t)KD, sizeof(double));
+    double* att = (double*)calloc((size_t)QD, sizeof(double));
+    double* t = (double*)calloc((size_t)(D > F ? D : F), sizeof(double));
+    double* g = (double*)calloc((size_t)F, sizeof(double));
+    double* u = (double*)calloc((size_t)F, sizeof(double));
+    float* erow = (float*)calloc((size_t)D, sizeof(float));
+    int rc = 0;
+    if (!x || !xn || !q || !k || !v || !att || !t || !g || !u || !erow) {
+        rc = -2;
+        goto done;
+    }
+    /* embedding: row `token` of the table ([llmoxide] s3) */
+    dequant_row(c->emb_fmt, (const uint8_t*)tensors[0], c->vocab, D, token, erow);
+    for (int i = 0; i < D; ++i) x[i] = erow[i];
+
+    for (int l = 0; l < c->layers; ++l) {
+        const void* const* L = tensors + 3 + 9 * l;
+        float* kl = k_cache + (int64_t)l * layer_stride;
+        float* vl = v_cache + (int64_t)l * layer_stride;
+        /* attention block */
+        or_rmsnorm_d(x, (const float*)L[0], D, c->eps, xn);
+        gemv_rows_d(c->w_fmt, (const uint8_t*)L[1], QD, D, xn, 1, D, q, QD, 0, QD);
+        gemv_rows_d(c->w_fmt, (const uint8_t*)L[2], KD, D, xn, 1, D, k, KD, 0, KD);
+        gemv_rows_d(c->w_fmt, (const uint8_t*)L[3], KD, D, xn, 1, D, v, KD, 0, KD);
+        for (int h = 0; h < hq; ++h) or_rope_head_d(q + (int64_t)h * hd, hd, pos, c->pairing, c->rope_theta);
+        for (int h = 0; h < hk; ++h) or_rope_head_d(k + (int64_t)h * hd, hd, pos, c->pairing, c->rope_theta);
+        for (int h = 0; h < hk; ++h)
+            for (int i = 0; i < hd; ++i) {
+                kl[((int64_t)h * c->max_ctx + pos) * hd + i] = (float)k[h * hd + i];
+                vl[((int64_t)h * c->max_ctx + pos) * hd + i] = (float)v[h * hd + i];
+            }
+        or_attention_d(q, kl, vl, hq, hk, hd, pos + 1, c->max_ctx, att);
+        gemv_rows_d(c->w_fmt, (const uint8_t*)L[4], D, QD, att, 1, QD, t, D, 0, D);
+        for (int i = 0; i < D; ++i) x[i] += t[i];
+        /* feed-forward block */
+        or_rmsnorm_d(x, (const float*)L[5], D, c->eps, xn);
+        gemv_rows_d(c->w_fmt, (const uint8_t*)L[6], F, D, xn, 1, D, g, F, 0, F);
+        gemv_rows_d(c->w_fmt, (const uint8_t*)L[7], F, D, xn, 1, D, u, F, 0, F);
+        for (int i = 0; i < F; ++i) g[i] = or_silu(g[i]) * u[i];
+        gemv_rows_d(c->w_fmt, (const uint8_t*)L[8], D, F, g, 1, F, t, D, 0, D);
+        for (int i = 0; i < D; ++i) x[i] += t[i];
+    }
+    or_rmsnorm_d(x, (const float*)tensors[1], D, c->eps, xn);
+    {
+        const uint8_t* head = (const uint8_t*)(tensors[2] ? tensors[2] : tensors[0]);
+        gemv_rows_d(c->emb_fmt, head, c->vocab, D, xn, 1, D, logits, c->vocab, 0, c->vocab);
+    }
+    if (next_token) *next_token = or_argmax_f64(logits, c->vocab);
+done:
+    free(x); free(xn); free(q); free(k); free(v); free(att); free(t); free(g); free(u); free(erow);
+    return rc;
+}
+
+int or_abi_version(void) { return 1; }
