@@ -1,0 +1,512 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized decode path on GB300.
+
+One step = one greedy generation of the 135M-shaped model (dim 576, 30 layers, 9/3 heads,
+head_dim 64, ffn 1536, vocab 49152, Q4_0 matrices, tied Q8_0 embedding, f32 KV cache):
+128 seeded prompt ids then 128 generated tokens, i.e. 256 calls of qd_decode_step
+(positions 0..255, batch 1), starting from an empty cache.  ``value`` is tokens processed
+per second with the prompt already resident in device memory; ``e2e`` is the same through
+the C ABI with pinned host token buffers (a 4-byte host->device copy and a 4-byte
+device->host copy per token inside the timed region).
+
+L2 is flushed (a 256 MB device write) between timed steps, outside the step's events.  Within
+a step, consecutive tokens re-read the same 90 MB of weights, which the 129 MB L2 may hold.
+
+The JSON line also carries: the roofline of the dominant kernel (timed live with CUDA events
+on the launching stream), the q_gemv GB/s sweep at the 7B-like and TinyLlama shapes, the
+1.7B-shaped INT8 step at context 4096 (batch 1 and 16), the oracle's CPU rate on a bounded
+sample, SM clocks sampled during the timed region, and the kernel-launch count.
+
+Multi-GPU: the decode path is replicated, one independent sequence per rank, with no
+collective on the data path ("weak" scaling); rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "q_gemv achieved HBM GB/s (% of peak); decode tokens/s at 135M and 1.7B shapes"
+PROMPT, GEN = 128, 128
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1913.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a float over ranks (host-side coordination only)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def build_smol135m(qd, torch, seed):
+    import qdsynth
+
+    cfg = qdsynth.SMOL_135M
+    host = qdsynth.model_tensors(cfg, seed)
+    srcs = [None if t is None else torch.from_numpy(np.ascontiguousarray(t)).cuda() for t in host]
+    model = qd.Model(qd.make_config(cfg, PROMPT + GEN, 1), srcs)
+    torch.cuda.synchronize()
+    del srcs
+    return cfg, model
+
+
+def time_gemv_cold(qd, torch, fmt, rows, cols, batch, stream, reps=None, seed=0):
+    """Average duration of qd_q_gemv over back-to-back launches, each on a distinct weight
+    copy so that the weights come from HBM (copies total >= 2x L2).  Returns seconds."""
+    import qdsynth
+
+    src = qdsynth.weight_src(fmt, seed, f"bench.{fmt}.{rows}x{cols}", rows, cols)
+    pb = qd.packed_bytes(fmt, rows, cols)
+    pbuf = torch.empty(pb, dtype=torch.uint8, device="cuda")
+    qd.repack(fmt, torch.from_numpy(src).cuda(), rows, cols, pbuf)
+    n = max(8, min(400, (2 * L2_FLUSH_BYTES) // pb + 1)) if reps is None else reps
+    copies = pbuf.repeat(n).view(n, pb)  # n contiguous copies (each 256-byte aligned: pb % 16 == 0)
+    x = torch.from_numpy(qdsynth.activations(seed, "bench.x", batch, cols)).cuda()
+    y = torch.empty(batch, rows, device="cuda")
+    ptrs = [copies[i].data_ptr() for i in range(n)]
+    aligned = [p for p in ptrs if p % 16 == 0]
+    for p in aligned[:3]:
+        qd.q_gemv(fmt, p, rows, cols, x, y, batch, stream=stream)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    best = None
+    for _ in range(3):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for p in aligned:
+            qd.q_gemv(fmt, p, rows, cols, x, y, batch, stream=stream)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / len(aligned)
+        best = t if best is None else min(best, t)
+    del copies, flush
+    return best, len(aligned)
+
+
+def algorithmic_bytes(fmt, rows, cols, batch, qd):
+    return qd.packed_bytes(fmt, rows, cols) + 4 * batch * (rows + cols)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import qdsynth
+    import quantized_decode_gemv_gb300 as qd
+
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    if not os.path.exists(qd.LIB_PATH):
+        qd.build()
+    qd.load()
+    stream = torch.cuda.current_stream()
+    cfg, model = build_smol135m(qd, torch, seed=rank)
+    T = PROMPT + GEN
+    prompt = qdsynth.tokens(rank, "smol135m.prompt", PROMPT, cfg["vocab"]).astype(np.int32)
+    # device-resident token slots: slot t is the input of position t; outputs of prompt
+    # positions go to scratch, outputs from position 127 on feed the next slot.
+    tok = torch.zeros(T + 1, dtype=torch.int32, device="cuda")
+    tok[:PROMPT] = torch.from_numpy(prompt).cuda()
+    scratch = torch.zeros(T, dtype=torch.int32, device="cuda")
+    tok_h = torch.zeros(T + 1, dtype=torch.int32).pin_memory()
+    tok_h[:PROMPT] = torch.from_numpy(prompt)
+    scratch_h = torch.zeros(T, dtype=torch.int32).pin_memory()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def step(dev_side: bool):
+        model.reset(stream)
+        t_in, s_out = (tok, scratch) if dev_side else (tok_h, scratch_h)
+        base_in, base_s = t_in.data_ptr(), s_out.data_ptr()
+        for t in range(T):
+            out = base_in + 4 * (t + 1) if t >= PROMPT - 1 else base_s + 4 * t
+            model.decode_step(base_in + 4 * t, 1, out, None, stream)
+
+    for _ in range(args.warmup):
+        step(True)
+    torch.cuda.synchronize()
+    gen_dev = tok[PROMPT:T].cpu().numpy().copy()
+    launches_token = model.launches_per_step()
+    reset_launches = 4
+
+    # ---- timed region: device-resident inputs
+    times = []
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            flush.fill_(0)  # L2 flush between steps (outside the step's events)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step(True)
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize()
+        barrier(world)
+        wall = time.perf_counter() - wall0
+    step_s = [a.elapsed_time(b) / 1e3 for a, b in times]
+    t_total = reduce_max(sum(step_s), world)
+    value = world * args.steps * T / t_total
+    assert np.array_equal(tok[PROMPT:T].cpu().numpy(), gen_dev), "generation changed between runs"
+
+    # ---- end to end: pinned host token buffers through the C ABI
+    for _ in range(2):
+        step(False)
+    torch.cuda.synchronize()
+    e_times = []
+    barrier(world)
+    for _ in range(args.steps):
+        flush.fill_(0)
+        torch.cuda.synchronize()
+        w0 = time.perf_counter()
+        step(False)
+        torch.cuda.synchronize()
+        got = tok_h[PROMPT:T].numpy().copy()  # the step's result, read on the host
+        e_times.append(time.perf_counter() - w0)
+    assert np.array_equal(got, gen_dev), "host-buffer generation differs from device-buffer generation"
+    e2e_total = reduce_max(sum(e_times), world)
+    e2e_value = world * args.steps * T / e2e_total
+
+    hbm, bf16, peak_kind = peaks()
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * t_total / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 activations; q4_0/q8_0 weights",
+        "data": "synthetic (seeded SplitMix64 weights and prompt, 135M-shaped)",
+        "config": {"workload": "135M-shaped greedy decode: 128 prompt ids + 128 generated tokens, batch 1",
+                   "model": "llama-style 135M shape (dim 576, 30 layers, 9/3 heads, ffn 1536, vocab 49152)",
+                   "w_fmt": "q4_0", "emb_fmt": "q8_0 (tied)", "global_batch": world, "seq_len": T,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed (256 MB write) between timed steps; inputs (90 MB weights) fit in L2 within a step"},
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 4 * T,
+                "d2h_bytes_per_step": 4 * T},
+        "gpu_launches": int(args.steps * (T * launches_token + reset_launches)),
+        "launches_per_token": launches_token,
+        "wall_s_timed": round(wall, 3),
+        "ms_per_token": round(1e3 * t_total / (args.steps * T), 4),
+    }
+    out["clocks"] = clk.summary()
+
+    if rank == 0 and not args.quick:
+        out["roofline"] = roofline_dominant(qd, torch, stream, hbm, peak_kind)
+        out["q_gemv_sweep"] = gemv_sweep(qd, torch, stream, hbm, args)
+        del model
+        torch.cuda.empty_cache()
+        if not args.no_1p7b:
+            out["decode_1p7b"] = bench_1p7b(qd, torch, stream, args)
+        if world == 1:
+            out["cpu_baseline"] = cpu_baseline(cfg, seconds=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def profile_traffic(kernel_tag: str):
+    """Per-launch DRAM bytes from the committed ncu summary, or None when the kernel source
+    changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{16,64})", text)
+    src = os.path.join(ROOT, "quantized_decode_gemv_gb300", "csrc", "qd_gemv.cu")
+    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if not m or not h or not cur.startswith(h.group(1)):
+        return None
+    return float(m.group(1))
+
+
+def roofline_dominant(qd, torch, stream, hbm, peak_kind):
+    """The step's dominant kernel is the Q4_0 GEMV (120 launches per token over the four
+    per-layer shapes).  Its achieved bandwidth: algorithmic bytes of the four shapes over the
+    sum of their average launch durations (cold weights)."""
+    shapes = [(960, 576), (576, 576), (3072, 576), (576, 1536)]
+    tot_b, tot_t = 0, 0.0
+    per = {}
+    for r, c in shapes:
+        t, n = time_gemv_cold(qd, torch, "q4_0", r, c, 1, stream)
+        b = algorithmic_bytes("q4_0", r, c, 1, qd)
+        tot_b += b
+        tot_t += t
+        per[f"{r}x{c}"] = {"us": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1)}
+    achieved = tot_b / tot_t / 1e9
+    traffic = profile_traffic("q_gemv_q4_0_decode_shapes")
+    return {"kernel": "k_gemv_blocks<Q4_0> (decode-step shapes 960x576, 576x576, 3072x576, 576x1536)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
+            "traffic": traffic, "algorithmic_bytes_per_launch": round(tot_b / len(shapes)),
+            "per_shape": per}
+
+
+def gemv_sweep(qd, torch, stream, hbm, args):
+    res = {}
+    shapes = [("q4_0", 576, 1536)]
+    for fmt in ("q8_0", "q4_0"):
+        for r, c in [(4096, 4096), (11008, 4096), (4096, 11008), (14336, 4096)]:
+            shapes.append((fmt, r, c))
+    for r, c in [(2048, 2048), (5632, 2048), (2048, 5632), (32000, 2048)]:
+        shapes.append(("q4_k", r, c))
+    batches = (1, 2, 4, 8) if args.full_sweep else (1,)
+    for fmt, r, c in shapes:
+        for b in (batches if fmt != "q4_k" and (r, c) != (576, 1536) else (1,)):
+            t, n = time_gemv_cold(qd, torch, fmt, r, c, b, stream)
+            by = algorithmic_bytes(fmt, r, c, b, qd)
+            res[f"{fmt} {r}x{c} b{b}"] = {"us": round(t * 1e6, 2), "GB/s": round(by / t / 1e9, 1),
+                                          "frac": round(by / t / 1e9 / hbm, 3)}
+    return res
+
+
+def bench_1p7b(qd, torch, stream, args):
+    """1.7B-shaped INT8 step at context 4096 (pos 4095): batch 1 and 16, cache entries N(0,1)
+    drawn on the device with a seeded torch generator (timing only; the parity tests use the
+    host generator)."""
+    import qdsynth
+
+    cfg = qdsynth.SMOL_1_7B
+    ctx = 4096
+    host = qdsynth.model_tensors(cfg, 0)
+    out = {}
+    for batch in (1, 16):
+        srcs = [None if t is None else torch.from_numpy(np.ascontiguousarray(t)).cuda() for t in host]
+        m = qd.Model(qd.make_config(cfg, ctx, batch), srcs)
+        torch.cuda.synchronize()
+        del srcs
+        kp, vp = m.kv_cache_ptrs()
+        base = m.state.data_ptr()
+        n = cfg["layers"] * batch * cfg["n_kv_heads"] * ctx * cfg["head_dim"]
+        g = torch.Generator(device="cuda").manual_seed(1234)
+        for ptr in (kp, vp):
+            m.state[ptr - base:ptr - base + 4 * n].view(torch.float32).normal_(generator=g)
+        toks = torch.from_numpy(qdsynth.tokens(0, "c5.tokens", 16, cfg["vocab"])[:batch].astype(np.int32)).cuda()
+        outt = torch.empty(batch, dtype=torch.int32, device="cuda")
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        ts = []
+        for i in range(3 + 5):
+            m.set_pos([ctx - 1] * batch, stream)
+            flush.fill_(0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            m.decode_step(toks, batch, outt, None, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(e0.elapsed_time(e1) / 1e3)
+        t = statistics.median(ts)
+        wbytes = m.weights.numel()
+        kv = 2 * n * 4
+        out[f"batch{batch}"] = {"ms_per_step": round(t * 1e3, 3), "tokens/s": round(batch / t, 1),
+                                "bytes_per_step": int(wbytes + kv),
+                                "GB/s": round((wbytes + kv) / t / 1e9, 1)}
+        m.close()
+        del m, flush
+        torch.cuda.empty_cache()
+    return out
+
+
+def cpu_baseline(cfg, seconds=15.0, max_tokens=64):
+    """The oracle, as it stands, on the host cores: the first tokens of the same run (prompt
+    positions 0, 1, ...), until about `seconds` of CPU work."""
+    import oracle
+    import qdsynth
+
+    host = qdsynth.model_tensors(cfg, 0)
+    om = oracle.Model(dict(cfg, max_ctx=PROMPT + GEN), host)
+    L, hk, hd = cfg["layers"], cfg["n_kv_heads"], cfg["head_dim"]
+    ctx = PROMPT + GEN
+    kc = np.zeros(L * hk * ctx * hd, np.float32)
+    vc = np.zeros_like(kc)
+    prompt = qdsynth.tokens(0, "smol135m.prompt", PROMPT, cfg["vocab"])
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_tokens and (time.perf_counter() - t0) < seconds:
+        om.decode_step(kc, vc, hk * ctx * hd, n, int(prompt[n]))
+        n += 1
+    dt = time.perf_counter() - t0
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} tokens (positions 0..{n - 1}) of the 135M 128+128 run, batch 1, "
+                      f"{dt:.1f} s; oracle C code, double accumulation, OpenMP over matrix rows"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank, local):
+    """The oracle timed as the reference arm, on the same workload: each step is a bounded
+    sample (the first `ref_tokens` positions of the 135M run)."""
+    if rank != 0:
+        return
+    import oracle
+    import qdsynth
+
+    cfg = qdsynth.SMOL_135M
+    host = qdsynth.model_tensors(cfg, 0)
+    ctx = PROMPT + GEN
+    om = oracle.Model(dict(cfg, max_ctx=ctx), host)
+    L, hk, hd = cfg["layers"], cfg["n_kv_heads"], cfg["head_dim"]
+    prompt = qdsynth.tokens(0, "smol135m.prompt", PROMPT, cfg["vocab"])
+    nt = args.ref_tokens
+
+    def one():
+        kc = np.zeros(L * hk * ctx * hd, np.float32)
+        vc = np.zeros_like(kc)
+        for p in range(nt):
+            om.decode_step(kc, vc, hk * ctx * hd, p, int(prompt[p]))
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = time.perf_counter() - t0
+    v = args.steps * nt / dt
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    sample = f"{nt} tokens per step (positions 0..{nt - 1} of the 135M 128+128 run), batch 1"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulation",
+        "data": "synthetic (seeded SplitMix64 weights and prompt, 135M-shaped)",
+        "config": {"workload": "135M-shaped greedy decode: 128 prompt ids + 128 generated tokens, batch 1",
+                   "global_batch": 1, "seq_len": PROMPT + GEN, "parallelism": "CPU oracle"},
+        "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="main line only (no sweep, 1.7B, CPU baseline)")
+    ap.add_argument("--no-1p7b", action="store_true")
+    ap.add_argument("--full-sweep", action="store_true", help="q_gemv sweep at batch 1, 2, 4, 8")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-tokens", type=int, default=8)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,266 @@
+/*
+ * qdecode.h — C ABI of libqdecode, the single-token decode path of a llama-style
+ * transformer over block-quantised weights, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (the pages on quantized decode GEMV; each entry point
+ * below names its passage):
+ *   [llmoxide]  "Running an LLM, then forgetting it" (llmoxide blog), sections
+ *               1 "A neuron is a dot product", 2 "Layers, and the bend between them",
+ *               3 "Text in, vectors out", 4 "Keeping the numbers in range",
+ *               5 "Attention", 6 "Where things are: RoPE", 7 "The block, and the
+ *               residual stream", 10 "Loading weights", 11 "Prefill and decode",
+ *               12 "The KV cache".
+ *   [go-llm]    "llm" Go package documentation (go-wasmcontainers/llm v0.1.0):
+ *               "Design points", "Oracle tolerances", index (Argmax, F16ToF32,
+ *               CPU.Forward, CPU.Reset, CPU.Pos, Config).
+ *   [llamini]   "Building llamini.cpp: a from-scratch llama.cpp core in C99",
+ *               "What I reimplemented" (Q4_K scale/min unpacking).
+ *   [dasLLAMA]  "dasLLAMA-00 - The Problem Statement", 8.7.1.4 "Five small
+ *               functions", 8.7.1.6.2 "Attention", 8.7.1.6.3 "Feed-forward",
+ *               8.7.1.6.4 "Logits", 8.7.1.7 "Prompting is repeated forward".
+ *   [minillm]   minillm-cpp README, "Loader", "NEON kernels", "Quantization".
+ *
+ * Conventions for every entry point:
+ *  - Device pointers unless stated "host".  The caller owns and allocates every
+ *    buffer; no entry point calls cudaMalloc or frees caller memory.  (The model
+ *    object is a small host struct; qd_model_create captures CUDA graphs, which the
+ *    driver allocates for itself.)
+ *  - All device work is enqueued on `stream` and is asynchronous; host-side
+ *    results (sizes, statuses) are synchronous.
+ *  - Every call validates its arguments before enqueuing anything.  A failed check
+ *    returns a status other than QD_OK and enqueues nothing.  Launch failures
+ *    return QD_ERR_CUDA.  Kernels never trap: a condition only the device can see
+ *    (a token id or position out of range inside a captured step) sets a bit in the
+ *    model's device error word and the kernel skips the access; qd_model_check
+ *    reports it.
+ *  - Activations are f32, batch-major: x[batch][n].  Batch is 1..QD_MAX_BATCH.
+ *  - Every device buffer must be 16-byte aligned.
+ *  - No entry point is thread-safe on the same model or buffers.
+ */
+#ifndef QDECODE_H
+#define QDECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* qd_stream_t;
+
+#define QD_MAX_BATCH 16
+
+typedef enum {
+    QD_OK = 0,
+    QD_ERR_INVALID_ARG = 1, /* null pointer, bad enum, negative size          */
+    QD_ERR_SHAPE = 2,       /* size not allowed for the format / operation     */
+    QD_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned         */
+    QD_ERR_UNSUPPORTED = 4, /* unknown format, pairing or configuration        */
+    QD_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed     */
+    QD_ERR_NOMEM = 6,       /* a caller-provided buffer is too small           */
+    QD_ERR_DEVICE_FLAG = 7  /* a kernel flagged an out-of-range token/position */
+} qd_status;
+
+/* Weight formats ([llmoxide] 10; [go-llm] "Design points"; [llamini]; [minillm]
+ * "Quantization"):
+ *  QD_Q4_0   blocks of 32 weights, 18 B: f16 d, 16 B of 4-bit codes; value (q-8)*d.
+ *            Element j (0..15) is the low nibble of code byte j, element j+16 its
+ *            high nibble.
+ *  QD_Q8_0   blocks of 32 weights, 34 B: f16 d, 32 int8 codes; value q*d.
+ *  QD_Q4_K   super-blocks of 256 weights, 144 B: f16 d, f16 dmin, 12 B of packed
+ *            6-bit (scale, min) for 8 sub-blocks of 32, 128 B of 4-bit codes;
+ *            value d*sc*q - dmin*m.  Code byte 32c+l holds element 64c+l (low
+ *            nibble, sub-block 2c) and element 64c+32+l (high nibble, sub-block 2c+1).
+ *  QD_I8_ROW per-row symmetric INT8: int8 codes [rows][cols], then one f32 scale
+ *            per row; value q*s_row.
+ * The "source" layout of a tensor is the model-file layout above, rows in order
+ * (for QD_I8_ROW: all codes, then all scales, in one buffer). */
+typedef enum { QD_Q4_0 = 0, QD_Q8_0 = 1, QD_Q4_K = 2, QD_I8_ROW = 3 } qd_fmt;
+
+/* RoPE pairing ([llmoxide] 6): ADJACENT rotates (2i, 2i+1) (llama files), HALF
+ * rotates (i, i + head_dim/2) (NeoX/Qwen). */
+typedef enum { QD_ROPE_ADJACENT = 0, QD_ROPE_HALF = 1 } qd_rope_pairing;
+
+const char* qd_status_str(qd_status s);
+int qd_abi_version(void);
+
+/* ------------------------------------------------------------------------- */
+/* Scalar conversions ([go-llm] index F16ToF32; [minillm] "Loader").          */
+/* ------------------------------------------------------------------------- */
+
+/* Device kernels converting n binary16 / bfloat16 bit patterns to f32 (exact;
+ * bf16 is the zero-extension bits << 16).  in, out: device, n >= 0. */
+qd_status qd_f16_to_f32(const uint16_t* in, float* out, int64_t n, qd_stream_t stream);
+qd_status qd_bf16_to_f32(const uint16_t* in, float* out, int64_t n, qd_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Load-time repacking ([go-llm] "Design points": blocks are repacked into    */
+/* aligned quants and scales on upload).                                      */
+/* Packed layouts (all regions 16-byte aligned, rows in order):               */
+/*  Q4_0: codes [rows][cols/32][16 B], then f16 d [rows][cols/32].            */
+/*  Q8_0: codes [rows][cols/32][32 B], then f16 d [rows][cols/32].            */
+/*  Q4_K: codes [rows][cols/256][128 B], then headers [rows][cols/256][16 B]  */
+/*        (d, dmin, 12 scale bytes).                                          */
+/*  I8_ROW: codes [rows][cols], then f32 scales [rows].                       */
+/* The repack is lossless: qd_unpack restores the source bytes exactly.       */
+/* ------------------------------------------------------------------------- */
+
+/* Bytes of the source / packed layout; 0 for a shape the format does not allow
+ * (rows < 1, cols < 1, cols % 32 for Q4_0/Q8_0, cols % 256 for Q4_K, cols % 16
+ * for I8_ROW). */
+size_t qd_src_bytes(qd_fmt fmt, int64_t rows, int64_t cols);
+size_t qd_packed_bytes(qd_fmt fmt, int64_t rows, int64_t cols);
+
+/* src (device, source layout, qd_src_bytes) -> dst (device, packed layout,
+ * dst_bytes >= qd_packed_bytes).  src and dst must not overlap. */
+qd_status qd_repack(qd_fmt fmt, const void* src, int64_t rows, int64_t cols, void* dst, size_t dst_bytes,
+                    qd_stream_t stream);
+/* Inverse of qd_repack (for tests): packed -> source layout (dst_bytes >= qd_src_bytes). */
+qd_status qd_unpack(qd_fmt fmt, const void* packed, int64_t rows, int64_t cols, void* dst, size_t dst_bytes,
+                    qd_stream_t stream);
+/* Dequantised values of a packed tensor: out f32 [rows][cols] (device), each value
+ * rounded once to f32 (for the bit-exact block-value tests). */
+qd_status qd_dequant(qd_fmt fmt, const void* packed, int64_t rows, int64_t cols, float* out, qd_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Fused dequantise-and-dot GEMV ([llmoxide] 1 matvec, 10 (the Q8_0 row dot), */
+/* 11 (t rows of x through one read of W); [dasLLAMA] 8.7.1.4 matmul;         */
+/* [minillm] "NEON kernels": fused, no f32 temporary).                        */
+/* y[b][r] = sum_c deq(W)[r][c] * x[b][c], for b < batch, r < rows.           */
+/* W: packed layout (qd_repack).  x: f32 [batch][cols].  y: f32 [batch][rows], */
+/* must not overlap x.  batch 1..16.  workspace: currently unused (pass NULL, 0);*/
+/* qd_q_gemv_workspace returns the bytes a call needs.                         */
+/* ------------------------------------------------------------------------- */
+size_t qd_q_gemv_workspace(qd_fmt fmt, int64_t rows, int64_t cols, int batch);
+qd_status qd_q_gemv(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch,
+                    void* workspace, size_t workspace_bytes, qd_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Decode-step operations                                                      */
+/* ------------------------------------------------------------------------- */
+
+/* RMSNorm ([llmoxide] 4 rms_norm_mul; [dasLLAMA] 8.7.1.6.2 rmsnorm):
+ * out[b][i] = x[b][i] * g[i] / sqrt(mean_i(x[b][i]^2) + eps).  x, out: f32
+ * [batch][n] (may alias); g: f32 [n].  n 1..65536, eps >= 0. */
+qd_status qd_rmsnorm(const float* x, const float* g, float* out, int n, int batch, float eps, qd_stream_t stream);
+
+/* Host: fill dst_host f32 [ctx][head_dim/2][2] with (cos, sin) of the angle
+ * p * theta^(-2i/head_dim), computed in double and rounded to f32 ([go-llm]
+ * "Design points": RoPE angles on the CPU in double precision).  head_dim even. */
+qd_status qd_rope_table(float theta, int head_dim, int ctx, float* dst_host);
+
+/* RoPE in place ([llmoxide] 6 rope; [dasLLAMA] 8.7.1.6.2 rope): rotate each of the
+ * n_heads heads of row b of v (v + b*batch_stride, f32 [n_heads][head_dim]) by the
+ * angles of position pos[b] (device int32 [batch]) from cos_sin (device, the table
+ * of qd_rope_table for max_ctx positions).  A pos[b] outside [0, max_ctx) leaves
+ * that row unchanged. */
+qd_status qd_rope(float* v, int n_heads, int head_dim, int64_t batch_stride, const int32_t* pos,
+                  qd_rope_pairing pairing, const float* cos_sin, int max_ctx, int batch, qd_stream_t stream);
+
+/* KV-cache append ([llmoxide] 12; [dasLLAMA] 8.7.1.6.2: the rotated K and the V of
+ * the current token go to the layer's cache at its position).  k, v: rows
+ * b*src_batch_stride of f32 [n_kv_heads][head_dim]; caches: f32
+ * [batch][n_kv_heads][max_ctx][head_dim]; position pos[b] (device).  A pos[b]
+ * outside [0, max_ctx) writes nothing for that row. */
+qd_status qd_kv_append(const float* k, const float* v, int64_t src_batch_stride, float* k_cache, float* v_cache,
+                       int n_kv_heads, int head_dim, const int32_t* pos, int max_ctx, int batch,
+                       qd_stream_t stream);
+
+/* Causal grouped-query decode attention ([llmoxide] 5; [dasLLAMA] 8.7.1.6.2 score,
+ * softmax and weighted sum).  For row b and q head h: kvh = h / (n_heads /
+ * n_kv_heads); s_p = q.k_p / sqrt(head_dim) over p = 0..pos[b]; out = sum_p
+ * softmax(s)_p v_p.  q: f32 [batch][n_heads][head_dim] (row stride q_batch_stride);
+ * caches as in qd_kv_append; out: f32 [batch][n_heads][head_dim].  head_dim 64
+ * (the models here); n_heads % n_kv_heads == 0, group size <= 8.  The context is
+ * split across CTAs and merged with log-sum-exp weights; workspace (device) holds
+ * the partial results, qd_gqa_decode_attn_workspace bytes.  A pos[b] outside
+ * [0, max_ctx) yields zeros for that row. */
+size_t qd_gqa_decode_attn_workspace(int n_heads, int head_dim, int max_ctx, int batch);
+qd_status qd_gqa_decode_attn(const float* q, int64_t q_batch_stride, const float* k_cache, const float* v_cache,
+                             float* out, int n_heads, int n_kv_heads, int head_dim, const int32_t* pos, int max_ctx,
+                             int batch, void* workspace, size_t workspace_bytes, qd_stream_t stream);
+
+/* SwiGLU gate ([llmoxide] 2; [dasLLAMA] 8.7.1.6.3): out = silu(gate) * up with
+ * silu(z) = z / (1 + exp(-z)).  f32 [batch][n] each. */
+qd_status qd_swiglu(const float* gate, const float* up, float* out, int64_t n, int batch, qd_stream_t stream);
+
+/* Greedy argmax ([go-llm] index Argmax; [dasLLAMA] 8.7.1.6.4 most_likely): the
+ * index of the largest of logits[b][0..n), the first such index on ties.
+ * out_idx: device int32 [batch].  NaN never wins (inputs are expected NaN-free). */
+qd_status qd_argmax(const float* logits, int64_t n, int batch, int32_t* out_idx, qd_stream_t stream);
+
+/* Embedding lookup ([llmoxide] 3; [dasLLAMA] 8.7.1.6.1): x[b] = deq(E)[tokens[b]].
+ * E: packed [vocab][dim]; tokens: device int32 [batch]; an id outside [0, vocab)
+ * writes zeros. */
+qd_status qd_embed(qd_fmt fmt, const void* E, int64_t vocab, int64_t dim, const int32_t* tokens, int batch,
+                   float* x, qd_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Model and decode step ([llmoxide] 7, 11, 12; [dasLLAMA] 8.7.1.6 forward,    */
+/* 8.7.1.7; [go-llm] CPU.Forward / Reset / Pos, "One submit per token").       */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    int layers, dim, ffn, n_heads, n_kv_heads, head_dim, vocab;
+    int max_ctx;   /* positions per sequence in the KV cache                  */
+    int max_batch; /* independent sequences per step, 1..16                  */
+    float rope_theta, eps;
+    qd_rope_pairing pairing;
+    qd_fmt w_fmt;   /* the seven matrices of every layer                        */
+    qd_fmt emb_fmt; /* token embedding (and output head)                        */
+    int tied;       /* 1: logits use the token embedding as output head         */
+} qd_config;
+
+typedef struct qd_model qd_model;
+
+/* Bytes of the caller-provided regions: packed weights, and state (KV cache,
+ * activations, positions, error word, rope table).  0 for an invalid config. */
+size_t qd_model_weight_bytes(const qd_config* cfg);
+size_t qd_model_state_bytes(const qd_config* cfg);
+
+/* Build a model.  src_tensors: 3 + 9*layers device pointers to source-layout
+ * tensors: [0] token embedding (emb_fmt, vocab x dim), [1] output norm gains f32
+ * [dim], [2] output head (emb_fmt) or NULL when tied, then for layer l at 3+9l:
+ * attn_norm f32[dim], wq (n_heads*head_dim x dim), wk, wv (n_kv_heads*head_dim x
+ * dim), wo (dim x n_heads*head_dim), ffn_norm f32[dim], wg, wu (ffn x dim), wd
+ * (dim x ffn).  They are repacked into weight_mem (fused QKV rows and interleaved
+ * gate/up rows) on `stream`; the sources may be freed once the stream has passed
+ * this point.  state_mem is zeroed (empty caches, pos 0).  *out receives a host
+ * object, freed by qd_model_destroy. */
+qd_status qd_model_create(const qd_config* cfg, const void* const* src_tensors, void* weight_mem,
+                          size_t weight_bytes, void* state_mem, size_t state_bytes, qd_stream_t stream,
+                          qd_model** out);
+void qd_model_destroy(qd_model* m);
+
+/* One greedy decode step for sequences 0..batch-1 at their current positions:
+ * embed tokens[b], run every layer (appending K, V at pos[b]), compute the logits,
+ * write argmax to out_tokens[b], advance pos[b].  tokens / out_tokens may be host
+ * or device pointers (int32 [batch]); logits_out (f32 [batch][vocab], host or
+ * device) may be NULL.  The step is one CUDA graph replay on `stream` (captured on
+ * the first step of each batch size); host pointers make the call wait for the
+ * copies.  Prefill is this call once per prompt token ([go-llm] "Results":
+ * "Prefill is a decode pass per prompt token"). */
+qd_status qd_decode_step(qd_model* m, const int32_t* tokens, int batch, int32_t* out_tokens, float* logits_out,
+                         qd_stream_t stream);
+
+/* Zero the KV cache and set every position to 0 ([go-llm] CPU.Reset). */
+qd_status qd_model_reset(qd_model* m, qd_stream_t stream);
+/* Set the positions of sequences 0..batch-1 (host int32 [batch]) (e.g. after
+ * filling the cache directly). */
+qd_status qd_model_set_pos(qd_model* m, const int32_t* pos_host, int batch, qd_stream_t stream);
+/* Read positions (host int32 [batch]); synchronises `stream` ([go-llm] CPU.Pos). */
+qd_status qd_model_pos(qd_model* m, int32_t* pos_host, int batch, qd_stream_t stream);
+/* Device pointers to the KV cache, f32 [layers][max_batch][n_kv_heads][max_ctx][head_dim]. */
+qd_status qd_model_kv_cache(qd_model* m, float** k_cache, float** v_cache);
+/* Synchronise `stream` and return QD_ERR_DEVICE_FLAG (and clear the word) if a
+ * kernel met an out-of-range token or position since the last check. */
+qd_status qd_model_check(qd_model* m, qd_stream_t stream);
+/* Number of kernels one decode step launches (for launch accounting). */
+int qd_model_launches_per_step(const qd_model* m);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QDECODE_H */

@@ -1,0 +1,363 @@
+// Fused dequantise-and-dot GEMV over packed block-quantised weights.
+//
+// y[b][r] = sum_c deq(W)[r][c] * x[b][c]   (llmoxide blog, s1 "A neuron is a dot
+// product" and s10's Q8_0 row dot; dasLLAMA 8.7.1.4 matmul).  As in the
+// minillm-cpp README ("NEON kernels"), the weights are decoded in registers and
+// never written out as f32.
+//
+// Work decomposition.  A warp owns R consecutive output rows.  Its lanes walk the
+// row's "units" (32 weights for Q4_0/Q8_0/Q4_K, 16 for INT8) with stride 32, so a
+// warp load instruction reads 32 consecutive units of one row: 512 contiguous
+// bytes of Q4_0 codes, 1 KB of Q8_0 codes.  The codes of the next unit are loaded
+// before the current one is computed.  For each unit the lane turns the codes
+// into exact small-integer floats once per row (the byte lands in the mantissa of
+// 2^23 and 2^23 is subtracted), then streams x once per batch column and applies
+// the unit's scale to the unit's partial sum.  Block scales therefore multiply a
+// 32-term partial sum rather than every weight; the per-row f32 sums are reduced
+// across the warp with shuffles at the end.
+#include "qd_internal.cuh"
+
+namespace qd {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarpsPerCta = kThreads / kWarp;
+
+template <int FMT>
+struct Unit;  // raw codes + scale data of one unit of one row
+
+// ----------------------------------------------------------------- Q4_0
+template <>
+struct Unit<QD_Q4_0> {
+  static constexpr int kWeights = 32;
+  uint4 q;
+  uint32_t d;
+  __device__ __forceinline__ void load(const PackedView& W, int64_t r, int64_t u) {
+    q = ld_stream_v4(W.codes + r * W.row_code_bytes + u * 16);
+    d = __ldg(reinterpret_cast<const unsigned short*>(W.scales + r * W.row_scale_bytes) + u);
+  }
+  // w[j] = q_j - 8 for element j of the block (exact).
+  __device__ __forceinline__ void codes(float (&w)[32]) const {
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t lo = words[t] & 0x0F0F0F0Fu, hi = (words[t] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        w[4 * t + k] = byte_as_magic(lo, k) - (kMagic + 8.0f);
+        w[16 + 4 * t + k] = byte_as_magic(hi, k) - (kMagic + 8.0f);
+      }
+    }
+  }
+  __device__ __forceinline__ float scale() const { return f16_bits_to_f32(d); }
+  __device__ __forceinline__ static int64_t x_offset(int64_t u) { return u * 32; }
+};
+
+// ----------------------------------------------------------------- Q8_0
+template <>
+struct Unit<QD_Q8_0> {
+  static constexpr int kWeights = 32;
+  uint4 q0, q1;
+  uint32_t d;
+  __device__ __forceinline__ void load(const PackedView& W, int64_t r, int64_t u) {
+    const uint8_t* p = W.codes + r * W.row_code_bytes + u * 32;
+    q0 = ld_stream_v4(p);
+    q1 = ld_stream_v4(p + 16);
+    d = __ldg(reinterpret_cast<const unsigned short*>(W.scales + r * W.row_scale_bytes) + u);
+  }
+  __device__ __forceinline__ void codes(float (&w)[32]) const {
+    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const uint32_t b = words[t] ^ 0x80808080u;  // int8 q -> unsigned q + 128
+#pragma unroll
+      for (int k = 0; k < 4; ++k) w[4 * t + k] = byte_as_magic(b, k) - (kMagic + 128.0f);
+    }
+  }
+  __device__ __forceinline__ float scale() const { return f16_bits_to_f32(d); }
+  __device__ __forceinline__ static int64_t x_offset(int64_t u) { return u * 32; }
+};
+
+// ----------------------------------------------------------------- INT8 rows
+template <>
+struct Unit<QD_I8_ROW> {
+  static constexpr int kWeights = 16;
+  uint4 q;
+  __device__ __forceinline__ void load(const PackedView& W, int64_t r, int64_t u) {
+    q = ld_stream_v4(W.codes + r * W.row_code_bytes + u * 16);
+  }
+  __device__ __forceinline__ void codes(float (&w)[16]) const {
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t b = words[t] ^ 0x80808080u;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) w[4 * t + k] = byte_as_magic(b, k) - (kMagic + 128.0f);
+    }
+  }
+  __device__ __forceinline__ static int64_t x_offset(int64_t u) { return u * 16; }
+};
+
+template <int N>
+__device__ __forceinline__ float dot_x(const float (&w)[N], const float* __restrict__ xp) {
+  const float4* x4 = reinterpret_cast<const float4*>(xp);
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int t = 0; t < N / 4; ++t) {
+    const float4 v = __ldg(x4 + t);
+    s0 = fmaf(w[4 * t + 0], v.x, s0);
+    s1 = fmaf(w[4 * t + 1], v.y, s1);
+    s0 = fmaf(w[4 * t + 2], v.z, s0);
+    s1 = fmaf(w[4 * t + 3], v.w, s1);
+  }
+  return s0 + s1;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// Epilogue shared by every format: reduce each (row, batch) sum across the warp
+// and write it according to `mode`.
+template <int R, int NB>
+__device__ __forceinline__ void finish_rows(float (&acc)[R][NB], const float* row_scale, int64_t row0,
+                                            int64_t rows, float* __restrict__ y, int batch, int mode, int lane) {
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[i][b] = warp_sum(acc[i][b]);
+  if (lane != 0) return;
+  if (mode == kGemvSwiGLU) {
+    // rows (row0, row0+1) are (gate_i, up_i) with i = row0 / 2
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+      if (b < batch) {
+        const float g = acc[0][b] * row_scale[0];
+        const float u = acc[R - 1][b] * row_scale[R - 1];
+        y[(int64_t)b * (rows / 2) + row0 / 2] = silu(g) * u;
+      }
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int64_t r = row0 + i;
+    if (r >= rows) break;
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+      if (b < batch) {
+        const float v = acc[i][b] * row_scale[i];
+        float* dst = y + (int64_t)b * rows + r;
+        if (mode == kGemvAccumulate)
+          *dst += v;
+        else
+          *dst = v;
+      }
+  }
+}
+
+// Q4_0 / Q8_0 / INT8: one scale per block (or per row) times an integer-code dot.
+template <int FMT, int R, int NB>
+__global__ void __launch_bounds__(kThreads) k_gemv_blocks(PackedView W, const float* __restrict__ x,
+                                                           float* __restrict__ y, int batch, int mode) {
+  using U = Unit<FMT>;
+  constexpr int KW = U::kWeights;
+  const int lane = threadIdx.x & 31;
+  const int64_t row0 = ((int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)) * R;
+  if (row0 >= W.rows) return;
+  const int64_t units = W.cols / KW;
+  float acc[R][NB];
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[i][b] = 0.f;
+
+  U cur[R], nxt[R];
+  int64_t u = lane;
+  if (u < units) {
+#pragma unroll
+    for (int i = 0; i < R; ++i) cur[i].load(W, row0 + i < W.rows ? row0 + i : row0, u);
+  }
+  for (; u < units; u += 32) {
+    const int64_t un = u + 32;
+    if (un < units) {
+#pragma unroll
+      for (int i = 0; i < R; ++i) nxt[i].load(W, row0 + i < W.rows ? row0 + i : row0, un);
+    }
+    float w[R][KW];
+#pragma unroll
+    for (int i = 0; i < R; ++i) cur[i].codes(w[i]);
+    const int64_t xo = U::x_offset(u);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      if (b < batch) {
+        const float* xp = x + (int64_t)b * W.cols + xo;
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          const float s = dot_x<KW>(w[i], xp);
+          if constexpr (FMT == QD_I8_ROW)
+            acc[i][b] += s;
+          else
+            acc[i][b] = fmaf(cur[i].scale(), s, acc[i][b]);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i) cur[i] = nxt[i];
+  }
+  float row_scale[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    row_scale[i] = 1.0f;
+    if constexpr (FMT == QD_I8_ROW) {
+      const int64_t r = row0 + i < W.rows ? row0 + i : row0;
+      row_scale[i] = __ldg(reinterpret_cast<const float*>(W.scales) + r);
+    }
+  }
+  finish_rows<R, NB>(acc, row_scale, row0, W.rows, y, batch, mode, lane);
+}
+
+// Q4_K: a lane's unit is 16 code bytes of one 32-byte chunk c of a super-block:
+// their low nibbles are 16 elements of sub-block 2c, their high nibbles 16
+// elements of sub-block 2c+1.  With w = d*sc*q - dmin*m per sub-block,
+//   sum w x = (d*sc) * sum q x - (dmin*m) * sum x,
+// and sum x over each half is shared by the warp's rows.
+template <int R, int NB>
+__global__ void __launch_bounds__(kThreads) k_gemv_q4k(PackedView W, const float* __restrict__ x,
+                                                       float* __restrict__ y, int batch, int mode) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row0 = ((int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)) * R;
+  if (row0 >= W.rows) return;
+  const int64_t units = W.cols / 32;  // 8 per super-block
+  float acc[R][NB];
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[i][b] = 0.f;
+
+  for (int64_t u = lane; u < units; u += 32) {
+    const int64_t s = u >> 3;
+    const int c = (int)((u >> 1) & 3), h = (int)(u & 1);
+    float wlo[R][16], whi[R][16], a_lo[R], b_lo[R], a_hi[R], b_hi[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int64_t r = row0 + i < W.rows ? row0 + i : row0;
+      const uint4 q = ld_stream_v4(W.codes + r * W.row_code_bytes + s * 128 + 32 * c + 16 * h);
+      const uint4 hdr = __ldg(reinterpret_cast<const uint4*>(W.scales + r * W.row_scale_bytes + s * 16));
+      uint8_t sb[12];
+      const uint32_t hw[3] = {hdr.y, hdr.z, hdr.w};
+#pragma unroll
+      for (int k = 0; k < 12; ++k) sb[k] = (uint8_t)(hw[k >> 2] >> (8 * (k & 3)));
+      int sc0, m0, sc1, m1;
+      q4k_scale_min(2 * c, sb, sc0, m0);
+      q4k_scale_min(2 * c + 1, sb, sc1, m1);
+      const float d = f16_bits_to_f32(hdr.x & 0xFFFFu), dmin = f16_bits_to_f32(hdr.x >> 16);
+      a_lo[i] = d * (float)sc0;
+      b_lo[i] = dmin * (float)m0;
+      a_hi[i] = d * (float)sc1;
+      b_hi[i] = dmin * (float)m1;
+      const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const uint32_t lo = words[t] & 0x0F0F0F0Fu, hi = (words[t] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          wlo[i][4 * t + k] = byte_as_magic(lo, k) - kMagic;
+          whi[i][4 * t + k] = byte_as_magic(hi, k) - kMagic;
+        }
+      }
+    }
+    const int64_t xo = s * 256 + 64 * c + 16 * h;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      if (b < batch) {
+        const float* xp = x + (int64_t)b * W.cols + xo;
+        const float4* xl = reinterpret_cast<const float4*>(xp);
+        const float4* xh = reinterpret_cast<const float4*>(xp + 32);
+        float sxl = 0.f, sxh = 0.f;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float4 vl = __ldg(xl + t), vh = __ldg(xh + t);
+          sxl += (vl.x + vl.y) + (vl.z + vl.w);
+          sxh += (vh.x + vh.y) + (vh.z + vh.w);
+        }
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          const float ql = dot_x<16>(wlo[i], xp);
+          const float qh = dot_x<16>(whi[i], xp + 32);
+          float v = fmaf(a_lo[i], ql, -b_lo[i] * sxl);
+          v = fmaf(a_hi[i], qh, fmaf(-b_hi[i], sxh, v));
+          acc[i][b] += v;
+        }
+      }
+    }
+  }
+  float row_scale[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) row_scale[i] = 1.0f;
+  finish_rows<R, NB>(acc, row_scale, row0, W.rows, y, batch, mode, lane);
+}
+
+template <int FMT, int R, int NB>
+qd_status launch_t(const PackedView& W, const float* x, float* y, int batch, int mode, cudaStream_t stream) {
+  const int64_t warps = (W.rows + R - 1) / R;
+  const int64_t ctas = (warps + kWarpsPerCta - 1) / kWarpsPerCta;
+  if constexpr (FMT == QD_Q4_K)
+    k_gemv_q4k<R, NB><<<(unsigned)ctas, kThreads, 0, stream>>>(W, x, y, batch, mode);
+  else
+    k_gemv_blocks<FMT, R, NB><<<(unsigned)ctas, kThreads, 0, stream>>>(W, x, y, batch, mode);
+  return launch_status();
+}
+
+template <int FMT>
+qd_status launch_fmt(const PackedView& W, const float* x, float* y, int batch, int mode, cudaStream_t stream) {
+  // The SwiGLU epilogue needs each (gate, up) row pair in one warp: R = 2.
+  const bool pair = (mode == kGemvSwiGLU);
+  if (batch <= 1) return pair ? launch_t<FMT, 2, 1>(W, x, y, batch, mode, stream)
+                              : launch_t<FMT, 2, 1>(W, x, y, batch, mode, stream);
+  if (batch <= 2) return launch_t<FMT, 2, 2>(W, x, y, batch, mode, stream);
+  if (batch <= 4) return pair ? launch_t<FMT, 2, 4>(W, x, y, batch, mode, stream)
+                              : launch_t<FMT, 1, 4>(W, x, y, batch, mode, stream);
+  if (batch <= 8) return pair ? launch_t<FMT, 2, 8>(W, x, y, batch, mode, stream)
+                              : launch_t<FMT, 1, 8>(W, x, y, batch, mode, stream);
+  return pair ? launch_t<FMT, 2, 16>(W, x, y, batch, mode, stream)
+              : launch_t<FMT, 1, 16>(W, x, y, batch, mode, stream);
+}
+
+}  // namespace
+
+qd_status launch_q_gemv(int fmt, const PackedView& W, const float* x, float* y, int batch, GemvMode mode,
+                        cudaStream_t stream) {
+  switch (fmt) {
+    case QD_Q4_0: return launch_fmt<QD_Q4_0>(W, x, y, batch, mode, stream);
+    case QD_Q8_0: return launch_fmt<QD_Q8_0>(W, x, y, batch, mode, stream);
+    case QD_Q4_K: return launch_fmt<QD_Q4_K>(W, x, y, batch, mode, stream);
+    case QD_I8_ROW: return launch_fmt<QD_I8_ROW>(W, x, y, batch, mode, stream);
+    default: return QD_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace qd
+
+using namespace qd;
+
+extern "C" {
+
+size_t qd_q_gemv_workspace(qd_fmt fmt, int64_t rows, int64_t cols, int batch) {
+  (void)fmt;
+  (void)rows;
+  (void)cols;
+  (void)batch;
+  return 0;
+}
+
+qd_status qd_q_gemv(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch,
+                    void* workspace, size_t workspace_bytes, qd_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (!fmt_ok(fmt)) return QD_ERR_UNSUPPORTED;
+  if (!W || !x || !y) return QD_ERR_INVALID_ARG;
+  if (batch < 1 || batch > QD_MAX_BATCH) return QD_ERR_SHAPE;
+  if (!shape_ok(fmt, rows, cols)) return QD_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(x) || !aligned16(y)) return QD_ERR_ALIGN;
+  return launch_q_gemv(fmt, packed_view(fmt, W, rows, cols), x, y, batch, kGemvStore, (cudaStream_t)stream);
+}
+
+}  // extern "C"

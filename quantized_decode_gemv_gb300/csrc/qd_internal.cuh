@@ -1,0 +1,210 @@
+// Internal declarations shared by the libqdecode translation units.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/qdecode.h"
+
+namespace qd {
+
+constexpr int kWarp = 32;
+
+// Bits of the device error word.
+constexpr uint32_t kErrToken = 1u;     // token id outside [0, vocab)
+constexpr uint32_t kErrPosition = 2u;  // position outside [0, max_ctx)
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline qd_status launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? QD_OK : QD_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Packed layout of one tensor (see qdecode.h, "Load-time repacking").
+//   codes: per row, `row_code_bytes` contiguous bytes (16-byte aligned rows)
+//   scales: per row, `row_scale_bytes` contiguous bytes (f16 d per block for
+//           Q4_0/Q8_0, 16-byte headers per super-block for Q4_K, one f32 for I8)
+// ---------------------------------------------------------------------------
+struct PackedView {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  int64_t rows, cols;
+  int64_t row_code_bytes, row_scale_bytes;
+};
+
+__host__ __device__ inline int64_t row_code_bytes(int fmt, int64_t cols) {
+  switch (fmt) {
+    case QD_Q4_0: return cols / 2;
+    case QD_Q8_0: return cols;
+    case QD_Q4_K: return cols / 2;
+    default: return cols;  // QD_I8_ROW
+  }
+}
+
+__host__ __device__ inline int64_t row_scale_bytes(int fmt, int64_t cols) {
+  switch (fmt) {
+    case QD_Q4_0:
+    case QD_Q8_0: return (cols / 32) * 2;
+    case QD_Q4_K: return (cols / 256) * 16;
+    default: return 4;
+  }
+}
+
+inline bool shape_ok(int fmt, int64_t rows, int64_t cols) {
+  if (rows < 1 || cols < 1) return false;
+  switch (fmt) {
+    case QD_Q4_0:
+    case QD_Q8_0: return cols % 32 == 0;
+    case QD_Q4_K: return cols % 256 == 0;
+    case QD_I8_ROW: return cols % 16 == 0;
+    default: return false;
+  }
+}
+
+inline bool fmt_ok(int fmt) { return fmt >= QD_Q4_0 && fmt <= QD_I8_ROW; }
+
+inline size_t packed_code_region(int fmt, int64_t rows, int64_t cols) {
+  return align_up((size_t)rows * (size_t)row_code_bytes(fmt, cols), 16);
+}
+
+inline size_t packed_bytes(int fmt, int64_t rows, int64_t cols) {
+  if (!fmt_ok(fmt) || !shape_ok(fmt, rows, cols)) return 0;
+  return packed_code_region(fmt, rows, cols) + align_up((size_t)rows * (size_t)row_scale_bytes(fmt, cols), 16);
+}
+
+inline size_t src_bytes(int fmt, int64_t rows, int64_t cols) {
+  if (!fmt_ok(fmt) || !shape_ok(fmt, rows, cols)) return 0;
+  switch (fmt) {
+    case QD_Q4_0: return (size_t)rows * (cols / 32) * 18;
+    case QD_Q8_0: return (size_t)rows * (cols / 32) * 34;
+    case QD_Q4_K: return (size_t)rows * (cols / 256) * 144;
+    default: return (size_t)rows * cols + 4 * (size_t)rows;
+  }
+}
+
+inline PackedView packed_view(int fmt, const void* base, int64_t rows, int64_t cols) {
+  PackedView v;
+  v.codes = static_cast<const uint8_t*>(base);
+  v.scales = v.codes + packed_code_region(fmt, rows, cols);
+  v.rows = rows;
+  v.cols = cols;
+  v.row_code_bytes = row_code_bytes(fmt, cols);
+  v.row_scale_bytes = row_scale_bytes(fmt, cols);
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t h) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+}
+
+// Streaming 16-byte load that bypasses L1 allocation (weights are read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Byte k of w (as an unsigned 0..255) turned into the float 2^23 + byte:
+// the byte lands in the low mantissa bits of 0x4B000000.
+__device__ __forceinline__ float byte_as_magic(uint32_t w, int k) {
+  return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | (uint32_t)k));
+}
+
+constexpr float kMagic = 8388608.0f;  // 2^23
+
+// Q4_K: 6-bit (scale, min) of sub-block j from the 12-byte field q.
+__device__ __forceinline__ void q4k_scale_min(int j, const uint8_t* q, int& sc, int& m) {
+  if (j < 4) {
+    sc = q[j] & 63;
+    m = q[j + 4] & 63;
+  } else {
+    sc = (q[j + 4] & 0x0F) | ((q[j - 4] >> 6) << 4);
+    m = (q[j + 4] >> 4) | ((q[j] >> 6) << 4);
+  }
+}
+
+// One dequantised weight (row r, column c) of a packed tensor, rounded once to
+// f32.  Used by the embedding lookup and the test dequantiser; the GEMV kernels
+// never materialise weights.
+__device__ __forceinline__ float dequant_elem(int fmt, const PackedView& W, int64_t r, int64_t c) {
+  const uint8_t* code_row = W.codes + r * W.row_code_bytes;
+  const uint8_t* sc_row = W.scales + r * W.row_scale_bytes;
+  if (fmt == QD_Q4_0) {
+    const int64_t b = c >> 5;
+    const int j = (int)(c & 31);
+    const uint8_t byte = code_row[b * 16 + (j & 15)];
+    const int q = (j < 16) ? (byte & 15) : (byte >> 4);
+    const float d = f16_bits_to_f32(sc_row[2 * b] | (sc_row[2 * b + 1] << 8));
+    return (float)(q - 8) * d;
+  } else if (fmt == QD_Q8_0) {
+    const int64_t b = c >> 5;
+    const float d = f16_bits_to_f32(sc_row[2 * b] | (sc_row[2 * b + 1] << 8));
+    return (float)(int8_t)code_row[c] * d;
+  } else if (fmt == QD_Q4_K) {
+    const int64_t s = c >> 8;
+    const int e = (int)(c & 255);
+    const int chunk = e >> 6, hi = (e >> 5) & 1, l = e & 31;
+    const uint8_t* hdr = sc_row + s * 16;
+    const float d = f16_bits_to_f32(hdr[0] | (hdr[1] << 8));
+    const float dmin = f16_bits_to_f32(hdr[2] | (hdr[3] << 8));
+    int sc, m;
+    q4k_scale_min(2 * chunk + hi, hdr + 4, sc, m);
+    const uint8_t byte = code_row[s * 128 + 32 * chunk + l];
+    const int q = hi ? (byte >> 4) : (byte & 15);
+    // d*sc is exact in f32; the fma rounds d*sc*q - dmin*m once.
+    return fmaf(d * (float)sc, (float)q, -(dmin * (float)m));
+  } else {
+    float s;
+    memcpy(&s, sc_row, 4);
+    return (float)(int8_t)code_row[c] * s;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Launchers shared between translation units (return QD_OK or QD_ERR_CUDA)
+// ---------------------------------------------------------------------------
+enum GemvMode { kGemvStore = 0, kGemvAccumulate = 1, kGemvSwiGLU = 2 };
+
+// y = W x (mode store), y += W x (accumulate), or for rows interleaved as
+// (gate_i, up_i) pairs: y[b][i] = silu(gate_i . x) * (up_i . x) (swiglu; y has
+// rows/2 columns per batch row).
+qd_status launch_q_gemv(int fmt, const PackedView& W, const float* x, float* y, int batch, GemvMode mode,
+                        cudaStream_t stream);
+
+qd_status launch_rmsnorm(const float* x, const float* g, float* out, int n, int batch, float eps,
+                         cudaStream_t stream);
+qd_status launch_rope(float* v, int n_heads, int head_dim, int64_t batch_stride, const int32_t* pos, int pairing,
+                      const float* cos_sin, int max_ctx, int batch, uint32_t* err, cudaStream_t stream);
+qd_status launch_kv_append(const float* k, const float* v, int64_t src_stride, float* kc, float* vc, int n_kv,
+                           int head_dim, const int32_t* pos, int max_ctx, int batch, int64_t cache_batch_stride,
+                           uint32_t* err, cudaStream_t stream);
+size_t attn_workspace_bytes(int n_heads, int head_dim, int max_ctx, int batch);
+qd_status launch_attention(const float* q, int64_t q_stride, const float* kc, const float* vc,
+                           int64_t cache_batch_stride, float* out, int n_heads, int n_kv, int head_dim,
+                           const int32_t* pos, int max_ctx, int batch, void* ws, uint32_t* err,
+                           cudaStream_t stream);
+qd_status launch_swiglu(const float* g, const float* u, float* out, int64_t n, int batch, cudaStream_t stream);
+qd_status launch_argmax(const float* logits, int64_t n, int batch, int32_t* out, int32_t* pos_to_advance,
+                        cudaStream_t stream);
+qd_status launch_embed(int fmt, const PackedView& E, const int32_t* tokens, int batch, float* x, uint32_t* err,
+                       cudaStream_t stream);
+qd_status launch_repack_rows(int fmt, const void* src, int64_t n_rows, int64_t cols, void* dst_base,
+                             int64_t dst_rows, int64_t dst_row0, int64_t dst_row_step, cudaStream_t stream);
+
+}  // namespace qd

@@ -1,0 +1,217 @@
+// Load-time weight repacking, its inverse, the test dequantiser, and the f16 /
+// bf16 conversions.
+//
+// The pages' loaders hand each block to the GPU as it sits in the model file
+// (an 18-, 34- or 144-byte record).  Those records are not 16-byte aligned, so
+// the repack splits every tensor into a code region (16 B per Q4_0 block, 32 B
+// per Q8_0 block, 128 B per Q4_K super-block, one byte per INT8 weight) and a
+// scale region (f16 d per block, the 16-byte d/dmin/scales header per Q4_K
+// super-block, one f32 per INT8 row), both row-major.  Nothing is re-encoded:
+// the scales stay f16 (the Go "llm" package's "Design points" widen them to f32
+// only because its shading language has no f16), so the packed tensor is the
+// same number of bytes as the source plus at most 30 bytes of padding.
+#include "qd_internal.cuh"
+
+namespace qd {
+namespace {
+
+struct BlockGeom {
+  int src_bytes;    // bytes of one source block
+  int weights;      // weights per block
+  int code_off;     // offset of the codes inside the source block
+  int code_bytes;   // bytes of codes per block
+  int scale_bytes;  // bytes of scale data per block (copied from offset 0)
+};
+
+__host__ __device__ inline BlockGeom geom(int fmt) {
+  switch (fmt) {
+    case QD_Q4_0: return {18, 32, 2, 16, 2};
+    case QD_Q8_0: return {34, 32, 2, 32, 2};
+    default: return {144, 256, 16, 128, 16};  // QD_Q4_K
+  }
+}
+
+// One thread per (source row, block): copy its codes and its scale bytes.
+__global__ void k_repack_blocks(int fmt, const uint8_t* __restrict__ src, int64_t n_rows, int64_t nb,
+                                uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int64_t dst_row0,
+                                int64_t dst_step) {
+  const BlockGeom g = geom(fmt);
+  const int64_t total = n_rows * nb;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = t / nb, b = t % nb;
+    const int64_t r = dst_row0 + i * dst_step;
+    const uint8_t* s = src + t * g.src_bytes;
+    uint8_t* c = codes + (r * nb + b) * g.code_bytes;
+    uint8_t* sc = scales + (r * nb + b) * g.scale_bytes;
+    for (int k = 0; k < g.code_bytes; ++k) c[k] = s[g.code_off + k];
+    for (int k = 0; k < g.scale_bytes; ++k) sc[k] = s[k];
+  }
+}
+
+__global__ void k_unpack_blocks(int fmt, const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                                int64_t rows, int64_t nb, uint8_t* __restrict__ dst) {
+  const BlockGeom g = geom(fmt);
+  const int64_t total = rows * nb;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
+    uint8_t* d = dst + t * g.src_bytes;
+    const uint8_t* c = codes + t * g.code_bytes;
+    const uint8_t* sc = scales + t * g.scale_bytes;
+    for (int k = 0; k < g.scale_bytes; ++k) d[k] = sc[k];
+    for (int k = 0; k < g.code_bytes; ++k) d[g.code_off + k] = c[k];
+  }
+}
+
+// INT8 rows: codes copy 16 bytes per thread, scales one f32 per row.
+__global__ void k_repack_i8(const uint8_t* __restrict__ src, int64_t n_rows, int64_t cols,
+                            uint8_t* __restrict__ codes, float* __restrict__ scales, int64_t dst_row0,
+                            int64_t dst_step) {
+  const int64_t chunks = cols / 16;
+  const int64_t total = n_rows * chunks;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = t / chunks, c = t % chunks;
+    const int64_t r = dst_row0 + i * dst_step;
+    const uint8_t* s = src + i * cols + c * 16;
+    uint8_t* d = codes + r * cols + c * 16;
+    for (int k = 0; k < 16; ++k) d[k] = s[k];  // source rows are only byte-aligned in general
+    if (c == 0) {
+      float v;
+      memcpy(&v, src + n_rows * cols + 4 * i, 4);
+      scales[r] = v;
+    }
+  }
+}
+
+__global__ void k_unpack_i8(const uint8_t* __restrict__ codes, const float* __restrict__ scales, int64_t rows,
+                            int64_t cols, uint8_t* __restrict__ dst) {
+  const int64_t total = rows * cols;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
+    dst[t] = codes[t];
+    if (t % cols == 0) {
+      const float v = scales[t / cols];
+      memcpy(dst + total + 4 * (t / cols), &v, 4);
+    }
+  }
+}
+
+__global__ void k_dequant(int fmt, PackedView W, float* __restrict__ out) {
+  const int64_t total = W.rows * W.cols;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x)
+    out[t] = dequant_elem(fmt, W, t / W.cols, t % W.cols);
+}
+
+__global__ void k_f16_to_f32(const uint16_t* __restrict__ in, float* __restrict__ out, int64_t n) {
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x)
+    out[t] = f16_bits_to_f32(in[t]);
+}
+
+// bf16 -> f32 is the zero-extension of the bit pattern (minillm-cpp README, "Loader").
+__global__ void k_bf16_to_f32(const uint16_t* __restrict__ in, float* __restrict__ out, int64_t n) {
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x)
+    out[t] = __uint_as_float((uint32_t)in[t] << 16);
+}
+
+inline int grid_for(int64_t n, int threads) {
+  int64_t g = (n + threads - 1) / threads;
+  if (g < 1) g = 1;
+  return (int)(g > 65535 * 8 ? 65535 * 8 : g);
+}
+
+}  // namespace
+
+qd_status launch_repack_rows(int fmt, const void* src, int64_t n_rows, int64_t cols, void* dst_base,
+                             int64_t dst_rows, int64_t dst_row0, int64_t dst_row_step, cudaStream_t stream) {
+  PackedView v = packed_view(fmt, dst_base, dst_rows, cols);
+  uint8_t* codes = const_cast<uint8_t*>(v.codes);
+  uint8_t* scales = const_cast<uint8_t*>(v.scales);
+  if (fmt == QD_I8_ROW) {
+    const int64_t n = n_rows * (cols / 16);
+    k_repack_i8<<<grid_for(n, 256), 256, 0, stream>>>(static_cast<const uint8_t*>(src), n_rows, cols, codes,
+                                                       reinterpret_cast<float*>(scales), dst_row0, dst_row_step);
+  } else {
+    const int64_t nb = cols / geom(fmt).weights;
+    k_repack_blocks<<<grid_for(n_rows * nb, 256), 256, 0, stream>>>(fmt, static_cast<const uint8_t*>(src), n_rows,
+                                                                    nb, codes, scales, dst_row0, dst_row_step);
+  }
+  return launch_status();
+}
+
+}  // namespace qd
+
+using namespace qd;
+
+extern "C" {
+
+const char* qd_status_str(qd_status s) {
+  switch (s) {
+    case QD_OK: return "ok";
+    case QD_ERR_INVALID_ARG: return "invalid argument";
+    case QD_ERR_SHAPE: return "shape not allowed";
+    case QD_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case QD_ERR_UNSUPPORTED: return "unsupported format or configuration";
+    case QD_ERR_CUDA: return "CUDA error";
+    case QD_ERR_NOMEM: return "buffer too small";
+    case QD_ERR_DEVICE_FLAG: return "a kernel flagged an out-of-range token or position";
+    default: return "unknown status";
+  }
+}
+
+int qd_abi_version(void) { return 1; }
+
+size_t qd_src_bytes(qd_fmt fmt, int64_t rows, int64_t cols) { return src_bytes(fmt, rows, cols); }
+size_t qd_packed_bytes(qd_fmt fmt, int64_t rows, int64_t cols) { return packed_bytes(fmt, rows, cols); }
+
+qd_status qd_repack(qd_fmt fmt, const void* src, int64_t rows, int64_t cols, void* dst, size_t dst_bytes,
+                    qd_stream_t stream) {
+  if (!fmt_ok(fmt)) return QD_ERR_UNSUPPORTED;
+  if (!src || !dst) return QD_ERR_INVALID_ARG;
+  if (!shape_ok(fmt, rows, cols)) return QD_ERR_SHAPE;
+  if (!aligned16(dst)) return QD_ERR_ALIGN;
+  if (dst_bytes < packed_bytes(fmt, rows, cols)) return QD_ERR_NOMEM;
+  return launch_repack_rows(fmt, src, rows, cols, dst, rows, 0, 1, (cudaStream_t)stream);
+}
+
+qd_status qd_unpack(qd_fmt fmt, const void* packed, int64_t rows, int64_t cols, void* dst, size_t dst_bytes,
+                    qd_stream_t stream) {
+  if (!fmt_ok(fmt)) return QD_ERR_UNSUPPORTED;
+  if (!packed || !dst) return QD_ERR_INVALID_ARG;
+  if (!shape_ok(fmt, rows, cols)) return QD_ERR_SHAPE;
+  if (!aligned16(packed)) return QD_ERR_ALIGN;
+  if (dst_bytes < src_bytes(fmt, rows, cols)) return QD_ERR_NOMEM;
+  PackedView v = packed_view(fmt, packed, rows, cols);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (fmt == QD_I8_ROW) {
+    k_unpack_i8<<<grid_for(rows * cols, 256), 256, 0, s>>>(v.codes, reinterpret_cast<const float*>(v.scales), rows,
+                                                            cols, static_cast<uint8_t*>(dst));
+  } else {
+    const int64_t nb = cols / geom(fmt).weights;
+    k_unpack_blocks<<<grid_for(rows * nb, 256), 256, 0, s>>>(fmt, v.codes, v.scales, rows, nb,
+                                                             static_cast<uint8_t*>(dst));
+  }
+  return launch_status();
+}
+
+qd_status qd_dequant(qd_fmt fmt, const void* packed, int64_t rows, int64_t cols, float* out, qd_stream_t stream) {
+  if (!fmt_ok(fmt)) return QD_ERR_UNSUPPORTED;
+  if (!packed || !out) return QD_ERR_INVALID_ARG;
+  if (!shape_ok(fmt, rows, cols)) return QD_ERR_SHAPE;
+  if (!aligned16(packed) || !aligned16(out)) return QD_ERR_ALIGN;
+  k_dequant<<<grid_for(rows * cols, 256), 256, 0, (cudaStream_t)stream>>>(fmt, packed_view(fmt, packed, rows, cols),
+                                                                          out);
+  return launch_status();
+}
+
+qd_status qd_f16_to_f32(const uint16_t* in, float* out, int64_t n, qd_stream_t stream) {
+  if (n < 0 || (n > 0 && (!in || !out))) return QD_ERR_INVALID_ARG;
+  if (n == 0) return QD_OK;
+  k_f16_to_f32<<<grid_for(n, 256), 256, 0, (cudaStream_t)stream>>>(in, out, n);
+  return launch_status();
+}
+
+qd_status qd_bf16_to_f32(const uint16_t* in, float* out, int64_t n, qd_stream_t stream) {
+  if (n < 0 || (n > 0 && (!in || !out))) return QD_ERR_INVALID_ARG;
+  if (n == 0) return QD_OK;
+  k_bf16_to_f32<<<grid_for(n, 256), 256, 0, (cudaStream_t)stream>>>(in, out, n);
+  return launch_status();
+}
+
+}  // extern "C"

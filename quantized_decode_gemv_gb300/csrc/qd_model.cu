@@ -1,0 +1,359 @@
+// The decode-step driver: a llama-style model over caller-owned weight and state
+// memory, one CUDA graph replay per token.
+//
+// Step order (llmoxide blog s7 "The block, and the residual stream"; dasLLAMA
+// 8.7.1.6 forward):
+//   x = embed(token)
+//   per layer: xn = rmsnorm(x)*attn_norm; [q|k|v] = Wqkv xn; rope(q, k) at pos;
+//              cache[pos] = k, v; o = attention(q, cache[0..pos]); x += Wo o;
+//              xn = rmsnorm(x)*ffn_norm; a = silu(Wg xn) * (Wu xn); x += Wd a
+//   logits = W_out (rmsnorm(x)*out_norm); token = argmax(logits); pos += 1
+// As in the Go "llm" package ("Design points": one submit per token, only the
+// 4-byte token read back), the whole step is recorded once and replayed: here as
+// a CUDA graph per batch size whose kernels read each sequence's position from
+// device memory, so the same graph serves every token.
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "qd_internal.cuh"
+
+using namespace qd;
+
+namespace {
+
+struct LayerOff {
+  size_t attn_norm, ffn_norm, wqkv, wo, wgu, wd;
+};
+
+struct Layout {
+  // weights
+  size_t emb, head, out_norm;
+  std::vector<LayerOff> layer;
+  size_t weight_bytes;
+  // state
+  size_t kc, vc, x, xn, qkv, att, act, logits, attn_ws, tok_in, tok_out, pos, err, rope;
+  size_t state_bytes;
+  int64_t qkv_rows, cache_batch_stride, cache_layer_stride;
+};
+
+bool config_ok(const qd_config* c) {
+  if (!c) return false;
+  if (c->layers < 1 || c->dim < 1 || c->ffn < 1 || c->n_heads < 1 || c->n_kv_heads < 1 || c->vocab < 1) return false;
+  if (c->head_dim != 64) return false;  // the decode-attention kernel's head width
+  if (c->n_heads % c->n_kv_heads || c->n_heads / c->n_kv_heads > 8) return false;
+  if (c->max_ctx < 1 || c->max_batch < 1 || c->max_batch > QD_MAX_BATCH) return false;
+  if (c->pairing != QD_ROPE_ADJACENT && c->pairing != QD_ROPE_HALF) return false;
+  if (!fmt_ok(c->w_fmt) || !fmt_ok(c->emb_fmt)) return false;
+  if (!(c->eps >= 0.f) || !(c->rope_theta > 0.f)) return false;
+  const int64_t QD = (int64_t)c->n_heads * c->head_dim, KD = (int64_t)c->n_kv_heads * c->head_dim;
+  if (!shape_ok(c->w_fmt, QD + 2 * KD, c->dim) || !shape_ok(c->w_fmt, c->dim, QD) ||
+      !shape_ok(c->w_fmt, 2 * (int64_t)c->ffn, c->dim) || !shape_ok(c->w_fmt, c->dim, c->ffn))
+    return false;
+  if (!shape_ok(c->emb_fmt, c->vocab, c->dim)) return false;
+  return true;
+}
+
+Layout make_layout(const qd_config* c) {
+  Layout L{};
+  const int64_t D = c->dim, F = c->ffn, QD = (int64_t)c->n_heads * c->head_dim;
+  const int64_t KD = (int64_t)c->n_kv_heads * c->head_dim, B = c->max_batch;
+  L.qkv_rows = QD + 2 * KD;
+  size_t off = 0;
+  auto take = [&off](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.emb = take(packed_bytes(c->emb_fmt, c->vocab, D));
+  L.head = c->tied ? L.emb : take(packed_bytes(c->emb_fmt, c->vocab, D));
+  L.out_norm = take(4 * D);
+  L.layer.resize(c->layers);
+  for (int l = 0; l < c->layers; ++l) {
+    LayerOff& o = L.layer[l];
+    o.attn_norm = take(4 * D);
+    o.ffn_norm = take(4 * D);
+    o.wqkv = take(packed_bytes(c->w_fmt, L.qkv_rows, D));
+    o.wo = take(packed_bytes(c->w_fmt, D, QD));
+    o.wgu = take(packed_bytes(c->w_fmt, 2 * F, D));
+    o.wd = take(packed_bytes(c->w_fmt, D, F));
+  }
+  L.weight_bytes = off;
+
+  off = 0;
+  L.cache_batch_stride = KD * c->max_ctx;
+  L.cache_layer_stride = L.cache_batch_stride * B;
+  const size_t cache = (size_t)c->layers * L.cache_layer_stride * 4;
+  L.kc = take(cache);
+  L.vc = take(cache);
+  L.x = take(4 * B * D);
+  L.xn = take(4 * B * D);
+  L.qkv = take(4 * B * L.qkv_rows);
+  L.att = take(4 * B * QD);
+  L.act = take(4 * B * F);
+  L.logits = take(4 * B * (size_t)c->vocab);
+  L.attn_ws = take(attn_workspace_bytes(c->n_heads, c->head_dim, c->max_ctx, (int)B));
+  L.tok_in = take(4 * B);
+  L.tok_out = take(4 * B);
+  L.pos = take(4 * B);
+  L.err = take(4);
+  L.rope = take((size_t)c->max_ctx * c->head_dim * 4);
+  L.state_bytes = off;
+  return L;
+}
+
+__global__ void k_fill_zero(uint4* __restrict__ p, int64_t n16) {
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n16; t += (int64_t)gridDim.x * blockDim.x)
+    p[t] = make_uint4(0, 0, 0, 0);
+}
+
+qd_status zero_region(void* p, size_t bytes, cudaStream_t s) {
+  const int64_t n16 = (int64_t)(bytes / 16);
+  if (n16 == 0) return QD_OK;
+  int64_t g = (n16 + 255) / 256;
+  if (g > 152 * 64) g = 152 * 64;
+  k_fill_zero<<<(unsigned)g, 256, 0, s>>>(static_cast<uint4*>(p), n16);
+  return launch_status();
+}
+
+}  // namespace
+
+struct qd_model {
+  qd_config cfg;
+  Layout L;
+  uint8_t* w;  // weight memory (caller-owned)
+  uint8_t* s;  // state memory (caller-owned)
+  cudaStream_t capture_stream = nullptr;
+  cudaGraphExec_t graph[QD_MAX_BATCH + 1] = {};
+  int launches = 0;
+
+  float* f(size_t off) { return reinterpret_cast<float*>(s + off); }
+  int32_t* i(size_t off) { return reinterpret_cast<int32_t*>(s + off); }
+  PackedView W(int fmt, size_t off, int64_t rows, int64_t cols) const { return packed_view(fmt, w + off, rows, cols); }
+};
+
+namespace {
+
+#define QD_TRY(expr)                   \
+  do {                                 \
+    const qd_status st_ = (expr);      \
+    if (st_ != QD_OK) return st_;      \
+  } while (0)
+
+// Enqueue one decode step for `batch` sequences; counts the kernels it launches.
+qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
+  const qd_config& c = m->cfg;
+  const Layout& L = m->L;
+  const int64_t D = c.dim, F = c.ffn, QD = (int64_t)c.n_heads * c.head_dim, KD = (int64_t)c.n_kv_heads * c.head_dim;
+  uint32_t* err = reinterpret_cast<uint32_t*>(m->s + L.err);
+  const int32_t* pos = m->i(L.pos);
+  float *x = m->f(L.x), *xn = m->f(L.xn), *qkv = m->f(L.qkv), *att = m->f(L.att), *act = m->f(L.act);
+  int n = 0;
+  QD_TRY(launch_embed(c.emb_fmt, m->W(c.emb_fmt, L.emb, c.vocab, D), m->i(L.tok_in), batch, x, err, st));
+  ++n;
+  for (int l = 0; l < c.layers; ++l) {
+    const LayerOff& o = L.layer[l];
+    float* kc = m->f(L.kc) + (int64_t)l * L.cache_layer_stride;
+    float* vc = m->f(L.vc) + (int64_t)l * L.cache_layer_stride;
+    QD_TRY(launch_rmsnorm(x, reinterpret_cast<const float*>(m->w + o.attn_norm), xn, (int)D, batch, c.eps, st));
+    QD_TRY(launch_q_gemv(c.w_fmt, m->W(c.w_fmt, o.wqkv, L.qkv_rows, D), xn, qkv, batch, kGemvStore, st));
+    // q heads and k heads are adjacent in the fused output: one rotation pass
+    QD_TRY(launch_rope(qkv, c.n_heads + c.n_kv_heads, c.head_dim, L.qkv_rows, pos, c.pairing, m->f(L.rope),
+                       c.max_ctx, batch, err, st));
+    QD_TRY(launch_kv_append(qkv + QD, qkv + QD + KD, L.qkv_rows, kc, vc, c.n_kv_heads, c.head_dim, pos, c.max_ctx,
+                            batch, L.cache_batch_stride, err, st));
+    QD_TRY(launch_attention(qkv, L.qkv_rows, kc, vc, L.cache_batch_stride, att, c.n_heads, c.n_kv_heads, c.head_dim,
+                            pos, c.max_ctx, batch, m->s + L.attn_ws, err, st));
+    QD_TRY(launch_q_gemv(c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, x, batch, kGemvAccumulate, st));
+    QD_TRY(launch_rmsnorm(x, reinterpret_cast<const float*>(m->w + o.ffn_norm), xn, (int)D, batch, c.eps, st));
+    QD_TRY(launch_q_gemv(c.w_fmt, m->W(c.w_fmt, o.wgu, 2 * F, D), xn, act, batch, kGemvSwiGLU, st));
+    QD_TRY(launch_q_gemv(c.w_fmt, m->W(c.w_fmt, o.wd, D, F), act, x, batch, kGemvAccumulate, st));
+    n += 10;  // rmsnorm, qkv, rope, kv, attention (2), wo, rmsnorm, gate/up, wd
+  }
+  QD_TRY(launch_rmsnorm(x, reinterpret_cast<const float*>(m->w + L.out_norm), xn, (int)D, batch, c.eps, st));
+  QD_TRY(launch_q_gemv(c.emb_fmt, m->W(c.emb_fmt, L.head, c.vocab, D), xn, m->f(L.logits), batch, kGemvStore, st));
+  QD_TRY(launch_argmax(m->f(L.logits), c.vocab, batch, m->i(L.tok_out), m->i(L.pos), st));
+  n += 3;
+  m->launches = n;
+  return QD_OK;
+}
+
+qd_status get_graph(qd_model* m, int batch, cudaGraphExec_t* out) {
+  if (m->graph[batch]) {
+    *out = m->graph[batch];
+    return QD_OK;
+  }
+  cudaStream_t cs = m->capture_stream;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return QD_ERR_CUDA;
+  const qd_status st = enqueue_step(m, batch, cs);
+  cudaGraph_t g = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(cs, &g);
+  if (st != QD_OK || e != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return st != QD_OK ? st : QD_ERR_CUDA;
+  }
+  cudaGraphExec_t ex = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&ex, g, 0);
+  cudaGraphDestroy(g);
+  if (ei != cudaSuccess) return QD_ERR_CUDA;
+  m->graph[batch] = ex;
+  *out = ex;
+  return QD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t qd_model_weight_bytes(const qd_config* cfg) { return config_ok(cfg) ? make_layout(cfg).weight_bytes : 0; }
+size_t qd_model_state_bytes(const qd_config* cfg) { return config_ok(cfg) ? make_layout(cfg).state_bytes : 0; }
+
+qd_status qd_model_create(const qd_config* cfg, const void* const* src, void* weight_mem, size_t weight_bytes,
+                          void* state_mem, size_t state_bytes, qd_stream_t stream, qd_model** out) {
+  if (!cfg || !src || !weight_mem || !state_mem || !out) return QD_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!config_ok(cfg)) return QD_ERR_UNSUPPORTED;
+  const int nt = 3 + 9 * cfg->layers;
+  for (int t = 0; t < nt; ++t)
+    if (!src[t] && !(t == 2 && cfg->tied)) return QD_ERR_INVALID_ARG;
+  if (!aligned16(weight_mem) || !aligned16(state_mem)) return QD_ERR_ALIGN;
+  for (int l = 0; l < cfg->layers; ++l)
+    if (!aligned16(src[3 + 9 * l]) || !aligned16(src[3 + 9 * l + 5])) return QD_ERR_ALIGN;
+  if (!aligned16(src[1])) return QD_ERR_ALIGN;
+  Layout L = make_layout(cfg);
+  if (weight_bytes < L.weight_bytes || state_bytes < L.state_bytes) return QD_ERR_NOMEM;
+
+  qd_model* m = new (std::nothrow) qd_model();
+  if (!m) return QD_ERR_NOMEM;
+  m->cfg = *cfg;
+  m->L = L;
+  m->w = static_cast<uint8_t*>(weight_mem);
+  m->s = static_cast<uint8_t*>(state_mem);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t D = cfg->dim, F = cfg->ffn, QD = (int64_t)cfg->n_heads * cfg->head_dim;
+  const int64_t KD = (int64_t)cfg->n_kv_heads * cfg->head_dim;
+  auto fail = [m](qd_status s) {
+    delete m;
+    return s;
+  };
+  auto copy_f32 = [&](size_t off, const void* p, int64_t n) -> qd_status {
+    return cudaMemcpyAsync(m->w + off, p, 4 * n, cudaMemcpyDeviceToDevice, st) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
+  };
+  qd_status s;
+  if ((s = launch_repack_rows(cfg->emb_fmt, src[0], cfg->vocab, D, m->w + L.emb, cfg->vocab, 0, 1, st))) return fail(s);
+  if (!cfg->tied &&
+      (s = launch_repack_rows(cfg->emb_fmt, src[2], cfg->vocab, D, m->w + L.head, cfg->vocab, 0, 1, st)))
+    return fail(s);
+  if ((s = copy_f32(L.out_norm, src[1], D))) return fail(s);
+  const int wf = cfg->w_fmt;
+  for (int l = 0; l < cfg->layers; ++l) {
+    const void* const* T = src + 3 + 9 * l;
+    const LayerOff& o = L.layer[l];
+    if ((s = copy_f32(o.attn_norm, T[0], D))) return fail(s);
+    if ((s = copy_f32(o.ffn_norm, T[5], D))) return fail(s);
+    // fused QKV: q rows, then k rows, then v rows
+    if ((s = launch_repack_rows(wf, T[1], QD, D, m->w + o.wqkv, L.qkv_rows, 0, 1, st))) return fail(s);
+    if ((s = launch_repack_rows(wf, T[2], KD, D, m->w + o.wqkv, L.qkv_rows, QD, 1, st))) return fail(s);
+    if ((s = launch_repack_rows(wf, T[3], KD, D, m->w + o.wqkv, L.qkv_rows, QD + KD, 1, st))) return fail(s);
+    if ((s = launch_repack_rows(wf, T[4], D, QD, m->w + o.wo, D, 0, 1, st))) return fail(s);
+    // gate/up interleaved: row 2i = gate row i, row 2i+1 = up row i
+    if ((s = launch_repack_rows(wf, T[6], F, D, m->w + o.wgu, 2 * F, 0, 2, st))) return fail(s);
+    if ((s = launch_repack_rows(wf, T[7], F, D, m->w + o.wgu, 2 * F, 1, 2, st))) return fail(s);
+    if ((s = launch_repack_rows(wf, T[8], D, F, m->w + o.wd, D, 0, 1, st))) return fail(s);
+  }
+  if ((s = zero_region(m->s, L.state_bytes, st))) return fail(s);
+  std::vector<float> table((size_t)cfg->max_ctx * cfg->head_dim);
+  if ((s = qd_rope_table(cfg->rope_theta, cfg->head_dim, cfg->max_ctx, table.data()))) return fail(s);
+  if (cudaMemcpyAsync(m->s + L.rope, table.data(), table.size() * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return fail(QD_ERR_CUDA);
+  if (cudaStreamCreateWithFlags(&m->capture_stream, cudaStreamNonBlocking) != cudaSuccess) return fail(QD_ERR_CUDA);
+  *out = m;
+  return QD_OK;
+}
+
+void qd_model_destroy(qd_model* m) {
+  if (!m) return;
+  for (auto& g : m->graph)
+    if (g) cudaGraphExecDestroy(g);
+  if (m->capture_stream) cudaStreamDestroy(m->capture_stream);
+  delete m;
+}
+
+qd_status qd_decode_step(qd_model* m, const int32_t* tokens, int batch, int32_t* out_tokens, float* logits_out,
+                         qd_stream_t stream) {
+  if (!m || !tokens || !out_tokens) return QD_ERR_INVALID_ARG;
+  if (batch < 1 || batch > m->cfg.max_batch) return QD_ERR_SHAPE;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGraphExec_t g;
+  QD_TRY(get_graph(m, batch, &g));
+  if (cudaMemcpyAsync(m->s + m->L.tok_in, tokens, 4 * (size_t)batch, cudaMemcpyDefault, st) != cudaSuccess)
+    return QD_ERR_CUDA;
+  if (cudaGraphLaunch(g, st) != cudaSuccess) return QD_ERR_CUDA;
+  if (cudaMemcpyAsync(out_tokens, m->s + m->L.tok_out, 4 * (size_t)batch, cudaMemcpyDefault, st) != cudaSuccess)
+    return QD_ERR_CUDA;
+  if (logits_out &&
+      cudaMemcpyAsync(logits_out, m->s + m->L.logits, 4 * (size_t)batch * m->cfg.vocab, cudaMemcpyDefault, st) !=
+          cudaSuccess)
+    return QD_ERR_CUDA;
+  return QD_OK;
+}
+
+qd_status qd_model_reset(qd_model* m, qd_stream_t stream) {
+  if (!m) return QD_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t cache = (size_t)m->cfg.layers * m->L.cache_layer_stride * 4;
+  QD_TRY(zero_region(m->s + m->L.kc, align_up(cache, 16), st));
+  QD_TRY(zero_region(m->s + m->L.vc, align_up(cache, 16), st));
+  QD_TRY(zero_region(m->s + m->L.pos, 16 * ((4 * m->cfg.max_batch + 15) / 16), st));
+  QD_TRY(zero_region(m->s + m->L.err, 16, st));
+  return QD_OK;
+}
+
+qd_status qd_model_set_pos(qd_model* m, const int32_t* pos_host, int batch, qd_stream_t stream) {
+  if (!m || !pos_host) return QD_ERR_INVALID_ARG;
+  if (batch < 1 || batch > m->cfg.max_batch) return QD_ERR_SHAPE;
+  for (int b = 0; b < batch; ++b)
+    if (pos_host[b] < 0 || pos_host[b] >= m->cfg.max_ctx) return QD_ERR_SHAPE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(m->s + m->L.pos, pos_host, 4 * (size_t)batch, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return QD_ERR_CUDA;
+  return QD_OK;
+}
+
+qd_status qd_model_pos(qd_model* m, int32_t* pos_host, int batch, qd_stream_t stream) {
+  if (!m || !pos_host) return QD_ERR_INVALID_ARG;
+  if (batch < 1 || batch > m->cfg.max_batch) return QD_ERR_SHAPE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(pos_host, m->s + m->L.pos, 4 * (size_t)batch, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return QD_ERR_CUDA;
+  return QD_OK;
+}
+
+qd_status qd_model_kv_cache(qd_model* m, float** k_cache, float** v_cache) {
+  if (!m || !k_cache || !v_cache) return QD_ERR_INVALID_ARG;
+  *k_cache = m->f(m->L.kc);
+  *v_cache = m->f(m->L.vc);
+  return QD_OK;
+}
+
+qd_status qd_model_check(qd_model* m, qd_stream_t stream) {
+  if (!m) return QD_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, m->s + m->L.err, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return QD_ERR_CUDA;
+  if (word) {
+    QD_TRY(zero_region(m->s + m->L.err, 16, st));
+    return QD_ERR_DEVICE_FLAG;
+  }
+  return QD_OK;
+}
+
+int qd_model_launches_per_step(const qd_model* m) { return m ? m->launches : 0; }
+
+}  // extern "C"

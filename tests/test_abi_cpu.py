@@ -1,0 +1,120 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, sizes layouts,
+and refuses bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import quantized_decode_gemv_gb300 as qd
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "qdecode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(qd.LIB_PATH):
+        qd.build()
+    return qd.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qd_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declarations_match_binding():
+    assert declared_functions() == sorted(qd.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    assert qd.status_str(0) == "ok"
+    for s in range(1, 8):
+        assert qd.status_str(s) != "unknown status"
+    assert lib.qd_abi_version() == 1
+
+
+@pytest.mark.parametrize("fmt,rows,cols,src,packed", [
+    ("q4_0", 576, 1536, 576 * 48 * 18, 576 * 48 * 16 + 576 * 48 * 2),
+    ("q8_0", 3, 64, 3 * 2 * 34, 3 * 2 * 32 + 16),
+    ("q4_k", 2, 512, 2 * 2 * 144, 2 * 2 * 128 + 2 * 2 * 16),
+    ("i8", 5, 48, 5 * 48 + 20, 5 * 48 + 32),
+])
+def test_layout_sizes(lib, fmt, rows, cols, src, packed):
+    assert qd.src_bytes(fmt, rows, cols) == src
+    assert qd.packed_bytes(fmt, rows, cols) == packed
+
+
+@pytest.mark.parametrize("fmt,rows,cols", [("q4_0", 4, 48), ("q8_0", 0, 64), ("q4_k", 2, 128), ("i8", 3, 40),
+                                           ("q4_0", -1, 64)])
+def test_layout_sizes_reject_bad_shapes(lib, fmt, rows, cols):
+    assert qd.src_bytes(fmt, rows, cols) == 0
+    assert qd.packed_bytes(fmt, rows, cols) == 0
+
+
+def test_gemv_validation_before_any_device_work(lib):
+    good = 4096  # a fake 16-byte-aligned "device" address: never dereferenced on these paths
+    f = lib.qd_q_gemv
+    assert f(9, good, 8, 64, good, good, 1, None, 0, None) == 4            # unknown format
+    assert f(0, None, 8, 64, good, good, 1, None, 0, None) == 1            # null W
+    assert f(0, good, 8, 64, good, good, 0, None, 0, None) == 2            # batch 0
+    assert f(0, good, 8, 64, good, good, 17, None, 0, None) == 2           # batch > 16
+    assert f(0, good, 8, 48, good, good, 1, None, 0, None) == 2            # cols % 32
+    assert f(2, good, 8, 128, good, good, 1, None, 0, None) == 2           # Q4_K cols % 256
+    assert f(0, good + 4, 8, 64, good, good, 1, None, 0, None) == 3        # misaligned W
+    assert f(0, good, 8, 64, good, good + 8, 1, None, 0, None) == 3        # misaligned y
+
+
+def test_other_entry_points_validate(lib):
+    good = 4096
+    assert lib.qd_repack(0, good, 8, 64, good, 10, None) == 6              # dst too small
+    assert lib.qd_repack(0, good, 8, 64, good + 2, 1 << 20, None) == 3
+    assert lib.qd_rmsnorm(good, good, good, 0, 1, 1e-5, None) == 2
+    assert lib.qd_rmsnorm(good, good, good, 64, 1, -1.0, None) == 1
+    assert lib.qd_rope(good, 3, 63, 0, good, 1, good, 8, 1, None) == 2     # odd head_dim
+    assert lib.qd_rope(good, 3, 64, 192, good, 7, good, 8, 1, None) == 4   # unknown pairing
+    assert lib.qd_gqa_decode_attn(good, 576, good, good, good, 9, 3, 32, good, 8, 1, good, 1 << 20, None) == 4
+    assert lib.qd_gqa_decode_attn(good, 576, good, good, good, 9, 2, 64, good, 8, 1, good, 1 << 20, None) == 2
+    assert lib.qd_gqa_decode_attn(good, 576, good, good, good, 9, 3, 64, good, 8, 1, good, 1, None) == 6
+    assert lib.qd_argmax(good, 0, 1, good, None) == 2
+    assert lib.qd_embed(1, good, 100, 576, good, 1, good + 4, None) == 3
+    assert lib.qd_swiglu(None, good, good, 10, 1, None) == 1
+    assert lib.qd_decode_step(None, good, 1, good, None, None) == 1
+
+
+def test_model_sizes_and_config_refusals(lib):
+    import qdsynth
+
+    c = qd.make_config(qdsynth.SMOL_135M, max_ctx=256, max_batch=1)
+    wb = lib.qd_model_weight_bytes(ctypes.byref(c))
+    sb = lib.qd_model_state_bytes(ctypes.byref(c))
+    src = qdsynth.model_weight_src_bytes(qdsynth.SMOL_135M)
+    assert src <= wb <= src + 4096 * (3 + 9 * 30)  # same bytes as the source plus alignment padding
+    kv = 2 * 30 * 3 * 256 * 64 * 4
+    assert kv < sb < kv + (64 << 20)
+    bad = qd.make_config(dict(qdsynth.SMOL_135M, n_kv_heads=2), max_ctx=256, max_batch=1)  # 9 % 2
+    assert lib.qd_model_weight_bytes(ctypes.byref(bad)) == 0
+    bad = qd.make_config(dict(qdsynth.SMOL_135M, head_dim=32), max_ctx=256, max_batch=1)
+    assert lib.qd_model_state_bytes(ctypes.byref(bad)) == 0
+    bad = qd.make_config(qdsynth.SMOL_135M, max_ctx=256, max_batch=17)
+    assert lib.qd_model_state_bytes(ctypes.byref(bad)) == 0
+
+
+def test_rope_table_host_matches_oracle(lib):
+    """The library's host table and the oracle's both round double cos/sin of
+    p * theta^(-2i/hd) to f32; they must agree exactly."""
+    hd, ctx, theta = 64, 300, 1e5
+    got = np.empty((ctx, hd // 2, 2), np.float32)
+    qd.rope_table(theta, hd, ctx, got.ctypes.data)
+    want = oracle.rope_table(theta, hd, ctx)
+    assert np.array_equal(got, want)

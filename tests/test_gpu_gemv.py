@@ -1,0 +1,170 @@
+"""GPU parity of the repacker, the dequantiser and the q_gemv family against the oracle,
+through the C ABI.  Bit-exact where the result is integer/byte work or exactly representable;
+within 1e-3 of max |oracle| per output vector otherwise."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import qdsynth
+from gpu_helpers import TOL, assert_close, dev, packed, weights
+
+pytestmark = pytest.mark.gpu
+
+FMTS = ["q4_0", "q8_0", "q4_k", "i8"]
+SMALL = {"q4_0": [(1, 32), (7, 96), (67, 1056), (130, 4128)], "q8_0": [(1, 32), (9, 160), (67, 1056), (33, 4128)],
+         "q4_k": [(1, 256), (5, 512), (37, 2304), (19, 4352)], "i8": [(1, 16), (5, 48), (67, 1040), (41, 4112)]}
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_repack_unpack_round_trip_bit_exact(qd, fmt):
+    for rows, cols in SMALL[fmt]:
+        src = qdsynth.weight_src(fmt, 1, f"rt{rows}", rows, cols)
+        p = packed(qd, fmt, src, rows, cols)
+        back = torch.zeros(qd.src_bytes(fmt, rows, cols), dtype=torch.uint8, device="cuda")
+        qd.unpack(fmt, p, rows, cols, back)
+        torch.cuda.synchronize()
+        assert np.array_equal(back.cpu().numpy(), src.reshape(-1).view(np.uint8)), (rows, cols)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_dequant_block_values_bit_exact(qd, fmt):
+    for rows, cols in SMALL[fmt]:
+        src, p = weights(qd, fmt, 2, f"dq{rows}", rows, cols)
+        out = torch.empty(rows * cols, dtype=torch.float32, device="cuda")
+        qd.dequant(fmt, p, rows, cols, out)
+        want = oracle.dequant(fmt, src, rows, cols)
+        assert np.array_equal(out.cpu().numpy().reshape(rows, cols).view(np.uint32), want.view(np.uint32))
+
+
+def test_hand_worked_q4_0_blocks_on_gpu(qd):
+    from test_oracle_pins import _hand_q4_0
+
+    for blk, vals, total in _hand_q4_0():
+        p = packed(qd, "q4_0", blk, 1, 32)
+        out = torch.empty(32, dtype=torch.float32, device="cuda")
+        qd.dequant("q4_0", p, 1, 32, out)
+        assert np.array_equal(out.cpu().numpy().astype(np.float64), vals)
+        y = torch.empty(1, dtype=torch.float32, device="cuda")
+        qd.q_gemv("q4_0", p, 1, 32, torch.ones(32, device="cuda"), y, 1)
+        assert y.item() == total
+
+
+def test_f16_bf16_all_patterns_bit_exact(qd):
+    bits = np.arange(65536, dtype=np.uint16)
+    inp = dev(bits.view(np.int16))
+    out = torch.empty(65536, dtype=torch.float32, device="cuda")
+    qd.f16_to_f32(inp, out)
+    want = oracle.f16_to_f32_array(bits)
+    got = out.cpu().numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got.view(np.uint32)[~nan], want.view(np.uint32)[~nan])
+    qd.bf16_to_f32(inp, out)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), oracle.bf16_to_f32_array(bits).view(np.uint32))
+
+
+def _gemv(qd, fmt, p, rows, cols, x):
+    batch = x.shape[0]
+    y = torch.full((batch, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qd.q_gemv(fmt, p, rows, cols, dev(x), y, batch)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 8, 13, 16])
+def test_q_gemv_small_ragged_shapes(qd, fmt, batch):
+    for rows, cols in SMALL[fmt]:
+        src, p = weights(qd, fmt, 3, f"g{rows}x{cols}", rows, cols)
+        x = qdsynth.activations(3, f"x{cols}", batch, cols)
+        got = _gemv(qd, fmt, p, rows, cols, x)
+        assert_close(got, oracle.gemv(fmt, src, rows, cols, x), what=f"{fmt} {rows}x{cols} b{batch}")
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "i8", "q4_k"])
+def test_q_gemv_exact_case_bit_exact(qd, fmt):
+    """Power-of-two scales and integer x: every partial sum is exact in f32, so the GPU must
+    equal the oracle exactly whatever its summation order."""
+    rows, cols = 70, 2048
+    src = qdsynth.weight_src(fmt, 4, "ex", rows, cols).copy()
+    if fmt in ("q4_0", "q8_0"):
+        blk = src.reshape(rows, cols // 32, -1)
+        blk[:, :, 0:2] = np.array([2.0 ** -3], np.float16).view(np.uint8)
+    elif fmt == "q4_k":
+        blk = src.reshape(rows, cols // 256, 144)
+        blk[:, :, 0:2] = np.array([2.0 ** -3], np.float16).view(np.uint8)
+        blk[:, :, 2:4] = np.array([2.0 ** -4], np.float16).view(np.uint8)
+    else:
+        src[rows * cols:] = np.full(rows, 2.0 ** -3, np.float32).view(np.uint8)
+    p = packed(qd, fmt, src, rows, cols)
+    x = qdsynth.ints_i32(4, "xi", 3 * cols, -4, 4).reshape(3, cols).astype(np.float32)
+    got = _gemv(qd, fmt, p, rows, cols, x)
+    want = oracle.gemv(fmt, src, rows, cols, x)
+    assert np.array_equal(got.astype(np.float64), want)
+
+
+def test_q_gemv_config1_full(qd):
+    """Q4_0 576 x 1536, batch 1, seed 0 (the single-GEMV configuration), every output."""
+    rows, cols = 576, 1536
+    src, p = weights(qd, "q4_0", 0, "W", rows, cols)
+    x = qdsynth.activations(0, "x", 1, cols)
+    got = _gemv(qd, "q4_0", p, rows, cols, x)
+    err = assert_close(got, oracle.gemv("q4_0", src, rows, cols, x), what="C1")
+    print(f"C1 max rel err {err:.2e}")
+
+
+SWEEP = [(4096, 4096), (11008, 4096), (4096, 11008), (14336, 4096)]
+
+
+def _sampled_rows(rows, n=64, seed=0):
+    rng = np.random.default_rng(seed)
+    r = np.unique(np.concatenate([[0, rows - 1], rng.integers(0, rows, n)]))
+    return r
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("shape", SWEEP)
+def test_q_gemv_7b_sweep_sampled(qd, fmt, shape):
+    """The 7B-like sweep at full size, batch 1/2/4/8, on sampled output rows."""
+    rows, cols = shape
+    src, p = weights(qd, fmt, 0, f"sweep.{fmt}.{rows}x{cols}", rows, cols)
+    rs = _sampled_rows(rows)
+    for batch in (1, 2, 4, 8):
+        x = qdsynth.activations(0, f"sweep.x{cols}", batch, cols)
+        got = _gemv(qd, fmt, p, rows, cols, x)
+        assert np.all(np.isfinite(got))
+        want = np.concatenate([oracle.gemv(fmt, src, rows, cols, x, row0=int(r), nrows=1) for r in rs], axis=1)
+        assert_close(got[:, rs], want, what=f"{fmt} {shape} b{batch}")
+
+
+@pytest.mark.parametrize("shape", [(2048, 2048), (5632, 2048), (2048, 5632), (32000, 2048)])
+def test_q_gemv_q4k_tinyllama_sampled(qd, shape):
+    rows, cols = shape
+    src, p = weights(qd, "q4_k", 0, f"tl.{rows}x{cols}", rows, cols)
+    x = qdsynth.activations(0, f"tl.x{cols}", 1, cols)
+    got = _gemv(qd, "q4_k", p, rows, cols, x)
+    rs = _sampled_rows(rows)
+    want = np.concatenate([oracle.gemv("q4_k", src, rows, cols, x, row0=int(r), nrows=1) for r in rs], axis=1)
+    assert_close(got[:, rs], want, what=f"q4_k {shape}")
+
+
+@pytest.mark.parametrize("shape", [(6144, 2048), (2048, 2048), (16384, 2048), (2048, 8192), (49152, 2048)])
+@pytest.mark.parametrize("batch", [1, 16])
+def test_q_gemv_i8_1p7b_sampled(qd, shape, batch):
+    rows, cols = shape
+    src, p = weights(qd, "i8", 0, f"i8.{rows}x{cols}", rows, cols)
+    x = qdsynth.activations(0, f"i8.x{cols}", batch, cols)
+    got = _gemv(qd, "i8", p, rows, cols, x)
+    rs = _sampled_rows(rows, 32)
+    want = np.concatenate([oracle.gemv("i8", src, rows, cols, x, row0=int(r), nrows=1) for r in rs], axis=1)
+    assert_close(got[:, rs], want, what=f"i8 {shape} b{batch}")
+
+
+def test_q_gemv_is_deterministic(qd):
+    rows, cols = 4096, 4096
+    src, p = weights(qd, "q4_0", 5, "det", rows, cols)
+    x = qdsynth.activations(5, "xd", 4, cols)
+    a = _gemv(qd, "q4_0", p, rows, cols, x)
+    b = _gemv(qd, "q4_0", p, rows, cols, x)
+    assert np.array_equal(a, b)

@@ -1,0 +1,157 @@
+"""GPU parity of the whole decode step (qd_decode_step through the C ABI) against the oracle.
+
+Greedy tokens are compared with teacher forcing: the oracle is always fed the token the GPU
+chose, so both sides stay on one sequence.  A token may differ only at a near-tie: the
+oracle's logit gap between its choice and the GPU's must be <= 1e-3 * max |oracle logit|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import qdsynth
+from gpu_helpers import TOL, assert_close, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def build_model(qd, cfg, seed, max_ctx, max_batch):
+    host = qdsynth.model_tensors(cfg, seed)
+    srcs = [None if t is None else dev(t.view(np.uint8) if t.dtype != np.float32 else t) for t in host]
+    m = qd.Model(qd.make_config(cfg, max_ctx, max_batch), srcs)
+    torch.cuda.synchronize()
+    return m, host
+
+
+def check_token(ora_logits, ora_tok, gpu_tok):
+    if gpu_tok == ora_tok:
+        return 0
+    gap = ora_logits[ora_tok] - ora_logits[gpu_tok]
+    assert gap <= TOL * np.abs(ora_logits).max(), f"token {gpu_tok} vs oracle {ora_tok}, gap {gap}"
+    return 1
+
+
+def run_teacher_forced(qd, cfg, seed, prompt, n_gen, batch=1, max_ctx=None):
+    """Feed `prompt` (batch x P ids) then n_gen greedy tokens; compare every step's logits."""
+    P = prompt.shape[1]
+    max_ctx = max_ctx or (P + n_gen)
+    m, host = build_model(qd, cfg, seed, max_ctx, batch)
+    om = oracle.Model(dict(cfg, max_ctx=max_ctx), host)
+    L, hk, hd = cfg["layers"], cfg["n_kv_heads"], cfg["head_dim"]
+    okc = [np.zeros(L * hk * max_ctx * hd, np.float32) for _ in range(batch)]
+    ovc = [np.zeros_like(okc[0]) for _ in range(batch)]
+    logits = torch.empty(batch, cfg["vocab"], device="cuda")
+    out = torch.empty(batch, dtype=torch.int32)
+    cur = prompt[:, 0].astype(np.int32)
+    worst, near = 0.0, 0
+    for step in range(P + n_gen - 1):
+        m.decode_step(torch.from_numpy(cur.copy()), batch, out, logits)
+        torch.cuda.synchronize()
+        g = logits.cpu().numpy()
+        gt = out.numpy().copy()
+        assert m.check() == 0
+        for b in range(batch):
+            ol, ot = om.decode_step(okc[b], ovc[b], hk * max_ctx * hd, step, int(cur[b]))
+            worst = max(worst, assert_close(g[b], ol, what=f"logits step {step} seq {b}"))
+            assert gt[b] == int(np.argmax(g[b]))  # GPU argmax is exact on its own logits
+            near += check_token(ol, ot, int(gt[b]))
+        cur = prompt[:, step + 1].astype(np.int32) if step + 1 < P else gt.astype(np.int32)
+    assert m.pos(batch) == [P + n_gen - 1] * batch
+    m.close()
+    return worst, near
+
+
+TINY = dict(layers=2, dim=256, ffn=512, n_heads=4, n_kv_heads=2, head_dim=64, vocab=300, rope_theta=1e4, eps=1e-5,
+            pairing="half", w_fmt="q4_0", emb_fmt="q8_0")
+
+
+@pytest.mark.parametrize("w_fmt,emb_fmt,pairing", [("q4_0", "q8_0", "half"), ("q8_0", "q8_0", "adjacent"),
+                                                   ("i8", "i8", "half"), ("q4_k", "q4_0", "half")])
+def test_tiny_model_teacher_forced(qd, w_fmt, emb_fmt, pairing):
+    cfg = dict(TINY, w_fmt=w_fmt, emb_fmt=emb_fmt, pairing=pairing)
+    prompt = qdsynth.tokens(9, "tiny.prompt", 3 * 5, cfg["vocab"]).reshape(3, 5)
+    worst, near = run_teacher_forced(qd, cfg, 9, prompt, n_gen=6, batch=3, max_ctx=16)
+    print(f"tiny {w_fmt}/{emb_fmt}: worst rel err {worst:.2e}, near-tie tokens {near}")
+
+
+def test_model_reset_and_errors(qd):
+    cfg = dict(TINY)
+    m, _ = build_model(qd, cfg, 3, 4, 2)
+    out = torch.empty(2, dtype=torch.int32)
+    for _ in range(4):
+        m.decode_step(torch.tensor([1, 2], dtype=torch.int32), 2, out)
+    assert m.pos(2) == [4, 4]
+    m.decode_step(torch.tensor([1, 2], dtype=torch.int32), 2, out)  # pos == max_ctx: flagged, no write
+    assert m.check() == 7
+    m.reset()
+    assert m.pos(2) == [0, 0]
+    m.decode_step(torch.tensor([1, 300], dtype=torch.int32), 2, out)  # token == vocab: flagged
+    assert m.check() == 7
+    assert m.check() == 0  # the word was cleared
+    m.close()
+
+
+@pytest.mark.slow
+def test_smol135m_prompt128_gen128_teacher_forced(qd):
+    """135M-shaped model: 128 prompt ids ~U[0, 49152), then 128 greedy tokens, batch 1."""
+    cfg = qdsynth.SMOL_135M
+    prompt = qdsynth.tokens(0, "smol135m.prompt", 128, cfg["vocab"]).reshape(1, 128)
+    worst, near = run_teacher_forced(qd, cfg, 0, prompt, n_gen=128, batch=1, max_ctx=256)
+    print(f"135M: worst rel err {worst:.2e}, near-tie tokens {near}/255")
+
+
+def fill_cache_normal(m, cfg, seed, max_batch, max_ctx):
+    """KV cache entries ~N(0,1), generated in (layer, sequence) slices straight into the
+    model's cache (layout [layer][batch][kv_head][ctx][hd])."""
+    kp, vp = m.kv_cache_ptrs()
+    base = m.state.data_ptr()
+    n = cfg["layers"] * max_batch * cfg["n_kv_heads"] * max_ctx * cfg["head_dim"]
+    k = m.state[kp - base:kp - base + 4 * n].view(torch.float32)
+    v = m.state[vp - base:vp - base + 4 * n].view(torch.float32)
+    per = cfg["n_kv_heads"] * max_ctx * cfg["head_dim"]
+    buf = torch.empty(per, dtype=torch.float32).pin_memory()
+    for name, dst in (("c5.kcache", k), ("c5.vcache", v)):
+        for s in range(cfg["layers"] * max_batch):
+            qdsynth.normal_f32(seed, name, per, offset=s * per, out=buf.numpy())
+            dst[s * per:(s + 1) * per].copy_(buf, non_blocking=False)
+    torch.cuda.synchronize()
+
+
+def oracle_cache(cfg, seed, b, max_batch, max_ctx):
+    per = cfg["n_kv_heads"] * max_ctx * cfg["head_dim"]
+    L = cfg["layers"]
+    k = np.empty(L * per, np.float32)
+    v = np.empty(L * per, np.float32)
+    for l in range(L):
+        off = (l * max_batch + b) * per
+        qdsynth.normal_f32(seed, "c5.kcache", per, offset=off, out=k[l * per:(l + 1) * per])
+        qdsynth.normal_f32(seed, "c5.vcache", per, offset=off, out=v[l * per:(l + 1) * per])
+    return k, v
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("batch,check_seqs", [(1, [0]), (16, [0, 9, 15])])
+def test_smol1p7b_int8_ctx4096(qd, batch, check_seqs):
+    """1.7B-shaped INT8 model, f32 KV cache holding 4095 N(0,1) positions; one step at pos
+    4095 (attending over 4096 entries), independent sequences."""
+    cfg = qdsynth.SMOL_1_7B
+    ctx = 4096
+    m, host = build_model(qd, cfg, 0, ctx, batch)
+    fill_cache_normal(m, cfg, 0, batch, ctx)
+    m.set_pos([ctx - 1] * batch)
+    toks = qdsynth.tokens(0, "c5.tokens", 16, cfg["vocab"])[:batch].astype(np.int32)
+    logits = torch.empty(batch, cfg["vocab"], device="cuda")
+    out = torch.empty(batch, dtype=torch.int32)
+    m.decode_step(torch.from_numpy(toks.copy()), batch, out, logits)
+    torch.cuda.synchronize()
+    assert m.check() == 0
+    g = logits.cpu().numpy()
+    om = oracle.Model(dict(cfg, max_ctx=ctx), host)
+    per = cfg["n_kv_heads"] * ctx * cfg["head_dim"]
+    for b in check_seqs:
+        kc, vc = oracle_cache(cfg, 0, b, batch, ctx)
+        ol, ot = om.decode_step(kc, vc, per, ctx - 1, int(toks[b]))
+        err = assert_close(g[b], ol, what=f"1.7B seq {b}")
+        check_token(ol, ot, int(out[b]))
+        print(f"1.7B batch {batch} seq {b}: rel err {err:.2e}")
+    m.close()
