@@ -487,6 +487,32 @@ def run_reference(args, world, rank, local):
     }))
 
 
+def run_gemv_only(spec: str, reps: int):
+    """Microbenchmark of one q_gemv shape, e.g. "q4_0:14336x4096:1" (format:rowsxcols:batch):
+    `reps` cold-weight passes; prints one JSON line (not the benchmark contract line)."""
+    import torch
+
+    import quantized_decode_gemv_gb300 as qd
+
+    fmt, shape, b = spec.split(":")
+    r, c = (int(v) for v in shape.split("x"))
+    b = int(b)
+    if not os.path.exists(qd.LIB_PATH):
+        qd.build()
+    qd.load()
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps):
+        t, n = time_gemv_cold(qd, torch, fmt, r, c, b, stream)
+        ts.append(t)
+    by = algorithmic_bytes(fmt, r, c, b, qd)
+    hbm, _, kind = peaks()
+    t = min(ts)
+    print(json.dumps({"gemv": spec, "us": round(t * 1e6, 3), "GB/s": round(by / t / 1e9, 1),
+                      "frac": round(by / t / 1e9 / hbm, 4), "peak": hbm, "peak_kind": kind,
+                      "algorithmic_bytes": by, "launches_per_pass": n}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -498,7 +524,12 @@ def main(argv=None):
     ap.add_argument("--full-sweep", action="store_true", help="q_gemv sweep at batch 1, 2, 4, 8")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-tokens", type=int, default=8)
+    ap.add_argument("--gemv", default=None, help="microbenchmark one shape, FMT:ROWSxCOLS:BATCH")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
+    if args.gemv:
+        run_gemv_only(args.gemv, args.reps)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     world, rank, local = dist_env()
