@@ -182,6 +182,27 @@ qd_status qd_gqa_decode_attn(const float* q, int64_t q_batch_stride, const float
                              float* out, int n_heads, int n_kv_heads, int head_dim, const int32_t* pos, int max_ctx,
                              int batch, void* workspace, size_t workspace_bytes, qd_stream_t stream);
 
+/* Allocation-free variant of qd_gqa_decode_attn.  The pages have no counterpart: this is
+ * an interface convenience, not part of the method.  Some callers cannot allocate device
+ * memory for a workspace: code that runs after a fixed memory budget has been handed out
+ * (another allocator or runtime owns the rest of the device), and loops that must not
+ * call cudaMalloc because it can synchronise the device or fail at an unpredictable
+ * moment.  This entry point takes the same inputs and outputs as qd_gqa_decode_attn
+ * (same meaning, layout and validation) but keeps its partial results in a fixed 8 MiB
+ * device array that the library reserves on every GPU that loads it, until the process
+ * exits.  It calls no cudaMalloc or cudaFree.
+ *  - Size limit: calls whose workspace (qd_gqa_decode_attn_workspace) would exceed
+ *    8 MiB return QD_ERR_NOMEM and enqueue nothing.  The largest configuration here,
+ *    32 heads at context 4096 with batch 16, needs 4.3 MB.
+ *  - The first call on each device looks up the array's device address (with that
+ *    device current); make that first call before any stream capture.
+ *  - All calls share the one array and leave their partials in it.  Nothing needs to
+ *    start at zero, but calls that overlap on the GPU (e.g. on two streams) race on it:
+ *    order them on one stream. */
+qd_status qd_gqa_decode_attn_noalloc(const float* q, int64_t q_batch_stride, const float* k_cache,
+                                     const float* v_cache, float* out, int n_heads, int n_kv_heads, int head_dim,
+                                     const int32_t* pos, int max_ctx, int batch, qd_stream_t stream);
+
 /* SwiGLU gate ([llmoxide] 2; [dasLLAMA] 8.7.1.6.3): out = silu(gate) * up with
  * silu(z) = z / (1 + exp(-z)).  f32 [batch][n] each. */
 qd_status qd_swiglu(const float* gate, const float* up, float* out, int64_t n, int batch, qd_stream_t stream);

@@ -25,6 +25,7 @@ STATUS = {0: "QD_OK", 1: "QD_ERR_INVALID_ARG", 2: "QD_ERR_SHAPE", 3: "QD_ERR_ALI
 EXPORTS = ["qd_status_str", "qd_abi_version", "qd_f16_to_f32", "qd_bf16_to_f32", "qd_src_bytes", "qd_packed_bytes",
            "qd_repack", "qd_unpack", "qd_dequant", "qd_q_gemv_workspace", "qd_q_gemv", "qd_rmsnorm",
            "qd_rope_table", "qd_rope", "qd_kv_append", "qd_gqa_decode_attn_workspace", "qd_gqa_decode_attn",
+           "qd_gqa_decode_attn_noalloc",
            "qd_swiglu", "qd_argmax", "qd_embed", "qd_model_weight_bytes", "qd_model_state_bytes",
            "qd_model_create", "qd_model_destroy", "qd_decode_step", "qd_model_reset", "qd_model_set_pos",
            "qd_model_pos", "qd_model_kv_cache", "qd_model_check", "qd_model_launches_per_step"]
@@ -77,6 +78,7 @@ def load():
         "qd_kv_append": ([p, p, i64, p, p, i32, i32, p, i32, i32, p], i32),
         "qd_gqa_decode_attn_workspace": ([i32, i32, i32, i32], sz),
         "qd_gqa_decode_attn": ([p, i64, p, p, p, i32, i32, i32, p, i32, i32, p, sz, p], i32),
+        "qd_gqa_decode_attn_noalloc": ([p, i64, p, p, p, i32, i32, i32, p, i32, i32, p], i32),
         "qd_swiglu": ([p, p, p, i64, i32, p], i32),
         "qd_argmax": ([p, i64, i32, p, p], i32),
         "qd_embed": ([i32, p, i64, i64, p, i32, p, p], i32),
@@ -198,6 +200,15 @@ def gqa_decode_attn(q, q_batch_stride, k_cache, v_cache, out, n_heads, n_kv_head
            load().qd_gqa_decode_attn(_ptr(q), q_batch_stride, _ptr(k_cache), _ptr(v_cache), _ptr(out), n_heads,
                                      n_kv_heads, head_dim, _ptr(pos), max_ctx, batch, _ptr(workspace),
                                      workspace_bytes, _stream(stream)))
+
+
+def gqa_decode_attn_noalloc(q, q_batch_stride, k_cache, v_cache, out, n_heads, n_kv_heads, head_dim, pos, max_ctx,
+                            batch, stream=None):
+    """Attention without a caller workspace (the library's fixed device scratch)."""
+    _check("qd_gqa_decode_attn_noalloc",
+           load().qd_gqa_decode_attn_noalloc(_ptr(q), q_batch_stride, _ptr(k_cache), _ptr(v_cache), _ptr(out),
+                                             n_heads, n_kv_heads, head_dim, _ptr(pos), max_ctx, batch,
+                                             _stream(stream)))
 
 
 def swiglu(gate, up, out, n, batch, stream=None):

@@ -1,6 +1,7 @@
 // The decode step's operations other than the GEMV: RMSNorm, RoPE, KV-cache
 // append, split-KV grouped-query decode attention, SwiGLU, argmax, embedding.
 #include <cmath>
+#include <mutex>
 
 #include "qd_internal.cuh"
 
@@ -357,6 +358,37 @@ qd_status launch_embed(int fmt, const PackedView& E, const int32_t* tokens, int 
   return launch_status();
 }
 
+// ------------------------------------------------------------------ fixed scratch
+// Scratch for qd_gqa_decode_attn_noalloc: a file-scope device array that the driver
+// reserves when the library's module is loaded on a device and keeps until the process
+// exits.  Host code must not use its name as an address; the device address comes from
+// cudaGetSymbolAddress, looked up once per device.
+constexpr size_t kAttnScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_attn_scratch[kAttnScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_attn_scratch on the current device (looked up on first use).
+qd_status attn_scratch_ptr(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QD_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return QD_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return QD_OK;
+}
+}  // namespace
+
 }  // namespace qd
 
 using namespace qd;
@@ -430,6 +462,30 @@ qd_status qd_gqa_decode_attn(const float* q, int64_t q_batch_stride, const float
   const int64_t cbs = (int64_t)n_kv_heads * max_ctx * head_dim;
   return launch_attention(q, q_batch_stride, k_cache, v_cache, cbs, out, n_heads, n_kv_heads, head_dim, pos, max_ctx,
                           batch, workspace, nullptr, (cudaStream_t)stream);
+}
+
+// The same attention as qd_gqa_decode_attn, with its partial results kept in the
+// library's fixed device scratch instead of a caller-provided workspace, so the call
+// allocates nothing.  Every call shares that one scratch array; each call writes every
+// partial it later reads, so nothing needs clearing, but two calls that overlap on the GPU
+// (on different streams) race on it.
+qd_status qd_gqa_decode_attn_noalloc(const float* q, int64_t q_batch_stride, const float* k_cache,
+                                     const float* v_cache, float* out, int n_heads, int n_kv_heads, int head_dim,
+                                     const int32_t* pos, int max_ctx, int batch, qd_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !out || !pos) return QD_ERR_INVALID_ARG;
+  if (head_dim != 64) return QD_ERR_UNSUPPORTED;
+  if (n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads || n_heads / n_kv_heads > 8) return QD_ERR_SHAPE;
+  if (max_ctx < 1 || batch < 1 || batch > QD_MAX_BATCH) return QD_ERR_SHAPE;
+  if (batch > 1 && q_batch_stride < (int64_t)n_heads * head_dim) return QD_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return QD_ERR_ALIGN;
+  if ((q_batch_stride & 1) != 0) return QD_ERR_ALIGN;
+  if (attn_workspace_bytes(n_heads, head_dim, max_ctx, batch) > kAttnScratchBytes) return QD_ERR_NOMEM;
+  void* ws = nullptr;
+  const qd_status st = attn_scratch_ptr(&ws);
+  if (st != QD_OK) return st;
+  const int64_t cbs = (int64_t)n_kv_heads * max_ctx * head_dim;
+  return launch_attention(q, q_batch_stride, k_cache, v_cache, cbs, out, n_heads, n_kv_heads, head_dim, pos, max_ctx,
+                          batch, ws, nullptr, (cudaStream_t)stream);
 }
 
 qd_status qd_swiglu(const float* gate, const float* up, float* out, int64_t n, int batch, qd_stream_t stream) {
