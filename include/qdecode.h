@@ -23,8 +23,8 @@
  * Conventions for every entry point:
  *  - Device pointers unless stated "host".  The caller owns and allocates every
  *    buffer; no entry point calls cudaMalloc or frees caller memory.  (The model
- *    object is a small host struct; qd_model_create captures CUDA graphs, which the
- *    driver allocates for itself.)
+ *    object is a small host struct; the first qd_decode_step of each batch size
+ *    captures and instantiates a CUDA graph, which the driver allocates for itself.)
  *  - All device work is enqueued on `stream` and is asynchronous; host-side
  *    results (sizes, statuses) are synchronous.
  *  - Every call validates its arguments before enqueuing anything.  A failed check
@@ -220,7 +220,7 @@ qd_status qd_embed(qd_fmt fmt, const void* E, int64_t vocab, int64_t dim, const 
 
 /* ------------------------------------------------------------------------- */
 /* Model and decode step ([llmoxide] 7, 11, 12; [dasLLAMA] 8.7.1.6 forward,    */
-/* 8.7.1.7; [go-llm] CPU.Forward / Reset / Pos, "One submit per token").       */
+/* 8.7.1.7; [go-llm] CPU.Forward / Reset / Pos, "Design points").             */
 /* ------------------------------------------------------------------------- */
 
 typedef struct {
@@ -261,8 +261,8 @@ void qd_model_destroy(qd_model* m);
  * or device pointers (int32 [batch]); logits_out (f32 [batch][vocab], host or
  * device) may be NULL.  The step is one CUDA graph replay on `stream` (captured on
  * the first step of each batch size); host pointers make the call wait for the
- * copies.  Prefill is this call once per prompt token ([go-llm] "Results":
- * "Prefill is a decode pass per prompt token"). */
+ * copies.  Prefill is this call once per prompt token: the Go package's "Results"
+ * section runs its prompt the same way, one decode pass per token. */
 qd_status qd_decode_step(qd_model* m, const int32_t* tokens, int batch, int32_t* out_tokens, float* logits_out,
                          qd_stream_t stream);
 

@@ -52,9 +52,9 @@ enum { OR_ROPE_ADJACENT = 0, OR_ROPE_HALF = 1 };
 /* Scalar formats                                                             */
 /* ------------------------------------------------------------------------- */
 
-/* IEEE 754 binary16 -> double, exactly ([go-llm] index, F16ToF32: "converts an
- * IEEE binary16 value, exactly").  Written from the format's definition:
- * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+/* IEEE 754 binary16 -> double, exactly (the [go-llm] index entry F16ToF32 is an
+ * exact conversion).  Written from the format's definition: 1 sign bit, 5 exponent
+ * bits (bias 15), 10 fraction bits. */
 double or_f16_to_f64(uint16_t h) {
     const int sign = (h >> 15) & 1;
     const int e = (h >> 10) & 0x1F;
