@@ -161,8 +161,10 @@ def build_smol135m(qd, torch, seed):
 
 
 def time_gemv_cold(qd, torch, fmt, rows, cols, batch, stream, reps=None, seed=0):
-    """Average duration of qd_q_gemv over back-to-back launches, each on a distinct weight
-    copy so that the weights come from HBM (copies total >= 2x L2).  Returns seconds."""
+    """Average device time of one qd_q_gemv launch.  The launches run back to back from a
+    CUDA graph (so host launch overhead is not measured), each on a distinct weight copy so
+    the weights come from HBM: the copies total >= 2x L2, and L2 is flushed before each
+    replay.  Returns (seconds, launches per replay)."""
     import qdsynth
 
     src = qdsynth.weight_src(fmt, seed, f"bench.{fmt}.{rows}x{cols}", rows, cols)
@@ -170,27 +172,30 @@ def time_gemv_cold(qd, torch, fmt, rows, cols, batch, stream, reps=None, seed=0)
     pbuf = torch.empty(pb, dtype=torch.uint8, device="cuda")
     qd.repack(fmt, torch.from_numpy(src).cuda(), rows, cols, pbuf)
     n = max(8, min(400, (2 * L2_FLUSH_BYTES) // pb + 1)) if reps is None else reps
-    copies = pbuf.repeat(n).view(n, pb)  # n contiguous copies (each 256-byte aligned: pb % 16 == 0)
+    copies = pbuf.repeat(n).view(n, pb)  # n contiguous copies; pb % 16 == 0 keeps each aligned
     x = torch.from_numpy(qdsynth.activations(seed, "bench.x", batch, cols)).cuda()
     y = torch.empty(batch, rows, device="cuda")
     ptrs = [copies[i].data_ptr() for i in range(n)]
-    aligned = [p for p in ptrs if p % 16 == 0]
-    for p in aligned[:3]:
+    for p in ptrs[:3]:
         qd.q_gemv(fmt, p, rows, cols, x, y, batch, stream=stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for p in ptrs:
+            qd.q_gemv(fmt, p, rows, cols, x, y, batch)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     best = None
-    for _ in range(3):
+    for _ in range(4):
         flush.fill_(1)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for p in aligned:
-            qd.q_gemv(fmt, p, rows, cols, x, y, batch, stream=stream)
+        g.replay()
         e1.record()
         torch.cuda.synchronize()
-        t = e0.elapsed_time(e1) / 1e3 / len(aligned)
+        t = e0.elapsed_time(e1) / 1e3 / len(ptrs)
         best = t if best is None else min(best, t)
-    del copies, flush
-    return best, len(aligned)
+    del g, copies, flush
+    return best, len(ptrs)
 
 
 def algorithmic_bytes(fmt, rows, cols, batch, qd):

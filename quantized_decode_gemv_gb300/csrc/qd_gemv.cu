@@ -323,13 +323,20 @@ qd_status launch_fmt(const PackedView& W, const float* x, float* y, int batch, i
 
 }  // namespace
 
-qd_status launch_q_gemv(int fmt, const PackedView& W, const float* x, float* y, int batch, GemvMode mode,
-                        cudaStream_t stream) {
-  switch (fmt) {
-    case QD_Q4_0: return launch_fmt<QD_Q4_0>(W, x, y, batch, mode, stream);
-    case QD_Q8_0: return launch_fmt<QD_Q8_0>(W, x, y, batch, mode, stream);
-    case QD_Q4_K: return launch_fmt<QD_Q4_K>(W, x, y, batch, mode, stream);
-    case QD_I8_ROW: return launch_fmt<QD_I8_ROW>(W, x, y, batch, mode, stream);
+qd_status launch_q_gemv(const GemvArgs& a, cudaStream_t stream) {
+  // Batch 1-2: the TMA-staged streaming kernel (it also fuses RMSNorm).  Other
+  // batches: the register-path kernel below (RMSNorm must have been applied by the
+  // caller, see gemv_fuses_norm).
+  if (a.batch <= 2) {
+    const qd_status st = launch_q_gemv_stream(a, stream);
+    if (st != QD_ERR_UNSUPPORTED) return st;
+  }
+  if (a.norm_g) return QD_ERR_UNSUPPORTED;
+  switch (a.fmt) {
+    case QD_Q4_0: return launch_fmt<QD_Q4_0>(a.W, a.x, a.y, a.batch, a.mode, stream);
+    case QD_Q8_0: return launch_fmt<QD_Q8_0>(a.W, a.x, a.y, a.batch, a.mode, stream);
+    case QD_Q4_K: return launch_fmt<QD_Q4_K>(a.W, a.x, a.y, a.batch, a.mode, stream);
+    case QD_I8_ROW: return launch_fmt<QD_I8_ROW>(a.W, a.x, a.y, a.batch, a.mode, stream);
     default: return QD_ERR_UNSUPPORTED;
   }
 }
@@ -357,7 +364,13 @@ qd_status qd_q_gemv(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const
   if (batch < 1 || batch > QD_MAX_BATCH) return QD_ERR_SHAPE;
   if (!shape_ok(fmt, rows, cols)) return QD_ERR_SHAPE;
   if (!aligned16(W) || !aligned16(x) || !aligned16(y)) return QD_ERR_ALIGN;
-  return launch_q_gemv(fmt, packed_view(fmt, W, rows, cols), x, y, batch, kGemvStore, (cudaStream_t)stream);
+  GemvArgs a;
+  a.fmt = fmt;
+  a.W = packed_view(fmt, W, rows, cols);
+  a.x = x;
+  a.y = y;
+  a.batch = batch;
+  return launch_q_gemv(a, (cudaStream_t)stream);
 }
 
 }  // extern "C"

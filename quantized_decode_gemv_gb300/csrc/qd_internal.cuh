@@ -15,9 +15,11 @@ constexpr int kWarp = 32;
 // Bits of the device error word.
 constexpr uint32_t kErrToken = 1u;     // token id outside [0, vocab)
 constexpr uint32_t kErrPosition = 2u;  // position outside [0, max_ctx)
+constexpr uint32_t kErrTimeout = 4u;   // a bounded wait inside a kernel gave up
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+__host__ __device__ inline int64_t align16u(int64_t v) { return (v + 15) & ~(int64_t)15; }
 
 inline qd_status launch_status() {
   cudaError_t e = cudaGetLastError();
@@ -183,9 +185,25 @@ enum GemvMode { kGemvStore = 0, kGemvAccumulate = 1, kGemvSwiGLU = 2 };
 
 // y = W x (mode store), y += W x (accumulate), or for rows interleaved as
 // (gate_i, up_i) pairs: y[b][i] = silu(gate_i . x) * (up_i . x) (swiglu; y has
-// rows/2 columns per batch row).
-qd_status launch_q_gemv(int fmt, const PackedView& W, const float* x, float* y, int batch, GemvMode mode,
-                        cudaStream_t stream);
+// rows/2 columns per batch row).  With norm_g set, x is first replaced by
+// x * norm_g / sqrt(mean(x^2) + eps) (RMSNorm fused into the prologue).
+struct GemvArgs {
+  int fmt = QD_Q4_0;
+  PackedView W{};
+  const float* x = nullptr;
+  float* y = nullptr;
+  int batch = 1;
+  GemvMode mode = kGemvStore;
+  const float* norm_g = nullptr;
+  float eps = 0.f;
+  uint32_t* err = nullptr;  // device error word (null: the library's own)
+  bool pdl = false;         // launch as a programmatic dependent of the previous kernel
+};
+qd_status launch_q_gemv(const GemvArgs& a, cudaStream_t stream);
+qd_status launch_q_gemv_stream(const GemvArgs& a, cudaStream_t stream);
+// Whether launch_q_gemv runs the streaming kernel for these arguments (and so can
+// take norm_g and the pdl flag).
+bool gemv_streams(const GemvArgs& a);
 
 qd_status launch_rmsnorm(const float* x, const float* g, float* out, int n, int batch, float eps,
                          cudaStream_t stream);

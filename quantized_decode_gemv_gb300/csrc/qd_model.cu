@@ -151,12 +151,45 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
   int n = 0;
   QD_TRY(launch_embed(c.emb_fmt, m->W(c.emb_fmt, L.emb, c.vocab, D), m->i(L.tok_in), batch, x, err, st));
   ++n;
+  // GEMV with RMSNorm fused into its prologue when the streaming kernel runs, a
+  // separate norm kernel otherwise.  Returns the number of kernels launched.
+  auto normed_gemv = [&](int fmt, PackedView W, const float* gains, float* y, GemvMode mode, int& count) -> qd_status {
+    GemvArgs a;
+    a.fmt = fmt;
+    a.W = W;
+    a.x = x;
+    a.y = y;
+    a.batch = batch;
+    a.mode = mode;
+    a.err = err;
+    if (gemv_streams(a)) {
+      a.norm_g = gains;
+      a.eps = c.eps;
+      count += 1;
+      return launch_q_gemv(a, st);
+    }
+    QD_TRY(launch_rmsnorm(x, gains, xn, (int)D, batch, c.eps, st));
+    a.x = xn;
+    count += 2;
+    return launch_q_gemv(a, st);
+  };
+  auto plain_gemv = [&](int fmt, PackedView W, const float* in, float* y, GemvMode mode) -> qd_status {
+    GemvArgs a;
+    a.fmt = fmt;
+    a.W = W;
+    a.x = in;
+    a.y = y;
+    a.batch = batch;
+    a.mode = mode;
+    a.err = err;
+    return launch_q_gemv(a, st);
+  };
   for (int l = 0; l < c.layers; ++l) {
     const LayerOff& o = L.layer[l];
     float* kc = m->f(L.kc) + (int64_t)l * L.cache_layer_stride;
     float* vc = m->f(L.vc) + (int64_t)l * L.cache_layer_stride;
-    QD_TRY(launch_rmsnorm(x, reinterpret_cast<const float*>(m->w + o.attn_norm), xn, (int)D, batch, c.eps, st));
-    QD_TRY(launch_q_gemv(c.w_fmt, m->W(c.w_fmt, o.wqkv, L.qkv_rows, D), xn, qkv, batch, kGemvStore, st));
+    QD_TRY(normed_gemv(c.w_fmt, m->W(c.w_fmt, o.wqkv, L.qkv_rows, D),
+                       reinterpret_cast<const float*>(m->w + o.attn_norm), qkv, kGemvStore, n));
     // q heads and k heads are adjacent in the fused output: one rotation pass
     QD_TRY(launch_rope(qkv, c.n_heads + c.n_kv_heads, c.head_dim, L.qkv_rows, pos, c.pairing, m->f(L.rope),
                        c.max_ctx, batch, err, st));
@@ -164,16 +197,16 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
                             batch, L.cache_batch_stride, err, st));
     QD_TRY(launch_attention(qkv, L.qkv_rows, kc, vc, L.cache_batch_stride, att, c.n_heads, c.n_kv_heads, c.head_dim,
                             pos, c.max_ctx, batch, m->s + L.attn_ws, err, st));
-    QD_TRY(launch_q_gemv(c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, x, batch, kGemvAccumulate, st));
-    QD_TRY(launch_rmsnorm(x, reinterpret_cast<const float*>(m->w + o.ffn_norm), xn, (int)D, batch, c.eps, st));
-    QD_TRY(launch_q_gemv(c.w_fmt, m->W(c.w_fmt, o.wgu, 2 * F, D), xn, act, batch, kGemvSwiGLU, st));
-    QD_TRY(launch_q_gemv(c.w_fmt, m->W(c.w_fmt, o.wd, D, F), act, x, batch, kGemvAccumulate, st));
-    n += 10;  // rmsnorm, qkv, rope, kv, attention (2), wo, rmsnorm, gate/up, wd
+    QD_TRY(plain_gemv(c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, x, kGemvAccumulate));
+    QD_TRY(normed_gemv(c.w_fmt, m->W(c.w_fmt, o.wgu, 2 * F, D), reinterpret_cast<const float*>(m->w + o.ffn_norm),
+                       act, kGemvSwiGLU, n));
+    QD_TRY(plain_gemv(c.w_fmt, m->W(c.w_fmt, o.wd, D, F), act, x, kGemvAccumulate));
+    n += 6;  // rope, kv, attention (2), wo, wd
   }
-  QD_TRY(launch_rmsnorm(x, reinterpret_cast<const float*>(m->w + L.out_norm), xn, (int)D, batch, c.eps, st));
-  QD_TRY(launch_q_gemv(c.emb_fmt, m->W(c.emb_fmt, L.head, c.vocab, D), xn, m->f(L.logits), batch, kGemvStore, st));
+  QD_TRY(normed_gemv(c.emb_fmt, m->W(c.emb_fmt, L.head, c.vocab, D), reinterpret_cast<const float*>(m->w + L.out_norm),
+                     m->f(L.logits), kGemvStore, n));
   QD_TRY(launch_argmax(m->f(L.logits), c.vocab, batch, m->i(L.tok_out), m->i(L.pos), st));
-  n += 3;
+  n += 1;
   m->launches = n;
   return QD_OK;
 }
