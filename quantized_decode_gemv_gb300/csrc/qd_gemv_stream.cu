@@ -3,28 +3,28 @@
 // y[b][r] = sum_c deq(W)[r][c] * x[b][c]  (llmoxide blog s1 and s10's row dot;
 // dasLLAMA 8.7.1.4 matmul), the weights decoded in registers with no f32 copy
 // (minillm-cpp README, "NEON kernels").  Decode reads every weight byte once per
-// token (llmoxide s11); this kernel is shaped by measurements on GB300:
+// token (llmoxide s11); the kernel is shaped by measurements on GB300:
 //
-//  * Each warp owns groups of RW consecutive rows, assigned round-robin over every
-//    warp of the grid (so a tall or a short matrix spreads evenly over all SMs).
-//    Its lanes walk the rows' 32-weight units with stride 32: one 16-byte load per
-//    lane per 4-bit unit and row is a 512-byte coalesced read per warp.  The loads
-//    for the next two units are issued before the current one is computed.  The
-//    first loads are issued before `griddepcontrol.wait`, so under programmatic
-//    dependent launch a kernel's weight fetch overlaps its predecessor's tail.
-//    (A TMA-staged variant with a producer warp and an mbarrier ring measured the
-//    same DRAM rate but paid a CTA barrier per tile; it was replaced by this one.)
-//  * x is staged once per CTA in shared memory, chunk-swizzled so that the 32 lanes
-//    (32 different units) read it without bank conflicts, and reused for the RW
-//    rows of a group.  RMSNorm of x can be fused here (norm_g).
+//  * Each warp owns groups of RW consecutive rows, taken round-robin over every warp
+//    of the grid (global warp ids interleave the CTAs so left-over groups spread over
+//    all SMs); RW is chosen per shape so the groups split evenly.  Lanes walk a group's
+//    32-weight units with stride 32: one 16-byte chunk per lane, unit and row.
+//  * Weights stream through a per-warp 4-stage ring in shared memory filled with
+//    cp.async: each lane copies its own code chunks (and a few lanes the scale data),
+//    so up to three unit steps per warp are in flight without holding registers and
+//    without any CTA barrier.  The first copies are issued before
+//    `griddepcontrol.wait`, so under programmatic dependent launch the weight fetch
+//    overlaps the predecessor kernel.  (A TMA-staged variant with a producer warp and
+//    an mbarrier ring reached the same DRAM rate but paid a CTA barrier per tile.)
+//  * x * g is staged once per CTA in shared memory, padded to 9 float4 chunks per
+//    32-float unit so 32 lanes (32 units) read it without bank conflicts.  With RMSNorm
+//    fused, the factor 1/sqrt(mean(x^2) + eps) multiplies each finished row sum.
 //  * A 4-bit code q becomes the float 1 + q/16 with one byte permute (q lands in
-//    mantissa bits 19-22 of 1.0f); paired FFMA2s accumulate sum f*x; the block
-//    offset comes from the per-unit sum of x kept in shared memory:
-//    sum (q-8) x = 16 sum f x - 24 sum x.  8-bit codes land in the low mantissa of
-//    2^23 and 2^23 + 128 is subtracted (exact).  Each block scale multiplies a
-//    32-term partial sum.
-//  * A warp reduces its RW x NB row sums with one reduce-scatter (V-1 + 5 - log2 V
-//    shuffles for V sums) and writes them; there is no barrier in the main loop.
+//    mantissa bits 19-22 of 1.0f); paired FFMA2s accumulate sum f*x, and
+//    sum (q-8) x = 16 sum f x - 24 sum x.  8-bit codes land in the low mantissa of 2^23
+//    and 2^23 + 128 is subtracted (exact).  Each block scale multiplies a 32-term sum.
+//  * A warp reduces its RW x NB row sums with one reduce-scatter and writes them (or
+//    feeds the fused epilogues: SwiGLU, RoPE + KV append, argmax).
 #include "qd_internal.cuh"
 
 namespace qd {
@@ -33,10 +33,7 @@ namespace stream_gemv {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kDepth = 3;  // register ring: current unit + two in flight
 
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // 4-bit code byte k of m (prepared as 0x80 | q<<3 per byte) -> the float 1 + q/16.
 __device__ __forceinline__ float q4f(uint32_t m, int k) {
@@ -105,7 +102,43 @@ struct Params {
   float eps;
   int batch;
   int mode;
+  uint32_t* err;
+  QkvEpilogue qkv;
+  ArgmaxEpilogue am;
 };
+
+// kGemvQKV: rows r (even) and r+1 of batch b hold a RoPE pair (q or k) or two
+// consecutive v values; rotate and scatter them (see QkvEpilogue).
+__device__ __forceinline__ void qkv_pair_out(const Params& p, int64_t r, int b, float a, float bb) {
+  const QkvEpilogue& e = p.qkv;
+  const int pos = e.pos[b];
+  if (pos < 0 || pos >= e.max_ctx) {
+    if (p.err) atomicOr(p.err, kErrPosition);
+    return;
+  }
+  const int hd = e.head_dim, half = hd / 2;
+  if (r < e.q_rows + e.k_rows) {
+    const bool isq = r < e.q_rows;
+    const int64_t local = isq ? r : r - e.q_rows;
+    const int64_t h = local / hd;
+    const int pi = (int)(local % hd) / 2;
+    const int d0 = e.pairing == QD_ROPE_HALF ? pi : 2 * pi;
+    const int d1 = e.pairing == QD_ROPE_HALF ? pi + half : 2 * pi + 1;
+    const float2 cs = *reinterpret_cast<const float2*>(e.rope + ((int64_t)pos * half + pi) * 2);
+    const float o0 = a * cs.x - bb * cs.y, o1 = a * cs.y + bb * cs.x;
+    float* dst = isq ? e.q_out + (int64_t)b * e.q_stride + h * hd
+                     : e.kc + (int64_t)b * e.cache_batch_stride + (h * e.max_ctx + pos) * hd;
+    dst[d0] = o0;
+    dst[d1] = o1;
+  } else {
+    const int64_t local = r - e.q_rows - e.k_rows;
+    const int64_t h = local / hd;
+    const int d = (int)(local % hd);
+    float* dst = e.vc + (int64_t)b * e.cache_batch_stride + (h * e.max_ctx + pos) * hd;
+    dst[d] = a;
+    dst[d + 1] = bb;
+  }
+}
 
 // Row pointers (codes, scales) of the RW rows of a group; rows past the end repeat
 // the last row (their sums are never written).
@@ -180,7 +213,7 @@ struct Acc {
 // Compute one unit step from a staged slot into acc.
 template <int FMT, int NB, int RW>
 __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* slot, const float4* xs4, int xstride,
-                                             const float* sx, int units, int u, int lane) {
+                                             int u, int lane) {
   constexpr int CB = code_bytes<FMT>();
   const uint8_t* sc = slot + slot_code_bytes<FMT, RW>();
   const int ca = unit_ca<FMT>(u), cb = unit_cb<FMT>(u);
@@ -194,7 +227,13 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
       xb4[k] = xb[cb + k];
     }
     if constexpr (FMT == QD_Q4_0 || FMT == QD_Q4_K) {
-      const float sa = sx[(b * units + u) * 2], sbb = sx[(b * units + u) * 2 + 1];
+      // sums of the unit's two x halves (the 4-bit formats' block offsets)
+      float sa = 0.f, sbb = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        sa += (xa4[k].x + xa4[k].y) + (xa4[k].z + xa4[k].w);
+        sbb += (xb4[k].x + xb4[k].y) + (xb4[k].z + xb4[k].w);
+      }
 #pragma unroll
       for (int rr = 0; rr < RW; ++rr) {
         const uint4 q = *reinterpret_cast<const uint4*>(slot + (rr * 32 + lane) * CB);
@@ -261,7 +300,7 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
 
 template <int FMT, int NB, int RW>
 __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
-  extern __shared__ __align__(128) uint8_t smem[];  // [warps][kStages] slots, x [NB][units][9 float4], sx
+  extern __shared__ __align__(128) uint8_t smem[];  // [warps][kStages] slots, then x [NB][units][9 float4]
   __shared__ float red[kWarps][NB];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const PackedView& W = p.W;
@@ -277,7 +316,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
   const int xstride = units * 9;  // float4 chunks per batch column
   float4* xs4 = reinterpret_cast<float4*>(smem + (size_t)kWarps * kStages * SB);
-  float* sx = reinterpret_cast<float*>(xs4 + (size_t)NB * xstride);  // per unit: (sum A, sum B)
 
   // ---- start streaming the first steps (weights never depend on the previous kernel)
   int64_t lg = gw;  // group of the next copy
@@ -301,71 +339,50 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
 
   pdl_wait();  // x is the previous kernel's output
 
-  // ---- stage x (optionally RMS-normalised) in shared memory
+  // ---- stage x * g (x itself without norm) in shared memory.  RMSNorm is
+  // x * g / sqrt(mean(x^2) + eps): the scalar 1/sqrt(...) multiplies each finished row
+  // sum instead, so one barrier suffices.
+  float inv[NB];
   {
     const int chunks = cols / 4;
-    float inv[NB];
+    float ss[NB];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) inv[b] = 1.f;
-    if (p.norm_g) {
-      float ss[NB];
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        ss[b] = 0.f;
-        if (b < p.batch) {
-          const float4* xr = reinterpret_cast<const float4*>(p.x + (int64_t)b * cols);
-          for (int i = threadIdx.x; i < chunks; i += kThreads) {
-            const float4 v = xr[i];
-            ss[b] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[b]))));
-          }
+    for (int b = 0; b < NB; ++b) {
+      ss[b] = 0.f;
+      float4* dst = xs4 + b * xstride;
+      const float4* xr = reinterpret_cast<const float4*>(p.x + (int64_t)(b < p.batch ? b : 0) * cols);
+      const float4* gr = reinterpret_cast<const float4*>(p.norm_g);
+      for (int i = threadIdx.x; i < chunks; i += kThreads) {
+        float4 v = __ldcg(xr + i);
+        if (b >= p.batch) v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.norm_g) {
+          ss[b] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[b]))));
+          const float4 g = __ldg(gr + i);
+          v = make_float4(v.x * g.x, v.y * g.y, v.z * g.z, v.w * g.w);
         }
+        dst[(i >> 3) * 9 + (i & 7)] = v;
+      }
+      if (p.norm_g) {
         ss[b] = warp_sum(ss[b]);
         if (lane == 0) red[warp][b] = ss[b];
       }
-      __syncthreads();
+    }
+    __syncthreads();
 #pragma unroll
-      for (int b = 0; b < NB; ++b) {
+    for (int b = 0; b < NB; ++b) {
+      inv[b] = 1.f;
+      if (p.norm_g) {
         float t = 0.f;
 #pragma unroll
         for (int w2 = 0; w2 < kWarps; ++w2) t += red[w2][b];
         inv[b] = 1.0f / sqrtf(t / (float)cols + p.eps);
       }
     }
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      float4* dst = xs4 + b * xstride;
-      const float4* xr = reinterpret_cast<const float4*>(p.x + (int64_t)(b < p.batch ? b : 0) * cols);
-      const float4* gr = reinterpret_cast<const float4*>(p.norm_g);
-      for (int i = threadIdx.x; i < chunks; i += kThreads) {
-        float4 v = xr[i];
-        if (b >= p.batch) v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (p.norm_g) {
-          const float4 g = __ldg(gr + i);
-          v = make_float4(v.x * inv[b] * g.x, v.y * inv[b] * g.y, v.z * inv[b] * g.z, v.w * inv[b] * g.w);
-        }
-        dst[(i >> 3) * 9 + (i & 7)] = v;
-      }
-    }
-    __syncthreads();
-    if constexpr (FMT == QD_Q4_0 || FMT == QD_Q4_K) {  // per-unit sums of the halves
-      for (int t = threadIdx.x; t < NB * units; t += kThreads) {
-        const int b = t / units, u = t % units;
-        const float4* xb = xs4 + b * xstride;
-        float sa = 0.f, sb = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float4 va = xb[unit_ca<FMT>(u) + k], vb = xb[unit_cb<FMT>(u) + k];
-          sa += (va.x + va.y) + (va.z + va.w);
-          sb += (vb.x + vb.y) + (vb.z + vb.w);
-        }
-        sx[(b * units + u) * 2] = sa;
-        sx[(b * units + u) * 2 + 1] = sb;
-      }
-      __syncthreads();
-    }
   }
 
   // ---- main loop over this warp's (group, unit step) sequence
+  pdl_trigger();  // the next kernel may start its own weight prefetch now
+  unsigned long long best0 = 0, best1 = 0;  // kGemvArgmax: best (value, index) keys per batch row
   Acc<NB, RW> acc;
   int cs = 0;  // slot of the step being computed
   int j = 0;
@@ -382,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
     }
     const int u = lane + 32 * j;
     const uint8_t* slot = ring + (size_t)cs * SB;
-    if (u < units) compute_step<FMT, NB, RW>(acc, slot, xs4, xstride, sx, units, u, lane);
+    if (u < units) compute_step<FMT, NB, RW>(acc, slot, xs4, xstride, u, lane);
     float rsc[RW];  // INT8 row scales (staged with every step)
     if constexpr (FMT == QD_I8_ROW) {
 #pragma unroll
@@ -406,7 +423,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
     for (int rr = 0; rr < RW; ++rr)
 #pragma unroll
       for (int b = 0; b < NB; ++b) v[rr * NB + b] = acc.v[rr][b];
-    const float tot = reduce_scatter<V>(v, lane);
+    const int kb_ = (lane / GRP) % NB;  // batch row of this lane's reduced value
+    const float tot = reduce_scatter<V>(v, lane) * (kb_ == 0 ? inv[0] : inv[NB - 1]);
     const float partner = __shfl_down_sync(0xffffffffu, tot, (NB * GRP) & 31);  // row +1, same batch
     if ((lane % GRP) == 0) {
       const int k = lane / GRP, rr = k / NB, b = k % NB;
@@ -415,7 +433,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
         if (p.mode == kGemvSwiGLU) {
           if ((rr & 1) == 0 && r + 1 < W.rows)
             p.y[(int64_t)b * (W.rows / 2) + r / 2] = tot / (1.0f + expf(-tot)) * partner;
+        } else if (p.mode == kGemvQKV) {
+          if ((rr & 1) == 0 && r + 1 < W.rows) qkv_pair_out(p, r, b, tot, partner);
         } else {
+          if (p.mode == kGemvArgmax) {
+            const unsigned long long key = argmax_key(tot, (uint32_t)r);
+            if (b == 0)
+              best0 = key > best0 ? key : best0;
+            else
+              best1 = key > best1 ? key : best1;
+          }
           float* dst = p.y + (int64_t)b * W.rows + r;
           if (p.mode == kGemvAccumulate)
             *dst += tot;
@@ -427,7 +454,35 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
     g += nw;
   }
   cp_wait<0>();  // no copy may still target this CTA's shared memory at exit
-  pdl_trigger();
+  if (p.mode == kGemvArgmax) {
+    // warp max of the keys, one atomicMax per warp, then the last CTA finalises
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      unsigned long long k = b == 0 ? best0 : best1;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, k, off);
+        k = o > k ? o : k;
+      }
+      if (lane == 0 && k != 0 && b < p.batch) atomicMax(p.am.key + b, k);
+    }
+    __threadfence();
+    __syncthreads();
+    __shared__ bool last;
+    if (threadIdx.x == 0) {
+      last = atomicAdd(p.am.counter, 1u) == gridDim.x - 1;
+      if (last) {
+        __threadfence();
+        for (int b = 0; b < p.batch; ++b) {
+          const unsigned long long k = atomicExch(p.am.key + b, 0ull);
+          p.am.tok_out[b] = (int32_t)argmax_key_index(k);
+          p.am.pos[b] += 1;
+        }
+        *p.am.counter = 0u;
+        __threadfence();
+      }
+    }
+  }
 }
 
 int sm_count() {
@@ -469,8 +524,8 @@ template <int FMT, int NB, int RW>
 size_t smem_bytes_t(int64_t cols) {
   const size_t units = (size_t)cols / 32;
   const bool q4 = FMT == QD_Q4_0 || FMT == QD_Q4_K;
-  return (size_t)kWarps * kStages * slot_bytes<FMT, RW>() + (size_t)NB * units * 9 * 16 +
-         (q4 ? (size_t)NB * units * 8 : 0);
+  (void)q4;
+  return (size_t)kWarps * kStages * slot_bytes<FMT, RW>() + (size_t)NB * units * 9 * 16;
 }
 
 // Largest shared-memory need over the RW choices (for the support check).
@@ -526,10 +581,12 @@ qd_status launch_inst(const Params& p, bool pdl, cudaStream_t stream) {
   double best = -1.0;
   int brw = 2;
   int64_t bctas = 1;
-  // batch 2 keeps at most 2 rows per group (4 would spill registers), Q4_K batch 2 one
+  // batch 2 keeps at most 2 rows per group (4 would spill registers), Q4_K batch 2 one;
+  // the paired epilogues need an even number of rows per group
   constexpr int kMaxRW = NB == 1 ? 4 : (FMT == QD_Q4_K ? 1 : 2);
+  const bool pairs = p.mode == kGemvSwiGLU || p.mode == kGemvQKV;
   for (int rw : {4, 2, 1}) {
-    if (rw > kMaxRW) continue;
+    if (rw > kMaxRW || (pairs && rw == 1)) continue;
     int64_t ctas = 1;
     if constexpr (kMaxRW >= 4) {
       if (rw == 4) ctas = ctas_for<FMT, NB, 4>(rows, cols);
@@ -539,10 +596,17 @@ qd_status launch_inst(const Params& p, bool pdl, cudaStream_t stream) {
     }
     if (rw == 1) ctas = ctas_for<FMT, NB, 1>(rows, cols);
     const int64_t groups = (rows + rw - 1) / rw;
-    const double per = (double)groups / (double)(ctas * kWarps);
-    const double rounds = per <= 1.0 ? 1.0 : (double)((groups + ctas * kWarps - 1) / (ctas * kWarps));
-    // time ~ rounds * rw rows; quality = useful rows per unit time, small bonus for reuse
-    const double score = (double)rows / (rounds * rw * ctas * kWarps) * (1.0 + 0.03 * rw);
+    const int64_t slots = ctas * kWarps;
+    const int64_t rounds = (groups + slots - 1) / slots;
+    double score;
+    if (rounds <= 1) {
+      // every group runs at once: the kernel lasts one group, so fewer rows per group
+      // (more warps, shorter dependent chains) is faster
+      score = 1e6 / rw;
+    } else {
+      // time ~ rounds * rw rows; useful rows per unit time, small bonus for reuse of x
+      score = (double)rows / ((double)rounds * rw * slots) * (1.0 + 0.03 * rw);
+    }
     if (score > best) {
       best = score;
       brw = rw;
@@ -560,6 +624,7 @@ qd_status launch_inst(const Params& p, bool pdl, cudaStream_t stream) {
 
 bool supported(const GemvArgs& a) {
   if (a.batch > 2 || a.W.cols % 32) return false;
+  if ((a.mode == kGemvSwiGLU || a.mode == kGemvQKV) && a.batch == 2 && a.fmt == QD_Q4_K) return false;
   if (a.W.cols > (1 << 24)) return false;
   if (smem_bytes(a.fmt, a.W.cols, a.batch <= 1 ? 1 : 2) > 200 * 1024) return false;
   // 4-byte scale copies need an even number of blocks per row
@@ -584,6 +649,9 @@ qd_status launch_q_gemv_stream(const GemvArgs& a, cudaStream_t stream) {
   p.eps = a.eps;
   p.batch = a.batch;
   p.mode = a.mode;
+  p.err = a.err;
+  p.qkv = a.qkv;
+  p.am = a.am;
   const bool nb1 = a.batch <= 1;
   switch (a.fmt) {
     case QD_Q4_0: return nb1 ? launch_inst<QD_Q4_0, 1>(p, a.pdl, stream) : launch_inst<QD_Q4_0, 2>(p, a.pdl, stream);

@@ -181,7 +181,67 @@ __device__ __forceinline__ float dequant_elem(int fmt, const PackedView& W, int6
 // ---------------------------------------------------------------------------
 // Launchers shared between translation units (return QD_OK or QD_ERR_CUDA)
 // ---------------------------------------------------------------------------
-enum GemvMode { kGemvStore = 0, kGemvAccumulate = 1, kGemvSwiGLU = 2 };
+enum GemvMode { kGemvStore = 0, kGemvAccumulate = 1, kGemvSwiGLU = 2, kGemvQKV = 3, kGemvArgmax = 4 };
+
+// Fused epilogue of the QKV projection (mode kGemvQKV).  The packed QKV matrix holds
+// q_rows query rows, k_rows key rows, then the value rows; in the q and k parts, the
+// two rows of each RoPE pair are adjacent (pair i of a head at local rows 2i, 2i+1,
+// see the repacker).  The epilogue rotates each pair by the angles of pos[b], writes
+// q (natural order) to q_out[b*q_stride + ...], and appends k and v to the caches
+// [batch][kv_head][max_ctx][head_dim] at pos[b].
+struct QkvEpilogue {
+  int q_rows = 0, k_rows = 0, head_dim = 64, pairing = QD_ROPE_HALF;
+  const int32_t* pos = nullptr;
+  const float* rope = nullptr;  // [max_ctx][head_dim/2][2] (cos, sin)
+  float* q_out = nullptr;
+  int64_t q_stride = 0;
+  float* kc = nullptr;
+  float* vc = nullptr;
+  int64_t cache_batch_stride = 0;
+  int max_ctx = 0;
+};
+
+// Fused greedy argmax of the output head (mode kGemvArgmax): the logits are stored as
+// in kGemvStore, every warp folds its rows into a 64-bit key (ordered value, then
+// inverted index) merged with atomicMax into key[b]; the last CTA to finish writes the
+// winning index to tok_out[b], advances pos[b] and resets key and counter to zero.
+struct ArgmaxEpilogue {
+  unsigned long long* key = nullptr;  // [batch], zero between steps
+  unsigned int* counter = nullptr;    // zero between steps
+  int32_t* tok_out = nullptr;
+  int32_t* pos = nullptr;
+};
+
+__device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) {
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // order-preserving for non-NaN floats
+  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+}
+__device__ __forceinline__ uint32_t argmax_key_index(unsigned long long k) {
+  return 0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull);
+}
+
+// Programmatic dependent launch: a kernel launched with the PDL attribute may start
+// before its predecessor finishes; it must call pdl_wait() before it reads anything
+// the predecessor writes or writes anything the predecessor reads.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+qd_status launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                   Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
+}
 
 // y = W x (mode store), y += W x (accumulate), or for rows interleaved as
 // (gate_i, up_i) pairs: y[b][i] = silu(gate_i . x) * (up_i . x) (swiglu; y has
@@ -196,8 +256,10 @@ struct GemvArgs {
   GemvMode mode = kGemvStore;
   const float* norm_g = nullptr;
   float eps = 0.f;
-  uint32_t* err = nullptr;  // device error word (null: the library's own)
+  uint32_t* err = nullptr;  // device error word (may be null)
   bool pdl = false;         // launch as a programmatic dependent of the previous kernel
+  QkvEpilogue qkv{};
+  ArgmaxEpilogue am{};
 };
 qd_status launch_q_gemv(const GemvArgs& a, cudaStream_t stream);
 qd_status launch_q_gemv_stream(const GemvArgs& a, cudaStream_t stream);
@@ -222,7 +284,22 @@ qd_status launch_argmax(const float* logits, int64_t n, int batch, int32_t* out,
                         cudaStream_t stream);
 qd_status launch_embed(int fmt, const PackedView& E, const int32_t* tokens, int batch, float* x, uint32_t* err,
                        cudaStream_t stream);
+// Repack source rows [0, n_rows) into packed rows dst_row0 + i*dst_row_step.  With
+// pair_hd > 0 the rows are taken in blocks of pair_hd (one head) and, inside a block,
+// local row i goes to local row 2*(i % (pair_hd/2)) + i / (pair_hd/2): the two rows of
+// each half-pairing RoPE pair (i, i + pair_hd/2) become adjacent.
 qd_status launch_repack_rows(int fmt, const void* src, int64_t n_rows, int64_t cols, void* dst_base,
-                             int64_t dst_rows, int64_t dst_row0, int64_t dst_row_step, cudaStream_t stream);
+                             int64_t dst_rows, int64_t dst_row0, int64_t dst_row_step, cudaStream_t stream,
+                             int pair_hd = 0);
+// Standalone form of the kGemvQKV epilogue for the register-path GEMV: reads the
+// packed-order projection qkv[b][rows] and does the rotation, q write and cache append.
+qd_status launch_qkv_post(const float* qkv, int64_t qkv_stride, int batch, const QkvEpilogue& e, uint32_t* err,
+                          cudaStream_t stream, bool pdl);
+// Attention with the split merge done by the last CTA of each (sequence, kv head);
+// `counters` (batch*n_kv unsigned ints) must be zero and are left zero.
+qd_status launch_attention_fused(const float* q, int64_t q_stride, const float* kc, const float* vc,
+                                 int64_t cache_batch_stride, float* out, int n_heads, int n_kv, int head_dim,
+                                 const int32_t* pos, int max_ctx, int batch, void* ws, unsigned int* counters,
+                                 uint32_t* err, cudaStream_t stream, bool pdl);
 
 }  // namespace qd

@@ -31,15 +31,24 @@ __host__ __device__ inline BlockGeom geom(int fmt) {
   }
 }
 
+// Destination row of source row i (see launch_repack_rows).
+__host__ __device__ inline int64_t dst_row_of(int64_t i, int64_t row0, int64_t step, int pair_hd) {
+  if (pair_hd > 0) {
+    const int64_t h = i / pair_hd, l = i % pair_hd, half = pair_hd / 2;
+    i = h * pair_hd + 2 * (l % half) + l / half;
+  }
+  return row0 + i * step;
+}
+
 // One thread per (source row, block): copy its codes and its scale bytes.
 __global__ void k_repack_blocks(int fmt, const uint8_t* __restrict__ src, int64_t n_rows, int64_t nb,
                                 uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int64_t dst_row0,
-                                int64_t dst_step) {
+                                int64_t dst_step, int pair_hd) {
   const BlockGeom g = geom(fmt);
   const int64_t total = n_rows * nb;
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t i = t / nb, b = t % nb;
-    const int64_t r = dst_row0 + i * dst_step;
+    const int64_t r = dst_row_of(i, dst_row0, dst_step, pair_hd);
     const uint8_t* s = src + t * g.src_bytes;
     uint8_t* c = codes + (r * nb + b) * g.code_bytes;
     uint8_t* sc = scales + (r * nb + b) * g.scale_bytes;
@@ -64,12 +73,12 @@ __global__ void k_unpack_blocks(int fmt, const uint8_t* __restrict__ codes, cons
 // INT8 rows: codes copy 16 bytes per thread, scales one f32 per row.
 __global__ void k_repack_i8(const uint8_t* __restrict__ src, int64_t n_rows, int64_t cols,
                             uint8_t* __restrict__ codes, float* __restrict__ scales, int64_t dst_row0,
-                            int64_t dst_step) {
+                            int64_t dst_step, int pair_hd) {
   const int64_t chunks = cols / 16;
   const int64_t total = n_rows * chunks;
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t i = t / chunks, c = t % chunks;
-    const int64_t r = dst_row0 + i * dst_step;
+    const int64_t r = dst_row_of(i, dst_row0, dst_step, pair_hd);
     const uint8_t* s = src + i * cols + c * 16;
     uint8_t* d = codes + r * cols + c * 16;
     for (int k = 0; k < 16; ++k) d[k] = s[k];  // source rows are only byte-aligned in general
@@ -119,18 +128,22 @@ inline int grid_for(int64_t n, int threads) {
 }  // namespace
 
 qd_status launch_repack_rows(int fmt, const void* src, int64_t n_rows, int64_t cols, void* dst_base,
-                             int64_t dst_rows, int64_t dst_row0, int64_t dst_row_step, cudaStream_t stream) {
+                             int64_t dst_rows, int64_t dst_row0, int64_t dst_row_step, cudaStream_t stream,
+                             int pair_hd) {
+  if (pair_hd > 0 && ((pair_hd & 1) || n_rows % pair_hd)) return QD_ERR_SHAPE;
   PackedView v = packed_view(fmt, dst_base, dst_rows, cols);
   uint8_t* codes = const_cast<uint8_t*>(v.codes);
   uint8_t* scales = const_cast<uint8_t*>(v.scales);
   if (fmt == QD_I8_ROW) {
     const int64_t n = n_rows * (cols / 16);
     k_repack_i8<<<grid_for(n, 256), 256, 0, stream>>>(static_cast<const uint8_t*>(src), n_rows, cols, codes,
-                                                       reinterpret_cast<float*>(scales), dst_row0, dst_row_step);
+                                                       reinterpret_cast<float*>(scales), dst_row0, dst_row_step,
+                                                       pair_hd);
   } else {
     const int64_t nb = cols / geom(fmt).weights;
     k_repack_blocks<<<grid_for(n_rows * nb, 256), 256, 0, stream>>>(fmt, static_cast<const uint8_t*>(src), n_rows,
-                                                                    nb, codes, scales, dst_row0, dst_row_step);
+                                                                    nb, codes, scales, dst_row0, dst_row_step,
+                                                                    pair_hd);
   }
   return launch_status();
 }

@@ -32,7 +32,8 @@ struct Layout {
   std::vector<LayerOff> layer;
   size_t weight_bytes;
   // state
-  size_t kc, vc, x, xn, qkv, att, act, logits, attn_ws, tok_in, tok_out, pos, err, rope;
+  size_t kc, vc, x, xn, qkv, q, att, act, logits, attn_ws, attn_cnt, am_key, am_cnt, tok_in, tok_out, pos, err,
+      rope;
   size_t state_bytes;
   int64_t qkv_rows, cache_batch_stride, cache_layer_stride;
 };
@@ -89,10 +90,14 @@ Layout make_layout(const qd_config* c) {
   L.x = take(4 * B * D);
   L.xn = take(4 * B * D);
   L.qkv = take(4 * B * L.qkv_rows);
+  L.q = take(4 * B * QD);
   L.att = take(4 * B * QD);
   L.act = take(4 * B * F);
   L.logits = take(4 * B * (size_t)c->vocab);
   L.attn_ws = take(attn_workspace_bytes(c->n_heads, c->head_dim, c->max_ctx, (int)B));
+  L.attn_cnt = take(4 * B * (size_t)c->n_kv_heads);
+  L.am_key = take(8 * B);
+  L.am_cnt = take(4);
   L.tok_in = take(4 * B);
   L.tok_out = take(4 * B);
   L.pos = take(4 * B);
@@ -141,39 +146,20 @@ namespace {
   } while (0)
 
 // Enqueue one decode step for `batch` sequences; counts the kernels it launches.
+// Every kernel after the first is launched as a programmatic dependent of its
+// predecessor (it starts prefetching weights while the predecessor finishes).
 qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
   const qd_config& c = m->cfg;
   const Layout& L = m->L;
   const int64_t D = c.dim, F = c.ffn, QD = (int64_t)c.n_heads * c.head_dim, KD = (int64_t)c.n_kv_heads * c.head_dim;
   uint32_t* err = reinterpret_cast<uint32_t*>(m->s + L.err);
-  const int32_t* pos = m->i(L.pos);
-  float *x = m->f(L.x), *xn = m->f(L.xn), *qkv = m->f(L.qkv), *att = m->f(L.att), *act = m->f(L.act);
+  int32_t* pos = m->i(L.pos);
+  float *x = m->f(L.x), *xn = m->f(L.xn), *qkv = m->f(L.qkv), *q = m->f(L.q), *att = m->f(L.att),
+        *act = m->f(L.act);
   int n = 0;
   QD_TRY(launch_embed(c.emb_fmt, m->W(c.emb_fmt, L.emb, c.vocab, D), m->i(L.tok_in), batch, x, err, st));
   ++n;
-  // GEMV with RMSNorm fused into its prologue when the streaming kernel runs, a
-  // separate norm kernel otherwise.  Returns the number of kernels launched.
-  auto normed_gemv = [&](int fmt, PackedView W, const float* gains, float* y, GemvMode mode, int& count) -> qd_status {
-    GemvArgs a;
-    a.fmt = fmt;
-    a.W = W;
-    a.x = x;
-    a.y = y;
-    a.batch = batch;
-    a.mode = mode;
-    a.err = err;
-    if (gemv_streams(a)) {
-      a.norm_g = gains;
-      a.eps = c.eps;
-      count += 1;
-      return launch_q_gemv(a, st);
-    }
-    QD_TRY(launch_rmsnorm(x, gains, xn, (int)D, batch, c.eps, st));
-    a.x = xn;
-    count += 2;
-    return launch_q_gemv(a, st);
-  };
-  auto plain_gemv = [&](int fmt, PackedView W, const float* in, float* y, GemvMode mode) -> qd_status {
+  auto args = [&](int fmt, PackedView W, const float* in, float* y, GemvMode mode) {
     GemvArgs a;
     a.fmt = fmt;
     a.W = W;
@@ -182,31 +168,78 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
     a.batch = batch;
     a.mode = mode;
     a.err = err;
+    a.pdl = true;
+    return a;
+  };
+  // GEMV with RMSNorm fused into its prologue when the streaming kernel runs; a
+  // separate norm kernel (into xn) otherwise.
+  auto normed = [&](GemvArgs a, const float* gains) -> qd_status {
+    if (gemv_streams(a)) {
+      a.norm_g = gains;
+      a.eps = c.eps;
+      ++n;
+      return launch_q_gemv(a, st);
+    }
+    QD_TRY(launch_rmsnorm(x, gains, xn, (int)D, batch, c.eps, st));
+    a.x = xn;
+    n += 2;
     return launch_q_gemv(a, st);
   };
   for (int l = 0; l < c.layers; ++l) {
     const LayerOff& o = L.layer[l];
     float* kc = m->f(L.kc) + (int64_t)l * L.cache_layer_stride;
     float* vc = m->f(L.vc) + (int64_t)l * L.cache_layer_stride;
-    QD_TRY(normed_gemv(c.w_fmt, m->W(c.w_fmt, o.wqkv, L.qkv_rows, D),
-                       reinterpret_cast<const float*>(m->w + o.attn_norm), qkv, kGemvStore, n));
-    // q heads and k heads are adjacent in the fused output: one rotation pass
-    QD_TRY(launch_rope(qkv, c.n_heads + c.n_kv_heads, c.head_dim, L.qkv_rows, pos, c.pairing, m->f(L.rope),
-                       c.max_ctx, batch, err, st));
-    QD_TRY(launch_kv_append(qkv + QD, qkv + QD + KD, L.qkv_rows, kc, vc, c.n_kv_heads, c.head_dim, pos, c.max_ctx,
-                            batch, L.cache_batch_stride, err, st));
-    QD_TRY(launch_attention(qkv, L.qkv_rows, kc, vc, L.cache_batch_stride, att, c.n_heads, c.n_kv_heads, c.head_dim,
-                            pos, c.max_ctx, batch, m->s + L.attn_ws, err, st));
-    QD_TRY(plain_gemv(c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, x, kGemvAccumulate));
-    QD_TRY(normed_gemv(c.w_fmt, m->W(c.w_fmt, o.wgu, 2 * F, D), reinterpret_cast<const float*>(m->w + o.ffn_norm),
-                       act, kGemvSwiGLU, n));
-    QD_TRY(plain_gemv(c.w_fmt, m->W(c.w_fmt, o.wd, D, F), act, x, kGemvAccumulate));
-    n += 6;  // rope, kv, attention (2), wo, wd
+    // QKV projection with RoPE and the cache append fused into its epilogue
+    GemvArgs qa = args(c.w_fmt, m->W(c.w_fmt, o.wqkv, L.qkv_rows, D), x, qkv, kGemvQKV);
+    QkvEpilogue& e = qa.qkv;
+    e.q_rows = (int)QD;
+    e.k_rows = (int)KD;
+    e.head_dim = c.head_dim;
+    e.pairing = c.pairing;
+    e.pos = pos;
+    e.rope = m->f(L.rope);
+    e.q_out = q;
+    e.q_stride = QD;
+    e.kc = kc;
+    e.vc = vc;
+    e.cache_batch_stride = L.cache_batch_stride;
+    e.max_ctx = c.max_ctx;
+    const float* attn_norm = reinterpret_cast<const float*>(m->w + o.attn_norm);
+    if (gemv_streams(qa)) {
+      QD_TRY(normed(qa, attn_norm));
+    } else {
+      GemvArgs raw = qa;
+      raw.mode = kGemvStore;
+      QD_TRY(normed(raw, attn_norm));
+      QD_TRY(launch_qkv_post(qkv, L.qkv_rows, batch, e, err, st, true));
+      ++n;
+    }
+    QD_TRY(launch_attention_fused(q, QD, kc, vc, L.cache_batch_stride, att, c.n_heads, c.n_kv_heads, c.head_dim,
+                                  pos, c.max_ctx, batch, m->s + L.attn_ws,
+                                  reinterpret_cast<unsigned int*>(m->s + L.attn_cnt), err, st, true));
+    ++n;
+    QD_TRY(launch_q_gemv(args(c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, x, kGemvAccumulate), st));
+    ++n;
+    QD_TRY(normed(args(c.w_fmt, m->W(c.w_fmt, o.wgu, 2 * F, D), x, act, kGemvSwiGLU),
+                  reinterpret_cast<const float*>(m->w + o.ffn_norm)));
+    QD_TRY(launch_q_gemv(args(c.w_fmt, m->W(c.w_fmt, o.wd, D, F), act, x, kGemvAccumulate), st));
+    ++n;
   }
-  QD_TRY(normed_gemv(c.emb_fmt, m->W(c.emb_fmt, L.head, c.vocab, D), reinterpret_cast<const float*>(m->w + L.out_norm),
-                     m->f(L.logits), kGemvStore, n));
-  QD_TRY(launch_argmax(m->f(L.logits), c.vocab, batch, m->i(L.tok_out), m->i(L.pos), st));
-  n += 1;
+  // output head with the greedy argmax (and the position advance) fused in
+  GemvArgs ha = args(c.emb_fmt, m->W(c.emb_fmt, L.head, c.vocab, D), x, m->f(L.logits), kGemvArgmax);
+  ha.am.key = reinterpret_cast<unsigned long long*>(m->s + L.am_key);
+  ha.am.counter = reinterpret_cast<unsigned int*>(m->s + L.am_cnt);
+  ha.am.tok_out = m->i(L.tok_out);
+  ha.am.pos = pos;
+  const float* out_norm = reinterpret_cast<const float*>(m->w + L.out_norm);
+  if (gemv_streams(ha)) {
+    QD_TRY(normed(ha, out_norm));
+  } else {
+    ha.mode = kGemvStore;
+    QD_TRY(normed(ha, out_norm));
+    QD_TRY(launch_argmax(m->f(L.logits), c.vocab, batch, m->i(L.tok_out), pos, st));
+    ++n;
+  }
   m->launches = n;
   return QD_OK;
 }
@@ -285,9 +318,11 @@ qd_status qd_model_create(const qd_config* cfg, const void* const* src, void* we
     const LayerOff& o = L.layer[l];
     if ((s = copy_f32(o.attn_norm, T[0], D))) return fail(s);
     if ((s = copy_f32(o.ffn_norm, T[5], D))) return fail(s);
-    // fused QKV: q rows, then k rows, then v rows
-    if ((s = launch_repack_rows(wf, T[1], QD, D, m->w + o.wqkv, L.qkv_rows, 0, 1, st))) return fail(s);
-    if ((s = launch_repack_rows(wf, T[2], KD, D, m->w + o.wqkv, L.qkv_rows, QD, 1, st))) return fail(s);
+    // fused QKV: q rows, then k rows, then v rows; with half pairing the rows of each
+    // RoPE pair (i, i + head_dim/2) are made adjacent for the projection's epilogue
+    const int pair_hd = cfg->pairing == QD_ROPE_HALF ? cfg->head_dim : 0;
+    if ((s = launch_repack_rows(wf, T[1], QD, D, m->w + o.wqkv, L.qkv_rows, 0, 1, st, pair_hd))) return fail(s);
+    if ((s = launch_repack_rows(wf, T[2], KD, D, m->w + o.wqkv, L.qkv_rows, QD, 1, st, pair_hd))) return fail(s);
     if ((s = launch_repack_rows(wf, T[3], KD, D, m->w + o.wqkv, L.qkv_rows, QD + KD, 1, st))) return fail(s);
     if ((s = launch_repack_rows(wf, T[4], D, QD, m->w + o.wo, D, 0, 1, st))) return fail(s);
     // gate/up interleaved: row 2i = gate row i, row 2i+1 = up row i
@@ -341,6 +376,9 @@ qd_status qd_model_reset(qd_model* m, qd_stream_t stream) {
   QD_TRY(zero_region(m->s + m->L.vc, align_up(cache, 16), st));
   QD_TRY(zero_region(m->s + m->L.pos, 16 * ((4 * m->cfg.max_batch + 15) / 16), st));
   QD_TRY(zero_region(m->s + m->L.err, 16, st));
+  QD_TRY(zero_region(m->s + m->L.attn_cnt, align_up(4 * (size_t)m->cfg.max_batch * m->cfg.n_kv_heads, 16), st));
+  QD_TRY(zero_region(m->s + m->L.am_key, align_up(8 * (size_t)m->cfg.max_batch, 16), st));
+  QD_TRY(zero_region(m->s + m->L.am_cnt, 16, st));
   return QD_OK;
 }
 

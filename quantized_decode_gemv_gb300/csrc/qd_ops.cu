@@ -19,6 +19,8 @@ inline int grid1d(int64_t n, int threads) {
 __global__ void __launch_bounds__(512) k_rmsnorm(const float* __restrict__ x, const float* __restrict__ g,
                                                  float* __restrict__ out, int n, float eps) {
   __shared__ float red[32];
+  pdl_wait();
+  pdl_trigger();
   const float* xr = x + (int64_t)blockIdx.x * n;
   float* orow = out + (int64_t)blockIdx.x * n;
   float ss = 0.f;
@@ -94,10 +96,44 @@ constexpr int kAttnWarps = 4;
 constexpr int kHeadDim = 64;
 constexpr int kMaxGroup = 8;
 
-__host__ __device__ inline int attn_chunk(int max_ctx) { return max_ctx <= 1024 ? 64 : 128; }
+__host__ __device__ inline int attn_chunk(int max_ctx) { return max_ctx <= 1024 ? 32 : 128; }
 __host__ __device__ inline int attn_splits(int max_ctx) {
   const int c = attn_chunk(max_ctx);
   return (max_ctx + c - 1) / c;
+}
+
+// Online-softmax walk of positions [p_begin, p_end) by one warp of the CTA: the warp
+// takes batches of kPosBatch consecutive positions (warp-interleaved) and issues the
+// loads of a whole batch before using any of them.
+constexpr int kPosBatch = 8;
+template <int G>
+__device__ __forceinline__ void attn_walk(const float* kb, const float* vb, int p_begin, int p_end, int warp,
+                                          int lane, const float2 (&qv)[G], float (&m)[G], float (&l)[G],
+                                          float2 (&o)[G]) {
+  for (int p0 = p_begin + warp * kPosBatch; p0 < p_end; p0 += kAttnWarps * kPosBatch) {
+    float2 kk[kPosBatch], vv[kPosBatch];
+#pragma unroll
+    for (int i = 0; i < kPosBatch; ++i) {
+      const int p = min(p0 + i, p_end - 1);
+      kk[i] = __ldcg(reinterpret_cast<const float2*>(kb + (int64_t)p * kHeadDim) + lane);
+      vv[i] = __ldcg(reinterpret_cast<const float2*>(vb + (int64_t)p * kHeadDim) + lane);
+    }
+#pragma unroll
+    for (int i = 0; i < kPosBatch; ++i) {
+      if (p0 + i >= p_end) break;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float sc = warp_sum(fmaf(qv[g].x, kk[i].x, qv[g].y * kk[i].y));
+        const float mn = fmaxf(m[g], sc);
+        const float corr = expf(m[g] - mn);  // 0 when m was -inf
+        const float w = expf(sc - mn);
+        l[g] = fmaf(l[g], corr, w);
+        o[g].x = fmaf(o[g].x, corr, w * vv[i].x);
+        o[g].y = fmaf(o[g].y, corr, w * vv[i].y);
+        m[g] = mn;
+      }
+    }
+  }
 }
 
 template <int G>
@@ -119,7 +155,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_partial(
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     const int h = kvh * G + g;
-    const float2 t = reinterpret_cast<const float2*>(q + (int64_t)b * q_stride + (int64_t)h * kHeadDim)[lane];
+    const float2 t = __ldcg(reinterpret_cast<const float2*>(q + (int64_t)b * q_stride + (int64_t)h * kHeadDim) + lane);
     qv[g] = make_float2(t.x * scale, t.y * scale);
   }
   float m[G], l[G];
@@ -132,21 +168,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_partial(
   }
   const float* kb = kc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
   const float* vb = vc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
-  for (int p = p_begin + warp; p < p_end; p += kAttnWarps) {
-    const float2 kk = reinterpret_cast<const float2*>(kb + (int64_t)p * kHeadDim)[lane];
-    const float2 vv = reinterpret_cast<const float2*>(vb + (int64_t)p * kHeadDim)[lane];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float s = warp_sum(fmaf(qv[g].x, kk.x, qv[g].y * kk.y));
-      const float mn = fmaxf(m[g], s);
-      const float corr = expf(m[g] - mn);  // 0 when m was -inf
-      const float w = expf(s - mn);
-      l[g] = fmaf(l[g], corr, w);
-      o[g].x = fmaf(o[g].x, corr, w * vv.x);
-      o[g].y = fmaf(o[g].y, corr, w * vv.y);
-      m[g] = mn;
-    }
-  }
+  attn_walk<G>(kb, vb, p_begin, p_end, warp, lane, qv, m, l, o);
   // merge the warps of this CTA
   __shared__ float sm[kAttnWarps][kMaxGroup], sl[kAttnWarps][kMaxGroup];
   __shared__ float2 so[kAttnWarps][kMaxGroup][32];
@@ -204,6 +226,151 @@ __global__ void k_attn_merge(const float* __restrict__ ws_ml, const float* __res
   dst[d] = acc / lt;
 }
 
+// Single-kernel form for the decode step: each CTA computes its chunk as in
+// k_attn_partial, then the last CTA of its (sequence, kv head) to finish merges the
+// chunks of that kv head's q heads (the same log-sum-exp merge, in split order).  The
+// arrival counter lives in the model state, starts at zero and is reset by that CTA.
+template <int G>
+__global__ void __launch_bounds__(kAttnWarps * 32) k_attn_fused(
+    const float* __restrict__ q, int64_t q_stride, const float* __restrict__ kc, const float* __restrict__ vc,
+    int64_t cache_batch_stride, int n_heads, int n_kv, const int32_t* __restrict__ pos, int max_ctx, float scale,
+    float* __restrict__ ws_ml, float* __restrict__ ws_o, unsigned int* __restrict__ counters, float* __restrict__ out,
+    uint32_t* err) {
+  pdl_wait();     // q and the cache rows come from the QKV projection
+  pdl_trigger();  // let the next kernel start its weight prefetch
+  const int kvh = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
+  const int splits = gridDim.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p_cur = pos[b];
+  const bool valid = p_cur >= 0 && p_cur < max_ctx;
+  if (!valid && err && threadIdx.x == 0 && split == 0 && kvh == 0) atomicOr(err, kErrPosition);
+  const int chunk = attn_chunk(max_ctx);
+  const int p_begin = split * chunk;
+  const int p_end = valid ? min(p_begin + chunk, p_cur + 1) : p_begin;
+
+  float2 qv[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int h = kvh * G + g;
+    const float2 t = __ldcg(reinterpret_cast<const float2*>(q + (int64_t)b * q_stride + (int64_t)h * kHeadDim) + lane);
+    qv[g] = make_float2(t.x * scale, t.y * scale);
+  }
+  float m[G], l[G];
+  float2 o[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m[g] = -INFINITY;
+    l[g] = 0.f;
+    o[g] = make_float2(0.f, 0.f);
+  }
+  const float* kb = kc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
+  const float* vb = vc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
+  attn_walk<G>(kb, vb, p_begin, p_end, warp, lane, qv, m, l, o);
+  __shared__ float sm[kAttnWarps][kMaxGroup], sl[kAttnWarps][kMaxGroup];
+  __shared__ float2 so[kAttnWarps][kMaxGroup][32];
+  __shared__ bool last;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (lane == 0) {
+      sm[warp][g] = m[g];
+      sl[warp][g] = l[g];
+    }
+    so[warp][g][lane] = o[g];
+  }
+  __syncthreads();
+  for (int g = warp; g < G; g += kAttnWarps) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w2 = 0; w2 < kAttnWarps; ++w2) mx = fmaxf(mx, sm[w2][g]);
+    float lt = 0.f;
+    float2 ot = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int w2 = 0; w2 < kAttnWarps; ++w2) {
+      const float f = (sm[w2][g] == -INFINITY) ? 0.f : expf(sm[w2][g] - mx);
+      lt = fmaf(sl[w2][g], f, lt);
+      ot.x = fmaf(so[w2][g][lane].x, f, ot.x);
+      ot.y = fmaf(so[w2][g][lane].y, f, ot.y);
+    }
+    const int h = kvh * G + g;
+    const int64_t slot = ((int64_t)b * n_heads + h) * splits + split;
+    if (lane == 0) {
+      ws_ml[slot * 2] = mx;
+      ws_ml[slot * 2 + 1] = lt;
+    }
+    reinterpret_cast<float2*>(ws_o + slot * kHeadDim)[lane] = ot;
+  }
+  __threadfence();
+  __syncthreads();
+  unsigned int* cnt = counters + (int64_t)b * n_kv + kvh;
+  if (threadIdx.x == 0) last = atomicAdd(cnt, 1u) == (unsigned)splits - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const int used = valid ? p_cur / chunk + 1 : 0;
+  for (int g = warp; g < G; g += kAttnWarps) {
+    const int h = kvh * G + g;
+    float2* dst = reinterpret_cast<float2*>(out + ((int64_t)b * n_heads + h) * kHeadDim);
+    if (!valid) {
+      dst[lane] = make_float2(0.f, 0.f);
+      continue;
+    }
+    const int64_t base = ((int64_t)b * n_heads + h) * splits;
+    float mx = -INFINITY;
+    for (int s2 = 0; s2 < used; ++s2) mx = fmaxf(mx, __ldcg(ws_ml + (base + s2) * 2));
+    float lt = 0.f;
+    float2 acc = make_float2(0.f, 0.f);
+    for (int s2 = 0; s2 < used; ++s2) {
+      const float f = expf(__ldcg(ws_ml + (base + s2) * 2) - mx);
+      lt = fmaf(__ldcg(ws_ml + (base + s2) * 2 + 1), f, lt);
+      const float2 ov = __ldcg(reinterpret_cast<const float2*>(ws_o + (base + s2) * kHeadDim) + lane);
+      acc.x = fmaf(ov.x, f, acc.x);
+      acc.y = fmaf(ov.y, f, acc.y);
+    }
+    dst[lane] = make_float2(acc.x / lt, acc.y / lt);
+  }
+  if (threadIdx.x == 0) *cnt = 0u;
+}
+
+// ------------------------------------------------------------------ QKV post-processing
+// The kGemvQKV epilogue as a kernel, for projections computed by the register-path
+// GEMV: qkv[b] holds the packed-order rows (RoPE pairs adjacent in q and k).
+__global__ void k_qkv_post(const float* __restrict__ qkv, int64_t qkv_stride, QkvEpilogue e, int v_rows,
+                           uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.y;
+  const int pos = e.pos[b];
+  if (pos < 0 || pos >= e.max_ctx) {
+    if (err && threadIdx.x == 0 && blockIdx.x == 0) atomicOr(err, kErrPosition);
+    return;
+  }
+  const int hd = e.head_dim, half = hd / 2;
+  const int pairs = (e.q_rows + e.k_rows + v_rows) / 2;
+  const float* src = qkv + (int64_t)b * qkv_stride;
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < pairs; t += gridDim.x * blockDim.x) {
+    const int r = 2 * t;
+    const float a = src[r], bb = src[r + 1];
+    if (r < e.q_rows + e.k_rows) {
+      const bool isq = r < e.q_rows;
+      const int local = isq ? r : r - e.q_rows;
+      const int h = local / hd, pi = (local % hd) / 2;
+      const int d0 = e.pairing == QD_ROPE_HALF ? pi : 2 * pi;
+      const int d1 = e.pairing == QD_ROPE_HALF ? pi + half : 2 * pi + 1;
+      const float c = e.rope[((int64_t)pos * half + pi) * 2], s = e.rope[((int64_t)pos * half + pi) * 2 + 1];
+      float* dst = isq ? e.q_out + (int64_t)b * e.q_stride + (int64_t)h * hd
+                       : e.kc + (int64_t)b * e.cache_batch_stride + ((int64_t)h * e.max_ctx + pos) * hd;
+      dst[d0] = a * c - bb * s;
+      dst[d1] = a * s + bb * c;
+    } else {
+      const int local = r - e.q_rows - e.k_rows;
+      const int h = local / hd, d = local % hd;
+      float* dst = e.vc + (int64_t)b * e.cache_batch_stride + ((int64_t)h * e.max_ctx + pos) * hd;
+      dst[d] = a;
+      dst[d + 1] = bb;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ SwiGLU
 __global__ void k_swiglu(const float* __restrict__ g, const float* __restrict__ u, float* __restrict__ out,
                          int64_t n) {
@@ -227,6 +394,8 @@ __global__ void __launch_bounds__(1024) k_argmax(const float* __restrict__ logit
                                                  int32_t* __restrict__ out, int32_t* __restrict__ pos_adv) {
   __shared__ float sv[32];
   __shared__ int si[32];
+  pdl_wait();
+  pdl_trigger();
   const float* row = logits + (int64_t)blockIdx.x * n;
   float bv = -INFINITY;
   int bi = (int)n;
@@ -338,6 +507,43 @@ qd_status launch_attention(const float* q, int64_t q_stride, const float* kc, co
   k_attn_merge<<<dim3((unsigned)n_heads, (unsigned)batch), kHeadDim, 0, stream>>>(ws_ml, ws_o, n_heads, splits, pos,
                                                                                   max_ctx, out);
   return launch_status();
+}
+
+qd_status launch_attention_fused(const float* q, int64_t q_stride, const float* kc, const float* vc,
+                                 int64_t cache_batch_stride, float* out, int n_heads, int n_kv, int head_dim,
+                                 const int32_t* pos, int max_ctx, int batch, void* ws, unsigned int* counters,
+                                 uint32_t* err, cudaStream_t stream, bool pdl) {
+  const int splits = attn_splits(max_ctx);
+  const int G = n_heads / n_kv;
+  const size_t slots = (size_t)batch * n_heads * splits;
+  float* ws_ml = static_cast<float*>(ws);
+  float* ws_o = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(slots * 2 * sizeof(float), 256));
+  const float scale = 1.0f / sqrtf((float)head_dim);
+  const dim3 grid((unsigned)n_kv, (unsigned)splits, (unsigned)batch), block(kAttnWarps * 32);
+#define QD_ATTN_FUSED(GG)                                                                                      \
+  case GG:                                                                                                     \
+    return launch_k(k_attn_fused<GG>, grid, block, 0, stream, pdl, q, q_stride, kc, vc, cache_batch_stride,   \
+                    n_heads, n_kv, pos, max_ctx, scale, ws_ml, ws_o, counters, out, err);
+  switch (G) {
+    QD_ATTN_FUSED(1)
+    QD_ATTN_FUSED(2)
+    QD_ATTN_FUSED(3)
+    QD_ATTN_FUSED(4)
+    QD_ATTN_FUSED(5)
+    QD_ATTN_FUSED(6)
+    QD_ATTN_FUSED(7)
+    QD_ATTN_FUSED(8)
+    default: return QD_ERR_UNSUPPORTED;
+  }
+#undef QD_ATTN_FUSED
+}
+
+qd_status launch_qkv_post(const float* qkv, int64_t qkv_stride, int batch, const QkvEpilogue& e, uint32_t* err,
+                          cudaStream_t stream, bool pdl) {
+  const int v_rows = e.k_rows;  // as many value rows as key rows
+  const int pairs = (e.q_rows + e.k_rows + v_rows) / 2;
+  const dim3 grid((unsigned)grid1d(pairs, 256), (unsigned)batch);
+  return launch_k(k_qkv_post, grid, dim3(256), 0, stream, pdl, qkv, qkv_stride, e, v_rows, err);
 }
 
 qd_status launch_swiglu(const float* g, const float* u, float* out, int64_t n, int batch, cudaStream_t stream) {
