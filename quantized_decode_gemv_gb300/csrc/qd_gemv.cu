@@ -324,10 +324,10 @@ qd_status launch_fmt(const PackedView& W, const float* x, float* y, int batch, i
 }  // namespace
 
 qd_status launch_q_gemv(const GemvArgs& a, cudaStream_t stream) {
-  // Batch 1-2: the TMA-staged streaming kernel (it also fuses RMSNorm).  Other
-  // batches: the register-path kernel below (RMSNorm must have been applied by the
-  // caller, see gemv_fuses_norm).
-  if (a.batch <= 2) {
+  // Batch 1-8 and the shapes it supports: the streaming kernel (it also fuses
+  // RMSNorm).  Otherwise the register-path kernel below (RMSNorm must then have been
+  // applied by the caller, see gemv_streams).
+  {
     const qd_status st = launch_q_gemv_stream(a, stream);
     if (st != QD_ERR_UNSUPPORTED) return st;
   }

@@ -1,4 +1,4 @@
-// Streaming q_gemv for batch 1-2 on the CUDA cores.
+// Streaming q_gemv for batch 1-8 on the CUDA cores.
 //
 // y[b][r] = sum_c deq(W)[r][c] * x[b][c]  (llmoxide blog s1 and s10's row dot;
 // dasLLAMA 8.7.1.4 matmul), the weights decoded in registers with no f32 copy
@@ -16,13 +16,18 @@
 //    `griddepcontrol.wait`, so under programmatic dependent launch the weight fetch
 //    overlaps the predecessor kernel.  (A TMA-staged variant with a producer warp and
 //    an mbarrier ring reached the same DRAM rate but paid a CTA barrier per tile.)
-//  * x * g is staged once per CTA in shared memory, padded to 9 float4 chunks per
-//    32-float unit so 32 lanes (32 units) read it without bank conflicts.  With RMSNorm
-//    fused, the factor 1/sqrt(mean(x^2) + eps) multiplies each finished row sum.
-//  * A 4-bit code q becomes the float 1 + q/16 with one byte permute (q lands in
-//    mantissa bits 19-22 of 1.0f); paired FFMA2s accumulate sum f*x, and
-//    sum (q-8) x = 16 sum f x - 24 sum x.  8-bit codes land in the low mantissa of 2^23
-//    and 2^23 + 128 is subtracted (exact).  Each block scale multiplies a 32-term sum.
+//  * The dot products run on the integer pipe.  Once per CTA, each 32-element unit of
+//    x * g is written as 24-bit integers xq with one power-of-two scale s, 2^-22 of the
+//    unit's largest |x| rounded down to a power of two (error at most s/2 per element,
+//    about the rounding of an f32; exact for dyadic x), held as three byte
+//    planes (signed high, unsigned middle and low bytes) so that one dp4a multiplies
+//    four codes with four bytes of a plane: sum q x = s * (65536 sum q x2 +
+//    256 sum q x1 + sum q x0), each plane's sum exact in int32.  A 4-bit code word
+//    needs one LOP3 (and a shift) per four codes, so a Q4_0 weight costs under 1.5
+//    instructions instead of a float decode plus an FMA.  (Two planes, 16 bits, lost
+//    up to 2e-5 of a unit's largest |x| per element: too much where a short row sum
+//    cancels.)  With RMSNorm fused, 1/sqrt(mean(x^2) + eps) multiplies each finished
+//    row sum.
 //  * A warp reduces its RW x NB row sums with one reduce-scatter and writes them (or
 //    feeds the fused epilogues: SwiGLU, RoPE + KV append, argmax).
 #include "qd_internal.cuh"
@@ -34,12 +39,27 @@ namespace stream_gemv {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 
-
-// 4-bit code byte k of m (prepared as 0x80 | q<<3 per byte) -> the float 1 + q/16.
-__device__ __forceinline__ float q4f(uint32_t m, int k) {
-  return __uint_as_float(__byte_perm(m, 0x3F000000u, 0x7044u | ((uint32_t)k << 8)));
+// Four-way byte dot products with an int32 accumulator (a: weight codes, b: x bytes).
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {  // a unsigned, b signed
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
-__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {  // both unsigned
+  int d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {  // both signed
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c) {  // a signed, b unsigned
+  int d;
+  asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
 
 // Sum of v[k] over the warp for V values at once: afterwards lanes
 // [k*32/V, (k+1)*32/V) hold the total of value k.
@@ -61,13 +81,7 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[V], int lane) {
   return t;
 }
 
-// Shared-memory x: each 32-float unit occupies 9 float4 chunks (one of padding), so
-// unit u starts at chunk 9u.  Lanes reading the same chunk of 8 consecutive units land
-// on 8 different 16-byte bank groups, and a lane's 8 chunks sit at fixed immediate
-// offsets from its unit base.
-__device__ __forceinline__ int xchunk(int e) { return (e >> 5) * 9 + ((e & 31) >> 2); }
-
-// Element offsets (in x) of the two 16-float halves A, B of unit u:
+// Element offsets (in x) of the two 16-element halves A, B of unit u:
 //  Q4_0: A = [32u, 32u+16), B = [32u+16, 32u+32); code byte i: low nibble -> A[i], high -> B[i]
 //  Q4_K: u = 8s + 2c + h, A = [256s+64c+16h, +16), B = A + 32; same nibble rule
 //  Q8_0 / INT8: A <- code bytes 0..15, B <- bytes 16..31
@@ -80,19 +94,18 @@ template <int FMT>
 __device__ __forceinline__ int unit_xb(int u) {
   return unit_xa<FMT>(u) + ((FMT == QD_Q4_K) ? 32 : 16);
 }
-// Padded-layout chunk index of the first float4 of half A / B of unit u.
-template <int FMT>
-__device__ __forceinline__ int unit_ca(int u) {
-  return xchunk(unit_xa<FMT>(u));
-}
-template <int FMT>
-__device__ __forceinline__ int unit_cb(int u) {
-  return xchunk(unit_xb<FMT>(u));
-}
 template <int FMT>
 constexpr int code_bytes() {
   return (FMT == QD_Q8_0 || FMT == QD_I8_ROW) ? 32 : 16;
 }
+
+// Shared-memory x records: per batch row and unit, 112 bytes in seven 16-byte chunks:
+// 0/1 the high bytes of halves A/B, 2/3 the middle bytes, 4/5 the low bytes, 6 the
+// unit's metadata: the scale s and, for Q4_0, -8 times each plane's element sum (the
+// code offset, as int bits); for Q4_K, sum x over A and over B.  The 7-chunk stride
+// puts 8 lanes reading one chunk of 8 consecutive units on 8 different bank groups.
+constexpr int kRecBytes = 112;
+__device__ __forceinline__ int rec_off(int u, int k) { return u * kRecBytes + 16 * k; }
 
 struct Params {
   PackedView W;
@@ -174,7 +187,11 @@ __device__ __forceinline__ void cp_wait() {
 // lane reads back only what it copied) and then 64 bytes of scale data per row:
 // Q4_0/Q8_0 the 32 lanes' f16 scales, Q4_K the 4 super-block headers the 32 units
 // span, INT8 the row scale.
-constexpr int kStages = 4;
+#ifndef QD_GEMV_STAGES
+#define QD_GEMV_STAGES 4
+#endif
+constexpr int kStages = QD_GEMV_STAGES;
+static_assert(kStages >= 2 && kStages <= 16, "ring depth");
 template <int FMT, int RW>
 constexpr int slot_code_bytes() {
   return RW * 32 * code_bytes<FMT>();
@@ -210,89 +227,117 @@ struct Acc {
   float v[RW][NB];
 };
 
-// Compute one unit step from a staged slot into acc.
+// Q4_K (scale, min) of sub-block j (0..7) from the 12 scale bytes held as three
+// little-endian words; the same bit layout as q4k_scale_min, read from registers.
+__device__ __forceinline__ void q4k_sm_words(uint32_t w0, uint32_t w1, uint32_t w2, int j, int& sc, int& m) {
+  const int sh = 8 * (j & 3);
+  const uint32_t b0 = (w0 >> sh) & 0xFFu, b1 = (w1 >> sh) & 0xFFu, b2 = (w2 >> sh) & 0xFFu;
+  const int lo_sc = (int)(b0 & 63u), lo_m = (int)(b1 & 63u);
+  const int hi_sc = (int)((b2 & 15u) | ((b0 >> 6) << 4)), hi_m = (int)((b2 >> 4) | ((b1 >> 6) << 4));
+  sc = j < 4 ? lo_sc : hi_sc;
+  m = j < 4 ? lo_m : hi_m;
+}
+
+// Dot of 8 code words (half A: words 0-3, half B: words 4-7) with one byte plane of a
+// unit record (chunks ca, ca + 1), starting from c.
+template <bool CODES_SIGNED, bool PLANE_SIGNED>
+__device__ __forceinline__ int plane_dot(const uint32_t (&w)[8], uint4 pa, uint4 pb, int c) {
+  const uint32_t xv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    if constexpr (CODES_SIGNED && PLANE_SIGNED) c = dp4a_ss(w[t], xv[t], c);
+    else if constexpr (CODES_SIGNED) c = dp4a_su(w[t], xv[t], c);
+    else if constexpr (PLANE_SIGNED) c = dp4a_us(w[t], xv[t], c);
+    else c = dp4a_uu(w[t], xv[t], c);
+  }
+  return c;
+}
+// Same over 4 code words against one 16-byte chunk.
+template <bool PLANE_SIGNED>
+__device__ __forceinline__ int half_dot(const uint32_t* w, uint4 p, int c) {
+  const uint32_t xv[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) c = PLANE_SIGNED ? dp4a_us(w[t], xv[t], c) : dp4a_uu(w[t], xv[t], c);
+  return c;
+}
+// 65536 h + 256 m + l as a float (h exact; the rest rounded once).
+__device__ __forceinline__ float planes_value(int h, int m, int l) {
+  return fmaf((float)h, 65536.f, (float)(m * 256 + l));
+}
+
+// Compute one unit step (unit u of the RW rows staged in `slot`) into acc.
 template <int FMT, int NB, int RW>
-__device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* slot, const float4* xs4, int xstride,
-                                             int u, int lane) {
+__device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* slot, const uint8_t* xq, int units,
+                                             int u, int lane, int batch) {
   constexpr int CB = code_bytes<FMT>();
   const uint8_t* sc = slot + slot_code_bytes<FMT, RW>();
-  const int ca = unit_ca<FMT>(u), cb = unit_cb<FMT>(u);
+  // codes: Q4_0 / Q4_K word t < 4 = low nibbles of code bytes 4t..4t+3 (half A),
+  // t >= 4 = their high nibbles (half B); Q8_0 / INT8 the 32 code bytes in order
+  uint32_t w[RW][8];
+  float dq[RW], dm[RW];
+  int s0[RW], s1[RW], m0[RW], m1[RW];
+#pragma unroll
+  for (int rr = 0; rr < RW; ++rr) {
+    const uint8_t* cp = slot + (rr * 32 + lane) * CB;
+    if constexpr (FMT == QD_Q4_0 || FMT == QD_Q4_K) {
+      const uint4 q = *reinterpret_cast<const uint4*>(cp);
+      const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        w[rr][t] = wv[t] & 0x0F0F0F0Fu;
+        w[rr][t + 4] = (wv[t] >> 4) & 0x0F0F0F0Fu;
+      }
+    } else {
+      const uint4 q0 = *reinterpret_cast<const uint4*>(cp);
+      const uint4 q1 = *reinterpret_cast<const uint4*>(cp + 16);
+      w[rr][0] = q0.x; w[rr][1] = q0.y; w[rr][2] = q0.z; w[rr][3] = q0.w;
+      w[rr][4] = q1.x; w[rr][5] = q1.y; w[rr][6] = q1.z; w[rr][7] = q1.w;
+    }
+    dm[rr] = 0.f;
+    s0[rr] = s1[rr] = m0[rr] = m1[rr] = 0;
+    if constexpr (FMT == QD_Q4_0 || FMT == QD_Q8_0) {
+      dq[rr] = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sc + rr * 64 + 2 * lane));
+    } else if constexpr (FMT == QD_Q4_K) {
+      const uint4 hdr = *reinterpret_cast<const uint4*>(sc + rr * 64 + (lane >> 3) * 16);
+      const int j0 = 2 * ((u >> 1) & 3);
+      q4k_sm_words(hdr.y, hdr.z, hdr.w, j0, s0[rr], m0[rr]);
+      q4k_sm_words(hdr.y, hdr.z, hdr.w, j0 + 1, s1[rr], m1[rr]);
+      dq[rr] = f16_bits_to_f32(hdr.x & 0xFFFFu);
+      dm[rr] = f16_bits_to_f32(hdr.x >> 16);
+    } else {
+      dq[rr] = 1.f;  // INT8: the row scale multiplies the finished row sum
+    }
+  }
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
-    const float4* xb = xs4 + b * xstride;
-    float4 xa4[4], xb4[4];
+    if (NB > 1 && b >= batch) break;
+    const uint8_t* rec = xq + ((size_t)b * units + u) * kRecBytes;
+    const uint4 hA = *reinterpret_cast<const uint4*>(rec + 0), hB = *reinterpret_cast<const uint4*>(rec + 16);
+    const uint4 mA = *reinterpret_cast<const uint4*>(rec + 32), mB = *reinterpret_cast<const uint4*>(rec + 48);
+    const uint4 lA = *reinterpret_cast<const uint4*>(rec + 64), lB = *reinterpret_cast<const uint4*>(rec + 80);
+    const float4 mt = *reinterpret_cast<const float4*>(rec + 96);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      xa4[k] = xb[ca + k];
-      xb4[k] = xb[cb + k];
-    }
-    if constexpr (FMT == QD_Q4_0 || FMT == QD_Q4_K) {
-      // sums of the unit's two x halves (the 4-bit formats' block offsets)
-      float sa = 0.f, sbb = 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        sa += (xa4[k].x + xa4[k].y) + (xa4[k].z + xa4[k].w);
-        sbb += (xb4[k].x + xb4[k].y) + (xb4[k].z + xb4[k].w);
-      }
-#pragma unroll
-      for (int rr = 0; rr < RW; ++rr) {
-        const uint4 q = *reinterpret_cast<const uint4*>(slot + (rr * 32 + lane) * CB);
-        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
-        float2 aa = f2(0.f, 0.f), ab = f2(0.f, 0.f), ac = f2(0.f, 0.f), ad = f2(0.f, 0.f);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const uint32_t ml = ((wv[t] << 3) & 0x78787878u) | 0x80808080u;
-          const uint32_t mh = ((wv[t] >> 1) & 0x78787878u) | 0x80808080u;
-          aa = __ffma2_rn(f2(q4f(ml, 0), q4f(ml, 1)), f2(xa4[t].x, xa4[t].y), aa);
-          ab = __ffma2_rn(f2(q4f(ml, 2), q4f(ml, 3)), f2(xa4[t].z, xa4[t].w), ab);
-          ac = __ffma2_rn(f2(q4f(mh, 0), q4f(mh, 1)), f2(xb4[t].x, xb4[t].y), ac);
-          ad = __ffma2_rn(f2(q4f(mh, 2), q4f(mh, 3)), f2(xb4[t].z, xb4[t].w), ad);
-        }
-        const float fa = (aa.x + aa.y) + (ab.x + ab.y);  // sum f x over A
-        const float fb = (ac.x + ac.y) + (ad.x + ad.y);  // over B
-        if constexpr (FMT == QD_Q4_0) {
-          // sum (q-8) x = 16 (fa + fb) - 24 (sum A + sum B)
-          const float d = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sc + rr * 64 + 2 * lane));
-          acc.v[rr][b] = fmaf(d, fmaf(16.f, fa + fb, -24.f * (sa + sbb)), acc.v[rr][b]);
-        } else {
-          const uint4 hdr = *reinterpret_cast<const uint4*>(sc + rr * 64 + (lane >> 3) * 16);
-          const int cc = (u >> 1) & 3;
-          uint8_t sb8[12];
-          const uint32_t hw[3] = {hdr.y, hdr.z, hdr.w};
-#pragma unroll
-          for (int k = 0; k < 12; ++k) sb8[k] = (uint8_t)(hw[k >> 2] >> (8 * (k & 3)));
-          int sc0, m0, sc1, m1;
-          q4k_scale_min(2 * cc, sb8, sc0, m0);
-          q4k_scale_min(2 * cc + 1, sb8, sc1, m1);
-          const float dd = f16_bits_to_f32(hdr.x & 0xFFFFu), dmin = f16_bits_to_f32(hdr.x >> 16);
-          // sum q x_A = 16 (fa - sum A); value d sc q - dmin m
-          float v = fmaf(dd * (float)sc0, 16.f * (fa - sa), -(dmin * (float)m0) * sa);
-          v = fmaf(dd * (float)sc1, 16.f * (fb - sbb), fmaf(-(dmin * (float)m1), sbb, v));
-          acc.v[rr][b] += v;
-        }
-      }
-    } else {  // Q8_0, INT8: 32 signed bytes
-      const float2 off = f2(-(kMagic + 128.f), -(kMagic + 128.f));
-#pragma unroll
-      for (int rr = 0; rr < RW; ++rr) {
-        const uint4 q0 = *reinterpret_cast<const uint4*>(slot + (rr * 32 + lane) * CB);
-        const uint4 q1 = *reinterpret_cast<const uint4*>(slot + (rr * 32 + lane) * CB + 16);
-        const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        float2 a0 = f2(0.f, 0.f), a1 = f2(0.f, 0.f);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const uint32_t w = wv[t] ^ 0x80808080u;
-          const float4 xv = t < 4 ? xa4[t & 3] : xb4[t & 3];
-          a0 = __ffma2_rn(__fadd2_rn(f2(byte_as_magic(w, 0), byte_as_magic(w, 1)), off), f2(xv.x, xv.y), a0);
-          a1 = __ffma2_rn(__fadd2_rn(f2(byte_as_magic(w, 2), byte_as_magic(w, 3)), off), f2(xv.z, xv.w), a1);
-        }
-        const float s = (a0.x + a0.y) + (a1.x + a1.y);
-        if constexpr (FMT == QD_Q8_0) {
-          const float d = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sc + rr * 64 + 2 * lane));
-          acc.v[rr][b] = fmaf(d, s, acc.v[rr][b]);
-        } else {
-          acc.v[rr][b] += s;
-        }
+    for (int rr = 0; rr < RW; ++rr) {
+      if constexpr (FMT == QD_Q4_0) {
+        // planes start at -8 * their element sums: sum (q - 8) xq, plane by plane
+        const int h = plane_dot<false, true>(w[rr], hA, hB, __float_as_int(mt.y));
+        const int m = plane_dot<false, false>(w[rr], mA, mB, __float_as_int(mt.z));
+        const int l = plane_dot<false, false>(w[rr], lA, lB, __float_as_int(mt.w));
+        acc.v[rr][b] = fmaf(dq[rr] * mt.x, planes_value(h, m, l), acc.v[rr][b]);
+      } else if constexpr (FMT == QD_Q4_K) {
+        // value d sc q - dmin m, summed over halves A (sub-block 2c) and B (2c + 1)
+        const float va = planes_value(half_dot<true>(w[rr], hA, 0), half_dot<false>(w[rr], mA, 0),
+                                      half_dot<false>(w[rr], lA, 0));
+        const float vb = planes_value(half_dot<true>(w[rr] + 4, hB, 0), half_dot<false>(w[rr] + 4, mB, 0),
+                                      half_dot<false>(w[rr] + 4, lB, 0));
+        const float q = fmaf((float)s0[rr], va, (float)s1[rr] * vb);
+        const float mins = fmaf((float)m0[rr], mt.y, (float)m1[rr] * mt.z);
+        acc.v[rr][b] = fmaf(dq[rr] * mt.x, q, fmaf(-dm[rr], mins, acc.v[rr][b]));
+      } else {
+        const int h = plane_dot<true, true>(w[rr], hA, hB, 0);
+        const int m = plane_dot<true, false>(w[rr], mA, mB, 0);
+        const int l = plane_dot<true, false>(w[rr], lA, lB, 0);
+        acc.v[rr][b] = fmaf(dq[rr] * mt.x, planes_value(h, m, l), acc.v[rr][b]);
       }
     }
   }
@@ -300,7 +345,8 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
 
 template <int FMT, int NB, int RW>
 __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
-  extern __shared__ __align__(128) uint8_t smem[];  // [warps][kStages] slots, then x [NB][units][9 float4]
+  // dynamic shared memory: [warps][kStages] ring slots, then the x records [NB][units]
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float red[kWarps][NB];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const PackedView& W = p.W;
@@ -314,8 +360,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
   constexpr uint32_t SB = slot_bytes<FMT, RW>();
   uint8_t* ring = smem + (size_t)warp * kStages * SB;
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
-  const int xstride = units * 9;  // float4 chunks per batch column
-  float4* xs4 = reinterpret_cast<float4*>(smem + (size_t)kWarps * kStages * SB);
+  uint8_t* xq = smem + (size_t)kWarps * kStages * SB;
 
   // ---- start streaming the first steps (weights never depend on the previous kernel)
   int64_t lg = gw;  // group of the next copy
@@ -339,32 +384,81 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
 
   pdl_wait();  // x is the previous kernel's output
 
-  // ---- stage x * g (x itself without norm) in shared memory.  RMSNorm is
-  // x * g / sqrt(mean(x^2) + eps): the scalar 1/sqrt(...) multiplies each finished row
-  // sum instead, so one barrier suffices.
+  // ---- x * g as 24-bit integer records (see the header comment).  Eight lanes build
+  // one unit: lane k < 4 takes elements 4k..4k+3 of half A, lane k >= 4 those of half
+  // B.  RMSNorm's 1/sqrt(mean(x^2) + eps) multiplies the finished row sums instead, so
+  // one barrier suffices.
   float inv[NB];
   {
-    const int chunks = cols / 4;
-    float ss[NB];
+    const int k = lane & 7;
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
-      ss[b] = 0.f;
-      float4* dst = xs4 + b * xstride;
-      const float4* xr = reinterpret_cast<const float4*>(p.x + (int64_t)(b < p.batch ? b : 0) * cols);
-      const float4* gr = reinterpret_cast<const float4*>(p.norm_g);
-      for (int i = threadIdx.x; i < chunks; i += kThreads) {
-        float4 v = __ldcg(xr + i);
-        if (b >= p.batch) v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (p.norm_g) {
-          ss[b] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[b]))));
-          const float4 g = __ldg(gr + i);
-          v = make_float4(v.x * g.x, v.y * g.y, v.z * g.z, v.w * g.w);
+      float ss = 0.f;
+      if (b < p.batch) {
+        const float* xr = p.x + (int64_t)b * cols;
+        for (int ub = warp * 4; ub < units; ub += kWarps * 4) {  // uniform per warp
+          const int u = ub + (lane >> 3);
+          const bool ok = u < units;
+          const int e = k < 4 ? unit_xa<FMT>(u) + 4 * k : unit_xb<FMT>(u) + 4 * (k - 4);
+          float4 v = ok ? __ldcg(reinterpret_cast<const float4*>(xr + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (p.norm_g) {
+            ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+            const float4 g = ok ? __ldg(reinterpret_cast<const float4*>(p.norm_g + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v = make_float4(v.x * g.x, v.y * g.y, v.z * g.z, v.w * g.w);
+          }
+          float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+          if (isnan(v.x) || isnan(v.y) || isnan(v.z) || isnan(v.w)) m = INFINITY;  // fmaxf drops NaN
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          // Power-of-two scale s = 2^(F - 22) for a largest |value| m in [2^F, 2^(F+1)),
+          // so |x / s| < 2^23 and x / s is exact for dyadic x (integers, the tests'
+          // exact case).  Units with m below 2^-100 are stored as zeros.
+          const int F = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;
+          const bool live = F >= -100;
+          const float r = live ? __uint_as_float((uint32_t)(127 + 22 - F) << 23) : 0.f;
+          // a non-finite x (F = 128) gives a NaN scale, so the row sums become NaN
+          const float sc = F == 128 ? __uint_as_float(0x7FC00000u)
+                                    : live ? __uint_as_float((uint32_t)(127 - 22 + F) << 23) : 0.f;
+          // x / s may still round up to 2^23 (one fractional bit): clamp to 24 bits
+          auto to_q = [&](float f) { return max(min(__float2int_rn(f * r), 8388607), -8388607); };
+          const int q0 = to_q(v.x), q1 = to_q(v.y), q2 = to_q(v.z), q3 = to_q(v.w);
+          // bytes 2, 1, 0 of a 24-bit two's-complement value: its signed high part and
+          // two unsigned parts, q = 65536 * hi + 256 * mid + lo
+          const uint32_t w2 = __byte_perm(__byte_perm(q0, q1, 0x0062u), __byte_perm(q2, q3, 0x0062u), 0x5410u);
+          const uint32_t w1 = __byte_perm(__byte_perm(q0, q1, 0x0051u), __byte_perm(q2, q3, 0x0051u), 0x5410u);
+          const uint32_t w0 = __byte_perm(__byte_perm(q0, q1, 0x0040u), __byte_perm(q2, q3, 0x0040u), 0x5410u);
+          uint8_t* rec = xq + ((size_t)b * units + u) * kRecBytes;
+          const int off = 16 * (k >> 2) + 4 * (k & 3);
+          if (ok) {
+            *reinterpret_cast<uint32_t*>(rec + off) = w2;
+            *reinterpret_cast<uint32_t*>(rec + 32 + off) = w1;
+            *reinterpret_cast<uint32_t*>(rec + 64 + off) = w0;
+          }
+          float4 meta = make_float4(sc, 0.f, 0.f, 0.f);
+          if constexpr (FMT == QD_Q4_0) {
+            int s2 = (q0 >> 16) + (q1 >> 16) + (q2 >> 16) + (q3 >> 16);
+            int s1 = ((q0 >> 8) & 255) + ((q1 >> 8) & 255) + ((q2 >> 8) & 255) + ((q3 >> 8) & 255);
+            int s0 = (q0 & 255) + (q1 & 255) + (q2 & 255) + (q3 & 255);
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+              s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+              s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+              s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+            }
+            meta = make_float4(sc, __int_as_float(-8 * s2), __int_as_float(-8 * s1), __int_as_float(-8 * s0));
+          } else if constexpr (FMT == QD_Q4_K) {
+            float sv = (v.x + v.y) + (v.z + v.w);
+            sv += __shfl_xor_sync(0xffffffffu, sv, 1);
+            sv += __shfl_xor_sync(0xffffffffu, sv, 2);  // lanes 0-3: sum over A, 4-7: over B
+            meta = make_float4(sc, sv, __shfl_xor_sync(0xffffffffu, sv, 4), 0.f);
+          }
+          if (ok && k == 0) *reinterpret_cast<float4*>(rec + 96) = meta;
         }
-        dst[(i >> 3) * 9 + (i & 7)] = v;
       }
       if (p.norm_g) {
-        ss[b] = warp_sum(ss[b]);
-        if (lane == 0) red[warp][b] = ss[b];
+        ss = warp_sum(ss);
+        if (lane == 0) red[warp][b] = ss;
       }
     }
     __syncthreads();
@@ -382,7 +476,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
 
   // ---- main loop over this warp's (group, unit step) sequence
   pdl_trigger();  // the next kernel may start its own weight prefetch now
-  unsigned long long best0 = 0, best1 = 0;  // kGemvArgmax: best (value, index) keys per batch row
+  unsigned long long best[NB];  // kGemvArgmax: best (value, index) key per batch row
+#pragma unroll
+  for (int b = 0; b < NB; ++b) best[b] = 0ull;
   Acc<NB, RW> acc;
   int cs = 0;  // slot of the step being computed
   int j = 0;
@@ -399,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
     }
     const int u = lane + 32 * j;
     const uint8_t* slot = ring + (size_t)cs * SB;
-    if (u < units) compute_step<FMT, NB, RW>(acc, slot, xs4, xstride, u, lane);
+    if (u < units) compute_step<FMT, NB, RW>(acc, slot, xq, units, u, lane, p.batch);
     float rsc[RW];  // INT8 row scales (staged with every step)
     if constexpr (FMT == QD_I8_ROW) {
 #pragma unroll
@@ -418,16 +514,20 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
         for (int b = 0; b < NB; ++b) acc.v[rr][b] *= rsc[rr];
     }
     constexpr int V = RW * NB, GRP = 32 / V;
+    static_assert(V <= 32, "one reduce-scatter per group");
     float v[V];
 #pragma unroll
     for (int rr = 0; rr < RW; ++rr)
 #pragma unroll
       for (int b = 0; b < NB; ++b) v[rr * NB + b] = acc.v[rr][b];
-    const int kb_ = (lane / GRP) % NB;  // batch row of this lane's reduced value
-    const float tot = reduce_scatter<V>(v, lane) * (kb_ == 0 ? inv[0] : inv[NB - 1]);
+    const int kb = (lane / GRP) % NB;  // batch row of this lane's reduced value
+    float iv = inv[0];
+#pragma unroll
+    for (int b = 1; b < NB; ++b) iv = kb == b ? inv[b] : iv;
+    const float tot = reduce_scatter<V>(v, lane) * iv;
     const float partner = __shfl_down_sync(0xffffffffu, tot, (NB * GRP) & 31);  // row +1, same batch
     if ((lane % GRP) == 0) {
-      const int k = lane / GRP, rr = k / NB, b = k % NB;
+      const int kk = lane / GRP, rr = kk / NB, b = kk % NB;
       const int64_t r = row0 + rr;
       if (b < p.batch && r < W.rows) {
         if (p.mode == kGemvSwiGLU) {
@@ -438,10 +538,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
         } else {
           if (p.mode == kGemvArgmax) {
             const unsigned long long key = argmax_key(tot, (uint32_t)r);
-            if (b == 0)
-              best0 = key > best0 ? key : best0;
-            else
-              best1 = key > best1 ? key : best1;
+#pragma unroll
+            for (int bb = 0; bb < NB; ++bb)
+              if (bb == b) best[bb] = key > best[bb] ? key : best[bb];
           }
           float* dst = p.y + (int64_t)b * W.rows + r;
           if (p.mode == kGemvAccumulate)
@@ -455,10 +554,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
   }
   cp_wait<0>();  // no copy may still target this CTA's shared memory at exit
   if (p.mode == kGemvArgmax) {
-    // warp max of the keys, one atomicMax per warp, then the last CTA finalises
+    // warp max of the keys, one atomicMax per warp; after a CTA barrier one thread
+    // publishes the CTA's arrival (release) and the last CTA to arrive (acquire)
+    // finalises the tokens and re-arms the keys and the counter
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
-      unsigned long long k = b == 0 ? best0 : best1;
+      unsigned long long k = best[b];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
         const unsigned long long o = __shfl_xor_sync(0xffffffffu, k, off);
@@ -466,25 +567,21 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
       }
       if (lane == 0 && k != 0 && b < p.batch) atomicMax(p.am.key + b, k);
     }
-    __threadfence();
     __syncthreads();
-    __shared__ bool last;
     if (threadIdx.x == 0) {
-      last = atomicAdd(p.am.counter, 1u) == gridDim.x - 1;
-      if (last) {
-        __threadfence();
+      unsigned int old;
+      asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.am.counter) : "memory");
+      if (old == gridDim.x - 1) {
         for (int b = 0; b < p.batch; ++b) {
           const unsigned long long k = atomicExch(p.am.key + b, 0ull);
           p.am.tok_out[b] = (int32_t)argmax_key_index(k);
           p.am.pos[b] += 1;
         }
         *p.am.counter = 0u;
-        __threadfence();
       }
     }
   }
 }
-
 int sm_count() {
   static int n[64] = {};
   int dev = 0;
@@ -498,23 +595,26 @@ int sm_count() {
   return n[dev];
 }
 
-// Resident CTAs per SM for a kernel at a dynamic shared-memory size (cached).
+// Resident CTAs per SM for a kernel at a dynamic shared-memory size (cached per
+// kernel, size and device).
 template <typename K>
 int resident_ctas(K kern, size_t smem) {
-  static size_t keys[32] = {};
-  static int vals[32] = {};
-  static int dev_of[32] = {};
+  struct Entry {
+    const void* fn;
+    size_t smem;
+    int dev, ctas;
+  };
+  static Entry cache[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  for (int i = 0; i < 32; ++i)
-    if (keys[i] == smem + 1 && dev_of[i] == dev) return vals[i];
+  const void* fn = reinterpret_cast<const void*>(kern);
+  for (const Entry& e : cache)
+    if (e.fn == fn && e.smem == smem && e.dev == dev) return e.ctas;
   int o = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kThreads, smem) != cudaSuccess || o < 1) o = 1;
-  for (int i = 0; i < 32; ++i)
-    if (keys[i] == 0) {
-      keys[i] = smem + 1;
-      vals[i] = o;
-      dev_of[i] = dev;
+  for (Entry& e : cache)
+    if (!e.fn) {
+      e = Entry{fn, smem, dev, o};
       break;
     }
   return o;
@@ -523,20 +623,40 @@ int resident_ctas(K kern, size_t smem) {
 template <int FMT, int NB, int RW>
 size_t smem_bytes_t(int64_t cols) {
   const size_t units = (size_t)cols / 32;
-  const bool q4 = FMT == QD_Q4_0 || FMT == QD_Q4_K;
-  (void)q4;
-  return (size_t)kWarps * kStages * slot_bytes<FMT, RW>() + (size_t)NB * units * 9 * 16;
+  return (size_t)kWarps * kStages * slot_bytes<FMT, RW>() + (size_t)NB * units * kRecBytes;
 }
 
-// Largest shared-memory need over the RW choices (for the support check).
+// Rows per group available for NB batch rows (more rows would spill registers).
+template <int NB>
+constexpr int max_rw() {
+  return NB <= 2 ? 4 : 2;
+}
+template <int NB>
+constexpr int min_rw() {
+  return NB == 1 ? 1 : 2;
+}
+
+// Shared-memory need of the smallest-footprint RW for NB batch rows.
 size_t smem_bytes(int fmt, int64_t cols, int nb) {
   switch (fmt) {
-    case QD_Q4_0: return nb == 1 ? smem_bytes_t<QD_Q4_0, 1, 4>(cols) : smem_bytes_t<QD_Q4_0, 2, 2>(cols);
-    case QD_Q8_0: return nb == 1 ? smem_bytes_t<QD_Q8_0, 1, 4>(cols) : smem_bytes_t<QD_Q8_0, 2, 2>(cols);
-    case QD_Q4_K: return nb == 1 ? smem_bytes_t<QD_Q4_K, 1, 4>(cols) : smem_bytes_t<QD_Q4_K, 2, 1>(cols);
-    default: return nb == 1 ? smem_bytes_t<QD_I8_ROW, 1, 4>(cols) : smem_bytes_t<QD_I8_ROW, 2, 2>(cols);
+#define QD_SMEM_CASE(F)                                      \
+  case F:                                                    \
+    switch (nb) {                                            \
+      case 1: return smem_bytes_t<F, 1, min_rw<1>()>(cols);  \
+      case 2: return smem_bytes_t<F, 2, min_rw<2>()>(cols);  \
+      case 4: return smem_bytes_t<F, 4, min_rw<4>()>(cols);  \
+      default: return smem_bytes_t<F, 8, min_rw<8>()>(cols); \
+    }
+    QD_SMEM_CASE(QD_Q4_0)
+    QD_SMEM_CASE(QD_Q8_0)
+    QD_SMEM_CASE(QD_Q4_K)
+    QD_SMEM_CASE(QD_I8_ROW)
+#undef QD_SMEM_CASE
+    default: return ~(size_t)0;
   }
 }
+
+constexpr size_t kSmemCap = 200 * 1024;
 
 template <int FMT, int NB, int RW>
 qd_status launch_rw(const Params& p, bool pdl, cudaStream_t stream, int64_t ctas) {
@@ -546,7 +666,7 @@ qd_status launch_rw(const Params& p, bool pdl, cudaStream_t stream, int64_t ctas
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) != cudaSuccess)
       return QD_ERR_CUDA;
     attr_done[dev] = true;
   }
@@ -564,12 +684,15 @@ qd_status launch_rw(const Params& p, bool pdl, cudaStream_t stream, int64_t ctas
   return QD_OK;
 }
 
-// CTAs for RW rows per group: one wave of resident CTAs at most.
+// CTAs for RW rows per group: one wave of resident CTAs at most (0 when the shared
+// memory does not fit).
 template <int FMT, int NB, int RW>
 int64_t ctas_for(int64_t rows, int64_t cols) {
+  const size_t smem = smem_bytes_t<FMT, NB, RW>(cols);
+  if (smem > kSmemCap) return 0;
   const int64_t groups = (rows + RW - 1) / RW;
   const int64_t want = (groups + kWarps - 1) / kWarps;
-  const int64_t cap = (int64_t)sm_count() * resident_ctas(k_gemv_warp<FMT, NB, RW>, smem_bytes_t<FMT, NB, RW>(cols));
+  const int64_t cap = (int64_t)sm_count() * resident_ctas(k_gemv_warp<FMT, NB, RW>, smem);
   return want < cap ? want : cap;
 }
 
@@ -578,23 +701,22 @@ int64_t ctas_for(int64_t rows, int64_t cols) {
 template <int FMT, int NB>
 qd_status launch_inst(const Params& p, bool pdl, cudaStream_t stream) {
   const int64_t rows = p.W.rows, cols = p.W.cols;
+  constexpr int kMax = max_rw<NB>(), kMin = min_rw<NB>();
+  const bool pairs = p.mode == kGemvSwiGLU || p.mode == kGemvQKV;  // need even rows per group
   double best = -1.0;
-  int brw = 2;
-  int64_t bctas = 1;
-  // batch 2 keeps at most 2 rows per group (4 would spill registers), Q4_K batch 2 one;
-  // the paired epilogues need an even number of rows per group
-  constexpr int kMaxRW = NB == 1 ? 4 : (FMT == QD_Q4_K ? 1 : 2);
-  const bool pairs = p.mode == kGemvSwiGLU || p.mode == kGemvQKV;
+  int brw = 0;
+  int64_t bctas = 0;
   for (int rw : {4, 2, 1}) {
-    if (rw > kMaxRW || (pairs && rw == 1)) continue;
-    int64_t ctas = 1;
-    if constexpr (kMaxRW >= 4) {
+    if (rw > kMax || rw < kMin || (pairs && rw == 1)) continue;
+    int64_t ctas = 0;
+    if constexpr (kMax >= 4) {
       if (rw == 4) ctas = ctas_for<FMT, NB, 4>(rows, cols);
     }
-    if constexpr (kMaxRW >= 2) {
-      if (rw == 2) ctas = ctas_for<FMT, NB, 2>(rows, cols);
+    if (rw == 2) ctas = ctas_for<FMT, NB, 2>(rows, cols);
+    if constexpr (kMin <= 1) {
+      if (rw == 1) ctas = ctas_for<FMT, NB, 1>(rows, cols);
     }
-    if (rw == 1) ctas = ctas_for<FMT, NB, 1>(rows, cols);
+    if (ctas <= 0) continue;
     const int64_t groups = (rows + rw - 1) / rw;
     const int64_t slots = ctas * kWarps;
     const int64_t rounds = (groups + slots - 1) / slots;
@@ -613,20 +735,22 @@ qd_status launch_inst(const Params& p, bool pdl, cudaStream_t stream) {
       bctas = ctas;
     }
   }
-  if constexpr (kMaxRW >= 4) {
+  if constexpr (kMax >= 4) {
     if (brw == 4) return launch_rw<FMT, NB, 4>(p, pdl, stream, bctas);
   }
-  if constexpr (kMaxRW >= 2) {
-    if (brw == 2) return launch_rw<FMT, NB, 2>(p, pdl, stream, bctas);
+  if (brw == 2) return launch_rw<FMT, NB, 2>(p, pdl, stream, bctas);
+  if constexpr (kMin <= 1) {
+    if (brw == 1) return launch_rw<FMT, NB, 1>(p, pdl, stream, bctas);
   }
-  return launch_rw<FMT, NB, 1>(p, pdl, stream, bctas);
+  return QD_ERR_UNSUPPORTED;
 }
 
+int nb_for(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8; }
+
 bool supported(const GemvArgs& a) {
-  if (a.batch > 2 || a.W.cols % 32) return false;
-  if ((a.mode == kGemvSwiGLU || a.mode == kGemvQKV) && a.batch == 2 && a.fmt == QD_Q4_K) return false;
+  if (a.batch < 1 || a.batch > 8 || a.W.cols % 32) return false;
   if (a.W.cols > (1 << 24)) return false;
-  if (smem_bytes(a.fmt, a.W.cols, a.batch <= 1 ? 1 : 2) > 200 * 1024) return false;
+  if (smem_bytes(a.fmt, a.W.cols, nb_for(a.batch)) > kSmemCap) return false;
   // 4-byte scale copies need an even number of blocks per row
   if ((a.fmt == QD_Q4_0 || a.fmt == QD_Q8_0) && ((a.W.cols / 32) & 1)) return false;
   return true;
@@ -652,16 +776,22 @@ qd_status launch_q_gemv_stream(const GemvArgs& a, cudaStream_t stream) {
   p.err = a.err;
   p.qkv = a.qkv;
   p.am = a.am;
-  const bool nb1 = a.batch <= 1;
+  const int nb = nb_for(a.batch);
+#define QD_NB_SWITCH(F)                                      \
+  switch (nb) {                                              \
+    case 1: return launch_inst<F, 1>(p, a.pdl, stream);      \
+    case 2: return launch_inst<F, 2>(p, a.pdl, stream);      \
+    case 4: return launch_inst<F, 4>(p, a.pdl, stream);      \
+    default: return launch_inst<F, 8>(p, a.pdl, stream);     \
+  }
   switch (a.fmt) {
-    case QD_Q4_0: return nb1 ? launch_inst<QD_Q4_0, 1>(p, a.pdl, stream) : launch_inst<QD_Q4_0, 2>(p, a.pdl, stream);
-    case QD_Q8_0: return nb1 ? launch_inst<QD_Q8_0, 1>(p, a.pdl, stream) : launch_inst<QD_Q8_0, 2>(p, a.pdl, stream);
-    case QD_Q4_K: return nb1 ? launch_inst<QD_Q4_K, 1>(p, a.pdl, stream) : launch_inst<QD_Q4_K, 2>(p, a.pdl, stream);
-    case QD_I8_ROW:
-      return nb1 ? launch_inst<QD_I8_ROW, 1>(p, a.pdl, stream) : launch_inst<QD_I8_ROW, 2>(p, a.pdl, stream);
+    case QD_Q4_0: QD_NB_SWITCH(QD_Q4_0)
+    case QD_Q8_0: QD_NB_SWITCH(QD_Q8_0)
+    case QD_Q4_K: QD_NB_SWITCH(QD_Q4_K)
+    case QD_I8_ROW: QD_NB_SWITCH(QD_I8_ROW)
     default: return QD_ERR_UNSUPPORTED;
   }
+#undef QD_NB_SWITCH
 }
 
 }  // namespace qd
-

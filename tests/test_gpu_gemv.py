@@ -168,3 +168,26 @@ def test_q_gemv_is_deterministic(qd):
     a = _gemv(qd, "q4_0", p, rows, cols, x)
     b = _gemv(qd, "q4_0", p, rows, cols, x)
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("batch", [1, 2, 8])
+def test_q_gemv_activation_planes_precision(qd, fmt, batch):
+    """The streaming kernel holds x as 24-bit integers with a power-of-two scale per
+    32-element unit; its error stays near f32 rounding, far inside the 1e-3 bound."""
+    rows, cols = 96, 4096
+    src, p = weights(qd, fmt, 5, "prec", rows, cols)
+    x = qdsynth.activations(5, "xprec", batch, cols)
+    got = _gemv(qd, fmt, p, rows, cols, x)
+    assert_close(got, oracle.gemv(fmt, src, rows, cols, x), tol=2e-5, what=f"{fmt} b{batch}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_q_gemv_non_finite_x_propagates(qd, fmt):
+    rows, cols = 40, 512
+    src, p = weights(qd, fmt, 6, "nf", rows, cols)
+    x = qdsynth.activations(6, "xnf", 2, cols)
+    x[0, 37] = np.inf
+    x[1, 300] = np.nan
+    got = _gemv(qd, fmt, p, rows, cols, x)
+    assert not np.isfinite(got).any()
