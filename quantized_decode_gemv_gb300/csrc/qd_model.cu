@@ -32,7 +32,7 @@ struct Layout {
   std::vector<LayerOff> layer;
   size_t weight_bytes;
   // state
-  size_t kc, vc, x, xn, qkv, q, att, act, logits, attn_ws, attn_cnt, am_key, am_cnt, tok_in, tok_out, pos, err,
+  size_t kc, vc, x, xn, qkv, q, att, act, logits, am_key, am_cnt, tok_in, tok_out, pos, err,
       rope;
   size_t state_bytes;
   int64_t qkv_rows, cache_batch_stride, cache_layer_stride;
@@ -94,8 +94,6 @@ Layout make_layout(const qd_config* c) {
   L.att = take(4 * B * QD);
   L.act = take(4 * B * F);
   L.logits = take(4 * B * (size_t)c->vocab);
-  L.attn_ws = take(attn_workspace_bytes(c->n_heads, c->head_dim, c->max_ctx, (int)B));
-  L.attn_cnt = take(4 * B * (size_t)c->n_kv_heads);
   L.am_key = take(8 * B);
   L.am_cnt = take(4);
   L.tok_in = take(4 * B);
@@ -214,9 +212,8 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
       QD_TRY(launch_qkv_post(qkv, L.qkv_rows, batch, e, err, st, true));
       ++n;
     }
-    QD_TRY(launch_attention_fused(q, QD, kc, vc, L.cache_batch_stride, att, c.n_heads, c.n_kv_heads, c.head_dim,
-                                  pos, c.max_ctx, batch, m->s + L.attn_ws,
-                                  reinterpret_cast<unsigned int*>(m->s + L.attn_cnt), err, st, true));
+    QD_TRY(launch_attention_cluster(q, QD, kc, vc, L.cache_batch_stride, att, c.n_heads, c.n_kv_heads, c.head_dim,
+                                    pos, c.max_ctx, batch, err, st, true));
     ++n;
     QD_TRY(launch_q_gemv(args(c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, x, kGemvAccumulate), st));
     ++n;
@@ -376,7 +373,6 @@ qd_status qd_model_reset(qd_model* m, qd_stream_t stream) {
   QD_TRY(zero_region(m->s + m->L.vc, align_up(cache, 16), st));
   QD_TRY(zero_region(m->s + m->L.pos, 16 * ((4 * m->cfg.max_batch + 15) / 16), st));
   QD_TRY(zero_region(m->s + m->L.err, 16, st));
-  QD_TRY(zero_region(m->s + m->L.attn_cnt, align_up(4 * (size_t)m->cfg.max_batch * m->cfg.n_kv_heads, 16), st));
   QD_TRY(zero_region(m->s + m->L.am_key, align_up(8 * (size_t)m->cfg.max_batch, 16), st));
   QD_TRY(zero_region(m->s + m->L.am_cnt, 16, st));
   return QD_OK;

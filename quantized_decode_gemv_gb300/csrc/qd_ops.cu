@@ -1,5 +1,7 @@
 // The decode step's operations other than the GEMV: RMSNorm, RoPE, KV-cache
 // append, split-KV grouped-query decode attention, SwiGLU, argmax, embedding.
+#include <cooperative_groups.h>
+
 #include <cmath>
 #include <mutex>
 
@@ -226,27 +228,32 @@ __global__ void k_attn_merge(const float* __restrict__ ws_ml, const float* __res
   dst[d] = acc / lt;
 }
 
-// Single-kernel form for the decode step: each CTA computes its chunk as in
-// k_attn_partial, then the last CTA of its (sequence, kv head) to finish merges the
-// chunks of that kv head's q heads (the same log-sum-exp merge, in split order).  The
-// arrival counter lives in the model state, starts at zero and is reset by that CTA.
+// Single-kernel form for the decode step: one thread-block cluster of S CTAs per
+// (sequence, kv head).  The positions 0..pos are cut into S equal chunks at run time
+// (pos is read on the device), each CTA walks its chunk as in k_attn_partial and
+// merges its warps in shared memory; after a cluster barrier, warp w of CTA r merges
+// q head g = r + S w from the S CTAs' partials read through distributed shared memory
+// (the same log-sum-exp merge, in chunk order).  No global workspace, atomics or
+// fences; the second barrier keeps every CTA's shared memory alive until the reads end.
 template <int G>
-__global__ void __launch_bounds__(kAttnWarps * 32) k_attn_fused(
+__global__ void __launch_bounds__(kAttnWarps * 32) k_attn_cluster(
     const float* __restrict__ q, int64_t q_stride, const float* __restrict__ kc, const float* __restrict__ vc,
-    int64_t cache_batch_stride, int n_heads, int n_kv, const int32_t* __restrict__ pos, int max_ctx, float scale,
-    float* __restrict__ ws_ml, float* __restrict__ ws_o, unsigned int* __restrict__ counters, float* __restrict__ out,
-    uint32_t* err) {
+    int64_t cache_batch_stride, int n_heads, const int32_t* __restrict__ pos, int max_ctx, float scale,
+    float* __restrict__ out, uint32_t* err) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int S = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();     // q and the cache rows come from the QKV projection
   pdl_trigger();  // let the next kernel start its weight prefetch
-  const int kvh = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
-  const int splits = gridDim.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p_cur = pos[b];
   const bool valid = p_cur >= 0 && p_cur < max_ctx;
-  if (!valid && err && threadIdx.x == 0 && split == 0 && kvh == 0) atomicOr(err, kErrPosition);
-  const int chunk = attn_chunk(max_ctx);
-  const int p_begin = split * chunk;
-  const int p_end = valid ? min(p_begin + chunk, p_cur + 1) : p_begin;
+  if (!valid && err && threadIdx.x == 0 && rank == 0 && kvh == 0) atomicOr(err, kErrPosition);
+  const int n = valid ? p_cur + 1 : 0;
+  const int chunk = (n + S - 1) / S;
+  const int p_begin = min(rank * chunk, n), p_end = min(p_begin + chunk, n);
 
   float2 qv[G];
 #pragma unroll
@@ -266,9 +273,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_fused(
   const float* kb = kc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
   const float* vb = vc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
   attn_walk<G>(kb, vb, p_begin, p_end, warp, lane, qv, m, l, o);
+
   __shared__ float sm[kAttnWarps][kMaxGroup], sl[kAttnWarps][kMaxGroup];
   __shared__ float2 so[kAttnWarps][kMaxGroup][32];
-  __shared__ bool last;
+  __shared__ float cm[kMaxGroup], cl[kMaxGroup];  // this CTA's partial per q head
+  __shared__ float2 co[kMaxGroup][32];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     if (lane == 0) {
@@ -291,44 +300,31 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_fused(
       ot.x = fmaf(so[w2][g][lane].x, f, ot.x);
       ot.y = fmaf(so[w2][g][lane].y, f, ot.y);
     }
-    const int h = kvh * G + g;
-    const int64_t slot = ((int64_t)b * n_heads + h) * splits + split;
     if (lane == 0) {
-      ws_ml[slot * 2] = mx;
-      ws_ml[slot * 2 + 1] = lt;
+      cm[g] = mx;
+      cl[g] = lt;
     }
-    reinterpret_cast<float2*>(ws_o + slot * kHeadDim)[lane] = ot;
+    co[g][lane] = ot;
   }
-  __threadfence();
-  __syncthreads();
-  unsigned int* cnt = counters + (int64_t)b * n_kv + kvh;
-  if (threadIdx.x == 0) last = atomicAdd(cnt, 1u) == (unsigned)splits - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  const int used = valid ? p_cur / chunk + 1 : 0;
-  for (int g = warp; g < G; g += kAttnWarps) {
+  cluster.sync();
+  for (int g = rank + S * warp; g < G; g += S * kAttnWarps) {
     const int h = kvh * G + g;
     float2* dst = reinterpret_cast<float2*>(out + ((int64_t)b * n_heads + h) * kHeadDim);
-    if (!valid) {
-      dst[lane] = make_float2(0.f, 0.f);
-      continue;
-    }
-    const int64_t base = ((int64_t)b * n_heads + h) * splits;
     float mx = -INFINITY;
-    for (int s2 = 0; s2 < used; ++s2) mx = fmaxf(mx, __ldcg(ws_ml + (base + s2) * 2));
+    for (int r = 0; r < S; ++r) mx = fmaxf(mx, *cluster.map_shared_rank(&cm[g], r));
     float lt = 0.f;
     float2 acc = make_float2(0.f, 0.f);
-    for (int s2 = 0; s2 < used; ++s2) {
-      const float f = expf(__ldcg(ws_ml + (base + s2) * 2) - mx);
-      lt = fmaf(__ldcg(ws_ml + (base + s2) * 2 + 1), f, lt);
-      const float2 ov = __ldcg(reinterpret_cast<const float2*>(ws_o + (base + s2) * kHeadDim) + lane);
+    for (int r = 0; r < S; ++r) {
+      const float mr = *cluster.map_shared_rank(&cm[g], r);
+      const float f = mr == -INFINITY ? 0.f : expf(mr - mx);
+      lt = fmaf(*cluster.map_shared_rank(&cl[g], r), f, lt);
+      const float2 ov = *cluster.map_shared_rank(&co[g][lane], r);
       acc.x = fmaf(ov.x, f, acc.x);
       acc.y = fmaf(ov.y, f, acc.y);
     }
-    dst[lane] = make_float2(acc.x / lt, acc.y / lt);
+    dst[lane] = lt > 0.f ? make_float2(acc.x / lt, acc.y / lt) : make_float2(0.f, 0.f);
   }
-  if (threadIdx.x == 0) *cnt = 0u;
+  cluster.sync();
 }
 
 // ------------------------------------------------------------------ QKV post-processing
@@ -509,33 +505,65 @@ qd_status launch_attention(const float* q, int64_t q_stride, const float* kc, co
   return launch_status();
 }
 
-qd_status launch_attention_fused(const float* q, int64_t q_stride, const float* kc, const float* vc,
-                                 int64_t cache_batch_stride, float* out, int n_heads, int n_kv, int head_dim,
-                                 const int32_t* pos, int max_ctx, int batch, void* ws, unsigned int* counters,
-                                 uint32_t* err, cudaStream_t stream, bool pdl) {
-  const int splits = attn_splits(max_ctx);
+// CTAs per cluster for the decode-step attention: enough clusters x CTAs to cover the
+// SMs a few times over, at most 8 (the portable cluster size) and at most one CTA per
+// 32 positions of the cache.
+int attn_cluster_size(int n_kv, int batch, int max_ctx) {
+  static int sms[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int nsm = 152;
+  if (dev >= 0 && dev < 64) {
+    if (!sms[dev] && (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                      sms[dev] <= 0))
+      sms[dev] = 152;
+    nsm = sms[dev];
+  }
+  const int pairs = n_kv * batch;
+  const int target = 4 * nsm;
+  int s = 1;
+  while (s < 8 && s * pairs < target && s * 32 < max_ctx) s *= 2;
+  return s;
+}
+
+qd_status launch_attention_cluster(const float* q, int64_t q_stride, const float* kc, const float* vc,
+                                   int64_t cache_batch_stride, float* out, int n_heads, int n_kv, int head_dim,
+                                   const int32_t* pos, int max_ctx, int batch, uint32_t* err, cudaStream_t stream,
+                                   bool pdl) {
   const int G = n_heads / n_kv;
-  const size_t slots = (size_t)batch * n_heads * splits;
-  float* ws_ml = static_cast<float*>(ws);
-  float* ws_o = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(slots * 2 * sizeof(float), 256));
+  const int S = attn_cluster_size(n_kv, batch, max_ctx);
   const float scale = 1.0f / sqrtf((float)head_dim);
-  const dim3 grid((unsigned)n_kv, (unsigned)splits, (unsigned)batch), block(kAttnWarps * 32);
-#define QD_ATTN_FUSED(GG)                                                                                      \
-  case GG:                                                                                                     \
-    return launch_k(k_attn_fused<GG>, grid, block, 0, stream, pdl, q, q_stride, kc, vc, cache_batch_stride,   \
-                    n_heads, n_kv, pos, max_ctx, scale, ws_ml, ws_o, counters, out, err);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)S, (unsigned)n_kv, (unsigned)batch);
+  cfg.blockDim = dim3(kAttnWarps * 32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+#define QD_ATTN_CLUSTER(GG)                                                                                  \
+  case GG:                                                                                                   \
+    return cudaLaunchKernelEx(&cfg, k_attn_cluster<GG>, q, q_stride, kc, vc, cache_batch_stride, n_heads, pos, \
+                              max_ctx, scale, out, err) == cudaSuccess                                       \
+               ? QD_OK                                                                                       \
+               : QD_ERR_CUDA;
   switch (G) {
-    QD_ATTN_FUSED(1)
-    QD_ATTN_FUSED(2)
-    QD_ATTN_FUSED(3)
-    QD_ATTN_FUSED(4)
-    QD_ATTN_FUSED(5)
-    QD_ATTN_FUSED(6)
-    QD_ATTN_FUSED(7)
-    QD_ATTN_FUSED(8)
+    QD_ATTN_CLUSTER(1)
+    QD_ATTN_CLUSTER(2)
+    QD_ATTN_CLUSTER(3)
+    QD_ATTN_CLUSTER(4)
+    QD_ATTN_CLUSTER(5)
+    QD_ATTN_CLUSTER(6)
+    QD_ATTN_CLUSTER(7)
+    QD_ATTN_CLUSTER(8)
     default: return QD_ERR_UNSUPPORTED;
   }
-#undef QD_ATTN_FUSED
+#undef QD_ATTN_CLUSTER
 }
 
 qd_status launch_qkv_post(const float* qkv, int64_t qkv_stride, int batch, const QkvEpilogue& e, uint32_t* err,
