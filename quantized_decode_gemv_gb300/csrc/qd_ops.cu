@@ -104,36 +104,111 @@ __host__ __device__ inline int attn_splits(int max_ctx) {
   return (max_ctx + c - 1) / c;
 }
 
-// Online-softmax walk of positions [p_begin, p_end) by one warp of the CTA: the warp
-// takes batches of kPosBatch consecutive positions (warp-interleaved) and issues the
-// loads of a whole batch before using any of them.
-constexpr int kPosBatch = 8;
+// Walk of positions [p_begin, p_end) by the CTA's warps in tiles: warp w takes
+// positions tile + w * P + i (i < P) of each tile of kAttnWarps * P positions.
+//  * scores: L lanes share one position, lane j holding dims [j * 64/L, (j+1) * 64/L)
+//    of its key row and of every q head; the dot is finished with log2(L) shuffles.
+//    Scores are in log2 units (q was pre-scaled by log2(e) / sqrt(head_dim)).
+//  * softmax: one running max / sum update per tile and head (online softmax over
+//    tiles), weights 2^(s - m).
+//  * values: lane j holds dims 2j, 2j+1 of the P value rows; each position's weight
+//    is broadcast from its lane group.
+// The next tile's rows are loaded before the current tile is used.
 template <int G>
-__device__ __forceinline__ void attn_walk(const float* kb, const float* vb, int p_begin, int p_end, int warp,
-                                          int lane, const float2 (&qv)[G], float (&m)[G], float (&l)[G],
-                                          float2 (&o)[G]) {
-  for (int p0 = p_begin + warp * kPosBatch; p0 < p_end; p0 += kAttnWarps * kPosBatch) {
-    float2 kk[kPosBatch], vv[kPosBatch];
+struct AttnLayout {
+  static constexpr int L = G <= 4 ? 4 : 8;  // lanes per key row
+  static constexpr int P = 32 / L;          // positions per warp per tile
+  static constexpr int D = kHeadDim / L;    // key dims per lane
+};
+
+template <int G>
+__device__ __forceinline__ void attn_tiles(const float* kb, const float* vb, int p_begin, int p_end, int warp,
+                                           int lane, const float (&qs)[G][AttnLayout<G>::D], float (&m)[G],
+                                           float (&l)[G], float2 (&o)[G]) {
+  using A = AttnLayout<G>;
+  constexpr int L = A::L, P = A::P, D = A::D;
+  constexpr int kTile = kAttnWarps * P;
+  const int j = lane % L, pi = lane / L;  // this lane's dim slice and position in the warp tile
+  float4 kr[D / 4], kn[D / 4];
+  float2 vr[P], vn[P];
+  auto load = [&](int tile, float4 (&kd)[D / 4], float2 (&vd)[P]) {
+    const int p = min(tile + warp * P + pi, p_end - 1);
+    const float4* krow = reinterpret_cast<const float4*>(kb + (int64_t)p * kHeadDim + j * D);
 #pragma unroll
-    for (int i = 0; i < kPosBatch; ++i) {
-      const int p = min(p0 + i, p_end - 1);
-      kk[i] = __ldcg(reinterpret_cast<const float2*>(kb + (int64_t)p * kHeadDim) + lane);
-      vv[i] = __ldcg(reinterpret_cast<const float2*>(vb + (int64_t)p * kHeadDim) + lane);
+    for (int t = 0; t < D / 4; ++t) kd[t] = __ldcg(krow + t);
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+      const int pv = min(tile + warp * P + i, p_end - 1);
+      vd[i] = __ldcg(reinterpret_cast<const float2*>(vb + (int64_t)pv * kHeadDim) + lane);
     }
+  };
+  if (p_begin >= p_end) return;
+  load(p_begin, kr, vr);
+  for (int tile = p_begin; tile < p_end; tile += kTile) {
+    const bool more = tile + kTile < p_end;
+    if (more) load(tile + kTile, kn, vn);
+    const bool live = tile + warp * P + pi < p_end;  // this lane's position exists
+    const int nvalid = min(P, max(0, p_end - tile - warp * P));  // positions of this warp's tile
 #pragma unroll
-    for (int i = 0; i < kPosBatch; ++i) {
-      if (p0 + i >= p_end) break;
+    for (int g = 0; g < G; ++g) {
+      float sc = 0.f;
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float sc = warp_sum(fmaf(qv[g].x, kk[i].x, qv[g].y * kk[i].y));
-        const float mn = fmaxf(m[g], sc);
-        const float corr = expf(m[g] - mn);  // 0 when m was -inf
-        const float w = expf(sc - mn);
-        l[g] = fmaf(l[g], corr, w);
-        o[g].x = fmaf(o[g].x, corr, w * vv[i].x);
-        o[g].y = fmaf(o[g].y, corr, w * vv[i].y);
-        m[g] = mn;
+      for (int t = 0; t < D / 4; ++t) {
+        sc = fmaf(qs[g][4 * t], kr[t].x, sc);
+        sc = fmaf(qs[g][4 * t + 1], kr[t].y, sc);
+        sc = fmaf(qs[g][4 * t + 2], kr[t].z, sc);
+        sc = fmaf(qs[g][4 * t + 3], kr[t].w, sc);
       }
+#pragma unroll
+      for (int off = 1; off < L; off <<= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
+      sc = live ? sc : -INFINITY;
+      float tm = sc;
+#pragma unroll
+      for (int off = L; off < 32; off <<= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, off));
+      const float mn = fmaxf(m[g], tm);
+      const float corr = m[g] == mn ? 1.f : exp2f(m[g] - mn);
+      const float w = sc == -INFINITY ? 0.f : exp2f(sc - mn);
+      float ws = w;
+#pragma unroll
+      for (int off = L; off < 32; off <<= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
+      l[g] = fmaf(l[g], corr, ws);  // offsets >= L: one lane per position took part
+      float2 acc = make_float2(o[g].x * corr, o[g].y * corr);
+#pragma unroll
+      for (int i = 0; i < P; ++i) {
+        const float wi = __shfl_sync(0xffffffffu, w, i * L);
+        if (i < nvalid) {
+          acc.x = fmaf(wi, vr[i].x, acc.x);
+          acc.y = fmaf(wi, vr[i].y, acc.y);
+        }
+      }
+      o[g] = acc;
+      m[g] = mn;
+    }
+    if (more) {
+#pragma unroll
+      for (int t = 0; t < D / 4; ++t) kr[t] = kn[t];
+#pragma unroll
+      for (int i = 0; i < P; ++i) vr[i] = vn[i];
+    }
+  }
+}
+
+// q head g of kv head kvh, pre-scaled, as this lane's key-dim slice.
+template <int G>
+__device__ __forceinline__ void attn_load_q(const float* qb, int kvh, int lane, float scale,
+                                            float (&qs)[G][AttnLayout<G>::D]) {
+  using A = AttnLayout<G>;
+  const int j = lane % A::L;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float4* src = reinterpret_cast<const float4*>(qb + (int64_t)(kvh * G + g) * kHeadDim + j * A::D);
+#pragma unroll
+    for (int t = 0; t < A::D / 4; ++t) {
+      const float4 v = __ldcg(src + t);
+      qs[g][4 * t] = v.x * scale;
+      qs[g][4 * t + 1] = v.y * scale;
+      qs[g][4 * t + 2] = v.z * scale;
+      qs[g][4 * t + 3] = v.w * scale;
     }
   }
 }
@@ -153,13 +228,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_partial(
   const int p_begin = split * chunk;
   const int p_end = valid ? min(p_begin + chunk, p_cur + 1) : p_begin;  // exclusive
 
-  float2 qv[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const int h = kvh * G + g;
-    const float2 t = __ldcg(reinterpret_cast<const float2*>(q + (int64_t)b * q_stride + (int64_t)h * kHeadDim) + lane);
-    qv[g] = make_float2(t.x * scale, t.y * scale);
-  }
+  float qs[G][AttnLayout<G>::D];
+  attn_load_q<G>(q + (int64_t)b * q_stride, kvh, lane, scale, qs);
   float m[G], l[G];
   float2 o[G];
 #pragma unroll
@@ -170,7 +240,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_partial(
   }
   const float* kb = kc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
   const float* vb = vc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
-  attn_walk<G>(kb, vb, p_begin, p_end, warp, lane, qv, m, l, o);
+  attn_tiles<G>(kb, vb, p_begin, p_end, warp, lane, qs, m, l, o);
   // merge the warps of this CTA
   __shared__ float sm[kAttnWarps][kMaxGroup], sl[kAttnWarps][kMaxGroup];
   __shared__ float2 so[kAttnWarps][kMaxGroup][32];
@@ -191,7 +261,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_partial(
     float2 ot = make_float2(0.f, 0.f);
 #pragma unroll
     for (int w2 = 0; w2 < kAttnWarps; ++w2) {
-      const float f = (sm[w2][g] == -INFINITY) ? 0.f : expf(sm[w2][g] - mx);
+      const float f = (sm[w2][g] == -INFINITY) ? 0.f : exp2f(sm[w2][g] - mx);
       lt = fmaf(sl[w2][g], f, lt);
       ot.x = fmaf(so[w2][g][lane].x, f, ot.x);
       ot.y = fmaf(so[w2][g][lane].y, f, ot.y);
@@ -221,7 +291,7 @@ __global__ void k_attn_merge(const float* __restrict__ ws_ml, const float* __res
   for (int s = 0; s < used; ++s) mx = fmaxf(mx, ws_ml[(base + s) * 2]);
   float lt = 0.f, acc = 0.f;
   for (int s = 0; s < used; ++s) {
-    const float f = expf(ws_ml[(base + s) * 2] - mx);
+    const float f = exp2f(ws_ml[(base + s) * 2] - mx);
     lt = fmaf(ws_ml[(base + s) * 2 + 1], f, lt);
     acc = fmaf(ws_o[(base + s) * kHeadDim + d], f, acc);
   }
@@ -230,11 +300,12 @@ __global__ void k_attn_merge(const float* __restrict__ ws_ml, const float* __res
 
 // Single-kernel form for the decode step: one thread-block cluster of S CTAs per
 // (sequence, kv head).  The positions 0..pos are cut into S equal chunks at run time
-// (pos is read on the device), each CTA walks its chunk as in k_attn_partial and
-// merges its warps in shared memory; after a cluster barrier, warp w of CTA r merges
-// q head g = r + S w from the S CTAs' partials read through distributed shared memory
-// (the same log-sum-exp merge, in chunk order).  No global workspace, atomics or
-// fences; the second barrier keeps every CTA's shared memory alive until the reads end.
+// (pos is read on the device), each CTA walks its chunk as in k_attn_partial, merges
+// its warps, and stores its partial (m, l, o) per q head into the shared memory of the
+// cluster's first CTA (distributed shared memory, no global workspace, atomics or
+// fences).  After one cluster barrier that CTA merges the S partials (the same
+// log-sum-exp merge, in chunk order) and writes the output.
+constexpr int kMaxCluster = 8;
 template <int G>
 __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_cluster(
     const float* __restrict__ q, int64_t q_stride, const float* __restrict__ kc, const float* __restrict__ vc,
@@ -246,6 +317,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_cluster(
   const int rank = (int)cluster.block_rank();
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float sm[kAttnWarps][kMaxGroup], sl[kAttnWarps][kMaxGroup];
+  __shared__ float2 so[kAttnWarps][kMaxGroup][32];
+  // filled in the first CTA of the cluster by every CTA: partial of CTA r for head g
+  __shared__ float pm[kMaxCluster][kMaxGroup], pl[kMaxCluster][kMaxGroup];
+  __shared__ float2 po[kMaxCluster][kMaxGroup][32];
   pdl_wait();     // q and the cache rows come from the QKV projection
   pdl_trigger();  // let the next kernel start its weight prefetch
   const int p_cur = pos[b];
@@ -255,13 +331,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_cluster(
   const int chunk = (n + S - 1) / S;
   const int p_begin = min(rank * chunk, n), p_end = min(p_begin + chunk, n);
 
-  float2 qv[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const int h = kvh * G + g;
-    const float2 t = __ldcg(reinterpret_cast<const float2*>(q + (int64_t)b * q_stride + (int64_t)h * kHeadDim) + lane);
-    qv[g] = make_float2(t.x * scale, t.y * scale);
-  }
+  float qs[G][AttnLayout<G>::D];
+  attn_load_q<G>(q + (int64_t)b * q_stride, kvh, lane, scale, qs);
   float m[G], l[G];
   float2 o[G];
 #pragma unroll
@@ -272,12 +343,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_cluster(
   }
   const float* kb = kc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
   const float* vb = vc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
-  attn_walk<G>(kb, vb, p_begin, p_end, warp, lane, qv, m, l, o);
+  attn_tiles<G>(kb, vb, p_begin, p_end, warp, lane, qs, m, l, o);
 
-  __shared__ float sm[kAttnWarps][kMaxGroup], sl[kAttnWarps][kMaxGroup];
-  __shared__ float2 so[kAttnWarps][kMaxGroup][32];
-  __shared__ float cm[kMaxGroup], cl[kMaxGroup];  // this CTA's partial per q head
-  __shared__ float2 co[kMaxGroup][32];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     if (lane == 0) {
@@ -287,6 +354,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_cluster(
     so[warp][g][lane] = o[g];
   }
   __syncthreads();
+  float* rpm = cluster.map_shared_rank(&pm[0][0], 0);
+  float* rpl = cluster.map_shared_rank(&pl[0][0], 0);
+  float2* rpo = cluster.map_shared_rank(&po[0][0][0], 0);
   for (int g = warp; g < G; g += kAttnWarps) {
     float mx = -INFINITY;
 #pragma unroll
@@ -295,36 +365,42 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_cluster(
     float2 ot = make_float2(0.f, 0.f);
 #pragma unroll
     for (int w2 = 0; w2 < kAttnWarps; ++w2) {
-      const float f = (sm[w2][g] == -INFINITY) ? 0.f : expf(sm[w2][g] - mx);
+      const float f = (sm[w2][g] == -INFINITY) ? 0.f : exp2f(sm[w2][g] - mx);
       lt = fmaf(sl[w2][g], f, lt);
       ot.x = fmaf(so[w2][g][lane].x, f, ot.x);
       ot.y = fmaf(so[w2][g][lane].y, f, ot.y);
     }
     if (lane == 0) {
-      cm[g] = mx;
-      cl[g] = lt;
+      rpm[rank * kMaxGroup + g] = mx;
+      rpl[rank * kMaxGroup + g] = lt;
     }
-    co[g][lane] = ot;
+    rpo[(rank * kMaxGroup + g) * 32 + lane] = ot;
   }
-  cluster.sync();
-  for (int g = rank + S * warp; g < G; g += S * kAttnWarps) {
+  cluster.sync();  // the partials have landed in the first CTA
+  if (rank != 0) return;
+  for (int g = warp; g < G; g += kAttnWarps) {
     const int h = kvh * G + g;
     float2* dst = reinterpret_cast<float2*>(out + ((int64_t)b * n_heads + h) * kHeadDim);
+    float mr[kMaxCluster];
     float mx = -INFINITY;
-    for (int r = 0; r < S; ++r) mx = fmaxf(mx, *cluster.map_shared_rank(&cm[g], r));
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) {
+      mr[r] = r < S ? pm[r][g] : -INFINITY;
+      mx = fmaxf(mx, mr[r]);
+    }
     float lt = 0.f;
     float2 acc = make_float2(0.f, 0.f);
-    for (int r = 0; r < S; ++r) {
-      const float mr = *cluster.map_shared_rank(&cm[g], r);
-      const float f = mr == -INFINITY ? 0.f : expf(mr - mx);
-      lt = fmaf(*cluster.map_shared_rank(&cl[g], r), f, lt);
-      const float2 ov = *cluster.map_shared_rank(&co[g][lane], r);
-      acc.x = fmaf(ov.x, f, acc.x);
-      acc.y = fmaf(ov.y, f, acc.y);
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) {
+      if (r < S) {
+        const float f = mr[r] == -INFINITY ? 0.f : exp2f(mr[r] - mx);
+        lt = fmaf(pl[r][g], f, lt);
+        acc.x = fmaf(po[r][g][lane].x, f, acc.x);
+        acc.y = fmaf(po[r][g][lane].y, f, acc.y);
+      }
     }
     dst[lane] = lt > 0.f ? make_float2(acc.x / lt, acc.y / lt) : make_float2(0.f, 0.f);
   }
-  cluster.sync();
 }
 
 // ------------------------------------------------------------------ QKV post-processing
@@ -478,7 +554,7 @@ qd_status launch_attention(const float* q, int64_t q_stride, const float* kc, co
   const size_t slots = (size_t)batch * n_heads * splits;
   float* ws_ml = static_cast<float*>(ws);
   float* ws_o = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(slots * 2 * sizeof(float), 256));
-  const float scale = 1.0f / sqrtf((float)head_dim);
+  const float scale = 1.4426950408889634f / sqrtf((float)head_dim);  // scores in log2 units
   dim3 grid((unsigned)n_kv, (unsigned)splits, (unsigned)batch);
   const int threads = kAttnWarps * 32;
 #define QD_ATTN_CASE(GG)                                                                                      \
@@ -522,7 +598,7 @@ int attn_cluster_size(int n_kv, int batch, int max_ctx) {
   const int pairs = n_kv * batch;
   const int target = 4 * nsm;
   int s = 1;
-  while (s < 8 && s * pairs < target && s * 32 < max_ctx) s *= 2;
+  while (s < kMaxCluster && s * pairs < target && s * 32 < max_ctx) s *= 2;
   return s;
 }
 
@@ -532,7 +608,7 @@ qd_status launch_attention_cluster(const float* q, int64_t q_stride, const float
                                    bool pdl) {
   const int G = n_heads / n_kv;
   const int S = attn_cluster_size(n_kv, batch, max_ctx);
-  const float scale = 1.0f / sqrtf((float)head_dim);
+  const float scale = 1.4426950408889634f / sqrtf((float)head_dim);  // scores in log2 units
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)S, (unsigned)n_kv, (unsigned)batch);
   cfg.blockDim = dim3(kAttnWarps * 32);
