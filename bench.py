@@ -160,11 +160,13 @@ def build_smol135m(qd, torch, seed):
     return cfg, model
 
 
-def time_gemv_cold(qd, torch, fmt, rows, cols, batch, stream, reps=None, seed=0):
-    """Average device time of one qd_q_gemv launch.  The launches run back to back from a
+def time_gemv_cold(qd, torch, fmt, rows, cols, batch, stream, reps=None, seed=0, overlap=False):
+    """Average device time of one q_gemv launch.  The launches run back to back from a
     CUDA graph (so host launch overhead is not measured), each on a distinct weight copy so
     the weights come from HBM: the copies total >= 2x L2, and L2 is flushed before each
-    replay.  Returns (seconds, launches per replay)."""
+    replay.  overlap=True launches with QD_GEMV_OVERLAP, the decode step's launch mode (the
+    next launch streams its weights while the previous one finishes).  Returns (seconds,
+    launches per replay)."""
     import qdsynth
 
     src = qdsynth.weight_src(fmt, seed, f"bench.{fmt}.{rows}x{cols}", rows, cols)
@@ -176,13 +178,14 @@ def time_gemv_cold(qd, torch, fmt, rows, cols, batch, stream, reps=None, seed=0)
     x = torch.from_numpy(qdsynth.activations(seed, "bench.x", batch, cols)).cuda()
     y = torch.empty(batch, rows, device="cuda")
     ptrs = [copies[i].data_ptr() for i in range(n)]
+    flags = qd.GEMV_OVERLAP if overlap else 0
     for p in ptrs[:3]:
-        qd.q_gemv(fmt, p, rows, cols, x, y, batch, stream=stream)
+        qd.q_gemv_ex(fmt, p, rows, cols, x, y, batch, flags, stream=stream)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         for p in ptrs:
-            qd.q_gemv(fmt, p, rows, cols, x, y, batch)
+            qd.q_gemv_ex(fmt, p, rows, cols, x, y, batch, flags)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     best = None
     for _ in range(4):
@@ -318,45 +321,52 @@ def run_ours(args, world, rank, local):
         dist.destroy_process_group()
 
 
-def profile_traffic(kernel_tag: str):
-    """Per-launch DRAM bytes from the committed ncu summary, or None when the kernel source
-    changed since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+def profile_traffic(summary: str):
+    """Per-launch DRAM bytes from a committed ncu summary under profiles/, or None when the
+    GEMV kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     h = re.search(r"source_sha256:\s*([0-9a-f]{16,64})", text)
-    src = os.path.join(ROOT, "quantized_decode_gemv_gb300", "csrc", "qd_gemv.cu")
+    src = os.path.join(ROOT, "quantized_decode_gemv_gb300", "csrc", "qd_gemv_stream.cu")
     cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
     if not m or not h or not cur.startswith(h.group(1)):
         return None
     return float(m.group(1))
 
 
+DECODE_SHAPES = [(960, 576), (576, 576), (3072, 576), (576, 1536)]  # QKV, Wo, gate/up, down
+
+
 def roofline_dominant(qd, torch, stream, hbm, peak_kind):
-    """The step's dominant kernel is the Q4_0 GEMV (120 launches per token over the four
-    per-layer shapes).  Its achieved bandwidth: algorithmic bytes of the four shapes over the
-    sum of their average launch durations (cold weights)."""
-    shapes = [(960, 576), (576, 576), (3072, 576), (576, 1536)]
+    """The step's dominant kernel is the Q4_0 streaming GEMV, k_gemv_warp (120 of the 152
+    launches per token, over the four per-layer shapes).  Achieved bandwidth: algorithmic
+    bytes of the four shapes over the sum of their average launch durations, each shape
+    timed as back-to-back launches on cold weights in the decode step's launch mode
+    (QD_GEMV_OVERLAP)."""
     tot_b, tot_t = 0, 0.0
     per = {}
-    for r, c in shapes:
-        t, n = time_gemv_cold(qd, torch, "q4_0", r, c, 1, stream)
+    for r, c in DECODE_SHAPES:
+        t, n = time_gemv_cold(qd, torch, "q4_0", r, c, 1, stream, overlap=True)
         b = algorithmic_bytes("q4_0", r, c, 1, qd)
         tot_b += b
         tot_t += t
         per[f"{r}x{c}"] = {"us": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1)}
     achieved = tot_b / tot_t / 1e9
-    traffic = profile_traffic("q_gemv_q4_0_decode_shapes")
-    return {"kernel": "k_gemv_blocks<Q4_0> (decode-step shapes 960x576, 576x576, 3072x576, 576x1536)",
+    traffic = profile_traffic("q_gemv_q4_0_decode_shapes.md")
+    return {"kernel": "k_gemv_warp<Q4_0> (decode-step shapes 960x576, 576x576, 3072x576, 576x1536)",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
-            "traffic": traffic, "algorithmic_bytes_per_launch": round(tot_b / len(shapes)),
+            "traffic": traffic, "algorithmic_bytes_per_launch": round(tot_b / len(DECODE_SHAPES)),
             "per_shape": per}
 
 
 def gemv_sweep(qd, torch, stream, hbm, args):
+    """q_gemv at the sweep shapes: 'chained' = back-to-back launches in the decode step's
+    launch mode (QD_GEMV_OVERLAP), 'isolated' = plain launches (each waits for the previous
+    one to finish).  Cold weights throughout."""
     res = {}
     shapes = [("q4_0", 576, 1536)]
     for fmt in ("q8_0", "q4_0"):
@@ -364,13 +374,19 @@ def gemv_sweep(qd, torch, stream, hbm, args):
             shapes.append((fmt, r, c))
     for r, c in [(2048, 2048), (5632, 2048), (2048, 5632), (32000, 2048)]:
         shapes.append(("q4_k", r, c))
+    for r, c in [(6144, 2048), (2048, 2048), (16384, 2048), (2048, 8192), (49152, 2048)]:
+        shapes.append(("i8", r, c))
     batches = (1, 2, 4, 8) if args.full_sweep else (1,)
     for fmt, r, c in shapes:
-        for b in (batches if fmt != "q4_k" and (r, c) != (576, 1536) else (1,)):
-            t, n = time_gemv_cold(qd, torch, fmt, r, c, b, stream)
+        bs = (1, 16) if fmt == "i8" else (batches if fmt != "q4_k" and (r, c) != (576, 1536) else (1,))
+        for b in bs:
             by = algorithmic_bytes(fmt, r, c, b, qd)
-            res[f"{fmt} {r}x{c} b{b}"] = {"us": round(t * 1e6, 2), "GB/s": round(by / t / 1e9, 1),
-                                          "frac": round(by / t / 1e9 / hbm, 3)}
+            row = {}
+            for mode, ov in (("chained", True), ("isolated", False)):
+                t, n = time_gemv_cold(qd, torch, fmt, r, c, b, stream, overlap=ov)
+                row[mode] = {"us": round(t * 1e6, 2), "GB/s": round(by / t / 1e9, 1),
+                             "frac": round(by / t / 1e9 / hbm, 3)}
+            res[f"{fmt} {r}x{c} b{b}"] = row
     return res
 
 
@@ -506,16 +522,18 @@ def run_gemv_only(spec: str, reps: int):
         qd.build()
     qd.load()
     stream = torch.cuda.current_stream()
-    ts = []
-    for _ in range(reps):
-        t, n = time_gemv_cold(qd, torch, fmt, r, c, b, stream)
-        ts.append(t)
     by = algorithmic_bytes(fmt, r, c, b, qd)
     hbm, _, kind = peaks()
-    t = min(ts)
-    print(json.dumps({"gemv": spec, "us": round(t * 1e6, 3), "GB/s": round(by / t / 1e9, 1),
-                      "frac": round(by / t / 1e9 / hbm, 4), "peak": hbm, "peak_kind": kind,
-                      "algorithmic_bytes": by, "launches_per_pass": n}))
+    out = {"gemv": spec, "peak": hbm, "peak_kind": kind, "algorithmic_bytes": by}
+    for mode, ov in (("chained", True), ("isolated", False)):
+        ts = []
+        for _ in range(reps):
+            t, n = time_gemv_cold(qd, torch, fmt, r, c, b, stream, overlap=ov)
+            ts.append(t)
+        t = min(ts)
+        out[mode] = {"us": round(t * 1e6, 3), "GB/s": round(by / t / 1e9, 1), "frac": round(by / t / 1e9 / hbm, 4),
+                     "launches_per_pass": n}
+    print(json.dumps(out))
 
 
 def main(argv=None):

@@ -132,10 +132,23 @@ qd_status qd_dequant(qd_fmt fmt, const void* packed, int64_t rows, int64_t cols,
 /* W: packed layout (qd_repack).  x: f32 [batch][cols].  y: f32 [batch][rows], */
 /* must not overlap x.  batch 1..16.  workspace: currently unused (pass NULL, 0);*/
 /* qd_q_gemv_workspace returns the bytes a call needs.                         */
+/* Arithmetic: codes meet x through integer dot products, x held per 32-element */
+/* unit as 24-bit integers with a power-of-two scale (at most 2^-23 of the      */
+/* unit's largest |x| per element); sums are f32.  A non-finite x gives NaN.    */
 /* ------------------------------------------------------------------------- */
 size_t qd_q_gemv_workspace(qd_fmt fmt, int64_t rows, int64_t cols, int batch);
 qd_status qd_q_gemv(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch,
                     void* workspace, size_t workspace_bytes, qd_stream_t stream);
+
+/* qd_q_gemv with launch flags.  QD_GEMV_OVERLAP: the kernel may start streaming W
+ * while the kernel before it on `stream` is still running (programmatic dependent
+ * launch), as the decode step launches its projections; x and y are still read and
+ * written only after that kernel has finished.  Only valid when no kernel that can
+ * still be running on `stream` writes W.  No flags: same as qd_q_gemv.  Unknown
+ * flag bits: QD_ERR_INVALID_ARG. */
+#define QD_GEMV_OVERLAP 1u
+qd_status qd_q_gemv_ex(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch,
+                       unsigned int flags, qd_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* Decode-step operations                                                      */

@@ -23,7 +23,7 @@ STATUS = {0: "QD_OK", 1: "QD_ERR_INVALID_ARG", 2: "QD_ERR_SHAPE", 3: "QD_ERR_ALI
 
 # Every symbol include/qdecode.h declares (checked by the CPU test suite).
 EXPORTS = ["qd_status_str", "qd_abi_version", "qd_f16_to_f32", "qd_bf16_to_f32", "qd_src_bytes", "qd_packed_bytes",
-           "qd_repack", "qd_unpack", "qd_dequant", "qd_q_gemv_workspace", "qd_q_gemv", "qd_rmsnorm",
+           "qd_repack", "qd_unpack", "qd_dequant", "qd_q_gemv_workspace", "qd_q_gemv", "qd_q_gemv_ex", "qd_rmsnorm",
            "qd_rope_table", "qd_rope", "qd_kv_append", "qd_gqa_decode_attn_workspace", "qd_gqa_decode_attn",
            "qd_gqa_decode_attn_noalloc",
            "qd_swiglu", "qd_argmax", "qd_embed", "qd_model_weight_bytes", "qd_model_state_bytes",
@@ -72,6 +72,7 @@ def load():
         "qd_dequant": ([i32, p, i64, i64, p, p], i32),
         "qd_q_gemv_workspace": ([i32, i64, i64, i32], sz),
         "qd_q_gemv": ([i32, p, i64, i64, p, p, i32, p, sz, p], i32),
+        "qd_q_gemv_ex": ([i32, p, i64, i64, p, p, i32, ctypes.c_uint, p], i32),
         "qd_rmsnorm": ([p, p, p, i32, i32, f32, p], i32),
         "qd_rope_table": ([f32, i32, i32, p], i32),
         "qd_rope": ([p, i32, i32, i64, p, i32, p, i32, i32, p], i32),
@@ -170,6 +171,14 @@ def q_gemv_workspace(fmt, rows, cols, batch) -> int:
 def q_gemv(fmt, W, rows, cols, x, y, batch, workspace=None, workspace_bytes=0, stream=None):
     _check("qd_q_gemv", load().qd_q_gemv(FMT[fmt], _ptr(W), rows, cols, _ptr(x), _ptr(y), batch, _ptr(workspace),
                                          workspace_bytes, _stream(stream)))
+
+
+GEMV_OVERLAP = 1
+
+
+def q_gemv_ex(fmt, W, rows, cols, x, y, batch, flags=0, stream=None):
+    _check("qd_q_gemv_ex", load().qd_q_gemv_ex(FMT[fmt], _ptr(W), rows, cols, _ptr(x), _ptr(y), batch, flags,
+                                               _stream(stream)))
 
 
 def rmsnorm(x, g, out, n, batch, eps, stream=None):

@@ -359,6 +359,12 @@ qd_status qd_q_gemv(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const
                     void* workspace, size_t workspace_bytes, qd_stream_t stream) {
   (void)workspace;
   (void)workspace_bytes;
+  return qd_q_gemv_ex(fmt, W, rows, cols, x, y, batch, 0u, stream);
+}
+
+qd_status qd_q_gemv_ex(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch,
+                       unsigned int flags, qd_stream_t stream) {
+  if (flags & ~QD_GEMV_OVERLAP) return QD_ERR_INVALID_ARG;
   if (!fmt_ok(fmt)) return QD_ERR_UNSUPPORTED;
   if (!W || !x || !y) return QD_ERR_INVALID_ARG;
   if (batch < 1 || batch > QD_MAX_BATCH) return QD_ERR_SHAPE;
@@ -370,6 +376,7 @@ qd_status qd_q_gemv(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const
   a.x = x;
   a.y = y;
   a.batch = batch;
+  a.pdl = (flags & QD_GEMV_OVERLAP) != 0;
   return launch_q_gemv(a, (cudaStream_t)stream);
 }
 

@@ -182,16 +182,11 @@ __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Per-warp staging ring in shared memory: kStages slots, one unit step each.  A slot
-// holds, for the RW rows of the group, every lane's code chunk (lane-major, so each
-// lane reads back only what it copied) and then 64 bytes of scale data per row:
+// Per-warp staging ring in shared memory: stages<FMT, RW>() slots, one unit step each.
+// A slot holds, for the RW rows of the group, every lane's code chunk (lane-major, so
+// each lane reads back only what it copied) and then 64 bytes of scale data per row:
 // Q4_0/Q8_0 the 32 lanes' f16 scales, Q4_K the 4 super-block headers the 32 units
 // span, INT8 the row scale.
-#ifndef QD_GEMV_STAGES
-#define QD_GEMV_STAGES 4
-#endif
-constexpr int kStages = QD_GEMV_STAGES;
-static_assert(kStages >= 2 && kStages <= 16, "ring depth");
 template <int FMT, int RW>
 constexpr int slot_code_bytes() {
   return RW * 32 * code_bytes<FMT>();
@@ -199,6 +194,18 @@ constexpr int slot_code_bytes() {
 template <int FMT, int RW>
 constexpr int slot_bytes() {
   return slot_code_bytes<FMT, RW>() + RW * 64;
+}
+// Ring depth: every warp keeps about kInFlight bytes of codes in flight whatever the
+// rows per group (HBM latency times bandwidth over the SMs' warps wants several KB per
+// warp: a 4-stage ring of 512-byte single-row steps left the DRAM pipe half empty).
+#ifndef QD_GEMV_INFLIGHT
+#define QD_GEMV_INFLIGHT 8192
+#endif
+constexpr int kInFlight = QD_GEMV_INFLIGHT;
+template <int FMT, int RW>
+constexpr int stages() {
+  constexpr int s = kInFlight / slot_code_bytes<FMT, RW>() + 1;
+  return s < 4 ? 4 : (s > 16 ? 16 : s);
 }
 
 // Issue the copies of one unit step (unit u of the rows in rp) into the slot at `slot`.
@@ -345,7 +352,7 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
 
 template <int FMT, int NB, int RW>
 __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
-  // dynamic shared memory: [warps][kStages] ring slots, then the x records [NB][units]
+  // dynamic shared memory: [warps][stages] ring slots, then the x records [NB][units]
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float red[kWarps][NB];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -358,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
   // an even split land on warps spread over every CTA rather than on the first CTAs.
   const int64_t gw = (int64_t)warp * gridDim.x + blockIdx.x, nw = (int64_t)gridDim.x * kWarps;
   constexpr uint32_t SB = slot_bytes<FMT, RW>();
+  constexpr int kStages = stages<FMT, RW>();
   uint8_t* ring = smem + (size_t)warp * kStages * SB;
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
   uint8_t* xq = smem + (size_t)kWarps * kStages * SB;
@@ -623,7 +631,7 @@ int resident_ctas(K kern, size_t smem) {
 template <int FMT, int NB, int RW>
 size_t smem_bytes_t(int64_t cols) {
   const size_t units = (size_t)cols / 32;
-  return (size_t)kWarps * kStages * slot_bytes<FMT, RW>() + (size_t)NB * units * kRecBytes;
+  return (size_t)kWarps * stages<FMT, RW>() * slot_bytes<FMT, RW>() + (size_t)NB * units * kRecBytes;
 }
 
 // Rows per group available for NB batch rows (more rows would spill registers).
@@ -658,18 +666,28 @@ size_t smem_bytes(int fmt, int64_t cols, int nb) {
 
 constexpr size_t kSmemCap = 200 * 1024;
 
+// Raise the kernel's dynamic shared-memory limit to kSmemCap once per device; the
+// occupancy query and the launch both depend on it.
+template <int FMT, int NB, int RW>
+bool smem_attr_set() {
+  static bool done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return false;
+  if (!done[dev]) {
+    if (cudaFuncSetAttribute(k_gemv_warp<FMT, NB, RW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) !=
+        cudaSuccess)
+      return false;
+    done[dev] = true;
+  }
+  return true;
+}
+
 template <int FMT, int NB, int RW>
 qd_status launch_rw(const Params& p, bool pdl, cudaStream_t stream, int64_t ctas) {
   auto kern = k_gemv_warp<FMT, NB, RW>;
   const size_t smem = smem_bytes_t<FMT, NB, RW>(p.W.cols);
-  static bool attr_done[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) != cudaSuccess)
-      return QD_ERR_CUDA;
-    attr_done[dev] = true;
-  }
+  if (!smem_attr_set<FMT, NB, RW>()) return QD_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas);
   cfg.blockDim = dim3(kThreads);
@@ -684,15 +702,23 @@ qd_status launch_rw(const Params& p, bool pdl, cudaStream_t stream, int64_t ctas
   return QD_OK;
 }
 
-// CTAs for RW rows per group: one wave of resident CTAs at most (0 when the shared
-// memory does not fit).
+// CTAs for RW rows per group: one wave of at most kCtasPerSm CTAs per SM (0 when the
+// shared memory does not fit).  One CTA (8 warps) per SM measured as fast as two on
+// the large shapes and faster on several (the streams already fill the DRAM queues),
+// and it leaves room for the next kernel's CTAs to start their weight copies early.
+#ifndef QD_GEMV_CTAS_PER_SM
+#define QD_GEMV_CTAS_PER_SM 1
+#endif
+constexpr int kCtasPerSm = QD_GEMV_CTAS_PER_SM;
 template <int FMT, int NB, int RW>
 int64_t ctas_for(int64_t rows, int64_t cols) {
   const size_t smem = smem_bytes_t<FMT, NB, RW>(cols);
-  if (smem > kSmemCap) return 0;
+  if (smem > kSmemCap || !smem_attr_set<FMT, NB, RW>()) return 0;
   const int64_t groups = (rows + RW - 1) / RW;
   const int64_t want = (groups + kWarps - 1) / kWarps;
-  const int64_t cap = (int64_t)sm_count() * resident_ctas(k_gemv_warp<FMT, NB, RW>, smem);
+  int per_sm = resident_ctas(k_gemv_warp<FMT, NB, RW>, smem);
+  if (per_sm > kCtasPerSm) per_sm = kCtasPerSm;
+  const int64_t cap = (int64_t)sm_count() * per_sm;
   return want < cap ? want : cap;
 }
 

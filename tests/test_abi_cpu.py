@@ -73,6 +73,10 @@ def test_gemv_validation_before_any_device_work(lib):
     assert f(2, good, 8, 128, good, good, 1, None, 0, None) == 2           # Q4_K cols % 256
     assert f(0, good + 4, 8, 64, good, good, 1, None, 0, None) == 3        # misaligned W
     assert f(0, good, 8, 64, good, good + 8, 1, None, 0, None) == 3        # misaligned y
+    g = lib.qd_q_gemv_ex
+    assert g(0, good, 8, 64, good, good, 1, 2, None) == 1                  # unknown flag bit
+    assert g(0, good, 8, 48, good, good, 1, qd.GEMV_OVERLAP, None) == 2    # cols % 32
+    assert g(9, good, 8, 64, good, good, 1, 0, None) == 4                  # unknown format
 
 
 def test_other_entry_points_validate(lib):

@@ -191,3 +191,22 @@ def test_q_gemv_non_finite_x_propagates(qd, fmt):
     x[1, 300] = np.nan
     got = _gemv(qd, fmt, p, rows, cols, x)
     assert not np.isfinite(got).any()
+
+
+def test_q_gemv_overlap_chain_matches_plain_launches(qd):
+    """QD_GEMV_OVERLAP (weights streamed while the previous kernel finishes) must not change
+    any result: a chain y1 = W1 x, y2 = W2 y1, y3 = W3 y2 gives the same bits either way."""
+    shapes = [("q4_0", 576, 1536), ("q8_0", 1536, 576), ("q4_k", 256, 1536)]
+    ws = [weights(qd, f, 8, f"ov{i}", r, c)[1] for i, (f, r, c) in enumerate(shapes)]
+    x = dev(qdsynth.activations(8, "xov", 2, 1536))
+    outs = []
+    for flags in (qd.GEMV_OVERLAP, 0):
+        ys = [torch.empty(2, r, device="cuda") for (_, r, _) in shapes]
+        src = x
+        for (f, r, c), w, y in zip(shapes, ws, ys):
+            qd.q_gemv_ex(f, w, r, c, src, y, 2, flags)
+            src = y
+        torch.cuda.synchronize()
+        outs.append([y.cpu().numpy() for y in ys])
+    for a, b in zip(*outs):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
