@@ -88,6 +88,12 @@ def reduce_max(value: float, world: int) -> float:
     return float(t.item())
 
 
+def whole_job_rate(world: int, steps: int, units_per_step: int, t_max: float) -> float:
+    """Units processed by all ranks over the slowest rank's timed seconds (weak scaling:
+    every rank runs its own replica of the workload)."""
+    return world * steps * units_per_step / t_max
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -230,11 +236,13 @@ def run_ours(args, world, rank, local):
     scratch_h = torch.zeros(T, dtype=torch.int32).pin_memory()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
-    def step(dev_side: bool):
+    def step(dev_side: bool, mid=None):
         model.reset(stream)
         t_in, s_out = (tok, scratch) if dev_side else (tok_h, scratch_h)
         base_in, base_s = t_in.data_ptr(), s_out.data_ptr()
         for t in range(T):
+            if t == PROMPT and mid is not None:
+                mid.record(stream)  # prompt positions 0..127 done; generated tokens from here
             out = base_in + 4 * (t + 1) if t >= PROMPT - 1 else base_s + 4 * t
             model.decode_step(base_in + 4 * t, 1, out, None, stream)
 
@@ -253,17 +261,19 @@ def run_ours(args, world, rank, local):
         wall0 = time.perf_counter()
         for _ in range(args.steps):
             flush.fill_(0)  # L2 flush between steps (outside the step's events)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0, em, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             e0.record(stream)
-            step(True)
+            step(True, em)
             e1.record(stream)
-            times.append((e0, e1))
+            times.append((e0, em, e1))
         torch.cuda.synchronize()
         barrier(world)
         wall = time.perf_counter() - wall0
-    step_s = [a.elapsed_time(b) / 1e3 for a, b in times]
+    step_s = [a.elapsed_time(b) / 1e3 for a, _, b in times]
+    prefill_s = [a.elapsed_time(m) / 1e3 for a, m, _ in times]
+    decode_s = [m.elapsed_time(b) / 1e3 for _, m, b in times]
     t_total = reduce_max(sum(step_s), world)
-    value = world * args.steps * T / t_total
+    value = whole_job_rate(world, args.steps, T, t_total)
     assert np.array_equal(tok[PROMPT:T].cpu().numpy(), gen_dev), "generation changed between runs"
 
     # ---- end to end: pinned host token buffers through the C ABI
@@ -282,9 +292,24 @@ def run_ours(args, world, rank, local):
         e_times.append(time.perf_counter() - w0)
     assert np.array_equal(got, gen_dev), "host-buffer generation differs from device-buffer generation"
     e2e_total = reduce_max(sum(e_times), world)
-    e2e_value = world * args.steps * T / e2e_total
+    e2e_value = whole_job_rate(world, args.steps, T, e2e_total)
 
     hbm, bf16, peak_kind = peaks()
+    # weight-bytes-per-token roofline: every weight byte (tied head once) + the KV rows read
+    kv_per_pos = 2 * cfg["layers"] * cfg["n_kv_heads"] * cfg["head_dim"] * 4
+    wbytes = model.weights.numel()
+
+    def phase(ts, p0, p1):
+        n = p1 - p0
+        tput = n / statistics.median(ts)
+        bytes_ = sum(wbytes + kv_per_pos * (p + 1) for p in range(p0, p1))
+        roof = n / (bytes_ / (hbm * 1e9))
+        return {"tokens/s": round(tput, 1), "roofline_tokens/s": round(roof, 1), "frac": round(tput / roof, 4),
+                "frac_nominal_8tbs": round(tput / (n / (bytes_ / 8e12)), 4)}
+
+    phases = {"prefill (positions 0-127)": phase(prefill_s, 0, PROMPT),
+              "decode (positions 128-255)": phase(decode_s, PROMPT, T),
+              "whole step": phase(step_s, 0, T)}
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1e3 * t_total / args.steps, 3), "higher_is_better": True,
@@ -301,6 +326,8 @@ def run_ours(args, world, rank, local):
         "launches_per_token": launches_token,
         "wall_s_timed": round(wall, 3),
         "ms_per_token": round(1e3 * t_total / (args.steps * T), 4),
+        "phases": phases,
+        "bytes_per_token": {"weights": int(wbytes), "kv_per_position": kv_per_pos},
     }
     out["clocks"] = clk.summary()
 
@@ -310,7 +337,7 @@ def run_ours(args, world, rank, local):
         del model
         torch.cuda.empty_cache()
         if not args.no_1p7b:
-            out["decode_1p7b"] = bench_1p7b(qd, torch, stream, args)
+            out["decode_1p7b"] = bench_1p7b(qd, torch, stream, args, hbm)
         if world == 1:
             out["cpu_baseline"] = cpu_baseline(cfg, seconds=args.cpu_seconds)
     if rank == 0:
@@ -390,7 +417,7 @@ def gemv_sweep(qd, torch, stream, hbm, args):
     return res
 
 
-def bench_1p7b(qd, torch, stream, args):
+def bench_1p7b(qd, torch, stream, args, hbm):
     """1.7B-shaped INT8 step at context 4096 (pos 4095): batch 1 and 16, cache entries N(0,1)
     drawn on the device with a seeded torch generator (timing only; the parity tests use the
     host generator)."""
@@ -415,7 +442,7 @@ def bench_1p7b(qd, torch, stream, args):
         outt = torch.empty(batch, dtype=torch.int32, device="cuda")
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
         ts = []
-        for i in range(3 + 5):
+        for i in range(3 + 20):
             m.set_pos([ctx - 1] * batch, stream)
             flush.fill_(0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -428,9 +455,12 @@ def bench_1p7b(qd, torch, stream, args):
         t = statistics.median(ts)
         wbytes = m.weights.numel()
         kv = 2 * n * 4
-        out[f"batch{batch}"] = {"ms_per_step": round(t * 1e3, 3), "tokens/s": round(batch / t, 1),
-                                "bytes_per_step": int(wbytes + kv),
-                                "GB/s": round((wbytes + kv) / t / 1e9, 1)}
+        gbs = (wbytes + kv) / t / 1e9
+        roof = batch / ((wbytes + kv) / (hbm * 1e9))
+        out[f"batch{batch}"] = {"ms_per_step": round(t * 1e3, 3), "ms_per_step_best": round(min(ts) * 1e3, 3),
+                                "tokens/s": round(batch / t, 1), "bytes_per_step": int(wbytes + kv),
+                                "GB/s": round(gbs, 1), "roofline_tokens/s": round(roof, 1),
+                                "frac": round(gbs / hbm, 4), "frac_nominal_8tbs": round(gbs / 8000, 4)}
         m.close()
         del m, flush
         torch.cuda.empty_cache()
@@ -450,16 +480,24 @@ def cpu_baseline(cfg, seconds=15.0, max_tokens=64):
     kc = np.zeros(L * hk * ctx * hd, np.float32)
     vc = np.zeros_like(kc)
     prompt = qdsynth.tokens(0, "smol135m.prompt", PROMPT, cfg["vocab"])
-    t0 = time.perf_counter()
-    n = 0
-    while n < max_tokens and (time.perf_counter() - t0) < seconds:
-        om.decode_step(kc, vc, hk * ctx * hd, n, int(prompt[n]))
-        n += 1
-    dt = time.perf_counter() - t0
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    def run(threads, budget):
+        cores = oracle.set_threads(threads)
+        kc[:] = 0
+        vc[:] = 0
+        t0 = time.perf_counter()
+        n = 0
+        while n < max_tokens and (time.perf_counter() - t0) < budget:
+            om.decode_step(kc, vc, hk * ctx * hd, n, int(prompt[n]))
+            n += 1
+        return n, time.perf_counter() - t0, cores
+
+    n1, dt1, _ = run(1, seconds / 2)
+    n, dt, cores = run(os.cpu_count() or 1, seconds / 2)
     return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"first {n} tokens (positions 0..{n - 1}) of the 135M 128+128 run, batch 1, "
-                      f"{dt:.1f} s; oracle C code, double accumulation, OpenMP over matrix rows"}
+                      f"{dt:.1f} s; oracle C code, double accumulation, OpenMP over matrix rows",
+            "single_thread": {"value": round(n1 / dt1, 3), "unit": "tokens/s", "cores": 1,
+                              "sample": f"first {n1} tokens, {dt1:.1f} s"}}
 
 
 # ----------------------------------------------------------------------------- reference arm

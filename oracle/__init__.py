@@ -81,6 +81,8 @@ def _L():
         lib.or_attention.restype = i32
         lib.or_swiglu.argtypes = [p, p, i64, p]
         lib.or_swiglu.restype = i32
+        lib.or_set_threads.argtypes = [i32]
+        lib.or_set_threads.restype = i32
         lib.or_argmax_f32.argtypes = [p, i64]
         lib.or_argmax_f32.restype = i64
         lib.or_argmax_f64.argtypes = [p, i64]
@@ -245,3 +247,8 @@ class Model:
         if rc:
             raise ValueError(f"or_decode_step rc={rc}")
         return logits, int(nxt.value)
+
+
+def set_threads(n: int) -> int:
+    """OpenMP threads for the oracle's loops (results do not depend on it); returns the count in use."""
+    return int(_L().or_set_threads(int(n)))

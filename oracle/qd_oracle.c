@@ -44,6 +44,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 enum { OR_Q4_0 = 0, OR_Q8_0 = 1, OR_Q4_K = 2, OR_I8_ROW = 3 };
 enum { OR_ROPE_ADJACENT = 0, OR_ROPE_HALF = 1 };
@@ -465,3 +468,15 @@ done:
 }
 
 int or_abi_version(void) { return 1; }
+
+/* Threads for the OpenMP loops above (1 = single-threaded; the per-output summation order
+ * does not depend on it, so results are identical).  Returns the count now in use. */
+int or_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+  return omp_get_max_threads();
+#else
+  (void)n;
+  return 1;
+#endif
+}
