@@ -331,6 +331,11 @@ qd_status launch_q_gemv(const GemvArgs& a, cudaStream_t stream) {
     const qd_status st = launch_q_gemv_stream(a, stream);
     if (st != QD_ERR_UNSUPPORTED) return st;
   }
+  // Batch 9-16 INT8 rows: tensor cores.
+  {
+    const qd_status st = launch_q_gemv_tc(a, stream);
+    if (st != QD_ERR_UNSUPPORTED) return st;
+  }
   if (a.norm_g) return QD_ERR_UNSUPPORTED;
   switch (a.fmt) {
     case QD_Q4_0: return launch_fmt<QD_Q4_0>(a.W, a.x, a.y, a.batch, a.mode, stream);

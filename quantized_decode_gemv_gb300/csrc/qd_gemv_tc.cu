@@ -1,0 +1,468 @@
+// Batched q_gemv on the 5th-generation tensor cores: per-row INT8 weights, 9-16 batch
+// rows (independent sequences).
+//
+// y[b][r] = s_r * sum_c q[r][c] x[b][c]  (minillm-cpp README "Quantization": symmetric
+// per-row INT8, one f32 scale per output row; the row dot of llmoxide blog s1).  With
+// 16 sequences the product is a small dense contraction (M = rows, N = 16, K = cols), so
+// it runs as tcgen05.mma kind::f16 with an f32 accumulator in tensor memory:
+//
+//  * A (M = 128 rows x 16 K per instruction) is the weight tile.  The int8 codes stream
+//    through a per-thread cp.async ring in shared memory (each thread copies and later
+//    converts the same 16-byte chunks, so kRing - 1 stages are in flight without a CTA
+//    barrier), are converted exactly to f16 (q ^ 0x80 placed in the mantissa of 1024,
+//    then 1152 subtracted) into the K-major, no-swizzle canonical layout (8-row x 16-byte
+//    core matrices), double-buffered; one thread issues the MMAs and commits them to an
+//    mbarrier per buffer.
+//  * Persistent clusters: each cluster stages x once and walks row tiles
+//    cluster, cluster + clusters, ...; the weight ring runs on across tiles.
+//  * B (N = 32 x K) is x: each sequence's K-slice is scaled by a power of two (its largest
+//    |x| lands in [2^13, 2^14), exact) and split into an f16 high part and the f16 rounding
+//    of the remainder, columns 0-15 high, 16-31 low.  hi + lo holds x to about 2^-22
+//    relative; the tensor core's products of f16 values are exact and sum in f32.
+//  * Columns split over up to 8 CTAs of the cluster (split-K) when there are few row
+//    tiles; each CTA reads its 128 x 32 accumulator tile from tensor memory (tcgen05.ld,
+//    one row per thread), combines hi + lo and undoes its scales, and the cluster sums the
+//    partials through distributed shared memory in rank order (deterministic), then
+//    applies s_r and the epilogue (store, accumulate into y, or SwiGLU of interleaved
+//    gate/up rows).
+//
+// Every wait on an mbarrier is bounded; on a timeout the kernel sets kErrTimeout, stops
+// issuing, waits (bounded) once more, frees its tensor memory and returns.
+#include <cooperative_groups.h>
+#include <cuda_fp16.h>
+
+#include "qd_internal.cuh"
+
+namespace qd {
+namespace tc_gemv {
+
+constexpr int kM = 128;       // weight rows per CTA (the MMA's M)
+constexpr int kN = 32;        // B columns: 16 sequences x (high, low)
+constexpr int kNB = 16;       // sequences
+constexpr int kKT = 64;       // K elements per pipeline stage
+constexpr int kThreads = 128;
+constexpr int kMaxKc = 2048;  // K elements per CTA at most (shared memory for B)
+constexpr int kRing = 6;      // int8 weight stages in the cp.async ring
+constexpr int kMaxCluster = 8;
+constexpr uint32_t kTmemCols = 32;
+
+constexpr uint32_t kCoreBytes = 128;                   // one 8 x 16-byte core matrix
+constexpr uint32_t kASbo = (kKT / 8) * kCoreBytes;     // bytes between 8-row groups of A
+constexpr uint32_t kABytes = kM * kKT * 2;             // one f16 A stage
+constexpr uint32_t kPartBytes = kNB * kM * 4;          // the CTA's f32 partial tile
+constexpr uint32_t kI8Bytes = kM * kKT;                // one int8 weight stage
+constexpr int kChunks = kM * kKT / 16 / kThreads;      // 16-byte chunks per thread and stage
+
+struct Params {
+  const int8_t* codes;
+  const float* row_scale;
+  int64_t rows, cols;
+  const float* x;
+  float* y;
+  int batch;
+  int kc;  // columns per CTA
+  int mode;
+  uint32_t* err;
+};
+
+__host__ __device__ constexpr uint32_t b_bytes(int kc) { return (uint32_t)kN * (uint32_t)kc * 2u; }
+// dynamic shared memory: B | A[0] | A[1] | int8 ring | partial tile
+__host__ __device__ constexpr uint32_t smem_bytes(int kc) {
+  return b_bytes(kc) + 2 * kABytes + kRing * kI8Bytes + kPartBytes;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Shared-memory matrix descriptor, K-major, no swizzle: start address, byte offset
+// between core matrices along K (leading) and along M/N (stride), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+// Instruction descriptor, kind::f16: f32 accumulator, f16 A and B, both K-major, N, M.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+               : "memory");
+}
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Wait for the completion of mbarrier phase `parity`, at most kSpinLimit polls.  The
+// poll is mbarrier.test_wait (returns at once); try_wait may park the thread for a
+// hardware-chosen interval, which measured as microseconds per pipeline stage here.
+constexpr uint32_t kSpinLimit = 1u << 24;
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// 32 consecutive f32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Four int8 codes -> two f16 pairs, exactly: (q ^ 0x80) is q + 128 in 0..255; as the low
+// mantissa byte of 1024 it gives the f16 1024 + q + 128, and 1152 is subtracted.
+__device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& h01, uint32_t& h23) {
+  const uint32_t u = w ^ 0x80808080u;
+  const __half2 k1152 = __float2half2_rn(1152.f);
+  uint32_t a = __byte_perm(u, 0x64646464u, 0x4140u), b = __byte_perm(u, 0x64646464u, 0x4342u);
+  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), k1152);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), k1152);
+  h01 = *reinterpret_cast<uint32_t*>(&ha);
+  h23 = *reinterpret_cast<uint32_t*>(&hb);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) uint64_t mbar[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ float unscale[kNB];
+  __shared__ float wmax[kNB];
+  __shared__ int dead;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int64_t tiles = (p.rows + kM - 1) / kM;
+  const int64_t cl = blockIdx.y, ncl = gridDim.y;  // this cluster, clusters
+  const int64_t my_tiles = cl < tiles ? (tiles - cl + ncl - 1) / ncl : 0;
+  const int kc = p.kc;
+  const int64_t k0 = (int64_t)rank * kc;
+  const int nst = kc / kKT;  // stages per tile
+  uint8_t* Bs = smem;
+  uint8_t* ring = smem + b_bytes(kc) + 2 * kABytes;
+  float* part = reinterpret_cast<float*>(ring + kRing * kI8Bytes);  // [kNB][kM]
+  const uint32_t bsbo = (uint32_t)(kc / 8) * kCoreBytes;
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[0])) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[1])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    dead = 0;
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t taddr = tmem_base;
+
+  // ---- weight ring.  Global stage g = tile index t * nst + s; chunk j of a stage for
+  // this thread: row r = (tid + 128 j) / (kKT / 16), 16-byte column chunk (tid + 128 j) %
+  // (kKT / 16).  The weights never depend on the previous kernel: the first stages are
+  // issued before the dependency wait.
+  const int64_t total = my_tiles * nst;
+  const uint32_t ring_s = smem_u32(ring);
+  auto issue = [&](int64_t g) {
+    if (g < total) {
+      const int64_t row0 = (cl + (g / nst) * ncl) * kM;
+      const int s = (int)(g % nst);
+      const uint32_t slot = ring_s + (uint32_t)(g % kRing) * kI8Bytes;
+#pragma unroll
+      for (int j = 0; j < kChunks; ++j) {
+        const int c = tid + kThreads * j, r = c / (kKT / 16), k16 = c % (kKT / 16);
+        const int64_t row = min(row0 + r, p.rows - 1);  // rows past the end: any valid row
+        const int8_t* src = p.codes + row * p.cols + k0 + (int64_t)s * kKT + 16 * k16;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(slot + (uint32_t)c * 16u), "l"(src)
+                     : "memory");
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+#pragma unroll
+  for (int g = 0; g < kRing - 1; ++g) issue(g);
+
+  pdl_wait();  // x comes from the previous kernel
+
+  // ---- B: per sequence, the largest |x| of this CTA's columns, then the scaled high and
+  // low f16 parts in the canonical layout (row n = sequence n high, 16 + n low).
+  for (int b = warp; b < kNB; b += kThreads / 32) {
+    float m = 0.f;
+    if (b < p.batch) {
+      const float4* xr = reinterpret_cast<const float4*>(p.x + (int64_t)b * p.cols + k0);
+      for (int i = lane; i < kc / 4; i += 32) {
+        const float4 v = __ldcg(xr + i);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        if (isnan(v.x) || isnan(v.y) || isnan(v.z) || isnan(v.w)) m = INFINITY;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) wmax[b] = m;
+  }
+  __syncthreads();
+  float sc_b[kNB];  // multiplier into f16 range per sequence
+#pragma unroll
+  for (int b = 0; b < kNB; ++b) {
+    const float m = wmax[b];
+    const int F = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;
+    // m in [2^F, 2^(F+1)) -> scale 2^(13 - F); zero / tiny rows keep scale 1; a non-finite
+    // row gets a NaN unscale so its outputs become NaN
+    const bool live = m > 0.f && F > -100 && F < 128;
+    sc_b[b] = live ? __uint_as_float((uint32_t)(127 + 13 - F) << 23) : 1.f;
+    if (tid == 0)
+      unscale[b] = F == 128 ? __uint_as_float(0x7FC00000u) : (live ? __uint_as_float((uint32_t)(127 - 13 + F) << 23) : 1.f);
+  }
+  // 8 chunks (of 8 columns) per pass: all loads first, then the conversions and stores
+  const int nchunk = kNB * (kc / 8);
+  for (int c0 = tid; c0 < nchunk; c0 += 8 * kThreads) {
+    float4 v[8][2];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = c0 + u * kThreads, b = c / (kc / 8), k8 = c % (kc / 8);
+      v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c < nchunk && b < p.batch) {
+        const float4* src = reinterpret_cast<const float4*>(p.x + (int64_t)b * p.cols + k0 + 8 * k8);
+        v[u][0] = __ldcg(src);
+        v[u][1] = __ldcg(src + 1);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = c0 + u * kThreads, b = c / (kc / 8), k8 = c % (kc / 8);
+      if (c >= nchunk) break;
+      float sc = 1.f;
+#pragma unroll
+      for (int bb = 0; bb < kNB; ++bb) sc = bb == b ? sc_b[bb] : sc;
+      const float f[8] = {v[u][0].x * sc, v[u][0].y * sc, v[u][0].z * sc, v[u][0].w * sc,
+                          v[u][1].x * sc, v[u][1].y * sc, v[u][1].z * sc, v[u][1].w * sc};
+      uint32_t h[4], l[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const __half a = __float2half_rn(f[2 * t]), bq = __float2half_rn(f[2 * t + 1]);
+        const __half la = __float2half_rn(f[2 * t] - __half2float(a));
+        const __half lb = __float2half_rn(f[2 * t + 1] - __half2float(bq));
+        __half2 hh = __halves2half2(a, bq), ll = __halves2half2(la, lb);
+        h[t] = *reinterpret_cast<uint32_t*>(&hh);
+        l[t] = *reinterpret_cast<uint32_t*>(&ll);
+      }
+      const int nh = b, nl = kNB + b;
+      *reinterpret_cast<uint4*>(Bs + (nh >> 3) * bsbo + k8 * kCoreBytes + (nh & 7) * 16) =
+          make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(Bs + (nl >> 3) * bsbo + k8 * kCoreBytes + (nl & 7) * 16) =
+          make_uint4(l[0], l[1], l[2], l[3]);
+    }
+  }
+  pdl_trigger();  // the next kernel may launch (it waits for this one before reading y)
+
+  // ---- main loop over this cluster's tiles and their stages: convert stage g of the ring
+  // into A[g & 1], one thread issues its kKT / 16 MMAs and commits them to mbar[g & 1];
+  // after a tile's last stage the accumulator is read out and the tile finished.
+  bool ok = true;
+  for (int64_t g = 0; g < total; ++g) {
+    const int buf = (int)(g & 1);
+    const int s = (int)(g % nst);
+    const int64_t row0 = (cl + (g / nst) * ncl) * kM;
+    issue(g + kRing - 1);
+    asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");  // stage g landed
+    if (g >= 2) {
+      if (!mbar_wait(smem_u32(&mbar[buf]), (uint32_t)((g - 2) >> 1) & 1u)) ok = false;
+    }
+    uint8_t* A = smem + b_bytes(kc) + (uint32_t)buf * kABytes;
+    const uint8_t* slot = ring + (g % kRing) * kI8Bytes;
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) {
+      const int c = tid + kThreads * j, r = c / (kKT / 16), k16 = c % (kKT / 16);
+      uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
+      if (row0 + r < p.rows) {
+        const uint4 q = *reinterpret_cast<const uint4*>(slot + c * 16);
+        i8x4_to_h2x2(q.x, h0.x, h0.y);
+        i8x4_to_h2x2(q.y, h0.z, h0.w);
+        i8x4_to_h2x2(q.z, h1.x, h1.y);
+        i8x4_to_h2x2(q.w, h1.z, h1.w);
+      }
+      uint8_t* dst = A + (r >> 3) * kASbo + (2 * k16) * kCoreBytes + (r & 7) * 16;
+      *reinterpret_cast<uint4*>(dst) = h0;
+      *reinterpret_cast<uint4*>(dst + kCoreBytes) = h1;
+    }
+    fence_proxy_async();
+    __syncthreads();
+    if (!ok && tid == 0) dead = 1;
+    if (tid == 0 && !dead) {
+      fence_after_sync();
+      const uint32_t a0 = smem_u32(A), b0 = smem_u32(Bs) + (uint32_t)(s * kKT / 8) * kCoreBytes;
+#pragma unroll
+      for (int kk = 0; kk < kKT / 16; ++kk)
+        mma_f16(taddr, smem_desc(a0 + kk * 2 * kCoreBytes, kCoreBytes, kASbo),
+                smem_desc(b0 + kk * 2 * kCoreBytes, kCoreBytes, bsbo), (s > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(smem_u32(&mbar[buf]));
+    }
+    if (s != nst - 1) continue;
+
+    // ---- end of a tile: this commit covers every MMA so far
+    bool fin = mbar_wait(smem_u32(&mbar[buf]), (uint32_t)(g >> 1) & 1u);
+    if (!fin) fin = mbar_wait(smem_u32(&mbar[buf]), (uint32_t)(g >> 1) & 1u);
+    __syncthreads();
+    const bool good = fin && !dead;
+    if (!good && tid == 0) {
+      dead = 1;
+      if (p.err) atomicOr(p.err, kErrTimeout);
+    }
+    fence_after_sync();
+    float v[32];
+    tmem_ld32(taddr + ((uint32_t)(32 * warp) << 16), v);
+    const int r = 32 * warp + lane;
+#pragma unroll
+    for (int b = 0; b < kNB; ++b) part[b * kM + r] = good ? (v[b] + v[kNB + b]) * unscale[b] : 0.f;
+    fence_before_sync();  // the next tile's MMAs overwrite the accumulator after this
+    cluster.sync();       // every CTA's partial is in place
+    // rank-order sum over the cluster; CTA `rank` finishes rows [rank * R, (rank+1) * R)
+    const int R = kM / S;
+    for (int i = tid; i < kNB * R; i += kThreads) {
+      const int b = i / R, rr = rank * R + i % R;
+      float acc = 0.f;
+      for (int q = 0; q < S; ++q) acc += *cluster.map_shared_rank(part + b * kM + rr, q);
+      const int64_t row = row0 + rr;
+      const bool in = b < p.batch && row < p.rows;
+      const float val = in ? acc * __ldg(p.row_scale + row) : 0.f;
+      if (p.mode == kGemvSwiGLU) {
+        const float up = __shfl_down_sync(0xffffffffu, val, 1);  // row + 1 sits in the next lane
+        if (in && (rr & 1) == 0 && row + 1 < p.rows)
+          p.y[(int64_t)b * (p.rows / 2) + row / 2] = val / (1.0f + expf(-val)) * up;
+      } else if (in) {
+        float* dst = p.y + (int64_t)b * p.rows + row;
+        if (p.mode == kGemvAccumulate)
+          *dst += val;
+        else
+          *dst = val;
+      }
+    }
+    cluster.sync();  // the partials may be overwritten by the next tile
+    fence_after_sync();
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy in flight at exit
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kTmemCols)
+                              : "memory");
+}
+
+int sm_count_tc() {
+  static int n[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 152;
+  if (!n[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 152;
+    n[dev] = v;
+  }
+  return n[dev];
+}
+
+// Cluster size S (columns per CTA = cols / S): with as many row tiles as SMs, the smallest
+// legal S (no split); otherwise the largest power of two up to 8 that keeps tiles x S
+// within the SMs.  Legal: cols divisible by S * kKT and at most kMaxKc columns per CTA.
+int choose_split(int64_t rows, int64_t cols) {
+  const int64_t tiles = (rows + kM - 1) / kM;
+  const int64_t nsm = sm_count_tc();
+  int best = 0;
+  for (int s = 1; s <= kMaxCluster; s *= 2) {
+    if (cols % ((int64_t)s * kKT) || cols / s > kMaxKc) continue;
+    if (best == 0) best = s;  // smallest legal split
+    else if (tiles * s <= nsm) best = s;
+  }
+  return best;
+}
+
+}  // namespace tc_gemv
+
+bool gemv_tc_supported(const GemvArgs& a) {
+  using namespace tc_gemv;
+  if (a.fmt != QD_I8_ROW || a.batch <= 8 || a.batch > kNB || a.norm_g) return false;
+  if (a.mode != kGemvStore && a.mode != kGemvAccumulate && a.mode != kGemvSwiGLU) return false;
+  if (a.mode == kGemvSwiGLU && (a.W.rows & 1)) return false;
+  return choose_split(a.W.rows, a.W.cols) > 0;
+}
+
+qd_status launch_q_gemv_tc(const GemvArgs& a, cudaStream_t stream) {
+  using namespace tc_gemv;
+  if (!gemv_tc_supported(a)) return QD_ERR_UNSUPPORTED;
+  const int S = choose_split(a.W.rows, a.W.cols);
+  Params p;
+  p.codes = reinterpret_cast<const int8_t*>(a.W.codes);
+  p.row_scale = reinterpret_cast<const float*>(a.W.scales);
+  p.rows = a.W.rows;
+  p.cols = a.W.cols;
+  p.x = a.x;
+  p.y = a.y;
+  p.batch = a.batch;
+  p.kc = (int)(a.W.cols / S);
+  p.mode = a.mode;
+  p.err = a.err;
+  const uint32_t smem = smem_bytes(p.kc);
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(k_gemv_tc_i8, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(kMaxKc)) !=
+        cudaSuccess)
+      return QD_ERR_CUDA;
+    attr_done[dev] = true;
+  }
+  // one CTA per SM: persistent clusters, at most one per S SMs
+  const int64_t tiles = (a.W.rows + kM - 1) / kM;
+  int64_t clusters = sm_count_tc() / S;
+  if (clusters > tiles) clusters = tiles;
+  if (clusters < 1) clusters = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)S, (unsigned)clusters);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, k_gemv_tc_i8, p) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
+}
+
+}  // namespace qd

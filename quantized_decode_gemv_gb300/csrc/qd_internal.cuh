@@ -266,6 +266,9 @@ qd_status launch_q_gemv_stream(const GemvArgs& a, cudaStream_t stream);
 // Whether launch_q_gemv runs the streaming kernel for these arguments (and so can
 // take norm_g and the pdl flag).
 bool gemv_streams(const GemvArgs& a);
+// Batch 9-16 per-row INT8 on the tensor cores (store, accumulate or SwiGLU; no fused norm).
+bool gemv_tc_supported(const GemvArgs& a);
+qd_status launch_q_gemv_tc(const GemvArgs& a, cudaStream_t stream);
 
 qd_status launch_rmsnorm(const float* x, const float* g, float* out, int n, int batch, float eps,
                          cudaStream_t stream);

@@ -210,3 +210,41 @@ def test_q_gemv_overlap_chain_matches_plain_launches(qd):
         outs.append([y.cpu().numpy() for y in ys])
     for a, b in zip(*outs):
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+# Batch 9-16 per-row INT8 runs on the tensor cores (tcgen05, f16 hi/lo split of x, split-K
+# over a cluster); shapes chosen to hit ragged row tiles and cluster sizes 1-8.
+TC_SHAPES = [(1, 128), (129, 256), (200, 2048), (300, 1024), (2048, 2048), (640, 8192)]
+
+
+@pytest.mark.parametrize("batch", [9, 13, 16])
+def test_q_gemv_int8_tensor_core_batches(qd, batch):
+    for rows, cols in TC_SHAPES:
+        src, p = weights(qd, "i8", 11, f"tc{rows}x{cols}", rows, cols)
+        x = qdsynth.activations(11, f"xtc{cols}", batch, cols)
+        got = _gemv(qd, "i8", p, rows, cols, x)
+        assert_close(got, oracle.gemv("i8", src, rows, cols, x), tol=2e-5, what=f"i8 tc {rows}x{cols} b{batch}")
+
+
+def test_q_gemv_int8_tensor_core_exact_case(qd):
+    """Power-of-two row scales and small integer x: the f16 high parts are exact, the low parts
+    zero, every product and partial sum an integer below 2^24 -> bit-exact."""
+    rows, cols, batch = 260, 2048, 16
+    src = qdsynth.weight_src("i8", 12, "tcex", rows, cols).copy()
+    src[rows * cols:] = np.full(rows, 2.0 ** -5, np.float32).view(np.uint8)
+    p = packed(qd, "i8", src, rows, cols)
+    x = qdsynth.ints_i32(12, "tcxi", batch * cols, -3, 3).reshape(batch, cols).astype(np.float32)
+    got = _gemv(qd, "i8", p, rows, cols, x)
+    assert np.array_equal(got.astype(np.float64), oracle.gemv("i8", src, rows, cols, x))
+
+
+def test_q_gemv_int8_tensor_core_non_finite(qd):
+    rows, cols, batch = 130, 1024, 12
+    src, p = weights(qd, "i8", 13, "tcnf", rows, cols)
+    x = qdsynth.activations(13, "xtcnf", batch, cols)
+    x[3, 17] = np.nan
+    x[7, 900] = np.inf
+    got = _gemv(qd, "i8", p, rows, cols, x)
+    bad = {3, 7}
+    for b in range(batch):
+        assert (not np.isfinite(got[b]).any()) if b in bad else np.isfinite(got[b]).all(), b

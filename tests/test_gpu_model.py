@@ -74,6 +74,16 @@ def test_tiny_model_teacher_forced(qd, w_fmt, emb_fmt, pairing):
     print(f"tiny {w_fmt}/{emb_fmt}: worst rel err {worst:.2e}, near-tie tokens {near}")
 
 
+@pytest.mark.parametrize("batch", [12, 16])
+def test_tiny_int8_model_batch_over_8_tensor_cores(qd, batch):
+    """INT8 rows at batch 9-16 take the tensor-core GEMV (store, accumulate and SwiGLU
+    epilogues; separate RMSNorm, RoPE/KV-append and argmax kernels)."""
+    cfg = dict(TINY, w_fmt="i8", emb_fmt="i8", pairing="half")
+    prompt = qdsynth.tokens(10, "tiny.prompt16", batch * 3, cfg["vocab"]).reshape(batch, 3)
+    worst, near = run_teacher_forced(qd, cfg, 10, prompt, n_gen=3, batch=batch, max_ctx=8)
+    print(f"tiny i8 batch {batch}: worst rel err {worst:.2e}, near-tie tokens {near}")
+
+
 def test_model_reset_and_errors(qd):
     cfg = dict(TINY)
     m, _ = build_model(qd, cfg, 3, 4, 2)
