@@ -4,30 +4,31 @@
 // y[b][r] = s_r * sum_c q[r][c] x[b][c]  (minillm-cpp README "Quantization": symmetric
 // per-row INT8, one f32 scale per output row; the row dot of llmoxide blog s1).  With
 // 16 sequences the product is a small dense contraction (M = rows, N = 16, K = cols), so
-// it runs as tcgen05.mma kind::f16 with an f32 accumulator in tensor memory:
+// it runs as tcgen05.mma kind::f16 with an f32 accumulator in tensor memory.
 //
-//  * A (M = 128 rows x 16 K per instruction) is the weight tile.  The int8 codes stream
-//    through a per-thread cp.async ring in shared memory (each thread copies and later
-//    converts the same 16-byte chunks, so kRing - 1 stages are in flight without a CTA
-//    barrier), are converted exactly to f16 (q ^ 0x80 placed in the mantissa of 1024,
-//    then 1152 subtracted) into the K-major, no-swizzle canonical layout (8-row x 16-byte
-//    core matrices), double-buffered; one thread issues the MMAs and commits them to an
-//    mbarrier per buffer.
-//  * Persistent clusters: each cluster stages x once and walks row tiles
-//    cluster, cluster + clusters, ...; the weight ring runs on across tiles.
 //  * B (N = 32 x K) is x: each sequence's K-slice is scaled by a power of two (its largest
 //    |x| lands in [2^13, 2^14), exact) and split into an f16 high part and the f16 rounding
 //    of the remainder, columns 0-15 high, 16-31 low.  hi + lo holds x to about 2^-22
-//    relative; the tensor core's products of f16 values are exact and sum in f32.
-//  * Columns split over up to 8 CTAs of the cluster (split-K) when there are few row
-//    tiles; each CTA reads its 128 x 32 accumulator tile from tensor memory (tcgen05.ld,
-//    one row per thread), combines hi + lo and undoes its scales, and the cluster sums the
-//    partials through distributed shared memory in rank order (deterministic), then
-//    applies s_r and the epilogue (store, accumulate into y, or SwiGLU of interleaved
-//    gate/up rows).
+//    relative; the tensor core's products of f16 values are exact and sum in f32.  B is
+//    staged once per CTA in shared memory (K-major, no-swizzle canonical layout).
+//  * A (M = 128 rows x 16 K per instruction) is the weight tile.  Warp-specialised
+//    pipeline: four converter warps stream the int8 codes through a per-thread cp.async
+//    ring (each thread copies and later converts the same 16-byte chunks), convert them
+//    exactly to f16 (q ^ 0x80 placed in the mantissa of 1024, then 1152 subtracted) into
+//    one of two A buffers and arrive on its "full" mbarrier; one lane of the fifth warp
+//    waits for "full", issues the stage's MMAs and commits them to the buffer's "empty"
+//    mbarrier (which the converters wait for before reuse).  Tiles alternate between two
+//    accumulators in tensor memory; after a tile's last stage the MMA lane commits to the
+//    accumulator's "done" barrier, and the converter warps read it out (tcgen05.ld, one
+//    row per thread) a few stages into the next tile, then arrive on its "drained" barrier.
+//  * Many row tiles: one cluster-free CTA per SM walks tiles cta, cta + CTAs, ... with the
+//    weight ring running on across tiles.  Few row tiles: the columns split over up to 8
+//    CTAs of a thread-block cluster (one tile each); the partials are summed through
+//    distributed shared memory in rank order (deterministic) at the end.
+//  * Epilogue: s_r, then store, accumulate into y, or SwiGLU of interleaved gate/up rows.
 //
-// Every wait on an mbarrier is bounded; on a timeout the kernel sets kErrTimeout, stops
-// issuing, waits (bounded) once more, frees its tensor memory and returns.
+// Every mbarrier wait is bounded; on a timeout the kernel sets kErrTimeout, stops issuing
+// MMAs, finishes its loops without waiting, frees its tensor memory and returns.
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
 
@@ -36,22 +37,24 @@
 namespace qd {
 namespace tc_gemv {
 
-constexpr int kM = 128;       // weight rows per CTA (the MMA's M)
+constexpr int kM = 128;       // weight rows per tile (the MMA's M)
 constexpr int kN = 32;        // B columns: 16 sequences x (high, low)
 constexpr int kNB = 16;       // sequences
 constexpr int kKT = 64;       // K elements per pipeline stage
-constexpr int kThreads = 128;
+constexpr int kConv = 128;    // converter / epilogue threads (warps 0-3)
+constexpr int kThreads = kConv + 32;  // + the MMA warp
 constexpr int kMaxKc = 2048;  // K elements per CTA at most (shared memory for B)
-constexpr int kRing = 6;      // int8 weight stages in the cp.async ring
+constexpr int kRing = 5;      // int8 weight stages in the cp.async ring
+constexpr int kEpiDelay = 2;  // stages into the next tile before the previous one is read out
 constexpr int kMaxCluster = 8;
-constexpr uint32_t kTmemCols = 32;
+constexpr uint32_t kTmemCols = 64;  // two 32-column accumulators
 
-constexpr uint32_t kCoreBytes = 128;                   // one 8 x 16-byte core matrix
-constexpr uint32_t kASbo = (kKT / 8) * kCoreBytes;     // bytes between 8-row groups of A
-constexpr uint32_t kABytes = kM * kKT * 2;             // one f16 A stage
-constexpr uint32_t kPartBytes = kNB * kM * 4;          // the CTA's f32 partial tile
-constexpr uint32_t kI8Bytes = kM * kKT;                // one int8 weight stage
-constexpr int kChunks = kM * kKT / 16 / kThreads;      // 16-byte chunks per thread and stage
+constexpr uint32_t kCoreBytes = 128;                // one 8 x 16-byte core matrix
+constexpr uint32_t kASbo = (kKT / 8) * kCoreBytes;  // bytes between 8-row groups of A
+constexpr uint32_t kABytes = kM * kKT * 2;          // one f16 A buffer
+constexpr uint32_t kI8Bytes = kM * kKT;             // one int8 weight stage
+constexpr uint32_t kPartBytes = kNB * kM * 4;       // the CTA's f32 partial tile (split-K)
+constexpr int kChunks = kM * kKT / 16 / kConv;      // 16-byte chunks per converter thread and stage
 
 struct Params {
   const int8_t* codes;
@@ -100,10 +103,20 @@ __device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fenc
 __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// Wait for the completion of mbarrier phase `parity`, at most kSpinLimit polls.  The
-// poll is mbarrier.test_wait (returns at once); try_wait may park the thread for a
-// hardware-chosen interval, which measured as microseconds per pipeline stage here.
+// mbarrier helpers.  A wait polls mbarrier.test_wait (returns at once) at most
+// kSpinLimit times and reports whether the phase completed.
 constexpr uint32_t kSpinLimit = 1u << 24;
+__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+  asm volatile(
+      "{\n"
+      ".reg .b64 st;\n"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n"
+      "}\n" ::"r"(mbar)
+      : "memory");
+}
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
     uint32_t done;
@@ -149,234 +162,303 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& h01, uint32_t
   h23 = *reinterpret_cast<uint32_t*>(&hb);
 }
 
+__device__ __forceinline__ void conv_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) uint64_t mbar[2];
+  __shared__ __align__(8) uint64_t bar_full[2], bar_empty[2], bar_done[2], bar_drained[2];
   __shared__ uint32_t tmem_base;
   __shared__ float unscale[kNB];
   __shared__ float wmax[kNB];
-  __shared__ int dead;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
   const int64_t tiles = (p.rows + kM - 1) / kM;
-  const int64_t cl = blockIdx.y, ncl = gridDim.y;  // this cluster, clusters
-  const int64_t my_tiles = cl < tiles ? (tiles - cl + ncl - 1) / ncl : 0;
+  // S == 1: CTA blockIdx.y walks tiles blockIdx.y, + gridDim.y, ...; S > 1: one tile each
+  const int64_t first = blockIdx.y, stride = gridDim.y;
+  const int64_t my_tiles = first < tiles ? (tiles - first + stride - 1) / stride : 0;
   const int kc = p.kc;
   const int64_t k0 = (int64_t)rank * kc;
   const int nst = kc / kKT;  // stages per tile
+  const int64_t total = my_tiles * nst;
   uint8_t* Bs = smem;
   uint8_t* ring = smem + b_bytes(kc) + 2 * kABytes;
   float* part = reinterpret_cast<float*>(ring + kRing * kI8Bytes);  // [kNB][kM]
   const uint32_t bsbo = (uint32_t)(kc / 8) * kCoreBytes;
+  const uint32_t full0 = smem_u32(&bar_full[0]), empty0 = smem_u32(&bar_empty[0]);
+  const uint32_t done0 = smem_u32(&bar_done[0]), drained0 = smem_u32(&bar_drained[0]);
 
-  if (warp == 0) {
+  if (warp == 4) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
                  "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[0])) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[1])) : "memory");
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(full0 + 8 * i, kConv);
+      mbar_init(empty0 + 8 * i, 1);
+      mbar_init(done0 + 8 * i, 1);
+      mbar_init(drained0 + 8 * i, kConv);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    dead = 0;
   }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t taddr = tmem_base;
 
-  // ---- weight ring.  Global stage g = tile index t * nst + s; chunk j of a stage for
-  // this thread: row r = (tid + 128 j) / (kKT / 16), 16-byte column chunk (tid + 128 j) %
-  // (kKT / 16).  The weights never depend on the previous kernel: the first stages are
-  // issued before the dependency wait.
-  const int64_t total = my_tiles * nst;
-  const uint32_t ring_s = smem_u32(ring);
-  auto issue = [&](int64_t g) {
-    if (g < total) {
-      const int64_t row0 = (cl + (g / nst) * ncl) * kM;
-      const int s = (int)(g % nst);
-      const uint32_t slot = ring_s + (uint32_t)(g % kRing) * kI8Bytes;
+  if (warp < 4) {
+    // ======================= converter / epilogue warps =======================
+    bool bad = false;
+    const uint32_t ring_s = smem_u32(ring);
+    // weight ring: global stage g = tile index t * nst + s; chunk j of a stage for this
+    // thread: row r = (tid + 128 j) / (kKT / 16), 16-byte chunk (tid + 128 j) % (kKT / 16)
+    // copy cursor: the next stage to copy (tile it, stage is, ring slot islot); 32-bit
+    // counters updated by one step (no division in the loop)
+    int ig = 0, is = 0, islot = 0;
+    int64_t irow0 = first * kM;
+    auto issue = [&]() {
+      if (ig < total) {
+        const int64_t row0 = irow0;
+        const int s = is;
+        const uint32_t slot = ring_s + (uint32_t)islot * kI8Bytes;
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j) {
+          const int c = tid + kConv * j, r = c / (kKT / 16), k16 = c % (kKT / 16);
+          const int64_t row = min(row0 + r, p.rows - 1);  // rows past the end: any valid row
+          const int8_t* src = p.codes + row * p.cols + k0 + (int64_t)s * kKT + 16 * k16;
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(slot + (uint32_t)c * 16u), "l"(src)
+                       : "memory");
+        }
+        ++ig;
+        if (++is == nst) {
+          is = 0;
+          irow0 += stride * kM;
+        }
+        if (++islot == kRing) islot = 0;
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    // The epilogue of local tile t: wait for its accumulator, read it out (row 32 warp +
+    // lane), release the accumulator, then finish the row (S == 1) or park the partial.
+    auto epilogue = [&](int64_t t) {
+      const int acc = (int)(t & 1);
+      const int64_t row0 = (first + t * stride) * kM;
+      const bool ok = mbar_wait(done0 + 8 * acc, (uint32_t)(t >> 1) & 1u);
+      if (!ok) bad = true;
+      fence_after_sync();
+      float v[32];
+      tmem_ld32(taddr + (uint32_t)(32 * acc) + ((uint32_t)(32 * warp) << 16), v);
+      fence_before_sync();
+      mbar_arrive(drained0 + 8 * acc);
+      const int r = 32 * warp + lane;
+      const int64_t row = row0 + r;
+      if (S > 1) {
+#pragma unroll
+        for (int b = 0; b < kNB; ++b) part[b * kM + r] = bad ? 0.f : (v[b] + v[kNB + b]) * unscale[b];
+        return;
+      }
+      const float rs = row < p.rows ? __ldg(p.row_scale + row) : 0.f;
+#pragma unroll
+      for (int b = 0; b < kNB; ++b) {
+        const float val = bad ? 0.f : (v[b] + v[kNB + b]) * unscale[b] * rs;
+        const bool in = b < p.batch && row < p.rows;
+        if (p.mode == kGemvSwiGLU) {
+          const float up = __shfl_down_sync(0xffffffffu, val, 1);  // row + 1 sits in the next lane
+          if (in && (r & 1) == 0 && row + 1 < p.rows)
+            p.y[(int64_t)b * (p.rows / 2) + row / 2] = val / (1.0f + expf(-val)) * up;
+        } else if (in) {
+          float* dst = p.y + (int64_t)b * p.rows + row;
+          if (p.mode == kGemvAccumulate)
+            *dst += val;
+          else
+            *dst = val;
+        }
+      }
+    };
+
+#pragma unroll
+    for (int g = 0; g < kRing - 1; ++g) issue();
+
+    pdl_wait();  // x comes from the previous kernel
+
+    // ---- B: per sequence, the largest |x| of this CTA's columns, then the scaled high and
+    // low f16 parts in the canonical layout (row n = sequence n high, 16 + n low)
+    for (int b = warp; b < kNB; b += 4) {
+      float m = 0.f;
+      if (b < p.batch) {
+        const float4* xr = reinterpret_cast<const float4*>(p.x + (int64_t)b * p.cols + k0);
+        for (int i = lane; i < kc / 4; i += 32) {
+          const float4 v = __ldcg(xr + i);
+          m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+          if (isnan(v.x) || isnan(v.y) || isnan(v.z) || isnan(v.w)) m = INFINITY;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      if (lane == 0) wmax[b] = m;
+    }
+    conv_bar();
+    float sc_b[kNB];  // multiplier into f16 range per sequence
+#pragma unroll
+    for (int b = 0; b < kNB; ++b) {
+      const float m = wmax[b];
+      const int F = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;
+      // m in [2^F, 2^(F+1)) -> scale 2^(13 - F); zero / tiny rows keep scale 1; a
+      // non-finite row gets a NaN unscale so its outputs become NaN
+      const bool live = m > 0.f && F > -100 && F < 128;
+      sc_b[b] = live ? __uint_as_float((uint32_t)(127 + 13 - F) << 23) : 1.f;
+      if (tid == 0)
+        unscale[b] =
+            F == 128 ? __uint_as_float(0x7FC00000u) : (live ? __uint_as_float((uint32_t)(127 - 13 + F) << 23) : 1.f);
+    }
+    // 8 chunks (of 8 columns) per pass: all loads first, then the conversions and stores
+    const int nchunk = kNB * (kc / 8);
+    for (int c0 = tid; c0 < nchunk; c0 += 8 * kConv) {
+      float4 v[8][2];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * kConv, b = c / (kc / 8), k8 = c % (kc / 8);
+        v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < nchunk && b < p.batch) {
+          const float4* src = reinterpret_cast<const float4*>(p.x + (int64_t)b * p.cols + k0 + 8 * k8);
+          v[u][0] = __ldcg(src);
+          v[u][1] = __ldcg(src + 1);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * kConv, b = c / (kc / 8), k8 = c % (kc / 8);
+        if (c >= nchunk) break;
+        float sc = 1.f;
+#pragma unroll
+        for (int bb = 0; bb < kNB; ++bb) sc = bb == b ? sc_b[bb] : sc;
+        const float f[8] = {v[u][0].x * sc, v[u][0].y * sc, v[u][0].z * sc, v[u][0].w * sc,
+                            v[u][1].x * sc, v[u][1].y * sc, v[u][1].z * sc, v[u][1].w * sc};
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int t2 = 0; t2 < 4; ++t2) {
+          const __half a = __float2half_rn(f[2 * t2]), bq = __float2half_rn(f[2 * t2 + 1]);
+          const __half la = __float2half_rn(f[2 * t2] - __half2float(a));
+          const __half lb = __float2half_rn(f[2 * t2 + 1] - __half2float(bq));
+          __half2 hh = __halves2half2(a, bq), ll = __halves2half2(la, lb);
+          h[t2] = *reinterpret_cast<uint32_t*>(&hh);
+          l[t2] = *reinterpret_cast<uint32_t*>(&ll);
+        }
+        const int nh = b, nl = kNB + b;
+        *reinterpret_cast<uint4*>(Bs + (nh >> 3) * bsbo + k8 * kCoreBytes + (nh & 7) * 16) =
+            make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(Bs + (nl >> 3) * bsbo + k8 * kCoreBytes + (nl & 7) * 16) =
+            make_uint4(l[0], l[1], l[2], l[3]);
+      }
+    }
+    conv_bar();     // unscale is written; B is complete (made visible to the MMAs below)
+    pdl_trigger();  // the next kernel may launch (it waits for this one before reading y)
+
+    // ---- stage loop
+    const int epi_at = nst - 1 < kEpiDelay ? nst - 1 : kEpiDelay;
+    int t = 0, s = 0, slot_i = 0;  // tile, stage and ring slot of stage g
+    int64_t row0 = first * kM;
+    for (int g = 0; g < (int)total; ++g) {
+      const int buf = g & 1;
+      issue();  // stage g + kRing - 1
+      asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");  // stage g landed
+      if (g >= 2 && !bad) {
+        if (!mbar_wait(empty0 + 8 * buf, (uint32_t)((g - 2) >> 1) & 1u)) bad = true;  // A[buf] free
+      }
+      uint8_t* A = smem + b_bytes(kc) + (uint32_t)buf * kABytes;
+      const uint8_t* slot = ring + slot_i * kI8Bytes;
 #pragma unroll
       for (int j = 0; j < kChunks; ++j) {
-        const int c = tid + kThreads * j, r = c / (kKT / 16), k16 = c % (kKT / 16);
-        const int64_t row = min(row0 + r, p.rows - 1);  // rows past the end: any valid row
-        const int8_t* src = p.codes + row * p.cols + k0 + (int64_t)s * kKT + 16 * k16;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(slot + (uint32_t)c * 16u), "l"(src)
-                     : "memory");
+        const int c = tid + kConv * j, r = c / (kKT / 16), k16 = c % (kKT / 16);
+        uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
+        if (row0 + r < p.rows) {
+          const uint4 q = *reinterpret_cast<const uint4*>(slot + c * 16);
+          i8x4_to_h2x2(q.x, h0.x, h0.y);
+          i8x4_to_h2x2(q.y, h0.z, h0.w);
+          i8x4_to_h2x2(q.z, h1.x, h1.y);
+          i8x4_to_h2x2(q.w, h1.z, h1.w);
+        }
+        uint8_t* dst = A + (r >> 3) * kASbo + (2 * k16) * kCoreBytes + (r & 7) * 16;
+        *reinterpret_cast<uint4*>(dst) = h0;
+        *reinterpret_cast<uint4*>(dst + kCoreBytes) = h1;
+      }
+      fence_proxy_async();
+      mbar_arrive(full0 + 8 * buf);
+      if (s == epi_at && t >= 1) epilogue(t - 1);
+      if (++slot_i == kRing) slot_i = 0;
+      if (++s == nst) {
+        s = 0;
+        ++t;
+        row0 += stride * kM;
       }
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  };
-#pragma unroll
-  for (int g = 0; g < kRing - 1; ++g) issue(g);
-
-  pdl_wait();  // x comes from the previous kernel
-
-  // ---- B: per sequence, the largest |x| of this CTA's columns, then the scaled high and
-  // low f16 parts in the canonical layout (row n = sequence n high, 16 + n low).
-  for (int b = warp; b < kNB; b += kThreads / 32) {
-    float m = 0.f;
-    if (b < p.batch) {
-      const float4* xr = reinterpret_cast<const float4*>(p.x + (int64_t)b * p.cols + k0);
-      for (int i = lane; i < kc / 4; i += 32) {
-        const float4 v = __ldcg(xr + i);
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-        if (isnan(v.x) || isnan(v.y) || isnan(v.z) || isnan(v.w)) m = INFINITY;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if (lane == 0) wmax[b] = m;
-  }
-  __syncthreads();
-  float sc_b[kNB];  // multiplier into f16 range per sequence
-#pragma unroll
-  for (int b = 0; b < kNB; ++b) {
-    const float m = wmax[b];
-    const int F = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;
-    // m in [2^F, 2^(F+1)) -> scale 2^(13 - F); zero / tiny rows keep scale 1; a non-finite
-    // row gets a NaN unscale so its outputs become NaN
-    const bool live = m > 0.f && F > -100 && F < 128;
-    sc_b[b] = live ? __uint_as_float((uint32_t)(127 + 13 - F) << 23) : 1.f;
-    if (tid == 0)
-      unscale[b] = F == 128 ? __uint_as_float(0x7FC00000u) : (live ? __uint_as_float((uint32_t)(127 - 13 + F) << 23) : 1.f);
-  }
-  // 8 chunks (of 8 columns) per pass: all loads first, then the conversions and stores
-  const int nchunk = kNB * (kc / 8);
-  for (int c0 = tid; c0 < nchunk; c0 += 8 * kThreads) {
-    float4 v[8][2];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int c = c0 + u * kThreads, b = c / (kc / 8), k8 = c % (kc / 8);
-      v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (c < nchunk && b < p.batch) {
-        const float4* src = reinterpret_cast<const float4*>(p.x + (int64_t)b * p.cols + k0 + 8 * k8);
-        v[u][0] = __ldcg(src);
-        v[u][1] = __ldcg(src + 1);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int c = c0 + u * kThreads, b = c / (kc / 8), k8 = c % (kc / 8);
-      if (c >= nchunk) break;
-      float sc = 1.f;
-#pragma unroll
-      for (int bb = 0; bb < kNB; ++bb) sc = bb == b ? sc_b[bb] : sc;
-      const float f[8] = {v[u][0].x * sc, v[u][0].y * sc, v[u][0].z * sc, v[u][0].w * sc,
-                          v[u][1].x * sc, v[u][1].y * sc, v[u][1].z * sc, v[u][1].w * sc};
-      uint32_t h[4], l[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const __half a = __float2half_rn(f[2 * t]), bq = __float2half_rn(f[2 * t + 1]);
-        const __half la = __float2half_rn(f[2 * t] - __half2float(a));
-        const __half lb = __float2half_rn(f[2 * t + 1] - __half2float(bq));
-        __half2 hh = __halves2half2(a, bq), ll = __halves2half2(la, lb);
-        h[t] = *reinterpret_cast<uint32_t*>(&hh);
-        l[t] = *reinterpret_cast<uint32_t*>(&ll);
-      }
-      const int nh = b, nl = kNB + b;
-      *reinterpret_cast<uint4*>(Bs + (nh >> 3) * bsbo + k8 * kCoreBytes + (nh & 7) * 16) =
-          make_uint4(h[0], h[1], h[2], h[3]);
-      *reinterpret_cast<uint4*>(Bs + (nl >> 3) * bsbo + k8 * kCoreBytes + (nl & 7) * 16) =
-          make_uint4(l[0], l[1], l[2], l[3]);
-    }
-  }
-  pdl_trigger();  // the next kernel may launch (it waits for this one before reading y)
-
-  // ---- main loop over this cluster's tiles and their stages: convert stage g of the ring
-  // into A[g & 1], one thread issues its kKT / 16 MMAs and commits them to mbar[g & 1];
-  // after a tile's last stage the accumulator is read out and the tile finished.
-  bool ok = true;
-  for (int64_t g = 0; g < total; ++g) {
-    const int buf = (int)(g & 1);
-    const int s = (int)(g % nst);
-    const int64_t row0 = (cl + (g / nst) * ncl) * kM;
-    issue(g + kRing - 1);
-    asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");  // stage g landed
-    if (g >= 2) {
-      if (!mbar_wait(smem_u32(&mbar[buf]), (uint32_t)((g - 2) >> 1) & 1u)) ok = false;
-    }
-    uint8_t* A = smem + b_bytes(kc) + (uint32_t)buf * kABytes;
-    const uint8_t* slot = ring + (g % kRing) * kI8Bytes;
-#pragma unroll
-    for (int j = 0; j < kChunks; ++j) {
-      const int c = tid + kThreads * j, r = c / (kKT / 16), k16 = c % (kKT / 16);
-      uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
-      if (row0 + r < p.rows) {
-        const uint4 q = *reinterpret_cast<const uint4*>(slot + c * 16);
-        i8x4_to_h2x2(q.x, h0.x, h0.y);
-        i8x4_to_h2x2(q.y, h0.z, h0.w);
-        i8x4_to_h2x2(q.z, h1.x, h1.y);
-        i8x4_to_h2x2(q.w, h1.z, h1.w);
-      }
-      uint8_t* dst = A + (r >> 3) * kASbo + (2 * k16) * kCoreBytes + (r & 7) * 16;
-      *reinterpret_cast<uint4*>(dst) = h0;
-      *reinterpret_cast<uint4*>(dst + kCoreBytes) = h1;
-    }
-    fence_proxy_async();
-    __syncthreads();
-    if (!ok && tid == 0) dead = 1;
-    if (tid == 0 && !dead) {
+    if (my_tiles >= 1) epilogue(my_tiles - 1);
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy in flight at exit
+    if (bad && p.err) atomicOr(p.err, kErrTimeout);
+  } else if (lane == 0) {
+    // ======================= MMA lane =======================
+    bool bad = false;
+    int t = 0, s = 0;  // tile and stage of stage g
+    for (int g = 0; g < (int)total && !bad; ++g) {
+      const int buf = g & 1;
+      const int acc = t & 1;
+      if (s == 0 && t >= 2 && !mbar_wait(drained0 + 8 * acc, (uint32_t)((t - 2) >> 1) & 1u)) bad = true;
+      if (!bad && !mbar_wait(full0 + 8 * buf, (uint32_t)(g >> 1) & 1u)) bad = true;
+      if (bad) break;
       fence_after_sync();
-      const uint32_t a0 = smem_u32(A), b0 = smem_u32(Bs) + (uint32_t)(s * kKT / 8) * kCoreBytes;
+      const uint32_t a0 = smem_u32(smem + b_bytes(kc) + (uint32_t)buf * kABytes);
+      const uint32_t b0 = smem_u32(Bs) + (uint32_t)(s * kKT / 8) * kCoreBytes;
 #pragma unroll
       for (int kk = 0; kk < kKT / 16; ++kk)
-        mma_f16(taddr, smem_desc(a0 + kk * 2 * kCoreBytes, kCoreBytes, kASbo),
+        mma_f16(taddr + (uint32_t)(32 * acc), smem_desc(a0 + kk * 2 * kCoreBytes, kCoreBytes, kASbo),
                 smem_desc(b0 + kk * 2 * kCoreBytes, kCoreBytes, bsbo), (s > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(smem_u32(&mbar[buf]));
-    }
-    if (s != nst - 1) continue;
-
-    // ---- end of a tile: this commit covers every MMA so far
-    bool fin = mbar_wait(smem_u32(&mbar[buf]), (uint32_t)(g >> 1) & 1u);
-    if (!fin) fin = mbar_wait(smem_u32(&mbar[buf]), (uint32_t)(g >> 1) & 1u);
-    __syncthreads();
-    const bool good = fin && !dead;
-    if (!good && tid == 0) {
-      dead = 1;
-      if (p.err) atomicOr(p.err, kErrTimeout);
-    }
-    fence_after_sync();
-    float v[32];
-    tmem_ld32(taddr + ((uint32_t)(32 * warp) << 16), v);
-    const int r = 32 * warp + lane;
-#pragma unroll
-    for (int b = 0; b < kNB; ++b) part[b * kM + r] = good ? (v[b] + v[kNB + b]) * unscale[b] : 0.f;
-    fence_before_sync();  // the next tile's MMAs overwrite the accumulator after this
-    cluster.sync();       // every CTA's partial is in place
-    // rank-order sum over the cluster; CTA `rank` finishes rows [rank * R, (rank+1) * R)
-    const int R = kM / S;
-    for (int i = tid; i < kNB * R; i += kThreads) {
-      const int b = i / R, rr = rank * R + i % R;
-      float acc = 0.f;
-      for (int q = 0; q < S; ++q) acc += *cluster.map_shared_rank(part + b * kM + rr, q);
-      const int64_t row = row0 + rr;
-      const bool in = b < p.batch && row < p.rows;
-      const float val = in ? acc * __ldg(p.row_scale + row) : 0.f;
-      if (p.mode == kGemvSwiGLU) {
-        const float up = __shfl_down_sync(0xffffffffu, val, 1);  // row + 1 sits in the next lane
-        if (in && (rr & 1) == 0 && row + 1 < p.rows)
-          p.y[(int64_t)b * (p.rows / 2) + row / 2] = val / (1.0f + expf(-val)) * up;
-      } else if (in) {
-        float* dst = p.y + (int64_t)b * p.rows + row;
-        if (p.mode == kGemvAccumulate)
-          *dst += val;
-        else
-          *dst = val;
+      mma_commit(empty0 + 8 * buf);
+      if (s == nst - 1) mma_commit(done0 + 8 * acc);
+      if (++s == nst) {
+        s = 0;
+        ++t;
       }
     }
-    cluster.sync();  // the partials may be overwritten by the next tile
-    fence_after_sync();
+    if (bad && p.err) atomicOr(p.err, kErrTimeout);
   }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy in flight at exit
+
+  // ---- split-K: rank-order sum of the cluster's partials; CTA `rank` finishes rows
+  // [rank * R, (rank+1) * R) of its (single) tile
+  if (S > 1) {
+    cluster.sync();  // every CTA's partial is in place
+    if (warp < 4 && my_tiles == 1) {
+      const int R = kM / S;
+      const int64_t row0 = first * kM;
+      for (int i = tid; i < kNB * R; i += kConv) {
+        const int b = i / R, rr = rank * R + i % R;
+        float acc = 0.f;
+        for (int q = 0; q < S; ++q) acc += *cluster.map_shared_rank(part + b * kM + rr, q);
+        const int64_t row = row0 + rr;
+        const bool in = b < p.batch && row < p.rows;
+        const float val = in ? acc * __ldg(p.row_scale + row) : 0.f;
+        if (p.mode == kGemvSwiGLU) {
+          const float up = __shfl_down_sync(0xffffffffu, val, 1);  // row + 1 sits in the next lane
+          if (in && (rr & 1) == 0 && row + 1 < p.rows)
+            p.y[(int64_t)b * (p.rows / 2) + row / 2] = val / (1.0f + expf(-val)) * up;
+        } else if (in) {
+          float* dst = p.y + (int64_t)b * p.rows + row;
+          if (p.mode == kGemvAccumulate)
+            *dst += val;
+          else
+            *dst = val;
+        }
+      }
+    }
+    cluster.sync();  // keep this CTA's partial alive until every reader is done
+  }
   fence_before_sync();
   __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kTmemCols)
+  if (warp == 4) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kTmemCols)
                               : "memory");
 }
 
@@ -393,17 +475,22 @@ int sm_count_tc() {
   return n[dev];
 }
 
-// Cluster size S (columns per CTA = cols / S): with as many row tiles as SMs, the smallest
-// legal S (no split); otherwise the largest power of two up to 8 that keeps tiles x S
-// within the SMs.  Legal: cols divisible by S * kKT and at most kMaxKc columns per CTA.
+// Cluster size S (columns per CTA = cols / S).  With at least half as many row tiles as
+// SMs: the smallest legal S (S == 1 runs persistent CTAs over the tiles).  Otherwise the
+// largest power of two up to 8 with tiles x S within the SMs.  Legal: cols divisible by
+// S * kKT and at most kMaxKc columns per CTA.
 int choose_split(int64_t rows, int64_t cols) {
   const int64_t tiles = (rows + kM - 1) / kM;
   const int64_t nsm = sm_count_tc();
   int best = 0;
   for (int s = 1; s <= kMaxCluster; s *= 2) {
     if (cols % ((int64_t)s * kKT) || cols / s > kMaxKc) continue;
-    if (best == 0) best = s;  // smallest legal split
-    else if (tiles * s <= nsm) best = s;
+    if (best == 0) {
+      best = s;  // smallest legal split
+      if (2 * tiles >= nsm) break;
+    } else if (tiles * s <= nsm) {
+      best = s;
+    }
   }
   return best;
 }
@@ -443,13 +530,12 @@ qd_status launch_q_gemv_tc(const GemvArgs& a, cudaStream_t stream) {
       return QD_ERR_CUDA;
     attr_done[dev] = true;
   }
-  // one CTA per SM: persistent clusters, at most one per S SMs
+  // S == 1: persistent CTAs, one per SM at most; S > 1: one cluster per row tile
   const int64_t tiles = (a.W.rows + kM - 1) / kM;
-  int64_t clusters = sm_count_tc() / S;
-  if (clusters > tiles) clusters = tiles;
-  if (clusters < 1) clusters = 1;
+  int64_t ny = S == 1 ? (tiles < sm_count_tc() ? tiles : sm_count_tc()) : tiles;
+  if (ny < 1) ny = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)S, (unsigned)clusters);
+  cfg.gridDim = dim3((unsigned)S, (unsigned)ny);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
