@@ -372,16 +372,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
       }
       uint8_t* A = smem + b_bytes(kc) + (uint32_t)buf * kABytes;
       const uint8_t* slot = ring + slot_i * kI8Bytes;
+      // all of this thread's chunks are read before any is written: the stores to A must
+      // not order the next chunk's load behind them
+      uint4 q[kChunks];
+#pragma unroll
+      for (int j = 0; j < kChunks; ++j) q[j] = *reinterpret_cast<const uint4*>(slot + (tid + kConv * j) * 16);
 #pragma unroll
       for (int j = 0; j < kChunks; ++j) {
         const int c = tid + kConv * j, r = c / (kKT / 16), k16 = c % (kKT / 16);
         uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
         if (row0 + r < p.rows) {
-          const uint4 q = *reinterpret_cast<const uint4*>(slot + c * 16);
-          i8x4_to_h2x2(q.x, h0.x, h0.y);
-          i8x4_to_h2x2(q.y, h0.z, h0.w);
-          i8x4_to_h2x2(q.z, h1.x, h1.y);
-          i8x4_to_h2x2(q.w, h1.z, h1.w);
+          i8x4_to_h2x2(q[j].x, h0.x, h0.y);
+          i8x4_to_h2x2(q[j].y, h0.z, h0.w);
+          i8x4_to_h2x2(q[j].z, h1.x, h1.y);
+          i8x4_to_h2x2(q[j].w, h1.z, h1.w);
         }
         uint8_t* dst = A + (r >> 3) * kASbo + (2 * k16) * kCoreBytes + (r & 7) * 16;
         *reinterpret_cast<uint4*>(dst) = h0;
