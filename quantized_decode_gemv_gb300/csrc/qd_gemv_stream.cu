@@ -351,7 +351,7 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
 }
 
 template <int FMT, int NB, int RW>
-__global__ void __launch_bounds__(kThreads, 2) k_gemv_warp(const Params p) {
+__global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
   // dynamic shared memory: [warps][stages] ring slots, then the x records [NB][units]
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float red[kWarps][NB];
@@ -637,7 +637,7 @@ size_t smem_bytes_t(int64_t cols) {
 // Rows per group available for NB batch rows (more rows would spill registers).
 template <int NB>
 constexpr int max_rw() {
-  return NB <= 2 ? 4 : 2;
+  return 4;
 }
 template <int NB>
 constexpr int min_rw() {

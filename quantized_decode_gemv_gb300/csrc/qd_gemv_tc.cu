@@ -50,7 +50,8 @@ constexpr int kMaxCluster = 8;
 constexpr uint32_t kTmemCols = 64;  // two 32-column accumulators
 
 constexpr uint32_t kCoreBytes = 128;                // one 8 x 16-byte core matrix
-constexpr uint32_t kASbo = (kKT / 8) * kCoreBytes;  // bytes between 8-row groups of A
+constexpr uint32_t kASbo = 8 * 2 * kKT;             // bytes between 8-row groups of A (one swizzle atom)
+static_assert(2 * kKT == 128, "an A row of a stage is one 128-byte swizzle span");
 constexpr uint32_t kABytes = kM * kKT * 2;          // one f16 A buffer
 constexpr uint32_t kI8Bytes = kM * kKT;             // one int8 weight stage
 constexpr uint32_t kPartBytes = kNB * kM * 4;       // the CTA's f32 partial tile (split-K)
@@ -69,9 +70,10 @@ struct Params {
 };
 
 __host__ __device__ constexpr uint32_t b_bytes(int kc) { return (uint32_t)kN * (uint32_t)kc * 2u; }
-// dynamic shared memory: B | A[0] | A[1] | int8 ring | partial tile
+// dynamic shared memory, from its first 1024-byte boundary: A[0] | A[1] | B | int8 ring |
+// partial tile (the swizzled A buffers need 1024-byte alignment)
 __host__ __device__ constexpr uint32_t smem_bytes(int kc) {
-  return b_bytes(kc) + 2 * kABytes + kRing * kI8Bytes + kPartBytes;
+  return 1024 + 2 * kABytes + b_bytes(kc) + kRing * kI8Bytes + kPartBytes;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -81,6 +83,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)_
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+// The same for the K-major 128-byte-swizzled layout: 8-row x 128-byte atoms, 1024 bytes
+// apart (sbo); within an atom the 16-byte chunk j of row i sits at chunk j ^ i.  The
+// leading offset is unused for this layout (set to 16 bytes).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
+         (2ull << 61);
 }
 // Instruction descriptor, kind::f16: f32 accumulator, f16 A and B, both K-major, N, M.
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
@@ -184,8 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
   const int64_t k0 = (int64_t)rank * kc;
   const int nst = kc / kKT;  // stages per tile
   const int64_t total = my_tiles * nst;
-  uint8_t* Bs = smem;
-  uint8_t* ring = smem + b_bytes(kc) + 2 * kABytes;
+  uint8_t* const abase = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);  // A[0], 1024-aligned
+  uint8_t* Bs = abase + 2 * kABytes;
+  uint8_t* ring = Bs + b_bytes(kc);
   float* part = reinterpret_cast<float*>(ring + kRing * kI8Bytes);  // [kNB][kM]
   const uint32_t bsbo = (uint32_t)(kc / 8) * kCoreBytes;
   const uint32_t full0 = smem_u32(&bar_full[0]), empty0 = smem_u32(&bar_empty[0]);
@@ -370,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
       if (g >= 2 && !bad) {
         if (!mbar_wait(empty0 + 8 * buf, (uint32_t)((g - 2) >> 1) & 1u)) bad = true;  // A[buf] free
       }
-      uint8_t* A = smem + b_bytes(kc) + (uint32_t)buf * kABytes;
+      uint8_t* A = abase + (uint32_t)buf * kABytes;
       const uint8_t* slot = ring + slot_i * kI8Bytes;
       // all of this thread's chunks are read before any is written: the stores to A must
       // not order the next chunk's load behind them
@@ -387,9 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
           i8x4_to_h2x2(q[j].z, h1.x, h1.y);
           i8x4_to_h2x2(q[j].w, h1.z, h1.w);
         }
-        uint8_t* dst = A + (r >> 3) * kASbo + (2 * k16) * kCoreBytes + (r & 7) * 16;
-        *reinterpret_cast<uint4*>(dst) = h0;
-        *reinterpret_cast<uint4*>(dst + kCoreBytes) = h1;
+        // 128-byte swizzle: 16-byte chunk j of row r at chunk j ^ (r & 7) of the row's span
+        uint8_t* rowp = A + (r >> 3) * kASbo + (r & 7) * 128;
+        *reinterpret_cast<uint4*>(rowp + (((2 * k16) ^ (r & 7)) << 4)) = h0;
+        *reinterpret_cast<uint4*>(rowp + (((2 * k16 + 1) ^ (r & 7)) << 4)) = h1;
       }
       fence_proxy_async();
       mbar_arrive(full0 + 8 * buf);
@@ -415,11 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
       if (!bad && !mbar_wait(full0 + 8 * buf, (uint32_t)(g >> 1) & 1u)) bad = true;
       if (bad) break;
       fence_after_sync();
-      const uint32_t a0 = smem_u32(smem + b_bytes(kc) + (uint32_t)buf * kABytes);
+      const uint32_t a0 = smem_u32(abase + (uint32_t)buf * kABytes);
       const uint32_t b0 = smem_u32(Bs) + (uint32_t)(s * kKT / 8) * kCoreBytes;
 #pragma unroll
       for (int kk = 0; kk < kKT / 16; ++kk)
-        mma_f16(taddr + (uint32_t)(32 * acc), smem_desc(a0 + kk * 2 * kCoreBytes, kCoreBytes, kASbo),
+        mma_f16(taddr + (uint32_t)(32 * acc), smem_desc_sw128(a0 + kk * 32, kASbo),
                 smem_desc(b0 + kk * 2 * kCoreBytes, kCoreBytes, bsbo), (s > 0 || kk > 0) ? 1u : 0u);
       mma_commit(empty0 + 8 * buf);
       if (s == nst - 1) mma_commit(done0 + 8 * acc);
