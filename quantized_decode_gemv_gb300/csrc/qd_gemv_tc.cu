@@ -41,8 +41,15 @@ constexpr int kM = 128;       // weight rows per tile (the MMA's M)
 constexpr int kN = 32;        // B columns: 16 sequences x (high, low)
 constexpr int kNB = 16;       // sequences
 constexpr int kKT = 64;       // K elements per pipeline stage
-constexpr int kConv = 128;    // converter / epilogue threads (warps 0-3)
-constexpr int kThreads = kConv + 32;  // + the MMA warp
+#ifndef QD_TC_CONV_WARPS
+#define QD_TC_CONV_WARPS 8
+#endif
+constexpr int kConvWarps = QD_TC_CONV_WARPS;  // converter warps; warps 0-3 also read the accumulators
+constexpr int kConv = 32 * kConvWarps;        // converter threads
+constexpr int kEpi = 128;                     // accumulator readout threads (TMEM lanes 0-127)
+constexpr int kMmaWarp = kConvWarps;          // the warp after the converters
+constexpr int kThreads = kConv + 32;
+static_assert(kConvWarps == 4 || kConvWarps == 8, "converter warps");
 constexpr int kMaxKc = 2048;  // K elements per CTA at most (shared memory for B)
 constexpr int kRing = 5;      // int8 weight stages in the cp.async ring
 constexpr int kEpiDelay = 2;  // stages into the next tile before the previous one is read out
@@ -171,7 +178,7 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& h01, uint32_t
   h23 = *reinterpret_cast<uint32_t*>(&hb);
 }
 
-__device__ __forceinline__ void conv_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void conv_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConv) : "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
   namespace cg = cooperative_groups;
@@ -201,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
   const uint32_t full0 = smem_u32(&bar_full[0]), empty0 = smem_u32(&bar_empty[0]);
   const uint32_t done0 = smem_u32(&bar_done[0]), drained0 = smem_u32(&bar_drained[0]);
 
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
                  "r"(kTmemCols)
                  : "memory");
@@ -212,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
       mbar_init(full0 + 8 * i, kConv);
       mbar_init(empty0 + 8 * i, 1);
       mbar_init(done0 + 8 * i, 1);
-      mbar_init(drained0 + 8 * i, kConv);
+      mbar_init(drained0 + 8 * i, kEpi);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -221,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
   fence_after_sync();
   const uint32_t taddr = tmem_base;
 
-  if (warp < 4) {
+  if (warp < kConvWarps) {
     // ======================= converter / epilogue warps =======================
     bool bad = false;
     const uint32_t ring_s = smem_u32(ring);
@@ -256,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
     // The epilogue of local tile t: wait for its accumulator, read it out (row 32 warp +
     // lane), release the accumulator, then finish the row (S == 1) or park the partial.
     auto epilogue = [&](int64_t t) {
+      if (warp >= 4) return;  // warps 0-3 map onto the accumulator's 128 lanes
       const int acc = (int)(t & 1);
       const int64_t row0 = (first + t * stride) * kM;
       const bool ok = mbar_wait(done0 + 8 * acc, (uint32_t)(t >> 1) & 1u);
@@ -298,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
 
     // ---- B: per sequence, the largest |x| of this CTA's columns, then the scaled high and
     // low f16 parts in the canonical layout (row n = sequence n high, 16 + n low)
-    for (int b = warp; b < kNB; b += 4) {
+    for (int b = warp; b < kNB; b += kConvWarps) {
       float m = 0.f;
       if (b < p.batch) {
         const float4* xr = reinterpret_cast<const float4*>(p.x + (int64_t)b * p.cols + k0);
@@ -446,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
   // [rank * R, (rank+1) * R) of its (single) tile
   if (S > 1) {
     cluster.sync();  // every CTA's partial is in place
-    if (warp < 4 && my_tiles == 1) {
+    if (warp < kConvWarps && my_tiles == 1) {
       const int R = kM / S;
       const int64_t row0 = first * kM;
       for (int i = tid; i < kNB * R; i += kConv) {
@@ -473,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
   }
   fence_before_sync();
   __syncthreads();
-  if (warp == 4) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kTmemCols)
+  if (warp == kMmaWarp) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kTmemCols)
                               : "memory");
 }
 
