@@ -122,9 +122,20 @@ struct Params {
 
 // kGemvQKV: rows r (even) and r+1 of batch b hold a RoPE pair (q or k) or two
 // consecutive v values; rotate and scatter them (see QkvEpilogue).
-__device__ __forceinline__ void qkv_pair_out(const Params& p, int64_t r, int b, float a, float bb) {
+// The epilogue's own inputs for one writer lane of a group, loaded right after the
+// dependency wait (or when the previous group ends) so their latency overlaps the
+// prologue and the main loop: the old y (accumulate), the position and the RoPE
+// (cos, sin) of the row pair (QKV).
+struct EpiPrefetch {
+  float y_old = 0.f;
+  int pos = -1;
+  float2 cs = make_float2(1.f, 0.f);
+};
+
+__device__ __forceinline__ void qkv_pair_out(const Params& p, int64_t r, int b, float a, float bb,
+                                             const EpiPrefetch& pf) {
   const QkvEpilogue& e = p.qkv;
-  const int pos = e.pos[b];
+  const int pos = pf.pos;
   if (pos < 0 || pos >= e.max_ctx) {
     if (p.err) atomicOr(p.err, kErrPosition);
     return;
@@ -137,7 +148,7 @@ __device__ __forceinline__ void qkv_pair_out(const Params& p, int64_t r, int b, 
     const int pi = (int)(local % hd) / 2;
     const int d0 = e.pairing == QD_ROPE_HALF ? pi : 2 * pi;
     const int d1 = e.pairing == QD_ROPE_HALF ? pi + half : 2 * pi + 1;
-    const float2 cs = *reinterpret_cast<const float2*>(e.rope + ((int64_t)pos * half + pi) * 2);
+    const float2 cs = pf.cs;
     const float o0 = a * cs.x - bb * cs.y, o1 = a * cs.y + bb * cs.x;
     float* dst = isq ? e.q_out + (int64_t)b * e.q_stride + h * hd
                      : e.kc + (int64_t)b * e.cache_batch_stride + (h * e.max_ctx + pos) * hd;
@@ -151,6 +162,29 @@ __device__ __forceinline__ void qkv_pair_out(const Params& p, int64_t r, int b, 
     dst[d] = a;
     dst[d + 1] = bb;
   }
+}
+
+// Prefetch for the writer lane of group g (lanes with lane % grp == 0 write value
+// k = lane / grp: row g * RW + k / NB, batch row k % NB).
+template <int NB, int RW>
+__device__ __forceinline__ EpiPrefetch epi_prefetch(const Params& p, int64_t g, int lane) {
+  constexpr int V = RW * NB, GRP = 32 / V;
+  EpiPrefetch pf;
+  const int kk = lane / GRP, rr = kk / NB, b = kk % NB;
+  const int64_t r = g * RW + rr;
+  if ((lane % GRP) != 0 || b >= p.batch || r >= p.W.rows) return pf;
+  if (p.mode == kGemvAccumulate) {
+    pf.y_old = __ldcg(p.y + (int64_t)b * p.W.rows + r);
+  } else if (p.mode == kGemvQKV) {
+    const QkvEpilogue& e = p.qkv;
+    pf.pos = __ldcg(e.pos + b);
+    if ((rr & 1) == 0 && r < e.q_rows + e.k_rows && pf.pos >= 0 && pf.pos < e.max_ctx) {
+      const int64_t local = r < e.q_rows ? r : r - e.q_rows;
+      const int pi = (int)(local % e.head_dim) / 2;
+      pf.cs = __ldg(reinterpret_cast<const float2*>(e.rope + ((int64_t)pf.pos * (e.head_dim / 2) + pi) * 2));
+    }
+  }
+  return pf;
 }
 
 // Row pointers (codes, scales) of the RW rows of a group; rows past the end repeat
@@ -391,6 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
   for (int k = 0; k < kStages - 1; ++k) issue(k);
 
   pdl_wait();  // x is the previous kernel's output
+  EpiPrefetch pf;
+  if (gw < groups) pf = epi_prefetch<NB, RW>(p, gw, lane);
 
   // ---- x * g as 24-bit integer records (see the header comment).  Eight lanes build
   // one unit: lane k < 4 takes elements 4k..4k+3 of half A, lane k >= 4 those of half
@@ -542,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
           if ((rr & 1) == 0 && r + 1 < W.rows)
             p.y[(int64_t)b * (W.rows / 2) + r / 2] = tot / (1.0f + expf(-tot)) * partner;
         } else if (p.mode == kGemvQKV) {
-          if ((rr & 1) == 0 && r + 1 < W.rows) qkv_pair_out(p, r, b, tot, partner);
+          if ((rr & 1) == 0 && r + 1 < W.rows) qkv_pair_out(p, r, b, tot, partner, pf);
         } else {
           if (p.mode == kGemvArgmax) {
             const unsigned long long key = argmax_key(tot, (uint32_t)r);
@@ -551,14 +587,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
               if (bb == b) best[bb] = key > best[bb] ? key : best[bb];
           }
           float* dst = p.y + (int64_t)b * W.rows + r;
-          if (p.mode == kGemvAccumulate)
-            *dst += tot;
-          else
-            *dst = tot;
+          *dst = p.mode == kGemvAccumulate ? pf.y_old + tot : tot;
         }
       }
     }
     g += nw;
+    if (g < groups) pf = epi_prefetch<NB, RW>(p, g, lane);
   }
   cp_wait<0>();  // no copy may still target this CTA's shared memory at exit
   if (p.mode == kGemvArgmax) {
