@@ -440,14 +440,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
       float ss = 0.f;
       if (b < p.batch) {
         const float* xr = p.x + (int64_t)b * cols;
-        for (int ub = warp * 4; ub < units; ub += kWarps * 4) {  // uniform per warp
-          const int u = ub + (lane >> 3);
-          const bool ok = u < units;
-          const int e = k < 4 ? unit_xa<FMT>(u) + 4 * k : unit_xb<FMT>(u) + 4 * (k - 4);
-          float4 v = ok ? __ldcg(reinterpret_cast<const float4*>(xr + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        // one unit record from this lane's 4 elements v (gains g)
+        auto record = [&](int u, bool ok, float4 v, float4 g) {
           if (p.norm_g) {
             ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
-            const float4 g = ok ? __ldg(reinterpret_cast<const float4*>(p.norm_g + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
             v = make_float4(v.x * g.x, v.y * g.y, v.z * g.z, v.w * g.w);
           }
           float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
@@ -498,6 +494,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
             meta = make_float4(sc, sv, __shfl_xor_sync(0xffffffffu, sv, 4), 0.f);
           }
           if (ok && k == 0) *reinterpret_cast<float4*>(rec + 96) = meta;
+        };
+        auto load = [&](int u, float4& v, float4& g) {
+          const bool ok = u < units;
+          const int e = k < 4 ? unit_xa<FMT>(u) + 4 * k : unit_xb<FMT>(u) + 4 * (k - 4);
+          v = ok ? __ldcg(reinterpret_cast<const float4*>(xr + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          g = ok && p.norm_g ? __ldg(reinterpret_cast<const float4*>(p.norm_g + e)) : make_float4(1.f, 1.f, 1.f, 1.f);
+        };
+        constexpr int kPass = kWarps * 4;  // units per pass of the CTA
+        if (units <= kPass) {
+          if (warp * 4 < units) {  // uniform per warp
+            const int u = warp * 4 + (lane >> 3);
+            float4 v, g;
+            load(u, v, g);
+            record(u, u < units, v, g);
+          }
+        } else {
+          // kBatch passes of this warp at once: their loads are issued before any is used
+          constexpr int kBatch = 4;
+          for (int ub0 = warp * 4; ub0 < units; ub0 += kBatch * kPass) {  // uniform per warp
+            float4 vv[kBatch], gg[kBatch];
+#pragma unroll
+            for (int t = 0; t < kBatch; ++t) load(ub0 + t * kPass + (lane >> 3), vv[t], gg[t]);
+#pragma unroll
+            for (int t = 0; t < kBatch; ++t) {
+              if (ub0 + t * kPass >= units) break;  // uniform per warp
+              const int u = ub0 + t * kPass + (lane >> 3);
+              record(u, u < units, vv[t], gg[t]);
+            }
+          }
         }
       }
       if (p.norm_g) {

@@ -121,16 +121,18 @@ struct AttnLayout {
   static constexpr int D = kHeadDim / L;    // key dims per lane
 };
 
-template <int G>
+template <int G, int DEP>
 __device__ __forceinline__ void attn_tiles(const float* kb, const float* vb, int p_begin, int p_end, int warp,
                                            int lane, const float (&qs)[G][AttnLayout<G>::D], float (&m)[G],
                                            float (&l)[G], float2 (&o)[G]) {
   using A = AttnLayout<G>;
   constexpr int L = A::L, P = A::P, D = A::D;
   constexpr int kTile = kAttnWarps * P;
+  // DEP tiles in flight per warp: the rows of DEP tiles load while one is used (a
+  // register ring with static slots)
   const int j = lane % L, pi = lane / L;  // this lane's dim slice and position in the warp tile
-  float4 kr[D / 4], kn[D / 4];
-  float2 vr[P], vn[P];
+  float4 kr[DEP][D / 4];
+  float2 vr[DEP][P];
   auto load = [&](int tile, float4 (&kd)[D / 4], float2 (&vd)[P]) {
     const int p = min(tile + warp * P + pi, p_end - 1);
     const float4* krow = reinterpret_cast<const float4*>(kb + (int64_t)p * kHeadDim + j * D);
@@ -142,11 +144,8 @@ __device__ __forceinline__ void attn_tiles(const float* kb, const float* vb, int
       vd[i] = __ldcg(reinterpret_cast<const float2*>(vb + (int64_t)pv * kHeadDim) + lane);
     }
   };
-  if (p_begin >= p_end) return;
-  load(p_begin, kr, vr);
-  for (int tile = p_begin; tile < p_end; tile += kTile) {
-    const bool more = tile + kTile < p_end;
-    if (more) load(tile + kTile, kn, vn);
+  // one tile: scores, online-softmax update, weighted values
+  auto use = [&](int tile, const float4 (&kd)[D / 4], const float2 (&vd)[P]) {
     const bool live = tile + warp * P + pi < p_end;  // this lane's position exists
     const int nvalid = min(P, max(0, p_end - tile - warp * P));  // positions of this warp's tile
 #pragma unroll
@@ -154,10 +153,10 @@ __device__ __forceinline__ void attn_tiles(const float* kb, const float* vb, int
       float sc = 0.f;
 #pragma unroll
       for (int t = 0; t < D / 4; ++t) {
-        sc = fmaf(qs[g][4 * t], kr[t].x, sc);
-        sc = fmaf(qs[g][4 * t + 1], kr[t].y, sc);
-        sc = fmaf(qs[g][4 * t + 2], kr[t].z, sc);
-        sc = fmaf(qs[g][4 * t + 3], kr[t].w, sc);
+        sc = fmaf(qs[g][4 * t], kd[t].x, sc);
+        sc = fmaf(qs[g][4 * t + 1], kd[t].y, sc);
+        sc = fmaf(qs[g][4 * t + 2], kd[t].z, sc);
+        sc = fmaf(qs[g][4 * t + 3], kd[t].w, sc);
       }
 #pragma unroll
       for (int off = 1; off < L; off <<= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
@@ -177,18 +176,25 @@ __device__ __forceinline__ void attn_tiles(const float* kb, const float* vb, int
       for (int i = 0; i < P; ++i) {
         const float wi = __shfl_sync(0xffffffffu, w, i * L);
         if (i < nvalid) {
-          acc.x = fmaf(wi, vr[i].x, acc.x);
-          acc.y = fmaf(wi, vr[i].y, acc.y);
+          acc.x = fmaf(wi, vd[i].x, acc.x);
+          acc.y = fmaf(wi, vd[i].y, acc.y);
         }
       }
       o[g] = acc;
       m[g] = mn;
     }
-    if (more) {
+  };
+  if (p_begin >= p_end) return;
 #pragma unroll
-      for (int t = 0; t < D / 4; ++t) kr[t] = kn[t];
+  for (int d = 0; d < DEP; ++d)
+    if (p_begin + d * kTile < p_end) load(p_begin + d * kTile, kr[d], vr[d]);
+  for (int base = p_begin; base < p_end; base += DEP * kTile) {
 #pragma unroll
-      for (int i = 0; i < P; ++i) vr[i] = vn[i];
+    for (int d = 0; d < DEP; ++d) {
+      const int tile = base + d * kTile;
+      if (tile >= p_end) break;
+      use(tile, kr[d], vr[d]);
+      if (tile + DEP * kTile < p_end) load(tile + DEP * kTile, kr[d], vr[d]);  // refill this slot
     }
   }
 }
@@ -240,7 +246,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_partial(
   }
   const float* kb = kc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
   const float* vb = vc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
-  attn_tiles<G>(kb, vb, p_begin, p_end, warp, lane, qs, m, l, o);
+  attn_tiles<G, 2>(kb, vb, p_begin, p_end, warp, lane, qs, m, l, o);
   // merge the warps of this CTA
   __shared__ float sm[kAttnWarps][kMaxGroup], sl[kAttnWarps][kMaxGroup];
   __shared__ float2 so[kAttnWarps][kMaxGroup][32];
@@ -306,7 +312,7 @@ __global__ void k_attn_merge(const float* __restrict__ ws_ml, const float* __res
 // fences).  After one cluster barrier that CTA merges the S partials (the same
 // log-sum-exp merge, in chunk order) and writes the output.
 constexpr int kMaxCluster = 8;
-template <int G>
+template <int G, int DEP>
 __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_cluster(
     const float* __restrict__ q, int64_t q_stride, const float* __restrict__ kc, const float* __restrict__ vc,
     int64_t cache_batch_stride, int n_heads, const int32_t* __restrict__ pos, int max_ctx, float scale,
@@ -343,7 +349,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_cluster(
   }
   const float* kb = kc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
   const float* vb = vc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
-  attn_tiles<G>(kb, vb, p_begin, p_end, warp, lane, qs, m, l, o);
+  attn_tiles<G, DEP>(kb, vb, p_begin, p_end, warp, lane, qs, m, l, o);
 
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -584,17 +590,19 @@ qd_status launch_attention(const float* q, int64_t q_stride, const float* kc, co
 // CTAs per cluster for the decode-step attention: enough clusters x CTAs to cover the
 // SMs a few times over, at most 8 (the portable cluster size) and at most one CTA per
 // 32 positions of the cache.
-int attn_cluster_size(int n_kv, int batch, int max_ctx) {
+int attn_sm_count() {
   static int sms[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  int nsm = 152;
-  if (dev >= 0 && dev < 64) {
-    if (!sms[dev] && (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-                      sms[dev] <= 0))
-      sms[dev] = 152;
-    nsm = sms[dev];
-  }
+  if (dev < 0 || dev >= 64) return 152;
+  if (!sms[dev] && (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                    sms[dev] <= 0))
+    sms[dev] = 152;
+  return sms[dev];
+}
+
+int attn_cluster_size(int n_kv, int batch, int max_ctx) {
+  const int nsm = attn_sm_count();
   const int pairs = n_kv * batch;
   const int target = 4 * nsm;
   int s = 1;
@@ -622,11 +630,15 @@ qd_status launch_attention_cluster(const float* q, int64_t q_stride, const float
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-#define QD_ATTN_CLUSTER(GG)                                                                                  \
-  case GG:                                                                                                   \
-    return cudaLaunchKernelEx(&cfg, k_attn_cluster<GG>, q, q_stride, kc, vc, cache_batch_stride, n_heads, pos, \
-                              max_ctx, scale, out, err) == cudaSuccess                                       \
-               ? QD_OK                                                                                       \
+  // four tiles in flight when a tile is small (one or two q heads per kv head) and the
+  // CTAs still fit in one wave at two per SM; two otherwise
+  const bool deep = G <= 2 && (int64_t)S * n_kv * batch <= 2 * attn_sm_count();
+#define QD_ATTN_CLUSTER(GG)                                                                                 \
+  case GG:                                                                                                  \
+    return cudaLaunchKernelEx(&cfg, (GG <= 2 && deep) ? k_attn_cluster<GG, 4> : k_attn_cluster<GG, 2>, q,   \
+                              q_stride, kc, vc, cache_batch_stride, n_heads, pos, max_ctx, scale, out, err) == \
+                   cudaSuccess                                                                              \
+               ? QD_OK                                                                                      \
                : QD_ERR_CUDA;
   switch (G) {
     QD_ATTN_CLUSTER(1)
