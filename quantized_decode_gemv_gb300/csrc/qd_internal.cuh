@@ -300,6 +300,9 @@ qd_status launch_qkv_post(const float* qkv, int64_t qkv_stride, int batch, const
                           cudaStream_t stream, bool pdl);
 // Attention with the split merge done by the last CTA of each (sequence, kv head);
 // `counters` (batch*n_kv unsigned ints) must be zero and are left zero.
+// Cluster size and SM count used by the decode-step attention launchers.
+int attn_cluster_size(int n_kv, int batch, int max_ctx);
+int attn_sm_count();
 qd_status launch_attention_cluster(const float* q, int64_t q_stride, const float* kc, const float* vc,
                                    int64_t cache_batch_stride, float* out, int n_heads, int n_kv, int head_dim,
                                    const int32_t* pos, int max_ctx, int batch, uint32_t* err, cudaStream_t stream,

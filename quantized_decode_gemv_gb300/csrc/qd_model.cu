@@ -178,7 +178,7 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
       ++n;
       return launch_q_gemv(a, st);
     }
-    QD_TRY(launch_rmsnorm(x, gains, xn, (int)D, batch, c.eps, st));
+    QD_TRY(launch_rmsnorm(a.x, gains, xn, (int)D, batch, c.eps, st));
     a.x = xn;
     n += 2;
     return launch_q_gemv(a, st);
