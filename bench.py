@@ -348,6 +348,14 @@ def run_ours(args, world, rank, local):
         dist.destroy_process_group()
 
 
+def gemv_source_sha() -> str:
+    """sha256 over the streaming GEMV's sources (the kernel and its integer-dot header)."""
+    h = hashlib.sha256()
+    for f in ("qd_gemv_stream.cu", "qd_intdot.cuh"):
+        h.update(open(os.path.join(ROOT, "quantized_decode_gemv_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
 def profile_traffic(summary: str):
     """Per-launch DRAM bytes from a committed ncu summary under profiles/, or None when the
     GEMV kernel source changed since the counters were taken."""
@@ -357,8 +365,7 @@ def profile_traffic(summary: str):
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     h = re.search(r"source_sha256:\s*([0-9a-f]{16,64})", text)
-    src = os.path.join(ROOT, "quantized_decode_gemv_gb300", "csrc", "qd_gemv_stream.cu")
-    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    cur = gemv_source_sha()
     if not m or not h or not cur.startswith(h.group(1)):
         return None
     return float(m.group(1))
@@ -417,17 +424,17 @@ def gemv_sweep(qd, torch, stream, hbm, args):
     return res
 
 
-def bench_1p7b(qd, torch, stream, args, hbm):
+def bench_1p7b(qd, torch, stream, args, hbm, batches=(1, 16), layers=None):
     """1.7B-shaped INT8 step at context 4096 (pos 4095): batch 1 and 16, cache entries N(0,1)
     drawn on the device with a seeded torch generator (timing only; the parity tests use the
     host generator)."""
     import qdsynth
 
-    cfg = qdsynth.SMOL_1_7B
+    cfg = qdsynth.SMOL_1_7B if not layers else dict(qdsynth.SMOL_1_7B, layers=layers)
     ctx = 4096
     host = qdsynth.model_tensors(cfg, 0)
     out = {}
-    for batch in (1, 16):
+    for batch in batches:
         srcs = [None if t is None else torch.from_numpy(np.ascontiguousarray(t)).cuda() for t in host]
         m = qd.Model(qd.make_config(cfg, ctx, batch), srcs)
         torch.cuda.synchronize()
@@ -574,6 +581,23 @@ def run_gemv_only(spec: str, reps: int):
     print(json.dumps(out))
 
 
+def run_1p7b_only(spec: str, layers=None):
+    """The 1.7B-shaped INT8 step alone at the given batches ("1", "16" or "1,16"), optionally
+    with fewer layers (a small case for profiling); prints one JSON line (not the benchmark
+    contract line)."""
+    import torch
+
+    import quantized_decode_gemv_gb300 as qd
+
+    if not os.path.exists(qd.LIB_PATH):
+        qd.build()
+    qd.load()
+    stream = torch.cuda.current_stream()
+    hbm, _, kind = peaks()
+    res = bench_1p7b(qd, torch, stream, None, hbm, tuple(int(b) for b in spec.split(",")), layers)
+    print(json.dumps({"decode_1p7b": res, "layers": layers, "peak": hbm, "peak_kind": kind}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -587,9 +611,14 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--gemv", default=None, help="microbenchmark one shape, FMT:ROWSxCOLS:BATCH")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--decode-1p7b", default=None, help="the 1.7B-shaped step alone, at batches e.g. 1,16")
+    ap.add_argument("--layers", type=int, default=None, help="with --decode-1p7b: fewer layers (profiling)")
     args = ap.parse_args(argv)
     if args.gemv:
         run_gemv_only(args.gemv, args.reps)
+        return
+    if args.decode_1p7b:
+        run_1p7b_only(args.decode_1p7b, args.layers)
         return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

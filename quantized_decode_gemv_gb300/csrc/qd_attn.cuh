@@ -13,8 +13,8 @@ constexpr int kMaxGroup = 8;
 
 constexpr int kMaxCluster = 8;
 
-// Walk of positions [p_begin, p_end) by the CTA's warps in tiles: warp w takes
-// positions tile + w * P + i (i < P) of each tile of kAttnWarps * P positions.
+// Walk of positions [p_begin, p_end) by the CTA's W warps in tiles: warp w takes
+// positions tile + w * P + i (i < P) of each tile of W * P positions.
 //  * scores: L lanes share one position, lane j holding dims [j * 64/L, (j+1) * 64/L)
 //    of its key row and of every q head; the dot is finished with log2(L) shuffles.
 //    Scores are in log2 units (q was pre-scaled by log2(e) / sqrt(head_dim)).
@@ -30,13 +30,13 @@ struct AttnLayout {
   static constexpr int D = kHeadDim / L;    // key dims per lane
 };
 
-template <int G, int DEP>
+template <int G, int DEP, int W = kAttnWarps>
 __device__ __forceinline__ void attn_tiles(const float* kb, const float* vb, int p_begin, int p_end, int warp,
                                            int lane, const float (&qs)[G][AttnLayout<G>::D], float (&m)[G],
                                            float (&l)[G], float2 (&o)[G]) {
   using A = AttnLayout<G>;
   constexpr int L = A::L, P = A::P, D = A::D;
-  constexpr int kTile = kAttnWarps * P;
+  constexpr int kTile = W * P;
   // DEP tiles in flight per warp: the rows of DEP tiles load while one is used (a
   // register ring with static slots)
   const int j = lane % L, pi = lane / L;  // this lane's dim slice and position in the warp tile

@@ -1,0 +1,470 @@
+// Split-KV decode attention with a flat, even split, for long walks over the cache
+// (llmoxide blog s5 and dasLLAMA 8.7.1.6.2 attention: scores q.k / sqrt(head_dim),
+// softmax over positions 0..pos, weighted sum of the value rows).
+//
+// The cluster kernel gives each (sequence, kv head) pair S <= 8 CTAs.  When the pairs are
+// few and the walks long (32 kv heads at batch 1 and context 4096: 32 pairs of 4096
+// positions, 67 MB of f32 cache per layer) that grid cannot cover 152 SMs evenly, and the
+// walk must keep enough bytes in flight per SM to run at HBM speed.  Here:
+//  * every pair's positions 0..pos are cut into tiles of 64 positions; the tiles of all
+//    pairs are laid end to end (sequence-major, then kv head) and CTA i of a grid of C
+//    CTAs (one per SM) takes tiles [floor(i T / C), floor((i+1) T / C)), so every SM
+//    streams the same number of bytes whatever the pair count;
+//  * a tile's key rows and value rows are each one contiguous run of the cache (64 rows
+//    of 256 bytes).  One thread of a producer warp copies them into a ring of NS stages
+//    in shared memory with two bulk copies (cp.async.bulk, completion counted in bytes on
+//    the stage's "full" mbarrier), up to NS tiles ahead; eight consumer warps take 8
+//    positions each of every tile and release the stage on its "empty" mbarrier;
+//  * scores: 8 lanes per key row (8 dims each, three shuffles), 4 rows per step; one
+//    online-softmax update per tile and q head (log2 units: q is pre-scaled by
+//    log2(e) / sqrt(head_dim)); values: lane j holds dims 2j, 2j+1 of the output;
+//  * at the end of each pair in its run, a CTA merges its warps' states and stores them
+//    as its partial (m, l, o) for that pair in a global workspace, then counts itself in
+//    on the pair's arrival counter; the CTA that completes the count merges the pair's
+//    partials in CTA order (the same log-sum-exp merge, so the result does not depend on
+//    arrival order), writes the output and sets the counter back to zero for the next
+//    launch.  No CTA waits for another.
+// Every mbarrier wait is bounded: on a timeout the kernel sets kErrTimeout, stops
+// waiting and computing (its output is then undefined) and still reaches every barrier.
+#include <cmath>
+
+#include "qd_attn.cuh"
+
+namespace qd {
+namespace {
+
+using namespace attn;
+
+constexpr int kFlatWarps = 8;                       // consumer warps
+constexpr int kFlatRows = 8;                        // positions per consumer warp per tile
+constexpr int kFlatTile = kFlatWarps * kFlatRows;   // positions per tile
+constexpr int kFlatHalf = kFlatTile * kHeadDim;     // floats of one tile's key (or value) rows
+constexpr int kFlatStageBytes = 2 * kFlatHalf * 4;  // 32 KB: key rows, then value rows
+constexpr int kFlatStages = 4;
+constexpr int kFlatThreads = (kFlatWarps + 1) * 32;  // + the producer warp
+constexpr int kPartFloats = 2 + kHeadDim;            // one head's partial: m, l, o[64]
+constexpr uint32_t kFlatSpinLimit = 1u << 24;        // test_wait polls per wait (about a second)
+
+__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+  asm volatile(
+      "{\n"
+      ".reg .b64 st;\n"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n"
+      "}\n" ::"r"(mbar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile(
+      "{\n"
+      ".reg .b64 st;\n"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n"
+      "}\n" ::"r"(mbar),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+  for (uint32_t i = 0; i < kFlatSpinLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+// `bytes` (a multiple of 16) from global `src` to shared `dst`, counted on `mbar`
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+}
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kFlatWarps * 32) : "memory");
+}
+
+struct Cursor {
+  int b, kvh, tt;  // sequence, kv head, tile of that pair
+};
+
+template <int G, int NS>
+__global__ void __launch_bounds__(kFlatThreads, 1)
+    k_attn_flat(const float* __restrict__ q, int64_t q_stride, const float* __restrict__ kc,
+                const float* __restrict__ vc, int64_t cache_batch_stride, int n_heads, int n_kv,
+                const int32_t* __restrict__ pos, int max_ctx, int batch, float scale, float* __restrict__ out,
+                float* __restrict__ ws, unsigned int* __restrict__ cnt, uint32_t* err) {
+  constexpr int W = kFlatWarps;
+  extern __shared__ __align__(128) float ring[];  // [NS][key rows | value rows]
+  __shared__ __align__(8) uint64_t full_bar[NS], empty_bar[NS];
+  __shared__ int s_n[QD_MAX_BATCH], s_tiles[QD_MAX_BATCH];
+  __shared__ int64_t s_off[QD_MAX_BATCH + 1];  // tiles before sequence b (all its kv heads)
+  __shared__ float sm[W][G], sl[W][G];
+  __shared__ float2 so[W][G][32];
+  __shared__ int s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
+  const uint32_t full0 = (uint32_t)__cvta_generic_to_shared(full_bar);
+  const uint32_t empty0 = (uint32_t)__cvta_generic_to_shared(empty_bar);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, W);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // Before the dependency wait: the positions (advanced by the previous step) and every
+  // cache row before them (written by earlier steps) are final once this kernel runs,
+  // because each kernel of the step lets its successor launch only after its own wait, so
+  // the kernel two launches back has completed.  q and the row at each position come
+  // from the QKV projection that precedes this kernel.
+  if (threadIdx.x < batch) {
+    const int p = pos[threadIdx.x];
+    const bool ok = p >= 0 && p < max_ctx;
+    s_n[threadIdx.x] = ok ? p + 1 : 0;
+    s_tiles[threadIdx.x] = ok ? p / kFlatTile + 1 : 0;
+    if (!ok && err && blockIdx.x == 0) atomicOr(err, kErrPosition);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int64_t a = 0;
+    for (int b = 0; b < batch; ++b) {
+      s_off[b] = a;
+      a += (int64_t)s_tiles[b] * n_kv;
+    }
+    s_off[batch] = a;
+  }
+  __syncthreads();
+  const int64_t T = s_off[batch];
+  const int64_t C = min((int64_t)gridDim.x, T);  // CTAs with work: each gets >= 1 tile
+  if ((int64_t)blockIdx.x >= C || warp < W) {
+    pdl_wait();     // q and the rows at the current positions come from the QKV projection
+    pdl_trigger();  // let the next kernel start its weight prefetch
+    // a sequence whose position is out of range has no tiles: its rows are zeros
+    for (int b = 0; b < batch; ++b)
+      if (s_n[b] == 0 && b % (int)gridDim.x == (int)blockIdx.x && warp < W)
+        for (int t = threadIdx.x; t < n_heads * kHeadDim; t += W * 32)
+          out[(int64_t)b * n_heads * kHeadDim + t] = 0.f;
+  }
+  if ((int64_t)blockIdx.x >= C) return;
+  const int64_t t_begin = (int64_t)blockIdx.x * T / C, t_end = ((int64_t)blockIdx.x + 1) * T / C;
+  const int nst = (int)(t_end - t_begin);
+  auto advance = [&](Cursor& c) {
+    if (++c.tt == s_tiles[c.b]) {
+      c.tt = 0;
+      if (++c.kvh == n_kv) {
+        c.kvh = 0;
+        do {
+          ++c.b;
+        } while (c.b < batch && s_tiles[c.b] == 0);
+      }
+    }
+  };
+  Cursor start;
+  {
+    int b = 0;
+    while (b + 1 < batch && s_off[b + 1] <= t_begin) ++b;
+    const int64_t rem = t_begin - s_off[b];
+    start = Cursor{b, (int)(rem / s_tiles[b]), (int)(rem % s_tiles[b])};
+  }
+
+  if (warp == W) {
+    // ---- producer: one thread copies tile after tile into the ring, starting before the
+    // dependency wait; it waits only before a pair's last tile (the row the QKV
+    // projection appends)
+    if (lane == 0) {
+      Cursor c = start;
+      int slot = 0, issued = 0;
+      uint32_t use = 0;  // completed uses of this slot before this one
+      bool waited = false;
+      for (int s = 0; s < nst; ++s) {
+        if (use > 0 && !mbar_wait(empty0 + 8 * slot, (use - 1) & 1u)) {
+          if (err) atomicOr(err, kErrTimeout);
+          break;  // the consumers then time out on this stage's full barrier
+        }
+        if (!waited && c.tt == s_tiles[c.b] - 1) {
+          pdl_wait();
+          waited = true;
+        }
+        const int p0 = c.tt * kFlatTile;
+        const int rows = min(kFlatTile, s_n[c.b] - p0);
+        const int64_t off =
+            (int64_t)c.b * cache_batch_stride + ((int64_t)c.kvh * max_ctx + p0) * kHeadDim;  // row p0 of the pair
+        const uint32_t bytes = (uint32_t)rows * kHeadDim * 4;
+        const uint32_t dst = ring_s + (uint32_t)slot * kFlatStageBytes;
+        mbar_arrive_expect_tx(full0 + 8 * slot, 2 * bytes);
+        bulk_copy(dst, kc + off, bytes, full0 + 8 * slot);
+        bulk_copy(dst + kFlatHalf * 4, vc + off, bytes, full0 + 8 * slot);
+        ++issued;
+        advance(c);
+        if (++slot == NS) {
+          slot = 0;
+          ++use;
+        }
+      }
+      // stay until the last copy into each slot has landed: no copy may target the
+      // CTA's shared memory after it exits
+      for (int k = max(0, issued - NS); k < issued; ++k)
+        if (!mbar_wait(full0 + 8 * (k % NS), (uint32_t)(k / NS) & 1u) && err) atomicOr(err, kErrTimeout);
+    }
+    return;
+  }
+
+  // ---- consumers
+  auto cta_of = [&](int64_t x) { return (int)(((x + 1) * C + T - 1) / T - 1); };  // CTA holding tile x
+  const int j = lane & 7, pi = lane >> 3;  // dim slice (dims 4j.., 32+4j..) and row of a step
+  float qs[G][8];
+  float m[G], l[G];
+  float2 o[G];
+  auto start_pair = [&](const Cursor& c) {
+    const float* qb = q + (int64_t)c.b * q_stride + (int64_t)c.kvh * G * kHeadDim;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(qb + g * kHeadDim + 4 * j));
+      const float4 bq = __ldcg(reinterpret_cast<const float4*>(qb + g * kHeadDim + 32 + 4 * j));
+      qs[g][0] = a.x * scale;
+      qs[g][1] = a.y * scale;
+      qs[g][2] = a.z * scale;
+      qs[g][3] = a.w * scale;
+      qs[g][4] = bq.x * scale;
+      qs[g][5] = bq.y * scale;
+      qs[g][6] = bq.z * scale;
+      qs[g][7] = bq.w * scale;
+      m[g] = -INFINITY;
+      l[g] = 0.f;
+      o[g] = make_float2(0.f, 0.f);
+    }
+  };
+  // this warp's 8 positions of the tile in `slot`; rows past the pair's last position hold
+  // stale data and are masked out of both the scores and the values
+  auto use_tile = [&](int slot, const Cursor& c) {
+    const float* kt = ring + slot * (kFlatStageBytes / 4) + warp * kFlatRows * kHeadDim;
+    const float* vt = kt + kFlatHalf;
+    const int live_rows = s_n[c.b] - c.tt * kFlatTile - warp * kFlatRows;  // may be <= 0 or > 8
+    const bool live0 = pi < live_rows, live1 = 4 + pi < live_rows;
+    const float4 k0a = *reinterpret_cast<const float4*>(kt + pi * kHeadDim + 4 * j);
+    const float4 k0b = *reinterpret_cast<const float4*>(kt + pi * kHeadDim + 32 + 4 * j);
+    const float4 k1a = *reinterpret_cast<const float4*>(kt + (4 + pi) * kHeadDim + 4 * j);
+    const float4 k1b = *reinterpret_cast<const float4*>(kt + (4 + pi) * kHeadDim + 32 + 4 * j);
+    float2 v[kFlatRows];
+#pragma unroll
+    for (int i = 0; i < kFlatRows; ++i) v[i] = *reinterpret_cast<const float2*>(vt + i * kHeadDim + 2 * lane);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float s0 = qs[g][0] * k0a.x;
+      s0 = fmaf(qs[g][1], k0a.y, s0);
+      s0 = fmaf(qs[g][2], k0a.z, s0);
+      s0 = fmaf(qs[g][3], k0a.w, s0);
+      s0 = fmaf(qs[g][4], k0b.x, s0);
+      s0 = fmaf(qs[g][5], k0b.y, s0);
+      s0 = fmaf(qs[g][6], k0b.z, s0);
+      s0 = fmaf(qs[g][7], k0b.w, s0);
+      float s1 = qs[g][0] * k1a.x;
+      s1 = fmaf(qs[g][1], k1a.y, s1);
+      s1 = fmaf(qs[g][2], k1a.z, s1);
+      s1 = fmaf(qs[g][3], k1a.w, s1);
+      s1 = fmaf(qs[g][4], k1b.x, s1);
+      s1 = fmaf(qs[g][5], k1b.y, s1);
+      s1 = fmaf(qs[g][6], k1b.z, s1);
+      s1 = fmaf(qs[g][7], k1b.w, s1);
+#pragma unroll
+      for (int off = 1; off < 8; off <<= 1) {
+        s0 += __shfl_xor_sync(0xffffffffu, s0, off);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+      }
+      s0 = live0 ? s0 : -INFINITY;
+      s1 = live1 ? s1 : -INFINITY;
+      float tm = fmaxf(s0, s1);
+      tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+      tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+      const float mn = fmaxf(m[g], tm);
+      const float corr = m[g] == mn ? 1.f : exp2f(m[g] - mn);
+      const float w0 = live0 ? exp2f(s0 - mn) : 0.f;
+      const float w1 = live1 ? exp2f(s1 - mn) : 0.f;
+      float wsum = w0 + w1;  // the 8 lanes of a row hold the same weights: sum across rows only
+      wsum += __shfl_xor_sync(0xffffffffu, wsum, 8);
+      wsum += __shfl_xor_sync(0xffffffffu, wsum, 16);
+      l[g] = fmaf(l[g], corr, wsum);
+      float2 acc = make_float2(o[g].x * corr, o[g].y * corr);
+#pragma unroll
+      for (int i = 0; i < kFlatRows; ++i) {
+        const float wi = __shfl_sync(0xffffffffu, i < 4 ? w0 : w1, (i & 3) * 8);
+        if (i < live_rows) {
+          acc.x = fmaf(wi, v[i].x, acc.x);
+          acc.y = fmaf(wi, v[i].y, acc.y);
+        }
+      }
+      o[g] = acc;
+      m[g] = mn;
+    }
+  };
+  // end of this CTA's part of pair c: store the CTA partial, count in, and merge the
+  // pair if this CTA completes it
+  auto finish_pair = [&](const Cursor& c) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if (lane == 0) {
+        sm[warp][g] = m[g];
+        sl[warp][g] = l[g];
+      }
+      so[warp][g][lane] = o[g];
+    }
+    consumers_sync();
+    const int pair = c.b * n_kv + c.kvh;
+    const int64_t first = s_off[c.b] + (int64_t)c.kvh * s_tiles[c.b];
+    const int i0 = cta_of(first), i1 = cta_of(first + s_tiles[c.b] - 1);
+    for (int g = warp; g < G; g += W) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int w2 = 0; w2 < W; ++w2) mx = fmaxf(mx, sm[w2][g]);
+      float lt = 0.f;
+      float2 ot = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int w2 = 0; w2 < W; ++w2) {
+        const float f = sm[w2][g] == -INFINITY ? 0.f : exp2f(sm[w2][g] - mx);
+        lt = fmaf(sl[w2][g], f, lt);
+        ot.x = fmaf(so[w2][g][lane].x, f, ot.x);
+        ot.y = fmaf(so[w2][g][lane].y, f, ot.y);
+      }
+      float* part = ws + ((int64_t)(blockIdx.x + pair) * G + g) * kPartFloats;  // slot i + pair
+      if (lane == 0) {
+        part[0] = mx;
+        part[1] = lt;
+      }
+      reinterpret_cast<float2*>(part + 2)[lane] = ot;
+    }
+    __threadfence();
+    consumers_sync();
+    if (threadIdx.x == 0) s_last = atomicAdd(cnt + pair, 1u) == (unsigned)(i1 - i0);
+    consumers_sync();
+    if (s_last) {
+      __threadfence();
+      for (int g = warp; g < G; g += W) {
+        float mx = -INFINITY;
+        for (int i = i0; i <= i1; ++i) mx = fmaxf(mx, __ldcg(ws + ((int64_t)(i + pair) * G + g) * kPartFloats));
+        float lt = 0.f;
+        float2 acc = make_float2(0.f, 0.f);
+        for (int i = i0; i <= i1; ++i) {
+          const float* part = ws + ((int64_t)(i + pair) * G + g) * kPartFloats;
+          const float f = exp2f(__ldcg(part) - mx);  // every CTA of the pair saw >= 1 position
+          lt = fmaf(__ldcg(part + 1), f, lt);
+          const float2 po = __ldcg(reinterpret_cast<const float2*>(part + 2) + lane);
+          acc.x = fmaf(po.x, f, acc.x);
+          acc.y = fmaf(po.y, f, acc.y);
+        }
+        float2* dst = reinterpret_cast<float2*>(out + ((int64_t)c.b * n_heads + c.kvh * G + g) * kHeadDim);
+        dst[lane] = make_float2(acc.x / lt, acc.y / lt);
+      }
+      if (threadIdx.x == 0) cnt[pair] = 0u;
+    }
+    consumers_sync();  // sm, sl, so and s_last are reused by the next pair
+  };
+
+  Cursor cc = start, cur{-1, -1, 0};
+  bool bad = false;
+  int slot = 0;
+  uint32_t use = 0;
+  for (int s = 0; s < nst; ++s) {
+    if (!bad && !mbar_wait(full0 + 8 * slot, use & 1u)) {
+      bad = true;
+      if (err && lane == 0) atomicOr(err, kErrTimeout);
+    }
+    if (cc.b != cur.b || cc.kvh != cur.kvh) {
+      if (cur.b >= 0) finish_pair(cur);
+      cur = cc;
+      start_pair(cc);
+    }
+    if (!bad) use_tile(slot, cc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * slot);  // this warp is done with the slot
+    advance(cc);
+    if (++slot == NS) {
+      slot = 0;
+      ++use;
+    }
+  }
+  if (cur.b >= 0) finish_pair(cur);
+}
+
+template <int G>
+cudaError_t launch_flat_g(cudaLaunchConfig_t& cfg, const float* q, int64_t q_stride, const float* kc,
+                          const float* vc, int64_t cache_batch_stride, int n_heads, int n_kv, const int32_t* pos,
+                          int max_ctx, int batch, float scale, float* out, float* ws, unsigned int* cnt,
+                          uint32_t* err) {
+  constexpr int NS = kFlatStages;
+  auto kern = k_attn_flat<G, NS>;
+  const int smem = NS * kFlatStageBytes;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!done[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  cfg.blockDim = dim3(kFlatThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  return cudaLaunchKernelEx(&cfg, kern, q, q_stride, kc, vc, cache_batch_stride, n_heads, n_kv, pos, max_ctx, batch,
+                            scale, out, ws, cnt, err);
+}
+
+}  // namespace
+
+int attn_flat_ctas() { return attn_sm_count(); }
+
+size_t attn_flat_ws_floats(int n_heads, int n_kv, int batch, int ctas) {
+  const int G = n_heads / n_kv;
+  return (size_t)(ctas + n_kv * batch) * G * kPartFloats;
+}
+
+bool attn_use_flat(int n_kv, int batch, int max_ctx) {
+  // f32 key and value rows of every pair at full context: 512 bytes per position
+  return (int64_t)n_kv * batch * max_ctx * 2 * kHeadDim * 4 >= kAttnFlatMinBytes;
+}
+
+qd_status launch_attention_flat(const float* q, int64_t q_stride, const float* kc, const float* vc,
+                                int64_t cache_batch_stride, float* out, int n_heads, int n_kv, int head_dim,
+                                const int32_t* pos, int max_ctx, int batch, int ctas, float* ws, unsigned int* cnt,
+                                uint32_t* err, cudaStream_t stream, bool pdl) {
+  if (head_dim != kHeadDim || n_kv < 1 || n_heads % n_kv || batch < 1 || batch > QD_MAX_BATCH || ctas < 1)
+    return QD_ERR_SHAPE;
+  const int G = n_heads / n_kv;
+  const float scale = 1.4426950408889634f / sqrtf((float)head_dim);  // scores in log2 units
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t rc = cudaErrorInvalidValue;
+#define QD_FLAT_G(GG)                                                                                            \
+  case GG:                                                                                                       \
+    rc = launch_flat_g<GG>(cfg, q, q_stride, kc, vc, cache_batch_stride, n_heads, n_kv, pos, max_ctx, batch, scale, \
+                           out, ws, cnt, err);                                                                   \
+    break;
+  switch (G) {
+    QD_FLAT_G(1)
+    QD_FLAT_G(2)
+    QD_FLAT_G(3)
+    QD_FLAT_G(4)
+    QD_FLAT_G(5)
+    QD_FLAT_G(6)
+    QD_FLAT_G(7)
+    QD_FLAT_G(8)
+    default: return QD_ERR_UNSUPPORTED;
+  }
+#undef QD_FLAT_G
+  return rc == cudaSuccess ? QD_OK : QD_ERR_CUDA;
+}
+
+}  // namespace qd

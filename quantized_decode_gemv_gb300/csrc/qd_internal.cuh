@@ -298,14 +298,26 @@ qd_status launch_repack_rows(int fmt, const void* src, int64_t n_rows, int64_t c
 // packed-order projection qkv[b][rows] and does the rotation, q write and cache append.
 qd_status launch_qkv_post(const float* qkv, int64_t qkv_stride, int batch, const QkvEpilogue& e, uint32_t* err,
                           cudaStream_t stream, bool pdl);
-// Attention with the split merge done by the last CTA of each (sequence, kv head);
-// `counters` (batch*n_kv unsigned ints) must be zero and are left zero.
-// Cluster size and SM count used by the decode-step attention launchers.
+// Decode-step attention, one thread-block cluster per (sequence, kv head).  Cluster
+// size and SM count used by its launcher.
 int attn_cluster_size(int n_kv, int batch, int max_ctx);
 int attn_sm_count();
 qd_status launch_attention_cluster(const float* q, int64_t q_stride, const float* kc, const float* vc,
                                    int64_t cache_batch_stride, float* out, int n_heads, int n_kv, int head_dim,
                                    const int32_t* pos, int max_ctx, int batch, uint32_t* err, cudaStream_t stream,
                                    bool pdl);
+// Decode-step attention for long walks: an even split of all pairs' positions over one
+// CTA per SM (attn_flat_ctas), partials merged by the last CTA of each (sequence, kv
+// head).  `ws` holds attn_flat_ws_floats(..., ctas) floats for the same `ctas`; `cnt`
+// (batch * n_kv unsigned ints) must be zero and is left zero.  attn_use_flat picks it when the f32 cache of all pairs at full context holds at
+// least kAttnFlatMinBytes.
+constexpr int64_t kAttnFlatMinBytes = 8ll << 20;
+bool attn_use_flat(int n_kv, int batch, int max_ctx);
+int attn_flat_ctas();
+size_t attn_flat_ws_floats(int n_heads, int n_kv, int batch, int ctas);
+qd_status launch_attention_flat(const float* q, int64_t q_stride, const float* kc, const float* vc,
+                                int64_t cache_batch_stride, float* out, int n_heads, int n_kv, int head_dim,
+                                const int32_t* pos, int max_ctx, int batch, int ctas, float* ws, unsigned int* cnt,
+                                uint32_t* err, cudaStream_t stream, bool pdl);
 
 }  // namespace qd

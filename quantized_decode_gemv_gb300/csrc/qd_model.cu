@@ -34,6 +34,9 @@ struct Layout {
   // state
   size_t kc, vc, x, xn, qkv, q, att, act, logits, am_key, am_cnt, tok_in, tok_out, pos, err,
       rope;
+  size_t attn_ws, attn_cnt;  // flat-split attention: partials and per-pair counters
+  bool attn_flat;
+  int attn_ctas;  // its grid (one CTA per SM), fixed with the workspace size
   size_t state_bytes;
   int64_t qkv_rows, cache_batch_stride, cache_layer_stride;
 };
@@ -101,6 +104,10 @@ Layout make_layout(const qd_config* c) {
   L.pos = take(4 * B);
   L.err = take(4);
   L.rope = take((size_t)c->max_ctx * c->head_dim * 4);
+  L.attn_flat = attn_use_flat(c->n_kv_heads, c->max_batch, c->max_ctx);
+  L.attn_ctas = attn_flat_ctas();
+  L.attn_ws = L.attn_flat ? take(4 * attn_flat_ws_floats(c->n_heads, c->n_kv_heads, c->max_batch, L.attn_ctas)) : 0;
+  L.attn_cnt = L.attn_flat ? take(4 * (size_t)c->n_kv_heads * c->max_batch) : 0;
   L.state_bytes = off;
   return L;
 }
@@ -212,8 +219,13 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
       QD_TRY(launch_qkv_post(qkv, L.qkv_rows, batch, e, err, st, true));
       ++n;
     }
-    QD_TRY(launch_attention_cluster(q, QD, kc, vc, L.cache_batch_stride, att, c.n_heads, c.n_kv_heads, c.head_dim,
-                                    pos, c.max_ctx, batch, err, st, true));
+    if (L.attn_flat)
+      QD_TRY(launch_attention_flat(q, QD, kc, vc, L.cache_batch_stride, att, c.n_heads, c.n_kv_heads, c.head_dim, pos,
+                                   c.max_ctx, batch, L.attn_ctas, m->f(L.attn_ws),
+                                   reinterpret_cast<unsigned int*>(m->s + L.attn_cnt), err, st, true));
+    else
+      QD_TRY(launch_attention_cluster(q, QD, kc, vc, L.cache_batch_stride, att, c.n_heads, c.n_kv_heads,
+                                      c.head_dim, pos, c.max_ctx, batch, err, st, true));
     ++n;
     QD_TRY(launch_q_gemv(args(c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, x, kGemvAccumulate), st));
     ++n;

@@ -194,8 +194,8 @@ __global__ void k_attn_merge(const float* __restrict__ ws_ml, const float* __res
 // cluster's first CTA (distributed shared memory, no global workspace, atomics or
 // fences).  After one cluster barrier that CTA merges the S partials (the same
 // log-sum-exp merge, in chunk order) and writes the output.
-template <int G, int DEP>
-__global__ void __launch_bounds__(kAttnWarps * 32) k_attn_cluster(
+template <int G, int DEP, int W>
+__global__ void __launch_bounds__(W * 32) k_attn_cluster(
     const float* __restrict__ q, int64_t q_stride, const float* __restrict__ kc, const float* __restrict__ vc,
     int64_t cache_batch_stride, int n_heads, const int32_t* __restrict__ pos, int max_ctx, float scale,
     float* __restrict__ out, uint32_t* err) {
@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_cluster(
   const int rank = (int)cluster.block_rank();
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ float sm[kAttnWarps][kMaxGroup], sl[kAttnWarps][kMaxGroup];
-  __shared__ float2 so[kAttnWarps][kMaxGroup][32];
+  __shared__ float sm[W][kMaxGroup], sl[W][kMaxGroup];
+  __shared__ float2 so[W][kMaxGroup][32];
   // filled in the first CTA of the cluster by every CTA: partial of CTA r for head g
   __shared__ float pm[kMaxCluster][kMaxGroup], pl[kMaxCluster][kMaxGroup];
   __shared__ float2 po[kMaxCluster][kMaxGroup][32];
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_cluster(
   }
   const float* kb = kc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
   const float* vb = vc + (int64_t)b * cache_batch_stride + (int64_t)kvh * max_ctx * kHeadDim;
-  attn_tiles<G, DEP>(kb, vb, p_begin, p_end, warp, lane, qs, m, l, o);
+  attn_tiles<G, DEP, W>(kb, vb, p_begin, p_end, warp, lane, qs, m, l, o);
 
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -245,14 +245,14 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_cluster(
   float* rpm = cluster.map_shared_rank(&pm[0][0], 0);
   float* rpl = cluster.map_shared_rank(&pl[0][0], 0);
   float2* rpo = cluster.map_shared_rank(&po[0][0][0], 0);
-  for (int g = warp; g < G; g += kAttnWarps) {
+  for (int g = warp; g < G; g += W) {
     float mx = -INFINITY;
 #pragma unroll
-    for (int w2 = 0; w2 < kAttnWarps; ++w2) mx = fmaxf(mx, sm[w2][g]);
+    for (int w2 = 0; w2 < W; ++w2) mx = fmaxf(mx, sm[w2][g]);
     float lt = 0.f;
     float2 ot = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int w2 = 0; w2 < kAttnWarps; ++w2) {
+    for (int w2 = 0; w2 < W; ++w2) {
       const float f = (sm[w2][g] == -INFINITY) ? 0.f : exp2f(sm[w2][g] - mx);
       lt = fmaf(sl[w2][g], f, lt);
       ot.x = fmaf(so[w2][g][lane].x, f, ot.x);
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_cluster(
   }
   cluster.sync();  // the partials have landed in the first CTA
   if (rank != 0) return;
-  for (int g = warp; g < G; g += kAttnWarps) {
+  for (int g = warp; g < G; g += W) {
     const int h = kvh * G + g;
     float2* dst = reinterpret_cast<float2*>(out + ((int64_t)b * n_heads + h) * kHeadDim);
     float mr[kMaxCluster];
@@ -492,6 +492,34 @@ int attn_cluster_size(int n_kv, int batch, int max_ctx) {
   return s;
 }
 
+// Warps per CTA and tiles in flight per warp for the cluster attention.  Four tiles in
+// flight when a tile is small (one or two q heads per kv head) and the CTAs still fit in
+// one wave at two per SM; two otherwise.
+struct AttnPlan {
+  int warps, dep;
+};
+
+AttnPlan attn_plan(int G, int S, int n_kv, int batch) {
+  const bool deep = G <= 2 && (int64_t)S * n_kv * batch <= 2 * attn_sm_count();
+  return AttnPlan{kAttnWarps, deep ? 4 : 2};
+}
+
+template <int G>
+cudaError_t launch_attn_cluster_g(cudaLaunchConfig_t& cfg, const AttnPlan& plan, const float* q, int64_t q_stride,
+                                  const float* kc, const float* vc, int64_t cache_batch_stride, int n_heads,
+                                  const int32_t* pos, int max_ctx, float scale, float* out, uint32_t* err) {
+  if constexpr (G <= 2) {
+    if (plan.warps == 8)
+      return cudaLaunchKernelEx(&cfg, plan.dep == 4 ? k_attn_cluster<G, 4, 8> : k_attn_cluster<G, 2, 8>, q, q_stride,
+                                kc, vc, cache_batch_stride, n_heads, pos, max_ctx, scale, out, err);
+    return cudaLaunchKernelEx(&cfg, plan.dep == 4 ? k_attn_cluster<G, 4, 4> : k_attn_cluster<G, 2, 4>, q, q_stride,
+                              kc, vc, cache_batch_stride, n_heads, pos, max_ctx, scale, out, err);
+  } else {
+    return cudaLaunchKernelEx(&cfg, k_attn_cluster<G, 2, 4>, q, q_stride, kc, vc, cache_batch_stride, n_heads, pos,
+                              max_ctx, scale, out, err);
+  }
+}
+
 qd_status launch_attention_cluster(const float* q, int64_t q_stride, const float* kc, const float* vc,
                                    int64_t cache_batch_stride, float* out, int n_heads, int n_kv, int head_dim,
                                    const int32_t* pos, int max_ctx, int batch, uint32_t* err, cudaStream_t stream,
@@ -501,7 +529,6 @@ qd_status launch_attention_cluster(const float* q, int64_t q_stride, const float
   const float scale = 1.4426950408889634f / sqrtf((float)head_dim);  // scores in log2 units
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)S, (unsigned)n_kv, (unsigned)batch);
-  cfg.blockDim = dim3(kAttnWarps * 32);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -512,28 +539,27 @@ qd_status launch_attention_cluster(const float* q, int64_t q_stride, const float
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  // four tiles in flight when a tile is small (one or two q heads per kv head) and the
-  // CTAs still fit in one wave at two per SM; two otherwise
-  const bool deep = G <= 2 && (int64_t)S * n_kv * batch <= 2 * attn_sm_count();
-#define QD_ATTN_CLUSTER(GG)                                                                                 \
-  case GG:                                                                                                  \
-    return cudaLaunchKernelEx(&cfg, (GG <= 2 && deep) ? k_attn_cluster<GG, 4> : k_attn_cluster<GG, 2>, q,   \
-                              q_stride, kc, vc, cache_batch_stride, n_heads, pos, max_ctx, scale, out, err) == \
-                   cudaSuccess                                                                              \
-               ? QD_OK                                                                                      \
-               : QD_ERR_CUDA;
+  const AttnPlan plan = attn_plan(G, S, n_kv, batch);
+  cfg.blockDim = dim3((unsigned)plan.warps * 32);
+  cudaError_t rc = cudaErrorInvalidValue;
+#define QD_ATTN_G(GG)                                                                                         \
+  case GG:                                                                                                    \
+    rc = launch_attn_cluster_g<GG>(cfg, plan, q, q_stride, kc, vc, cache_batch_stride, n_heads, pos, max_ctx, scale, \
+                                   out, err);                                                                 \
+    break;
   switch (G) {
-    QD_ATTN_CLUSTER(1)
-    QD_ATTN_CLUSTER(2)
-    QD_ATTN_CLUSTER(3)
-    QD_ATTN_CLUSTER(4)
-    QD_ATTN_CLUSTER(5)
-    QD_ATTN_CLUSTER(6)
-    QD_ATTN_CLUSTER(7)
-    QD_ATTN_CLUSTER(8)
+    QD_ATTN_G(1)
+    QD_ATTN_G(2)
+    QD_ATTN_G(3)
+    QD_ATTN_G(4)
+    QD_ATTN_G(5)
+    QD_ATTN_G(6)
+    QD_ATTN_G(7)
+    QD_ATTN_G(8)
     default: return QD_ERR_UNSUPPORTED;
   }
-#undef QD_ATTN_CLUSTER
+#undef QD_ATTN_G
+  return rc == cudaSuccess ? QD_OK : QD_ERR_CUDA;
 }
 
 qd_status launch_qkv_post(const float* qkv, int64_t qkv_stride, int batch, const QkvEpilogue& e, uint32_t* err,

@@ -165,3 +165,56 @@ def test_smol1p7b_int8_ctx4096(qd, batch, check_seqs):
         check_token(ol, ot, int(out[b]))
         print(f"1.7B batch {batch} seq {b}: rel err {err:.2e}")
     m.close()
+
+
+def flat_cfg(n_heads, n_kv):
+    """A 2-layer model whose f32 cache at batch 4 and context 2048 holds >= 8 MiB over all
+    (sequence, kv head) pairs: the decode step takes the flat-split attention kernel."""
+    return dict(layers=2, dim=512, ffn=1024, n_heads=n_heads, n_kv_heads=n_kv, head_dim=64, vocab=300,
+                rope_theta=1e4, eps=1e-5, pairing="half", w_fmt="q8_0", emb_fmt="q8_0")
+
+
+FLAT_CTX, FLAT_BATCH = 2048, 4
+
+
+@pytest.mark.parametrize("n_heads,n_kv", [(8, 8), (8, 4), (12, 4), (16, 2)])
+def test_flat_attention_ragged_positions(qd, n_heads, n_kv):
+    """Four sequences at ragged positions over an N(0,1) cache: one at the last position
+    (2048 entries), one at position 0 (a single entry), one mid-context, one just past a
+    64-position tile edge; two consecutive steps, every sequence checked against the oracle.
+    On the second step the first sequence has run past the context: it is flagged and the
+    others are unaffected."""
+    cfg = flat_cfg(n_heads, n_kv)
+    m, host = build_model(qd, cfg, 21, FLAT_CTX, FLAT_BATCH)
+    fill_cache_normal(m, cfg, 21, FLAT_BATCH, FLAT_CTX)
+    start = [FLAT_CTX - 1, 0, 700, 64]
+    m.set_pos(start)
+    om = oracle.Model(dict(cfg, max_ctx=FLAT_CTX), host)
+    per = cfg["n_kv_heads"] * FLAT_CTX * cfg["head_dim"]
+    caches = [oracle_cache(cfg, 21, b, FLAT_BATCH, FLAT_CTX) for b in range(FLAT_BATCH)]
+    toks = qdsynth.tokens(21, "flat.tokens", 2 * FLAT_BATCH, cfg["vocab"]).astype(np.int32).reshape(2, FLAT_BATCH)
+    logits = torch.empty(FLAT_BATCH, cfg["vocab"], device="cuda")
+    out = torch.empty(FLAT_BATCH, dtype=torch.int32)
+    for step in range(2):
+        m.decode_step(torch.from_numpy(toks[step].copy()), FLAT_BATCH, out, logits)
+        torch.cuda.synchronize()
+        status = m.check()
+        assert status == (0 if step == 0 else 7), status  # 7: QD_ERR_DEVICE_FLAG
+        g = logits.cpu().numpy()
+        for b in range(FLAT_BATCH):
+            p = start[b] + step
+            if p >= FLAT_CTX:
+                continue
+            ol, ot = om.decode_step(caches[b][0], caches[b][1], per, p, int(toks[step, b]))
+            assert_close(g[b], ol, what=f"flat attention G={n_heads // n_kv} step {step} seq {b} pos {p}")
+            check_token(ol, ot, int(out[b]))
+    m.close()
+
+
+def test_flat_attention_teacher_forced_from_empty_cache(qd):
+    """The flat split from position 0 on (a handful of tiles over 152 CTAs: most CTAs idle,
+    several CTAs per pair only later), batch 2 at context 2048 with 8 kv heads."""
+    cfg = flat_cfg(8, 8)
+    prompt = qdsynth.tokens(22, "flat.prompt", 2 * 6, cfg["vocab"]).reshape(2, 6)
+    worst, near = run_teacher_forced(qd, cfg, 22, prompt, n_gen=4, batch=2, max_ctx=FLAT_CTX)
+    print(f"flat split from an empty cache: worst rel err {worst:.2e}, near-tie tokens {near}")
