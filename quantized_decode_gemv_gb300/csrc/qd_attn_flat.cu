@@ -18,10 +18,11 @@
 //  * scores: 8 lanes per key row (8 dims each, three shuffles), 4 rows per step; one
 //    online-softmax update per tile and q head (log2 units: q is pre-scaled by
 //    log2(e) / sqrt(head_dim)); values: lane j holds dims 2j, 2j+1 of the output;
-//  * at the end of each pair in its run, a CTA merges its warps' states and stores them
-//    as its partial (m, l, o) for that pair in a global workspace, then counts itself in
-//    on the pair's arrival counter; the CTA that completes the count merges the pair's
-//    partials in CTA order (the same log-sum-exp merge, so the result does not depend on
+//  * where its run leaves a pair, each warp stores its online-softmax state (m, l, o) as
+//    a partial in a global workspace and walks on, with no barrier; at the end of the run
+//    the CTA counts itself in on the arrival counter of every pair the run covered.  The
+//    CTA that completes a pair's count merges all of the pair's warp partials in a fixed
+//    order (CTA, then warp; the same log-sum-exp merge, so the result does not depend on
 //    arrival order), writes the output and sets the counter back to zero for the next
 //    launch.  No CTA waits for another.
 // Every mbarrier wait is bounded: on a timeout the kernel sets kErrTimeout, stops
@@ -43,6 +44,7 @@ constexpr int kFlatStageBytes = 2 * kFlatHalf * 4;  // 32 KB: key rows, then val
 constexpr int kFlatStages = 4;
 constexpr int kFlatThreads = (kFlatWarps + 1) * 32;  // + the producer warp
 constexpr int kPartFloats = 2 + kHeadDim;            // one head's partial: m, l, o[64]
+constexpr int kFlatSlotHeads = 8;  // parked (pair, head) warp states a CTA holds before settling them
 constexpr uint32_t kFlatSpinLimit = 1u << 24;        // test_wait polls per wait (about a second)
 
 __device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
@@ -87,6 +89,7 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_
                "l"(src), "r"(bytes), "r"(mbar)
                : "memory");
 }
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kFlatWarps * 32) : "memory");
 }
@@ -106,9 +109,7 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
   __shared__ __align__(8) uint64_t full_bar[NS], empty_bar[NS];
   __shared__ int s_n[QD_MAX_BATCH], s_tiles[QD_MAX_BATCH];
   __shared__ int64_t s_off[QD_MAX_BATCH + 1];  // tiles before sequence b (all its kv heads)
-  __shared__ float sm[W][G], sl[W][G];
-  __shared__ float2 so[W][G][32];
-  __shared__ int s_last;
+  __shared__ int s_pairs[kFlatSlotHeads], s_last[kFlatSlotHeads];  // pairs of this run not yet settled
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
   const uint32_t full0 = (uint32_t)__cvta_generic_to_shared(full_bar);
@@ -305,66 +306,142 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
       m[g] = mn;
     }
   };
-  // end of this CTA's part of pair c: store the CTA partial, count in, and merge the
-  // pair if this CTA completes it
-  auto finish_pair = [&](const Cursor& c) {
+  // Pairs this run has left and not yet settled: each warp parks its state for pair slot t
+  // in shared memory (slots after the ring: m[W][G], l[W][G], o[W][G][64] per slot).
+  constexpr int kSlots = kFlatSlotHeads / G > 0 ? kFlatSlotHeads / G : 1;
+  constexpr int kSlotFloats = W * G * kPartFloats;
+  float* slots = ring + NS * (kFlatStageBytes / 4);
+  int npairs = 0;  // the same in every consumer thread: all walk the same tiles
+  auto end_pair = [&](const Cursor& c) {
+    float* sl = slots + npairs * kSlotFloats;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       if (lane == 0) {
-        sm[warp][g] = m[g];
-        sl[warp][g] = l[g];
+        sl[warp * G + g] = m[g];
+        sl[W * G + warp * G + g] = l[g];
       }
-      so[warp][g][lane] = o[g];
+      reinterpret_cast<float2*>(sl + 2 * W * G + (warp * G + g) * kHeadDim)[lane] = o[g];
     }
-    consumers_sync();
-    const int pair = c.b * n_kv + c.kvh;
-    const int64_t first = s_off[c.b] + (int64_t)c.kvh * s_tiles[c.b];
-    const int i0 = cta_of(first), i1 = cta_of(first + s_tiles[c.b] - 1);
-    for (int g = warp; g < G; g += W) {
+    if (warp == 0 && lane == 0) s_pairs[npairs] = c.b * n_kv + c.kvh;
+    ++npairs;
+  };
+  auto pair_ctas = [&](int pair, int& i0, int& i1) {
+    const int b = pair / n_kv, kvh = pair % n_kv;
+    const int64_t first = s_off[b] + (int64_t)kvh * s_tiles[b];
+    i0 = cta_of(first);
+    i1 = cta_of(first + s_tiles[b] - 1);
+  };
+  // Settle the parked pairs: merge each pair's W warp states into this CTA's partial (m, l,
+  // o) in the global workspace (slot i + pair), count in on the pair's arrival counter,
+  // and, for each pair this CTA completes, merge the pair's CTA partials i0..i1 and write
+  // the output.  That merge is spread over the warps: warp w takes head w % G and the CTAs
+  // i0 + w / G, i0 + w / G + S, ... (S = W / G subsets), eight partials' loads at a time;
+  // the subsets are then combined in subset order.
+  auto settle = [&]() {
+    consumers_sync();  // every warp's parked states are in shared memory
+    const int np = npairs;
+    for (int it = warp; it < np * G; it += W) {
+      const int t = it / G, g = it % G;
+      const float* sl = slots + t * kSlotFloats;
       float mx = -INFINITY;
 #pragma unroll
-      for (int w2 = 0; w2 < W; ++w2) mx = fmaxf(mx, sm[w2][g]);
+      for (int w2 = 0; w2 < W; ++w2) mx = fmaxf(mx, sl[w2 * G + g]);
       float lt = 0.f;
       float2 ot = make_float2(0.f, 0.f);
 #pragma unroll
       for (int w2 = 0; w2 < W; ++w2) {
-        const float f = sm[w2][g] == -INFINITY ? 0.f : exp2f(sm[w2][g] - mx);
-        lt = fmaf(sl[w2][g], f, lt);
-        ot.x = fmaf(so[w2][g][lane].x, f, ot.x);
-        ot.y = fmaf(so[w2][g][lane].y, f, ot.y);
+        const float mw = sl[w2 * G + g];
+        const float f = mw == -INFINITY ? 0.f : exp2f(mw - mx);  // a warp may have seen no position
+        lt = fmaf(sl[W * G + w2 * G + g], f, lt);
+        const float2 ow = reinterpret_cast<const float2*>(sl + 2 * W * G + (w2 * G + g) * kHeadDim)[lane];
+        ot.x = fmaf(ow.x, f, ot.x);
+        ot.y = fmaf(ow.y, f, ot.y);
       }
-      float* part = ws + ((int64_t)(blockIdx.x + pair) * G + g) * kPartFloats;  // slot i + pair
+      float* part = ws + (((int64_t)blockIdx.x + s_pairs[t]) * G + g) * kPartFloats;
       if (lane == 0) {
         part[0] = mx;
         part[1] = lt;
       }
       reinterpret_cast<float2*>(part + 2)[lane] = ot;
     }
-    __threadfence();
+    consumers_sync();  // the CTA's partial stores are ordered before the counting threads' fences
+    if (threadIdx.x < np) {
+      int i0, i1;
+      pair_ctas(s_pairs[threadIdx.x], i0, i1);
+      fence_acq_rel_gpu();  // release: this CTA's partials before its count
+      s_last[threadIdx.x] = atomicAdd(cnt + s_pairs[threadIdx.x], 1u) == (unsigned)(i1 - i0);
+      fence_acq_rel_gpu();  // acquire: the partials of the CTAs counted before this one
+    }
     consumers_sync();
-    if (threadIdx.x == 0) s_last = atomicAdd(cnt + pair, 1u) == (unsigned)(i1 - i0);
-    consumers_sync();
-    if (s_last) {
-      __threadfence();
-      for (int g = warp; g < G; g += W) {
+    constexpr int S = W / G;  // CTA subsets per head in the final merge
+    for (int t = 0; t < np; ++t) {
+      if (!s_last[t]) continue;
+      const int pair = s_pairs[t];
+      int i0, i1;
+      pair_ctas(pair, i0, i1);
+      float* scratch = slots;  // [W][kPartFloats]: the parked states are no longer needed
+      if (warp < G * S) {
+        const int g = warp % G, sub = warp / G;
+        float mx = -INFINITY, lt = 0.f;
+        float2 acc = make_float2(0.f, 0.f);
+        for (int i = i0 + sub; i <= i1; i += 8 * S) {
+          float mk[8], lk[8];
+          float2 ok[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {  // the loads of eight partials, then their use
+            const int ii = i + u * S;
+            const float* part = ws + (((int64_t)(ii <= i1 ? ii : i) + pair) * G + g) * kPartFloats;
+            mk[u] = ii <= i1 ? __ldcg(part) : -INFINITY;
+            lk[u] = __ldcg(part + 1);
+            ok[u] = __ldcg(reinterpret_cast<const float2*>(part + 2) + lane);
+          }
+          float mb = mx;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mb = fmaxf(mb, mk[u]);
+          const float corr = mx == mb ? 1.f : exp2f(mx - mb);
+          lt *= corr;
+          acc.x *= corr;
+          acc.y *= corr;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float f = mk[u] == -INFINITY ? 0.f : exp2f(mk[u] - mb);
+            lt = fmaf(lk[u], f, lt);
+            acc.x = fmaf(ok[u].x, f, acc.x);
+            acc.y = fmaf(ok[u].y, f, acc.y);
+          }
+          mx = mb;
+        }
+        if (lane == 0) {
+          scratch[warp * kPartFloats] = mx;
+          scratch[warp * kPartFloats + 1] = lt;
+        }
+        reinterpret_cast<float2*>(scratch + warp * kPartFloats + 2)[lane] = acc;
+      }
+      consumers_sync();
+      if (warp < G) {
+        const int g = warp;
         float mx = -INFINITY;
-        for (int i = i0; i <= i1; ++i) mx = fmaxf(mx, __ldcg(ws + ((int64_t)(i + pair) * G + g) * kPartFloats));
+#pragma unroll
+        for (int sub = 0; sub < S; ++sub) mx = fmaxf(mx, scratch[(sub * G + g) * kPartFloats]);
         float lt = 0.f;
         float2 acc = make_float2(0.f, 0.f);
-        for (int i = i0; i <= i1; ++i) {
-          const float* part = ws + ((int64_t)(i + pair) * G + g) * kPartFloats;
-          const float f = exp2f(__ldcg(part) - mx);  // every CTA of the pair saw >= 1 position
-          lt = fmaf(__ldcg(part + 1), f, lt);
-          const float2 po = __ldcg(reinterpret_cast<const float2*>(part + 2) + lane);
-          acc.x = fmaf(po.x, f, acc.x);
-          acc.y = fmaf(po.y, f, acc.y);
+#pragma unroll
+        for (int sub = 0; sub < S; ++sub) {
+          const float* sp = scratch + (sub * G + g) * kPartFloats;
+          const float f = sp[0] == -INFINITY ? 0.f : exp2f(sp[0] - mx);  // a subset may be empty
+          lt = fmaf(sp[1], f, lt);
+          const float2 so2 = reinterpret_cast<const float2*>(sp + 2)[lane];
+          acc.x = fmaf(so2.x, f, acc.x);
+          acc.y = fmaf(so2.y, f, acc.y);
         }
-        float2* dst = reinterpret_cast<float2*>(out + ((int64_t)c.b * n_heads + c.kvh * G + g) * kHeadDim);
+        const int b = pair / n_kv, kvh = pair % n_kv;
+        float2* dst = reinterpret_cast<float2*>(out + ((int64_t)b * n_heads + kvh * G + g) * kHeadDim);
         dst[lane] = make_float2(acc.x / lt, acc.y / lt);
       }
       if (threadIdx.x == 0) cnt[pair] = 0u;
+      consumers_sync();  // the scratch is reused by the next pair
     }
-    consumers_sync();  // sm, sl, so and s_last are reused by the next pair
+    npairs = 0;
   };
 
   Cursor cc = start, cur{-1, -1, 0};
@@ -377,7 +454,10 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
       if (err && lane == 0) atomicOr(err, kErrTimeout);
     }
     if (cc.b != cur.b || cc.kvh != cur.kvh) {
-      if (cur.b >= 0) finish_pair(cur);
+      if (cur.b >= 0) {
+        end_pair(cur);
+        if (npairs == kSlots) settle();  // (short pairs: more in one run than the slots hold)
+      }
       cur = cc;
       start_pair(cc);
     }
@@ -390,7 +470,15 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
       ++use;
     }
   }
-  if (cur.b >= 0) finish_pair(cur);
+  if (cur.b >= 0) {
+    end_pair(cur);
+    settle();
+  }
+}
+
+// ring stages, then the parked warp states (at least one pair's worth)
+constexpr int flat_smem_bytes(int G, int NS) {
+  return NS * kFlatStageBytes + (kFlatSlotHeads / G > 0 ? kFlatSlotHeads / G : 1) * kFlatWarps * G * kPartFloats * 4;
 }
 
 template <int G>
@@ -400,7 +488,7 @@ cudaError_t launch_flat_g(cudaLaunchConfig_t& cfg, const float* q, int64_t q_str
                           uint32_t* err) {
   constexpr int NS = kFlatStages;
   auto kern = k_attn_flat<G, NS>;
-  const int smem = NS * kFlatStageBytes;
+  const int smem = flat_smem_bytes(G, NS);
   static bool done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);

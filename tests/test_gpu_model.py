@@ -218,3 +218,30 @@ def test_flat_attention_teacher_forced_from_empty_cache(qd):
     prompt = qdsynth.tokens(22, "flat.prompt", 2 * 6, cfg["vocab"]).reshape(2, 6)
     worst, near = run_teacher_forced(qd, cfg, 22, prompt, n_gen=4, batch=2, max_ctx=FLAT_CTX)
     print(f"flat split from an empty cache: worst rel err {worst:.2e}, near-tie tokens {near}")
+
+
+def test_flat_attention_many_short_pairs(qd):
+    """96 kv heads x 16 sequences at positions < 64: 1536 one-tile pairs over 152 CTAs, so
+    a CTA's run covers more pairs than it holds before settling them mid-run."""
+    cfg = dict(layers=1, dim=256, ffn=512, n_heads=96, n_kv_heads=96, head_dim=64, vocab=300, rope_theta=1e4,
+               eps=1e-5, pairing="adjacent", w_fmt="q8_0", emb_fmt="q8_0")
+    ctx, batch = 64, 16
+    m, host = build_model(qd, cfg, 23, ctx, batch)
+    fill_cache_normal(m, cfg, 23, batch, ctx)
+    start = [int(v) for v in qdsynth.tokens(23, "flat.short.pos", batch, ctx)]
+    m.set_pos(start)
+    toks = qdsynth.tokens(23, "flat.short.tokens", batch, cfg["vocab"]).astype(np.int32)
+    logits = torch.empty(batch, cfg["vocab"], device="cuda")
+    out = torch.empty(batch, dtype=torch.int32)
+    m.decode_step(torch.from_numpy(toks.copy()), batch, out, logits)
+    torch.cuda.synchronize()
+    assert m.check() == 0
+    g = logits.cpu().numpy()
+    om = oracle.Model(dict(cfg, max_ctx=ctx), host)
+    per = cfg["n_kv_heads"] * ctx * cfg["head_dim"]
+    for b in range(batch):
+        kc, vc = oracle_cache(cfg, 23, b, batch, ctx)
+        ol, ot = om.decode_step(kc, vc, per, start[b], int(toks[b]))
+        assert_close(g[b], ol, what=f"short pairs seq {b} pos {start[b]}")
+        check_token(ol, ot, int(out[b]))
+    m.close()
