@@ -18,13 +18,13 @@
 //  * scores: 8 lanes per key row (8 dims each, three shuffles), 4 rows per step; one
 //    online-softmax update per tile and q head (log2 units: q is pre-scaled by
 //    log2(e) / sqrt(head_dim)); values: lane j holds dims 2j, 2j+1 of the output;
-//  * where its run leaves a pair, each warp stores its online-softmax state (m, l, o) as
-//    a partial in a global workspace and walks on, with no barrier; at the end of the run
-//    the CTA counts itself in on the arrival counter of every pair the run covered.  The
-//    CTA that completes a pair's count merges all of the pair's warp partials in a fixed
-//    order (CTA, then warp; the same log-sum-exp merge, so the result does not depend on
-//    arrival order), writes the output and sets the counter back to zero for the next
-//    launch.  No CTA waits for another.
+//  * where its run leaves a pair, each warp parks its online-softmax state (m, l, o) in a
+//    shared-memory slot area and walks on, with no barrier.  At the end of the run the CTA
+//    merges its warps per pair, stores one partial per (CTA, pair) in a global workspace
+//    and counts itself in on the arrival counter of every pair the run covered.  The CTA
+//    that completes a pair's count merges that pair's CTA partials in CTA order (the same
+//    log-sum-exp merge, so the result does not depend on arrival order), writes the output
+//    and sets the counter back to zero for the next launch.  No CTA waits for another.
 // Every mbarrier wait is bounded: on a timeout the kernel sets kErrTimeout, stops
 // waiting and computing (its output is then undefined) and still reaches every barrier.
 #include <cmath>
