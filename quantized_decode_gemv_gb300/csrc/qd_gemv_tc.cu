@@ -11,16 +11,22 @@
 //    of the remainder, columns 0-15 high, 16-31 low.  hi + lo holds x to about 2^-22
 //    relative; the tensor core's products of f16 values are exact and sum in f32.  B is
 //    staged once per CTA in shared memory (K-major, no-swizzle canonical layout).
-//  * A (M = 128 rows x 16 K per instruction) is the weight tile.  Warp-specialised
-//    pipeline: four converter warps stream the int8 codes through a per-thread cp.async
-//    ring (each thread copies and later converts the same 16-byte chunks), convert them
-//    exactly to f16 (q ^ 0x80 placed in the mantissa of 1024, then 1152 subtracted) into
-//    one of two A buffers and arrive on its "full" mbarrier; one lane of the fifth warp
-//    waits for "full", issues the stage's MMAs and commits them to the buffer's "empty"
-//    mbarrier (which the converters wait for before reuse).  Tiles alternate between two
-//    accumulators in tensor memory; after a tile's last stage the MMA lane commits to the
-//    accumulator's "done" barrier, and the converter warps read it out (tcgen05.ld, one
-//    row per thread) a few stages into the next tile, then arrive on its "drained" barrier.
+//  * A (M = 128 rows x 16 K per instruction) is the weight tile, held in tensor memory
+//    (row r in lane r, two f16 per 32-bit column).  Warp-specialised pipeline over stages
+//    of 128 columns: eight converter warps stream the int8 codes through a per-thread
+//    cp.async ring; thread (w, l) owns row 32 (w % 4) + l of the tile (a warp reaches only
+//    its quarter of the tensor-memory lanes) and half of each stage: it copies its 64
+//    codes, converts them exactly to f16 (q ^ 0x80 placed in the mantissa of 1024, then
+//    1152 subtracted) and writes them with one tcgen05.st into one of seven A stages in
+//    tensor memory; each warp then arrives once on the stage's "full" mbarrier.  One lane
+//    of the ninth warp waits for "full", issues the stage's eight MMAs (A from tensor
+//    memory, B from shared memory) and commits them to the stage's "empty" mbarrier, which
+//    the converters wait for before refilling it.  (Per stage, the MMA lane and the
+//    converters each pay a fixed hand-off cost; 128-column stages halve it per byte.)
+//    Tiles alternate between two accumulators in tensor memory; after a tile's last stage
+//    the MMA lane commits to the accumulator's "done" barrier, and converter warps 0-3
+//    read it out (tcgen05.ld, one row per thread) a few stages into the next tile, then
+//    arrive on its "drained" barrier.
 //  * Many row tiles: one cluster-free CTA per SM walks tiles cta, cta + CTAs, ... with the
 //    weight ring running on across tiles.  Few row tiles: the columns split over up to 8
 //    CTAs of a thread-block cluster (one tile each); the partials are summed through
@@ -40,7 +46,7 @@ namespace tc_gemv {
 constexpr int kM = 128;       // weight rows per tile (the MMA's M)
 constexpr int kN = 32;        // B columns: 16 sequences x (high, low)
 constexpr int kNB = 16;       // sequences
-constexpr int kKT = 64;       // K elements per pipeline stage
+constexpr int kKT = 128;      // K elements per pipeline stage
 #ifndef QD_TC_CONV_WARPS
 #define QD_TC_CONV_WARPS 8
 #endif
@@ -54,15 +60,23 @@ constexpr int kMaxKc = 2048;  // K elements per CTA at most (shared memory for B
 constexpr int kRing = 5;      // int8 weight stages in the cp.async ring
 constexpr int kEpiDelay = 2;  // stages into the next tile before the previous one is read out
 constexpr int kMaxCluster = 8;
-constexpr uint32_t kTmemCols = 64;  // two 32-column accumulators
+// Tensor memory: two 32-column f32 accumulators, then kNA f16 A stages of kKT / 2 columns
+// (row r of the tile in lane r, two K elements per 32-bit column).
+constexpr int kNA = 7;
+constexpr uint32_t kAccCols = 64;
+constexpr uint32_t kACols = kKT / 2;
+constexpr uint32_t kTmemCols = 512;
+static_assert(kAccCols + kNA * kACols <= kTmemCols, "tensor memory columns");
 
 constexpr uint32_t kCoreBytes = 128;                // one 8 x 16-byte core matrix
-constexpr uint32_t kASbo = 8 * 2 * kKT;             // bytes between 8-row groups of A (one swizzle atom)
-static_assert(2 * kKT == 128, "an A row of a stage is one 128-byte swizzle span");
-constexpr uint32_t kABytes = kM * kKT * 2;          // one f16 A buffer
 constexpr uint32_t kI8Bytes = kM * kKT;             // one int8 weight stage
 constexpr uint32_t kPartBytes = kNB * kM * 4;       // the CTA's f32 partial tile (split-K)
 constexpr int kChunks = kM * kKT / 16 / kConv;      // 16-byte chunks per converter thread and stage
+// Converter thread (warp w, lane l) owns row 32 (w % 4) + l of the tile (a warp reaches only
+// its quarter of the tensor-memory lanes) and K elements [kPartK (w / 4), + kPartK) of
+// each stage: it copies, converts and stores exactly those.
+constexpr int kPartK = kKT / (kConvWarps / 4);
+static_assert(kConvWarps == 8 && kPartK == 64 && kChunks == 4, "converter layout");
 
 struct Params {
   const int8_t* codes;
@@ -77,11 +91,8 @@ struct Params {
 };
 
 __host__ __device__ constexpr uint32_t b_bytes(int kc) { return (uint32_t)kN * (uint32_t)kc * 2u; }
-// dynamic shared memory, from its first 1024-byte boundary: A[0] | A[1] | B | int8 ring |
-// partial tile (the swizzled A buffers need 1024-byte alignment)
-__host__ __device__ constexpr uint32_t smem_bytes(int kc) {
-  return 1024 + 2 * kABytes + b_bytes(kc) + kRing * kI8Bytes + kPartBytes;
-}
+// dynamic shared memory, from its first 128-byte boundary: B | int8 ring | partial tile
+__host__ __device__ constexpr uint32_t smem_bytes(int kc) { return 128 + b_bytes(kc) + kRing * kI8Bytes + kPartBytes; }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -91,24 +102,29 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
-// The same for the K-major 128-byte-swizzled layout: 8-row x 128-byte atoms, 1024 bytes
-// apart (sbo); within an atom the 16-byte chunk j of row i sits at chunk j ^ i.  The
-// leading offset is unused for this layout (set to 16 bytes).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t sbo) {
-  return (uint64_t)((addr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
-         (2ull << 61);
-}
 // Instruction descriptor, kind::f16: f32 accumulator, f16 A and B, both K-major, N, M.
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
 
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+// D (tensor memory) += A (tensor memory, K-major: row i in lane i) x B (shared memory).
+__device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t accumulate) {
   asm volatile(
       "{\n"
       ".reg .pred p;\n"
       "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
       "}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "r"(tmem_a), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane (warp-collective).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t mbar) {
@@ -117,7 +133,6 @@ __device__ __forceinline__ void mma_commit(uint32_t mbar) {
 }
 __device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // mbarrier helpers.  A wait polls mbarrier.test_wait (returns at once) at most
 // kSpinLimit times and reports whether the phase completed.
@@ -184,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bar_full[2], bar_empty[2], bar_done[2], bar_drained[2];
+  __shared__ __align__(8) uint64_t bar_full[kNA], bar_empty[kNA], bar_done[2], bar_drained[2];
   __shared__ uint32_t tmem_base;
   __shared__ float unscale[kNB];
   __shared__ float wmax[kNB];
@@ -200,8 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
   const int64_t k0 = (int64_t)rank * kc;
   const int nst = kc / kKT;  // stages per tile
   const int64_t total = my_tiles * nst;
-  uint8_t* const abase = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);  // A[0], 1024-aligned
-  uint8_t* Bs = abase + 2 * kABytes;
+  uint8_t* Bs = smem + ((128u - (smem_u32(smem) & 127u)) & 127u);
   uint8_t* ring = Bs + b_bytes(kc);
   float* part = reinterpret_cast<float*>(ring + kRing * kI8Bytes);  // [kNB][kM]
   const uint32_t bsbo = (uint32_t)(kc / 8) * kCoreBytes;
@@ -215,9 +229,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(full0 + 8 * i, kConv);
+    for (int i = 0; i < kNA; ++i) {
+      mbar_init(full0 + 8 * i, kConvWarps);  // one arrival per converter warp
       mbar_init(empty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(done0 + 8 * i, 1);
       mbar_init(drained0 + 8 * i, kEpi);
     }
@@ -232,25 +248,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
     // ======================= converter / epilogue warps =======================
     bool bad = false;
     const uint32_t ring_s = smem_u32(ring);
-    // weight ring: global stage g = tile index t * nst + s; chunk j of a stage for this
-    // thread: row r = (tid + 128 j) / (kKT / 16), 16-byte chunk (tid + 128 j) % (kKT / 16)
+    // weight ring: global stage g = tile index t * nst + s.  This thread's row of the
+    // tile and K offset within a stage; chunk j of its kChunks 16-byte chunks sits at
+    // 16 (kConv j + tid) of a ring slot (the thread reads back only what it copied, and a
+    // warp's lanes touch consecutive 16-byte words: no bank conflicts).
+    const int r = 32 * (warp & 3) + lane, kb = (warp >> 2) * kPartK;
     // copy cursor: the next stage to copy (tile it, stage is, ring slot islot); 32-bit
     // counters updated by one step (no division in the loop)
     int ig = 0, is = 0, islot = 0;
     int64_t irow0 = first * kM;
     auto issue = [&]() {
       if (ig < total) {
-        const int64_t row0 = irow0;
-        const int s = is;
-        const uint32_t slot = ring_s + (uint32_t)islot * kI8Bytes;
+        const int64_t row = min(irow0 + r, p.rows - 1);  // rows past the end: any valid row
+        const int8_t* src = p.codes + row * p.cols + k0 + (int64_t)is * kKT + kb;
+        const uint32_t slot = ring_s + (uint32_t)islot * kI8Bytes + 16u * (uint32_t)tid;
 #pragma unroll
-        for (int j = 0; j < kChunks; ++j) {
-          const int c = tid + kConv * j, r = c / (kKT / 16), k16 = c % (kKT / 16);
-          const int64_t row = min(row0 + r, p.rows - 1);  // rows past the end: any valid row
-          const int8_t* src = p.codes + row * p.cols + k0 + (int64_t)s * kKT + 16 * k16;
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(slot + (uint32_t)c * 16u), "l"(src)
+        for (int j = 0; j < kChunks; ++j)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(slot + 16u * kConv * j), "l"(src + 16 * j)
                        : "memory");
-        }
         ++ig;
         if (++is == nst) {
           is = 0;
@@ -377,43 +392,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
     conv_bar();     // unscale is written; B is complete (made visible to the MMAs below)
     pdl_trigger();  // the next kernel may launch (it waits for this one before reading y)
 
-    // ---- stage loop
+    // ---- stage loop: convert this thread's kPartK codes of stage g into A stage `ab` of
+    // tensor memory (its row's lane, columns kb / 2 .. kb / 2 + kPartK / 2 - 1 of the stage)
     const int epi_at = nst - 1 < kEpiDelay ? nst - 1 : kEpiDelay;
     int t = 0, s = 0, slot_i = 0;  // tile, stage and ring slot of stage g
+    int ab = 0;                    // A stage in tensor memory
+    uint32_t afills = 0;           // earlier fills of A stage ab
     int64_t row0 = first * kM;
+    const uint32_t ta_row = taddr + ((uint32_t)(32 * (warp & 3)) << 16) + kAccCols + (uint32_t)(kb / 2);
     for (int g = 0; g < (int)total; ++g) {
-      const int buf = g & 1;
       issue();  // stage g + kRing - 1
       asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");  // stage g landed
-      if (g >= 2 && !bad) {
-        if (!mbar_wait(empty0 + 8 * buf, (uint32_t)((g - 2) >> 1) & 1u)) bad = true;  // A[buf] free
-      }
-      uint8_t* A = abase + (uint32_t)buf * kABytes;
-      const uint8_t* slot = ring + slot_i * kI8Bytes;
-      // all of this thread's chunks are read before any is written: the stores to A must
-      // not order the next chunk's load behind them
+      if (afills > 0 && !bad && !mbar_wait(empty0 + 8 * ab, (afills - 1) & 1u)) bad = true;  // A stage free
+      fence_after_sync();
+      const uint8_t* slot = ring + slot_i * kI8Bytes + 16 * tid;
       uint4 q[kChunks];
 #pragma unroll
-      for (int j = 0; j < kChunks; ++j) q[j] = *reinterpret_cast<const uint4*>(slot + (tid + kConv * j) * 16);
+      for (int j = 0; j < kChunks; ++j) q[j] = *reinterpret_cast<const uint4*>(slot + 16 * kConv * j);
+      uint32_t h[kPartK / 2] = {};
+      if (row0 + r < p.rows) {
 #pragma unroll
-      for (int j = 0; j < kChunks; ++j) {
-        const int c = tid + kConv * j, r = c / (kKT / 16), k16 = c % (kKT / 16);
-        uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
-        if (row0 + r < p.rows) {
-          i8x4_to_h2x2(q[j].x, h0.x, h0.y);
-          i8x4_to_h2x2(q[j].y, h0.z, h0.w);
-          i8x4_to_h2x2(q[j].z, h1.x, h1.y);
-          i8x4_to_h2x2(q[j].w, h1.z, h1.w);
+        for (int j = 0; j < kChunks; ++j) {
+          i8x4_to_h2x2(q[j].x, h[8 * j + 0], h[8 * j + 1]);
+          i8x4_to_h2x2(q[j].y, h[8 * j + 2], h[8 * j + 3]);
+          i8x4_to_h2x2(q[j].z, h[8 * j + 4], h[8 * j + 5]);
+          i8x4_to_h2x2(q[j].w, h[8 * j + 6], h[8 * j + 7]);
         }
-        // 128-byte swizzle: 16-byte chunk j of row r at chunk j ^ (r & 7) of the row's span
-        uint8_t* rowp = A + (r >> 3) * kASbo + (r & 7) * 128;
-        *reinterpret_cast<uint4*>(rowp + (((2 * k16) ^ (r & 7)) << 4)) = h0;
-        *reinterpret_cast<uint4*>(rowp + (((2 * k16 + 1) ^ (r & 7)) << 4)) = h1;
       }
-      fence_proxy_async();
-      mbar_arrive(full0 + 8 * buf);
+      tmem_st32(ta_row + (uint32_t)ab * kACols, h);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full0 + 8 * ab);
       if (s == epi_at && t >= 1) epilogue(t - 1);
       if (++slot_i == kRing) slot_i = 0;
+      if (++ab == kNA) {
+        ab = 0;
+        ++afills;
+      }
       if (++s == nst) {
         s = 0;
         ++t;
@@ -426,22 +442,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
   } else if (lane == 0) {
     // ======================= MMA lane =======================
     bool bad = false;
-    int t = 0, s = 0;  // tile and stage of stage g
+    int t = 0, s = 0;     // tile and stage of stage g
+    int ab = 0;           // A stage in tensor memory
+    uint32_t afills = 0;  // earlier fills of A stage ab
     for (int g = 0; g < (int)total && !bad; ++g) {
-      const int buf = g & 1;
       const int acc = t & 1;
       if (s == 0 && t >= 2 && !mbar_wait(drained0 + 8 * acc, (uint32_t)((t - 2) >> 1) & 1u)) bad = true;
-      if (!bad && !mbar_wait(full0 + 8 * buf, (uint32_t)(g >> 1) & 1u)) bad = true;
+      if (!bad && !mbar_wait(full0 + 8 * ab, afills & 1u)) bad = true;
       if (bad) break;
       fence_after_sync();
-      const uint32_t a0 = smem_u32(abase + (uint32_t)buf * kABytes);
+      const uint32_t a0 = taddr + kAccCols + (uint32_t)ab * kACols;
       const uint32_t b0 = smem_u32(Bs) + (uint32_t)(s * kKT / 8) * kCoreBytes;
 #pragma unroll
-      for (int kk = 0; kk < kKT / 16; ++kk)
-        mma_f16(taddr + (uint32_t)(32 * acc), smem_desc_sw128(a0 + kk * 32, kASbo),
-                smem_desc(b0 + kk * 2 * kCoreBytes, kCoreBytes, bsbo), (s > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(empty0 + 8 * buf);
+      for (int kk = 0; kk < kKT / 16; ++kk)  // 16 K elements = 8 columns of A per instruction
+        mma_f16_ta(taddr + (uint32_t)(32 * acc), a0 + 8u * kk, smem_desc(b0 + kk * 2 * kCoreBytes, kCoreBytes, bsbo),
+                   (s > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(empty0 + 8 * ab);
       if (s == nst - 1) mma_commit(done0 + 8 * acc);
+      if (++ab == kNA) {
+        ab = 0;
+        ++afills;
+      }
       if (++s == nst) {
         s = 0;
         ++t;
