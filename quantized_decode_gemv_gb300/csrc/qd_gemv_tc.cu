@@ -17,16 +17,18 @@
 //    cp.async ring; thread (w, l) owns row 32 (w % 4) + l of the tile (a warp reaches only
 //    its quarter of the tensor-memory lanes) and half of each stage: it copies its 64
 //    codes, converts them exactly to f16 (q ^ 0x80 placed in the mantissa of 1024, then
-//    1152 subtracted) and writes them with one tcgen05.st into one of seven A stages in
-//    tensor memory; each warp then arrives once on the stage's "full" mbarrier.  One lane
-//    of the ninth warp waits for "full", issues the stage's eight MMAs (A from tensor
-//    memory, B from shared memory) and commits them to the stage's "empty" mbarrier, which
-//    the converters wait for before refilling it.  (Per stage, the MMA lane and the
-//    converters each pay a fixed hand-off cost; 128-column stages halve it per byte.)
-//    Tiles alternate between two accumulators in tensor memory; after a tile's last stage
-//    the MMA lane commits to the accumulator's "done" barrier, and converter warps 0-3
-//    read it out (tcgen05.ld, one row per thread) a few stages into the next tile, then
-//    arrive on its "drained" barrier.
+//    1152 subtracted) and writes them with one tcgen05.st into one of five A stages in
+//    tensor memory; each warp then arrives once on the stage's "full" mbarrier.  Two MMA
+//    lanes (lane 0 of warps 8 and 9) take a tile's even and odd stages: each waits for
+//    "full", issues the stage's eight MMAs (A from tensor memory, B from shared memory)
+//    into its half of the tile's accumulator and commits them to the stage's "empty"
+//    mbarrier, which the converters wait for before refilling it.  (Per stage, the MMA
+//    issue and the converters each pay a fixed hand-off cost; 128-column stages halve it
+//    per byte, and a second issuing thread keeps about 1.7 times the MMAs in flight.)
+//    Tiles alternate between two accumulators in tensor memory; after its last stage of a
+//    tile each MMA lane commits to the accumulator's "done" barrier, and converter warps
+//    0-3 read both halves out (tcgen05.ld, one row per thread) a few stages into the next
+//    tile, then arrive on its "drained" barrier.
 //  * Many row tiles: one cluster-free CTA per SM walks tiles cta, cta + CTAs, ... with the
 //    weight ring running on across tiles.  Few row tiles: the columns split over up to 8
 //    CTAs of a thread-block cluster (one tile each); the partials are summed through
@@ -53,17 +55,19 @@ constexpr int kKT = 128;      // K elements per pipeline stage
 constexpr int kConvWarps = QD_TC_CONV_WARPS;  // converter warps; warps 0-3 also read the accumulators
 constexpr int kConv = 32 * kConvWarps;        // converter threads
 constexpr int kEpi = 128;                     // accumulator readout threads (TMEM lanes 0-127)
-constexpr int kMmaWarp = kConvWarps;          // the warp after the converters
-constexpr int kThreads = kConv + 32;
+constexpr int kMmaWarp = kConvWarps;          // the two warps after the converters issue the MMAs
+constexpr int kThreads = kConv + 64;
 static_assert(kConvWarps == 4 || kConvWarps == 8, "converter warps");
 constexpr int kMaxKc = 2048;  // K elements per CTA at most (shared memory for B)
 constexpr int kRing = 5;      // int8 weight stages in the cp.async ring
 constexpr int kEpiDelay = 2;  // stages into the next tile before the previous one is read out
 constexpr int kMaxCluster = 8;
-// Tensor memory: two 32-column f32 accumulators, then kNA f16 A stages of kKT / 2 columns
-// (row r of the tile in lane r, two K elements per 32-bit column).
-constexpr int kNA = 7;
-constexpr uint32_t kAccCols = 64;
+// Tensor memory: two tiles' accumulators, each two 32-column f32 halves (one per MMA lane:
+// lane 0 takes a tile's even stages, lane 1 its odd ones; the epilogue adds the halves),
+// then kNA f16 A stages of kKT / 2 columns (row r of the tile in lane r, two K elements per
+// 32-bit column).
+constexpr int kNA = 5;
+constexpr uint32_t kAccCols = 128;
 constexpr uint32_t kACols = kKT / 2;
 constexpr uint32_t kTmemCols = 512;
 static_assert(kAccCols + kNA * kACols <= kTmemCols, "tensor memory columns");
@@ -234,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
       mbar_init(empty0 + 8 * i, 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(done0 + 8 * i, 1);
+      mbar_init(done0 + 8 * i, nst >= 2 ? 2 : 1);  // one commit per MMA lane with a stage in the tile
       mbar_init(drained0 + 8 * i, kEpi);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -285,7 +289,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
       if (!ok) bad = true;
       fence_after_sync();
       float v[32];
-      tmem_ld32(taddr + (uint32_t)(32 * acc) + ((uint32_t)(32 * warp) << 16), v);
+      tmem_ld32(taddr + (uint32_t)(64 * acc) + ((uint32_t)(32 * warp) << 16), v);
+      if (nst >= 2) {  // the odd stages' half
+        float w[32];
+        tmem_ld32(taddr + (uint32_t)(64 * acc + 32) + ((uint32_t)(32 * warp) << 16), w);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] += w[i];
+      }
       fence_before_sync();
       mbar_arrive(drained0 + 8 * acc);
       const int r = 32 * warp + lane;
@@ -439,26 +449,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc_i8(const Params p) {
     if (my_tiles >= 1) epilogue(my_tiles - 1);
     asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy in flight at exit
     if (bad && p.err) atomicOr(p.err, kErrTimeout);
-  } else if (lane == 0) {
-    // ======================= MMA lane =======================
+  } else if (lane == 0 && (warp == kMmaWarp || nst >= 2)) {
+    // ======================= MMA lanes =======================
+    // Lane L (warp kMmaWarp + L) issues the MMAs of the stages s of every tile with
+    // s % 2 == L into half L of the tile's accumulator: two issuing threads keep about
+    // 1.7 times the MMAs in flight of one.
+    const int L = warp - kMmaWarp;
+    const int s_last = nst - 1 - ((nst - 1 - L) & 1);  // this lane's last stage of a tile
     bool bad = false;
     int t = 0, s = 0;     // tile and stage of stage g
     int ab = 0;           // A stage in tensor memory
     uint32_t afills = 0;  // earlier fills of A stage ab
     for (int g = 0; g < (int)total && !bad; ++g) {
       const int acc = t & 1;
-      if (s == 0 && t >= 2 && !mbar_wait(drained0 + 8 * acc, (uint32_t)((t - 2) >> 1) & 1u)) bad = true;
-      if (!bad && !mbar_wait(full0 + 8 * ab, afills & 1u)) bad = true;
-      if (bad) break;
-      fence_after_sync();
-      const uint32_t a0 = taddr + kAccCols + (uint32_t)ab * kACols;
-      const uint32_t b0 = smem_u32(Bs) + (uint32_t)(s * kKT / 8) * kCoreBytes;
+      if ((s & 1) == L) {
+        if (s == L && t >= 2 && !mbar_wait(drained0 + 8 * acc, (uint32_t)((t - 2) >> 1) & 1u)) bad = true;
+        if (!bad && !mbar_wait(full0 + 8 * ab, afills & 1u)) bad = true;
+        if (bad) break;
+        fence_after_sync();
+        const uint32_t a0 = taddr + kAccCols + (uint32_t)ab * kACols;
+        const uint32_t b0 = smem_u32(Bs) + (uint32_t)(s * kKT / 8) * kCoreBytes;
+        const uint32_t d = taddr + (uint32_t)(64 * acc + 32 * L);
 #pragma unroll
-      for (int kk = 0; kk < kKT / 16; ++kk)  // 16 K elements = 8 columns of A per instruction
-        mma_f16_ta(taddr + (uint32_t)(32 * acc), a0 + 8u * kk, smem_desc(b0 + kk * 2 * kCoreBytes, kCoreBytes, bsbo),
-                   (s > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(empty0 + 8 * ab);
-      if (s == nst - 1) mma_commit(done0 + 8 * acc);
+        for (int kk = 0; kk < kKT / 16; ++kk)  // 16 K elements = 8 columns of A per instruction
+          mma_f16_ta(d, a0 + 8u * kk, smem_desc(b0 + kk * 2 * kCoreBytes, kCoreBytes, bsbo), (s > L || kk > 0) ? 1u : 0u);
+        mma_commit(empty0 + 8 * ab);
+        if (s == s_last) mma_commit(done0 + 8 * acc);
+      }
       if (++ab == kNA) {
         ab = 0;
         ++afills;
