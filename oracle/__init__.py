@@ -81,6 +81,8 @@ def _L():
         lib.or_attention.restype = i32
         lib.or_swiglu.argtypes = [p, p, i64, p]
         lib.or_swiglu.restype = i32
+        lib.or_quantize_i8_rows.argtypes = [p, i64, i64, p, p]
+        lib.or_quantize_i8_rows.restype = i32
         lib.or_set_threads.argtypes = [i32]
         lib.or_set_threads.restype = i32
         lib.or_argmax_f32.argtypes = [p, i64]
@@ -206,6 +208,19 @@ def swiglu(g, u) -> np.ndarray:
     if rc:
         raise ValueError(f"or_swiglu rc={rc}")
     return out
+
+
+def quantize_i8_rows(w_bf16, rows: int, cols: int) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row symmetric INT8 of BF16 weights (bit patterns, uint16 [rows][cols]):
+    (codes int8 [rows][cols], scales f32 [rows]); see or_quantize_i8_rows."""
+    w, wp = _c(np.asarray(w_bf16, np.uint16).reshape(-1), np.uint16)
+    assert w.size == rows * cols
+    codes = np.empty(rows * cols, np.int8)
+    scales = np.empty(rows, np.float32)
+    rc = _L().or_quantize_i8_rows(wp, rows, cols, codes.ctypes.data, scales.ctypes.data)
+    if rc != 0:
+        raise ValueError("quantize_i8_rows: bad shape")
+    return codes.reshape(rows, cols), scales
 
 
 def silu(z: float) -> float:

@@ -359,6 +359,48 @@ int or_swiglu(const float* g, const float* u, int64_t n, double* out) {
 }
 
 /* ------------------------------------------------------------------------- */
+/* Load-time per-row INT8 quantisation of BF16 weights ([minillm] "Direct INT8 */
+/* loading": each matrix quantised row by row from the BF16 file; "Quantization":*/
+/* symmetric, one scale per output row).  The pages do not print the rule; the  */
+/* reading taken: s = max|w| / 127 in f32, q = w / s (f32) rounded to nearest   */
+/* with ties away from zero (C roundf), clamped to [-127, 127].  A row of zeros  */
+/* gets s = 0 and codes 0; a row holding a non-finite value gets codes 0 and a   */
+/* NaN scale.  Output: the per-row INT8 tensor bytes (codes [rows][cols], then   */
+/* f32 scales [rows]).                                                          */
+/* ------------------------------------------------------------------------- */
+
+int or_quantize_i8_rows(const uint16_t* w, int64_t rows, int64_t cols, int8_t* codes, float* scales) {
+    if (rows < 1 || cols < 1) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t* wr = w + r * cols;
+        int8_t* qr = codes + r * cols;
+        float m = 0.0f;
+        int finite = 1;
+        for (int64_t c = 0; c < cols; ++c) {
+            const float v = or_bf16_to_f32(wr[c]);
+            if (!isfinite(v))
+                finite = 0;
+            else if (fabsf(v) > m)
+                m = fabsf(v);
+        }
+        if (!finite || m == 0.0f) {
+            scales[r] = finite ? 0.0f : NAN;
+            for (int64_t c = 0; c < cols; ++c) qr[c] = 0;
+            continue;
+        }
+        const float s = m / 127.0f;
+        scales[r] = s;
+        for (int64_t c = 0; c < cols; ++c) {
+            float q = roundf(or_bf16_to_f32(wr[c]) / s);
+            if (q > 127.0f) q = 127.0f;
+            if (q < -127.0f) q = -127.0f;
+            qr[c] = (int8_t)q;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Greedy argmax: the largest value, the first index on ties ([go-llm] index, */
 /* Argmax; [dasLLAMA] 8.7.1.6.4 most_likely: strict '>' from index 0).        */
 /* ------------------------------------------------------------------------- */
