@@ -334,6 +334,7 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.quick:
         out["roofline"] = roofline_dominant(qd, torch, stream, hbm, peak_kind)
         out["q_gemv_sweep"] = gemv_sweep(qd, torch, stream, hbm, args)
+        out["quantize_i8"] = bench_quantize(qd, torch, 49152, 2048, hbm)
         del model
         torch.cuda.empty_cache()
         if not args.no_1p7b:
@@ -395,6 +396,34 @@ def roofline_dominant(qd, torch, stream, hbm, peak_kind):
             "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
             "traffic": traffic, "algorithmic_bytes_per_launch": round(tot_b / len(DECODE_SHAPES)),
             "per_shape": per}
+
+
+def bench_quantize(qd, torch, rows, cols, hbm, reps=10):
+    """Load-time per-row INT8 quantisation of a BF16 matrix (qd_quantize_i8_rows): average
+    device time per launch over `reps` launches, L2 flushed before each (the bf16 input of
+    the default shape, 201 MB, also exceeds L2).  Algorithmic bytes: 2 read + 1 written per
+    weight, 4 written per row."""
+    g = torch.Generator(device="cuda").manual_seed(7)
+    w = torch.randn(rows, cols, generator=g, device="cuda").to(torch.bfloat16).view(torch.int16)
+    out = torch.empty(qd.src_bytes("i8", rows, cols), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        qd.quantize_i8_rows(w, rows, cols, out)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        qd.quantize_i8_rows(w, rows, cols, out)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) / 1e3)
+    t = statistics.median(ts)
+    by = 3 * rows * cols + 4 * rows
+    del w, out, flush
+    return {"shape": f"{rows}x{cols}", "us": round(t * 1e6, 2), "us_best": round(min(ts) * 1e6, 2),
+            "algorithmic_bytes": by, "GB/s": round(by / t / 1e9, 1), "frac": round(by / t / 1e9 / hbm, 4)}
 
 
 def gemv_sweep(qd, torch, stream, hbm, args):
@@ -581,6 +610,22 @@ def run_gemv_only(spec: str, reps: int):
     print(json.dumps(out))
 
 
+def run_quantize_only(spec: str, reps: int):
+    """The BF16 -> INT8 quantiser alone at ROWSxCOLS; prints one JSON line (not the
+    benchmark contract line)."""
+    import torch
+
+    import quantized_decode_gemv_gb300 as qd
+
+    rows, cols = (int(v) for v in spec.split("x"))
+    if not os.path.exists(qd.LIB_PATH):
+        qd.build()
+    qd.load()
+    hbm, _, kind = peaks()
+    print(json.dumps({"quantize_i8": bench_quantize(qd, torch, rows, cols, hbm, max(reps, 3)), "peak": hbm,
+                      "peak_kind": kind}))
+
+
 def run_1p7b_only(spec: str, layers=None):
     """The 1.7B-shaped INT8 step alone at the given batches ("1", "16" or "1,16"), optionally
     with fewer layers (a small case for profiling); prints one JSON line (not the benchmark
@@ -613,12 +658,16 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--decode-1p7b", default=None, help="the 1.7B-shaped step alone, at batches e.g. 1,16")
     ap.add_argument("--layers", type=int, default=None, help="with --decode-1p7b: fewer layers (profiling)")
+    ap.add_argument("--quantize", default=None, help="the BF16 -> INT8 quantiser alone at ROWSxCOLS")
     args = ap.parse_args(argv)
     if args.gemv:
         run_gemv_only(args.gemv, args.reps)
         return
     if args.decode_1p7b:
         run_1p7b_only(args.decode_1p7b, args.layers)
+        return
+    if args.quantize:
+        run_quantize_only(args.quantize, args.reps)
         return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

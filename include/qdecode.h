@@ -124,6 +124,19 @@ qd_status qd_unpack(qd_fmt fmt, const void* packed, int64_t rows, int64_t cols, 
  * rounded once to f32 (for the bit-exact block-value tests). */
 qd_status qd_dequant(qd_fmt fmt, const void* packed, int64_t rows, int64_t cols, float* out, qd_stream_t stream);
 
+/* Load-time per-row INT8 quantisation of BF16 weights ([minillm] "Direct INT8
+ * loading": each matrix quantised row by row from the BF16 checkpoint;
+ * "Quantization": symmetric, one scale per output row).  The page prints no rule;
+ * the one implemented: s_r = max_c |w_rc| / 127 in f32, q_rc = w_rc / s_r (f32)
+ * rounded to nearest with ties away from zero, clamped to [-127, 127]; a row of
+ * zeros gets s_r = 0 and codes 0, a row holding a non-finite value codes 0 and a NaN
+ * scale.  w_bf16: device bf16 bit patterns [rows][cols] (16-byte aligned; value =
+ * bits << 16 as f32).  out: device, the QD_I8_ROW source layout (codes [rows][cols],
+ * then f32 scales [rows]; out_bytes >= qd_src_bytes(QD_I8_ROW, rows, cols)), ready for
+ * qd_repack or a model's INT8 weights; must not overlap w_bf16.  cols % 16 == 0. */
+qd_status qd_quantize_i8_rows(const uint16_t* w_bf16, int64_t rows, int64_t cols, void* out, size_t out_bytes,
+                              qd_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* Fused dequantise-and-dot GEMV ([llmoxide] 1 matvec, 10 (the Q8_0 row dot), */
 /* 11 (t rows of x through one read of W); [dasLLAMA] 8.7.1.4 matmul;         */

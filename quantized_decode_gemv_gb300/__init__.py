@@ -23,7 +23,8 @@ STATUS = {0: "QD_OK", 1: "QD_ERR_INVALID_ARG", 2: "QD_ERR_SHAPE", 3: "QD_ERR_ALI
 
 # Every symbol include/qdecode.h declares (checked by the CPU test suite).
 EXPORTS = ["qd_status_str", "qd_abi_version", "qd_f16_to_f32", "qd_bf16_to_f32", "qd_src_bytes", "qd_packed_bytes",
-           "qd_repack", "qd_unpack", "qd_dequant", "qd_q_gemv_workspace", "qd_q_gemv", "qd_q_gemv_ex", "qd_rmsnorm",
+           "qd_repack", "qd_unpack", "qd_dequant", "qd_quantize_i8_rows", "qd_q_gemv_workspace", "qd_q_gemv",
+           "qd_q_gemv_ex", "qd_rmsnorm",
            "qd_rope_table", "qd_rope", "qd_kv_append", "qd_gqa_decode_attn_workspace", "qd_gqa_decode_attn",
            "qd_gqa_decode_attn_noalloc",
            "qd_swiglu", "qd_argmax", "qd_embed", "qd_model_weight_bytes", "qd_model_state_bytes",
@@ -70,6 +71,7 @@ def load():
         "qd_repack": ([i32, p, i64, i64, p, sz, p], i32),
         "qd_unpack": ([i32, p, i64, i64, p, sz, p], i32),
         "qd_dequant": ([i32, p, i64, i64, p, p], i32),
+        "qd_quantize_i8_rows": ([p, i64, i64, p, sz, p], i32),
         "qd_q_gemv_workspace": ([i32, i64, i64, i32], sz),
         "qd_q_gemv": ([i32, p, i64, i64, p, p, i32, p, sz, p], i32),
         "qd_q_gemv_ex": ([i32, p, i64, i64, p, p, i32, ctypes.c_uint, p], i32),
@@ -162,6 +164,13 @@ def unpack(fmt, packed, rows, cols, dst, dst_bytes=None, stream=None):
 
 def dequant(fmt, packed, rows, cols, out, stream=None):
     _check("qd_dequant", load().qd_dequant(FMT[fmt], _ptr(packed), rows, cols, _ptr(out), _stream(stream)))
+
+
+def quantize_i8_rows(w_bf16, rows, cols, out, out_bytes=None, stream=None):
+    """BF16 weights (uint16/int16/bfloat16 tensor [rows][cols]) -> per-row INT8 source layout."""
+    nbytes = out.numel() * out.element_size() if out_bytes is None else out_bytes
+    _check("qd_quantize_i8_rows",
+           load().qd_quantize_i8_rows(_ptr(w_bf16), rows, cols, _ptr(out), nbytes, _stream(stream)))
 
 
 def q_gemv_workspace(fmt, rows, cols, batch) -> int:

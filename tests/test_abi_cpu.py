@@ -94,6 +94,13 @@ def test_other_entry_points_validate(lib):
     assert lib.qd_embed(1, good, 100, 576, good, 1, good + 4, None) == 3
     assert lib.qd_swiglu(None, good, good, 10, 1, None) == 1
     assert lib.qd_decode_step(None, good, 1, good, None, None) == 1
+    q = lib.qd_quantize_i8_rows
+    assert q(None, 8, 64, good, 1 << 20, None) == 1                        # null weights
+    assert q(good, 8, 40, good, 1 << 20, None) == 2                        # cols % 16
+    assert q(good, 0, 64, good, 1 << 20, None) == 2                        # no rows
+    assert q(good + 2, 8, 64, good, 1 << 20, None) == 3                    # misaligned weights
+    assert q(good, 8, 64, good + 4, 1 << 20, None) == 3                    # misaligned output
+    assert q(good, 8, 64, good, 8 * 64 + 8 * 4 - 1, None) == 6             # output one byte short
 
 
 def test_model_sizes_and_config_refusals(lib):
