@@ -51,7 +51,7 @@ class _Config(ctypes.Structure):
                 ("n_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("vocab", ctypes.c_int), ("max_ctx", ctypes.c_int), ("rope_theta", ctypes.c_double),
                 ("eps", ctypes.c_double), ("pairing", ctypes.c_int), ("w_fmt", ctypes.c_int),
-                ("emb_fmt", ctypes.c_int)]
+                ("emb_fmt", ctypes.c_int), ("kv_f16", ctypes.c_int)]
 
 
 def _L():
@@ -81,6 +81,8 @@ def _L():
         lib.or_attention.restype = i32
         lib.or_swiglu.argtypes = [p, p, i64, p]
         lib.or_swiglu.restype = i32
+        lib.or_round_f16.argtypes = [ctypes.c_float]
+        lib.or_round_f16.restype = ctypes.c_float
         lib.or_quantize_i8_rows.argtypes = [p, i64, i64, p, p]
         lib.or_quantize_i8_rows.restype = i32
         lib.or_set_threads.argtypes = [i32]
@@ -210,6 +212,11 @@ def swiglu(g, u) -> np.ndarray:
     return out
 
 
+def round_f16(f: float) -> float:
+    """f32 rounded through binary16 (what an f16 KV cache stores)."""
+    return float(_L().or_round_f16(float(np.float32(f))))
+
+
 def quantize_i8_rows(w_bf16, rows: int, cols: int) -> tuple[np.ndarray, np.ndarray]:
     """Per-row symmetric INT8 of BF16 weights (bit patterns, uint16 [rows][cols]):
     (codes int8 [rows][cols], scales f32 [rows]); see or_quantize_i8_rows."""
@@ -245,7 +252,8 @@ class Model:
         self._ptrs = (ctypes.c_void_p * len(ptrs))(*ptrs)
         self._c = _Config(cfg["layers"], cfg["dim"], cfg["ffn"], cfg["n_heads"], cfg["n_kv_heads"],
                           cfg["head_dim"], cfg["vocab"], cfg["max_ctx"], cfg["rope_theta"], cfg["eps"],
-                          PAIRING[cfg["pairing"]], FMT[cfg["w_fmt"]], FMT[cfg["emb_fmt"]])
+                          PAIRING[cfg["pairing"]], FMT[cfg["w_fmt"]], FMT[cfg["emb_fmt"]],
+                          1 if cfg.get("kv_f16") else 0)
 
     def decode_step(self, k_cache: np.ndarray, v_cache: np.ndarray, layer_stride: int, pos: int,
                     token: int, seq_offset: int = 0):

@@ -81,6 +81,31 @@ float or_bf16_to_f32(uint16_t b) {
     return f;
 }
 
+/* f32 rounded through IEEE binary16 and back ([go-llm] index RoundF16: what an f16 KV
+ * cache stores).  Written from the format's definition: the nearest binary16 value, ties
+ * to the even significand; magnitudes from 65520 up become infinity; below 2^-14 the
+ * spacing is the subnormal one, 2^-24; NaN stays NaN, the sign of zero is kept. */
+float or_round_f16(float f) {
+    if (isnan(f)) return f;
+    const double a = fabs((double)f);
+    double r;
+    if (a >= 65520.0) {
+        r = INFINITY;
+    } else {
+        int e;
+        frexp(a, &e);                 /* a = m * 2^e, m in [0.5, 1) */
+        int ex = e - 1;               /* a in [2^ex, 2^(ex+1)) */
+        if (ex < -14) ex = -14;       /* subnormal range: fixed spacing 2^-24 */
+        const double ulp = ldexp(1.0, ex - 10);
+        const double q = a / ulp;     /* exact: a has at most 24 significant bits */
+        double n = floor(q);
+        const double frac = q - n;
+        if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) != 0.0)) n += 1.0;
+        r = n * ulp;
+    }
+    return (float)(f < 0.0f || (f == 0.0f && signbit(f)) ? -r : r);
+}
+
 /* Array form of the two conversions, writing f32 bit patterns (keeps NaN payloads). */
 void or_bf16_to_f32_array(const uint16_t* in, int64_t n, float* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = or_bf16_to_f32(in[i]);
@@ -429,7 +454,8 @@ int64_t or_argmax_f64(const double* v, int64_t n) {
 /*              x += Wd . (silu(Wg xn) * (Wu xn)), xn = rmsnorm(x) * ffn_norm */
 /*   logits = W_out . (rmsnorm(x) * out_norm); next = argmax(logits)           */
 /* The new k, v are appended to the f32 cache at pos before attending over    */
-/* positions 0..pos ([llmoxide] s12; [dasLLAMA] 8.7.1.6.2).                   */
+/* positions 0..pos ([llmoxide] s12; [dasLLAMA] 8.7.1.6.2); with kv_f16 they  */
+/* are rounded through binary16 first (the cache then holds f16 values).     */
 /*                                                                            */
 /* tensors[] (host pointers, model-file layouts):                             */
 /*   [0] token embedding (emb_fmt, vocab x dim)  [1] out_norm f32[dim]        */
@@ -444,6 +470,7 @@ typedef struct {
     int layers, dim, ffn, n_heads, n_kv_heads, head_dim, vocab, max_ctx;
     double rope_theta, eps;
     int pairing, w_fmt, emb_fmt;
+    int kv_f16; /* 1: the cache stores k and v rounded through binary16 ([go-llm] RoundF16) */
 } or_config;
 
 int or_decode_step(const or_config* c, const void* const* tensors, float* k_cache, float* v_cache,
@@ -484,8 +511,13 @@ int or_decode_step(const or_config* c, const void* const* tensors, float* k_cach
         for (int h = 0; h < hk; ++h) or_rope_head_d(k + (int64_t)h * hd, hd, pos, c->pairing, c->rope_theta);
         for (int h = 0; h < hk; ++h)
             for (int i = 0; i < hd; ++i) {
-                kl[((int64_t)h * c->max_ctx + pos) * hd + i] = (float)k[h * hd + i];
-                vl[((int64_t)h * c->max_ctx + pos) * hd + i] = (float)v[h * hd + i];
+                float kf = (float)k[h * hd + i], vf = (float)v[h * hd + i];
+                if (c->kv_f16) {
+                    kf = or_round_f16(kf);
+                    vf = or_round_f16(vf);
+                }
+                kl[((int64_t)h * c->max_ctx + pos) * hd + i] = kf;
+                vl[((int64_t)h * c->max_ctx + pos) * hd + i] = vf;
             }
         or_attention_d(q, kl, vl, hq, hk, hd, pos + 1, c->max_ctx, att);
         gemv_rows_d(c->w_fmt, (const uint8_t*)L[4], D, QD, att, 1, QD, t, D, 0, D);

@@ -104,3 +104,29 @@ def test_zero_and_non_finite_rows():
     w[2, 5] = 0x7F80  # +inf
     q, s = oracle.quantize_i8_rows(w, 3, 16)
     assert np.isnan(s[2]) and not q[2].any()
+
+
+def test_round_f16_worked_values():
+    """RoundF16 (go-llm index: what an f16 KV cache stores): nearest binary16, ties to even."""
+    r = oracle.round_f16
+    assert r(1.0) == 1.0 and r(-2.5) == -2.5
+    assert r(1.0 / 3.0) == 0.333251953125                       # 1/3 -> 0x3555
+    assert r(65504.0) == 65504.0 and r(65519.0) == 65504.0      # largest finite
+    assert r(65520.0) == np.inf and r(-70000.0) == -np.inf      # the tie at 65520 rounds up to inf
+    assert r(1.0 + 2.0 ** -11) == 1.0                           # tie, even significand below
+    assert r(1.0 + 3 * 2.0 ** -11) == 1.0 + 2.0 ** -9           # tie, even significand above
+    assert r(2.0 ** -24) == 2.0 ** -24 and r(2.0 ** -25) == 0.0  # smallest subnormal; tie to 0
+    assert r(3 * 2.0 ** -26) == 2.0 ** -24
+    assert np.isnan(r(np.nan))
+    assert np.signbit(r(-0.0)) and r(-0.0) == 0.0
+
+
+def test_round_f16_matches_numpy_binary16_on_random_values():
+    # numpy's float32 -> float16 cast is round-to-nearest-even: an independent implementation
+    x = np.concatenate([qdsynth.activations(44, "f16.rt", 1, 4000).reshape(-1) * 3.0,
+                        qdsynth.activations(45, "f16.rt2", 1, 2000).reshape(-1) * 1e-5,
+                        qdsynth.activations(46, "f16.rt3", 1, 2000).reshape(-1) * 3e4]).astype(np.float32)
+    got = np.array([oracle.round_f16(v) for v in x], np.float32)
+    with np.errstate(over="ignore"):  # values past 65504 become infinity, as intended
+        want = x.astype(np.float16).astype(np.float32)
+    assert np.array_equal(got, want)
