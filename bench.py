@@ -339,6 +339,7 @@ def run_ours(args, world, rank, local):
         torch.cuda.empty_cache()
         if not args.no_1p7b:
             out["decode_1p7b"] = bench_1p7b(qd, torch, stream, args, hbm)
+            out["decode_1p7b"].update(bench_1p7b(qd, torch, stream, args, hbm, kv_f16=True))
         if world == 1:
             out["cpu_baseline"] = cpu_baseline(cfg, seconds=args.cpu_seconds)
     if rank == 0:
@@ -453,13 +454,15 @@ def gemv_sweep(qd, torch, stream, hbm, args):
     return res
 
 
-def bench_1p7b(qd, torch, stream, args, hbm, batches=(1, 16), layers=None):
+def bench_1p7b(qd, torch, stream, args, hbm, batches=(1, 16), layers=None, kv_f16=False):
     """1.7B-shaped INT8 step at context 4096 (pos 4095): batch 1 and 16, cache entries N(0,1)
     drawn on the device with a seeded torch generator (timing only; the parity tests use the
     host generator)."""
     import qdsynth
 
     cfg = qdsynth.SMOL_1_7B if not layers else dict(qdsynth.SMOL_1_7B, layers=layers)
+    cfg = dict(cfg, kv_f16=kv_f16)
+    esz = 2 if kv_f16 else 4  # bytes per cache element
     ctx = 4096
     host = qdsynth.model_tensors(cfg, 0)
     out = {}
@@ -473,7 +476,8 @@ def bench_1p7b(qd, torch, stream, args, hbm, batches=(1, 16), layers=None):
         n = cfg["layers"] * batch * cfg["n_kv_heads"] * ctx * cfg["head_dim"]
         g = torch.Generator(device="cuda").manual_seed(1234)
         for ptr in (kp, vp):
-            m.state[ptr - base:ptr - base + 4 * n].view(torch.float32).normal_(generator=g)
+            m.state[ptr - base:ptr - base + esz * n].view(torch.float16 if kv_f16 else torch.float32).normal_(
+                generator=g)
         toks = torch.from_numpy(qdsynth.tokens(0, "c5.tokens", 16, cfg["vocab"])[:batch].astype(np.int32)).cuda()
         outt = torch.empty(batch, dtype=torch.int32, device="cuda")
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -490,10 +494,10 @@ def bench_1p7b(qd, torch, stream, args, hbm, batches=(1, 16), layers=None):
                 ts.append(e0.elapsed_time(e1) / 1e3)
         t = statistics.median(ts)
         wbytes = m.weights.numel()
-        kv = 2 * n * 4
+        kv = 2 * n * esz
         gbs = (wbytes + kv) / t / 1e9
         roof = batch / ((wbytes + kv) / (hbm * 1e9))
-        out[f"batch{batch}"] = {"ms_per_step": round(t * 1e3, 3), "ms_per_step_best": round(min(ts) * 1e3, 3),
+        out[f"batch{batch}" + ("_kv_f16" if kv_f16 else "")] = {"ms_per_step": round(t * 1e3, 3), "ms_per_step_best": round(min(ts) * 1e3, 3),
                                 "tokens/s": round(batch / t, 1), "bytes_per_step": int(wbytes + kv),
                                 "GB/s": round(gbs, 1), "roofline_tokens/s": round(roof, 1),
                                 "frac": round(gbs / hbm, 4), "frac_nominal_8tbs": round(gbs / 8000, 4)}
@@ -626,7 +630,7 @@ def run_quantize_only(spec: str, reps: int):
                       "peak_kind": kind}))
 
 
-def run_1p7b_only(spec: str, layers=None):
+def run_1p7b_only(spec: str, layers=None, kv_f16=False):
     """The 1.7B-shaped INT8 step alone at the given batches ("1", "16" or "1,16"), optionally
     with fewer layers (a small case for profiling); prints one JSON line (not the benchmark
     contract line)."""
@@ -639,7 +643,7 @@ def run_1p7b_only(spec: str, layers=None):
     qd.load()
     stream = torch.cuda.current_stream()
     hbm, _, kind = peaks()
-    res = bench_1p7b(qd, torch, stream, None, hbm, tuple(int(b) for b in spec.split(",")), layers)
+    res = bench_1p7b(qd, torch, stream, None, hbm, tuple(int(b) for b in spec.split(",")), layers, kv_f16)
     print(json.dumps({"decode_1p7b": res, "layers": layers, "peak": hbm, "peak_kind": kind}))
 
 
@@ -659,12 +663,13 @@ def main(argv=None):
     ap.add_argument("--decode-1p7b", default=None, help="the 1.7B-shaped step alone, at batches e.g. 1,16")
     ap.add_argument("--layers", type=int, default=None, help="with --decode-1p7b: fewer layers (profiling)")
     ap.add_argument("--quantize", default=None, help="the BF16 -> INT8 quantiser alone at ROWSxCOLS")
+    ap.add_argument("--kv-f16", action="store_true", help="with --decode-1p7b: binary16 KV cache")
     args = ap.parse_args(argv)
     if args.gemv:
         run_gemv_only(args.gemv, args.reps)
         return
     if args.decode_1p7b:
-        run_1p7b_only(args.decode_1p7b, args.layers)
+        run_1p7b_only(args.decode_1p7b, args.layers, args.kv_f16)
         return
     if args.quantize:
         run_quantize_only(args.quantize, args.reps)

@@ -258,6 +258,9 @@ typedef struct {
     qd_fmt w_fmt;   /* the seven matrices of every layer                        */
     qd_fmt emb_fmt; /* token embedding (and output head)                        */
     int tied;       /* 1: logits use the token embedding as output head         */
+    int kv_f16;     /* 0: f32 KV cache; 1: binary16 KV cache (go-llm's ggml-exact  */
+                    /* cache: k and v rounded to nearest binary16 when appended,  */
+                    /* read back exactly; half the cache bytes)                   */
 } qd_config;
 
 typedef struct qd_model qd_model;
@@ -299,8 +302,9 @@ qd_status qd_model_reset(qd_model* m, qd_stream_t stream);
 qd_status qd_model_set_pos(qd_model* m, const int32_t* pos_host, int batch, qd_stream_t stream);
 /* Read positions (host int32 [batch]); synchronises `stream` ([go-llm] CPU.Pos). */
 qd_status qd_model_pos(qd_model* m, int32_t* pos_host, int batch, qd_stream_t stream);
-/* Device pointers to the KV cache, f32 [layers][max_batch][n_kv_heads][max_ctx][head_dim]. */
-qd_status qd_model_kv_cache(qd_model* m, float** k_cache, float** v_cache);
+/* Device pointers to the KV cache, [layers][max_batch][n_kv_heads][max_ctx][head_dim] of
+ * f32 (kv_f16 == 0) or binary16 bit patterns (kv_f16 == 1). */
+qd_status qd_model_kv_cache(qd_model* m, void** k_cache, void** v_cache);
 /* Synchronise `stream` and return QD_ERR_DEVICE_FLAG (and clear the word) if a
  * kernel met an out-of-range token or position since the last check. */
 qd_status qd_model_check(qd_model* m, qd_stream_t stream);

@@ -39,9 +39,16 @@ using namespace attn;
 constexpr int kFlatWarps = 8;                       // consumer warps
 constexpr int kFlatRows = 8;                        // positions per consumer warp per tile
 constexpr int kFlatTile = kFlatWarps * kFlatRows;   // positions per tile
-constexpr int kFlatHalf = kFlatTile * kHeadDim;     // floats of one tile's key (or value) rows
-constexpr int kFlatStageBytes = 2 * kFlatHalf * 4;  // 32 KB: key rows, then value rows
-constexpr int kFlatStages = 4;
+constexpr int kFlatHalf = kFlatTile * kHeadDim;     // elements of one tile's key (or value) rows
+// ring stages: f32 caches 4 x 32 KB, binary16 caches 6 x 16 KB
+template <typename T>
+constexpr int flat_stage_bytes() {
+  return 2 * kFlatHalf * (int)sizeof(T);  // key rows, then value rows
+}
+template <typename T>
+constexpr int flat_stages() {
+  return sizeof(T) == 4 ? 4 : 6;
+}
 constexpr int kFlatThreads = (kFlatWarps + 1) * 32;  // + the producer warp
 constexpr int kPartFloats = 2 + kHeadDim;            // one head's partial: m, l, o[64]
 constexpr int kFlatSlotHeads = 8;  // parked (pair, head) warp states a CTA holds before settling them
@@ -98,14 +105,27 @@ struct Cursor {
   int b, kvh, tt;  // sequence, kv head, tile of that pair
 };
 
-template <int G, int NS>
+// K, V rows of the cache's element type (f32, or binary16 read back exactly), widened to
+// f32 in the consumers.
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const __half* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ float2 load2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 load2(const __half* p) { return __half22float2(*reinterpret_cast<const __half2*>(p)); }
+
+template <int G, int NS, typename CT>
 __global__ void __launch_bounds__(kFlatThreads, 1)
-    k_attn_flat(const float* __restrict__ q, int64_t q_stride, const float* __restrict__ kc,
-                const float* __restrict__ vc, int64_t cache_batch_stride, int n_heads, int n_kv,
+    k_attn_flat(const float* __restrict__ q, int64_t q_stride, const CT* __restrict__ kc,
+                const CT* __restrict__ vc, int64_t cache_batch_stride, int n_heads, int n_kv,
                 const int32_t* __restrict__ pos, int max_ctx, int batch, float scale, float* __restrict__ out,
                 float* __restrict__ ws, unsigned int* __restrict__ cnt, uint32_t* err) {
   constexpr int W = kFlatWarps;
-  extern __shared__ __align__(128) float ring[];  // [NS][key rows | value rows]
+  constexpr int kStageBytes = flat_stage_bytes<CT>();
+  extern __shared__ __align__(128) float ring[];  // [NS][key rows | value rows] of CT, then the slots
   __shared__ __align__(8) uint64_t full_bar[NS], empty_bar[NS];
   __shared__ int s_n[QD_MAX_BATCH], s_tiles[QD_MAX_BATCH];
   __shared__ int64_t s_off[QD_MAX_BATCH + 1];  // tiles before sequence b (all its kv heads)
@@ -198,11 +218,11 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
         const int rows = min(kFlatTile, s_n[c.b] - p0);
         const int64_t off =
             (int64_t)c.b * cache_batch_stride + ((int64_t)c.kvh * max_ctx + p0) * kHeadDim;  // row p0 of the pair
-        const uint32_t bytes = (uint32_t)rows * kHeadDim * 4;
-        const uint32_t dst = ring_s + (uint32_t)slot * kFlatStageBytes;
+        const uint32_t bytes = (uint32_t)rows * kHeadDim * (uint32_t)sizeof(CT);
+        const uint32_t dst = ring_s + (uint32_t)slot * kStageBytes;
         mbar_arrive_expect_tx(full0 + 8 * slot, 2 * bytes);
         bulk_copy(dst, kc + off, bytes, full0 + 8 * slot);
-        bulk_copy(dst + kFlatHalf * 4, vc + off, bytes, full0 + 8 * slot);
+        bulk_copy(dst + kFlatHalf * (uint32_t)sizeof(CT), vc + off, bytes, full0 + 8 * slot);
         ++issued;
         advance(c);
         if (++slot == NS) {
@@ -246,17 +266,18 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
   // this warp's 8 positions of the tile in `slot`; rows past the pair's last position hold
   // stale data and are masked out of both the scores and the values
   auto use_tile = [&](int slot, const Cursor& c) {
-    const float* kt = ring + slot * (kFlatStageBytes / 4) + warp * kFlatRows * kHeadDim;
-    const float* vt = kt + kFlatHalf;
+    const CT* kt = reinterpret_cast<const CT*>(reinterpret_cast<const uint8_t*>(ring) + slot * kStageBytes) +
+                  warp * kFlatRows * kHeadDim;
+    const CT* vt = kt + kFlatHalf;
     const int live_rows = s_n[c.b] - c.tt * kFlatTile - warp * kFlatRows;  // may be <= 0 or > 8
     const bool live0 = pi < live_rows, live1 = 4 + pi < live_rows;
-    const float4 k0a = *reinterpret_cast<const float4*>(kt + pi * kHeadDim + 4 * j);
-    const float4 k0b = *reinterpret_cast<const float4*>(kt + pi * kHeadDim + 32 + 4 * j);
-    const float4 k1a = *reinterpret_cast<const float4*>(kt + (4 + pi) * kHeadDim + 4 * j);
-    const float4 k1b = *reinterpret_cast<const float4*>(kt + (4 + pi) * kHeadDim + 32 + 4 * j);
+    const float4 k0a = load4(kt + pi * kHeadDim + 4 * j);
+    const float4 k0b = load4(kt + pi * kHeadDim + 32 + 4 * j);
+    const float4 k1a = load4(kt + (4 + pi) * kHeadDim + 4 * j);
+    const float4 k1b = load4(kt + (4 + pi) * kHeadDim + 32 + 4 * j);
     float2 v[kFlatRows];
 #pragma unroll
-    for (int i = 0; i < kFlatRows; ++i) v[i] = *reinterpret_cast<const float2*>(vt + i * kHeadDim + 2 * lane);
+    for (int i = 0; i < kFlatRows; ++i) v[i] = load2(vt + i * kHeadDim + 2 * lane);
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       float s0 = qs[g][0] * k0a.x;
@@ -310,7 +331,7 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
   // in shared memory (slots after the ring: m[W][G], l[W][G], o[W][G][64] per slot).
   constexpr int kSlots = kFlatSlotHeads / G > 0 ? kFlatSlotHeads / G : 1;
   constexpr int kSlotFloats = W * G * kPartFloats;
-  float* slots = ring + NS * (kFlatStageBytes / 4);
+  float* slots = ring + NS * (kStageBytes / 4);
   int npairs = 0;  // the same in every consumer thread: all walk the same tiles
   auto end_pair = [&](const Cursor& c) {
     float* sl = slots + npairs * kSlotFloats;
@@ -477,18 +498,20 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
 }
 
 // ring stages, then the parked warp states (at least one pair's worth)
-constexpr int flat_smem_bytes(int G, int NS) {
-  return NS * kFlatStageBytes + (kFlatSlotHeads / G > 0 ? kFlatSlotHeads / G : 1) * kFlatWarps * G * kPartFloats * 4;
+template <typename T>
+constexpr int flat_smem_bytes(int G) {
+  return flat_stages<T>() * flat_stage_bytes<T>() +
+         (kFlatSlotHeads / G > 0 ? kFlatSlotHeads / G : 1) * kFlatWarps * G * kPartFloats * 4;
 }
 
-template <int G>
-cudaError_t launch_flat_g(cudaLaunchConfig_t& cfg, const float* q, int64_t q_stride, const float* kc,
-                          const float* vc, int64_t cache_batch_stride, int n_heads, int n_kv, const int32_t* pos,
-                          int max_ctx, int batch, float scale, float* out, float* ws, unsigned int* cnt,
-                          uint32_t* err) {
-  constexpr int NS = kFlatStages;
-  auto kern = k_attn_flat<G, NS>;
-  const int smem = flat_smem_bytes(G, NS);
+template <int G, typename T>
+cudaError_t launch_flat_gt(cudaLaunchConfig_t& cfg, const float* q, int64_t q_stride, const void* kc,
+                           const void* vc, int64_t cache_batch_stride, int n_heads, int n_kv, const int32_t* pos,
+                           int max_ctx, int batch, float scale, float* out, float* ws, unsigned int* cnt,
+                           uint32_t* err) {
+  constexpr int NS = flat_stages<T>();
+  auto kern = k_attn_flat<G, NS, T>;
+  const int smem = flat_smem_bytes<T>(G);
   static bool done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -500,8 +523,19 @@ cudaError_t launch_flat_g(cudaLaunchConfig_t& cfg, const float* q, int64_t q_str
   }
   cfg.blockDim = dim3(kFlatThreads);
   cfg.dynamicSmemBytes = (size_t)smem;
-  return cudaLaunchKernelEx(&cfg, kern, q, q_stride, kc, vc, cache_batch_stride, n_heads, n_kv, pos, max_ctx, batch,
-                            scale, out, ws, cnt, err);
+  return cudaLaunchKernelEx(&cfg, kern, q, q_stride, static_cast<const T*>(kc), static_cast<const T*>(vc),
+                            cache_batch_stride, n_heads, n_kv, pos, max_ctx, batch, scale, out, ws, cnt, err);
+}
+
+template <int G>
+cudaError_t launch_flat_g(cudaLaunchConfig_t& cfg, bool kv_f16, const float* q, int64_t q_stride, const void* kc,
+                          const void* vc, int64_t cache_batch_stride, int n_heads, int n_kv, const int32_t* pos,
+                          int max_ctx, int batch, float scale, float* out, float* ws, unsigned int* cnt,
+                          uint32_t* err) {
+  return kv_f16 ? launch_flat_gt<G, __half>(cfg, q, q_stride, kc, vc, cache_batch_stride, n_heads, n_kv, pos, max_ctx,
+                                            batch, scale, out, ws, cnt, err)
+                : launch_flat_gt<G, float>(cfg, q, q_stride, kc, vc, cache_batch_stride, n_heads, n_kv, pos, max_ctx,
+                                           batch, scale, out, ws, cnt, err);
 }
 
 }  // namespace
@@ -518,7 +552,7 @@ bool attn_use_flat(int n_kv, int batch, int max_ctx) {
   return (int64_t)n_kv * batch * max_ctx * 2 * kHeadDim * 4 >= kAttnFlatMinBytes;
 }
 
-qd_status launch_attention_flat(const float* q, int64_t q_stride, const float* kc, const float* vc,
+qd_status launch_attention_flat(const float* q, int64_t q_stride, const void* kc, const void* vc, bool kv_f16,
                                 int64_t cache_batch_stride, float* out, int n_heads, int n_kv, int head_dim,
                                 const int32_t* pos, int max_ctx, int batch, int ctas, float* ws, unsigned int* cnt,
                                 uint32_t* err, cudaStream_t stream, bool pdl) {
@@ -537,8 +571,8 @@ qd_status launch_attention_flat(const float* q, int64_t q_stride, const float* k
   cudaError_t rc = cudaErrorInvalidValue;
 #define QD_FLAT_G(GG)                                                                                            \
   case GG:                                                                                                       \
-    rc = launch_flat_g<GG>(cfg, q, q_stride, kc, vc, cache_batch_stride, n_heads, n_kv, pos, max_ctx, batch, scale, \
-                           out, ws, cnt, err);                                                                   \
+    rc = launch_flat_g<GG>(cfg, kv_f16, q, q_stride, kc, vc, cache_batch_stride, n_heads, n_kv, pos, max_ctx, batch, \
+                           scale, out, ws, cnt, err);                                                            \
     break;
   switch (G) {
     QD_FLAT_G(1)

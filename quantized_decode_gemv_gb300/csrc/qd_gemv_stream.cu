@@ -104,17 +104,22 @@ __device__ __forceinline__ void qkv_pair_out(const Params& p, int64_t r, int b, 
     const int d1 = e.pairing == QD_ROPE_HALF ? pi + half : 2 * pi + 1;
     const float2 cs = pf.cs;
     const float o0 = a * cs.x - bb * cs.y, o1 = a * cs.y + bb * cs.x;
-    float* dst = isq ? e.q_out + (int64_t)b * e.q_stride + h * hd
-                     : e.kc + (int64_t)b * e.cache_batch_stride + (h * e.max_ctx + pos) * hd;
-    dst[d0] = o0;
-    dst[d1] = o1;
+    if (isq) {
+      float* dst = e.q_out + (int64_t)b * e.q_stride + h * hd;
+      dst[d0] = o0;
+      dst[d1] = o1;
+    } else {
+      const int64_t row = (int64_t)b * e.cache_batch_stride + (h * e.max_ctx + pos) * hd;
+      cache_store(e.kc, e.kv_f16, row + d0, o0);
+      cache_store(e.kc, e.kv_f16, row + d1, o1);
+    }
   } else {
     const int64_t local = r - e.q_rows - e.k_rows;
     const int64_t h = local / hd;
     const int d = (int)(local % hd);
-    float* dst = e.vc + (int64_t)b * e.cache_batch_stride + (h * e.max_ctx + pos) * hd;
-    dst[d] = a;
-    dst[d + 1] = bb;
+    const int64_t row = (int64_t)b * e.cache_batch_stride + (h * e.max_ctx + pos) * hd;
+    cache_store(e.vc, e.kv_f16, row + d, a);
+    cache_store(e.vc, e.kv_f16, row + d + 1, bb);
   }
 }
 

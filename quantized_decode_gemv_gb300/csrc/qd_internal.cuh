@@ -195,11 +195,20 @@ struct QkvEpilogue {
   const float* rope = nullptr;  // [max_ctx][head_dim/2][2] (cos, sin)
   float* q_out = nullptr;
   int64_t q_stride = 0;
-  float* kc = nullptr;
-  float* vc = nullptr;
-  int64_t cache_batch_stride = 0;
+  void* kc = nullptr;  // f32 or binary16 elements (kv_f16)
+  void* vc = nullptr;
+  int64_t cache_batch_stride = 0;  // elements
   int max_ctx = 0;
+  bool kv_f16 = false;
 };
+
+// Store one cache element (index i) as f32 or binary16 (round to nearest even).
+__device__ __forceinline__ void cache_store(void* base, bool f16, int64_t i, float v) {
+  if (f16)
+    reinterpret_cast<__half*>(base)[i] = __float2half_rn(v);
+  else
+    reinterpret_cast<float*>(base)[i] = v;
+}
 
 // Fused greedy argmax of the output head (mode kGemvArgmax): the logits are stored as
 // in kGemvStore, every warp folds its rows into a 64-bit key (ordered value, then
@@ -309,13 +318,15 @@ qd_status launch_attention_cluster(const float* q, int64_t q_stride, const float
 // Decode-step attention for long walks: an even split of all pairs' positions over one
 // CTA per SM (attn_flat_ctas), partials merged by the last CTA of each (sequence, kv
 // head).  `ws` holds attn_flat_ws_floats(..., ctas) floats for the same `ctas`; `cnt`
-// (batch * n_kv unsigned ints) must be zero and is left zero.  attn_use_flat picks it when the f32 cache of all pairs at full context holds at
-// least kAttnFlatMinBytes.
+// (batch * n_kv unsigned ints) must be zero and is left zero.  kc, vc hold f32 or
+// (kv_f16) binary16 elements.  The decode step takes it when attn_use_flat says so (the f32
+// cache of all pairs at full context holds at least kAttnFlatMinBytes) and always for a
+// binary16 cache.
 constexpr int64_t kAttnFlatMinBytes = 8ll << 20;
 bool attn_use_flat(int n_kv, int batch, int max_ctx);
 int attn_flat_ctas();
 size_t attn_flat_ws_floats(int n_heads, int n_kv, int batch, int ctas);
-qd_status launch_attention_flat(const float* q, int64_t q_stride, const float* kc, const float* vc,
+qd_status launch_attention_flat(const float* q, int64_t q_stride, const void* kc, const void* vc, bool kv_f16,
                                 int64_t cache_batch_stride, float* out, int n_heads, int n_kv, int head_dim,
                                 const int32_t* pos, int max_ctx, int batch, int ctas, float* ws, unsigned int* cnt,
                                 uint32_t* err, cudaStream_t stream, bool pdl);

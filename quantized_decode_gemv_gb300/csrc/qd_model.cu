@@ -48,6 +48,7 @@ bool config_ok(const qd_config* c) {
   if (c->n_heads % c->n_kv_heads || c->n_heads / c->n_kv_heads > 8) return false;
   if (c->max_ctx < 1 || c->max_batch < 1 || c->max_batch > QD_MAX_BATCH) return false;
   if (c->pairing != QD_ROPE_ADJACENT && c->pairing != QD_ROPE_HALF) return false;
+  if (c->kv_f16 != 0 && c->kv_f16 != 1) return false;
   if (!fmt_ok(c->w_fmt) || !fmt_ok(c->emb_fmt)) return false;
   if (!(c->eps >= 0.f) || !(c->rope_theta > 0.f)) return false;
   const int64_t QD = (int64_t)c->n_heads * c->head_dim, KD = (int64_t)c->n_kv_heads * c->head_dim;
@@ -87,7 +88,7 @@ Layout make_layout(const qd_config* c) {
   off = 0;
   L.cache_batch_stride = KD * c->max_ctx;
   L.cache_layer_stride = L.cache_batch_stride * B;
-  const size_t cache = (size_t)c->layers * L.cache_layer_stride * 4;
+  const size_t cache = (size_t)c->layers * L.cache_layer_stride * (c->kv_f16 ? 2 : 4);
   L.kc = take(cache);
   L.vc = take(cache);
   L.x = take(4 * B * D);
@@ -104,7 +105,7 @@ Layout make_layout(const qd_config* c) {
   L.pos = take(4 * B);
   L.err = take(4);
   L.rope = take((size_t)c->max_ctx * c->head_dim * 4);
-  L.attn_flat = attn_use_flat(c->n_kv_heads, c->max_batch, c->max_ctx);
+  L.attn_flat = c->kv_f16 || attn_use_flat(c->n_kv_heads, c->max_batch, c->max_ctx);
   L.attn_ctas = attn_flat_ctas();
   L.attn_ws = L.attn_flat ? take(4 * attn_flat_ws_floats(c->n_heads, c->n_kv_heads, c->max_batch, L.attn_ctas)) : 0;
   L.attn_cnt = L.attn_flat ? take(4 * (size_t)c->n_kv_heads * c->max_batch) : 0;
@@ -192,8 +193,9 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
   };
   for (int l = 0; l < c.layers; ++l) {
     const LayerOff& o = L.layer[l];
-    float* kc = m->f(L.kc) + (int64_t)l * L.cache_layer_stride;
-    float* vc = m->f(L.vc) + (int64_t)l * L.cache_layer_stride;
+    const int64_t esz = c.kv_f16 ? 2 : 4;  // bytes per cache element
+    void* kc = m->s + L.kc + (int64_t)l * L.cache_layer_stride * esz;
+    void* vc = m->s + L.vc + (int64_t)l * L.cache_layer_stride * esz;
     // QKV projection with RoPE and the cache append fused into its epilogue
     GemvArgs qa = args(c.w_fmt, m->W(c.w_fmt, o.wqkv, L.qkv_rows, D), x, qkv, kGemvQKV);
     QkvEpilogue& e = qa.qkv;
@@ -207,6 +209,7 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
     e.q_stride = QD;
     e.kc = kc;
     e.vc = vc;
+    e.kv_f16 = c.kv_f16 != 0;
     e.cache_batch_stride = L.cache_batch_stride;
     e.max_ctx = c.max_ctx;
     const float* attn_norm = reinterpret_cast<const float*>(m->w + o.attn_norm);
@@ -220,11 +223,12 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
       ++n;
     }
     if (L.attn_flat)
-      QD_TRY(launch_attention_flat(q, QD, kc, vc, L.cache_batch_stride, att, c.n_heads, c.n_kv_heads, c.head_dim, pos,
-                                   c.max_ctx, batch, L.attn_ctas, m->f(L.attn_ws),
+      QD_TRY(launch_attention_flat(q, QD, kc, vc, c.kv_f16 != 0, L.cache_batch_stride, att, c.n_heads, c.n_kv_heads,
+                                   c.head_dim, pos, c.max_ctx, batch, L.attn_ctas, m->f(L.attn_ws),
                                    reinterpret_cast<unsigned int*>(m->s + L.attn_cnt), err, st, true));
     else
-      QD_TRY(launch_attention_cluster(q, QD, kc, vc, L.cache_batch_stride, att, c.n_heads, c.n_kv_heads,
+      QD_TRY(launch_attention_cluster(q, QD, static_cast<const float*>(kc), static_cast<const float*>(vc),
+                                      L.cache_batch_stride, att, c.n_heads, c.n_kv_heads,
                                       c.head_dim, pos, c.max_ctx, batch, err, st, true));
     ++n;
     QD_TRY(launch_q_gemv(args(c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, x, kGemvAccumulate), st));
@@ -380,7 +384,7 @@ qd_status qd_decode_step(qd_model* m, const int32_t* tokens, int batch, int32_t*
 qd_status qd_model_reset(qd_model* m, qd_stream_t stream) {
   if (!m) return QD_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
-  const size_t cache = (size_t)m->cfg.layers * m->L.cache_layer_stride * 4;
+  const size_t cache = (size_t)m->cfg.layers * m->L.cache_layer_stride * (m->cfg.kv_f16 ? 2 : 4);
   QD_TRY(zero_region(m->s + m->L.kc, align_up(cache, 16), st));
   QD_TRY(zero_region(m->s + m->L.vc, align_up(cache, 16), st));
   QD_TRY(zero_region(m->s + m->L.pos, 16 * ((4 * m->cfg.max_batch + 15) / 16), st));
@@ -412,10 +416,10 @@ qd_status qd_model_pos(qd_model* m, int32_t* pos_host, int batch, qd_stream_t st
   return QD_OK;
 }
 
-qd_status qd_model_kv_cache(qd_model* m, float** k_cache, float** v_cache) {
+qd_status qd_model_kv_cache(qd_model* m, void** k_cache, void** v_cache) {
   if (!m || !k_cache || !v_cache) return QD_ERR_INVALID_ARG;
-  *k_cache = m->f(m->L.kc);
-  *v_cache = m->f(m->L.vc);
+  *k_cache = m->s + m->L.kc;
+  *v_cache = m->s + m->L.vc;
   return QD_OK;
 }
 

@@ -317,16 +317,21 @@ __global__ void k_qkv_post(const float* __restrict__ qkv, int64_t qkv_stride, Qk
       const int d0 = e.pairing == QD_ROPE_HALF ? pi : 2 * pi;
       const int d1 = e.pairing == QD_ROPE_HALF ? pi + half : 2 * pi + 1;
       const float c = e.rope[((int64_t)pos * half + pi) * 2], s = e.rope[((int64_t)pos * half + pi) * 2 + 1];
-      float* dst = isq ? e.q_out + (int64_t)b * e.q_stride + (int64_t)h * hd
-                       : e.kc + (int64_t)b * e.cache_batch_stride + ((int64_t)h * e.max_ctx + pos) * hd;
-      dst[d0] = a * c - bb * s;
-      dst[d1] = a * s + bb * c;
+      if (isq) {
+        float* dst = e.q_out + (int64_t)b * e.q_stride + (int64_t)h * hd;
+        dst[d0] = a * c - bb * s;
+        dst[d1] = a * s + bb * c;
+      } else {
+        const int64_t row = (int64_t)b * e.cache_batch_stride + ((int64_t)h * e.max_ctx + pos) * hd;
+        cache_store(e.kc, e.kv_f16, row + d0, a * c - bb * s);
+        cache_store(e.kc, e.kv_f16, row + d1, a * s + bb * c);
+      }
     } else {
       const int local = r - e.q_rows - e.k_rows;
       const int h = local / hd, d = local % hd;
-      float* dst = e.vc + (int64_t)b * e.cache_batch_stride + ((int64_t)h * e.max_ctx + pos) * hd;
-      dst[d] = a;
-      dst[d + 1] = bb;
+      const int64_t row = (int64_t)b * e.cache_batch_stride + ((int64_t)h * e.max_ctx + pos) * hd;
+      cache_store(e.vc, e.kv_f16, row + d, a);
+      cache_store(e.vc, e.kv_f16, row + d + 1, bb);
     }
   }
 }

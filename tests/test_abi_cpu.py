@@ -41,7 +41,7 @@ def test_status_strings(lib):
     assert qd.status_str(0) == "ok"
     for s in range(1, 8):
         assert qd.status_str(s) != "unknown status"
-    assert lib.qd_abi_version() == 1
+    assert lib.qd_abi_version() == 2
 
 
 @pytest.mark.parametrize("fmt,rows,cols,src,packed", [
@@ -119,6 +119,13 @@ def test_model_sizes_and_config_refusals(lib):
     assert lib.qd_model_state_bytes(ctypes.byref(bad)) == 0
     bad = qd.make_config(qdsynth.SMOL_135M, max_ctx=256, max_batch=17)
     assert lib.qd_model_state_bytes(ctypes.byref(bad)) == 0
+    bad = qd.make_config(qdsynth.SMOL_135M, max_ctx=256, max_batch=1)
+    bad.kv_f16 = 2
+    assert lib.qd_model_state_bytes(ctypes.byref(bad)) == 0
+    # a binary16 cache takes half the bytes (the state also gains the flat attention's workspace)
+    h = qd.make_config(qdsynth.SMOL_135M, max_ctx=256, max_batch=1, kv_f16=True)
+    sh = lib.qd_model_state_bytes(ctypes.byref(h))
+    assert kv // 2 < sh < sb - kv // 2 + (1 << 20)
 
 
 def test_rope_table_host_matches_oracle(lib):

@@ -112,18 +112,23 @@ def test_smol135m_prompt128_gen128_teacher_forced(qd):
 
 def fill_cache_normal(m, cfg, seed, max_batch, max_ctx):
     """KV cache entries ~N(0,1), generated in (layer, sequence) slices straight into the
-    model's cache (layout [layer][batch][kv_head][ctx][hd])."""
+    model's cache (layout [layer][batch][kv_head][ctx][hd]); for a binary16 cache
+    (cfg["kv_f16"]) the values rounded to binary16 (numpy's round-to-nearest-even cast)."""
+    f16 = cfg.get("kv_f16", False)
+    esz = 2 if f16 else 4
     kp, vp = m.kv_cache_ptrs()
     base = m.state.data_ptr()
     n = cfg["layers"] * max_batch * cfg["n_kv_heads"] * max_ctx * cfg["head_dim"]
-    k = m.state[kp - base:kp - base + 4 * n].view(torch.float32)
-    v = m.state[vp - base:vp - base + 4 * n].view(torch.float32)
+    k = m.state[kp - base:kp - base + esz * n].view(torch.int16 if f16 else torch.float32)
+    v = m.state[vp - base:vp - base + esz * n].view(torch.int16 if f16 else torch.float32)
     per = cfg["n_kv_heads"] * max_ctx * cfg["head_dim"]
-    buf = torch.empty(per, dtype=torch.float32).pin_memory()
+    buf = np.empty(per, np.float32)
+    host = torch.empty(per, dtype=torch.int16 if f16 else torch.float32).pin_memory()
     for name, dst in (("c5.kcache", k), ("c5.vcache", v)):
         for s in range(cfg["layers"] * max_batch):
-            qdsynth.normal_f32(seed, name, per, offset=s * per, out=buf.numpy())
-            dst[s * per:(s + 1) * per].copy_(buf, non_blocking=False)
+            qdsynth.normal_f32(seed, name, per, offset=s * per, out=buf)
+            host.numpy()[:] = buf.astype(np.float16).view(np.int16) if f16 else buf
+            dst[s * per:(s + 1) * per].copy_(host, non_blocking=False)
     torch.cuda.synchronize()
 
 
@@ -136,15 +141,18 @@ def oracle_cache(cfg, seed, b, max_batch, max_ctx):
         off = (l * max_batch + b) * per
         qdsynth.normal_f32(seed, "c5.kcache", per, offset=off, out=k[l * per:(l + 1) * per])
         qdsynth.normal_f32(seed, "c5.vcache", per, offset=off, out=v[l * per:(l + 1) * per])
+    if cfg.get("kv_f16", False):  # the binary16 cache holds these values exactly
+        k = k.astype(np.float16).astype(np.float32)
+        v = v.astype(np.float16).astype(np.float32)
     return k, v
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("batch,check_seqs", [(1, [0]), (16, [0, 9, 15])])
-def test_smol1p7b_int8_ctx4096(qd, batch, check_seqs):
-    """1.7B-shaped INT8 model, f32 KV cache holding 4095 N(0,1) positions; one step at pos
-    4095 (attending over 4096 entries), independent sequences."""
-    cfg = qdsynth.SMOL_1_7B
+@pytest.mark.parametrize("batch,check_seqs,kv_f16", [(1, [0], False), (16, [0, 9, 15], False), (1, [0], True)])
+def test_smol1p7b_int8_ctx4096(qd, batch, check_seqs, kv_f16):
+    """1.7B-shaped INT8 model, KV cache (f32, or binary16) holding 4095 N(0,1) positions;
+    one step at pos 4095 (attending over 4096 entries), independent sequences."""
+    cfg = dict(qdsynth.SMOL_1_7B, kv_f16=kv_f16)
     ctx = 4096
     m, host = build_model(qd, cfg, 0, ctx, batch)
     fill_cache_normal(m, cfg, 0, batch, ctx)
@@ -177,14 +185,15 @@ def flat_cfg(n_heads, n_kv):
 FLAT_CTX, FLAT_BATCH = 2048, 4
 
 
-@pytest.mark.parametrize("n_heads,n_kv", [(8, 8), (8, 4), (12, 4), (16, 2)])
-def test_flat_attention_ragged_positions(qd, n_heads, n_kv):
+@pytest.mark.parametrize("n_heads,n_kv,kv_f16", [(8, 8, False), (8, 4, False), (12, 4, False), (16, 2, False),
+                                                  (8, 8, True), (16, 2, True)])
+def test_flat_attention_ragged_positions(qd, n_heads, n_kv, kv_f16):
     """Four sequences at ragged positions over an N(0,1) cache: one at the last position
     (2048 entries), one at position 0 (a single entry), one mid-context, one just past a
     64-position tile edge; two consecutive steps, every sequence checked against the oracle.
     On the second step the first sequence has run past the context: it is flagged and the
-    others are unaffected."""
-    cfg = flat_cfg(n_heads, n_kv)
+    others are unaffected.  With kv_f16 the cache holds binary16 values."""
+    cfg = dict(flat_cfg(n_heads, n_kv), kv_f16=kv_f16)
     m, host = build_model(qd, cfg, 21, FLAT_CTX, FLAT_BATCH)
     fill_cache_normal(m, cfg, 21, FLAT_BATCH, FLAT_CTX)
     start = [FLAT_CTX - 1, 0, 700, 64]
@@ -245,3 +254,13 @@ def test_flat_attention_many_short_pairs(qd):
         assert_close(g[b], ol, what=f"short pairs seq {b} pos {start[b]}")
         check_token(ol, ot, int(out[b]))
     m.close()
+
+
+@pytest.mark.parametrize("w_fmt,emb_fmt,pairing,batch", [("q4_0", "q8_0", "half", 1), ("i8", "i8", "adjacent", 3)])
+def test_kv_f16_teacher_forced(qd, w_fmt, emb_fmt, pairing, batch):
+    """Binary16 KV cache (go-llm's ggml-exact cache): k and v rounded through binary16 when
+    appended, on both sides; the decode step takes the flat-split attention over it."""
+    cfg = dict(TINY, w_fmt=w_fmt, emb_fmt=emb_fmt, pairing=pairing, kv_f16=True)
+    prompt = qdsynth.tokens(24, "f16.prompt", batch * 5, cfg["vocab"]).reshape(batch, 5)
+    worst, near = run_teacher_forced(qd, cfg, 24, prompt, n_gen=5, batch=batch, max_ctx=72)
+    print(f"kv_f16 {w_fmt}: worst rel err {worst:.2e}, near-tie tokens {near}")
