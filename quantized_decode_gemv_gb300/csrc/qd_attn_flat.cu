@@ -28,6 +28,7 @@
 // Every mbarrier wait is bounded: on a timeout the kernel sets kErrTimeout, stops
 // waiting and computing (its output is then undefined) and still reaches every barrier.
 #include <cmath>
+#include <type_traits>
 
 #include "qd_attn.cuh"
 
@@ -117,6 +118,16 @@ __device__ __forceinline__ float4 load4(const __half* p) {
 __device__ __forceinline__ float2 load2(const float* p) { return *reinterpret_cast<const float2*>(p); }
 __device__ __forceinline__ float2 load2(const __half* p) { return __half22float2(*reinterpret_cast<const __half2*>(p)); }
 
+// Packed pair arithmetic: fma.rn.f32x2 rounds each half as fmaf does.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+        "l"(*reinterpret_cast<const uint64_t*>(&c)));
+  return *reinterpret_cast<const float2*>(&r);
+}
+
 template <int G, int NS, typename CT>
 __global__ void __launch_bounds__(kFlatThreads, 1)
     k_attn_flat(const float* __restrict__ q, int64_t q_stride, const CT* __restrict__ kc,
@@ -130,6 +141,8 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
   __shared__ int s_n[QD_MAX_BATCH], s_tiles[QD_MAX_BATCH];
   __shared__ int64_t s_off[QD_MAX_BATCH + 1];  // tiles before sequence b (all its kv heads)
   __shared__ int s_pairs[kFlatSlotHeads], s_last[kFlatSlotHeads];  // pairs of this run not yet settled
+  constexpr int kFuse = G == 1 ? 2 : 1;  // tiles a consumer step may take (see use_tiles)
+  __shared__ __align__(16) float2 s_w[W][G][kFuse * kFlatRows];  // a warp's weights of a step, each twice
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
   const uint32_t full0 = (uint32_t)__cvta_generic_to_shared(full_bar);
@@ -241,8 +254,8 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
   // ---- consumers
   auto cta_of = [&](int64_t x) { return (int)(((x + 1) * C + T - 1) / T - 1); };  // CTA holding tile x
   const int j = lane & 7, pi = lane >> 3;  // dim slice (dims 4j.., 32+4j..) and row of a step
-  float qs[G][8];
-  float m[G], l[G];
+  float2 qs[G][4];  // (scaled) q dims 4j..4j+3, 32+4j..32+4j+3 as pairs
+  float m[G], l[G];  // l: the weight sum of the rows this lane owned (see use_tiles)
   float2 o[G];
   auto start_pair = [&](const Cursor& c) {
     const float* qb = q + (int64_t)c.b * q_stride + (int64_t)c.kvh * G * kHeadDim;
@@ -250,80 +263,103 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
     for (int g = 0; g < G; ++g) {
       const float4 a = __ldcg(reinterpret_cast<const float4*>(qb + g * kHeadDim + 4 * j));
       const float4 bq = __ldcg(reinterpret_cast<const float4*>(qb + g * kHeadDim + 32 + 4 * j));
-      qs[g][0] = a.x * scale;
-      qs[g][1] = a.y * scale;
-      qs[g][2] = a.z * scale;
-      qs[g][3] = a.w * scale;
-      qs[g][4] = bq.x * scale;
-      qs[g][5] = bq.y * scale;
-      qs[g][6] = bq.z * scale;
-      qs[g][7] = bq.w * scale;
+      qs[g][0] = make_float2(a.x * scale, a.y * scale);
+      qs[g][1] = make_float2(a.z * scale, a.w * scale);
+      qs[g][2] = make_float2(bq.x * scale, bq.y * scale);
+      qs[g][3] = make_float2(bq.z * scale, bq.w * scale);
       m[g] = -INFINITY;
       l[g] = 0.f;
       o[g] = make_float2(0.f, 0.f);
     }
   };
-  // this warp's 8 positions of the tile in `slot`; rows past the pair's last position hold
-  // stale data and are masked out of both the scores and the values
-  auto use_tile = [&](int slot, const Cursor& c) {
-    const CT* kt = reinterpret_cast<const CT*>(reinterpret_cast<const uint8_t*>(ring) + slot * kStageBytes) +
-                  warp * kFlatRows * kHeadDim;
-    const CT* vt = kt + kFlatHalf;
-    const int live_rows = s_n[c.b] - c.tt * kFlatTile - warp * kFlatRows;  // may be <= 0 or > 8
-    const bool live0 = pi < live_rows, live1 = 4 + pi < live_rows;
-    const float4 k0a = load4(kt + pi * kHeadDim + 4 * j);
-    const float4 k0b = load4(kt + pi * kHeadDim + 32 + 4 * j);
-    const float4 k1a = load4(kt + (4 + pi) * kHeadDim + 4 * j);
-    const float4 k1b = load4(kt + (4 + pi) * kHeadDim + 32 + 4 * j);
-    float2 v[kFlatRows];
+  // This warp's 8 positions of NT consecutive tiles of one pair (stages s, s + 1, ...).
+  // Lane (pi, j) forms the partial dot products of rows pi and 4 + pi of each tile over its
+  // dims; exchanges with lanes j ^ 1 (and j ^ 2 for two tiles) leave each lane one row to
+  // finish (row pi or 4 + pi by bit 0 of j, the tile by bit 1), so the max, the weight
+  // and the weight sum take one value per lane, and lanes j < 2 NT own distinct rows.
+  // The weights reach every lane through shared memory as (w, w) pairs and meet the value
+  // rows in packed FMAs.  Rows past the pair's last position hold stale ring data: their
+  // scores are -inf and their values zero.  Two tiles at a time give a warp two
+  // independent chains of shared loads, shuffles and FMAs where one head per kv head
+  // would leave it one.
+  auto use_tiles = [&](auto ntc, int s, const Cursor& c) {
+    constexpr int NT = decltype(ntc)::value;
+    const CT* kt[NT];
+    int live_rows[NT];  // may be <= 0 or > 8
 #pragma unroll
-    for (int i = 0; i < kFlatRows; ++i) v[i] = load2(vt + i * kHeadDim + 2 * lane);
+    for (int t = 0; t < NT; ++t) {
+      kt[t] = reinterpret_cast<const CT*>(reinterpret_cast<const uint8_t*>(ring) + ((s + t) % NS) * kStageBytes) +
+              warp * kFlatRows * kHeadDim;
+      live_rows[t] = s_n[c.b] - (c.tt + t) * kFlatTile - warp * kFlatRows;
+    }
+    const bool odd = j & 1, hi = NT == 2 && (j & 2);
+    const int r = odd ? 4 + pi : pi;  // the row this lane finishes, of tile `hi`
+    const bool owner = j < 2 * NT;
+    const bool live = r < (hi ? live_rows[NT - 1] : live_rows[0]);
+    float4 ka[NT][2], kb[NT][2];  // rows pi and 4 + pi: dims 4j.., 32 + 4j..
+    float2 v[NT][kFlatRows];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        ka[t][h] = load4(kt[t] + (4 * h + pi) * kHeadDim + 4 * j);
+        kb[t][h] = load4(kt[t] + (4 * h + pi) * kHeadDim + 32 + 4 * j);
+      }
+#pragma unroll
+      for (int i = 0; i < kFlatRows; ++i) v[t][i] = load2(kt[t] + kFlatHalf + i * kHeadDim + 2 * lane);
+      if (live_rows[t] < kFlatRows) {  // the pair's last tile (warp-uniform)
+#pragma unroll
+        for (int i = 0; i < kFlatRows; ++i)
+          if (i >= live_rows[t]) v[t][i] = make_float2(0.f, 0.f);
+      }
+    }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      float s0 = qs[g][0] * k0a.x;
-      s0 = fmaf(qs[g][1], k0a.y, s0);
-      s0 = fmaf(qs[g][2], k0a.z, s0);
-      s0 = fmaf(qs[g][3], k0a.w, s0);
-      s0 = fmaf(qs[g][4], k0b.x, s0);
-      s0 = fmaf(qs[g][5], k0b.y, s0);
-      s0 = fmaf(qs[g][6], k0b.z, s0);
-      s0 = fmaf(qs[g][7], k0b.w, s0);
-      float s1 = qs[g][0] * k1a.x;
-      s1 = fmaf(qs[g][1], k1a.y, s1);
-      s1 = fmaf(qs[g][2], k1a.z, s1);
-      s1 = fmaf(qs[g][3], k1a.w, s1);
-      s1 = fmaf(qs[g][4], k1b.x, s1);
-      s1 = fmaf(qs[g][5], k1b.y, s1);
-      s1 = fmaf(qs[g][6], k1b.z, s1);
-      s1 = fmaf(qs[g][7], k1b.w, s1);
+      float x[NT];  // after the first exchange: row r of tile t, summed over j and j ^ 1
 #pragma unroll
-      for (int off = 1; off < 8; off <<= 1) {
-        s0 += __shfl_xor_sync(0xffffffffu, s0, off);
-        s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+      for (int t = 0; t < NT; ++t) {
+        float sp[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float2 p = make_float2(qs[g][0].x * ka[t][h].x, qs[g][0].y * ka[t][h].y);
+          p = ffma2(qs[g][1], make_float2(ka[t][h].z, ka[t][h].w), p);
+          p = ffma2(qs[g][2], make_float2(kb[t][h].x, kb[t][h].y), p);
+          p = ffma2(qs[g][3], make_float2(kb[t][h].z, kb[t][h].w), p);
+          sp[h] = p.x + p.y;
+        }
+        x[t] = (odd ? sp[1] : sp[0]) + __shfl_xor_sync(0xffffffffu, odd ? sp[0] : sp[1], 1);
       }
-      s0 = live0 ? s0 : -INFINITY;
-      s1 = live1 ? s1 : -INFINITY;
-      float tm = fmaxf(s0, s1);
+      float sc;
+      if constexpr (NT == 2)
+        sc = (hi ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, hi ? x[0] : x[1], 2);
+      else
+        sc = x[0] + __shfl_xor_sync(0xffffffffu, x[0], 2);
+      sc += __shfl_xor_sync(0xffffffffu, sc, 4);
+      sc = live ? sc : -INFINITY;
+      float tm = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, 1));
+      if constexpr (NT == 2) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
       tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
       tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
       const float mn = fmaxf(m[g], tm);
       const float corr = m[g] == mn ? 1.f : exp2f(m[g] - mn);
-      const float w0 = live0 ? exp2f(s0 - mn) : 0.f;
-      const float w1 = live1 ? exp2f(s1 - mn) : 0.f;
-      float wsum = w0 + w1;  // the 8 lanes of a row hold the same weights: sum across rows only
-      wsum += __shfl_xor_sync(0xffffffffu, wsum, 8);
-      wsum += __shfl_xor_sync(0xffffffffu, wsum, 16);
-      l[g] = fmaf(l[g], corr, wsum);
-      float2 acc = make_float2(o[g].x * corr, o[g].y * corr);
+      const float w = live ? exp2f(sc - mn) : 0.f;
+      l[g] = fmaf(l[g], corr, owner ? w : 0.f);
+      if (owner) s_w[warp][g][(hi ? kFlatRows : 0) + r] = make_float2(w, w);
+      __syncwarp();
+      const float4* wq = reinterpret_cast<const float4*>(s_w[warp][g]);
+      float2 acc[NT];
 #pragma unroll
-      for (int i = 0; i < kFlatRows; ++i) {
-        const float wi = __shfl_sync(0xffffffffu, i < 4 ? w0 : w1, (i & 3) * 8);
-        if (i < live_rows) {
-          acc.x = fmaf(wi, v[i].x, acc.x);
-          acc.y = fmaf(wi, v[i].y, acc.y);
+      for (int t = 0; t < NT; ++t) {
+        acc[t] = t == 0 ? ffma2(o[g], make_float2(corr, corr), make_float2(0.f, 0.f)) : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < kFlatRows / 2; ++i) {
+          const float4 w2 = wq[t * kFlatRows / 2 + i];
+          acc[t] = ffma2(make_float2(w2.x, w2.y), v[t][2 * i], acc[t]);
+          acc[t] = ffma2(make_float2(w2.z, w2.w), v[t][2 * i + 1], acc[t]);
         }
       }
-      o[g] = acc;
+      if constexpr (NT == 2) acc[0] = make_float2(acc[0].x + acc[1].x, acc[0].y + acc[1].y);
+      o[g] = acc[0];
       m[g] = mn;
     }
   };
@@ -337,6 +373,9 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
     float* sl = slots + npairs * kSlotFloats;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
+      // the weight sum over the warp's rows: each row's weights were taken by one lane
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) l[g] += __shfl_xor_sync(0xffffffffu, l[g], off);
       if (lane == 0) {
         sl[warp * G + g] = m[g];
         sl[W * G + warp * G + g] = l[g];
@@ -467,10 +506,8 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
 
   Cursor cc = start, cur{-1, -1, 0};
   bool bad = false;
-  int slot = 0;
-  uint32_t use = 0;
-  for (int s = 0; s < nst; ++s) {
-    if (!bad && !mbar_wait(full0 + 8 * slot, use & 1u)) {
+  for (int s = 0; s < nst;) {
+    if (!bad && !mbar_wait(full0 + 8 * (s % NS), (uint32_t)(s / NS) & 1u)) {
       bad = true;
       if (err && lane == 0) atomicOr(err, kErrTimeout);
     }
@@ -482,14 +519,27 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
       cur = cc;
       start_pair(cc);
     }
-    if (!bad) use_tile(slot, cc);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * slot);  // this warp is done with the slot
-    advance(cc);
-    if (++slot == NS) {
-      slot = 0;
-      ++use;
+    // take the next tile too when it is this run's and the same pair's (the same in every
+    // consumer thread)
+    const bool two = kFuse == 2 && s + 1 < nst && cc.tt + 1 < s_tiles[cc.b];
+    if (two && !bad && !mbar_wait(full0 + 8 * ((s + 1) % NS), (uint32_t)((s + 1) / NS) & 1u)) {
+      bad = true;
+      if (err && lane == 0) atomicOr(err, kErrTimeout);
     }
+    if (!bad) {
+      if (two)
+        use_tiles(std::integral_constant<int, kFuse>{}, s, cc);
+      else
+        use_tiles(std::integral_constant<int, 1>{}, s, cc);
+    }
+    __syncwarp();
+    if (lane == 0) {  // this warp is done with the slots
+      mbar_arrive(empty0 + 8 * (s % NS));
+      if (two) mbar_arrive(empty0 + 8 * ((s + 1) % NS));
+    }
+    advance(cc);
+    if (two) advance(cc);
+    s += two ? 2 : 1;
   }
   if (cur.b >= 0) {
     end_pair(cur);
