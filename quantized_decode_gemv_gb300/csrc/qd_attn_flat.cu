@@ -37,20 +37,22 @@ namespace {
 
 using namespace attn;
 
-constexpr int kFlatWarps = 8;                       // consumer warps
-constexpr int kFlatRows = 8;                        // positions per consumer warp per tile
-constexpr int kFlatTile = kFlatWarps * kFlatRows;   // positions per tile
-constexpr int kFlatHalf = kFlatTile * kHeadDim;     // elements of one tile's key (or value) rows
-// ring stages: f32 caches 4 x 32 KB, binary16 caches 6 x 16 KB
-template <typename T>
-constexpr int flat_stage_bytes() {
-  return 2 * kFlatHalf * (int)sizeof(T);  // key rows, then value rows
-}
-template <typename T>
-constexpr int flat_stages() {
-  return sizeof(T) == 4 ? 4 : 6;
-}
-constexpr int kFlatThreads = (kFlatWarps + 1) * 32;  // + the producer warp
+constexpr int kFlatRows = 8;  // positions per consumer warp per tile
+// The shape of a launch: W consumer warps take a tile of W x 8 positions, whose key rows
+// and value rows (each one contiguous run of the cache) fill one stage of an NS-stage
+// ring.  Eight warps (64 positions, f32 4 x 32 KB, binary16 6 x 16 KB) except for a
+// binary16 cache with one query head per kv head: there the consumer's dependent chain,
+// not the bytes, sets the pace, so sixteen warps (128 positions, 4 x 32 KB) run two tiles'
+// chains each (120 registers: 17 warps fill the register file).
+template <int G, typename T>
+struct FlatShape {
+  static constexpr int W = (G == 1 && sizeof(T) == 2) ? 16 : 8;
+  static constexpr int kTile = W * kFlatRows;       // positions per tile
+  static constexpr int kHalf = kTile * kHeadDim;    // elements of one tile's key (or value) rows
+  static constexpr int kStageBytes = 2 * kHalf * (int)sizeof(T);  // key rows, then value rows
+  static constexpr int NS = kStageBytes >= 32768 ? 4 : 6;
+  static constexpr int kThreads = (W + 1) * 32;     // + the producer warp
+};
 constexpr int kPartFloats = 2 + kHeadDim;            // one head's partial: m, l, o[64]
 constexpr int kFlatSlotHeads = 8;  // parked (pair, head) warp states a CTA holds before settling them
 constexpr uint32_t kFlatSpinLimit = 1u << 24;        // test_wait polls per wait (about a second)
@@ -98,8 +100,9 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+template <int W>
 __device__ __forceinline__ void consumers_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kFlatWarps * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory");
 }
 
 struct Cursor {
@@ -128,14 +131,15 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return *reinterpret_cast<const float2*>(&r);
 }
 
-template <int G, int NS, typename CT>
-__global__ void __launch_bounds__(kFlatThreads, 1)
+template <int G, typename CT>
+__global__ void __launch_bounds__(FlatShape<G, CT>::kThreads, 1)
     k_attn_flat(const float* __restrict__ q, int64_t q_stride, const CT* __restrict__ kc,
                 const CT* __restrict__ vc, int64_t cache_batch_stride, int n_heads, int n_kv,
                 const int32_t* __restrict__ pos, int max_ctx, int batch, float scale, float* __restrict__ out,
                 float* __restrict__ ws, unsigned int* __restrict__ cnt, uint32_t* err) {
-  constexpr int W = kFlatWarps;
-  constexpr int kStageBytes = flat_stage_bytes<CT>();
+  using Shape = FlatShape<G, CT>;
+  constexpr int W = Shape::W, NS = Shape::NS, kStageBytes = Shape::kStageBytes;
+  constexpr int kFlatTile = Shape::kTile, kFlatHalf = Shape::kHalf;
   extern __shared__ __align__(128) float ring[];  // [NS][key rows | value rows] of CT, then the slots
   __shared__ __align__(8) uint64_t full_bar[NS], empty_bar[NS];
   __shared__ int s_n[QD_MAX_BATCH], s_tiles[QD_MAX_BATCH];
@@ -398,7 +402,7 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
   // i0 + w / G, i0 + w / G + S, ... (S = W / G subsets), eight partials' loads at a time;
   // the subsets are then combined in subset order.
   auto settle = [&]() {
-    consumers_sync();  // every warp's parked states are in shared memory
+    consumers_sync<W>();  // every warp's parked states are in shared memory
     const int np = npairs;
     for (int it = warp; it < np * G; it += W) {
       const int t = it / G, g = it % G;
@@ -424,7 +428,7 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
       }
       reinterpret_cast<float2*>(part + 2)[lane] = ot;
     }
-    consumers_sync();  // the CTA's partial stores are ordered before the counting threads' fences
+    consumers_sync<W>();  // the CTA's partial stores are ordered before the counting threads' fences
     if (threadIdx.x < np) {
       int i0, i1;
       pair_ctas(s_pairs[threadIdx.x], i0, i1);
@@ -432,7 +436,7 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
       s_last[threadIdx.x] = atomicAdd(cnt + s_pairs[threadIdx.x], 1u) == (unsigned)(i1 - i0);
       fence_acq_rel_gpu();  // acquire: the partials of the CTAs counted before this one
     }
-    consumers_sync();
+    consumers_sync<W>();
     constexpr int S = W / G;  // CTA subsets per head in the final merge
     for (int t = 0; t < np; ++t) {
       if (!s_last[t]) continue;
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
         }
         reinterpret_cast<float2*>(scratch + warp * kPartFloats + 2)[lane] = acc;
       }
-      consumers_sync();
+      consumers_sync<W>();
       if (warp < G) {
         const int g = warp;
         float mx = -INFINITY;
@@ -499,7 +503,7 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
         dst[lane] = make_float2(acc.x / lt, acc.y / lt);
       }
       if (threadIdx.x == 0) cnt[pair] = 0u;
-      consumers_sync();  // the scratch is reused by the next pair
+      consumers_sync<W>();  // the scratch is reused by the next pair
     }
     npairs = 0;
   };
@@ -548,10 +552,11 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
 }
 
 // ring stages, then the parked warp states (at least one pair's worth)
-template <typename T>
-constexpr int flat_smem_bytes(int G) {
-  return flat_stages<T>() * flat_stage_bytes<T>() +
-         (kFlatSlotHeads / G > 0 ? kFlatSlotHeads / G : 1) * kFlatWarps * G * kPartFloats * 4;
+template <int G, typename T>
+constexpr int flat_smem_bytes() {
+  using Shape = FlatShape<G, T>;
+  return Shape::NS * Shape::kStageBytes +
+         (kFlatSlotHeads / G > 0 ? kFlatSlotHeads / G : 1) * Shape::W * G * kPartFloats * 4;
 }
 
 template <int G, typename T>
@@ -559,9 +564,9 @@ cudaError_t launch_flat_gt(cudaLaunchConfig_t& cfg, const float* q, int64_t q_st
                            const void* vc, int64_t cache_batch_stride, int n_heads, int n_kv, const int32_t* pos,
                            int max_ctx, int batch, float scale, float* out, float* ws, unsigned int* cnt,
                            uint32_t* err) {
-  constexpr int NS = flat_stages<T>();
-  auto kern = k_attn_flat<G, NS, T>;
-  const int smem = flat_smem_bytes<T>(G);
+  auto kern = k_attn_flat<G, T>;
+  constexpr int smem = flat_smem_bytes<G, T>();
+  static_assert(smem <= 220 * 1024, "ring and parked states exceed the shared memory of a CTA");
   static bool done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -571,7 +576,7 @@ cudaError_t launch_flat_gt(cudaLaunchConfig_t& cfg, const float* q, int64_t q_st
     if (e != cudaSuccess) return e;
     done[dev] = true;
   }
-  cfg.blockDim = dim3(kFlatThreads);
+  cfg.blockDim = dim3(FlatShape<G, T>::kThreads);
   cfg.dynamicSmemBytes = (size_t)smem;
   return cudaLaunchKernelEx(&cfg, kern, q, q_stride, static_cast<const T*>(kc), static_cast<const T*>(vc),
                             cache_batch_stride, n_heads, n_kv, pos, max_ctx, batch, scale, out, ws, cnt, err);

@@ -229,11 +229,13 @@ def test_flat_attention_teacher_forced_from_empty_cache(qd):
     print(f"flat split from an empty cache: worst rel err {worst:.2e}, near-tie tokens {near}")
 
 
-def test_flat_attention_many_short_pairs(qd):
+@pytest.mark.parametrize("kv_f16", [False, True])
+def test_flat_attention_many_short_pairs(qd, kv_f16):
     """96 kv heads x 16 sequences at positions < 64: 1536 one-tile pairs over 152 CTAs, so
-    a CTA's run covers more pairs than it holds before settling them mid-run."""
+    a CTA's run covers more pairs than it holds before settling them mid-run.  With the
+    binary16 cache a tile spans 128 positions: the warps past position 63 see no live row."""
     cfg = dict(layers=1, dim=256, ffn=512, n_heads=96, n_kv_heads=96, head_dim=64, vocab=300, rope_theta=1e4,
-               eps=1e-5, pairing="adjacent", w_fmt="q8_0", emb_fmt="q8_0")
+               eps=1e-5, pairing="adjacent", w_fmt="q8_0", emb_fmt="q8_0", kv_f16=kv_f16)
     ctx, batch = 64, 16
     m, host = build_model(qd, cfg, 23, ctx, batch)
     fill_cache_normal(m, cfg, 23, batch, ctx)
