@@ -614,6 +614,58 @@ def run_gemv_only(spec: str, reps: int):
     print(json.dumps(out))
 
 
+def bench_gemm(qd, torch, fmt, rows, cols, t, reps=20):
+    """The prefill product (qd_q_gemm) at t tokens: median and best of `reps` launches of the
+    call (the x split prologue and the tensor-core kernel) with L2 flushed before each, the
+    useful flops 2 t rows cols, and the two kernels' shares timed apart (CUDA events on the
+    launching stream)."""
+    import qdsynth
+
+    src = qdsynth.weight_src(fmt, 0, f"gemm{rows}x{cols}", rows, cols)
+    s = torch.from_numpy(np.ascontiguousarray(src.reshape(-1).view(np.uint8))).cuda()
+    w = torch.empty(qd.packed_bytes(fmt, rows, cols), dtype=torch.uint8, device="cuda")
+    qd.repack(fmt, s, rows, cols, w)
+    del s
+    x = torch.from_numpy(qdsynth.activations(0, f"gemmx{cols}", t, cols)).cuda()
+    y = torch.empty(t, rows, dtype=torch.float32, device="cuda")
+    ws = torch.empty(qd.q_gemm_workspace(fmt, rows, cols, t), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    ts = []
+    for i in range(3 + reps):
+        flush.fill_(0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        qd.q_gemm(fmt, w, rows, cols, x, y, t, ws, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            ts.append(e0.elapsed_time(e1) / 1e3)
+    flops = 2.0 * t * rows * cols
+    med, best = statistics.median(ts), min(ts)
+    return {"fmt": fmt, "rows": rows, "cols": cols, "t": t, "us": round(med * 1e6, 2), "us_best": round(best * 1e6, 2),
+            "useful_TFLOP/s": round(flops / med / 1e12, 1), "weight_bytes": int(w.numel()),
+            "note": "cold L2 per launch; includes the x split prologue"}
+
+
+def run_gemm_only(spec: str, reps: int):
+    """The prefill product alone, e.g. "q4_0:14336x4096:512" (format:rowsxcols:tokens); prints
+    one JSON line (not the benchmark contract line)."""
+    import torch
+
+    import quantized_decode_gemv_gb300 as qd
+
+    fmt, shape, t = spec.split(":")
+    r, c = (int(v) for v in shape.split("x"))
+    if not os.path.exists(qd.LIB_PATH):
+        qd.build()
+    qd.load()
+    _, bf16, kind = peaks()
+    res = bench_gemm(qd, torch, fmt, r, c, int(t), max(reps, 5))
+    res["frac_of_bf16_peak"] = round(res["useful_TFLOP/s"] / bf16, 4)
+    print(json.dumps({"gemm": res, "bf16_peak_tflops": bf16, "peak_kind": kind}))
+
+
 def run_quantize_only(spec: str, reps: int):
     """The BF16 -> INT8 quantiser alone at ROWSxCOLS; prints one JSON line (not the
     benchmark contract line)."""
@@ -663,6 +715,7 @@ def main(argv=None):
     ap.add_argument("--decode-1p7b", default=None, help="the 1.7B-shaped step alone, at batches e.g. 1,16")
     ap.add_argument("--layers", type=int, default=None, help="with --decode-1p7b: fewer layers (profiling)")
     ap.add_argument("--quantize", default=None, help="the BF16 -> INT8 quantiser alone at ROWSxCOLS")
+    ap.add_argument("--gemm", default=None, help="the prefill product alone, FMT:ROWSxCOLS:TOKENS")
     ap.add_argument("--kv-f16", action="store_true", help="with --decode-1p7b: binary16 KV cache")
     args = ap.parse_args(argv)
     if args.gemv:
@@ -673,6 +726,9 @@ def main(argv=None):
         return
     if args.quantize:
         run_quantize_only(args.quantize, args.reps)
+        return
+    if args.gemm:
+        run_gemm_only(args.gemm, args.reps)
         return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -164,6 +164,29 @@ qd_status qd_q_gemv_ex(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, co
                        unsigned int flags, qd_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
+/* Batched prefill product ([llmoxide] 11 "Prefill and decode": the decode     */
+/* product with t rows of x through one read of the weights, compute-bound;    */
+/* its Metal GEMM dequantises a weight tile once into on-chip memory for the   */
+/* matrix units).  y[n][r] = sum_c deq(W)[r][c] * x[n][c] for n < t, r < rows. */
+/* fmt: QD_Q4_0, QD_Q8_0 or QD_I8_ROW (others: QD_ERR_UNSUPPORTED).  W: packed  */
+/* layout (qd_repack).  x: f32 [t][cols].  y: f32 [t][rows], must not overlap  */
+/* x or the workspace.  cols a multiple of 64, 1 <= t <= QD_MAX_GEMM_TOKENS.     */
+/* workspace: device, 16-byte aligned, >= qd_q_gemm_workspace bytes (0 for an  */
+/* unsupported format or shape); it holds the split x between the call's two   */
+/* kernels and may be reused once the call has completed on `stream`.          */
+/* Arithmetic (5th-generation tensor cores, f32 accumulation): each token's x  */
+/* is scaled by a power of two and split into two binary16 parts (about 2^-22  */
+/* relative); Q4_0 / Q8_0 weights enter as the binary16 rounding of d * q       */
+/* (relative error at most 2^-11 per weight; for |d * q| below 2^-14 the        */
+/* binary16 subnormal step 2^-24 bounds it); INT8 codes enter exactly and the   */
+/* row scale is applied in f32.  A non-finite x row gives NaN in its y row.     */
+/* ------------------------------------------------------------------------- */
+#define QD_MAX_GEMM_TOKENS 65536
+size_t qd_q_gemm_workspace(qd_fmt fmt, int64_t rows, int64_t cols, int t);
+qd_status qd_q_gemm(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int t,
+                    void* workspace, size_t workspace_bytes, qd_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* Decode-step operations                                                      */
 /* ------------------------------------------------------------------------- */
 

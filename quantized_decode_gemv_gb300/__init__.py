@@ -24,7 +24,7 @@ STATUS = {0: "QD_OK", 1: "QD_ERR_INVALID_ARG", 2: "QD_ERR_SHAPE", 3: "QD_ERR_ALI
 # Every symbol include/qdecode.h declares (checked by the CPU test suite).
 EXPORTS = ["qd_status_str", "qd_abi_version", "qd_f16_to_f32", "qd_bf16_to_f32", "qd_src_bytes", "qd_packed_bytes",
            "qd_repack", "qd_unpack", "qd_dequant", "qd_quantize_i8_rows", "qd_q_gemv_workspace", "qd_q_gemv",
-           "qd_q_gemv_ex", "qd_rmsnorm",
+           "qd_q_gemv_ex", "qd_q_gemm_workspace", "qd_q_gemm", "qd_rmsnorm",
            "qd_rope_table", "qd_rope", "qd_kv_append", "qd_gqa_decode_attn_workspace", "qd_gqa_decode_attn",
            "qd_gqa_decode_attn_noalloc",
            "qd_swiglu", "qd_argmax", "qd_embed", "qd_model_weight_bytes", "qd_model_state_bytes",
@@ -76,6 +76,8 @@ def load():
         "qd_q_gemv_workspace": ([i32, i64, i64, i32], sz),
         "qd_q_gemv": ([i32, p, i64, i64, p, p, i32, p, sz, p], i32),
         "qd_q_gemv_ex": ([i32, p, i64, i64, p, p, i32, ctypes.c_uint, p], i32),
+        "qd_q_gemm_workspace": ([i32, i64, i64, i32], sz),
+        "qd_q_gemm": ([i32, p, i64, i64, p, p, i32, p, sz, p], i32),
         "qd_rmsnorm": ([p, p, p, i32, i32, f32, p], i32),
         "qd_rope_table": ([f32, i32, i32, p], i32),
         "qd_rope": ([p, i32, i32, i64, p, i32, p, i32, i32, p], i32),
@@ -176,6 +178,18 @@ def quantize_i8_rows(w_bf16, rows, cols, out, out_bytes=None, stream=None):
 
 def q_gemv_workspace(fmt, rows, cols, batch) -> int:
     return int(load().qd_q_gemv_workspace(FMT[fmt], rows, cols, batch))
+
+
+def q_gemm_workspace(fmt, rows, cols, t) -> int:
+    return int(load().qd_q_gemm_workspace(FMT[fmt], rows, cols, t))
+
+
+def q_gemm(fmt, W, rows, cols, x, y, t, workspace, workspace_bytes=None, stream=None):
+    """y[n][r] = sum_c deq(W)[r][c] x[n][c] for n < t on the tensor cores (see qdecode.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("qd_q_gemm", load().qd_q_gemm(FMT[fmt], _ptr(W), rows, cols, _ptr(x), _ptr(y), t, _ptr(workspace),
+                                         workspace_bytes, _stream(stream)))
 
 
 def q_gemv(fmt, W, rows, cols, x, y, batch, workspace=None, workspace_bytes=0, stream=None):

@@ -385,4 +385,24 @@ qd_status qd_q_gemv_ex(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, co
   return launch_q_gemv(a, (cudaStream_t)stream);
 }
 
+size_t qd_q_gemm_workspace(qd_fmt fmt, int64_t rows, int64_t cols, int t) {
+  if ((fmt != QD_Q4_0 && fmt != QD_Q8_0 && fmt != QD_I8_ROW) || rows < 1 || cols < 64 || cols % 64 || t < 1 ||
+      t > QD_MAX_GEMM_TOKENS)
+    return 0;
+  return gemm_workspace_bytes(cols, t);
+}
+
+qd_status qd_q_gemm(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int t,
+                    void* workspace, size_t workspace_bytes, qd_stream_t stream) {
+  if (!fmt_ok(fmt)) return QD_ERR_UNSUPPORTED;
+  if (fmt != QD_Q4_0 && fmt != QD_Q8_0 && fmt != QD_I8_ROW) return QD_ERR_UNSUPPORTED;
+  if (!W || !x || !y || !workspace) return QD_ERR_INVALID_ARG;
+  if (rows < 1 || rows > (int64_t)1 << 30 || cols < 64 || cols % 64 || cols > (int64_t)1 << 20 || t < 1 ||
+      t > QD_MAX_GEMM_TOKENS)
+    return QD_ERR_SHAPE;
+  if (workspace_bytes < gemm_workspace_bytes(cols, t)) return QD_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(x) || !aligned16(y) || !aligned16(workspace)) return QD_ERR_ALIGN;
+  return launch_q_gemm(fmt, packed_view(fmt, W, rows, cols), x, y, t, workspace, nullptr, (cudaStream_t)stream);
+}
+
 }  // extern "C"

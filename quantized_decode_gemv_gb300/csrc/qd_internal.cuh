@@ -279,6 +279,12 @@ bool gemv_streams(const GemvArgs& a);
 bool gemv_tc_supported(const GemvArgs& a);
 qd_status launch_q_gemv_tc(const GemvArgs& a, cudaStream_t stream);
 
+// Batched prefill product on the tensor cores (Q4_0, Q8_0, INT8 rows; cols % 64 == 0):
+// y[n][r] = sum_c deq(W)[r][c] x[n][c] for n < t; ws holds gemm_workspace_bytes(cols, t).
+size_t gemm_workspace_bytes(int64_t cols, int t);
+qd_status launch_q_gemm(int fmt, const PackedView& W, const float* x, float* y, int t, void* ws, uint32_t* err,
+                        cudaStream_t stream);
+
 qd_status launch_rmsnorm(const float* x, const float* g, float* out, int n, int batch, float eps,
                          cudaStream_t stream);
 qd_status launch_rope(float* v, int n_heads, int head_dim, int64_t batch_stride, const int32_t* pos, int pairing,

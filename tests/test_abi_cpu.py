@@ -79,6 +79,28 @@ def test_gemv_validation_before_any_device_work(lib):
     assert g(9, good, 8, 64, good, good, 1, 0, None) == 4                  # unknown format
 
 
+def test_gemm_validation_before_any_device_work(lib):
+    good = 4096
+    f, w = lib.qd_q_gemm, lib.qd_q_gemm_workspace
+    need = w(0, 300, 512, 80)
+    # B images: 2 token tiles x 8 stages x 16 KB, then 128 f32 unscale factors
+    assert need == 2 * 8 * 16384 + 128 * 4
+    assert w(1, 300, 512, 80) == need and w(3, 300, 512, 80) == need
+    assert w(2, 300, 512, 80) == 0 and w(0, 300, 480, 80) == 0 and w(0, 300, 512, 0) == 0
+    assert w(0, 300, 512, 65537) == 0
+    assert f(2, good, 300, 512, good, good, 80, good, need, None) == 4      # Q4_K: no prefill kernel
+    assert f(9, good, 300, 512, good, good, 80, good, need, None) == 4      # unknown format
+    assert f(0, None, 300, 512, good, good, 80, good, need, None) == 1      # null W
+    assert f(0, good, 300, 512, good, good, 80, None, need, None) == 1      # null workspace
+    assert f(0, good, 300, 480, good, good, 80, good, need, None) == 2      # cols % 64
+    assert f(0, good, 300, 512, good, good, 0, good, need, None) == 2       # t = 0
+    assert f(0, good, 300, 512, good, good, 65537, good, need, None) == 2   # t too large
+    assert f(0, good, 0, 512, good, good, 80, good, need, None) == 2        # no rows
+    assert f(0, good, 300, 512, good, good, 80, good, need - 1, None) == 1  # workspace too small
+    assert f(0, good + 4, 300, 512, good, good, 80, good, need, None) == 3  # misaligned W
+    assert f(0, good, 300, 512, good, good, 80, good + 8, need, None) == 3  # misaligned workspace
+
+
 def test_other_entry_points_validate(lib):
     good = 4096
     assert lib.qd_repack(0, good, 8, 64, good, 10, None) == 6              # dst too small
