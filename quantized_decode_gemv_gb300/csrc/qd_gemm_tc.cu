@@ -41,22 +41,26 @@ constexpr int kMT = 256;          // weight rows per CTA tile
 constexpr int kTN = 64;           // tokens per CTA tile
 constexpr int kN = 2 * kTN;       // MMA N: the tokens' high parts, then their low parts
 constexpr int kKS = 64;           // K elements per stage
-constexpr int kStages = 3;        // A/B stages in shared memory
-constexpr int kCodeRing = 4;      // code stages in flight per converter thread
+constexpr int kAStages = 4;       // A stages in tensor memory
+constexpr int kBStages = 6;       // B stages in shared memory
+constexpr int kCodeRing = 6;      // code stages in flight per converter thread
 constexpr int kConvWarps = 8;     // converter thread = weight row of the tile
 constexpr int kConv = 32 * kConvWarps;
 constexpr int kMmaWarp = kConvWarps, kBWarp = kConvWarps + 1;
 constexpr int kThreads = kConv + 64;
-constexpr uint32_t kASub = 128 * kKS * 2;             // one 128-row A image (16 KB)
-constexpr uint32_t kABytes = 2 * kASub;               // both A images of a stage
 constexpr uint32_t kBBytes = kN * kKS * 2;            // one B image (16 KB)
 constexpr uint32_t kCodeSlot = kConv * 64;            // up to 64 code bytes per row and stage
 constexpr uint32_t kScaleSlot = kConv * 4;            // two f16 block scales per row and stage
 constexpr uint32_t kSbo = (kKS / 8) * kCoreBytes;     // core-matrix step along M/N (1 KB)
-constexpr uint32_t kTmemCols = 512;                   // two sets x two 128-column accumulators
+// Tensor memory: the two 128-row accumulators (kN columns each), then kAStages A stages,
+// each the two 128-row halves of the tile (row r in lane r, two f16 per 32-bit column).
+constexpr uint32_t kAccCols = kN;
+constexpr uint32_t kACols = kKS / 2;                  // one 128-row half of an A stage
+constexpr uint32_t kAStageCols = 2 * kACols;
+constexpr uint32_t kTmemCols = 512;
+static_assert(2 * kAccCols + kAStages * kAStageCols <= kTmemCols, "tensor memory columns");
 constexpr uint32_t kIdesc = idesc_f16(128, kN);
-constexpr uint32_t kSmemBytes =
-    1024 + kStages * (kABytes + kBBytes) + kCodeRing * (kCodeSlot + kScaleSlot);
+constexpr uint32_t kSmemBytes = 1024 + kBStages * kBBytes + kCodeRing * (kCodeSlot + kScaleSlot);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 // code bytes of one row and stage, in 16-byte chunks
@@ -185,16 +189,17 @@ __device__ __forceinline__ void dequant_stage(const uint4 (&q)[4], uint32_t dd, 
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_fa[kStages], bar_fb[kStages], bar_empty[kStages], bar_done[2], bar_drained[2];
+  __shared__ __align__(8) uint64_t bar_fa[kAStages], bar_ea[kAStages], bar_fb[kBStages], bar_eb[kBStages];
+  __shared__ __align__(8) uint64_t bar_done, bar_drained;
   __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* As = smem;                              // [kStages][2][128-row image]
-  uint8_t* Bs = As + kStages * kABytes;            // [kStages][B image]
-  uint8_t* codes = Bs + kStages * kBBytes;         // [kCodeRing][chunk][thread] 16 B
+  uint8_t* Bs = smem;                              // [kBStages][B image]
+  uint8_t* codes = Bs + kBStages * kBBytes;        // [kCodeRing][chunk][thread] 16 B
   uint8_t* dsc = codes + kCodeRing * kCodeSlot;    // [kCodeRing][thread] 4 B
-  const uint32_t fa0 = smem_u32(&bar_fa[0]), fb0 = smem_u32(&bar_fb[0]), empty0 = smem_u32(&bar_empty[0]);
-  const uint32_t done0 = smem_u32(&bar_done[0]), drained0 = smem_u32(&bar_drained[0]);
+  const uint32_t fa0 = smem_u32(&bar_fa[0]), ea0 = smem_u32(&bar_ea[0]);
+  const uint32_t fb0 = smem_u32(&bar_fb[0]), eb0 = smem_u32(&bar_eb[0]);
+  const uint32_t done = smem_u32(&bar_done), drained = smem_u32(&bar_drained);
   const int64_t G = gridDim.x, first = blockIdx.x;
   const int64_t my_tiles = first < p.tiles ? (p.tiles - first + G - 1) / G : 0;
   const int nks = p.nks;
@@ -207,15 +212,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const Params p) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kAStages; ++i) {
       mbar_init(fa0 + 8 * i, kConvWarps);  // one arrival per converter warp
-      mbar_init(fb0 + 8 * i, 1);           // the B copy (bytes)
-      mbar_init(empty0 + 8 * i, 1);        // the MMA commit
+      mbar_init(ea0 + 8 * i, 1);           // the MMA commit
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(done0 + 8 * i, 1);
-      mbar_init(drained0 + 8 * i, kConvWarps);
+    for (int i = 0; i < kBStages; ++i) {
+      mbar_init(fb0 + 8 * i, 1);  // the B copy (bytes)
+      mbar_init(eb0 + 8 * i, 1);  // the MMA commit
     }
+    mbar_init(done, 1);
+    mbar_init(drained, kConvWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   fence_before_sync();
@@ -228,22 +234,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const Params p) {
     bool bad = false;
     constexpr int CH = code_chunks<FMT>();
     const uint32_t codes_s = smem_u32(codes), dsc_s = smem_u32(dsc);
-    // copy cursor: the next stage to copy (local tile it, stage is, ring slot islot)
+    // copy cursor: the next stage to copy (stage is of tile itile, ring slot islot); the
+    // row moves once per tile
     int64_t ig = 0;
-    int64_t it = 0;
+    int64_t itile = first;
     int is = 0, islot = 0;
+    // this thread's row of tile `tile` (rows past the end: any valid row)
+    auto row_of = [&](int64_t tile) { return min((tile / p.tt_tiles) * kMT + tid, p.rows - 1); };
+    int64_t irow = row_of(itile);
     auto issue = [&]() {
       if (ig < total) {
-        const int64_t tile = first + it * G;
-        const int64_t row = min((tile / p.tt_tiles) * kMT + tid, p.rows - 1);  // rows past the end: any valid row
-        const uint8_t* src = p.codes + row * p.row_code_bytes + (int64_t)is * (CH * 16);
+        const uint8_t* src = p.codes + irow * p.row_code_bytes + (int64_t)is * (CH * 16);
         const uint32_t slot = codes_s + (uint32_t)islot * kCodeSlot + 16u * (uint32_t)tid;
 #pragma unroll
         for (int j = 0; j < CH; ++j)
           asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(slot + 16u * kConv * j), "l"(src + 16 * j)
                        : "memory");
         if constexpr (FMT != QD_I8_ROW) {
-          const uint8_t* ssrc = p.scales + row * p.row_scale_bytes + (int64_t)is * 4;
+          const uint8_t* ssrc = p.scales + irow * p.row_scale_bytes + (int64_t)is * 4;
           asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dsc_s + (uint32_t)islot * kScaleSlot +
                                                                           4u * (uint32_t)tid),
                        "l"(ssrc)
@@ -252,7 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const Params p) {
         ++ig;
         if (++is == nks) {
           is = 0;
-          ++it;
+          itile += G;
+          irow = row_of(itile);
         }
         if (++islot == kCodeRing) islot = 0;
       }
@@ -261,65 +270,75 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const Params p) {
     // Read out local tile i: wait for its accumulators, load this thread's row (high and
     // low columns), release them, then scale and store.
     const int sub = warp >> 2, quarter = warp & 3;
+    const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
     auto epilogue = [&](int64_t i) {
-      const int set = (int)(i & 1);
       const int64_t tile = first + i * G;
-      const int64_t row = (tile / p.tt_tiles) * kMT + 128 * sub + 32 * quarter + lane;
+      const int64_t row = (tile / p.tt_tiles) * kMT + tid;
       const int n0 = (int)(tile % p.tt_tiles) * kTN;
-      if (!bad && !mbar_wait(done0 + 8 * set, (uint32_t)(i >> 1) & 1u)) bad = true;
+      if (!bad && !mbar_wait_sleep(done, (uint32_t)i & 1u)) bad = true;
       fence_after_sync();
-      const uint32_t acc = taddr + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(256 * set + 128 * sub);
+      const uint32_t acc = taddr + lane_base + (uint32_t)(kAccCols * sub);
       const float rs = (FMT == QD_I8_ROW && row < p.rows)
                            ? __ldg(reinterpret_cast<const float*>(p.scales + row * p.row_scale_bytes))
                            : 1.f;
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {  // tokens 32 h .. 32 h + 31
+      float v[kTN];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // tokens 32 h .. 32 h + 31: high part + low part
         float hi[32], lo[32];
         tmem_ld32(acc + (uint32_t)(32 * h), hi);
         tmem_ld32(acc + (uint32_t)(kTN + 32 * h), lo);
-        if (h == 1) {
-          fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(drained0 + 8 * set);
-        }
-        if (row < p.rows) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int n = n0 + 32 * h + k;
-            if (n < p.t) p.y[(int64_t)n * p.rows + row] = bad ? 0.f : (hi[k] + lo[k]) * __ldg(p.unscale + n) * rs;
-          }
+        for (int k = 0; k < 32; ++k) v[32 * h + k] = hi[k] + lo[k];
+      }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(drained);  // the accumulators may be overwritten
+      if (row < p.rows) {
+#pragma unroll
+        for (int k = 0; k < kTN; ++k) {
+          const int n = n0 + k;
+          if (n < p.t) p.y[(int64_t)n * p.rows + row] = bad ? 0.f : v[k] * __ldg(p.unscale + n) * rs;
         }
       }
     };
 
 #pragma unroll
     for (int g = 0; g < kCodeRing - 1; ++g) issue();
-    const int epi_at = nks > 1 ? 1 : 0;  // read out the previous tile one stage into this one
     int64_t t = 0;
     int s = 0, cslot = 0, aslot = 0;
     uint32_t afills = 0;  // earlier fills of A stage aslot
-    const uint32_t arow = (uint32_t)(tid & 127);
-    const uint32_t aoff = (uint32_t)sub * kASub + (arow >> 3) * kSbo + (arow & 7) * 16;
+    const uint32_t a_row = taddr + lane_base + kAccCols * 2 + (uint32_t)(kACols * sub);
     for (int64_t g = 0; g < total; ++g) {
       issue();  // stage g + kCodeRing - 1
       asm volatile("cp.async.wait_group %0;" ::"n"(kCodeRing - 1) : "memory");  // stage g landed
       uint4 q[4];
       const uint8_t* cs = codes + cslot * kCodeSlot + 16 * tid;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) q[j] = j < CH ? *reinterpret_cast<const uint4*>(cs + 16 * kConv * j) : make_uint4(0, 0, 0, 0);
-      const uint32_t dd = FMT != QD_I8_ROW ? *reinterpret_cast<const uint32_t*>(dsc + cslot * kScaleSlot + 4 * tid) : 0u;
+      for (int j = 0; j < 4; ++j)
+        q[j] = j < CH ? *reinterpret_cast<const uint4*>(cs + 16 * kConv * j) : make_uint4(0, 0, 0, 0);
+      const uint32_t dd =
+          FMT != QD_I8_ROW ? *reinterpret_cast<const uint32_t*>(dsc + cslot * kScaleSlot + 4 * tid) : 0u;
       uint4 out[8];
       dequant_stage<FMT>(q, dd, out);
-      if (afills > 0 && !bad && !mbar_wait(empty0 + 8 * aslot, (afills - 1) & 1u)) bad = true;  // A stage free
-      uint8_t* dst = As + aslot * kABytes + aoff;
+      uint32_t h[32];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst + c * kCoreBytes) = out[c];
-      fence_proxy_async_smem();
+      for (int c = 0; c < 8; ++c) {
+        h[4 * c + 0] = out[c].x;
+        h[4 * c + 1] = out[c].y;
+        h[4 * c + 2] = out[c].z;
+        h[4 * c + 3] = out[c].w;
+      }
+      if (afills > 0 && !bad && !mbar_wait_sleep(ea0 + 8 * aslot, (afills - 1) & 1u)) bad = true;  // A stage free
+      fence_after_sync();
+      tmem_st32(a_row + (uint32_t)aslot * kAStageCols, h);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(fa0 + 8 * aslot);
-      if (s == epi_at && t >= 1) epilogue(t - 1);
+      // the previous tile's read-out, once this tile's first stage is on its way
+      if (s == 0 && t >= 1) epilogue(t - 1);
       if (++cslot == kCodeRing) cslot = 0;
-      if (++aslot == kStages) {
+      if (++aslot == kAStages) {
         aslot = 0;
         ++afills;
       }
@@ -334,35 +353,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const Params p) {
   } else if (warp == kMmaWarp && lane == 0) {
     // ======================= MMA issue =======================
     bool bad = false;
-    int slot = 0;
-    uint32_t fills = 0;  // earlier fills of stage `slot`
-    const uint32_t a_s = smem_u32(As), b_s = smem_u32(Bs);
+    int64_t g = 0;
+    const uint32_t b_s = smem_u32(Bs);
     for (int64_t i = 0; i < my_tiles && !bad; ++i) {
-      const int set = (int)(i & 1);
-      if (i >= 2 && !mbar_wait(drained0 + 8 * set, (uint32_t)((i - 2) >> 1) & 1u)) bad = true;
+      if (i >= 1 && !mbar_wait(drained, (uint32_t)(i - 1) & 1u)) bad = true;  // the last tile is read out
       fence_after_sync();
-      for (int ks = 0; ks < nks && !bad; ++ks) {
-        if (!mbar_wait(fa0 + 8 * slot, fills & 1u) || !mbar_wait(fb0 + 8 * slot, fills & 1u)) {
+      for (int ks = 0; ks < nks && !bad; ++ks, ++g) {
+        const int as = (int)(g % kAStages), bs = (int)(g % kBStages);
+        if (!mbar_wait(fa0 + 8 * as, (uint32_t)(g / kAStages) & 1u) ||
+            !mbar_wait(fb0 + 8 * bs, (uint32_t)(g / kBStages) & 1u)) {
           bad = true;
           break;
         }
         fence_after_sync();
+        const uint32_t b0 = b_s + (uint32_t)bs * kBBytes;
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-          const uint32_t d = taddr + (uint32_t)(256 * set + 128 * m);
-          const uint32_t a0 = a_s + (uint32_t)slot * kABytes + (uint32_t)m * kASub;
-          const uint32_t b0 = b_s + (uint32_t)slot * kBBytes;
+          const uint32_t d = taddr + (uint32_t)(kAccCols * m);
+          const uint32_t a0 = taddr + kAccCols * 2 + (uint32_t)as * kAStageCols + (uint32_t)(kACols * m);
 #pragma unroll
-          for (int kk = 0; kk < kKS / 16; ++kk)  // 16 K elements = two core matrices per instruction
-            mma_f16_ss(d, smem_desc(a0 + kk * 2 * kCoreBytes, kCoreBytes, kSbo),
-                       smem_desc(b0 + kk * 2 * kCoreBytes, kCoreBytes, kSbo), kIdesc, (ks > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kKS / 16; ++kk)  // 16 K elements: 8 columns of A, two core matrices of B
+            mma_f16_ts(d, a0 + 8u * kk, smem_desc(b0 + kk * 2 * kCoreBytes, kCoreBytes, kSbo), kIdesc,
+                       (ks > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(empty0 + 8 * slot);
-        if (ks == nks - 1) mma_commit(done0 + 8 * set);
-        if (++slot == kStages) {
-          slot = 0;
-          ++fills;
-        }
+        mma_commit(ea0 + 8 * as);
+        mma_commit(eb0 + 8 * bs);
+        if (ks == nks - 1) mma_commit(done);
       }
     }
     if (bad && p.err) atomicOr(p.err, kErrTimeout);
@@ -376,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const Params p) {
     for (int64_t i = 0; i < my_tiles && !bad; ++i) {
       const int64_t tt = (first + i * G) % p.tt_tiles;
       for (int ks = 0; ks < nks; ++ks) {
-        if (fills > 0 && !mbar_wait(empty0 + 8 * slot, (fills - 1) & 1u)) {
+        if (fills > 0 && !mbar_wait(eb0 + 8 * slot, (fills - 1) & 1u)) {
           bad = true;
           break;
         }
@@ -384,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const Params p) {
         bulk_copy_g2s(b_s + (uint32_t)slot * kBBytes, p.bimg + (tt * nks + ks) * (int64_t)kBBytes, kBBytes,
                       fb0 + 8 * slot);
         ++issued;
-        if (++slot == kStages) {
+        if (++slot == kBStages) {
           slot = 0;
           ++fills;
         }
@@ -392,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const Params p) {
     }
     // stay until the last copy into each stage has landed: no copy may target the CTA's
     // shared memory after it exits
-    for (int64_t k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
-      if (!mbar_wait(fb0 + 8 * (int)(k % kStages), (uint32_t)(k / kStages) & 1u)) bad = true;
+    for (int64_t k = issued > kBStages ? issued - kBStages : 0; k < issued; ++k)
+      if (!mbar_wait(fb0 + 8 * (int)(k % kBStages), (uint32_t)(k / kBStages) & 1u)) bad = true;
     if (bad && p.err) atomicOr(p.err, kErrTimeout);
   }
   fence_before_sync();
