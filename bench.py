@@ -335,6 +335,12 @@ def run_ours(args, world, rank, local):
         out["roofline"] = roofline_dominant(qd, torch, stream, hbm, peak_kind)
         out["q_gemv_sweep"] = gemv_sweep(qd, torch, stream, hbm, args)
         out["quantize_i8"] = bench_quantize(qd, torch, 49152, 2048, hbm)
+        _, bf16, _ = peaks()
+        out["prefill_gemm"] = []
+        for fmt, r_, c_ in (("q4_0", 14336, 4096), ("q8_0", 14336, 4096), ("i8", 8192, 2048)):
+            g = bench_gemm(qd, torch, fmt, r_, c_, 512, 10)
+            g["frac_of_bf16_peak"] = round(g["useful_TFLOP/s"] / bf16, 4)
+            out["prefill_gemm"].append(g)
         del model
         torch.cuda.empty_cache()
         if not args.no_1p7b:

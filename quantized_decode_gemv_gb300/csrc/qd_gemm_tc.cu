@@ -5,21 +5,24 @@
 //
 //  * A (the weights): a CTA tile is 256 rows (two MMA tiles of M = 128) by 64 tokens.  Eight
 //    converter warps, one thread per row, stream the packed codes of each 64-column stage
-//    through a per-thread cp.async ring and write the dequantised f16 values into the
-//    stage's two A images (shared memory, K-major, no-swizzle canonical layout).  Q4_0 and
-//    Q8_0: the code is widened exactly (magic-number f16) and multiplied by the block's
-//    f16 scale in f16: the weight enters as the binary16 rounding of d * q.  INT8 rows:
-//    the code enters exactly, the row scale is applied in f32 at the end.
+//    through a per-thread cp.async ring (six stages deep), dequantise them to f16 and write
+//    them with one tcgen05.st into one of four A stages in tensor memory (row r of an MMA
+//    tile in lane r, two f16 per 32-bit column).  Q4_0 and Q8_0: the code is widened
+//    exactly (magic-number f16) and multiplied by the block's f16 scale in f16: the weight
+//    enters as the binary16 rounding of d * q.  INT8 rows: the code enters exactly, the row
+//    scale is applied in f32 at the end.
 //  * B (x): a prologue kernel scales each token's x by a power of two (its largest |x| in
 //    [2^13, 2^14), exact) and splits it into an f16 high part and the f16 rounding of the
 //    remainder (about 2^-22 relative together), laid out in a workspace as the exact
-//    shared-memory image of each (64-token tile, stage): 64 high rows, then 64 low rows.
-//    One thread streams the images in with bulk copies.
+//    shared-memory image of each (64-token tile, stage): 64 high rows, then 64 low rows
+//    (K-major, no-swizzle canonical layout).  One thread streams the images into a
+//    six-stage ring with bulk copies.
 //  * MMAs: one thread issues, per stage, 2 x 4 tcgen05.mma kind::f16 (M = 128, N = 128,
-//    K = 16) into the tile's two accumulators in tensor memory; tiles alternate between
-//    two accumulator sets (all 512 columns), so the read-out of one tile overlaps the
-//    MMAs of the next.  The converter warps read a tile's accumulators out (tcgen05.ld)
-//    one stage into the next tile: y = (high + low) * 2^-e (* row scale).
+//    K = 16; A from tensor memory, B from shared memory) into the tile's two 128-column
+//    accumulators.  The A stages take the rest of tensor memory, so there is one
+//    accumulator set: the converter warps read a tile out (tcgen05.ld) right after the
+//    next tile's first stage, y = (high + low) * 2^-e (* row scale), and the MMAs of the
+//    next tile start once the read-out has released the accumulators.
 //  * Tiles (row tile, token tile), token tile fastest, are dealt to persistent CTAs (one
 //    per SM): CTAs running at the same time share row tiles, so the weights come from
 //    HBM about once and from L2 for the other token tiles.
