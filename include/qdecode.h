@@ -75,9 +75,40 @@ typedef enum {
  *            nibble, sub-block 2c) and element 64c+32+l (high nibble, sub-block 2c+1).
  *  QD_I8_ROW per-row symmetric INT8: int8 codes [rows][cols], then one f32 scale
  *            per row; value q*s_row.
+ * The formats a Q4_K_M-class file mixes in ([go-llm] package overview: its first
+ * model's Q4_0 file holds Q4_0, Q4_1 and Q8_0 tensors; [llamini] summary table,
+ * "Quants": Q4_K, Q6_K, Q5_0, Q5_K, Q4_0, Q4_1, Q8_0, F16; [llmoxide] 10: Q6_K).  The pages name them and give Q6_K's 6.6 bits per weight; the
+ * byte layouts (not on the pages) are the GGUF ones:
+ *  QD_Q4_1   blocks of 32, 20 B: f16 d, f16 m, 16 B of 4-bit codes (order as Q4_0);
+ *            value d*q + m.
+ *  QD_Q5_0   blocks of 32, 22 B: f16 d, 4 B qh (little-endian; bit j is the fifth bit
+ *            of element j), 16 B of low nibbles (order as Q4_0); value (q-16)*d.
+ *  QD_Q5_K   super-blocks of 256, 176 B: f16 d, f16 dmin, 12 B of 6-bit (scale, min)
+ *            as Q4_K, 32 B qh, 128 B of low nibbles (order as Q4_K); element 64c+l
+ *            takes bit 2c of qh[l] as its fifth bit, element 64c+32+l bit 2c+1;
+ *            value d*sc*q - dmin*m.
+ *  QD_Q6_K   super-blocks of 256, 210 B: 128 B ql (low nibbles), 64 B qh (two-bit
+ *            high parts), 16 int8 scales (one per 16 weights), f16 d; in half h
+ *            (elements 128h..128h+127) element 128h+32k+l (k 0..3, l 0..31) takes the
+ *            low (k < 2) or high (k >= 2) nibble of ql[64h + l + 32 (k & 1)], bits
+ *            2k, 2k+1 of qh[32h + l] above it, and scale 8h + 2k + l/16;
+ *            value d*sc*(q-32).
+ *  QD_F16    binary16 weights, 2 B each (little-endian).
  * The "source" layout of a tensor is the model-file layout above, rows in order
- * (for QD_I8_ROW: all codes, then all scales, in one buffer). */
-typedef enum { QD_Q4_0 = 0, QD_Q8_0 = 1, QD_Q4_K = 2, QD_I8_ROW = 3 } qd_fmt;
+ * (for QD_I8_ROW: all codes, then all scales, in one buffer).  The decode step
+ * (qd_model_*) takes QD_Q4_0, QD_Q8_0, QD_Q4_K and QD_I8_ROW; the layout calls,
+ * qd_dequant, qd_embed and qd_q_gemv take every format. */
+typedef enum {
+    QD_Q4_0 = 0,
+    QD_Q8_0 = 1,
+    QD_Q4_K = 2,
+    QD_I8_ROW = 3,
+    QD_Q4_1 = 4,
+    QD_Q5_0 = 5,
+    QD_Q5_K = 6,
+    QD_Q6_K = 7,
+    QD_F16 = 8
+} qd_fmt;
 
 /* RoPE pairing ([llmoxide] 6): ADJACENT rotates (2i, 2i+1) (llama files), HALF
  * rotates (i, i + head_dim/2) (NeoX/Qwen). */
@@ -104,12 +135,19 @@ qd_status qd_bf16_to_f32(const uint16_t* in, float* out, int64_t n, qd_stream_t 
 /*  Q4_K: codes [rows][cols/256][128 B], then headers [rows][cols/256][16 B]  */
 /*        (d, dmin, 12 scale bytes).                                          */
 /*  I8_ROW: codes [rows][cols], then f32 scales [rows].                       */
+/*  Q4_1: codes [rows][cols/32][16 B], then (d, m) [rows][cols/32][4 B].      */
+/*  Q5_0: low nibbles [rows][cols/32][16 B], then (d, qh) [rows][cols/32][6 B]. */
+/*  Q5_K: (qh, low nibbles) [rows][cols/256][160 B], then headers            */
+/*        [rows][cols/256][16 B] (d, dmin, 12 scale bytes).                   */
+/*  Q6_K: (ql, qh) [rows][cols/256][192 B], then (16 scales, d)               */
+/*        [rows][cols/256][18 B].                                             */
+/*  F16:  weights [rows][cols] (2 B each); no scale region.                   */
 /* The repack is lossless: qd_unpack restores the source bytes exactly.       */
 /* ------------------------------------------------------------------------- */
 
 /* Bytes of the source / packed layout; 0 for a shape the format does not allow
- * (rows < 1, cols < 1, cols % 32 for Q4_0/Q8_0, cols % 256 for Q4_K, cols % 16
- * for I8_ROW). */
+ * (rows < 1, cols < 1, cols % 32 for Q4_0/Q8_0/Q4_1/Q5_0/F16, cols % 256 for
+ * Q4_K/Q5_K/Q6_K, cols % 16 for I8_ROW). */
 size_t qd_src_bytes(qd_fmt fmt, int64_t rows, int64_t cols);
 size_t qd_packed_bytes(qd_fmt fmt, int64_t rows, int64_t cols);
 

@@ -20,7 +20,7 @@ _SRC = os.path.join(_HERE, "qd_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
-FMT = {"q4_0": 0, "q8_0": 1, "q4_k": 2, "i8": 3}
+FMT = {"q4_0": 0, "q8_0": 1, "q4_k": 2, "i8": 3, "q4_1": 4, "q5_0": 5, "q5_k": 6, "q6_k": 7, "f16": 8}
 PAIRING = {"adjacent": 0, "half": 1}
 
 

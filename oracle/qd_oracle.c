@@ -48,7 +48,7 @@
 #include <omp.h>
 #endif
 
-enum { OR_Q4_0 = 0, OR_Q8_0 = 1, OR_Q4_K = 2, OR_I8_ROW = 3 };
+enum { OR_Q4_0 = 0, OR_Q8_0 = 1, OR_Q4_K = 2, OR_I8_ROW = 3, OR_Q4_1 = 4, OR_Q5_0 = 5, OR_Q5_K = 6, OR_Q6_K = 7, OR_F16 = 8 };
 enum { OR_ROPE_ADJACENT = 0, OR_ROPE_HALF = 1 };
 
 /* ------------------------------------------------------------------------- */
@@ -142,6 +142,11 @@ static int64_t row_bytes(int fmt, int64_t cols) {
         case OR_Q8_0: return (cols / 32) * 34;
         case OR_Q4_K: return (cols / 256) * 144;
         case OR_I8_ROW: return cols;
+        case OR_Q4_1: return (cols / 32) * 20;
+        case OR_Q5_0: return (cols / 32) * 22;
+        case OR_Q5_K: return (cols / 256) * 176;
+        case OR_Q6_K: return (cols / 256) * 210;
+        case OR_F16: return cols * 2;
         default: return -1;
     }
 }
@@ -150,9 +155,14 @@ int or_shape_ok(int fmt, int64_t rows, int64_t cols) {
     if (rows <= 0 || cols <= 0) return 0;
     switch (fmt) {
         case OR_Q4_0:
-        case OR_Q8_0: return cols % 32 == 0;
-        case OR_Q4_K: return cols % 256 == 0;
-        case OR_I8_ROW: return 1;
+        case OR_Q8_0:
+        case OR_Q4_1:
+        case OR_Q5_0: return cols % 32 == 0;
+        case OR_Q4_K:
+        case OR_Q5_K:
+        case OR_Q6_K: return cols % 256 == 0;
+        case OR_I8_ROW:
+        case OR_F16: return 1;
         default: return 0;
     }
 }
@@ -195,6 +205,81 @@ static void dequant_row(int fmt, const uint8_t* w, int64_t rows, int64_t cols, i
                 }
             }
         }
+    } else if (fmt == OR_Q4_1) {
+        /* d, m, then 16 bytes of codes as Q4_0; value d*q + m */
+        for (int64_t b = 0; b < cols / 32; ++b) {
+            const uint8_t* blk = row + b * 20;
+            const double d = f16_at(blk), m = f16_at(blk + 2);
+            for (int j = 0; j < 16; ++j) {
+                out[b * 32 + j] = (float)(d * (blk[4 + j] & 0x0F) + m);
+                out[b * 32 + j + 16] = (float)(d * (blk[4 + j] >> 4) + m);
+            }
+        }
+    } else if (fmt == OR_Q5_0) {
+        /* d, a 32-bit word of fifth bits (bit j for element j), low nibbles as Q4_0;
+         * value (q - 16) * d */
+        for (int64_t b = 0; b < cols / 32; ++b) {
+            const uint8_t* blk = row + b * 22;
+            const double d = f16_at(blk);
+            const uint32_t qh = (uint32_t)blk[2] | ((uint32_t)blk[3] << 8) | ((uint32_t)blk[4] << 16) |
+                                ((uint32_t)blk[5] << 24);
+            for (int j = 0; j < 16; ++j) {
+                const int lo = (blk[6 + j] & 0x0F) | (int)(((qh >> j) & 1u) << 4);
+                const int hi = (blk[6 + j] >> 4) | (int)(((qh >> (j + 16)) & 1u) << 4);
+                out[b * 32 + j] = (float)((lo - 16) * d);
+                out[b * 32 + j + 16] = (float)((hi - 16) * d);
+            }
+        }
+    } else if (fmt == OR_Q5_K) {
+        /* Q4_K's header, then 32 bytes of fifth bits and 128 bytes of low nibbles: chunk c
+         * of 64 takes bit 2c of byte l for element l and bit 2c+1 for element 32+l */
+        for (int64_t s = 0; s < cols / 256; ++s) {
+            const uint8_t* blk = row + s * 176;
+            const double d = f16_at(blk), dmin = f16_at(blk + 2);
+            const uint8_t* scales = blk + 4;
+            const uint8_t* qh = blk + 16;
+            const uint8_t* qs = blk + 48;
+            for (int c = 0; c < 4; ++c) {
+                uint8_t sc0, m0, sc1, m1;
+                or_get_scale_min_k4(2 * c, scales, &sc0, &m0);
+                or_get_scale_min_k4(2 * c + 1, scales, &sc1, &m1);
+                for (int l = 0; l < 32; ++l) {
+                    const int lo = (qs[32 * c + l] & 0x0F) + (((qh[l] >> (2 * c)) & 1) ? 16 : 0);
+                    const int hi = (qs[32 * c + l] >> 4) + (((qh[l] >> (2 * c + 1)) & 1) ? 16 : 0);
+                    out[s * 256 + 64 * c + l] = (float)(d * sc0 * lo - dmin * m0);
+                    out[s * 256 + 64 * c + 32 + l] = (float)(d * sc1 * hi - dmin * m1);
+                }
+            }
+        }
+    } else if (fmt == OR_Q6_K) {
+        /* 128 bytes of low nibbles, 64 bytes of two-bit high parts, 16 signed scales, d.
+         * Each half of 128 elements uses 64 low-nibble bytes and 32 high-part bytes: byte l
+         * of the half's high parts carries, two bits each, the high parts of elements l,
+         * 32+l, 64+l and 96+l; low-nibble bytes l and 32+l give elements l, 32+l (low
+         * nibbles) and 64+l, 96+l (high nibbles).  Scale i covers elements 16i..16i+15.
+         * value d * scale * (q - 32) */
+        for (int64_t s = 0; s < cols / 256; ++s) {
+            const uint8_t* blk = row + s * 210;
+            const double d = f16_at(blk + 208);
+            const int8_t* sc = (const int8_t*)(blk + 192);
+            for (int h = 0; h < 2; ++h) {
+                const uint8_t* ql = blk + 64 * h;
+                const uint8_t* qh = blk + 128 + 32 * h;
+                float* o = out + s * 256 + 128 * h;
+                for (int l = 0; l < 32; ++l) {
+                    const int q0 = (ql[l] & 0x0F) | ((qh[l] & 3) << 4);
+                    const int q1 = (ql[32 + l] & 0x0F) | (((qh[l] >> 2) & 3) << 4);
+                    const int q2 = (ql[l] >> 4) | (((qh[l] >> 4) & 3) << 4);
+                    const int q3 = (ql[32 + l] >> 4) | (((qh[l] >> 6) & 3) << 4);
+                    o[l] = (float)(d * sc[8 * h + (l / 16)] * (q0 - 32));
+                    o[32 + l] = (float)(d * sc[8 * h + 2 + (l / 16)] * (q1 - 32));
+                    o[64 + l] = (float)(d * sc[8 * h + 4 + (l / 16)] * (q2 - 32));
+                    o[96 + l] = (float)(d * sc[8 * h + 6 + (l / 16)] * (q3 - 32));
+                }
+            }
+        }
+    } else if (fmt == OR_F16) {
+        for (int64_t c = 0; c < cols; ++c) out[c] = (float)f16_at(row + 2 * c);
     } else { /* OR_I8_ROW ([minillm] "Quantization": one scale per output row) */
         float s;
         memcpy(&s, w + rows * cols + 4 * r, sizeof s);

@@ -30,8 +30,8 @@ _SRC = os.path.join(_HERE, "qdsynth.c")
 _LIB_PATH = os.path.join(_HERE, "libqdsynth.so")
 _lib = None
 
-BLOCK_BYTES = {"q4_0": 18, "q8_0": 34, "q4_k": 144}
-BLOCK_WEIGHTS = {"q4_0": 32, "q8_0": 32, "q4_k": 256}
+BLOCK_BYTES = {"q4_0": 18, "q8_0": 34, "q4_k": 144, "q4_1": 20, "q5_0": 22, "q5_k": 176, "q6_k": 210, "f16": 2}
+BLOCK_WEIGHTS = {"q4_0": 32, "q8_0": 32, "q4_k": 256, "q4_1": 32, "q5_0": 32, "q5_k": 256, "q6_k": 256, "f16": 1}
 
 
 def build(force: bool = False) -> str:
@@ -167,6 +167,82 @@ def q4_k_blocks(seed, name, rows, cols, row0=0, nrows=None) -> np.ndarray:
     return out
 
 
+def _f16_field(out, lo_byte, seed, name, nrows, nb, rng, row0):
+    v = f16_bits_uniform(seed, name, nrows * nb, *rng, offset=row0 * nb)
+    out[:, :, lo_byte:lo_byte + 2] = v.reshape(nrows, nb, 1).view(np.uint8).reshape(nrows, nb, 2)
+
+
+def _byte_field(out, lo, hi, seed, name, nrows, nb, row0, vlo=0, vhi=255):
+    n = hi - lo
+    q = ints_u8(seed, name, nrows * nb * n, vlo, vhi, offset=row0 * nb * n)
+    out[:, :, lo:hi] = q.reshape(nrows, nb, n)
+
+
+M_RANGE = (-0.16, 0.0)  # Q4_1 block minimum (about -8 d, so values straddle 0)
+
+
+def q4_1_blocks(seed, name, rows, cols, row0=0, nrows=None) -> np.ndarray:
+    """Q4_1 tensor as uint8 ``[nrows][cols/32][20]``: d, m, 16 code bytes."""
+    assert cols % 32 == 0
+    nrows = rows - row0 if nrows is None else nrows
+    nb = cols // 32
+    out = np.empty((nrows, nb, 20), dtype=np.uint8)
+    _f16_field(out, 0, seed, name + ".d", nrows, nb, D_RANGE, row0)
+    _f16_field(out, 2, seed, name + ".m", nrows, nb, M_RANGE, row0)
+    _byte_field(out, 4, 20, seed, name + ".qs", nrows, nb, row0)
+    return out
+
+
+def q5_0_blocks(seed, name, rows, cols, row0=0, nrows=None) -> np.ndarray:
+    """Q5_0 tensor as uint8 ``[nrows][cols/32][22]``: d, 4 bytes of fifth bits, 16 code bytes."""
+    assert cols % 32 == 0
+    nrows = rows - row0 if nrows is None else nrows
+    nb = cols // 32
+    out = np.empty((nrows, nb, 22), dtype=np.uint8)
+    _f16_field(out, 0, seed, name + ".d", nrows, nb, D_RANGE, row0)
+    _byte_field(out, 2, 6, seed, name + ".qh", nrows, nb, row0)
+    _byte_field(out, 6, 22, seed, name + ".qs", nrows, nb, row0)
+    return out
+
+
+def q5_k_blocks(seed, name, rows, cols, row0=0, nrows=None) -> np.ndarray:
+    """Q5_K tensor as uint8 ``[nrows][cols/256][176]``: d, dmin, 12 scale bytes, 32 bytes
+    of fifth bits, 128 code bytes."""
+    assert cols % 256 == 0
+    nrows = rows - row0 if nrows is None else nrows
+    nb = cols // 256
+    out = np.empty((nrows, nb, 176), dtype=np.uint8)
+    _f16_field(out, 0, seed, name + ".d", nrows, nb, D_RANGE, row0)
+    _f16_field(out, 2, seed, name + ".dmin", nrows, nb, D_RANGE, row0)
+    _byte_field(out, 4, 16, seed, name + ".scales", nrows, nb, row0)
+    _byte_field(out, 16, 48, seed, name + ".qh", nrows, nb, row0)
+    _byte_field(out, 48, 176, seed, name + ".qs", nrows, nb, row0)
+    return out
+
+
+Q6K_D_RANGE = (0.0002, 0.002)  # d of a Q6_K super-block (scales are whole int8)
+
+
+def q6_k_blocks(seed, name, rows, cols, row0=0, nrows=None) -> np.ndarray:
+    """Q6_K tensor as uint8 ``[nrows][cols/256][210]``: 128 low-nibble bytes, 64 high-part
+    bytes, 16 int8 scales, d."""
+    assert cols % 256 == 0
+    nrows = rows - row0 if nrows is None else nrows
+    nb = cols // 256
+    out = np.empty((nrows, nb, 210), dtype=np.uint8)
+    _byte_field(out, 0, 192, seed, name + ".q", nrows, nb, row0)
+    _byte_field(out, 192, 208, seed, name + ".scales", nrows, nb, row0, -127, 127)
+    _f16_field(out, 208, seed, name + ".d", nrows, nb, Q6K_D_RANGE, row0)
+    return out
+
+
+def f16_weights(seed, name, rows, cols, row0=0, nrows=None) -> np.ndarray:
+    """F16 tensor as uint8 ``[nrows][cols][2]``: values ~U[-1, 1) rounded to binary16."""
+    nrows = rows - row0 if nrows is None else nrows
+    v = f16_bits_uniform(seed, name, nrows * cols, -1.0, 1.0, offset=row0 * cols)
+    return v.view(np.uint8).reshape(nrows, cols, 2)
+
+
 I8_SCALE_RANGE = (1e-4, 1e-2)
 
 
@@ -194,7 +270,11 @@ def weight_src(fmt: str, seed: int, name: str, rows: int, cols: int) -> np.ndarr
         return q4_k_blocks(seed, name, rows, cols).reshape(-1)
     if fmt == "i8":
         return i8_row_src(seed, name, rows, cols)
-    raise ValueError(fmt)
+    gen = {"q4_1": q4_1_blocks, "q5_0": q5_0_blocks, "q5_k": q5_k_blocks, "q6_k": q6_k_blocks,
+           "f16": f16_weights}.get(fmt)
+    if gen is None:
+        raise ValueError(fmt)
+    return gen(seed, name, rows, cols).reshape(-1)
 
 
 def src_bytes(fmt: str, rows: int, cols: int) -> int:

@@ -15,7 +15,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqdecode.so")
 _lib = None
 
-FMT = {"q4_0": 0, "q8_0": 1, "q4_k": 2, "i8": 3}
+FMT = {"q4_0": 0, "q8_0": 1, "q4_k": 2, "i8": 3, "q4_1": 4, "q5_0": 5, "q5_k": 6, "q6_k": 7, "f16": 8}
 PAIRING = {"adjacent": 0, "half": 1}
 MAX_BATCH = 16
 STATUS = {0: "QD_OK", 1: "QD_ERR_INVALID_ARG", 2: "QD_ERR_SHAPE", 3: "QD_ERR_ALIGN", 4: "QD_ERR_UNSUPPORTED",

@@ -295,12 +295,148 @@ __global__ void __launch_bounds__(kThreads) k_gemv_q4k(PackedView W, const float
   finish_rows<R, NB>(acc, row_scale, row0, W.rows, y, batch, mode, lane);
 }
 
+// The formats a Q4_K_M-class file mixes in (Q4_1, Q5_0, Q5_K, Q6_K, F16): the 32
+// dequantised f32 values of unit u (columns 32u .. 32u + 31) of row r, each rounded once
+// (as the test dequantiser).
+__device__ __forceinline__ float f16lo(uint32_t w) { return f16_bits_to_f32(w & 0xFFFFu); }
+__device__ __forceinline__ float f16hi(uint32_t w) { return f16_bits_to_f32(w >> 16); }
+
+template <int FMT>
+__device__ __forceinline__ void deq_unit(const PackedView& W, int64_t r, int64_t u, float (&w)[32]) {
+  const uint8_t* cr = W.codes + r * W.row_code_bytes;
+  const uint8_t* sr = W.scales + r * W.row_scale_bytes;
+  if constexpr (FMT == QD_F16) {
+    const uint4* p = reinterpret_cast<const uint4*>(cr + 64 * u);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint4 v = ld_stream_v4(p + t);
+      const uint32_t h[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        w[8 * t + 2 * k] = f16lo(h[k]);
+        w[8 * t + 2 * k + 1] = f16hi(h[k]);
+      }
+    }
+  } else if constexpr (FMT == QD_Q4_1 || FMT == QD_Q5_0) {
+    const uint4 q = ld_stream_v4(cr + 16 * u);
+    const uint8_t bytes[16] = {
+        (uint8_t)q.x, (uint8_t)(q.x >> 8), (uint8_t)(q.x >> 16), (uint8_t)(q.x >> 24),
+        (uint8_t)q.y, (uint8_t)(q.y >> 8), (uint8_t)(q.y >> 16), (uint8_t)(q.y >> 24),
+        (uint8_t)q.z, (uint8_t)(q.z >> 8), (uint8_t)(q.z >> 16), (uint8_t)(q.z >> 24),
+        (uint8_t)q.w, (uint8_t)(q.w >> 8), (uint8_t)(q.w >> 16), (uint8_t)(q.w >> 24)};
+    if constexpr (FMT == QD_Q4_1) {
+      const uint32_t dm = __ldg(reinterpret_cast<const uint32_t*>(sr + 4 * u));
+      const float d = f16lo(dm), m = f16hi(dm);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        w[j] = fmaf(d, (float)(bytes[j] & 15), m);
+        w[j + 16] = fmaf(d, (float)(bytes[j] >> 4), m);
+      }
+    } else {
+      const unsigned short* h = reinterpret_cast<const unsigned short*>(sr + 6 * u);
+      const float d = f16_bits_to_f32(__ldg(h));
+      const uint32_t qh = (uint32_t)__ldg(h + 1) | ((uint32_t)__ldg(h + 2) << 16);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        w[j] = (float)((int)((bytes[j] & 15) | (((qh >> j) & 1u) << 4)) - 16) * d;
+        w[j + 16] = (float)((int)((bytes[j] >> 4) | (((qh >> (j + 16)) & 1u) << 4)) - 16) * d;
+      }
+    }
+  } else {  // Q5_K, Q6_K: unit v = u % 8 of super-block s = u / 8
+    const int64_t sb = u >> 3;
+    const int v = (int)(u & 7);
+    uint8_t lq[32], hq[32];  // low-nibble bytes and high-bit bytes of the unit
+    const uint8_t* lp;
+    const uint8_t* hp;
+    if constexpr (FMT == QD_Q5_K) {
+      lp = cr + sb * 160 + 32 + 32 * (v >> 1);
+      hp = cr + sb * 160;
+    } else {
+      lp = cr + sb * 192 + 64 * (v >> 2) + 32 * (v & 1);
+      hp = cr + sb * 192 + 128 + 32 * (v >> 2);
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const uint4 a = ld_stream_v4(lp + 16 * t), b = ld_stream_v4(hp + 16 * t);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        lq[16 * t + k] = (uint8_t)(aw[k >> 2] >> (8 * (k & 3)));
+        hq[16 * t + k] = (uint8_t)(bw[k >> 2] >> (8 * (k & 3)));
+      }
+    }
+    if constexpr (FMT == QD_Q5_K) {
+      const uint4 hdr = __ldg(reinterpret_cast<const uint4*>(sr + sb * 16));
+      uint8_t sbytes[12];
+      const uint32_t hw[3] = {hdr.y, hdr.z, hdr.w};
+#pragma unroll
+      for (int k = 0; k < 12; ++k) sbytes[k] = (uint8_t)(hw[k >> 2] >> (8 * (k & 3)));
+      int sc, m;
+      q4k_scale_min(v, sbytes, sc, m);  // sub-block v = 2 chunk + high
+      const float a = f16lo(hdr.x) * (float)sc, b = -(f16hi(hdr.x) * (float)m);
+      const int shift = v & 1 ? 4 : 0;
+#pragma unroll
+      for (int l = 0; l < 32; ++l) {
+        const int q = ((lq[l] >> shift) & 15) | (((hq[l] >> v) & 1) << 4);
+        w[l] = fmaf(a, (float)q, b);
+      }
+    } else {
+      const int h = v >> 2, k = v & 3;
+      const uint8_t* hdr = sr + sb * 18;
+      const float d = f16_bits_to_f32(__ldg(reinterpret_cast<const unsigned short*>(hdr + 16)));
+      const float s0 = d * (float)(int8_t)__ldg(hdr + 8 * h + 2 * k);
+      const float s1 = d * (float)(int8_t)__ldg(hdr + 8 * h + 2 * k + 1);
+      const int shift = k < 2 ? 0 : 4;
+#pragma unroll
+      for (int l = 0; l < 32; ++l) {
+        const int q = ((lq[l] >> shift) & 15) | (((hq[l] >> (2 * k)) & 3) << 4);
+        w[l] = (l < 16 ? s0 : s1) * (float)(q - 32);
+      }
+    }
+  }
+}
+
+// Q4_1, Q5_0, Q5_K, Q6_K, F16: each lane dequantises its 32-column units to f32 and dots
+// them with x.
+template <int FMT, int R, int NB>
+__global__ void __launch_bounds__(kThreads) k_gemv_deq(PackedView W, const float* __restrict__ x,
+                                                        float* __restrict__ y, int batch, int mode) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row0 = ((int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)) * R;
+  if (row0 >= W.rows) return;
+  const int64_t units = W.cols / 32;
+  float acc[R][NB];
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[i][b] = 0.f;
+  for (int64_t u = lane; u < units; u += 32) {
+    float w[R][32];
+#pragma unroll
+    for (int i = 0; i < R; ++i) deq_unit<FMT>(W, row0 + i < W.rows ? row0 + i : row0, u, w[i]);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      if (b < batch) {
+        const float* xp = x + (int64_t)b * W.cols + u * 32;
+#pragma unroll
+        for (int i = 0; i < R; ++i) acc[i][b] += dot_x<32>(w[i], xp);
+      }
+    }
+  }
+  float row_scale[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) row_scale[i] = 1.0f;
+  finish_rows<R, NB>(acc, row_scale, row0, W.rows, y, batch, mode, lane);
+}
+
 template <int FMT, int R, int NB>
 qd_status launch_t(const PackedView& W, const float* x, float* y, int batch, int mode, cudaStream_t stream) {
   const int64_t warps = (W.rows + R - 1) / R;
   const int64_t ctas = (warps + kWarpsPerCta - 1) / kWarpsPerCta;
   if constexpr (FMT == QD_Q4_K)
     k_gemv_q4k<R, NB><<<(unsigned)ctas, kThreads, 0, stream>>>(W, x, y, batch, mode);
+  else if constexpr (FMT >= QD_Q4_1)
+    k_gemv_deq<FMT, R, NB><<<(unsigned)ctas, kThreads, 0, stream>>>(W, x, y, batch, mode);
   else
     k_gemv_blocks<FMT, R, NB><<<(unsigned)ctas, kThreads, 0, stream>>>(W, x, y, batch, mode);
   return launch_status();
@@ -342,6 +478,11 @@ qd_status launch_q_gemv(const GemvArgs& a, cudaStream_t stream) {
     case QD_Q8_0: return launch_fmt<QD_Q8_0>(a.W, a.x, a.y, a.batch, a.mode, stream);
     case QD_Q4_K: return launch_fmt<QD_Q4_K>(a.W, a.x, a.y, a.batch, a.mode, stream);
     case QD_I8_ROW: return launch_fmt<QD_I8_ROW>(a.W, a.x, a.y, a.batch, a.mode, stream);
+    case QD_Q4_1: return launch_fmt<QD_Q4_1>(a.W, a.x, a.y, a.batch, a.mode, stream);
+    case QD_Q5_0: return launch_fmt<QD_Q5_0>(a.W, a.x, a.y, a.batch, a.mode, stream);
+    case QD_Q5_K: return launch_fmt<QD_Q5_K>(a.W, a.x, a.y, a.batch, a.mode, stream);
+    case QD_Q6_K: return launch_fmt<QD_Q6_K>(a.W, a.x, a.y, a.batch, a.mode, stream);
+    case QD_F16: return launch_fmt<QD_F16>(a.W, a.x, a.y, a.batch, a.mode, stream);
     default: return QD_ERR_UNSUPPORTED;
   }
 }

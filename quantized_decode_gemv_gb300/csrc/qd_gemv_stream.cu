@@ -707,6 +707,7 @@ qd_status launch_inst(const Params& p, bool pdl, cudaStream_t stream) {
 int nb_for(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8; }
 
 bool supported(const GemvArgs& a) {
+  if (!model_fmt_ok(a.fmt)) return false;  // Q4_0, Q8_0, Q4_K, INT8 rows
   if (a.batch < 1 || a.batch > 8 || a.W.cols % 32) return false;
   if (a.W.cols > (1 << 24)) return false;
   if (smem_bytes(a.fmt, a.W.cols, nb_for(a.batch)) > kSmemCap) return false;

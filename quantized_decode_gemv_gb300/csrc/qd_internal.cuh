@@ -41,9 +41,14 @@ struct PackedView {
 
 __host__ __device__ inline int64_t row_code_bytes(int fmt, int64_t cols) {
   switch (fmt) {
-    case QD_Q4_0: return cols / 2;
-    case QD_Q8_0: return cols;
+    case QD_Q4_0:
+    case QD_Q4_1:
+    case QD_Q5_0:
     case QD_Q4_K: return cols / 2;
+    case QD_Q8_0: return cols;
+    case QD_Q5_K: return (cols / 256) * 160;  // qh, then low nibbles
+    case QD_Q6_K: return (cols / 256) * 192;  // ql, then qh
+    case QD_F16: return cols * 2;
     default: return cols;  // QD_I8_ROW
   }
 }
@@ -52,7 +57,12 @@ __host__ __device__ inline int64_t row_scale_bytes(int fmt, int64_t cols) {
   switch (fmt) {
     case QD_Q4_0:
     case QD_Q8_0: return (cols / 32) * 2;
-    case QD_Q4_K: return (cols / 256) * 16;
+    case QD_Q4_1: return (cols / 32) * 4;    // d, m
+    case QD_Q5_0: return (cols / 32) * 6;    // d, qh
+    case QD_Q4_K:
+    case QD_Q5_K: return (cols / 256) * 16;  // d, dmin, 12 scale bytes
+    case QD_Q6_K: return (cols / 256) * 18;  // 16 int8 scales, d
+    case QD_F16: return 0;
     default: return 4;
   }
 }
@@ -61,14 +71,21 @@ inline bool shape_ok(int fmt, int64_t rows, int64_t cols) {
   if (rows < 1 || cols < 1) return false;
   switch (fmt) {
     case QD_Q4_0:
-    case QD_Q8_0: return cols % 32 == 0;
-    case QD_Q4_K: return cols % 256 == 0;
+    case QD_Q8_0:
+    case QD_Q4_1:
+    case QD_Q5_0:
+    case QD_F16: return cols % 32 == 0;
+    case QD_Q4_K:
+    case QD_Q5_K:
+    case QD_Q6_K: return cols % 256 == 0;
     case QD_I8_ROW: return cols % 16 == 0;
     default: return false;
   }
 }
 
-inline bool fmt_ok(int fmt) { return fmt >= QD_Q4_0 && fmt <= QD_I8_ROW; }
+inline bool fmt_ok(int fmt) { return fmt >= QD_Q4_0 && fmt <= QD_F16; }
+// The formats the decode step's fused kernels take.
+inline bool model_fmt_ok(int fmt) { return fmt >= QD_Q4_0 && fmt <= QD_I8_ROW; }
 
 inline size_t packed_code_region(int fmt, int64_t rows, int64_t cols) {
   return align_up((size_t)rows * (size_t)row_code_bytes(fmt, cols), 16);
@@ -85,6 +102,11 @@ inline size_t src_bytes(int fmt, int64_t rows, int64_t cols) {
     case QD_Q4_0: return (size_t)rows * (cols / 32) * 18;
     case QD_Q8_0: return (size_t)rows * (cols / 32) * 34;
     case QD_Q4_K: return (size_t)rows * (cols / 256) * 144;
+    case QD_Q4_1: return (size_t)rows * (cols / 32) * 20;
+    case QD_Q5_0: return (size_t)rows * (cols / 32) * 22;
+    case QD_Q5_K: return (size_t)rows * (cols / 256) * 176;
+    case QD_Q6_K: return (size_t)rows * (cols / 256) * 210;
+    case QD_F16: return (size_t)rows * cols * 2;
     default: return (size_t)rows * cols + 4 * (size_t)rows;
   }
 }
@@ -171,6 +193,48 @@ __device__ __forceinline__ float dequant_elem(int fmt, const PackedView& W, int6
     const int q = hi ? (byte >> 4) : (byte & 15);
     // d*sc is exact in f32; the fma rounds d*sc*q - dmin*m once.
     return fmaf(d * (float)sc, (float)q, -(dmin * (float)m));
+  } else if (fmt == QD_Q4_1) {
+    const int64_t b = c >> 5;
+    const int j = (int)(c & 31);
+    const uint8_t byte = code_row[b * 16 + (j & 15)];
+    const int q = (j < 16) ? (byte & 15) : (byte >> 4);
+    const uint8_t* h = sc_row + 4 * b;
+    // d*q + m rounded once
+    return fmaf(f16_bits_to_f32(h[0] | (h[1] << 8)), (float)q, f16_bits_to_f32(h[2] | (h[3] << 8)));
+  } else if (fmt == QD_Q5_0) {
+    const int64_t b = c >> 5;
+    const int j = (int)(c & 31);
+    const uint8_t byte = code_row[b * 16 + (j & 15)];
+    const uint8_t* h = sc_row + 6 * b;
+    const uint32_t qh = (uint32_t)h[2] | ((uint32_t)h[3] << 8) | ((uint32_t)h[4] << 16) | ((uint32_t)h[5] << 24);
+    const int q = ((j < 16) ? (byte & 15) : (byte >> 4)) | (int)(((qh >> j) & 1u) << 4);
+    return (float)(q - 16) * f16_bits_to_f32(h[0] | (h[1] << 8));
+  } else if (fmt == QD_Q5_K) {
+    const int64_t s = c >> 8;
+    const int e = (int)(c & 255);
+    const int chunk = e >> 6, hi = (e >> 5) & 1, l = e & 31;
+    const uint8_t* hdr = sc_row + s * 16;
+    const float d = f16_bits_to_f32(hdr[0] | (hdr[1] << 8));
+    const float dmin = f16_bits_to_f32(hdr[2] | (hdr[3] << 8));
+    int sc, m;
+    q4k_scale_min(2 * chunk + hi, hdr + 4, sc, m);
+    const uint8_t* blk = code_row + s * 160;
+    const uint8_t byte = blk[32 + 32 * chunk + l];
+    const int q = (hi ? (byte >> 4) : (byte & 15)) | (((blk[l] >> (2 * chunk + hi)) & 1) << 4);
+    return fmaf(d * (float)sc, (float)q, -(dmin * (float)m));
+  } else if (fmt == QD_Q6_K) {
+    const int64_t s = c >> 8;
+    const int e = (int)(c & 255);
+    const int h = e >> 7, k = (e >> 5) & 3, l = e & 31;
+    const uint8_t* blk = code_row + s * 192;
+    const uint8_t lb = blk[64 * h + l + 32 * (k & 1)];
+    const int q = ((k < 2) ? (lb & 15) : (lb >> 4)) | (((blk[128 + 32 * h + l] >> (2 * k)) & 3) << 4);
+    const uint8_t* hdr = sc_row + s * 18;
+    const int sc = (int8_t)hdr[8 * h + 2 * k + (l >> 4)];
+    // d*sc*(q-32): at most 11 + 7 + 5 significant bits, exact in f32
+    return f16_bits_to_f32(hdr[16] | (hdr[17] << 8)) * (float)sc * (float)(q - 32);
+  } else if (fmt == QD_F16) {
+    return f16_bits_to_f32(code_row[2 * c] | (code_row[2 * c + 1] << 8));
   } else {
     float s;
     memcpy(&s, sc_row, 4);

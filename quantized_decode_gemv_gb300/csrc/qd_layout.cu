@@ -2,11 +2,12 @@
 // bf16 conversions.
 //
 // The pages' loaders hand each block to the GPU as it sits in the model file
-// (an 18-, 34- or 144-byte record).  Those records are not 16-byte aligned, so
-// the repack splits every tensor into a code region (16 B per Q4_0 block, 32 B
-// per Q8_0 block, 128 B per Q4_K super-block, one byte per INT8 weight) and a
-// scale region (f16 d per block, the 16-byte d/dmin/scales header per Q4_K
-// super-block, one f32 per INT8 row), both row-major.  Nothing is re-encoded:
+// (an 18-, 20-, 22-, 34-, 144-, 176- or 210-byte record).  Those records are not
+// 16-byte aligned, so the repack splits every tensor into a code region (16 B per
+// Q4_0 / Q4_1 / Q5_0 block, 32 B per Q8_0 block, 128 / 160 / 192 B per Q4_K / Q5_K /
+// Q6_K super-block, one byte per INT8 weight, two per F16 weight) and a scale region
+// (the rest of each record: f16 d, d and m, d and qh, the 16-byte d/dmin/scales header,
+// Q6_K's 16 scales and d; one f32 per INT8 row; nothing for F16), both row-major.  Nothing is re-encoded:
 // the scales stay f16 (the Go "llm" package's "Design points" widen them to f32
 // only because its shading language has no f16), so the packed tensor is the
 // same number of bytes as the source plus at most 30 bytes of padding.
@@ -20,14 +21,20 @@ struct BlockGeom {
   int weights;      // weights per block
   int code_off;     // offset of the codes inside the source block
   int code_bytes;   // bytes of codes per block
-  int scale_bytes;  // bytes of scale data per block (copied from offset 0)
+  int scale_off;    // offset of the scale data inside the source block
+  int scale_bytes;  // bytes of scale data per block
 };
 
 __host__ __device__ inline BlockGeom geom(int fmt) {
   switch (fmt) {
-    case QD_Q4_0: return {18, 32, 2, 16, 2};
-    case QD_Q8_0: return {34, 32, 2, 32, 2};
-    default: return {144, 256, 16, 128, 16};  // QD_Q4_K
+    case QD_Q4_0: return {18, 32, 2, 16, 0, 2};
+    case QD_Q8_0: return {34, 32, 2, 32, 0, 2};
+    case QD_Q4_1: return {20, 32, 4, 16, 0, 4};      // d, m | codes
+    case QD_Q5_0: return {22, 32, 6, 16, 0, 6};      // d, qh | low nibbles
+    case QD_Q5_K: return {176, 256, 16, 160, 0, 16};  // d, dmin, scales | qh, low nibbles
+    case QD_Q6_K: return {210, 256, 0, 192, 192, 18};  // ql, qh | scales, d
+    case QD_F16: return {32, 16, 0, 32, 0, 0};       // 16 weights as one "block"
+    default: return {144, 256, 16, 128, 0, 16};       // QD_Q4_K
   }
 }
 
@@ -53,7 +60,7 @@ __global__ void k_repack_blocks(int fmt, const uint8_t* __restrict__ src, int64_
     uint8_t* c = codes + (r * nb + b) * g.code_bytes;
     uint8_t* sc = scales + (r * nb + b) * g.scale_bytes;
     for (int k = 0; k < g.code_bytes; ++k) c[k] = s[g.code_off + k];
-    for (int k = 0; k < g.scale_bytes; ++k) sc[k] = s[k];
+    for (int k = 0; k < g.scale_bytes; ++k) sc[k] = s[g.scale_off + k];
   }
 }
 
@@ -65,7 +72,7 @@ __global__ void k_unpack_blocks(int fmt, const uint8_t* __restrict__ codes, cons
     uint8_t* d = dst + t * g.src_bytes;
     const uint8_t* c = codes + t * g.code_bytes;
     const uint8_t* sc = scales + t * g.scale_bytes;
-    for (int k = 0; k < g.scale_bytes; ++k) d[k] = sc[k];
+    for (int k = 0; k < g.scale_bytes; ++k) d[g.scale_off + k] = sc[k];
     for (int k = 0; k < g.code_bytes; ++k) d[g.code_off + k] = c[k];
   }
 }

@@ -49,7 +49,7 @@ bool config_ok(const qd_config* c) {
   if (c->max_ctx < 1 || c->max_batch < 1 || c->max_batch > QD_MAX_BATCH) return false;
   if (c->pairing != QD_ROPE_ADJACENT && c->pairing != QD_ROPE_HALF) return false;
   if (c->kv_f16 != 0 && c->kv_f16 != 1) return false;
-  if (!fmt_ok(c->w_fmt) || !fmt_ok(c->emb_fmt)) return false;
+  if (!model_fmt_ok(c->w_fmt) || !model_fmt_ok(c->emb_fmt)) return false;
   if (!(c->eps >= 0.f) || !(c->rope_theta > 0.f)) return false;
   const int64_t QD = (int64_t)c->n_heads * c->head_dim, KD = (int64_t)c->n_kv_heads * c->head_dim;
   if (!shape_ok(c->w_fmt, QD + 2 * KD, c->dim) || !shape_ok(c->w_fmt, c->dim, QD) ||

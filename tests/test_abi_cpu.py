@@ -49,6 +49,13 @@ def test_status_strings(lib):
     ("q8_0", 3, 64, 3 * 2 * 34, 3 * 2 * 32 + 16),
     ("q4_k", 2, 512, 2 * 2 * 144, 2 * 2 * 128 + 2 * 2 * 16),
     ("i8", 5, 48, 5 * 48 + 20, 5 * 48 + 32),
+    # Q4_1 / Q5_0: 16 code bytes per block, then 4 (d, m) / 6 (d, qh) scale bytes per block
+    ("q4_1", 3, 64, 3 * 2 * 20, 3 * 2 * 16 + 32),
+    ("q5_0", 3, 64, 3 * 2 * 22, 3 * 2 * 16 + 48),
+    # Q5_K: 160 code bytes (qh, nibbles) + 16 header bytes; Q6_K: 192 + 18 (padded to 16)
+    ("q5_k", 2, 512, 2 * 2 * 176, 2 * 2 * 160 + 2 * 2 * 16),
+    ("q6_k", 3, 256, 3 * 210, 3 * 192 + 64),
+    ("f16", 3, 32, 3 * 32 * 2, 3 * 32 * 2),
 ])
 def test_layout_sizes(lib, fmt, rows, cols, src, packed):
     assert qd.src_bytes(fmt, rows, cols) == src
@@ -56,7 +63,8 @@ def test_layout_sizes(lib, fmt, rows, cols, src, packed):
 
 
 @pytest.mark.parametrize("fmt,rows,cols", [("q4_0", 4, 48), ("q8_0", 0, 64), ("q4_k", 2, 128), ("i8", 3, 40),
-                                           ("q4_0", -1, 64)])
+                                           ("q4_0", -1, 64), ("q4_1", 2, 48), ("q5_0", 2, 80), ("q5_k", 2, 384),
+                                           ("q6_k", 1, 128), ("f16", 2, 48)])
 def test_layout_sizes_reject_bad_shapes(lib, fmt, rows, cols):
     assert qd.src_bytes(fmt, rows, cols) == 0
     assert qd.packed_bytes(fmt, rows, cols) == 0
@@ -144,6 +152,12 @@ def test_model_sizes_and_config_refusals(lib):
     bad = qd.make_config(qdsynth.SMOL_135M, max_ctx=256, max_batch=1)
     bad.kv_f16 = 2
     assert lib.qd_model_state_bytes(ctypes.byref(bad)) == 0
+    # the decode step's fused kernels take Q4_0, Q8_0, Q4_K and INT8 rows only
+    for f in ("q4_1", "q5_0", "q5_k", "q6_k", "f16"):
+        bad = qd.make_config(dict(qdsynth.SMOL_135M, w_fmt=f), max_ctx=256, max_batch=1)
+        assert lib.qd_model_weight_bytes(ctypes.byref(bad)) == 0, f
+        bad = qd.make_config(dict(qdsynth.SMOL_135M, emb_fmt=f), max_ctx=256, max_batch=1)
+        assert lib.qd_model_state_bytes(ctypes.byref(bad)) == 0, f
     # a binary16 cache takes half the bytes (the state also gains the flat attention's workspace)
     h = qd.make_config(qdsynth.SMOL_135M, max_ctx=256, max_batch=1, kv_f16=True)
     sh = lib.qd_model_state_bytes(ctypes.byref(h))
