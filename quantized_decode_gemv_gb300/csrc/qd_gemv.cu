@@ -301,100 +301,109 @@ __global__ void __launch_bounds__(kThreads) k_gemv_q4k(PackedView W, const float
 __device__ __forceinline__ float f16lo(uint32_t w) { return f16_bits_to_f32(w & 0xFFFFu); }
 __device__ __forceinline__ float f16hi(uint32_t w) { return f16_bits_to_f32(w >> 16); }
 
+// Raw bytes of unit u (columns 32u .. 32u + 31) of row r, loaded in one step so that the
+// next unit's loads can be in flight while this one is decoded.
 template <int FMT>
-__device__ __forceinline__ void deq_unit(const PackedView& W, int64_t r, int64_t u, float (&w)[32]) {
-  const uint8_t* cr = W.codes + r * W.row_code_bytes;
-  const uint8_t* sr = W.scales + r * W.row_scale_bytes;
-  if constexpr (FMT == QD_F16) {
-    const uint4* p = reinterpret_cast<const uint4*>(cr + 64 * u);
+struct RawUnit {
+  uint4 a[4];     // codes: F16 a[0..3]; Q4_1 / Q5_0 a[0]; Q5_K / Q6_K a[0..1] low nibbles, a[2..3] high bits
+  uint4 hdr;      // Q5_K header (d, dmin, 12 scale bytes)
+  uint32_t s0, s1;  // Q4_1 (d, m); Q5_0 d, qh; Q6_K d, the unit's two scale bytes
+  __device__ __forceinline__ void load(const PackedView& W, int64_t r, int64_t u) {
+    const uint8_t* cr = W.codes + r * W.row_code_bytes;
+    const uint8_t* sr = W.scales + r * W.row_scale_bytes;
+    if constexpr (FMT == QD_F16) {
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const uint4 v = ld_stream_v4(p + t);
-      const uint32_t h[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        w[8 * t + 2 * k] = f16lo(h[k]);
-        w[8 * t + 2 * k + 1] = f16hi(h[k]);
-      }
-    }
-  } else if constexpr (FMT == QD_Q4_1 || FMT == QD_Q5_0) {
-    const uint4 q = ld_stream_v4(cr + 16 * u);
-    const uint8_t bytes[16] = {
-        (uint8_t)q.x, (uint8_t)(q.x >> 8), (uint8_t)(q.x >> 16), (uint8_t)(q.x >> 24),
-        (uint8_t)q.y, (uint8_t)(q.y >> 8), (uint8_t)(q.y >> 16), (uint8_t)(q.y >> 24),
-        (uint8_t)q.z, (uint8_t)(q.z >> 8), (uint8_t)(q.z >> 16), (uint8_t)(q.z >> 24),
-        (uint8_t)q.w, (uint8_t)(q.w >> 8), (uint8_t)(q.w >> 16), (uint8_t)(q.w >> 24)};
-    if constexpr (FMT == QD_Q4_1) {
-      const uint32_t dm = __ldg(reinterpret_cast<const uint32_t*>(sr + 4 * u));
-      const float d = f16lo(dm), m = f16hi(dm);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        w[j] = fmaf(d, (float)(bytes[j] & 15), m);
-        w[j + 16] = fmaf(d, (float)(bytes[j] >> 4), m);
-      }
-    } else {
+      for (int t = 0; t < 4; ++t) a[t] = ld_stream_v4(cr + 64 * u + 16 * t);
+    } else if constexpr (FMT == QD_Q4_1) {
+      a[0] = ld_stream_v4(cr + 16 * u);
+      s0 = __ldg(reinterpret_cast<const uint32_t*>(sr + 4 * u));
+    } else if constexpr (FMT == QD_Q5_0) {
+      a[0] = ld_stream_v4(cr + 16 * u);
       const unsigned short* h = reinterpret_cast<const unsigned short*>(sr + 6 * u);
-      const float d = f16_bits_to_f32(__ldg(h));
-      const uint32_t qh = (uint32_t)__ldg(h + 1) | ((uint32_t)__ldg(h + 2) << 16);
+      s0 = __ldg(h);
+      s1 = (uint32_t)__ldg(h + 1) | ((uint32_t)__ldg(h + 2) << 16);
+    } else {  // Q5_K, Q6_K: unit v = u % 8 of super-block u / 8
+      const int64_t sb = u >> 3;
+      const int v = (int)(u & 7);
+      const uint8_t *lp, *hp;
+      if constexpr (FMT == QD_Q5_K) {
+        lp = cr + sb * 160 + 32 + 32 * (v >> 1);
+        hp = cr + sb * 160;
+        hdr = __ldg(reinterpret_cast<const uint4*>(sr + sb * 16));
+      } else {
+        lp = cr + sb * 192 + 64 * (v >> 2) + 32 * (v & 1);
+        hp = cr + sb * 192 + 128 + 32 * (v >> 2);
+        const uint8_t* h = sr + sb * 18;
+        s0 = __ldg(reinterpret_cast<const unsigned short*>(h + 16));
+        s1 = __ldg(reinterpret_cast<const unsigned short*>(h + 2 * v));  // scales 2k, 2k + 1 of half v / 4
+      }
+      a[0] = ld_stream_v4(lp);
+      a[1] = ld_stream_v4(lp + 16);
+      a[2] = ld_stream_v4(hp);
+      a[3] = ld_stream_v4(hp + 16);
+    }
+  }
+  // the 32 dequantised f32 values, each rounded once (as the test dequantiser)
+  __device__ __forceinline__ void decode(int64_t u, float (&w)[32]) const {
+    if constexpr (FMT == QD_F16) {
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const uint32_t h[4] = {a[t].x, a[t].y, a[t].z, a[t].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          w[8 * t + 2 * k] = f16lo(h[k]);
+          w[8 * t + 2 * k + 1] = f16hi(h[k]);
+        }
+      }
+    } else if constexpr (FMT == QD_Q4_1 || FMT == QD_Q5_0) {
+      const uint32_t q[4] = {a[0].x, a[0].y, a[0].z, a[0].w};
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        w[j] = (float)((int)((bytes[j] & 15) | (((qh >> j) & 1u) << 4)) - 16) * d;
-        w[j + 16] = (float)((int)((bytes[j] >> 4) | (((qh >> (j + 16)) & 1u) << 4)) - 16) * d;
-      }
-    }
-  } else {  // Q5_K, Q6_K: unit v = u % 8 of super-block s = u / 8
-    const int64_t sb = u >> 3;
-    const int v = (int)(u & 7);
-    uint8_t lq[32], hq[32];  // low-nibble bytes and high-bit bytes of the unit
-    const uint8_t* lp;
-    const uint8_t* hp;
-    if constexpr (FMT == QD_Q5_K) {
-      lp = cr + sb * 160 + 32 + 32 * (v >> 1);
-      hp = cr + sb * 160;
-    } else {
-      lp = cr + sb * 192 + 64 * (v >> 2) + 32 * (v & 1);
-      hp = cr + sb * 192 + 128 + 32 * (v >> 2);
-    }
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      const uint4 a = ld_stream_v4(lp + 16 * t), b = ld_stream_v4(hp + 16 * t);
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        lq[16 * t + k] = (uint8_t)(aw[k >> 2] >> (8 * (k & 3)));
-        hq[16 * t + k] = (uint8_t)(bw[k >> 2] >> (8 * (k & 3)));
-      }
-    }
-    if constexpr (FMT == QD_Q5_K) {
-      const uint4 hdr = __ldg(reinterpret_cast<const uint4*>(sr + sb * 16));
-      uint8_t sbytes[12];
-      const uint32_t hw[3] = {hdr.y, hdr.z, hdr.w};
-#pragma unroll
-      for (int k = 0; k < 12; ++k) sbytes[k] = (uint8_t)(hw[k >> 2] >> (8 * (k & 3)));
-      int sc, m;
-      q4k_scale_min(v, sbytes, sc, m);  // sub-block v = 2 chunk + high
-      const float a = f16lo(hdr.x) * (float)sc, b = -(f16hi(hdr.x) * (float)m);
-      const int shift = v & 1 ? 4 : 0;
-#pragma unroll
-      for (int l = 0; l < 32; ++l) {
-        const int q = ((lq[l] >> shift) & 15) | (((hq[l] >> v) & 1) << 4);
-        w[l] = fmaf(a, (float)q, b);
+        const uint32_t byte = (q[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+        if constexpr (FMT == QD_Q4_1) {
+          const float d = f16lo(s0), m = f16hi(s0);
+          w[j] = fmaf(d, (float)(byte & 15u), m);
+          w[j + 16] = fmaf(d, (float)(byte >> 4), m);
+        } else {
+          const float d = f16_bits_to_f32(s0);
+          w[j] = (float)((int)((byte & 15u) | (((s1 >> j) & 1u) << 4)) - 16) * d;
+          w[j + 16] = (float)((int)((byte >> 4) | (((s1 >> (j + 16)) & 1u) << 4)) - 16) * d;
+        }
       }
     } else {
-      const int h = v >> 2, k = v & 3;
-      const uint8_t* hdr = sr + sb * 18;
-      const float d = f16_bits_to_f32(__ldg(reinterpret_cast<const unsigned short*>(hdr + 16)));
-      const float s0 = d * (float)(int8_t)__ldg(hdr + 8 * h + 2 * k);
-      const float s1 = d * (float)(int8_t)__ldg(hdr + 8 * h + 2 * k + 1);
-      const int shift = k < 2 ? 0 : 4;
+      const int v = (int)(u & 7);
+      const uint32_t lw[8] = {a[0].x, a[0].y, a[0].z, a[0].w, a[1].x, a[1].y, a[1].z, a[1].w};
+      const uint32_t hw[8] = {a[2].x, a[2].y, a[2].z, a[2].w, a[3].x, a[3].y, a[3].z, a[3].w};
+      if constexpr (FMT == QD_Q5_K) {
+        uint8_t sbytes[12];
+        const uint32_t hs[3] = {hdr.y, hdr.z, hdr.w};
 #pragma unroll
-      for (int l = 0; l < 32; ++l) {
-        const int q = ((lq[l] >> shift) & 15) | (((hq[l] >> (2 * k)) & 3) << 4);
-        w[l] = (l < 16 ? s0 : s1) * (float)(q - 32);
+        for (int k = 0; k < 12; ++k) sbytes[k] = (uint8_t)(hs[k >> 2] >> (8 * (k & 3)));
+        int sc, m;
+        q4k_scale_min(v, sbytes, sc, m);  // sub-block v = 2 chunk + high
+        const float ca = f16lo(hdr.x) * (float)sc, cb = -(f16hi(hdr.x) * (float)m);
+        const int shift = (v & 1) ? 4 : 0;
+#pragma unroll
+        for (int l = 0; l < 32; ++l) {
+          const uint32_t lb = (lw[l >> 2] >> (8 * (l & 3))) & 0xFFu, hb = (hw[l >> 2] >> (8 * (l & 3))) & 0xFFu;
+          const int q = (int)(((lb >> shift) & 15u) | (((hb >> v) & 1u) << 4));
+          w[l] = fmaf(ca, (float)q, cb);
+        }
+      } else {
+        const int k = v & 3;
+        const float d = f16_bits_to_f32(s0);
+        const float c0 = d * (float)(int8_t)(s1 & 0xFFu), c1 = d * (float)(int8_t)(s1 >> 8);
+        const int shift = k < 2 ? 0 : 4;
+#pragma unroll
+        for (int l = 0; l < 32; ++l) {
+          const uint32_t lb = (lw[l >> 2] >> (8 * (l & 3))) & 0xFFu, hb = (hw[l >> 2] >> (8 * (l & 3))) & 0xFFu;
+          const int q = (int)(((lb >> shift) & 15u) | (((hb >> (2 * k)) & 3u) << 4));
+          w[l] = (l < 16 ? c0 : c1) * (float)(q - 32);
+        }
       }
     }
   }
-}
+};
 
 // Q4_1, Q5_0, Q5_K, Q6_K, F16: each lane dequantises its 32-column units to f32 and dots
 // them with x.
@@ -410,10 +419,20 @@ __global__ void __launch_bounds__(kThreads) k_gemv_deq(PackedView W, const float
   for (int i = 0; i < R; ++i)
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc[i][b] = 0.f;
-  for (int64_t u = lane; u < units; u += 32) {
+  RawUnit<FMT> cur[R], nxt[R];
+  int64_t u = lane;
+  if (u < units) {
+#pragma unroll
+    for (int i = 0; i < R; ++i) cur[i].load(W, row0 + i < W.rows ? row0 + i : row0, u);
+  }
+  for (; u < units; u += 32) {
+    if (u + 32 < units) {  // the next unit's loads, in flight during this one's arithmetic
+#pragma unroll
+      for (int i = 0; i < R; ++i) nxt[i].load(W, row0 + i < W.rows ? row0 + i : row0, u + 32);
+    }
     float w[R][32];
 #pragma unroll
-    for (int i = 0; i < R; ++i) deq_unit<FMT>(W, row0 + i < W.rows ? row0 + i : row0, u, w[i]);
+    for (int i = 0; i < R; ++i) cur[i].decode(u, w[i]);
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       if (b < batch) {
@@ -422,6 +441,8 @@ __global__ void __launch_bounds__(kThreads) k_gemv_deq(PackedView W, const float
         for (int i = 0; i < R; ++i) acc[i][b] += dot_x<32>(w[i], xp);
       }
     }
+#pragma unroll
+    for (int i = 0; i < R; ++i) cur[i] = nxt[i];
   }
   float row_scale[R];
 #pragma unroll
