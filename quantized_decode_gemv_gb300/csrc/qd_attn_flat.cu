@@ -31,6 +31,7 @@
 #include <type_traits>
 
 #include "qd_attn.cuh"
+#include "qd_tc.cuh"
 
 namespace qd {
 namespace {
@@ -55,49 +56,13 @@ struct FlatShape {
 };
 constexpr int kPartFloats = 2 + kHeadDim;            // one head's partial: m, l, o[64]
 constexpr int kFlatSlotHeads = 8;  // parked (pair, head) warp states a CTA holds before settling them
-constexpr uint32_t kFlatSpinLimit = 1u << 24;        // test_wait polls per wait (about a second)
-
-__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
-  asm volatile(
-      "{\n"
-      ".reg .b64 st;\n"
-      "mbarrier.arrive.shared::cta.b64 st, [%0];\n"
-      "}\n" ::"r"(mbar)
-      : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
-  asm volatile(
-      "{\n"
-      ".reg .b64 st;\n"
-      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n"
-      "}\n" ::"r"(mbar),
-      "r"(bytes)
-      : "memory");
-}
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
-  for (uint32_t i = 0; i < kFlatSpinLimit; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n"
-        "}\n"
-        : "=r"(done)
-        : "r"(mbar), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
+using tc::mbar_arrive;  // mbarrier helpers: every wait is a bounded poll (tc::kSpinLimit)
+using tc::mbar_arrive_expect_tx;
+using tc::mbar_init;
+using tc::mbar_wait;
 // `bytes` (a multiple of 16) from global `src` to shared `dst`, counted on `mbar`
 __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(mbar)
-               : "memory");
+  tc::bulk_copy_g2s(dst, src, bytes, mbar);
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 template <int W>

@@ -41,9 +41,12 @@
 #include <cuda_fp16.h>
 
 #include "qd_internal.cuh"
+#include "qd_tc.cuh"
 
 namespace qd {
 namespace tc_gemv {
+
+using namespace tc;
 
 constexpr int kM = 128;       // weight rows per tile (the MMA's M)
 constexpr int kN = 32;        // B columns: 16 sequences x (high, low)
@@ -72,7 +75,6 @@ constexpr uint32_t kACols = kKT / 2;
 constexpr uint32_t kTmemCols = 512;
 static_assert(kAccCols + kNA * kACols <= kTmemCols, "tensor memory columns");
 
-constexpr uint32_t kCoreBytes = 128;                // one 8 x 16-byte core matrix
 constexpr uint32_t kI8Bytes = kM * kKT;             // one int8 weight stage
 constexpr uint32_t kPartBytes = kNB * kM * 4;       // the CTA's f32 partial tile (split-K)
 constexpr int kChunks = kM * kKT / 16 / kConv;      // 16-byte chunks per converter thread and stage
@@ -98,103 +100,12 @@ __host__ __device__ constexpr uint32_t b_bytes(int kc) { return (uint32_t)kN * (
 // dynamic shared memory, from its first 128-byte boundary: B | int8 ring | partial tile
 __host__ __device__ constexpr uint32_t smem_bytes(int kc) { return 128 + b_bytes(kc) + kRing * kI8Bytes + kPartBytes; }
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-// Shared-memory matrix descriptor, K-major, no swizzle: start address, byte offset
-// between core matrices along K (leading) and along M/N (stride), descriptor version 1.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
-}
 // Instruction descriptor, kind::f16: f32 accumulator, f16 A and B, both K-major, N, M.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
+constexpr uint32_t kIdesc = idesc_f16(kM, kN);
 
 // D (tensor memory) += A (tensor memory, K-major: row i in lane i) x B (shared memory).
 __device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      ".reg .pred p;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
-      "}\n" ::"r"(tmem_d),
-      "r"(tmem_a), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-// 32 consecutive 32-bit columns of this thread's tensor-memory lane (warp-collective).
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
-      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
-      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint32_t mbar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
-               : "memory");
-}
-__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// mbarrier helpers.  A wait polls mbarrier.test_wait (returns at once) at most
-// kSpinLimit times and reports whether the phase completed.
-constexpr uint32_t kSpinLimit = 1u << 24;
-__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
-  asm volatile(
-      "{\n"
-      ".reg .b64 st;\n"
-      "mbarrier.arrive.shared::cta.b64 st, [%0];\n"
-      "}\n" ::"r"(mbar)
-      : "memory");
-}
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n"
-        "}\n"
-        : "=r"(done)
-        : "r"(mbar), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-
-// 32 consecutive f32 columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Four int8 codes -> two f16 pairs, exactly: (q ^ 0x80) is q + 128 in 0..255; as the low
-// mantissa byte of 1024 it gives the f16 1024 + q + 128, and 1152 is subtracted.
-__device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& h01, uint32_t& h23) {
-  const uint32_t u = w ^ 0x80808080u;
-  const __half2 k1152 = __float2half2_rn(1152.f);
-  uint32_t a = __byte_perm(u, 0x64646464u, 0x4140u), b = __byte_perm(u, 0x64646464u, 0x4342u);
-  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), k1152);
-  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), k1152);
-  h01 = *reinterpret_cast<uint32_t*>(&ha);
-  h23 = *reinterpret_cast<uint32_t*>(&hb);
+  mma_f16_ts(tmem_d, tmem_a, bdesc, kIdesc, accumulate);
 }
 
 __device__ __forceinline__ void conv_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConv) : "memory"); }
