@@ -71,6 +71,10 @@ def _L():
         lib.or_dequant.restype = i32
         lib.or_gemv.argtypes = [i32, p, i64, i64, p, i32, i64, i64, p]
         lib.or_gemv.restype = i32
+        lib.or_quantize_q8.argtypes = [p, i64, p, p, p]
+        lib.or_quantize_q8.restype = i32
+        lib.or_gemv_q8act.argtypes = [i32, p, i64, i64, p, p, p, i32, i64, i64, p]
+        lib.or_gemv_q8act.restype = i32
         lib.or_rmsnorm.argtypes = [p, p, i32, i32, d, p]
         lib.or_rmsnorm.restype = i32
         lib.or_rope.argtypes = [p, i32, i32, i32, i32, d, p]
@@ -215,6 +219,42 @@ def swiglu(g, u) -> np.ndarray:
 def round_f16(f: float) -> float:
     """f32 rounded through binary16 (what an f16 KV cache stores)."""
     return float(_L().or_round_f16(float(np.float32(f))))
+
+
+def quantize_q8(x, with_sum: bool = False):
+    """ggml-exact Q8_0 (Q8_1 with with_sum) activations of x f32 [batch][cols] (see
+    or_quantize_q8): (codes int8 [batch][cols], d f32 [batch][cols/32], s or None), d and
+    s holding their binary16 values."""
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    batch, cols = x.shape
+    q = np.empty((batch, cols), np.int8)
+    d = np.empty((batch, cols // 32), np.float32)
+    s = np.empty((batch, cols // 32), np.float32) if with_sum else None
+    for b in range(batch):
+        rc = _L().or_quantize_q8(x[b].ctypes.data, cols, q[b].ctypes.data, d[b].ctypes.data,
+                                 s[b].ctypes.data if with_sum else None)
+        if rc:
+            raise ValueError(f"or_quantize_q8 rc={rc}")
+    return q, d, s
+
+
+def gemv_q8act(fmt: str, w, rows: int, cols: int, xq, xd, xs=None, row0: int = 0, nrows: int | None = None):
+    """The product over quantised activations (or_gemv_q8act), double [batch][nrows]."""
+    nrows = rows - row0 if nrows is None else nrows
+    xq = np.ascontiguousarray(np.atleast_2d(xq), dtype=np.int8)
+    xd = np.ascontiguousarray(np.atleast_2d(xd), dtype=np.float32)
+    batch = xq.shape[0]
+    w, wp = _c(w, np.uint8)
+    y = np.empty((batch, nrows), dtype=np.float64)
+    xsp = None
+    if xs is not None:
+        xs = np.ascontiguousarray(np.atleast_2d(xs), dtype=np.float32)
+        xsp = xs.ctypes.data
+    rc = _L().or_gemv_q8act(FMT[fmt], wp, rows, cols, xq.ctypes.data, xd.ctypes.data, xsp, batch, row0, nrows,
+                            y.ctypes.data)
+    if rc:
+        raise ValueError(f"or_gemv_q8act rc={rc}")
+    return y
 
 
 def quantize_i8_rows(w_bf16, rows: int, cols: int) -> tuple[np.ndarray, np.ndarray]:

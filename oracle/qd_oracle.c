@@ -511,6 +511,93 @@ int or_quantize_i8_rows(const uint16_t* w, int64_t rows, int64_t cols, int8_t* c
 }
 
 /* ------------------------------------------------------------------------- */
+/* ggml-exact activations ([go-llm] type CPU, "ExactGGML": activations are      */
+/* quantised to Q8_0 -- Q8_1 for Q4_1 weights -- before every quantised matrix  */
+/* product).  The page prints no rule; the one implemented, per 32-element      */
+/* block: d = max|x| / 127 (f32), q = x / d (f32) rounded to nearest with ties  */
+/* away from zero (C roundf), clamped to +-127; the block keeps d rounded to    */
+/* binary16 and, for Q8_1, s = d * sum(q) (f32) rounded to binary16.  A zero    */
+/* block has d = 0 and codes 0; a block holding a non-finite value codes 0 and  */
+/* d = s = NaN.  d16 / s16 receive the binary16 values (s16 may be NULL).       */
+/* ------------------------------------------------------------------------- */
+int or_quantize_q8(const float* x, int64_t n, int8_t* q, float* d16, float* s16) {
+    if (n < 1 || n % 32) return -1;
+    for (int64_t b = 0; b < n / 32; ++b) {
+        const float* xb = x + 32 * b;
+        int8_t* qb = q + 32 * b;
+        float m = 0.0f;
+        int finite = 1;
+        for (int j = 0; j < 32; ++j) {
+            if (!isfinite(xb[j]))
+                finite = 0;
+            else if (fabsf(xb[j]) > m)
+                m = fabsf(xb[j]);
+        }
+        if (!finite || m == 0.0f) {
+            for (int j = 0; j < 32; ++j) qb[j] = 0;
+            d16[b] = finite ? 0.0f : NAN;
+            if (s16) s16[b] = d16[b];
+            continue;
+        }
+        const float d = m / 127.0f;
+        int sum = 0;
+        for (int j = 0; j < 32; ++j) {
+            float v = roundf(xb[j] / d);
+            if (v > 127.0f) v = 127.0f;
+            if (v < -127.0f) v = -127.0f;
+            qb[j] = (int8_t)v;
+            sum += qb[j];
+        }
+        d16[b] = or_round_f16(d);
+        if (s16) s16[b] = or_round_f16(d * (float)sum);
+    }
+    return 0;
+}
+
+/* The product over quantised activations, in the block's own integers ([llamini]
+ * "What I reimplemented": ggml's dot products multiply the packed bytes directly and
+ * convert to float only for the scaled sum): y[b][r] = sum over blocks k of row r of
+ *   Q8_0: d_w d_x sum_j q_w q_x;   Q4_0: d_w d_x sum_j (q_w - 8) q_x;
+ *   Q4_1: d_w d_x sum_j q_w q_x + m_w s_x,
+ * with x's binary16 d and s; accumulated in double. */
+int or_gemv_q8act(int fmt, const uint8_t* w, int64_t rows, int64_t cols, const int8_t* xq, const float* xd,
+                  const float* xs, int batch, int64_t row0, int64_t nrows, double* y) {
+    if ((fmt != OR_Q8_0 && fmt != OR_Q4_0 && fmt != OR_Q4_1) || !or_shape_ok(fmt, rows, cols) || batch < 1 ||
+        row0 < 0 || nrows < 0 || row0 + nrows > rows || (fmt == OR_Q4_1 && !xs))
+        return -1;
+    const int64_t nb = cols / 32, rb = row_bytes(fmt, cols);
+#pragma omp parallel for schedule(static) if (nrows * cols * batch > 262144)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const uint8_t* row = w + (row0 + r) * rb;
+        for (int bt = 0; bt < batch; ++bt) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < nb; ++k) {
+                const int8_t* qx = xq + (int64_t)bt * cols + 32 * k;
+                const double dx = xd[(int64_t)bt * nb + k];
+                long sumi = 0;
+                if (fmt == OR_Q8_0) {
+                    const uint8_t* blk = row + k * 34;
+                    for (int j = 0; j < 32; ++j) sumi += (long)(int8_t)blk[2 + j] * qx[j];
+                    acc += f16_at(blk) * dx * (double)sumi;
+                } else if (fmt == OR_Q4_0) {
+                    const uint8_t* blk = row + k * 18;
+                    for (int j = 0; j < 16; ++j)
+                        sumi += (long)((blk[2 + j] & 0x0F) - 8) * qx[j] + (long)((blk[2 + j] >> 4) - 8) * qx[16 + j];
+                    acc += f16_at(blk) * dx * (double)sumi;
+                } else {
+                    const uint8_t* blk = row + k * 20;
+                    for (int j = 0; j < 16; ++j)
+                        sumi += (long)(blk[4 + j] & 0x0F) * qx[j] + (long)(blk[4 + j] >> 4) * qx[16 + j];
+                    acc += f16_at(blk) * dx * (double)sumi + f16_at(blk + 2) * (double)xs[(int64_t)bt * nb + k];
+                }
+            }
+            y[(int64_t)bt * nrows + r] = acc;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Greedy argmax: the largest value, the first index on ties ([go-llm] index, */
 /* Argmax; [dasLLAMA] 8.7.1.6.4 most_likely: strict '>' from index 0).        */
 /* ------------------------------------------------------------------------- */

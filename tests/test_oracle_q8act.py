@@ -1,0 +1,82 @@
+"""Pins of the oracle's ggml-exact activation path (go-llm type CPU, "ExactGGML": activations
+quantised to Q8_0, Q8_1 for Q4_1 weights, before every quantised product).  The page prints
+no quantisation rule; the reading (or_quantize_q8): per 32 values d = max|x| / 127 in f32,
+q = x / d rounded to nearest with ties away from zero, d kept in binary16 (Q8_1 also
+s = d * sum q in binary16).  Pinned by hand-worked blocks whose d is exact, and by the
+identity with the already-pinned f32-activation product when x is exactly q * 2^-k."""
+import numpy as np
+
+import oracle
+import qdsynth
+
+
+def test_quantize_hand_block_d_one():
+    # max |x| = 127 -> d = 1 exactly; codes are x rounded, ties away from zero
+    x = np.zeros(32, np.float32)
+    x[:8] = [-127.0, 126.5, -0.5, 0.5, 2.5, -2.5, 1.49, -100.25]
+    q, d, s = oracle.quantize_q8(x[None, :], with_sum=True)
+    assert q[0, :8].tolist() == [-127, 127, -1, 1, 3, -3, 1, -100]
+    assert (q[0, 8:] == 0).all()
+    assert d[0, 0] == 1.0
+    assert s[0, 0] == -99.0  # d * (-127 + 127 - 1 + 1 + 3 - 3 + 1 - 100)
+
+
+def test_quantize_hand_block_d_half():
+    # max |x| = 63.5 -> d = 0.5 exactly: 0.25 / 0.5 = 0.5 -> 1, -0.75 / 0.5 = -1.5 -> -2
+    x = np.zeros(32, np.float32)
+    x[0], x[1], x[2], x[31] = 63.5, 0.25, -0.75, -10.0
+    q, d, _ = oracle.quantize_q8(x[None, :])
+    assert (q[0, 0], q[0, 1], q[0, 2], q[0, 31]) == (127, 1, -2, -20)
+    assert d[0, 0] == 0.5
+
+
+def test_quantize_zero_and_non_finite_blocks():
+    x = np.zeros((1, 96), np.float32)
+    x[0, 40] = np.nan
+    x[0, 64:] = 3.0
+    q, d, s = oracle.quantize_q8(x, with_sum=True)
+    assert d[0, 0] == 0.0 and s[0, 0] == 0.0 and (q[0, :32] == 0).all()       # zero block
+    assert np.isnan(d[0, 1]) and np.isnan(s[0, 1]) and (q[0, 32:64] == 0).all()  # NaN block
+    assert (q[0, 64:] == 127).all() and d[0, 2] == np.float32(np.float16(3.0 / 127))
+
+
+def test_product_hand_block():
+    # W: one Q8_0 block, d_w = 0.25, code 4 at element 0; x: 127 at element 0 (d_x = 1)
+    blk = np.zeros(34, np.uint8)
+    blk[0:2] = np.array([0.25], np.float16).view(np.uint8)
+    blk[2] = 4
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0] = 127.0
+    q, d, _ = oracle.quantize_q8(x)
+    assert oracle.gemv_q8act("q8_0", blk, 1, 32, q, d)[0, 0] == 127.0  # 0.25 * 1 * 4 * 127
+
+
+def _exact_x(seed, batch, cols, k):
+    """x = q * 2^-k with every block's largest |q| = 127: the quantiser returns q and
+    d = 2^-k exactly."""
+    q = qdsynth.ints_i32(seed, "xq", batch * cols, -20, 20).reshape(batch, cols)
+    q[:, ::32] = 127
+    return (q * 2.0 ** -k).astype(np.float32), q
+
+
+def test_product_equals_f32_product_for_exact_x():
+    for fmt in ("q8_0", "q4_0"):
+        rows, cols = 9, 256
+        w = qdsynth.weight_src(fmt, 11, "w" + fmt, rows, cols)
+        x, qx = _exact_x(11, 3, cols, 6)
+        q, d, _ = oracle.quantize_q8(x)
+        assert np.array_equal(q, qx) and (d == 2.0 ** -6).all()
+        np.testing.assert_allclose(oracle.gemv_q8act(fmt, w, rows, cols, q, d), oracle.gemv(fmt, w, rows, cols, x),
+                                   rtol=1e-12, atol=0)
+
+
+def test_q4_1_product_uses_the_block_sum():
+    # Q4_1: sum (d q_w + m) x = d d_x sum q_w q_x + m * (d_x sum q_x); with x exact and the
+    # block sums small, s = d_x sum q_x is exact in binary16 and the two products agree
+    rows, cols = 7, 128
+    w = qdsynth.weight_src("q4_1", 12, "w41", rows, cols)
+    x, qx = _exact_x(12, 2, cols, 5)
+    q, d, s = oracle.quantize_q8(x, with_sum=True)
+    assert np.array_equal(s, (qx.reshape(2, -1, 32).sum(axis=2) * 2.0 ** -5).astype(np.float32))
+    np.testing.assert_allclose(oracle.gemv_q8act("q4_1", w, rows, cols, q, d, s),
+                               oracle.gemv("q4_1", w, rows, cols, x), rtol=1e-12, atol=0)
