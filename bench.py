@@ -672,6 +672,53 @@ def run_gemm_only(spec: str, reps: int):
     print(json.dumps({"gemm": res, "bf16_peak_tflops": bf16, "peak_kind": kind}))
 
 
+def run_q8act_only(spec: str, reps: int):
+    """The ggml-exact activation path alone, e.g. "q4_0:14336x4096:1": the Q8 quantiser and
+    the integer product, each timed with L2 flushed before every launch; prints one JSON
+    line (not the benchmark contract line)."""
+    import torch
+
+    import qdsynth
+    import quantized_decode_gemv_gb300 as qd
+
+    fmt, shape, b = spec.split(":")
+    rows, cols = (int(v) for v in shape.split("x"))
+    batch = int(b)
+    if not os.path.exists(qd.LIB_PATH):
+        qd.build()
+    qd.load()
+    hbm, _, kind = peaks()
+    src = qdsynth.weight_src(fmt, 0, f"q8a{rows}x{cols}", rows, cols)
+    s = torch.from_numpy(np.ascontiguousarray(src.reshape(-1).view(np.uint8))).cuda()
+    w = torch.empty(qd.packed_bytes(fmt, rows, cols), dtype=torch.uint8, device="cuda")
+    qd.repack(fmt, s, rows, cols, w)
+    x = torch.from_numpy(qdsynth.activations(0, f"q8ax{cols}", batch, cols)).cuda()
+    with_sum = fmt == "q4_1"
+    xq = torch.empty(qd.q8_bytes(batch, cols, with_sum), dtype=torch.uint8, device="cuda")
+    y = torch.empty(batch, rows, dtype=torch.float32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name, call in (("quantize", lambda: qd.quantize_q8(x, batch, cols, xq, with_sum, stream=stream)),
+                       ("product", lambda: qd.q_gemv_q8(fmt, w, rows, cols, xq, y, batch, stream=stream))):
+        ts = []
+        for i in range(3 + max(reps, 10)):
+            flush.fill_(0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(e0.elapsed_time(e1) / 1e3)
+        res[name] = {"us": round(statistics.median(ts) * 1e6, 2)}
+    by = qd.packed_bytes(fmt, rows, cols) + xq.numel() + 4 * batch * rows
+    t = res["product"]["us"] / 1e6
+    res["product"].update({"algorithmic_bytes": int(by), "GB/s": round(by / t / 1e9, 1),
+                           "frac": round(by / t / 1e9 / hbm, 4)})
+    print(json.dumps({"q8act": spec, **res, "peak": hbm, "peak_kind": kind}))
+
+
 def run_quantize_only(spec: str, reps: int):
     """The BF16 -> INT8 quantiser alone at ROWSxCOLS; prints one JSON line (not the
     benchmark contract line)."""
@@ -722,6 +769,7 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=None, help="with --decode-1p7b: fewer layers (profiling)")
     ap.add_argument("--quantize", default=None, help="the BF16 -> INT8 quantiser alone at ROWSxCOLS")
     ap.add_argument("--gemm", default=None, help="the prefill product alone, FMT:ROWSxCOLS:TOKENS")
+    ap.add_argument("--q8act", default=None, help="the ggml-exact activation path alone, FMT:ROWSxCOLS:BATCH")
     ap.add_argument("--kv-f16", action="store_true", help="with --decode-1p7b: binary16 KV cache")
     args = ap.parse_args(argv)
     if args.gemv:
@@ -735,6 +783,9 @@ def main(argv=None):
         return
     if args.gemm:
         run_gemm_only(args.gemm, args.reps)
+        return
+    if args.q8act:
+        run_q8act_only(args.q8act, args.reps)
         return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -225,6 +225,30 @@ qd_status qd_q_gemm(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const
                     void* workspace, size_t workspace_bytes, qd_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
+/* ggml-exact activations ([go-llm] type CPU, "ExactGGML": activations are     */
+/* quantised to Q8_0, Q8_1 for Q4_1 weights, before every quantised product)  */
+/* and the product over them in integers ([llamini] "What I reimplemented":   */
+/* ggml multiplies packed bytes and converts only the scaled sum to float).   */
+/* Quantisation (the page prints no rule), per 32 values of a row of x:       */
+/* d = max|x| / 127 and q = x / d rounded to nearest, ties away from zero,    */
+/* clamped to +-127, both divisions IEEE round-to-nearest in f32; d is kept   */
+/* as binary16 and, with with_sum (Q8_1), s = d * sum(q) as binary16.  A zero */
+/* block has d = 0 and codes 0; a block holding a non-finite value codes 0    */
+/* and d = s = NaN.  Buffer layout (device, each region 16-byte aligned):     */
+/* int8 codes [batch][cols], then f16 d [batch][cols/32], then (with_sum)      */
+/* f16 s [batch][cols/32]; qd_q8_bytes gives its size (0: bad shape).          */
+/* batch 1..QD_MAX_BATCH, cols a multiple of 32.                               */
+/* qd_q_gemv_q8: y[b][r] = sum over blocks k of d_w d_x sum_j q_w q_x (Q4_0:  */
+/* q_w - 8; Q4_1: plus m_w s_x, so its activations need with_sum = 1), f32.   */
+/* fmt: QD_Q4_0, QD_Q8_0 or QD_Q4_1.  y: f32 [batch][rows].                    */
+/* ------------------------------------------------------------------------- */
+size_t qd_q8_bytes(int batch, int64_t cols, int with_sum);
+qd_status qd_quantize_q8(const float* x, int batch, int64_t cols, int with_sum, void* out, size_t out_bytes,
+                         qd_stream_t stream);
+qd_status qd_q_gemv_q8(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const void* xq, size_t xq_bytes,
+                       float* y, int batch, qd_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* Decode-step operations                                                      */
 /* ------------------------------------------------------------------------- */
 

@@ -24,7 +24,8 @@ STATUS = {0: "QD_OK", 1: "QD_ERR_INVALID_ARG", 2: "QD_ERR_SHAPE", 3: "QD_ERR_ALI
 # Every symbol include/qdecode.h declares (checked by the CPU test suite).
 EXPORTS = ["qd_status_str", "qd_abi_version", "qd_f16_to_f32", "qd_bf16_to_f32", "qd_src_bytes", "qd_packed_bytes",
            "qd_repack", "qd_unpack", "qd_dequant", "qd_quantize_i8_rows", "qd_q_gemv_workspace", "qd_q_gemv",
-           "qd_q_gemv_ex", "qd_q_gemm_workspace", "qd_q_gemm", "qd_rmsnorm",
+           "qd_q_gemv_ex", "qd_q_gemm_workspace", "qd_q_gemm", "qd_q8_bytes",
+           "qd_quantize_q8", "qd_q_gemv_q8", "qd_rmsnorm",
            "qd_rope_table", "qd_rope", "qd_kv_append", "qd_gqa_decode_attn_workspace", "qd_gqa_decode_attn",
            "qd_gqa_decode_attn_noalloc",
            "qd_swiglu", "qd_argmax", "qd_embed", "qd_model_weight_bytes", "qd_model_state_bytes",
@@ -78,6 +79,9 @@ def load():
         "qd_q_gemv_ex": ([i32, p, i64, i64, p, p, i32, ctypes.c_uint, p], i32),
         "qd_q_gemm_workspace": ([i32, i64, i64, i32], sz),
         "qd_q_gemm": ([i32, p, i64, i64, p, p, i32, p, sz, p], i32),
+        "qd_q8_bytes": ([i32, i64, i32], sz),
+        "qd_quantize_q8": ([p, i32, i64, i32, p, sz, p], i32),
+        "qd_q_gemv_q8": ([i32, p, i64, i64, p, sz, p, i32, p], i32),
         "qd_rmsnorm": ([p, p, p, i32, i32, f32, p], i32),
         "qd_rope_table": ([f32, i32, i32, p], i32),
         "qd_rope": ([p, i32, i32, i64, p, i32, p, i32, i32, p], i32),
@@ -190,6 +194,24 @@ def q_gemm(fmt, W, rows, cols, x, y, t, workspace, workspace_bytes=None, stream=
         workspace_bytes = workspace.numel() * workspace.element_size()
     _check("qd_q_gemm", load().qd_q_gemm(FMT[fmt], _ptr(W), rows, cols, _ptr(x), _ptr(y), t, _ptr(workspace),
                                          workspace_bytes, _stream(stream)))
+
+
+def q8_bytes(batch, cols, with_sum=False) -> int:
+    return int(load().qd_q8_bytes(batch, cols, 1 if with_sum else 0))
+
+
+def quantize_q8(x, batch, cols, out, with_sum=False, out_bytes=None, stream=None):
+    """ggml-exact Q8_0 (Q8_1 with with_sum) activations of x [batch][cols] into out."""
+    nbytes = out.numel() * out.element_size() if out_bytes is None else out_bytes
+    _check("qd_quantize_q8", load().qd_quantize_q8(_ptr(x), batch, cols, 1 if with_sum else 0, _ptr(out), nbytes,
+                                                   _stream(stream)))
+
+
+def q_gemv_q8(fmt, W, rows, cols, xq, y, batch, xq_bytes=None, stream=None):
+    """y = W x over quantised activations xq (quantize_q8 output) in integers."""
+    nbytes = xq.numel() * xq.element_size() if xq_bytes is None else xq_bytes
+    _check("qd_q_gemv_q8", load().qd_q_gemv_q8(FMT[fmt], _ptr(W), rows, cols, _ptr(xq), nbytes, _ptr(y), batch,
+                                               _stream(stream)))
 
 
 def q_gemv(fmt, W, rows, cols, x, y, batch, workspace=None, workspace_bytes=0, stream=None):

@@ -109,6 +109,23 @@ def test_gemm_validation_before_any_device_work(lib):
     assert f(0, good, 300, 512, good, good, 80, good + 8, need, None) == 3  # misaligned workspace
 
 
+def test_q8_activation_validation(lib):
+    good = 4096
+    assert lib.qd_q8_bytes(3, 64, 0) == 3 * 64 + 16             # codes, then 3 x 2 f16 d (padded)
+    assert lib.qd_q8_bytes(3, 64, 1) == 3 * 64 + 16 + 16        # ... then 3 x 2 f16 s
+    assert lib.qd_q8_bytes(0, 64, 0) == 0 and lib.qd_q8_bytes(17, 64, 0) == 0 and lib.qd_q8_bytes(3, 48, 0) == 0
+    assert lib.qd_q8_bytes(3, 64, 2) == 0
+    q = lib.qd_quantize_q8
+    assert q(None, 3, 64, 0, good, 4096, None) == 1              # null x
+    assert q(good, 3, 48, 0, good, 4096, None) == 2              # cols % 32
+    assert q(good, 3, 64, 0, good + 4, 4096, None) == 3          # misaligned out
+    assert q(good, 3, 64, 0, good, 100, None) == 6               # out too small
+    g = lib.qd_q_gemv_q8
+    assert g(2, good, 8, 256, good, 4096, good, 1, None) == 4    # Q4_K: no integer product here
+    assert g(0, good, 8, 48, good, 4096, good, 1, None) == 2     # cols % 32
+    assert g(4, good, 8, 64, good, lib.qd_q8_bytes(1, 64, 0), good, 1, None) == 6  # Q4_1 needs the sums
+
+
 def test_other_entry_points_validate(lib):
     good = 4096
     assert lib.qd_repack(0, good, 8, 64, good, 10, None) == 6              # dst too small
