@@ -643,7 +643,36 @@ typedef struct {
     double rope_theta, eps;
     int pairing, w_fmt, emb_fmt;
     int kv_f16; /* 1: the cache stores k and v rounded through binary16 ([go-llm] RoundF16) */
+    int act_q8; /* 1: every quantised product takes its activations (rounded to f32) as Q8_0
+                 * -- Q8_1 for Q4_1 weights -- and multiplies in integers ([go-llm]
+                 * "ExactGGML"; or_quantize_q8, or_gemv_q8act) */
 } or_config;
+
+int or_quantize_q8(const float* x, int64_t n, int8_t* q, float* d16, float* s16);
+int or_gemv_q8act(int fmt, const uint8_t* w, int64_t rows, int64_t cols, const int8_t* xq, const float* xd,
+                  const float* xs, int batch, int64_t row0, int64_t nrows, double* y);
+
+/* y[0..rows) = W x for one activation vector: over the f32-rounded activations' Q8 blocks
+ * (act_q8) or, otherwise, the plain double product. */
+static int product(const or_config* c, int fmt, const uint8_t* w, int64_t rows, int64_t cols, const double* x,
+                   double* y) {
+    if (!c->act_q8) {
+        gemv_rows_d(fmt, w, rows, cols, x, 1, cols, y, rows, 0, rows);
+        return 0;
+    }
+    float* xf = (float*)malloc(sizeof(float) * (size_t)cols);
+    int8_t* q = (int8_t*)malloc((size_t)cols);
+    float* d = (float*)malloc(sizeof(float) * (size_t)(cols / 32));
+    float* sm = (float*)malloc(sizeof(float) * (size_t)(cols / 32));
+    int rc = -2;
+    if (xf && q && d && sm) {
+        for (int64_t i = 0; i < cols; ++i) xf[i] = (float)x[i];
+        rc = or_quantize_q8(xf, cols, q, d, sm);
+        if (!rc) rc = or_gemv_q8act(fmt, w, rows, cols, q, d, sm, 1, 0, rows, y);
+    }
+    free(xf); free(q); free(d); free(sm);
+    return rc;
+}
 
 int or_decode_step(const or_config* c, const void* const* tensors, float* k_cache, float* v_cache,
                    int64_t layer_stride, int pos, int token, double* logits, int64_t* next_token) {
@@ -676,9 +705,10 @@ int or_decode_step(const or_config* c, const void* const* tensors, float* k_cach
         float* vl = v_cache + (int64_t)l * layer_stride;
         /* attention block */
         or_rmsnorm_d(x, (const float*)L[0], D, c->eps, xn);
-        gemv_rows_d(c->w_fmt, (const uint8_t*)L[1], QD, D, xn, 1, D, q, QD, 0, QD);
-        gemv_rows_d(c->w_fmt, (const uint8_t*)L[2], KD, D, xn, 1, D, k, KD, 0, KD);
-        gemv_rows_d(c->w_fmt, (const uint8_t*)L[3], KD, D, xn, 1, D, v, KD, 0, KD);
+        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[1], QD, D, xn, q)) ||
+            (rc = product(c, c->w_fmt, (const uint8_t*)L[2], KD, D, xn, k)) ||
+            (rc = product(c, c->w_fmt, (const uint8_t*)L[3], KD, D, xn, v)))
+            goto done;
         for (int h = 0; h < hq; ++h) or_rope_head_d(q + (int64_t)h * hd, hd, pos, c->pairing, c->rope_theta);
         for (int h = 0; h < hk; ++h) or_rope_head_d(k + (int64_t)h * hd, hd, pos, c->pairing, c->rope_theta);
         for (int h = 0; h < hk; ++h)
@@ -692,20 +722,21 @@ int or_decode_step(const or_config* c, const void* const* tensors, float* k_cach
                 vl[((int64_t)h * c->max_ctx + pos) * hd + i] = vf;
             }
         or_attention_d(q, kl, vl, hq, hk, hd, pos + 1, c->max_ctx, att);
-        gemv_rows_d(c->w_fmt, (const uint8_t*)L[4], D, QD, att, 1, QD, t, D, 0, D);
+        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[4], D, QD, att, t))) goto done;
         for (int i = 0; i < D; ++i) x[i] += t[i];
         /* feed-forward block */
         or_rmsnorm_d(x, (const float*)L[5], D, c->eps, xn);
-        gemv_rows_d(c->w_fmt, (const uint8_t*)L[6], F, D, xn, 1, D, g, F, 0, F);
-        gemv_rows_d(c->w_fmt, (const uint8_t*)L[7], F, D, xn, 1, D, u, F, 0, F);
+        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[6], F, D, xn, g)) ||
+            (rc = product(c, c->w_fmt, (const uint8_t*)L[7], F, D, xn, u)))
+            goto done;
         for (int i = 0; i < F; ++i) g[i] = or_silu(g[i]) * u[i];
-        gemv_rows_d(c->w_fmt, (const uint8_t*)L[8], D, F, g, 1, F, t, D, 0, D);
+        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[8], D, F, g, t))) goto done;
         for (int i = 0; i < D; ++i) x[i] += t[i];
     }
     or_rmsnorm_d(x, (const float*)tensors[1], D, c->eps, xn);
     {
         const uint8_t* head = (const uint8_t*)(tensors[2] ? tensors[2] : tensors[0]);
-        gemv_rows_d(c->emb_fmt, head, c->vocab, D, xn, 1, D, logits, c->vocab, 0, c->vocab);
+        if ((rc = product(c, c->emb_fmt, head, c->vocab, D, xn, logits))) goto done;
     }
     if (next_token) *next_token = or_argmax_f64(logits, c->vocab);
 done:

@@ -80,3 +80,22 @@ def test_q4_1_product_uses_the_block_sum():
     assert np.array_equal(s, (qx.reshape(2, -1, 32).sum(axis=2) * 2.0 ** -5).astype(np.float32))
     np.testing.assert_allclose(oracle.gemv_q8act("q4_1", w, rows, cols, q, d, s),
                                oracle.gemv("q4_1", w, rows, cols, x), rtol=1e-12, atol=0)
+
+
+def test_decode_step_ggml_exact_mode_close_to_f32():
+    """The decode step with every product over Q8 activations and a binary16 cache stays
+    within the activation quantisation's reach of the f32 step (each value moves by at most
+    1/254 of its block's largest |x|): 2e-2 of the largest logit over three steps."""
+    cfg = dict(layers=2, dim=256, ffn=512, n_heads=4, n_kv_heads=2, head_dim=64, vocab=300, rope_theta=1e4,
+               eps=1e-5, pairing="half", w_fmt="q4_0", emb_fmt="q8_0", max_ctx=16)
+    host = qdsynth.model_tensors(cfg, 3)
+    out = {}
+    for exact in (False, True):
+        om = oracle.Model(dict(cfg, act_q8=exact, kv_f16=exact), host)
+        kc = np.zeros(2 * 2 * 16 * 64, np.float32)
+        vc = np.zeros_like(kc)
+        for p, tok in enumerate([5, 17, 200]):
+            lg, _ = om.decode_step(kc, vc, 2 * 16 * 64, p, tok)
+        out[exact] = lg
+    diff = np.abs(out[True] - out[False]).max() / np.abs(out[False]).max()
+    assert 0 < diff < 2e-2
