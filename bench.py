@@ -343,6 +343,7 @@ def run_ours(args, world, rank, local):
             out["prefill_gemm"].append(g)
         del model
         torch.cuda.empty_cache()
+        out["decode_135m_modes"] = bench_135m_modes(qd, torch, stream)
         if not args.no_1p7b:
             out["decode_1p7b"] = bench_1p7b(qd, torch, stream, args, hbm)
             out["decode_1p7b"].update(bench_1p7b(qd, torch, stream, args, hbm, kv_f16=True))
@@ -509,6 +510,41 @@ def bench_1p7b(qd, torch, stream, args, hbm, batches=(1, 16), layers=None, kv_f1
                                 "frac": round(gbs / hbm, 4), "frac_nominal_8tbs": round(gbs / 8000, 4)}
         m.close()
         del m, flush
+        torch.cuda.empty_cache()
+    return out
+
+
+def bench_135m_modes(qd, torch, stream, steps=50):
+    """135M-shaped decode, batch 1, in the default mode (f32 activations, f32 cache) and in
+    the pages' ggml-exact mode (Q8_0 activations before every product, binary16 cache):
+    tokens/s over `steps` consecutive steps from position 150 (graph replays)."""
+    import qdsynth
+
+    out = {}
+    for name, extra in (("f32", {}), ("ggml_exact", {"act_q8": True, "kv_f16": True})):
+        cfg = dict(qdsynth.SMOL_135M, **extra)
+        host = qdsynth.model_tensors(cfg, 0)
+        srcs = [None if t is None else torch.from_numpy(np.ascontiguousarray(t)).cuda() for t in host]
+        m = qd.Model(qd.make_config(cfg, 256, 1), srcs)
+        del srcs
+        tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+        outt = torch.empty(1, dtype=torch.int32, device="cuda")
+        for _ in range(3):
+            m.set_pos([150], stream)
+            m.decode_step(tok, 1, outt, None, stream)
+        m.set_pos([150], stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            m.decode_step(outt, 1, outt, None, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / steps
+        out[name] = {"ms_per_token": round(t * 1e3, 4), "tokens/s": round(1 / t, 1),
+                     "launches_per_token": m.launches_per_step()}
+        m.close()
+        del m
         torch.cuda.empty_cache()
     return out
 
@@ -770,6 +806,7 @@ def main(argv=None):
     ap.add_argument("--quantize", default=None, help="the BF16 -> INT8 quantiser alone at ROWSxCOLS")
     ap.add_argument("--gemm", default=None, help="the prefill product alone, FMT:ROWSxCOLS:TOKENS")
     ap.add_argument("--q8act", default=None, help="the ggml-exact activation path alone, FMT:ROWSxCOLS:BATCH")
+    ap.add_argument("--modes-135m", action="store_true", help="135M decode in the default and ggml-exact modes")
     ap.add_argument("--kv-f16", action="store_true", help="with --decode-1p7b: binary16 KV cache")
     args = ap.parse_args(argv)
     if args.gemv:
@@ -786,6 +823,14 @@ def main(argv=None):
         return
     if args.q8act:
         run_q8act_only(args.q8act, args.reps)
+        return
+    if args.modes_135m:
+        import torch
+
+        import quantized_decode_gemv_gb300 as qd
+
+        qd.load()
+        print(json.dumps({"decode_135m_modes": bench_135m_modes(qd, torch, torch.cuda.current_stream())}))
         return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

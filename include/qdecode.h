@@ -346,6 +346,11 @@ typedef struct {
     int kv_f16;     /* 0: f32 KV cache; 1: binary16 KV cache (go-llm's ggml-exact  */
                     /* cache: k and v rounded to nearest binary16 when appended,  */
                     /* read back exactly; half the cache bytes)                   */
+    int act_q8;     /* 0: products over f32 activations; 1: every quantised       */
+                    /* product over Q8_0 activations (qd_quantize_q8 rule) in     */
+                    /* integers (go-llm's ggml-exact products); w_fmt and emb_fmt */
+                    /* must then be QD_Q4_0 or QD_Q8_0.  With kv_f16 = 1 this is  */
+                    /* the pages' whole ggml-exact mode.                           */
 } qd_config;
 
 typedef struct qd_model qd_model;

@@ -349,6 +349,14 @@ size_t gemm_workspace_bytes(int64_t cols, int t);
 qd_status launch_q_gemm(int fmt, const PackedView& W, const float* x, float* y, int t, void* ws, uint32_t* err,
                         cudaStream_t stream);
 
+// ggml-exact activations: Q8_0 (Q8_1 with with_sum) quantisation of x [batch][cols] into
+// out (codes, then f16 d, then f16 s; q8_buffer_bytes), and the product over them with the
+// store / accumulate / SwiGLU epilogues (Q4_0, Q8_0, Q4_1).
+size_t q8_buffer_bytes(int batch, int64_t cols, bool with_sum);
+qd_status launch_quantize_q8(const float* x, int batch, int64_t cols, bool with_sum, void* out, cudaStream_t stream);
+qd_status launch_q_gemv_q8(int fmt, const PackedView& W, const void* xq, int batch, float* y, int mode,
+                           cudaStream_t stream);
+
 qd_status launch_rmsnorm(const float* x, const float* g, float* out, int n, int batch, float eps,
                          cudaStream_t stream);
 qd_status launch_rope(float* v, int n_heads, int head_dim, int64_t batch_stride, const int32_t* pos, int pairing,

@@ -12,6 +12,7 @@
 // 4-byte token read back), the whole step is recorded once and replayed: here as
 // a CUDA graph per batch size whose kernels read each sequence's position from
 // device memory, so the same graph serves every token.
+#include <algorithm>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -35,6 +36,7 @@ struct Layout {
   size_t kc, vc, x, xn, qkv, q, att, act, logits, am_key, am_cnt, tok_in, tok_out, pos, err,
       rope;
   size_t attn_ws, attn_cnt;  // flat-split attention: partials and per-pair counters
+  size_t xq;                 // act_q8: the quantised activations of the current product
   bool attn_flat;
   int attn_ctas;  // its grid (one CTA per SM), fixed with the workspace size
   size_t state_bytes;
@@ -49,6 +51,10 @@ bool config_ok(const qd_config* c) {
   if (c->max_ctx < 1 || c->max_batch < 1 || c->max_batch > QD_MAX_BATCH) return false;
   if (c->pairing != QD_ROPE_ADJACENT && c->pairing != QD_ROPE_HALF) return false;
   if (c->kv_f16 != 0 && c->kv_f16 != 1) return false;
+  if (c->act_q8 != 0 && c->act_q8 != 1) return false;
+  // the integer products over Q8_0 activations take Q4_0 and Q8_0 weights
+  if (c->act_q8 && ((c->w_fmt != QD_Q4_0 && c->w_fmt != QD_Q8_0) || (c->emb_fmt != QD_Q4_0 && c->emb_fmt != QD_Q8_0)))
+    return false;
   if (!model_fmt_ok(c->w_fmt) || !model_fmt_ok(c->emb_fmt)) return false;
   if (!(c->eps >= 0.f) || !(c->rope_theta > 0.f)) return false;
   const int64_t QD = (int64_t)c->n_heads * c->head_dim, KD = (int64_t)c->n_kv_heads * c->head_dim;
@@ -109,6 +115,7 @@ Layout make_layout(const qd_config* c) {
   L.attn_ctas = attn_flat_ctas();
   L.attn_ws = L.attn_flat ? take(4 * attn_flat_ws_floats(c->n_heads, c->n_kv_heads, c->max_batch, L.attn_ctas)) : 0;
   L.attn_cnt = L.attn_flat ? take(4 * (size_t)c->n_kv_heads * c->max_batch) : 0;
+  L.xq = c->act_q8 ? take(q8_buffer_bytes((int)B, std::max(std::max(D, F), QD), false)) : 0;
   L.state_bytes = off;
   return L;
 }
@@ -177,6 +184,23 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
     a.pdl = true;
     return a;
   };
+  // ggml-exact products (act_q8): the norm (into xn) when the product has one, the Q8_0
+  // quantisation of its input, then the integer product; launched without programmatic
+  // dependence (they run once their predecessor has completed and never let their
+  // successor start early).
+  void* xq = m->s + L.xq;
+  auto q8prod = [&](int fmt, PackedView W, const float* in, const float* gains, float* y,
+                    GemvMode mode) -> qd_status {
+    if (gains) {
+      QD_TRY(launch_rmsnorm(in, gains, xn, (int)W.cols, batch, c.eps, st));
+      in = xn;
+      ++n;
+    }
+    QD_TRY(launch_quantize_q8(in, batch, W.cols, false, xq, st));
+    QD_TRY(launch_q_gemv_q8(fmt, W, xq, batch, y, mode, st));
+    n += 2;
+    return QD_OK;
+  };
   // GEMV with RMSNorm fused into its prologue when the streaming kernel runs; a
   // separate norm kernel (into xn) otherwise.
   auto normed = [&](GemvArgs a, const float* gains) -> qd_status {
@@ -213,7 +237,11 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
     e.cache_batch_stride = L.cache_batch_stride;
     e.max_ctx = c.max_ctx;
     const float* attn_norm = reinterpret_cast<const float*>(m->w + o.attn_norm);
-    if (gemv_streams(qa)) {
+    if (c.act_q8) {
+      QD_TRY(q8prod(c.w_fmt, qa.W, x, attn_norm, qkv, kGemvStore));
+      QD_TRY(launch_qkv_post(qkv, L.qkv_rows, batch, e, err, st, true));
+      ++n;
+    } else if (gemv_streams(qa)) {
       QD_TRY(normed(qa, attn_norm));
     } else {
       GemvArgs raw = qa;
@@ -231,6 +259,13 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
                                       L.cache_batch_stride, att, c.n_heads, c.n_kv_heads,
                                       c.head_dim, pos, c.max_ctx, batch, err, st, true));
     ++n;
+    if (c.act_q8) {
+      QD_TRY(q8prod(c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, nullptr, x, kGemvAccumulate));
+      QD_TRY(q8prod(c.w_fmt, m->W(c.w_fmt, o.wgu, 2 * F, D), x, reinterpret_cast<const float*>(m->w + o.ffn_norm),
+                    act, kGemvSwiGLU));
+      QD_TRY(q8prod(c.w_fmt, m->W(c.w_fmt, o.wd, D, F), act, nullptr, x, kGemvAccumulate));
+      continue;
+    }
     QD_TRY(launch_q_gemv(args(c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, x, kGemvAccumulate), st));
     ++n;
     QD_TRY(normed(args(c.w_fmt, m->W(c.w_fmt, o.wgu, 2 * F, D), x, act, kGemvSwiGLU),
@@ -245,7 +280,11 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
   ha.am.tok_out = m->i(L.tok_out);
   ha.am.pos = pos;
   const float* out_norm = reinterpret_cast<const float*>(m->w + L.out_norm);
-  if (gemv_streams(ha)) {
+  if (c.act_q8) {
+    QD_TRY(q8prod(c.emb_fmt, ha.W, x, out_norm, m->f(L.logits), kGemvStore));
+    QD_TRY(launch_argmax(m->f(L.logits), c.vocab, batch, m->i(L.tok_out), pos, st));
+    ++n;
+  } else if (gemv_streams(ha)) {
     QD_TRY(normed(ha, out_norm));
   } else {
     ha.mode = kGemvStore;

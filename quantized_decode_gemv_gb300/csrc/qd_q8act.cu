@@ -67,7 +67,7 @@ __device__ __forceinline__ int dot_words(const uint32_t (&w)[8], const uint32_t 
 }
 
 template <int FMT, int R, int NB>
-__global__ void __launch_bounds__(256) k_gemv_q8(PackedView W, Q8View X, float* __restrict__ y, int batch) {
+__global__ void __launch_bounds__(256) k_gemv_q8(PackedView W, Q8View X, float* __restrict__ y, int batch, int mode) {
   const int lane = threadIdx.x & 31;
   const int64_t row0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * R;
   if (row0 >= W.rows) return;
@@ -139,28 +139,47 @@ __global__ void __launch_bounds__(256) k_gemv_q8(PackedView W, Q8View X, float* 
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc[i][b] = warp_sum(acc[i][b]);
   if (lane != 0) return;
+  if (mode == kGemvSwiGLU) {  // rows (row0, row0 + 1) are (gate_i, up_i), i = row0 / 2
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+      if (b < batch) {
+        const float g = acc[0][b];
+        y[(int64_t)b * (W.rows / 2) + row0 / 2] = g / (1.0f + expf(-g)) * acc[R - 1][b];
+      }
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     if (row0 + i >= W.rows) break;
 #pragma unroll
     for (int b = 0; b < NB; ++b)
-      if (b < batch) y[(int64_t)b * W.rows + row0 + i] = acc[i][b];
+      if (b < batch) {
+        float* dst = y + (int64_t)b * W.rows + row0 + i;
+        if (mode == kGemvAccumulate)
+          *dst += acc[i][b];
+        else
+          *dst = acc[i][b];
+      }
   }
 }
 
 template <int FMT, int R, int NB>
-qd_status launch_q8_t(const PackedView& W, const Q8View& X, float* y, int batch, cudaStream_t stream) {
+qd_status launch_q8_t(const PackedView& W, const Q8View& X, float* y, int batch, int mode, cudaStream_t stream) {
   const int64_t warps = (W.rows + R - 1) / R;
-  k_gemv_q8<FMT, R, NB><<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(W, X, y, batch);
+  k_gemv_q8<FMT, R, NB><<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(W, X, y, batch, mode);
   return launch_status();
 }
 
+// The SwiGLU epilogue needs each (gate, up) row pair in one warp: R = 2.
 template <int FMT>
-qd_status launch_q8_fmt(const PackedView& W, const Q8View& X, float* y, int batch, cudaStream_t stream) {
-  if (batch <= 1) return launch_q8_t<FMT, 2, 1>(W, X, y, batch, stream);
-  if (batch <= 4) return launch_q8_t<FMT, 2, 4>(W, X, y, batch, stream);
-  if (batch <= 8) return launch_q8_t<FMT, 1, 8>(W, X, y, batch, stream);
-  return launch_q8_t<FMT, 1, 16>(W, X, y, batch, stream);
+qd_status launch_q8_fmt(const PackedView& W, const Q8View& X, float* y, int batch, int mode, cudaStream_t stream) {
+  const bool pair = mode == kGemvSwiGLU;
+  if (batch <= 1) return launch_q8_t<FMT, 2, 1>(W, X, y, batch, mode, stream);
+  if (batch <= 4) return launch_q8_t<FMT, 2, 4>(W, X, y, batch, mode, stream);
+  if (batch <= 8) return pair ? launch_q8_t<FMT, 2, 8>(W, X, y, batch, mode, stream)
+                              : launch_q8_t<FMT, 1, 8>(W, X, y, batch, mode, stream);
+  return pair ? launch_q8_t<FMT, 2, 16>(W, X, y, batch, mode, stream)
+              : launch_q8_t<FMT, 1, 16>(W, X, y, batch, mode, stream);
 }
 
 // Layout of a quantised activation buffer: codes [batch][cols], then f16 d [batch][cols/32],
@@ -176,7 +195,39 @@ size_t q8_bytes(int batch, int64_t cols, bool with_sum) {
 
 bool q8_shape_ok(int batch, int64_t cols) { return batch >= 1 && batch <= QD_MAX_BATCH && cols >= 32 && cols % 32 == 0; }
 
+Q8View q8_view(const void* xq, int batch, int64_t cols, bool with_sum) {
+  const uint8_t* base = static_cast<const uint8_t*>(xq);
+  Q8View X;
+  X.q = reinterpret_cast<const int8_t*>(base);
+  X.d = reinterpret_cast<const __half*>(base + q8_d_offset(batch, cols));
+  X.s = with_sum ? reinterpret_cast<const __half*>(base + q8_s_offset(batch, cols)) : nullptr;
+  return X;
+}
+
 }  // namespace
+
+size_t q8_buffer_bytes(int batch, int64_t cols, bool with_sum) { return q8_bytes(batch, cols, with_sum); }
+
+qd_status launch_quantize_q8(const float* x, int batch, int64_t cols, bool with_sum, void* out, cudaStream_t stream) {
+  uint8_t* base = static_cast<uint8_t*>(out);
+  const int64_t blocks = (int64_t)batch * (cols / 32);
+  k_quantize_q8<<<(unsigned)((blocks + kQ8Warps - 1) / kQ8Warps), kQ8Warps * 32, 0, stream>>>(
+      x, blocks, reinterpret_cast<int8_t*>(base), reinterpret_cast<__half*>(base + q8_d_offset(batch, cols)),
+      with_sum ? reinterpret_cast<__half*>(base + q8_s_offset(batch, cols)) : nullptr);
+  return launch_status();
+}
+
+qd_status launch_q_gemv_q8(int fmt, const PackedView& W, const void* xq, int batch, float* y, int mode,
+                           cudaStream_t stream) {
+  const Q8View X = q8_view(xq, batch, W.cols, fmt == QD_Q4_1);
+  switch (fmt) {
+    case QD_Q4_0: return launch_q8_fmt<QD_Q4_0>(W, X, y, batch, mode, stream);
+    case QD_Q8_0: return launch_q8_fmt<QD_Q8_0>(W, X, y, batch, mode, stream);
+    case QD_Q4_1: return launch_q8_fmt<QD_Q4_1>(W, X, y, batch, mode, stream);
+    default: return QD_ERR_UNSUPPORTED;
+  }
+}
+
 }  // namespace qd
 
 using namespace qd;
@@ -194,12 +245,7 @@ qd_status qd_quantize_q8(const float* x, int batch, int64_t cols, int with_sum, 
   if (!q8_shape_ok(batch, cols)) return QD_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(out)) return QD_ERR_ALIGN;
   if (out_bytes < q8_bytes(batch, cols, with_sum != 0)) return QD_ERR_NOMEM;
-  uint8_t* base = static_cast<uint8_t*>(out);
-  const int64_t blocks = (int64_t)batch * (cols / 32);
-  k_quantize_q8<<<(unsigned)((blocks + kQ8Warps - 1) / kQ8Warps), kQ8Warps * 32, 0, (cudaStream_t)stream>>>(
-      x, blocks, reinterpret_cast<int8_t*>(base), reinterpret_cast<__half*>(base + q8_d_offset(batch, cols)),
-      with_sum ? reinterpret_cast<__half*>(base + q8_s_offset(batch, cols)) : nullptr);
-  return launch_status();
+  return launch_quantize_q8(x, batch, cols, with_sum != 0, out, (cudaStream_t)stream);
 }
 
 qd_status qd_q_gemv_q8(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const void* xq, size_t xq_bytes,
@@ -208,20 +254,8 @@ qd_status qd_q_gemv_q8(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, co
   if (!W || !xq || !y) return QD_ERR_INVALID_ARG;
   if (!q8_shape_ok(batch, cols) || !shape_ok(fmt, rows, cols)) return QD_ERR_SHAPE;
   if (!aligned16(W) || !aligned16(xq) || !aligned16(y)) return QD_ERR_ALIGN;
-  const bool with_sum = fmt == QD_Q4_1;  // Q8_1 activations
-  if (xq_bytes < q8_bytes(batch, cols, with_sum)) return QD_ERR_NOMEM;
-  const uint8_t* base = static_cast<const uint8_t*>(xq);
-  Q8View X;
-  X.q = reinterpret_cast<const int8_t*>(base);
-  X.d = reinterpret_cast<const __half*>(base + q8_d_offset(batch, cols));
-  X.s = with_sum ? reinterpret_cast<const __half*>(base + q8_s_offset(batch, cols)) : nullptr;
-  const PackedView v = packed_view(fmt, W, rows, cols);
-  cudaStream_t s = (cudaStream_t)stream;
-  switch (fmt) {
-    case QD_Q4_0: return launch_q8_fmt<QD_Q4_0>(v, X, y, batch, s);
-    case QD_Q8_0: return launch_q8_fmt<QD_Q8_0>(v, X, y, batch, s);
-    default: return launch_q8_fmt<QD_Q4_1>(v, X, y, batch, s);
-  }
+  if (xq_bytes < q8_bytes(batch, cols, fmt == QD_Q4_1)) return QD_ERR_NOMEM;  // Q4_1 takes Q8_1 activations
+  return launch_q_gemv_q8(fmt, packed_view(fmt, W, rows, cols), xq, batch, y, kGemvStore, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -41,7 +41,7 @@ def test_status_strings(lib):
     assert qd.status_str(0) == "ok"
     for s in range(1, 8):
         assert qd.status_str(s) != "unknown status"
-    assert lib.qd_abi_version() == 2
+    assert lib.qd_abi_version() == 3
 
 
 @pytest.mark.parametrize("fmt,rows,cols,src,packed", [
@@ -175,6 +175,14 @@ def test_model_sizes_and_config_refusals(lib):
         assert lib.qd_model_weight_bytes(ctypes.byref(bad)) == 0, f
         bad = qd.make_config(dict(qdsynth.SMOL_135M, emb_fmt=f), max_ctx=256, max_batch=1)
         assert lib.qd_model_state_bytes(ctypes.byref(bad)) == 0, f
+    # ggml-exact products take Q4_0 / Q8_0 weights only, and act_q8 is a flag
+    ok = qd.make_config(qdsynth.SMOL_135M, max_ctx=256, max_batch=1, act_q8=True)
+    assert lib.qd_model_state_bytes(ctypes.byref(ok)) > sb  # plus the quantised-activation buffer
+    bad = qd.make_config(dict(qdsynth.SMOL_135M, w_fmt="q4_k"), max_ctx=256, max_batch=1, act_q8=True)
+    assert lib.qd_model_state_bytes(ctypes.byref(bad)) == 0
+    bad = qd.make_config(qdsynth.SMOL_135M, max_ctx=256, max_batch=1)
+    bad.act_q8 = 2
+    assert lib.qd_model_state_bytes(ctypes.byref(bad)) == 0
     # a binary16 cache takes half the bytes (the state also gains the flat attention's workspace)
     h = qd.make_config(qdsynth.SMOL_135M, max_ctx=256, max_batch=1, kv_f16=True)
     sh = lib.qd_model_state_bytes(ctypes.byref(h))

@@ -23,16 +23,17 @@ def build_model(qd, cfg, seed, max_ctx, max_batch):
     return m, host
 
 
-def check_token(ora_logits, ora_tok, gpu_tok):
+def check_token(ora_logits, ora_tok, gpu_tok, tol=TOL):
     if gpu_tok == ora_tok:
         return 0
     gap = ora_logits[ora_tok] - ora_logits[gpu_tok]
-    assert gap <= TOL * np.abs(ora_logits).max(), f"token {gpu_tok} vs oracle {ora_tok}, gap {gap}"
+    assert gap <= tol * np.abs(ora_logits).max(), f"token {gpu_tok} vs oracle {ora_tok}, gap {gap}"
     return 1
 
 
-def run_teacher_forced(qd, cfg, seed, prompt, n_gen, batch=1, max_ctx=None):
-    """Feed `prompt` (batch x P ids) then n_gen greedy tokens; compare every step's logits."""
+def run_teacher_forced(qd, cfg, seed, prompt, n_gen, batch=1, max_ctx=None, tol=TOL):
+    """Feed `prompt` (batch x P ids) then n_gen greedy tokens; compare every step's logits
+    (within `tol` of max |oracle|; near-tie tokens within the same gap)."""
     P = prompt.shape[1]
     max_ctx = max_ctx or (P + n_gen)
     m, host = build_model(qd, cfg, seed, max_ctx, batch)
@@ -52,9 +53,9 @@ def run_teacher_forced(qd, cfg, seed, prompt, n_gen, batch=1, max_ctx=None):
         assert m.check() == 0
         for b in range(batch):
             ol, ot = om.decode_step(okc[b], ovc[b], hk * max_ctx * hd, step, int(cur[b]))
-            worst = max(worst, assert_close(g[b], ol, what=f"logits step {step} seq {b}"))
+            worst = max(worst, assert_close(g[b], ol, tol=tol, what=f"logits step {step} seq {b}"))
             assert gt[b] == int(np.argmax(g[b]))  # GPU argmax is exact on its own logits
-            near += check_token(ol, ot, int(gt[b]))
+            near += check_token(ol, ot, int(gt[b]), tol)
         cur = prompt[:, step + 1].astype(np.int32) if step + 1 < P else gt.astype(np.int32)
     assert m.pos(batch) == [P + n_gen - 1] * batch
     m.close()
@@ -266,3 +267,21 @@ def test_kv_f16_teacher_forced(qd, w_fmt, emb_fmt, pairing, batch):
     prompt = qdsynth.tokens(24, "f16.prompt", batch * 5, cfg["vocab"]).reshape(batch, 5)
     worst, near = run_teacher_forced(qd, cfg, 24, prompt, n_gen=5, batch=batch, max_ctx=72)
     print(f"kv_f16 {w_fmt}: worst rel err {worst:.2e}, near-tie tokens {near}")
+
+
+@pytest.mark.parametrize("w_fmt,emb_fmt,batch,kv_f16", [("q4_0", "q8_0", 1, True), ("q8_0", "q8_0", 3, True),
+                                                        ("q4_0", "q8_0", 2, False)])
+def test_ggml_exact_teacher_forced(qd, w_fmt, emb_fmt, batch, kv_f16):
+    """go-llm's ggml-exact mode: every quantised product over Q8_0 activations in integers
+    (act_q8), with and without the binary16 cache, against the oracle in the same mode.  The
+    two sides form their f32 activations in different orders, so where a value sits within an
+    ulp of a rounding boundary a Q8 code or a binary16 cache value can differ by one step: a
+    flipped code moves a product by one quantum (1/127 of its block's largest |x|).  The page
+    says of this mode that it does not reproduce llama.cpp to 1e-3 and claims no tighter
+    bound; here: 1e-3 with the f32 cache (no flips on these inputs), 2e-2 (one quantum's
+    reach) with the binary16 cache, whose rounding adds the flips."""
+    cfg = dict(TINY, w_fmt=w_fmt, emb_fmt=emb_fmt, act_q8=True, kv_f16=kv_f16)
+    prompt = qdsynth.tokens(25, "q8.prompt", batch * 5, cfg["vocab"]).reshape(batch, 5)
+    worst, near = run_teacher_forced(qd, cfg, 25, prompt, n_gen=5, batch=batch, max_ctx=72,
+                                     tol=2e-2 if kv_f16 else 1e-3)
+    print(f"ggml-exact {w_fmt} kv_f16={kv_f16}: worst rel err {worst:.2e}, near-tie tokens {near}")
