@@ -20,7 +20,7 @@ _SRC = os.path.join(_HERE, "qd_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
-FMT = {"q4_0": 0, "q8_0": 1, "q4_k": 2, "i8": 3, "q4_1": 4, "q5_0": 5, "q5_k": 6, "q6_k": 7, "f16": 8}
+FMT = {"q4_0": 0, "q8_0": 1, "q4_k": 2, "i8": 3, "q4_1": 4, "q5_0": 5, "q5_k": 6, "q6_k": 7, "f16": 8, "i4": 9}
 PAIRING = {"adjacent": 0, "half": 1}
 
 
@@ -71,6 +71,8 @@ def _L():
         lib.or_dequant.restype = i32
         lib.or_gemv.argtypes = [i32, p, i64, i64, p, i32, i64, i64, p]
         lib.or_gemv.restype = i32
+        lib.or_quantize_i4_rows.argtypes = [p, i64, i64, p, p]
+        lib.or_quantize_i4_rows.restype = i32
         lib.or_quantize_q8.argtypes = [p, i64, p, p, p]
         lib.or_quantize_q8.restype = i32
         lib.or_gemv_q8act.argtypes = [i32, p, i64, i64, p, p, p, i32, i64, i64, p]
@@ -219,6 +221,19 @@ def swiglu(g, u) -> np.ndarray:
 def round_f16(f: float) -> float:
     """f32 rounded through binary16 (what an f16 KV cache stores)."""
     return float(_L().or_round_f16(float(np.float32(f))))
+
+
+def quantize_i4_rows(w_bf16, rows: int, cols: int) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row symmetric INT4 of BF16 weights (bit patterns, uint16 [rows][cols]):
+    (codes uint8 [rows][cols/2], two per byte, scales f32 [rows]); see or_quantize_i4_rows."""
+    w, wp = _c(np.asarray(w_bf16, np.uint16).reshape(-1), np.uint16)
+    assert w.size == rows * cols
+    codes = np.empty(rows * (cols // 2), np.uint8)
+    scales = np.empty(rows, np.float32)
+    rc = _L().or_quantize_i4_rows(wp, rows, cols, codes.ctypes.data, scales.ctypes.data)
+    if rc:
+        raise ValueError(f"or_quantize_i4_rows rc={rc}")
+    return codes.reshape(rows, cols // 2), scales
 
 
 def quantize_q8(x, with_sum: bool = False):

@@ -48,7 +48,8 @@
 #include <omp.h>
 #endif
 
-enum { OR_Q4_0 = 0, OR_Q8_0 = 1, OR_Q4_K = 2, OR_I8_ROW = 3, OR_Q4_1 = 4, OR_Q5_0 = 5, OR_Q5_K = 6, OR_Q6_K = 7, OR_F16 = 8 };
+enum { OR_Q4_0 = 0, OR_Q8_0 = 1, OR_Q4_K = 2, OR_I8_ROW = 3, OR_Q4_1 = 4, OR_Q5_0 = 5, OR_Q5_K = 6, OR_Q6_K = 7, OR_F16 = 8,
+       OR_I4_ROW = 9 };
 enum { OR_ROPE_ADJACENT = 0, OR_ROPE_HALF = 1 };
 
 /* ------------------------------------------------------------------------- */
@@ -147,6 +148,7 @@ static int64_t row_bytes(int fmt, int64_t cols) {
         case OR_Q5_K: return (cols / 256) * 176;
         case OR_Q6_K: return (cols / 256) * 210;
         case OR_F16: return cols * 2;
+        case OR_I4_ROW: return cols / 2;
         default: return -1;
     }
 }
@@ -163,6 +165,7 @@ int or_shape_ok(int fmt, int64_t rows, int64_t cols) {
         case OR_Q6_K: return cols % 256 == 0;
         case OR_I8_ROW:
         case OR_F16: return 1;
+        case OR_I4_ROW: return cols % 2 == 0;
         default: return 0;
     }
 }
@@ -280,6 +283,17 @@ static void dequant_row(int fmt, const uint8_t* w, int64_t rows, int64_t cols, i
         }
     } else if (fmt == OR_F16) {
         for (int64_t c = 0; c < cols; ++c) out[c] = (float)f16_at(row + 2 * c);
+    } else if (fmt == OR_I4_ROW) {
+        /* [minillm] "Quantization": symmetric per-row INT4, one scale per output row; codes
+         * two per byte (element 2i in the low nibble), two's complement, then the f32 row
+         * scales after all codes */
+        float sc;
+        memcpy(&sc, w + rows * (cols / 2) + 4 * r, sizeof sc);
+        for (int64_t c = 0; c < cols; ++c) {
+            const int nib = (row[c / 2] >> (4 * (c & 1))) & 0x0F;
+            const int q = nib >= 8 ? nib - 16 : nib;
+            out[c] = (float)((double)sc * q);
+        }
     } else { /* OR_I8_ROW ([minillm] "Quantization": one scale per output row) */
         float s;
         memcpy(&s, w + rows * cols + 4 * r, sizeof s);
@@ -505,6 +519,43 @@ int or_quantize_i8_rows(const uint16_t* w, int64_t rows, int64_t cols, int8_t* c
             if (q > 127.0f) q = 127.0f;
             if (q < -127.0f) q = -127.0f;
             qr[c] = (int8_t)q;
+        }
+    }
+    return 0;
+}
+
+/* Per-row symmetric INT4 of BF16 weights ([minillm] "Quantization": INT8 and INT4, one
+ * scale per output row).  The page prints no rule; the one implemented mirrors the INT8
+ * one with the 4-bit code range: s = max|w| / 7 (f32), q = w / s (f32) rounded to nearest
+ * with ties away from zero (C roundf), clamped to +-7; a row of zeros gets s = 0 and codes
+ * 0, a row holding a non-finite value codes 0 and a NaN scale.  codes: [rows][cols / 2]
+ * bytes, element 2i in the low nibble (two's complement). */
+int or_quantize_i4_rows(const uint16_t* w, int64_t rows, int64_t cols, uint8_t* codes, float* scales) {
+    if (rows < 1 || cols < 2 || cols % 2) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t* wr = w + r * cols;
+        uint8_t* qr = codes + r * (cols / 2);
+        float m = 0.0f;
+        int finite = 1;
+        for (int64_t c = 0; c < cols; ++c) {
+            const float v = or_bf16_to_f32(wr[c]);
+            if (!isfinite(v))
+                finite = 0;
+            else if (fabsf(v) > m)
+                m = fabsf(v);
+        }
+        for (int64_t c = 0; c < cols / 2; ++c) qr[c] = 0;
+        if (!finite || m == 0.0f) {
+            scales[r] = finite ? 0.0f : NAN;
+            continue;
+        }
+        const float s = m / 7.0f;
+        scales[r] = s;
+        for (int64_t c = 0; c < cols; ++c) {
+            float q = roundf(or_bf16_to_f32(wr[c]) / s);
+            if (q > 7.0f) q = 7.0f;
+            if (q < -7.0f) q = -7.0f;
+            qr[c / 2] |= (uint8_t)(((int)q & 0x0F) << (4 * (c & 1)));
         }
     }
     return 0;

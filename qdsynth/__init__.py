@@ -260,6 +260,18 @@ def i8_row_src(seed, name, rows, cols) -> np.ndarray:
     return np.concatenate([q.reshape(-1).view(np.uint8), s.view(np.uint8)])
 
 
+I4_SCALE_RANGE = (1e-3, 1e-1)
+
+
+def i4_row_src(seed, name, rows, cols) -> np.ndarray:
+    """Per-row INT4 tensor as one byte buffer: codes ``[rows][cols/2]`` (two nibbles per byte,
+    values -7..7 in two's complement) then f32 scales ``[rows]``."""
+    q = ints_u8(seed, name + ".q", rows * cols, -7, 7).reshape(rows, cols // 2, 2) & 0x0F
+    packed = (q[:, :, 0] | (q[:, :, 1] << 4)).astype(np.uint8)
+    s = uniform_f32(seed, name + ".s", rows, *I4_SCALE_RANGE)
+    return np.concatenate([packed.reshape(-1), s.view(np.uint8)])
+
+
 def weight_src(fmt: str, seed: int, name: str, rows: int, cols: int) -> np.ndarray:
     """Any format's tensor as the flat byte buffer both sides read."""
     if fmt == "q4_0":
@@ -270,6 +282,8 @@ def weight_src(fmt: str, seed: int, name: str, rows: int, cols: int) -> np.ndarr
         return q4_k_blocks(seed, name, rows, cols).reshape(-1)
     if fmt == "i8":
         return i8_row_src(seed, name, rows, cols)
+    if fmt == "i4":
+        return i4_row_src(seed, name, rows, cols)
     gen = {"q4_1": q4_1_blocks, "q5_0": q5_0_blocks, "q5_k": q5_k_blocks, "q6_k": q6_k_blocks,
            "f16": f16_weights}.get(fmt)
     if gen is None:
@@ -280,6 +294,8 @@ def weight_src(fmt: str, seed: int, name: str, rows: int, cols: int) -> np.ndarr
 def src_bytes(fmt: str, rows: int, cols: int) -> int:
     if fmt == "i8":
         return rows * cols + 4 * rows
+    if fmt == "i4":
+        return rows * cols // 2 + 4 * rows
     return rows * (cols // BLOCK_WEIGHTS[fmt]) * BLOCK_BYTES[fmt]
 
 
