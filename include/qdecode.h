@@ -94,6 +94,10 @@ typedef enum {
  *            2k, 2k+1 of qh[32h + l] above it, and scale 8h + 2k + l/16;
  *            value d*sc*(q-32).
  *  QD_F16    binary16 weights, 2 B each (little-endian).
+ *  QD_I4_ROW per-row symmetric INT4 ([minillm] "Quantization": INT8 and INT4, one
+ *            scale per output row): codes [rows][cols/2], two per byte (element 2i in
+ *            the low nibble, two's complement, -7..7), then one f32 scale per row;
+ *            value q*s_row.
  * The "source" layout of a tensor is the model-file layout above, rows in order
  * (for QD_I8_ROW: all codes, then all scales, in one buffer).  The decode step
  * (qd_model_*) takes QD_Q4_0, QD_Q8_0, QD_Q4_K and QD_I8_ROW; the layout calls,
@@ -107,7 +111,8 @@ typedef enum {
     QD_Q5_0 = 5,
     QD_Q5_K = 6,
     QD_Q6_K = 7,
-    QD_F16 = 8
+    QD_F16 = 8,
+    QD_I4_ROW = 9
 } qd_fmt;
 
 /* RoPE pairing ([llmoxide] 6): ADJACENT rotates (2i, 2i+1) (llama files), HALF
@@ -142,12 +147,13 @@ qd_status qd_bf16_to_f32(const uint16_t* in, float* out, int64_t n, qd_stream_t 
 /*  Q6_K: (ql, qh) [rows][cols/256][192 B], then (16 scales, d)               */
 /*        [rows][cols/256][18 B].                                             */
 /*  F16:  weights [rows][cols] (2 B each); no scale region.                   */
+/*  I4_ROW: codes [rows][cols/2], then f32 scales [rows].                     */
 /* The repack is lossless: qd_unpack restores the source bytes exactly.       */
 /* ------------------------------------------------------------------------- */
 
 /* Bytes of the source / packed layout; 0 for a shape the format does not allow
- * (rows < 1, cols < 1, cols % 32 for Q4_0/Q8_0/Q4_1/Q5_0/F16, cols % 256 for
- * Q4_K/Q5_K/Q6_K, cols % 16 for I8_ROW). */
+ * (rows < 1, cols < 1, cols % 32 for Q4_0/Q8_0/Q4_1/Q5_0/F16/I4_ROW, cols % 256
+ * for Q4_K/Q5_K/Q6_K, cols % 16 for I8_ROW). */
 size_t qd_src_bytes(qd_fmt fmt, int64_t rows, int64_t cols);
 size_t qd_packed_bytes(qd_fmt fmt, int64_t rows, int64_t cols);
 
@@ -173,6 +179,14 @@ qd_status qd_dequant(qd_fmt fmt, const void* packed, int64_t rows, int64_t cols,
  * then f32 scales [rows]; out_bytes >= qd_src_bytes(QD_I8_ROW, rows, cols)), ready for
  * qd_repack or a model's INT8 weights; must not overlap w_bf16.  cols % 16 == 0. */
 qd_status qd_quantize_i8_rows(const uint16_t* w_bf16, int64_t rows, int64_t cols, void* out, size_t out_bytes,
+                              qd_stream_t stream);
+
+/* The same for per-row INT4 ([minillm] "Quantization"): s_r = max_c |w_rc| / 7 (f32),
+ * q_rc = w_rc / s_r (f32) rounded to nearest with ties away from zero, clamped to
+ * [-7, 7]; zero and non-finite rows as above.  out: the QD_I4_ROW source layout (codes
+ * [rows][cols/2], then f32 scales [rows]; out_bytes >= qd_src_bytes(QD_I4_ROW, rows,
+ * cols)).  cols % 32 == 0. */
+qd_status qd_quantize_i4_rows(const uint16_t* w_bf16, int64_t rows, int64_t cols, void* out, size_t out_bytes,
                               qd_stream_t stream);
 
 /* ------------------------------------------------------------------------- */

@@ -15,7 +15,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqdecode.so")
 _lib = None
 
-FMT = {"q4_0": 0, "q8_0": 1, "q4_k": 2, "i8": 3, "q4_1": 4, "q5_0": 5, "q5_k": 6, "q6_k": 7, "f16": 8}
+FMT = {"q4_0": 0, "q8_0": 1, "q4_k": 2, "i8": 3, "q4_1": 4, "q5_0": 5, "q5_k": 6, "q6_k": 7, "f16": 8, "i4": 9}
 PAIRING = {"adjacent": 0, "half": 1}
 MAX_BATCH = 16
 STATUS = {0: "QD_OK", 1: "QD_ERR_INVALID_ARG", 2: "QD_ERR_SHAPE", 3: "QD_ERR_ALIGN", 4: "QD_ERR_UNSUPPORTED",
@@ -23,7 +23,8 @@ STATUS = {0: "QD_OK", 1: "QD_ERR_INVALID_ARG", 2: "QD_ERR_SHAPE", 3: "QD_ERR_ALI
 
 # Every symbol include/qdecode.h declares (checked by the CPU test suite).
 EXPORTS = ["qd_status_str", "qd_abi_version", "qd_f16_to_f32", "qd_bf16_to_f32", "qd_src_bytes", "qd_packed_bytes",
-           "qd_repack", "qd_unpack", "qd_dequant", "qd_quantize_i8_rows", "qd_q_gemv_workspace", "qd_q_gemv",
+           "qd_repack", "qd_unpack", "qd_dequant", "qd_quantize_i8_rows", "qd_quantize_i4_rows",
+           "qd_q_gemv_workspace", "qd_q_gemv",
            "qd_q_gemv_ex", "qd_q_gemm_workspace", "qd_q_gemm", "qd_q8_bytes",
            "qd_quantize_q8", "qd_q_gemv_q8", "qd_rmsnorm",
            "qd_rope_table", "qd_rope", "qd_kv_append", "qd_gqa_decode_attn_workspace", "qd_gqa_decode_attn",
@@ -74,6 +75,7 @@ def load():
         "qd_unpack": ([i32, p, i64, i64, p, sz, p], i32),
         "qd_dequant": ([i32, p, i64, i64, p, p], i32),
         "qd_quantize_i8_rows": ([p, i64, i64, p, sz, p], i32),
+        "qd_quantize_i4_rows": ([p, i64, i64, p, sz, p], i32),
         "qd_q_gemv_workspace": ([i32, i64, i64, i32], sz),
         "qd_q_gemv": ([i32, p, i64, i64, p, p, i32, p, sz, p], i32),
         "qd_q_gemv_ex": ([i32, p, i64, i64, p, p, i32, ctypes.c_uint, p], i32),
@@ -171,6 +173,12 @@ def unpack(fmt, packed, rows, cols, dst, dst_bytes=None, stream=None):
 
 def dequant(fmt, packed, rows, cols, out, stream=None):
     _check("qd_dequant", load().qd_dequant(FMT[fmt], _ptr(packed), rows, cols, _ptr(out), _stream(stream)))
+
+
+def quantize_i4_rows(w_bf16, rows, cols, out, out_bytes=None, stream=None):
+    nbytes = out.numel() * out.element_size() if out_bytes is None else out_bytes
+    _check("qd_quantize_i4_rows", load().qd_quantize_i4_rows(_ptr(w_bf16), rows, cols, _ptr(out), nbytes,
+                                                             _stream(stream)))
 
 
 def quantize_i8_rows(w_bf16, rows, cols, out, out_bytes=None, stream=None):

@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(kThreads) k_gemv_q4k(PackedView W, const float
   finish_rows<R, NB>(acc, row_scale, row0, W.rows, y, batch, mode, lane);
 }
 
-// The formats a Q4_K_M-class file mixes in (Q4_1, Q5_0, Q5_K, Q6_K, F16): the 32
+// The formats a Q4_K_M-class file mixes in (Q4_1, Q5_0, Q5_K, Q6_K, F16) and per-row INT4: the 32
 // dequantised f32 values of unit u (columns 32u .. 32u + 31) of row r, each rounded once
 // (as the test dequantiser).
 __device__ __forceinline__ float f16lo(uint32_t w) { return f16_bits_to_f32(w & 0xFFFFu); }
@@ -314,6 +314,9 @@ struct RawUnit {
     if constexpr (FMT == QD_F16) {
 #pragma unroll
       for (int t = 0; t < 4; ++t) a[t] = ld_stream_v4(cr + 64 * u + 16 * t);
+    } else if constexpr (FMT == QD_I4_ROW) {
+      a[0] = ld_stream_v4(cr + 16 * u);
+      s0 = __ldg(reinterpret_cast<const uint32_t*>(sr));  // the row scale (f32 bits)
     } else if constexpr (FMT == QD_Q4_1) {
       a[0] = ld_stream_v4(cr + 16 * u);
       s0 = __ldg(reinterpret_cast<const uint32_t*>(sr + 4 * u));
@@ -354,6 +357,15 @@ struct RawUnit {
           w[8 * t + 2 * k] = f16lo(h[k]);
           w[8 * t + 2 * k + 1] = f16hi(h[k]);
         }
+      }
+    } else if constexpr (FMT == QD_I4_ROW) {
+      // element 2i in the low nibble of byte i, two's complement
+      const uint32_t q[4] = {a[0].x, a[0].y, a[0].z, a[0].w};
+      const float sc = __uint_as_float(s0);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int nib = (int)((q[j >> 3] >> (4 * (j & 7))) & 15u);
+        w[j] = sc * (float)(nib >= 8 ? nib - 16 : nib);
       }
     } else if constexpr (FMT == QD_Q4_1 || FMT == QD_Q5_0) {
       const uint32_t q[4] = {a[0].x, a[0].y, a[0].z, a[0].w};
@@ -504,6 +516,7 @@ qd_status launch_q_gemv(const GemvArgs& a, cudaStream_t stream) {
     case QD_Q5_K: return launch_fmt<QD_Q5_K>(a.W, a.x, a.y, a.batch, a.mode, stream);
     case QD_Q6_K: return launch_fmt<QD_Q6_K>(a.W, a.x, a.y, a.batch, a.mode, stream);
     case QD_F16: return launch_fmt<QD_F16>(a.W, a.x, a.y, a.batch, a.mode, stream);
+    case QD_I4_ROW: return launch_fmt<QD_I4_ROW>(a.W, a.x, a.y, a.batch, a.mode, stream);
     default: return QD_ERR_UNSUPPORTED;
   }
 }

@@ -49,6 +49,7 @@ __host__ __device__ inline int64_t row_code_bytes(int fmt, int64_t cols) {
     case QD_Q5_K: return (cols / 256) * 160;  // qh, then low nibbles
     case QD_Q6_K: return (cols / 256) * 192;  // ql, then qh
     case QD_F16: return cols * 2;
+    case QD_I4_ROW: return cols / 2;
     default: return cols;  // QD_I8_ROW
   }
 }
@@ -79,11 +80,12 @@ inline bool shape_ok(int fmt, int64_t rows, int64_t cols) {
     case QD_Q5_K:
     case QD_Q6_K: return cols % 256 == 0;
     case QD_I8_ROW: return cols % 16 == 0;
+    case QD_I4_ROW: return cols % 32 == 0;
     default: return false;
   }
 }
 
-inline bool fmt_ok(int fmt) { return fmt >= QD_Q4_0 && fmt <= QD_F16; }
+inline bool fmt_ok(int fmt) { return fmt >= QD_Q4_0 && fmt <= QD_I4_ROW; }
 // The formats the decode step's fused kernels take.
 inline bool model_fmt_ok(int fmt) { return fmt >= QD_Q4_0 && fmt <= QD_I8_ROW; }
 
@@ -107,6 +109,7 @@ inline size_t src_bytes(int fmt, int64_t rows, int64_t cols) {
     case QD_Q5_K: return (size_t)rows * (cols / 256) * 176;
     case QD_Q6_K: return (size_t)rows * (cols / 256) * 210;
     case QD_F16: return (size_t)rows * cols * 2;
+    case QD_I4_ROW: return (size_t)rows * (cols / 2) + 4 * (size_t)rows;
     default: return (size_t)rows * cols + 4 * (size_t)rows;
   }
 }
@@ -235,6 +238,11 @@ __device__ __forceinline__ float dequant_elem(int fmt, const PackedView& W, int6
     return f16_bits_to_f32(hdr[16] | (hdr[17] << 8)) * (float)sc * (float)(q - 32);
   } else if (fmt == QD_F16) {
     return f16_bits_to_f32(code_row[2 * c] | (code_row[2 * c + 1] << 8));
+  } else if (fmt == QD_I4_ROW) {
+    const int nib = (code_row[c >> 1] >> (4 * (c & 1))) & 15;
+    float s;
+    memcpy(&s, sc_row, 4);
+    return s * (float)(nib >= 8 ? nib - 16 : nib);
   } else {
     float s;
     memcpy(&s, sc_row, 4);

@@ -77,7 +77,8 @@ __global__ void k_unpack_blocks(int fmt, const uint8_t* __restrict__ codes, cons
   }
 }
 
-// INT8 rows: codes copy 16 bytes per thread, scales one f32 per row.
+// INT8 / INT4 rows: `cols` code bytes per row (the INT4 row's cols / 2), copied 16 bytes per
+// thread, then one f32 scale per row.
 __global__ void k_repack_i8(const uint8_t* __restrict__ src, int64_t n_rows, int64_t cols,
                             uint8_t* __restrict__ codes, float* __restrict__ scales, int64_t dst_row0,
                             int64_t dst_step, int pair_hd) {
@@ -141,9 +142,10 @@ qd_status launch_repack_rows(int fmt, const void* src, int64_t n_rows, int64_t c
   PackedView v = packed_view(fmt, dst_base, dst_rows, cols);
   uint8_t* codes = const_cast<uint8_t*>(v.codes);
   uint8_t* scales = const_cast<uint8_t*>(v.scales);
-  if (fmt == QD_I8_ROW) {
-    const int64_t n = n_rows * (cols / 16);
-    k_repack_i8<<<grid_for(n, 256), 256, 0, stream>>>(static_cast<const uint8_t*>(src), n_rows, cols, codes,
+  if (fmt == QD_I8_ROW || fmt == QD_I4_ROW) {  // codes row by row, then one f32 scale per row
+    const int64_t rb = row_code_bytes(fmt, cols);
+    const int64_t n = n_rows * (rb / 16);
+    k_repack_i8<<<grid_for(n, 256), 256, 0, stream>>>(static_cast<const uint8_t*>(src), n_rows, rb, codes,
                                                        reinterpret_cast<float*>(scales), dst_row0, dst_row_step,
                                                        pair_hd);
   } else {
@@ -199,9 +201,10 @@ qd_status qd_unpack(qd_fmt fmt, const void* packed, int64_t rows, int64_t cols, 
   if (dst_bytes < src_bytes(fmt, rows, cols)) return QD_ERR_NOMEM;
   PackedView v = packed_view(fmt, packed, rows, cols);
   cudaStream_t s = (cudaStream_t)stream;
-  if (fmt == QD_I8_ROW) {
-    k_unpack_i8<<<grid_for(rows * cols, 256), 256, 0, s>>>(v.codes, reinterpret_cast<const float*>(v.scales), rows,
-                                                            cols, static_cast<uint8_t*>(dst));
+  if (fmt == QD_I8_ROW || fmt == QD_I4_ROW) {
+    const int64_t rb = row_code_bytes(fmt, cols);
+    k_unpack_i8<<<grid_for(rows * rb, 256), 256, 0, s>>>(v.codes, reinterpret_cast<const float*>(v.scales), rows, rb,
+                                                          static_cast<uint8_t*>(dst));
   } else {
     const int64_t nb = cols / geom(fmt).weights;
     k_unpack_blocks<<<grid_for(rows * nb, 256), 256, 0, s>>>(fmt, v.codes, v.scales, rows, nb,

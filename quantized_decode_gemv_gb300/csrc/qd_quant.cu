@@ -85,10 +85,66 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
   if (lane == 0) scales[r] = !finite ? __uint_as_float(0x7FC00000u) : (m16 == 0u ? 0.f : s);
 }
 
+// Per-row INT4 (the same rule with the 4-bit code range: s = max|w| / 7, codes w / s
+// rounded to nearest with ties away from zero, clamped to +-7): one warp per row; the codes
+// are two's-complement nibbles, element 2i in the low nibble of byte i.  The quotients are
+// IEEE round-to-nearest divisions, as the rule takes its decision in f32.
+__global__ void __launch_bounds__(kQuantWarps * 32) k_quantize_i4_rows(const uint16_t* __restrict__ w, int64_t rows,
+                                                                       int64_t cols, uint8_t* __restrict__ codes,
+                                                                       float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const uint16_t* wr = w + r * cols;
+  uint32_t mbits = 0;  // largest |w| as bf16 magnitude bits (monotonic for finite values)
+  bool finite = true;
+  for (int64_t c = lane; c < cols; c += 32) {
+    const uint32_t a = wr[c] & 0x7FFFu;
+    finite = finite && a < 0x7F80u;
+    mbits = max(mbits, a);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mbits = max(mbits, __shfl_xor_sync(0xffffffffu, mbits, off));
+  finite = __all_sync(0xffffffffu, finite);
+  uint8_t* qr = codes + r * (cols / 2);
+  const float m = __uint_as_float(mbits << 16);
+  if (!finite || m == 0.f) {
+    for (int64_t c = lane; c < cols / 2; c += 32) qr[c] = 0;
+    if (lane == 0) scales[r] = finite ? 0.f : __uint_as_float(0x7FC00000u);
+    return;
+  }
+  const float sc = __fdiv_rn(m, 7.0f);
+  for (int64_t c = lane; c < cols / 2; c += 32) {
+    int q[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float v = __uint_as_float((uint32_t)wr[2 * c + k] << 16);
+      q[k] = (int)fminf(fmaxf(roundf(__fdiv_rn(v, sc)), -7.0f), 7.0f);
+    }
+    qr[c] = (uint8_t)((q[0] & 0x0F) | ((q[1] & 0x0F) << 4));
+  }
+  if (lane == 0) scales[r] = sc;
+}
+
 }  // namespace
 }  // namespace qd
 
 using namespace qd;
+
+extern "C" qd_status qd_quantize_i4_rows(const uint16_t* w_bf16, int64_t rows, int64_t cols, void* out,
+                                         size_t out_bytes, qd_stream_t stream) {
+  if (!w_bf16 || !out) return QD_ERR_INVALID_ARG;
+  if (!shape_ok(QD_I4_ROW, rows, cols)) return QD_ERR_SHAPE;
+  if (!aligned16(w_bf16) || !aligned16(out)) return QD_ERR_ALIGN;
+  if (out_bytes < src_bytes(QD_I4_ROW, rows, cols)) return QD_ERR_NOMEM;
+  uint8_t* codes = static_cast<uint8_t*>(out);
+  float* scales = reinterpret_cast<float*>(codes + rows * (cols / 2));
+  const int64_t grid = (rows + kQuantWarps - 1) / kQuantWarps;
+  if (grid > 0x7FFFFFFF) return QD_ERR_SHAPE;
+  k_quantize_i4_rows<<<(unsigned)grid, kQuantWarps * 32, 0, (cudaStream_t)stream>>>(w_bf16, rows, cols, codes,
+                                                                                    scales);
+  return launch_status();
+}
 
 extern "C" qd_status qd_quantize_i8_rows(const uint16_t* w_bf16, int64_t rows, int64_t cols, void* out,
                                          size_t out_bytes, qd_stream_t stream) {

@@ -56,6 +56,7 @@ def test_status_strings(lib):
     ("q5_k", 2, 512, 2 * 2 * 176, 2 * 2 * 160 + 2 * 2 * 16),
     ("q6_k", 3, 256, 3 * 210, 3 * 192 + 64),
     ("f16", 3, 32, 3 * 32 * 2, 3 * 32 * 2),
+    ("i4", 3, 64, 3 * 32 + 12, 3 * 32 + 16),
 ])
 def test_layout_sizes(lib, fmt, rows, cols, src, packed):
     assert qd.src_bytes(fmt, rows, cols) == src
@@ -64,7 +65,7 @@ def test_layout_sizes(lib, fmt, rows, cols, src, packed):
 
 @pytest.mark.parametrize("fmt,rows,cols", [("q4_0", 4, 48), ("q8_0", 0, 64), ("q4_k", 2, 128), ("i8", 3, 40),
                                            ("q4_0", -1, 64), ("q4_1", 2, 48), ("q5_0", 2, 80), ("q5_k", 2, 384),
-                                           ("q6_k", 1, 128), ("f16", 2, 48)])
+                                           ("q6_k", 1, 128), ("f16", 2, 48), ("i4", 2, 48)])
 def test_layout_sizes_reject_bad_shapes(lib, fmt, rows, cols):
     assert qd.src_bytes(fmt, rows, cols) == 0
     assert qd.packed_bytes(fmt, rows, cols) == 0
@@ -73,7 +74,7 @@ def test_layout_sizes_reject_bad_shapes(lib, fmt, rows, cols):
 def test_gemv_validation_before_any_device_work(lib):
     good = 4096  # a fake 16-byte-aligned "device" address: never dereferenced on these paths
     f = lib.qd_q_gemv
-    assert f(9, good, 8, 64, good, good, 1, None, 0, None) == 4            # unknown format
+    assert f(99, good, 8, 64, good, good, 1, None, 0, None) == 4           # unknown format
     assert f(0, None, 8, 64, good, good, 1, None, 0, None) == 1            # null W
     assert f(0, good, 8, 64, good, good, 0, None, 0, None) == 2            # batch 0
     assert f(0, good, 8, 64, good, good, 17, None, 0, None) == 2           # batch > 16
@@ -84,7 +85,7 @@ def test_gemv_validation_before_any_device_work(lib):
     g = lib.qd_q_gemv_ex
     assert g(0, good, 8, 64, good, good, 1, 2, None) == 1                  # unknown flag bit
     assert g(0, good, 8, 48, good, good, 1, qd.GEMV_OVERLAP, None) == 2    # cols % 32
-    assert g(9, good, 8, 64, good, good, 1, 0, None) == 4                  # unknown format
+    assert g(99, good, 8, 64, good, good, 1, 0, None) == 4                 # unknown format
 
 
 def test_gemm_validation_before_any_device_work(lib):
@@ -97,7 +98,7 @@ def test_gemm_validation_before_any_device_work(lib):
     assert w(2, 300, 512, 80) == 0 and w(0, 300, 480, 80) == 0 and w(0, 300, 512, 0) == 0
     assert w(0, 300, 512, 65537) == 0
     assert f(2, good, 300, 512, good, good, 80, good, need, None) == 4      # Q4_K: no prefill kernel
-    assert f(9, good, 300, 512, good, good, 80, good, need, None) == 4      # unknown format
+    assert f(99, good, 300, 512, good, good, 80, good, need, None) == 4     # unknown format
     assert f(0, None, 300, 512, good, good, 80, good, need, None) == 1      # null W
     assert f(0, good, 300, 512, good, good, 80, None, need, None) == 1      # null workspace
     assert f(0, good, 300, 480, good, good, 80, good, need, None) == 2      # cols % 64

@@ -1,4 +1,5 @@
-"""GPU parity for the formats a Q4_K_M-class file mixes in (Q4_1, Q5_0, Q5_K, Q6_K, F16)
+"""GPU parity for the formats a Q4_K_M-class file mixes in (Q4_1, Q5_0, Q5_K, Q6_K, F16) and
+per-row INT4
 through the C ABI: the repack round trip and the dequantiser bit-exact against the oracle,
 the embedding row bit-exact, q_gemv within 1e-3 of max |oracle| per output vector at batch
 1-16 (several row tiles, ragged rows), and the 7B-like shapes at full size on sampled rows."""
@@ -12,10 +13,10 @@ from gpu_helpers import assert_close, dev, packed, weights
 
 pytestmark = pytest.mark.gpu
 
-NEW = ["q4_1", "q5_0", "q5_k", "q6_k", "f16"]
+NEW = ["q4_1", "q5_0", "q5_k", "q6_k", "f16", "i4"]
 SHAPES = {"q4_1": [(1, 32), (67, 1056), (130, 4128)], "q5_0": [(1, 32), (67, 1056), (33, 4128)],
           "q5_k": [(1, 256), (37, 2304), (19, 4352)], "q6_k": [(1, 256), (37, 2304), (19, 4352)],
-          "f16": [(1, 32), (67, 1056), (41, 4128)]}
+          "f16": [(1, 32), (67, 1056), (41, 4128)], "i4": [(1, 32), (67, 1056), (41, 4128)]}
 
 
 @pytest.mark.parametrize("fmt", NEW)

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import qdsynth
-from gpu_helpers import assert_close
+from gpu_helpers import assert_close, dev
 from test_oracle_quant import bf16, random_bf16
 
 pytestmark = pytest.mark.gpu
@@ -90,3 +90,24 @@ def test_quantize_full_1p7b_head_sampled_rows(qd):
     codes = out[: rows * cols].view(rows, cols)[torch.from_numpy(pick).cuda()].cpu().numpy().view(np.int8)
     scales = out[rows * cols:].view(torch.float32)[torch.from_numpy(pick).cuda()].cpu().numpy()
     assert np.array_equal(codes, oq) and np.array_equal(scales, os_)
+
+
+def test_quantize_i4_rows_bit_exact(qd):
+    """Per-row INT4 (s = max|w| / 7, codes rounded ties away, +-7): codes and scales bit-exact
+    against the oracle, including a zero row, a non-finite row and rows whose quotients sit
+    at the ties; the result feeds the INT4 q_gemv."""
+    rows, cols = 70, 1024
+    w = qdsynth.normal_f32(71, "i4q", rows * cols).reshape(rows, cols)
+    w[3] = 0.0
+    w[5, 17] = np.inf
+    w[8] = (np.arange(cols) % 15 - 7) * 0.5  # multiples of s / 2: the ties
+    wb = (w.view(np.uint32) >> 16).astype(np.uint16)
+    out = torch.zeros(qd.src_bytes("i4", rows, cols), dtype=torch.uint8, device="cuda")
+    qd.quantize_i4_rows(dev(wb.view(np.int16)), rows, cols, out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    codes, scales = oracle.quantize_i4_rows(wb, rows, cols)
+    assert np.array_equal(got[:rows * cols // 2], codes.reshape(-1))
+    gs = got[rows * cols // 2:].view(np.float32)
+    assert np.array_equal(np.isnan(gs), np.isnan(scales))
+    assert np.array_equal(gs[~np.isnan(gs)].view(np.uint32), scales[~np.isnan(scales)].view(np.uint32))
