@@ -364,6 +364,9 @@ size_t q8_buffer_bytes(int batch, int64_t cols, bool with_sum);
 qd_status launch_quantize_q8(const float* x, int batch, int64_t cols, bool with_sum, void* out, cudaStream_t stream);
 qd_status launch_q_gemv_q8(int fmt, const PackedView& W, const void* xq, int batch, float* y, int mode,
                            cudaStream_t stream);
+// RMSNorm (the same f32 values as launch_rmsnorm) quantised to Q8_0 into out in one kernel.
+qd_status launch_rmsnorm_q8(const float* x, const float* g, int n, float eps, int batch, void* out,
+                            cudaStream_t stream);
 
 qd_status launch_rmsnorm(const float* x, const float* g, float* out, int n, int batch, float eps,
                          cudaStream_t stream);

@@ -184,19 +184,17 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
     a.pdl = true;
     return a;
   };
-  // ggml-exact products (act_q8): the norm (into xn) when the product has one, the Q8_0
-  // quantisation of its input, then the integer product; launched without programmatic
+  // ggml-exact products (act_q8): the Q8_0 quantisation of the product's input (fused with
+  // the RMSNorm when it has one), then the integer product; launched without programmatic
   // dependence (they run once their predecessor has completed and never let their
   // successor start early).
   void* xq = m->s + L.xq;
   auto q8prod = [&](int fmt, PackedView W, const float* in, const float* gains, float* y,
                     GemvMode mode) -> qd_status {
-    if (gains) {
-      QD_TRY(launch_rmsnorm(in, gains, xn, (int)W.cols, batch, c.eps, st));
-      in = xn;
-      ++n;
-    }
-    QD_TRY(launch_quantize_q8(in, batch, W.cols, false, xq, st));
+    if (gains)  // the norm quantised as it is formed (the same f32 values as the norm kernel)
+      QD_TRY(launch_rmsnorm_q8(in, gains, (int)W.cols, c.eps, batch, xq, st));
+    else
+      QD_TRY(launch_quantize_q8(in, batch, W.cols, false, xq, st));
     QD_TRY(launch_q_gemv_q8(fmt, W, xq, batch, y, mode, st));
     n += 2;
     return QD_OK;

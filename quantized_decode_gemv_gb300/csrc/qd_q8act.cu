@@ -18,24 +18,18 @@ namespace {
 
 constexpr int kQ8Warps = 8;
 
-// One warp per block of 32 values (lane = value).
-__global__ void __launch_bounds__(kQ8Warps * 32) k_quantize_q8(const float* __restrict__ x, int64_t blocks,
-                                                                int8_t* __restrict__ q, __half* __restrict__ d,
-                                                                __half* __restrict__ s) {
-  const int lane = threadIdx.x & 31;
-  const int64_t b = (int64_t)blockIdx.x * kQ8Warps + (threadIdx.x >> 5);
-  if (b >= blocks) return;
-  const float v = __ldg(x + 32 * b + lane);
+// One block of 32 values (lane = value, whole warp): codes, d and s (s may be null).
+__device__ __forceinline__ void quantize_block(float v, int lane, int8_t* q, __half* d, __half* s) {
   const bool bad = __any_sync(0xffffffffu, !isfinite(v));
   float m = fabsf(v);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   if (bad || m == 0.f) {
-    q[32 * b + lane] = 0;
+    q[lane] = 0;
     if (lane == 0) {
       const __half z = bad ? __float2half_rn(__int_as_float(0x7FC00000)) : __float2half_rn(0.f);
-      d[b] = z;
-      if (s) s[b] = z;
+      *d = z;
+      if (s) *s = z;
     }
     return;
   }
@@ -43,13 +37,50 @@ __global__ void __launch_bounds__(kQ8Warps * 32) k_quantize_q8(const float* __re
   float t = roundf(__fdiv_rn(v, dd));
   t = fminf(fmaxf(t, -127.0f), 127.0f);
   const int qi = (int)t;
-  q[32 * b + lane] = (int8_t)qi;
+  q[lane] = (int8_t)qi;
   int sum = qi;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
   if (lane == 0) {
-    d[b] = __float2half_rn(dd);
-    if (s) s[b] = __float2half_rn(__fmul_rn(dd, (float)sum));
+    *d = __float2half_rn(dd);
+    if (s) *s = __float2half_rn(__fmul_rn(dd, (float)sum));
+  }
+}
+
+// One warp per block of 32 values.
+__global__ void __launch_bounds__(kQ8Warps * 32) k_quantize_q8(const float* __restrict__ x, int64_t blocks,
+                                                                int8_t* __restrict__ q, __half* __restrict__ d,
+                                                                __half* __restrict__ s) {
+  const int lane = threadIdx.x & 31;
+  const int64_t b = (int64_t)blockIdx.x * kQ8Warps + (threadIdx.x >> 5);
+  if (b >= blocks) return;
+  quantize_block(__ldg(x + 32 * b + lane), lane, q + 32 * b, d + b, s ? s + b : nullptr);
+}
+
+// RMSNorm of one row (one CTA per row, the same reduction and products as the RMSNorm
+// kernel, so the normalised values are the same f32 numbers) quantised to Q8_0 as it is
+// formed: out[b][i] = x[b][i] * g[i] / sqrt(mean(x^2) + eps), never stored as f32.
+__global__ void __launch_bounds__(512) k_rmsnorm_q8(const float* __restrict__ x, const float* __restrict__ g, int n,
+                                                    float eps, int8_t* __restrict__ q, __half* __restrict__ d) {
+  __shared__ float red[32];
+  const float* xr = x + (int64_t)blockIdx.x * n;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    v = warp_sum(v);
+    if (threadIdx.x == 0) red[0] = 1.0f / sqrtf(v / (float)n + eps);
+  }
+  __syncthreads();
+  const float scale = red[0];
+  const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int64_t row_blocks = n / 32, b0 = (int64_t)blockIdx.x * row_blocks;
+  for (int64_t k = threadIdx.x >> 5; k < row_blocks; k += nw) {
+    const int i = (int)(32 * k) + lane;
+    quantize_block(xr[i] * scale * g[i], lane, q + 32 * (b0 + k), d + b0 + k, nullptr);
   }
 }
 
@@ -214,6 +245,15 @@ qd_status launch_quantize_q8(const float* x, int batch, int64_t cols, bool with_
   k_quantize_q8<<<(unsigned)((blocks + kQ8Warps - 1) / kQ8Warps), kQ8Warps * 32, 0, stream>>>(
       x, blocks, reinterpret_cast<int8_t*>(base), reinterpret_cast<__half*>(base + q8_d_offset(batch, cols)),
       with_sum ? reinterpret_cast<__half*>(base + q8_s_offset(batch, cols)) : nullptr);
+  return launch_status();
+}
+
+qd_status launch_rmsnorm_q8(const float* x, const float* g, int n, float eps, int batch, void* out,
+                            cudaStream_t stream) {
+  uint8_t* base = static_cast<uint8_t*>(out);
+  const int threads = n >= 2048 ? 512 : 256;  // as the RMSNorm kernel: the same sums
+  k_rmsnorm_q8<<<batch, threads, 0, stream>>>(x, g, n, eps, reinterpret_cast<int8_t*>(base),
+                                              reinterpret_cast<__half*>(base + q8_d_offset(batch, n)));
   return launch_status();
 }
 
