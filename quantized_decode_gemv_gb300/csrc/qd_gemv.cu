@@ -98,6 +98,31 @@ struct Unit<QD_I8_ROW> {
   __device__ __forceinline__ static int64_t x_offset(int64_t u) { return u * 16; }
 };
 
+// ----------------------------------------------------------------- INT4 rows
+template <>
+struct Unit<QD_I4_ROW> {
+  static constexpr int kWeights = 32;
+  uint4 q;
+  __device__ __forceinline__ void load(const PackedView& W, int64_t r, int64_t u) {
+    q = ld_stream_v4(W.codes + r * W.row_code_bytes + u * 16);
+  }
+  // Element 2i is the low nibble of byte i, 2i + 1 the high one (two's complement): the
+  // nibble with its top bit flipped is q + 8 in 0..15, widened exactly by the magic number.
+  __device__ __forceinline__ void codes(float (&w)[32]) const {
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t lo = (words[t] & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((words[t] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        w[8 * t + 2 * k] = byte_as_magic(lo, k) - (kMagic + 8.0f);
+        w[8 * t + 2 * k + 1] = byte_as_magic(hi, k) - (kMagic + 8.0f);
+      }
+    }
+  }
+  __device__ __forceinline__ static int64_t x_offset(int64_t u) { return u * 32; }
+};
+
 template <int N>
 __device__ __forceinline__ float dot_x(const float (&w)[N], const float* __restrict__ xp) {
   const float4* x4 = reinterpret_cast<const float4*>(xp);
@@ -192,7 +217,7 @@ __global__ void __launch_bounds__(kThreads) k_gemv_blocks(PackedView W, const fl
 #pragma unroll
         for (int i = 0; i < R; ++i) {
           const float s = dot_x<KW>(w[i], xp);
-          if constexpr (FMT == QD_I8_ROW)
+          if constexpr (FMT == QD_I8_ROW || FMT == QD_I4_ROW)  // one scale per row, applied at the end
             acc[i][b] += s;
           else
             acc[i][b] = fmaf(cur[i].scale(), s, acc[i][b]);
@@ -206,7 +231,7 @@ __global__ void __launch_bounds__(kThreads) k_gemv_blocks(PackedView W, const fl
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     row_scale[i] = 1.0f;
-    if constexpr (FMT == QD_I8_ROW) {
+    if constexpr (FMT == QD_I8_ROW || FMT == QD_I4_ROW) {
       const int64_t r = row0 + i < W.rows ? row0 + i : row0;
       row_scale[i] = __ldg(reinterpret_cast<const float*>(W.scales) + r);
     }
@@ -295,7 +320,7 @@ __global__ void __launch_bounds__(kThreads) k_gemv_q4k(PackedView W, const float
   finish_rows<R, NB>(acc, row_scale, row0, W.rows, y, batch, mode, lane);
 }
 
-// The formats a Q4_K_M-class file mixes in (Q4_1, Q5_0, Q5_K, Q6_K, F16) and per-row INT4: the 32
+// The formats a Q4_K_M-class file mixes in (Q4_1, Q5_0, Q5_K, Q6_K, F16): the 32
 // dequantised f32 values of unit u (columns 32u .. 32u + 31) of row r, each rounded once
 // (as the test dequantiser).
 __device__ __forceinline__ float f16lo(uint32_t w) { return f16_bits_to_f32(w & 0xFFFFu); }
@@ -314,9 +339,6 @@ struct RawUnit {
     if constexpr (FMT == QD_F16) {
 #pragma unroll
       for (int t = 0; t < 4; ++t) a[t] = ld_stream_v4(cr + 64 * u + 16 * t);
-    } else if constexpr (FMT == QD_I4_ROW) {
-      a[0] = ld_stream_v4(cr + 16 * u);
-      s0 = __ldg(reinterpret_cast<const uint32_t*>(sr));  // the row scale (f32 bits)
     } else if constexpr (FMT == QD_Q4_1) {
       a[0] = ld_stream_v4(cr + 16 * u);
       s0 = __ldg(reinterpret_cast<const uint32_t*>(sr + 4 * u));
@@ -357,15 +379,6 @@ struct RawUnit {
           w[8 * t + 2 * k] = f16lo(h[k]);
           w[8 * t + 2 * k + 1] = f16hi(h[k]);
         }
-      }
-    } else if constexpr (FMT == QD_I4_ROW) {
-      // element 2i in the low nibble of byte i, two's complement
-      const uint32_t q[4] = {a[0].x, a[0].y, a[0].z, a[0].w};
-      const float sc = __uint_as_float(s0);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int nib = (int)((q[j >> 3] >> (4 * (j & 7))) & 15u);
-        w[j] = sc * (float)(nib >= 8 ? nib - 16 : nib);
       }
     } else if constexpr (FMT == QD_Q4_1 || FMT == QD_Q5_0) {
       const uint32_t q[4] = {a[0].x, a[0].y, a[0].z, a[0].w};
@@ -468,7 +481,7 @@ qd_status launch_t(const PackedView& W, const float* x, float* y, int batch, int
   const int64_t ctas = (warps + kWarpsPerCta - 1) / kWarpsPerCta;
   if constexpr (FMT == QD_Q4_K)
     k_gemv_q4k<R, NB><<<(unsigned)ctas, kThreads, 0, stream>>>(W, x, y, batch, mode);
-  else if constexpr (FMT >= QD_Q4_1)
+  else if constexpr (FMT >= QD_Q4_1 && FMT != QD_I4_ROW)
     k_gemv_deq<FMT, R, NB><<<(unsigned)ctas, kThreads, 0, stream>>>(W, x, y, batch, mode);
   else
     k_gemv_blocks<FMT, R, NB><<<(unsigned)ctas, kThreads, 0, stream>>>(W, x, y, batch, mode);
