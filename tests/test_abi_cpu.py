@@ -149,6 +149,12 @@ def test_other_entry_points_validate(lib):
     assert q(good + 2, 8, 64, good, 1 << 20, None) == 3                    # misaligned weights
     assert q(good, 8, 64, good + 4, 1 << 20, None) == 3                    # misaligned output
     assert q(good, 8, 64, good, 8 * 64 + 8 * 4 - 1, None) == 6             # output one byte short
+    q4 = lib.qd_quantize_i4_rows
+    assert q4(None, 8, 64, good, 1 << 20, None) == 1                       # null weights
+    assert q4(good, 8, 48, good, 1 << 20, None) == 2                       # INT4 rows need cols % 32
+    assert q4(good, 0, 64, good, 1 << 20, None) == 2                       # no rows
+    assert q4(good, 8, 64, good + 8, 1 << 20, None) == 3                   # misaligned output
+    assert q4(good, 8, 64, good, 8 * 32 + 8 * 4 - 1, None) == 6            # output one byte short
 
 
 def test_model_sizes_and_config_refusals(lib):
