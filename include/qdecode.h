@@ -147,7 +147,9 @@ qd_status qd_bf16_to_f32(const uint16_t* in, float* out, int64_t n, qd_stream_t 
 /*  Q6_K: (ql, qh) [rows][cols/256][192 B], then (16 scales, d)               */
 /*        [rows][cols/256][18 B].                                             */
 /*  F16:  weights [rows][cols] (2 B each); no scale region.                   */
-/*  I4_ROW: codes [rows][cols/2], then f32 scales [rows].                     */
+/*  I4_ROW: codes [rows][cols/32][16 B], each 32-element unit in Q4_0's order  */
+/*        (element j: low nibble of byte j, j+16: its high nibble) and in      */
+/*        offset binary (q + 8); then f32 scales [rows].                      */
 /* The repack is lossless: qd_unpack restores the source bytes exactly.       */
 /* ------------------------------------------------------------------------- */
 

@@ -106,17 +106,17 @@ struct Unit<QD_I4_ROW> {
   __device__ __forceinline__ void load(const PackedView& W, int64_t r, int64_t u) {
     q = ld_stream_v4(W.codes + r * W.row_code_bytes + u * 16);
   }
-  // Element 2i is the low nibble of byte i, 2i + 1 the high one (two's complement): the
-  // nibble with its top bit flipped is q + 8 in 0..15, widened exactly by the magic number.
+  // Packed as Q4_0 codes in offset binary: element j of the unit is the low nibble of
+  // code byte j, element j + 16 its high nibble, each q + 8 (exact through the magic number).
   __device__ __forceinline__ void codes(float (&w)[32]) const {
     const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const uint32_t lo = (words[t] & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((words[t] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+      const uint32_t lo = words[t] & 0x0F0F0F0Fu, hi = (words[t] >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        w[8 * t + 2 * k] = byte_as_magic(lo, k) - (kMagic + 8.0f);
-        w[8 * t + 2 * k + 1] = byte_as_magic(hi, k) - (kMagic + 8.0f);
+        w[4 * t + k] = byte_as_magic(lo, k) - (kMagic + 8.0f);
+        w[16 + 4 * t + k] = byte_as_magic(hi, k) - (kMagic + 8.0f);
       }
     }
   }

@@ -241,7 +241,7 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
 #pragma unroll
   for (int rr = 0; rr < RW; ++rr) {
     const uint8_t* cp = slot + (rr * 32 + lane) * CB;
-    if constexpr (FMT == QD_Q4_0 || FMT == QD_Q4_K) {
+    if constexpr (FMT == QD_Q4_0 || FMT == QD_Q4_K || FMT == QD_I4_ROW) {
       const uint4 q = *reinterpret_cast<const uint4*>(cp);
       const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -267,7 +267,7 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
       dq[rr] = f16_bits_to_f32(hdr.x & 0xFFFFu);
       dm[rr] = f16_bits_to_f32(hdr.x >> 16);
     } else {
-      dq[rr] = 1.f;  // INT8: the row scale multiplies the finished row sum
+      dq[rr] = 1.f;  // INT8 / INT4 rows: the row scale multiplies the finished row sum
     }
   }
 #pragma unroll
@@ -280,8 +280,9 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
     const float4 mt = *reinterpret_cast<const float4*>(rec + 96);
 #pragma unroll
     for (int rr = 0; rr < RW; ++rr) {
-      if constexpr (FMT == QD_Q4_0) {
-        // planes start at -8 * their element sums: sum (q - 8) xq, plane by plane
+      if constexpr (FMT == QD_Q4_0 || FMT == QD_I4_ROW) {
+        // planes start at -8 * their element sums: sum (q - 8) xq, plane by plane (INT4
+        // rows are packed as Q4_0 codes in offset binary, q + 8)
         const int h = plane_dot<false, true>(w[rr], hA, hB, __float_as_int(mt.y));
         const int m = plane_dot<false, false>(w[rr], mA, mB, __float_as_int(mt.z));
         const int l = plane_dot<false, false>(w[rr], lA, lB, __float_as_int(mt.w));
@@ -439,8 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
     const int u = lane + 32 * j;
     const uint8_t* slot = ring + (size_t)cs * SB;
     if (u < units) compute_step<FMT, NB, RW>(acc, slot, xq, units, u, lane, p.batch);
-    float rsc[RW];  // INT8 row scales (staged with every step)
-    if constexpr (FMT == QD_I8_ROW) {
+    float rsc[RW];  // INT8 / INT4 row scales (staged with every step)
+    if constexpr (FMT == QD_I8_ROW || FMT == QD_I4_ROW) {
 #pragma unroll
       for (int rr = 0; rr < RW; ++rr) rsc[rr] = *reinterpret_cast<const float*>(slot + slot_code_bytes<FMT, RW>() + rr * 64);
     }
@@ -450,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
 
     // ---- end of a group: reduce and write its RW rows
     const int64_t row0 = g * RW;
-    if constexpr (FMT == QD_I8_ROW) {
+    if constexpr (FMT == QD_I8_ROW || FMT == QD_I4_ROW) {
 #pragma unroll
       for (int rr = 0; rr < RW; ++rr)
 #pragma unroll
@@ -592,6 +593,7 @@ size_t smem_bytes(int fmt, int64_t cols, int nb) {
     QD_SMEM_CASE(QD_Q8_0)
     QD_SMEM_CASE(QD_Q4_K)
     QD_SMEM_CASE(QD_I8_ROW)
+    QD_SMEM_CASE(QD_I4_ROW)
 #undef QD_SMEM_CASE
     default: return ~(size_t)0;
   }
@@ -707,7 +709,7 @@ qd_status launch_inst(const Params& p, bool pdl, cudaStream_t stream) {
 int nb_for(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8; }
 
 bool supported(const GemvArgs& a) {
-  if (!model_fmt_ok(a.fmt)) return false;  // Q4_0, Q8_0, Q4_K, INT8 rows
+  if (!model_fmt_ok(a.fmt) && a.fmt != QD_I4_ROW) return false;  // Q4_0, Q8_0, Q4_K, INT8 / INT4 rows
   if (a.batch < 1 || a.batch > 8 || a.W.cols % 32) return false;
   if (a.W.cols > (1 << 24)) return false;
   if (smem_bytes(a.fmt, a.W.cols, nb_for(a.batch)) > kSmemCap) return false;
@@ -749,6 +751,7 @@ qd_status launch_q_gemv_stream(const GemvArgs& a, cudaStream_t stream) {
     case QD_Q8_0: QD_NB_SWITCH(QD_Q8_0)
     case QD_Q4_K: QD_NB_SWITCH(QD_Q4_K)
     case QD_I8_ROW: QD_NB_SWITCH(QD_I8_ROW)
+    case QD_I4_ROW: QD_NB_SWITCH(QD_I4_ROW)
     default: return QD_ERR_UNSUPPORTED;
   }
 #undef QD_NB_SWITCH

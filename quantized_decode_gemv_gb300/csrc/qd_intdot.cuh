@@ -55,9 +55,10 @@ constexpr int code_bytes() {
 
 // Shared-memory x records: per batch row and unit, 112 bytes in seven 16-byte chunks:
 // 0/1 the high bytes of halves A/B, 2/3 the middle bytes, 4/5 the low bytes, 6 the
-// unit's metadata: the scale s and, for Q4_0, -8 times each plane's element sum (the
-// code offset, as int bits); for Q4_K, sum x over A and over B.  The 7-chunk stride
-// puts 8 lanes reading one chunk of 8 consecutive units on 8 different bank groups.
+// unit's metadata: the scale s and, for Q4_0 (and INT4 rows, packed as Q4_0 codes), -8
+// times each plane's element sum (the code offset, as int bits); for Q4_K, sum x over A
+// and over B.  The 7-chunk stride puts 8 lanes reading one chunk of 8 consecutive units
+// on 8 different bank groups.
 constexpr int kRecBytes = 112;
 __device__ __forceinline__ int rec_off(int u, int k) { return u * kRecBytes + 16 * k; }
 
@@ -133,7 +134,7 @@ __device__ __forceinline__ void write_record(uint8_t* rec, int k, bool ok, float
     *reinterpret_cast<uint32_t*>(rec + 64 + off) = w0;
   }
   float4 meta = make_float4(sc, 0.f, 0.f, 0.f);
-  if constexpr (FMT == QD_Q4_0) {
+  if constexpr (FMT == QD_Q4_0 || FMT == QD_I4_ROW) {
     int s2 = (q0 >> 16) + (q1 >> 16) + (q2 >> 16) + (q3 >> 16);
     int s1 = ((q0 >> 8) & 255) + ((q1 >> 8) & 255) + ((q2 >> 8) & 255) + ((q3 >> 8) & 255);
     int s0 = (q0 & 255) + (q1 & 255) + (q2 & 255) + (q3 & 255);

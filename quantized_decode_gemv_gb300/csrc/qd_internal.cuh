@@ -238,11 +238,12 @@ __device__ __forceinline__ float dequant_elem(int fmt, const PackedView& W, int6
     return f16_bits_to_f32(hdr[16] | (hdr[17] << 8)) * (float)sc * (float)(q - 32);
   } else if (fmt == QD_F16) {
     return f16_bits_to_f32(code_row[2 * c] | (code_row[2 * c + 1] << 8));
-  } else if (fmt == QD_I4_ROW) {
-    const int nib = (code_row[c >> 1] >> (4 * (c & 1))) & 15;
+  } else if (fmt == QD_I4_ROW) {  // packed as Q4_0 codes in offset binary (q + 8)
+    const int j = (int)(c & 31);
+    const uint8_t byte = code_row[(c >> 5) * 16 + (j & 15)];
     float s;
     memcpy(&s, sc_row, 4);
-    return s * (float)(nib >= 8 ? nib - 16 : nib);
+    return s * (float)(((j < 16) ? (byte & 15) : (byte >> 4)) - 8);
   } else {
     float s;
     memcpy(&s, sc_row, 4);

@@ -77,8 +77,7 @@ __global__ void k_unpack_blocks(int fmt, const uint8_t* __restrict__ codes, cons
   }
 }
 
-// INT8 / INT4 rows: `cols` code bytes per row (the INT4 row's cols / 2), copied 16 bytes per
-// thread, then one f32 scale per row.
+// INT8 rows: codes copy 16 bytes per thread, scales one f32 per row.
 __global__ void k_repack_i8(const uint8_t* __restrict__ src, int64_t n_rows, int64_t cols,
                             uint8_t* __restrict__ codes, float* __restrict__ scales, int64_t dst_row0,
                             int64_t dst_step, int pair_hd) {
@@ -94,6 +93,51 @@ __global__ void k_repack_i8(const uint8_t* __restrict__ src, int64_t n_rows, int
       float v;
       memcpy(&v, src + n_rows * cols + 4 * i, 4);
       scales[r] = v;
+    }
+  }
+}
+
+// INT4 rows: the source holds element 2i in the low nibble of byte i (two's complement);
+// the packed codes hold each 32-element unit as Q4_0 orders it (element j in the low
+// nibble of byte j, element j + 16 in its high nibble) in offset binary (q + 8), which the
+// streaming GEMV's Q4_0 path reads.  One thread per (source row, unit).
+__device__ __forceinline__ int src_i4_nibble(const uint8_t* unit, int e) { return (unit[e >> 1] >> (4 * (e & 1))) & 15; }
+
+__global__ void k_repack_i4(const uint8_t* __restrict__ src, int64_t n_rows, int64_t cols, uint8_t* __restrict__ codes,
+                            float* __restrict__ scales, int64_t dst_row0, int64_t dst_step, int pair_hd) {
+  const int64_t units = cols / 32, total = n_rows * units;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = t / units, u = t % units;
+    const int64_t r = dst_row_of(i, dst_row0, dst_step, pair_hd);
+    const uint8_t* s = src + i * (cols / 2) + 16 * u;
+    uint8_t* d = codes + r * (cols / 2) + 16 * u;
+    for (int j = 0; j < 16; ++j)
+      d[j] = (uint8_t)((src_i4_nibble(s, j) ^ 8) | ((src_i4_nibble(s, j + 16) ^ 8) << 4));
+    if (u == 0) {
+      float v;
+      memcpy(&v, src + n_rows * (cols / 2) + 4 * i, 4);
+      scales[r] = v;
+    }
+  }
+}
+
+__global__ void k_unpack_i4(const uint8_t* __restrict__ codes, const float* __restrict__ scales, int64_t rows,
+                            int64_t cols, uint8_t* __restrict__ dst) {
+  const int64_t units = cols / 32, total = rows * units;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
+    const uint8_t* c = codes + 16 * t;  // unit u of row r = t / units, rows contiguous
+    uint8_t* d = dst + 16 * t;
+    for (int i = 0; i < 16; ++i) {  // source byte i: elements 2i, 2i + 1
+      int nib[2];
+      for (int h = 0; h < 2; ++h) {
+        const int e = 2 * i + h;
+        nib[h] = ((e < 16 ? c[e] : c[e - 16] >> 4) & 15) ^ 8;
+      }
+      d[i] = (uint8_t)(nib[0] | (nib[1] << 4));
+    }
+    if (t % units == 0) {
+      const float v = scales[t / units];
+      memcpy(dst + rows * (cols / 2) + 4 * (t / units), &v, 4);
     }
   }
 }
@@ -142,7 +186,11 @@ qd_status launch_repack_rows(int fmt, const void* src, int64_t n_rows, int64_t c
   PackedView v = packed_view(fmt, dst_base, dst_rows, cols);
   uint8_t* codes = const_cast<uint8_t*>(v.codes);
   uint8_t* scales = const_cast<uint8_t*>(v.scales);
-  if (fmt == QD_I8_ROW || fmt == QD_I4_ROW) {  // codes row by row, then one f32 scale per row
+  if (fmt == QD_I4_ROW) {
+    k_repack_i4<<<grid_for(n_rows * (cols / 32), 256), 256, 0, stream>>>(
+        static_cast<const uint8_t*>(src), n_rows, cols, codes, reinterpret_cast<float*>(scales), dst_row0,
+        dst_row_step, pair_hd);
+  } else if (fmt == QD_I8_ROW) {  // codes row by row, then one f32 scale per row
     const int64_t rb = row_code_bytes(fmt, cols);
     const int64_t n = n_rows * (rb / 16);
     k_repack_i8<<<grid_for(n, 256), 256, 0, stream>>>(static_cast<const uint8_t*>(src), n_rows, rb, codes,
@@ -201,10 +249,12 @@ qd_status qd_unpack(qd_fmt fmt, const void* packed, int64_t rows, int64_t cols, 
   if (dst_bytes < src_bytes(fmt, rows, cols)) return QD_ERR_NOMEM;
   PackedView v = packed_view(fmt, packed, rows, cols);
   cudaStream_t s = (cudaStream_t)stream;
-  if (fmt == QD_I8_ROW || fmt == QD_I4_ROW) {
-    const int64_t rb = row_code_bytes(fmt, cols);
-    k_unpack_i8<<<grid_for(rows * rb, 256), 256, 0, s>>>(v.codes, reinterpret_cast<const float*>(v.scales), rows, rb,
-                                                          static_cast<uint8_t*>(dst));
+  if (fmt == QD_I4_ROW) {
+    k_unpack_i4<<<grid_for(rows * (cols / 32), 256), 256, 0, s>>>(v.codes, reinterpret_cast<const float*>(v.scales),
+                                                                  rows, cols, static_cast<uint8_t*>(dst));
+  } else if (fmt == QD_I8_ROW) {
+    k_unpack_i8<<<grid_for(rows * cols, 256), 256, 0, s>>>(v.codes, reinterpret_cast<const float*>(v.scales), rows,
+                                                            cols, static_cast<uint8_t*>(dst));
   } else {
     const int64_t nb = cols / geom(fmt).weights;
     k_unpack_blocks<<<grid_for(rows * nb, 256), 256, 0, s>>>(fmt, v.codes, v.scales, rows, nb,
