@@ -1,7 +1,8 @@
 // Inline-PTX building blocks for the 5th-generation tensor-core kernels (tcgen05 MMAs with
 // f32 accumulators in tensor memory, shared-memory operand descriptors, mbarriers, bulk
 // copies).  Every mbarrier wait is bounded (kSpinLimit polls of mbarrier.test_wait, which
-// returns at once) and reports whether the phase completed.
+// returns at once, or kSleepLimit tries of mbarrier.try_wait, which may suspend the thread
+// for a while) and reports whether the phase completed.
 #pragma once
 
 #include <cuda_fp16.h>
