@@ -177,16 +177,21 @@ __device__ __forceinline__ void cp_wait() {
 
 // Per-warp staging ring in shared memory: stages<FMT, RW>() slots, one unit step each.
 // A slot holds, for the RW rows of the group, every lane's code chunk (lane-major, so
-// each lane reads back only what it copied) and then 64 bytes of scale data per row:
-// Q4_0/Q8_0 the 32 lanes' f16 scales, Q4_K the 4 super-block headers the 32 units
-// span, INT8 the row scale.
+// each lane reads back only what it copied) and then the scale data of each row: 64
+// bytes (Q4_0/Q8_0 the 32 lanes' f16 scales, Q4_K the 4 super-block headers the 32 units
+// span, INT8 / INT4 the row scale) or, for Q4_1, 128 (the 32 lanes' (d, m) pairs).
 template <int FMT, int RW>
 constexpr int slot_code_bytes() {
   return RW * 32 * code_bytes<FMT>();
 }
+// scale bytes per row of a slot: Q4_1 one (d, m) pair per lane's unit, the others 64
+template <int FMT>
+constexpr int slot_scale_bytes() {
+  return FMT == QD_Q4_1 ? 128 : 64;
+}
 template <int FMT, int RW>
 constexpr int slot_bytes() {
-  return slot_code_bytes<FMT, RW>() + RW * 64;
+  return slot_code_bytes<FMT, RW>() + RW * slot_scale_bytes<FMT>();
 }
 // Ring depth: every warp keeps about kInFlight bytes of codes in flight whatever the
 // rows per group (HBM latency times bandwidth over the SMs' warps wants several KB per
@@ -211,8 +216,10 @@ __device__ __forceinline__ void stage_step(uint32_t slot, const RowPtrs<RW>& rp,
     const uint32_t dst = slot + (uint32_t)(rr * 32 + lane) * CB;
 #pragma unroll
     for (int k = 0; k < CB / 16; ++k) cp16(dst + 16 * k, c + 16 * k);
-    const uint32_t sdst = slot + slot_code_bytes<FMT, RW>() + rr * 64;
-    if constexpr (FMT == QD_Q4_0 || FMT == QD_Q8_0) {
+    const uint32_t sdst = slot + slot_code_bytes<FMT, RW>() + rr * slot_scale_bytes<FMT>();
+    if constexpr (FMT == QD_Q4_1) {
+      cp4(sdst + 4 * lane, rp.s[rr] + 4 * (uint32_t)u);  // (d, m) of this lane's unit
+    } else if constexpr (FMT == QD_Q4_0 || FMT == QD_Q8_0) {
       if ((lane & 1) == 0) cp4(sdst + 2 * lane, rp.s[rr] + 2 * (uint32_t)u);  // d of units u, u+1
     } else if constexpr (FMT == QD_Q4_K) {
       if ((lane & 7) == 0) cp16(sdst + 2 * lane, rp.s[rr] + (uint32_t)(u >> 3) * 16u);  // header
@@ -241,7 +248,7 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
 #pragma unroll
   for (int rr = 0; rr < RW; ++rr) {
     const uint8_t* cp = slot + (rr * 32 + lane) * CB;
-    if constexpr (FMT == QD_Q4_0 || FMT == QD_Q4_K || FMT == QD_I4_ROW) {
+    if constexpr (FMT == QD_Q4_0 || FMT == QD_Q4_K || FMT == QD_I4_ROW || FMT == QD_Q4_1) {
       const uint4 q = *reinterpret_cast<const uint4*>(cp);
       const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -257,7 +264,11 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
     }
     dm[rr] = 0.f;
     s0[rr] = s1[rr] = m0[rr] = m1[rr] = 0;
-    if constexpr (FMT == QD_Q4_0 || FMT == QD_Q8_0) {
+    if constexpr (FMT == QD_Q4_1) {
+      const uint32_t dmv = *reinterpret_cast<const uint32_t*>(sc + rr * slot_scale_bytes<FMT>() + 4 * lane);
+      dq[rr] = f16_bits_to_f32(dmv & 0xFFFFu);
+      dm[rr] = f16_bits_to_f32(dmv >> 16);
+    } else if constexpr (FMT == QD_Q4_0 || FMT == QD_Q8_0) {
       dq[rr] = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sc + rr * 64 + 2 * lane));
     } else if constexpr (FMT == QD_Q4_K) {
       const uint4 hdr = *reinterpret_cast<const uint4*>(sc + rr * 64 + (lane >> 3) * 16);
@@ -287,6 +298,12 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
         const int m = plane_dot<false, false>(w[rr], mA, mB, __float_as_int(mt.z));
         const int l = plane_dot<false, false>(w[rr], lA, lB, __float_as_int(mt.w));
         acc.v[rr][b] = fmaf(dq[rr] * mt.x, planes_value(h, m, l), acc.v[rr][b]);
+      } else if constexpr (FMT == QD_Q4_1) {
+        // value d q + m: d sum q xq (plane by plane) + m sum x (the record's half sums)
+        const int h = plane_dot<false, true>(w[rr], hA, hB, 0);
+        const int m = plane_dot<false, false>(w[rr], mA, mB, 0);
+        const int l = plane_dot<false, false>(w[rr], lA, lB, 0);
+        acc.v[rr][b] = fmaf(dq[rr] * mt.x, planes_value(h, m, l), fmaf(dm[rr], mt.y + mt.z, acc.v[rr][b]));
       } else if constexpr (FMT == QD_Q4_K) {
         // value d sc q - dmin m, summed over halves A (sub-block 2c) and B (2c + 1)
         const float va = planes_value(half_dot<true>(w[rr], hA, 0), half_dot<false>(w[rr], mA, 0),
@@ -594,6 +611,7 @@ size_t smem_bytes(int fmt, int64_t cols, int nb) {
     QD_SMEM_CASE(QD_Q4_K)
     QD_SMEM_CASE(QD_I8_ROW)
     QD_SMEM_CASE(QD_I4_ROW)
+    QD_SMEM_CASE(QD_Q4_1)
 #undef QD_SMEM_CASE
     default: return ~(size_t)0;
   }
@@ -709,7 +727,7 @@ qd_status launch_inst(const Params& p, bool pdl, cudaStream_t stream) {
 int nb_for(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8; }
 
 bool supported(const GemvArgs& a) {
-  if (!model_fmt_ok(a.fmt) && a.fmt != QD_I4_ROW) return false;  // Q4_0, Q8_0, Q4_K, INT8 / INT4 rows
+  if (!model_fmt_ok(a.fmt) && a.fmt != QD_I4_ROW && a.fmt != QD_Q4_1) return false;  // + INT4 rows, Q4_1
   if (a.batch < 1 || a.batch > 8 || a.W.cols % 32) return false;
   if (a.W.cols > (1 << 24)) return false;
   if (smem_bytes(a.fmt, a.W.cols, nb_for(a.batch)) > kSmemCap) return false;
@@ -752,6 +770,7 @@ qd_status launch_q_gemv_stream(const GemvArgs& a, cudaStream_t stream) {
     case QD_Q4_K: QD_NB_SWITCH(QD_Q4_K)
     case QD_I8_ROW: QD_NB_SWITCH(QD_I8_ROW)
     case QD_I4_ROW: QD_NB_SWITCH(QD_I4_ROW)
+    case QD_Q4_1: QD_NB_SWITCH(QD_Q4_1)
     default: return QD_ERR_UNSUPPORTED;
   }
 #undef QD_NB_SWITCH

@@ -56,8 +56,8 @@ constexpr int code_bytes() {
 // Shared-memory x records: per batch row and unit, 112 bytes in seven 16-byte chunks:
 // 0/1 the high bytes of halves A/B, 2/3 the middle bytes, 4/5 the low bytes, 6 the
 // unit's metadata: the scale s and, for Q4_0 (and INT4 rows, packed as Q4_0 codes), -8
-// times each plane's element sum (the code offset, as int bits); for Q4_K, sum x over A
-// and over B.  The 7-chunk stride puts 8 lanes reading one chunk of 8 consecutive units
+// times each plane's element sum (the code offset, as int bits); for Q4_K and Q4_1, sum x
+// over A and over B.  The 7-chunk stride puts 8 lanes reading one chunk of 8 consecutive units
 // on 8 different bank groups.
 constexpr int kRecBytes = 112;
 __device__ __forceinline__ int rec_off(int u, int k) { return u * kRecBytes + 16 * k; }
@@ -145,7 +145,7 @@ __device__ __forceinline__ void write_record(uint8_t* rec, int k, bool ok, float
       s0 += __shfl_xor_sync(0xffffffffu, s0, o);
     }
     meta = make_float4(sc, __int_as_float(-8 * s2), __int_as_float(-8 * s1), __int_as_float(-8 * s0));
-  } else if constexpr (FMT == QD_Q4_K) {
+  } else if constexpr (FMT == QD_Q4_K || FMT == QD_Q4_1) {
     float sv = (v.x + v.y) + (v.z + v.w);
     sv += __shfl_xor_sync(0xffffffffu, sv, 1);
     sv += __shfl_xor_sync(0xffffffffu, sv, 2);  // lanes 0-3: sum over A, 4-7: over B
