@@ -13,6 +13,11 @@
 // pass over the same chunks (now in L1) that writes 8 codes per lane and chunk; codes are
 // computed from a reciprocal multiply, with the division kept for near-ties (code_byte).  HBM
 // traffic: 2 bytes read and 1 byte written per weight, 4 bytes per row.
+//
+// Per-row INT4 ("Quantization" names symmetric per-channel INT8 and INT4 with one scale per
+// output row): the same rule with the 4-bit range, s_r = max |w| / 7, codes clamped to
+// [-7, 7], written as the INT4 source layout (two's-complement nibbles, element 2i in the
+// low nibble of byte i, then f32 scales [rows]).
 #include "qd_internal.cuh"
 
 namespace qd {
