@@ -14,7 +14,9 @@
 // 2^23 and 2^23 is subtracted), then streams x once per batch column and applies
 // the unit's scale to the unit's partial sum.  Block scales therefore multiply a
 // 32-term partial sum rather than every weight; the per-row f32 sums are reduced
-// across the warp with shuffles at the end.
+// across the warp with shuffles at the end.  (Per-row INT4 takes the same path with
+// 32-weight units; Q4_1, Q5_0, Q5_K, Q6_K and F16 units are decoded to f32 values by
+// k_gemv_deq.)
 #include "qd_internal.cuh"
 
 namespace qd {
