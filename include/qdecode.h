@@ -11,14 +11,18 @@
  *               residual stream", 10 "Loading weights", 11 "Prefill and decode",
  *               12 "The KV cache".
  *   [go-llm]    "llm" Go package documentation (go-wasmcontainers/llm v0.1.0):
- *               "Design points", "Oracle tolerances", index (Argmax, F16ToF32,
- *               CPU.Forward, CPU.Reset, CPU.Pos, Config).
+ *               package overview, "Design points", "Oracle tolerances", index
+ *               (Argmax, F16ToF32, RoundF16, type CPU and ExactGGML, CPU.Forward,
+ *               CPU.Reset, CPU.Pos, Config).
  *   [llamini]   "Building llamini.cpp: a from-scratch llama.cpp core in C99",
- *               "What I reimplemented" (Q4_K scale/min unpacking).
+ *               summary table ("Quants"), "What I reimplemented" (Q4_K
+ *               scale/min unpacking), "Optimizing for CPU, and finding out what
+ *               was actually true".
  *   [dasLLAMA]  "dasLLAMA-00 - The Problem Statement", 8.7.1.4 "Five small
  *               functions", 8.7.1.6.2 "Attention", 8.7.1.6.3 "Feed-forward",
  *               8.7.1.6.4 "Logits", 8.7.1.7 "Prompting is repeated forward".
- *   [minillm]   minillm-cpp README, "Loader", "NEON kernels", "Quantization".
+ *   [minillm]   minillm-cpp README, "Loader", "Direct INT8 loading", "NEON
+ *               kernels", "Quantization".
  *
  * Conventions for every entry point:
  *  - Device pointers unless stated "host".  The caller owns and allocates every
@@ -243,8 +247,9 @@ qd_status qd_q_gemm(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const
 /* ------------------------------------------------------------------------- */
 /* ggml-exact activations ([go-llm] type CPU, "ExactGGML": activations are     */
 /* quantised to Q8_0, Q8_1 for Q4_1 weights, before every quantised product)  */
-/* and the product over them in integers ([llamini] "What I reimplemented":   */
-/* ggml multiplies packed bytes and converts only the scaled sum to float).   */
+/* and the product over them in integers ([llamini] "Optimizing for CPU, and  */
+/* finding out what was actually true": ggml multiplies packed bytes and      */
+/* converts only the scaled sum to float).                                     */
 /* Quantisation (the page prints no rule), per 32 values of a row of x:       */
 /* d = max|x| / 127 and q = x / d rounded to nearest, ties away from zero,    */
 /* clamped to +-127, both divisions IEEE round-to-nearest in f32; d is kept   */

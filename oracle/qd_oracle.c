@@ -606,8 +606,8 @@ int or_quantize_q8(const float* x, int64_t n, int8_t* q, float* d16, float* s16)
 }
 
 /* The product over quantised activations, in the block's own integers ([llamini]
- * "What I reimplemented": ggml's dot products multiply the packed bytes directly and
- * convert to float only for the scaled sum): y[b][r] = sum over blocks k of row r of
+ * "Optimizing for CPU, and finding out what was actually true": ggml's dot products
+ * multiply the packed bytes directly and convert to float only for the scaled sum): y[b][r] = sum over blocks k of row r of
  *   Q8_0: d_w d_x sum_j q_w q_x;   Q4_0: d_w d_x sum_j (q_w - 8) q_x;
  *   Q4_1: d_w d_x sum_j q_w q_x + m_w s_x,
  * with x's binary16 d and s; accumulated in double. */

@@ -1,7 +1,8 @@
 // ggml-exact activations (go-llm type CPU, "ExactGGML": activations are quantised to Q8_0,
 // Q8_1 for Q4_1 weights, before every quantised matrix product) and the product over them
-// in the blocks' own integers (llamini, "What I reimplemented": ggml multiplies the packed
-// bytes and converts to float only for the scaled sum).
+// in the blocks' own integers (llamini, "Optimizing for CPU, and finding out what was
+// actually true": ggml multiplies the packed bytes and converts to float only for the
+// scaled sum).
 //
 // Quantisation, per 32 values of a row of x: d = max|x| / 127, q = x / d rounded to nearest
 // with ties away from zero, clamped to +-127 (both divisions IEEE round-to-nearest in f32);
