@@ -99,3 +99,19 @@ def test_decode_step_ggml_exact_mode_close_to_f32():
         out[exact] = lg
     diff = np.abs(out[True] - out[False]).max() / np.abs(out[False]).max()
     assert 0 < diff < 2e-2
+
+
+def test_quantize_error_bound_and_extreme_code():
+    """Every value lies within half a step of its code times the f32 scale m / 127 (the
+    binary16 d differs from it by at most 2^-11 relative, times |q| <= 127), and each
+    block's largest |x| takes the code +-127."""
+    x = qdsynth.activations(13, "q8bound", 4, 4096)
+    q, d, _ = oracle.quantize_q8(x)
+    xb = x.reshape(4, -1, 32).astype(np.float64)
+    qb = q.reshape(4, -1, 32).astype(np.float64)
+    m = np.abs(xb).max(axis=2, keepdims=True)
+    step = (m.astype(np.float32) / np.float32(127)).astype(np.float64)
+    assert (np.abs(xb - qb * step) <= step * (0.5 + 1e-5)).all()
+    d16 = d.reshape(4, -1, 1).astype(np.float64)
+    assert (np.abs(d16 - step) <= step * 2.0 ** -11).all()
+    assert (np.abs(qb).max(axis=2) == 127).all()
