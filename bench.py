@@ -349,6 +349,10 @@ def run_ours(args, world, rank, local):
             out["decode_1p7b"].update(bench_1p7b(qd, torch, stream, args, hbm, kv_f16=True))
         if world == 1:
             out["cpu_baseline"] = cpu_baseline(cfg, seconds=args.cpu_seconds)
+            try:  # an auxiliary host measurement: a failure is recorded, not fatal to the line
+                out["cpu_baseline_1p7b"] = cpu_baseline_1p7b()
+            except Exception as e:  # noqa: BLE001
+                out["cpu_baseline_1p7b"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0:
         print(json.dumps(out))
     if world > 1:
@@ -580,6 +584,41 @@ def cpu_baseline(cfg, seconds=15.0, max_tokens=64):
                       f"{dt:.1f} s; oracle C code, double accumulation, OpenMP over matrix rows",
             "single_thread": {"value": round(n1 / dt1, 3), "unit": "tokens/s", "cores": 1,
                               "sample": f"first {n1} tokens, {dt1:.1f} s"}}
+
+
+def cpu_baseline_1p7b():
+    """The oracle on the host cores at the 1.7B shape, context 4096 (one step at position
+    4095 over a 4095-entry N(0,1) cache): one step on all cores and on one core, and a
+    batch-16 step as 16 sequences' steps one after another (the oracle takes one sequence
+    per call; the 16 calls share one cache here, which changes no arithmetic)."""
+    import oracle
+    import qdsynth
+
+    cfg = qdsynth.SMOL_1_7B
+    ctx = 4096
+    host = qdsynth.model_tensors(cfg, 0)
+    om = oracle.Model(dict(cfg, max_ctx=ctx), host)
+    L, hk, hd = cfg["layers"], cfg["n_kv_heads"], cfg["head_dim"]
+    n = L * hk * ctx * hd
+    kc = qdsynth.normal_f32(0, "c5.kc", n)
+    vc = qdsynth.normal_f32(0, "c5.vc", n)
+    toks = qdsynth.tokens(0, "c5.tokens", 16, cfg["vocab"])
+
+    def steps(threads, count):
+        cores = oracle.set_threads(threads)
+        t0 = time.perf_counter()
+        for i in range(count):
+            om.decode_step(kc, vc, hk * ctx * hd, ctx - 1, int(toks[i]))
+        return time.perf_counter() - t0, cores
+
+    t_all, cores = steps(os.cpu_count() or 1, 1)
+    t_one, _ = steps(1, 1)
+    t_b16, _ = steps(os.cpu_count() or 1, 16)
+    return {"kind": "oracle", "cores": cores, "unit": "ms/step",
+            "batch1": round(t_all * 1e3, 1), "batch1_single_thread": round(t_one * 1e3, 1),
+            "batch16": round(t_b16 * 1e3, 1), "batch16_tokens/s": round(16 / t_b16, 2),
+            "sample": "one step at position 4095 per sequence (context 4096), INT8 1.7B shape; batch 16 as "
+                      "16 one-sequence calls sharing one cache; oracle C code, double accumulation"}
 
 
 # ----------------------------------------------------------------------------- reference arm
