@@ -377,7 +377,10 @@ typedef struct {
 typedef struct qd_model qd_model;
 
 /* Bytes of the caller-provided regions: packed weights, and state (KV cache,
- * activations, positions, error word, rope table).  0 for an invalid config. */
+ * activations, positions, error word, rope table; the flat-split attention's partials
+ * and counters when the model takes it; the quantised-activation buffer with act_q8).
+ * 0 for an invalid config (including act_q8 with formats other than Q4_0 / Q8_0, and
+ * the formats the decode step does not take). */
 size_t qd_model_weight_bytes(const qd_config* cfg);
 size_t qd_model_state_bytes(const qd_config* cfg);
 
