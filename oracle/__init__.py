@@ -102,6 +102,17 @@ def _L():
         lib.or_decode_step.argtypes = [ctypes.POINTER(_Config), p, p, p, i64, i32, i32, p,
                                        ctypes.POINTER(ctypes.c_int64)]
         lib.or_decode_step.restype = i32
+        lib.or_decode_step_tf.argtypes = [ctypes.POINTER(_Config), p, p, p, i64, i32, i32, p,
+                                          ctypes.POINTER(ctypes.c_int64), i32, p, p]
+        lib.or_decode_step_tf.restype = i32
+        lib.or_gemv_xd.argtypes = [i32, p, i64, i64, p, i32, i64, i64, p]
+        lib.or_gemv_xd.restype = i32
+        lib.or_rmsnorm_d.argtypes = [p, p, i32, d, p]
+        lib.or_rmsnorm_d.restype = None
+        lib.or_rope_head_d.argtypes = [p, i32, i32, i32, d]
+        lib.or_rope_head_d.restype = None
+        lib.or_attention_d.argtypes = [p, p, p, i32, i32, i32, i32, i64, p]
+        lib.or_attention_d.restype = None
         _lib = lib
     return _lib
 
@@ -164,6 +175,52 @@ def gemv(fmt: str, w, rows: int, cols: int, x, row0: int = 0, nrows: int | None 
     if rc:
         raise ValueError(f"or_gemv rc={rc}")
     return y
+
+
+def gemv_xd(fmt: str, w, rows: int, cols: int, x) -> np.ndarray:
+    """The product over double activations x float64 [batch][cols] (the decode step's own
+    intermediate vectors are double): y float64 [batch][rows]."""
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float64)
+    batch = x.shape[0]
+    assert x.shape[1] == cols
+    w, wp = _c(w, np.uint8)
+    y = np.empty((batch, rows), dtype=np.float64)
+    rc = _L().or_gemv_xd(FMT[fmt], wp, rows, cols, x.ctypes.data, batch, 0, rows, y.ctypes.data)
+    if rc:
+        raise ValueError(f"or_gemv_xd rc={rc}")
+    return y
+
+
+def rmsnorm_d(x, g, eps: float) -> np.ndarray:
+    """RMSNorm of one double vector (the step's own form): float64 [n]."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    g, gp = _c(g, np.float32)
+    assert g.size == x.size
+    out = np.empty(x.size, dtype=np.float64)
+    _L().or_rmsnorm_d(x.ctypes.data, gp, x.size, eps, out.ctypes.data)
+    return out
+
+
+def rope_d(v, n_heads: int, head_dim: int, pos: int, pairing: str, theta: float) -> np.ndarray:
+    """RoPE of n_heads heads of a double vector (the step's own form): a rotated copy."""
+    out = np.array(v, dtype=np.float64, copy=True)
+    assert out.size == n_heads * head_dim and head_dim % 2 == 0 and pos >= 0
+    for h in range(n_heads):
+        _L().or_rope_head_d(out.ctypes.data + 8 * h * head_dim, head_dim, pos, PAIRING[pairing], theta)
+    return out
+
+
+def attention_d(q, k_cache, v_cache, n_heads: int, n_kv_heads: int, head_dim: int, n_pos: int,
+                max_ctx: int) -> np.ndarray:
+    """attention() over a double q (the step's own form)."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k_cache, kp = _c(k_cache, np.float32)
+    v_cache, vp = _c(v_cache, np.float32)
+    assert q.size == n_heads * head_dim and n_heads % n_kv_heads == 0 and 0 < n_pos <= max_ctx
+    assert k_cache.size >= n_kv_heads * max_ctx * head_dim and v_cache.size >= n_kv_heads * max_ctx * head_dim
+    out = np.empty(n_heads * head_dim, dtype=np.float64)
+    _L().or_attention_d(q.ctypes.data, kp, vp, n_heads, n_kv_heads, head_dim, n_pos, max_ctx, out.ctypes.data)
+    return out
 
 
 def rmsnorm(x, g, eps: float) -> np.ndarray:
@@ -325,6 +382,29 @@ class Model:
         if rc:
             raise ValueError(f"or_decode_step rc={rc}")
         return logits, int(nxt.value)
+
+
+    def decode_step_tf(self, k_cache: np.ndarray, v_cache: np.ndarray, layer_stride: int, pos: int, token: int,
+                       kv_given: bool, seq_offset: int = 0):
+        """The step with the teacher-forcing hooks of or_decode_step_tf: with ``kv_given`` the
+        caches already hold this step's k and v at ``pos`` (another implementation's values)
+        and are not written.  Returns (logits f64[vocab], argmax, kv f32 [layers][2][n_kv*hd]
+        as formed before any binary16 rounding, head input f32 [dim])."""
+        assert k_cache.dtype == np.float32 and v_cache.dtype == np.float32
+        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        c = self.cfg
+        kd = c["n_kv_heads"] * c["head_dim"]
+        logits = np.empty(c["vocab"], dtype=np.float64)
+        kv = np.empty((c["layers"], 2, kd), dtype=np.float32)
+        hx = np.empty(c["dim"], dtype=np.float32)
+        nxt = ctypes.c_int64()
+        rc = _L().or_decode_step_tf(ctypes.byref(self._c), self._ptrs, k_cache.ctypes.data + 4 * seq_offset,
+                                    v_cache.ctypes.data + 4 * seq_offset, layer_stride, pos, token,
+                                    logits.ctypes.data, ctypes.byref(nxt), 1 if kv_given else 0, kv.ctypes.data,
+                                    hx.ctypes.data)
+        if rc:
+            raise ValueError(f"or_decode_step_tf rc={rc}")
+        return logits, int(nxt.value), kv, hx
 
 
 def set_threads(n: int) -> int:

@@ -337,6 +337,15 @@ static void gemv_rows_d(int fmt, const uint8_t* w, int64_t rows, int64_t cols, c
 
 /* Public GEMV over f32 activations: x[batch][cols] (f32), y[batch][nrows]
  * (double) for rows [row0, row0+nrows). */
+/* The same product over double activations x[batch][cols] (the decode step's own
+ * intermediate vectors are double). */
+int or_gemv_xd(int fmt, const uint8_t* w, int64_t rows, int64_t cols, const double* x, int batch, int64_t row0,
+               int64_t nrows, double* y) {
+    if (!or_shape_ok(fmt, rows, cols) || batch <= 0 || row0 < 0 || nrows < 0 || row0 + nrows > rows) return -1;
+    gemv_rows_d(fmt, w, rows, cols, x, batch, cols, y, nrows, row0, nrows);
+    return 0;
+}
+
 int or_gemv(int fmt, const uint8_t* w, int64_t rows, int64_t cols, const float* x, int batch, int64_t row0,
             int64_t nrows, double* y) {
     if (!or_shape_ok(fmt, rows, cols) || batch <= 0 || row0 < 0 || nrows < 0 || row0 + nrows > rows) return -1;
@@ -725,8 +734,17 @@ static int product(const or_config* c, int fmt, const uint8_t* w, int64_t rows, 
     return rc;
 }
 
-int or_decode_step(const or_config* c, const void* const* tensors, float* k_cache, float* v_cache,
-                   int64_t layer_stride, int pos, int token, double* logits, int64_t* next_token) {
+/* The step with two test hooks for teacher forcing against another implementation; the
+ * arithmetic is the step's own.
+ *   kv_given = 1: the cache already holds this step's k and v at pos (the other
+ *     implementation's values); the step attends over the cache as it is and does not
+ *     write it.
+ *   kv_out (or NULL): receives the k and v the step formed, rounded to f32 but before any
+ *     binary16 rounding, as [layer][2][n_kv_heads * head_dim] (k, then v).
+ *   head_x (or NULL): receives the head's input, the final normed x rounded to f32. */
+int or_decode_step_tf(const or_config* c, const void* const* tensors, float* k_cache, float* v_cache,
+                      int64_t layer_stride, int pos, int token, double* logits, int64_t* next_token, int kv_given,
+                      float* kv_out, float* head_x) {
     if (!c || pos < 0 || pos >= c->max_ctx || token < 0 || token >= c->vocab) return -1;
     if (c->n_heads % c->n_kv_heads) return -1;
     const int D = c->dim, F = c->ffn, hd = c->head_dim, hq = c->n_heads, hk = c->n_kv_heads;
@@ -765,12 +783,18 @@ int or_decode_step(const or_config* c, const void* const* tensors, float* k_cach
         for (int h = 0; h < hk; ++h)
             for (int i = 0; i < hd; ++i) {
                 float kf = (float)k[h * hd + i], vf = (float)v[h * hd + i];
+                if (kv_out) {
+                    kv_out[(int64_t)l * 2 * KD + h * hd + i] = kf;
+                    kv_out[(int64_t)l * 2 * KD + KD + h * hd + i] = vf;
+                }
                 if (c->kv_f16) {
                     kf = or_round_f16(kf);
                     vf = or_round_f16(vf);
                 }
-                kl[((int64_t)h * c->max_ctx + pos) * hd + i] = kf;
-                vl[((int64_t)h * c->max_ctx + pos) * hd + i] = vf;
+                if (!kv_given) {
+                    kl[((int64_t)h * c->max_ctx + pos) * hd + i] = kf;
+                    vl[((int64_t)h * c->max_ctx + pos) * hd + i] = vf;
+                }
             }
         or_attention_d(q, kl, vl, hq, hk, hd, pos + 1, c->max_ctx, att);
         if ((rc = product(c, c->w_fmt, (const uint8_t*)L[4], D, QD, att, t))) goto done;
@@ -785,6 +809,8 @@ int or_decode_step(const or_config* c, const void* const* tensors, float* k_cach
         for (int i = 0; i < D; ++i) x[i] += t[i];
     }
     or_rmsnorm_d(x, (const float*)tensors[1], D, c->eps, xn);
+    if (head_x)
+        for (int i = 0; i < D; ++i) head_x[i] = (float)xn[i];
     {
         const uint8_t* head = (const uint8_t*)(tensors[2] ? tensors[2] : tensors[0]);
         if ((rc = product(c, c->emb_fmt, head, c->vocab, D, xn, logits))) goto done;
@@ -793,6 +819,12 @@ int or_decode_step(const or_config* c, const void* const* tensors, float* k_cach
 done:
     free(x); free(xn); free(q); free(k); free(v); free(att); free(t); free(g); free(u); free(erow);
     return rc;
+}
+
+int or_decode_step(const or_config* c, const void* const* tensors, float* k_cache, float* v_cache,
+                   int64_t layer_stride, int pos, int token, double* logits, int64_t* next_token) {
+    return or_decode_step_tf(c, tensors, k_cache, v_cache, layer_stride, pos, token, logits, next_token, 0, NULL,
+                             NULL);
 }
 
 int or_abi_version(void) { return 1; }

@@ -358,3 +358,30 @@ def test_argmax_first_index_on_ties():
     assert oracle.argmax(np.array([-5.0, -1.0, -1.0], np.float64)) == 1
     x = qdsynth.activations(9, "l", 1, 49152)[0]
     assert oracle.argmax(x) == int(np.argmax(x))  # numpy also returns the first maximum
+
+
+def test_double_input_forms_equal_their_f32_forms():
+    """The decode step's double-input forms of the product, RMSNorm, RoPE and attention (the
+    forms the step composes) give the same bits as the pinned f32-input forms above when the
+    double input holds f32 values, and differ when it does not (they read all 53 bits)."""
+    rows, cols = 40, 128
+    w = qdsynth.weight_src("q4_0", 31, "dform.w", rows, cols)
+    x = qdsynth.activations(31, "dform.x", 2, cols)
+    assert np.array_equal(oracle.gemv_xd("q4_0", w, rows, cols, x.astype(np.float64)),
+                          oracle.gemv("q4_0", w, rows, cols, x))
+    g = qdsynth.uniform_f32(31, "dform.g", cols, 0.9, 1.1)
+    assert np.array_equal(oracle.rmsnorm_d(x[0].astype(np.float64), g, 1e-5), oracle.rmsnorm(x[0], g, 1e-5)[0])
+    hd = 64
+    v = x.reshape(-1)[:2 * hd]
+    for pairing in ("adjacent", "half"):
+        assert np.array_equal(oracle.rope_d(v.astype(np.float64), 2, hd, 7, pairing, 1e4),
+                              oracle.rope(v, 2, hd, 7, pairing, 1e4))
+    ctx = 8
+    kc = qdsynth.normal_f32(31, "dform.k", 2 * ctx * hd)
+    vc = qdsynth.normal_f32(31, "dform.v", 2 * ctx * hd)
+    q = qdsynth.normal_f32(31, "dform.q", 4 * hd)
+    assert np.array_equal(oracle.attention_d(q.astype(np.float64), kc, vc, 4, 2, hd, 5, ctx),
+                          oracle.attention(q, kc, vc, 4, 2, hd, 5, ctx))
+    # a double input off the f32 grid changes the result: nothing rounds it to f32 first
+    xd = x[0].astype(np.float64) * (1.0 + 2.0 ** -40)
+    assert not np.array_equal(oracle.gemv_xd("q4_0", w, rows, cols, xd), oracle.gemv("q4_0", w, rows, cols, x[0]))
