@@ -104,13 +104,23 @@ class ClockSampler:
          "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+        # nvidia-smi numbers GPUs physically; under CUDA_VISIBLE_DEVICES the torch index can
+        # name another GPU, so query by the device's UUID (read-only, as before)
+        self.gpu = str(gpu_index)
+        try:
+            import torch
+
+            uuid = str(torch.cuda.get_device_properties(gpu_index).uuid)
+            if uuid:
+                self.gpu = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
         self.proc = None
         self.lines = []
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
@@ -451,13 +461,15 @@ def gemv_sweep(qd, torch, stream, hbm, args):
         shapes.append(("q4_k", r, c))
     for r, c in [(6144, 2048), (2048, 2048), (16384, 2048), (2048, 8192), (49152, 2048)]:
         shapes.append(("i8", r, c))
-    batches = (1, 2, 4, 8) if args.full_sweep else (1,)
+    batches = (1,) if args.batch1_sweep else (1, 2, 4, 8)
     for fmt, r, c in shapes:
         bs = (1, 16) if fmt == "i8" else (batches if fmt != "q4_k" and (r, c) != (576, 1536) else (1,))
         for b in bs:
             by = algorithmic_bytes(fmt, r, c, b, qd)
             row = {}
-            for mode, ov in (("chained", True), ("isolated", False)):
+            # the isolated launch mode at batch 1 only (the batch 2-8 lines keep the run short)
+            modes = (("chained", True), ("isolated", False)) if b == 1 or args.full_sweep else (("chained", True),)
+            for mode, ov in modes:
                 t, n = time_gemv_cold(qd, torch, fmt, r, c, b, stream, overlap=ov)
                 row[mode] = {"us": round(t * 1e6, 2), "GB/s": round(by / t / 1e9, 1),
                              "frac": round(by / t / 1e9 / hbm, 3)}
@@ -835,7 +847,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="main line only (no sweep, 1.7B, CPU baseline)")
     ap.add_argument("--no-1p7b", action="store_true")
-    ap.add_argument("--full-sweep", action="store_true", help="q_gemv sweep at batch 1, 2, 4, 8")
+    ap.add_argument("--full-sweep", action="store_true", help="q_gemv sweep: both launch modes at every batch size")
+    ap.add_argument("--batch1-sweep", action="store_true", help="q_gemv sweep at batch 1 only")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--gemv", default=None, help="microbenchmark one shape, FMT:ROWSxCOLS:BATCH")

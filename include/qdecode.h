@@ -230,8 +230,9 @@ qd_status qd_q_gemv_ex(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, co
 /* layout (qd_repack).  x: f32 [t][cols].  y: f32 [t][rows], must not overlap  */
 /* x or the workspace.  cols a multiple of 64, 1 <= t <= QD_MAX_GEMM_TOKENS.     */
 /* workspace: device, 16-byte aligned, >= qd_q_gemm_workspace bytes (0 for an  */
-/* unsupported format or shape); it holds the split x between the call's two   */
-/* kernels and may be reused once the call has completed on `stream`.          */
+/* unsupported format or shape; a smaller one: QD_ERR_NOMEM, as for the other */
+/* workspaces); it holds the split x between the call's two kernels and may be */
+/* reused once the call has completed on `stream`.                              */
 /* Arithmetic (5th-generation tensor cores, f32 accumulation): each token's x  */
 /* is scaled by a power of two and split into two binary16 parts (about 2^-22  */
 /* relative); Q4_0 / Q8_0 weights enter as the binary16 rounding of d * q       */
@@ -321,13 +322,18 @@ qd_status qd_gqa_decode_attn(const float* q, int64_t q_batch_stride, const float
  * call cudaMalloc because it can synchronise the device or fail at an unpredictable
  * moment.  This entry point takes the same inputs and outputs as qd_gqa_decode_attn
  * (same meaning, layout and validation) but keeps its partial results in a fixed 8 MiB
- * device array that the library reserves on every GPU that loads it, until the process
- * exits.  It calls no cudaMalloc or cudaFree.
+ * device array inside the library.  It calls no cudaMalloc or cudaFree.
+ *  - When the array is reserved: the CUDA driver reserves it when it loads the library's
+ *    module holding this function on a device, and keeps it until the process exits.
+ *    Under CUDA's lazy module loading (the default since CUDA 12.2) that load can happen
+ *    on the first call of this entry point on a device, and is itself a driver-side
+ *    allocation that may synchronise.  So make one warm-up call on each device at set-up,
+ *    before any stream capture and before any loop that must not allocate.
  *  - Size limit: calls whose workspace (qd_gqa_decode_attn_workspace) would exceed
  *    8 MiB return QD_ERR_NOMEM and enqueue nothing.  The largest configuration here,
  *    32 heads at context 4096 with batch 16, needs 4.3 MB.
- *  - The first call on each device looks up the array's device address (with that
- *    device current); make that first call before any stream capture.
+ *  - The first call on each device also looks up the array's device address (with that
+ *    device current); the warm-up call above covers it.
  *  - All calls share the one array and leave their partials in it.  Nothing needs to
  *    start at zero, but calls that overlap on the GPU (e.g. on two streams) race on it:
  *    order them on one stream. */
@@ -419,6 +425,13 @@ qd_status qd_model_pos(qd_model* m, int32_t* pos_host, int batch, qd_stream_t st
 /* Device pointers to the KV cache, [layers][max_batch][n_kv_heads][max_ctx][head_dim] of
  * f32 (kv_f16 == 0) or binary16 bit patterns (kv_f16 == 1). */
 qd_status qd_model_kv_cache(qd_model* m, void** k_cache, void** v_cache);
+/* Device pointer and size of the quantised-activation buffer of a model created with
+ * act_q8 == 1 (NULL and 0 otherwise).  Each product of the step quantises its input into
+ * it, so after a step over `batch` sequences it holds the output head's input in the
+ * layout of qd_quantize_q8 with cols = dim: int8 codes [batch][dim], then, from byte
+ * offset batch*dim rounded up to 16, f16 d [batch][dim/32].  For inspection (tests); the
+ * next step overwrites it. */
+qd_status qd_model_act_q8_buffer(qd_model* m, void** buf, size_t* bytes);
 /* Synchronise `stream` and return QD_ERR_DEVICE_FLAG (and clear the word) if a
  * kernel met an out-of-range token or position since the last check. */
 qd_status qd_model_check(qd_model* m, qd_stream_t stream);

@@ -590,7 +590,7 @@ qd_status qd_q_gemm(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const
   if (rows < 1 || rows > (int64_t)1 << 30 || cols < 64 || cols % 64 || cols > (int64_t)1 << 20 || t < 1 ||
       t > QD_MAX_GEMM_TOKENS)
     return QD_ERR_SHAPE;
-  if (workspace_bytes < gemm_workspace_bytes(cols, t)) return QD_ERR_INVALID_ARG;
+  if (workspace_bytes < gemm_workspace_bytes(cols, t)) return QD_ERR_NOMEM;
   if (!aligned16(W) || !aligned16(x) || !aligned16(y) || !aligned16(workspace)) return QD_ERR_ALIGN;
   return launch_q_gemm(fmt, packed_view(fmt, W, rows, cols), x, y, t, workspace, nullptr, (cudaStream_t)stream);
 }

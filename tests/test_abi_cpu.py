@@ -105,7 +105,7 @@ def test_gemm_validation_before_any_device_work(lib):
     assert f(0, good, 300, 512, good, good, 0, good, need, None) == 2       # t = 0
     assert f(0, good, 300, 512, good, good, 65537, good, need, None) == 2   # t too large
     assert f(0, good, 0, 512, good, good, 80, good, need, None) == 2        # no rows
-    assert f(0, good, 300, 512, good, good, 80, good, need - 1, None) == 1  # workspace too small
+    assert f(0, good, 300, 512, good, good, 80, good, need - 1, None) == 6  # workspace too small: NOMEM
     assert f(0, good + 4, 300, 512, good, good, 80, good, need, None) == 3  # misaligned W
     assert f(0, good, 300, 512, good, good, 80, good + 8, need, None) == 3  # misaligned workspace
 
