@@ -384,7 +384,8 @@ typedef struct qd_model qd_model;
 
 /* Bytes of the caller-provided regions: packed weights, and state (KV cache,
  * activations, positions, error word, rope table; the flat-split attention's partials
- * and counters when the model takes it; the quantised-activation buffer with act_q8).
+ * and counters when the model takes it; with act_q8 one quantised-input slot per product,
+ * 4 * layers + 1 of them).
  * 0 for an invalid config (including act_q8 with formats other than Q4_0 / Q8_0, and
  * the formats the decode step does not take). */
 size_t qd_model_weight_bytes(const qd_config* cfg);
@@ -425,13 +426,15 @@ qd_status qd_model_pos(qd_model* m, int32_t* pos_host, int batch, qd_stream_t st
 /* Device pointers to the KV cache, [layers][max_batch][n_kv_heads][max_ctx][head_dim] of
  * f32 (kv_f16 == 0) or binary16 bit patterns (kv_f16 == 1). */
 qd_status qd_model_kv_cache(qd_model* m, void** k_cache, void** v_cache);
-/* Device pointer and size of the quantised-activation buffer of a model created with
- * act_q8 == 1 (NULL and 0 otherwise).  Each product of the step quantises its input into
- * it, so after a step over `batch` sequences it holds the output head's input in the
- * layout of qd_quantize_q8 with cols = dim: int8 codes [batch][dim], then, from byte
- * offset batch*dim rounded up to 16, f16 d [batch][dim/32].  For inspection (tests); the
- * next step overwrites it. */
-qd_status qd_model_act_q8_buffer(qd_model* m, void** buf, size_t* bytes);
+/* The quantised inputs of the last step of a model created with act_q8 == 1 (buf NULL,
+ * slot_bytes 0 and slots 0 otherwise): one slot per quantised input, slot k at
+ * buf + k * slot_bytes, in step order -- for layer l the QKV input (4l), the attention
+ * output (4l + 1), the feed-forward input (4l + 2) and the SwiGLU output (4l + 3) -- then
+ * the head's input (slot 4 * layers).  After a step over `batch` sequences, a slot of an
+ * input of length n holds it in the layout of qd_quantize_q8: int8 codes [batch][n], then,
+ * from byte offset batch*n rounded up to 16, f16 d [batch][n/32].  For inspection (tests);
+ * the next step overwrites them. */
+qd_status qd_model_act_q8_buffer(qd_model* m, void** buf, size_t* slot_bytes, int* slots);
 /* Synchronise `stream` and return QD_ERR_DEVICE_FLAG (and clear the word) if a
  * kernel met an out-of-range token or position since the last check. */
 qd_status qd_model_check(qd_model* m, qd_stream_t stream);

@@ -54,6 +54,11 @@ class _Config(ctypes.Structure):
                 ("emb_fmt", ctypes.c_int), ("kv_f16", ctypes.c_int), ("act_q8", ctypes.c_int)]
 
 
+class _Q8TF(ctypes.Structure):
+    _fields_ = [("q_given", ctypes.c_void_p), ("d_given", ctypes.c_void_p), ("x_out", ctypes.c_void_p),
+                ("slot_cols", ctypes.c_int64)]
+
+
 def _L():
     global _lib
     if _lib is None:
@@ -103,7 +108,7 @@ def _L():
                                        ctypes.POINTER(ctypes.c_int64)]
         lib.or_decode_step.restype = i32
         lib.or_decode_step_tf.argtypes = [ctypes.POINTER(_Config), p, p, p, i64, i32, i32, p,
-                                          ctypes.POINTER(ctypes.c_int64), i32, p, p]
+                                          ctypes.POINTER(ctypes.c_int64), i32, p, p, ctypes.POINTER(_Q8TF)]
         lib.or_decode_step_tf.restype = i32
         lib.or_gemv_xd.argtypes = [i32, p, i64, i64, p, i32, i64, i64, p]
         lib.or_gemv_xd.restype = i32
@@ -384,12 +389,22 @@ class Model:
         return logits, int(nxt.value)
 
 
+    def q8_slots(self) -> tuple[int, int]:
+        """(slots, row length) of the step's quantised inputs in act_q8 mode: per layer the
+        QKV input, the attention output, the feed-forward input and the SwiGLU output, then
+        the head's input."""
+        c = self.cfg
+        return 4 * c["layers"] + 1, max(c["dim"], c["ffn"], c["n_heads"] * c["head_dim"])
+
     def decode_step_tf(self, k_cache: np.ndarray, v_cache: np.ndarray, layer_stride: int, pos: int, token: int,
-                       kv_given: bool, seq_offset: int = 0):
+                       kv_given: bool, seq_offset: int = 0, q8_codes=None, q8_d=None):
         """The step with the teacher-forcing hooks of or_decode_step_tf: with ``kv_given`` the
         caches already hold this step's k and v at ``pos`` (another implementation's values)
-        and are not written.  Returns (logits f64[vocab], argmax, kv f32 [layers][2][n_kv*hd]
-        as formed before any binary16 rounding, head input f32 [dim])."""
+        and are not written; with ``q8_codes`` (int8 [slots][cols]) and ``q8_d`` (f32
+        [slots][cols/32]) each quantised product (act_q8) multiplies those codes instead of
+        its own (slots as in q8_slots()).  Returns (logits f64[vocab], argmax, kv f32
+        [layers][2][n_kv*hd] as formed before any binary16 rounding, head input f32 [dim],
+        the f32 input of every quantised product [slots][cols] or None without act_q8)."""
         assert k_cache.dtype == np.float32 and v_cache.dtype == np.float32
         assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
         c = self.cfg
@@ -398,13 +413,24 @@ class Model:
         kv = np.empty((c["layers"], 2, kd), dtype=np.float32)
         hx = np.empty(c["dim"], dtype=np.float32)
         nxt = ctypes.c_int64()
+        tf, xo = None, None
+        if c.get("act_q8"):
+            slots, cols = self.q8_slots()
+            xo = np.zeros((slots, cols), np.float32)
+            tf = _Q8TF(None, None, xo.ctypes.data, cols)
+            if q8_codes is not None:
+                qg = np.ascontiguousarray(q8_codes, dtype=np.int8).reshape(slots, cols)
+                dg = np.ascontiguousarray(q8_d, dtype=np.float32).reshape(slots, cols // 32)
+                tf.q_given, tf.d_given = qg.ctypes.data, dg.ctypes.data
+        else:
+            assert q8_codes is None
         rc = _L().or_decode_step_tf(ctypes.byref(self._c), self._ptrs, k_cache.ctypes.data + 4 * seq_offset,
                                     v_cache.ctypes.data + 4 * seq_offset, layer_stride, pos, token,
                                     logits.ctypes.data, ctypes.byref(nxt), 1 if kv_given else 0, kv.ctypes.data,
-                                    hx.ctypes.data)
+                                    hx.ctypes.data, ctypes.byref(tf) if tf is not None else None)
         if rc:
             raise ValueError(f"or_decode_step_tf rc={rc}")
-        return logits, int(nxt.value), kv, hx
+        return logits, int(nxt.value), kv, hx, xo
 
 
 def set_threads(n: int) -> int:

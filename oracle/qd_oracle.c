@@ -712,14 +712,28 @@ int or_quantize_q8(const float* x, int64_t n, int8_t* q, float* d16, float* s16)
 int or_gemv_q8act(int fmt, const uint8_t* w, int64_t rows, int64_t cols, const int8_t* xq, const float* xd,
                   const float* xs, int batch, int64_t row0, int64_t nrows, double* y);
 
+/* Teacher-forcing slots of the Q8 activations (act_q8): one per quantised input of the
+ * step, in order -- per layer l the QKV input (4l), the attention output (4l + 1), the
+ * feed-forward input (4l + 2), the SwiGLU output (4l + 3) -- and the head's input (4L). */
+typedef struct {
+    const int8_t* q_given; /* [slots][slot_cols] codes to use instead of quantising, or NULL */
+    const float* d_given;  /* [slots][slot_cols / 32] their (binary16) block scales          */
+    float* x_out;          /* [slots][slot_cols] the f32 inputs the step formed, or NULL     */
+    int64_t slot_cols;     /* row length of the three arrays                                 */
+} or_q8_tf;
+
 /* y[0..rows) = W x for one activation vector: over the f32-rounded activations' Q8 blocks
- * (act_q8) or, otherwise, the plain double product. */
+ * (act_q8) or, otherwise, the plain double product.  With act_q8, slot `slot` of tf (when
+ * given) receives the f32 input, and supplies the codes and scales to multiply instead of
+ * the quantisation of that input (Q4_0 / Q8_0 weights only: Q4_1 would also need the
+ * Q8_1 sums). */
 static int product(const or_config* c, int fmt, const uint8_t* w, int64_t rows, int64_t cols, const double* x,
-                   double* y) {
+                   double* y, const or_q8_tf* tf, int slot) {
     if (!c->act_q8) {
         gemv_rows_d(fmt, w, rows, cols, x, 1, cols, y, rows, 0, rows);
         return 0;
     }
+    if (tf && tf->q_given && (fmt == OR_Q4_1 || !tf->d_given || cols > tf->slot_cols)) return -1;
     float* xf = (float*)malloc(sizeof(float) * (size_t)cols);
     int8_t* q = (int8_t*)malloc((size_t)cols);
     float* d = (float*)malloc(sizeof(float) * (size_t)(cols / 32));
@@ -727,24 +741,33 @@ static int product(const or_config* c, int fmt, const uint8_t* w, int64_t rows, 
     int rc = -2;
     if (xf && q && d && sm) {
         for (int64_t i = 0; i < cols; ++i) xf[i] = (float)x[i];
-        rc = or_quantize_q8(xf, cols, q, d, sm);
+        if (tf && tf->x_out) memcpy(tf->x_out + (int64_t)slot * tf->slot_cols, xf, sizeof(float) * (size_t)cols);
+        if (tf && tf->q_given) {
+            memcpy(q, tf->q_given + (int64_t)slot * tf->slot_cols, (size_t)cols);
+            memcpy(d, tf->d_given + (int64_t)slot * (tf->slot_cols / 32), sizeof(float) * (size_t)(cols / 32));
+            rc = 0;
+        } else {
+            rc = or_quantize_q8(xf, cols, q, d, sm);
+        }
         if (!rc) rc = or_gemv_q8act(fmt, w, rows, cols, q, d, sm, 1, 0, rows, y);
     }
     free(xf); free(q); free(d); free(sm);
     return rc;
 }
 
-/* The step with two test hooks for teacher forcing against another implementation; the
+/* The step with test hooks for teacher forcing against another implementation; the
  * arithmetic is the step's own.
  *   kv_given = 1: the cache already holds this step's k and v at pos (the other
  *     implementation's values); the step attends over the cache as it is and does not
  *     write it.
  *   kv_out (or NULL): receives the k and v the step formed, rounded to f32 but before any
  *     binary16 rounding, as [layer][2][n_kv_heads * head_dim] (k, then v).
- *   head_x (or NULL): receives the head's input, the final normed x rounded to f32. */
+ *   head_x (or NULL): receives the head's input, the final normed x rounded to f32.
+ *   tf (or NULL; act_q8 only): per quantised input, the f32 values formed and the codes
+ *     and scales to multiply instead (or_q8_tf above). */
 int or_decode_step_tf(const or_config* c, const void* const* tensors, float* k_cache, float* v_cache,
                       int64_t layer_stride, int pos, int token, double* logits, int64_t* next_token, int kv_given,
-                      float* kv_out, float* head_x) {
+                      float* kv_out, float* head_x, const or_q8_tf* tf) {
     if (!c || pos < 0 || pos >= c->max_ctx || token < 0 || token >= c->vocab) return -1;
     if (c->n_heads % c->n_kv_heads) return -1;
     const int D = c->dim, F = c->ffn, hd = c->head_dim, hq = c->n_heads, hk = c->n_kv_heads;
@@ -774,9 +797,9 @@ int or_decode_step_tf(const or_config* c, const void* const* tensors, float* k_c
         float* vl = v_cache + (int64_t)l * layer_stride;
         /* attention block */
         or_rmsnorm_d(x, (const float*)L[0], D, c->eps, xn);
-        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[1], QD, D, xn, q)) ||
-            (rc = product(c, c->w_fmt, (const uint8_t*)L[2], KD, D, xn, k)) ||
-            (rc = product(c, c->w_fmt, (const uint8_t*)L[3], KD, D, xn, v)))
+        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[1], QD, D, xn, q, tf, 4 * l)) ||
+            (rc = product(c, c->w_fmt, (const uint8_t*)L[2], KD, D, xn, k, tf, 4 * l)) ||
+            (rc = product(c, c->w_fmt, (const uint8_t*)L[3], KD, D, xn, v, tf, 4 * l)))
             goto done;
         for (int h = 0; h < hq; ++h) or_rope_head_d(q + (int64_t)h * hd, hd, pos, c->pairing, c->rope_theta);
         for (int h = 0; h < hk; ++h) or_rope_head_d(k + (int64_t)h * hd, hd, pos, c->pairing, c->rope_theta);
@@ -797,15 +820,15 @@ int or_decode_step_tf(const or_config* c, const void* const* tensors, float* k_c
                 }
             }
         or_attention_d(q, kl, vl, hq, hk, hd, pos + 1, c->max_ctx, att);
-        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[4], D, QD, att, t))) goto done;
+        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[4], D, QD, att, t, tf, 4 * l + 1))) goto done;
         for (int i = 0; i < D; ++i) x[i] += t[i];
         /* feed-forward block */
         or_rmsnorm_d(x, (const float*)L[5], D, c->eps, xn);
-        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[6], F, D, xn, g)) ||
-            (rc = product(c, c->w_fmt, (const uint8_t*)L[7], F, D, xn, u)))
+        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[6], F, D, xn, g, tf, 4 * l + 2)) ||
+            (rc = product(c, c->w_fmt, (const uint8_t*)L[7], F, D, xn, u, tf, 4 * l + 2)))
             goto done;
         for (int i = 0; i < F; ++i) g[i] = or_silu(g[i]) * u[i];
-        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[8], D, F, g, t))) goto done;
+        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[8], D, F, g, t, tf, 4 * l + 3))) goto done;
         for (int i = 0; i < D; ++i) x[i] += t[i];
     }
     or_rmsnorm_d(x, (const float*)tensors[1], D, c->eps, xn);
@@ -813,7 +836,7 @@ int or_decode_step_tf(const or_config* c, const void* const* tensors, float* k_c
         for (int i = 0; i < D; ++i) head_x[i] = (float)xn[i];
     {
         const uint8_t* head = (const uint8_t*)(tensors[2] ? tensors[2] : tensors[0]);
-        if ((rc = product(c, c->emb_fmt, head, c->vocab, D, xn, logits))) goto done;
+        if ((rc = product(c, c->emb_fmt, head, c->vocab, D, xn, logits, tf, 4 * c->layers))) goto done;
     }
     if (next_token) *next_token = or_argmax_f64(logits, c->vocab);
 done:
@@ -824,7 +847,7 @@ done:
 int or_decode_step(const or_config* c, const void* const* tensors, float* k_cache, float* v_cache,
                    int64_t layer_stride, int pos, int token, double* logits, int64_t* next_token) {
     return or_decode_step_tf(c, tensors, k_cache, v_cache, layer_stride, pos, token, logits, next_token, 0, NULL,
-                             NULL);
+                             NULL, NULL);
 }
 
 int or_abi_version(void) { return 1; }

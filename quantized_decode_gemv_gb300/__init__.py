@@ -31,7 +31,8 @@ EXPORTS = ["qd_status_str", "qd_abi_version", "qd_f16_to_f32", "qd_bf16_to_f32",
            "qd_gqa_decode_attn_noalloc",
            "qd_swiglu", "qd_argmax", "qd_embed", "qd_model_weight_bytes", "qd_model_state_bytes",
            "qd_model_create", "qd_model_destroy", "qd_decode_step", "qd_model_reset", "qd_model_set_pos",
-           "qd_model_pos", "qd_model_kv_cache", "qd_model_check", "qd_model_launches_per_step"]
+           "qd_model_pos", "qd_model_kv_cache", "qd_model_act_q8_buffer", "qd_model_check",
+           "qd_model_launches_per_step"]
 
 
 class QDError(RuntimeError):
@@ -103,6 +104,7 @@ def load():
         "qd_model_set_pos": ([p, p, i32, p], i32),
         "qd_model_pos": ([p, p, i32, p], i32),
         "qd_model_kv_cache": ([p, ctypes.POINTER(p), ctypes.POINTER(p)], i32),
+        "qd_model_act_q8_buffer": ([p, ctypes.POINTER(p), ctypes.POINTER(sz), ctypes.POINTER(i32)], i32),
         "qd_model_check": ([p, p], i32),
         "qd_model_launches_per_step": ([p], i32),
     }
@@ -350,6 +352,14 @@ class Model:
         k, v = ctypes.c_void_p(), ctypes.c_void_p()
         _check("qd_model_kv_cache", load().qd_model_kv_cache(self.handle, ctypes.byref(k), ctypes.byref(v)))
         return k.value, v.value
+
+    def act_q8_buffer(self):
+        """(device pointer, bytes per slot, slots) of the act_q8 quantised inputs of the last
+        step ((None, 0, 0) without act_q8)."""
+        b, n, k = ctypes.c_void_p(), ctypes.c_size_t(), ctypes.c_int()
+        _check("qd_model_act_q8_buffer", load().qd_model_act_q8_buffer(self.handle, ctypes.byref(b), ctypes.byref(n),
+                                                                       ctypes.byref(k)))
+        return b.value, n.value, k.value
 
     def check(self, stream=None) -> int:
         return int(load().qd_model_check(self.handle, _stream(stream)))

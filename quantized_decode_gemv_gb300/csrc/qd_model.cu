@@ -36,7 +36,8 @@ struct Layout {
   size_t kc, vc, x, xn, qkv, q, att, act, logits, am_key, am_cnt, tok_in, tok_out, pos, err,
       rope;
   size_t attn_ws, attn_cnt;  // flat-split attention: partials and per-pair counters
-  size_t xq;                 // act_q8: the quantised activations of the current product
+  size_t xq;                 // act_q8: the quantised input of each product, one slot each
+  size_t xq_slot;            // bytes per slot
   bool attn_flat;
   int attn_ctas;  // its grid (one CTA per SM), fixed with the workspace size
   size_t state_bytes;
@@ -115,7 +116,10 @@ Layout make_layout(const qd_config* c) {
   L.attn_ctas = attn_flat_ctas();
   L.attn_ws = L.attn_flat ? take(4 * attn_flat_ws_floats(c->n_heads, c->n_kv_heads, c->max_batch, L.attn_ctas)) : 0;
   L.attn_cnt = L.attn_flat ? take(4 * (size_t)c->n_kv_heads * c->max_batch) : 0;
-  L.xq = c->act_q8 ? take(q8_buffer_bytes((int)B, std::max(std::max(D, F), QD), false)) : 0;
+  // one slot per quantised input (4 per layer, then the head's), so after a step every
+  // product's codes can still be read
+  L.xq_slot = c->act_q8 ? align_up(q8_buffer_bytes((int)B, std::max(std::max(D, F), QD), false), 256) : 0;
+  L.xq = c->act_q8 ? take(L.xq_slot * (4 * (size_t)c->layers + 1)) : 0;
   L.state_bytes = off;
   return L;
 }
@@ -188,9 +192,9 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
   // the RMSNorm when it has one), then the integer product; launched without programmatic
   // dependence (they run once their predecessor has completed and never let their
   // successor start early).
-  void* xq = m->s + L.xq;
-  auto q8prod = [&](int fmt, PackedView W, const float* in, const float* gains, float* y,
+  auto q8prod = [&](int slot, int fmt, PackedView W, const float* in, const float* gains, float* y,
                     GemvMode mode) -> qd_status {
+    void* xq = m->s + L.xq + (size_t)slot * L.xq_slot;
     if (gains)  // the norm quantised as it is formed (the same f32 values as the norm kernel)
       QD_TRY(launch_rmsnorm_q8(in, gains, (int)W.cols, c.eps, batch, xq, st));
     else
@@ -236,7 +240,7 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
     e.max_ctx = c.max_ctx;
     const float* attn_norm = reinterpret_cast<const float*>(m->w + o.attn_norm);
     if (c.act_q8) {
-      QD_TRY(q8prod(c.w_fmt, qa.W, x, attn_norm, qkv, kGemvStore));
+      QD_TRY(q8prod(4 * l, c.w_fmt, qa.W, x, attn_norm, qkv, kGemvStore));
       QD_TRY(launch_qkv_post(qkv, L.qkv_rows, batch, e, err, st, true));
       ++n;
     } else if (gemv_streams(qa)) {
@@ -258,10 +262,10 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
                                       c.head_dim, pos, c.max_ctx, batch, err, st, true));
     ++n;
     if (c.act_q8) {
-      QD_TRY(q8prod(c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, nullptr, x, kGemvAccumulate));
-      QD_TRY(q8prod(c.w_fmt, m->W(c.w_fmt, o.wgu, 2 * F, D), x, reinterpret_cast<const float*>(m->w + o.ffn_norm),
+      QD_TRY(q8prod(4 * l + 1, c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, nullptr, x, kGemvAccumulate));
+      QD_TRY(q8prod(4 * l + 2, c.w_fmt, m->W(c.w_fmt, o.wgu, 2 * F, D), x, reinterpret_cast<const float*>(m->w + o.ffn_norm),
                     act, kGemvSwiGLU));
-      QD_TRY(q8prod(c.w_fmt, m->W(c.w_fmt, o.wd, D, F), act, nullptr, x, kGemvAccumulate));
+      QD_TRY(q8prod(4 * l + 3, c.w_fmt, m->W(c.w_fmt, o.wd, D, F), act, nullptr, x, kGemvAccumulate));
       continue;
     }
     QD_TRY(launch_q_gemv(args(c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, x, kGemvAccumulate), st));
@@ -279,7 +283,7 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
   ha.am.pos = pos;
   const float* out_norm = reinterpret_cast<const float*>(m->w + L.out_norm);
   if (c.act_q8) {
-    QD_TRY(q8prod(c.emb_fmt, ha.W, x, out_norm, m->f(L.logits), kGemvStore));
+    QD_TRY(q8prod(4 * c.layers, c.emb_fmt, ha.W, x, out_norm, m->f(L.logits), kGemvStore));
     QD_TRY(launch_argmax(m->f(L.logits), c.vocab, batch, m->i(L.tok_out), pos, st));
     ++n;
   } else if (gemv_streams(ha)) {
@@ -457,6 +461,15 @@ qd_status qd_model_kv_cache(qd_model* m, void** k_cache, void** v_cache) {
   if (!m || !k_cache || !v_cache) return QD_ERR_INVALID_ARG;
   *k_cache = m->s + m->L.kc;
   *v_cache = m->s + m->L.vc;
+  return QD_OK;
+}
+
+qd_status qd_model_act_q8_buffer(qd_model* m, void** buf, size_t* slot_bytes, int* slots) {
+  if (!m || !buf || !slot_bytes || !slots) return QD_ERR_INVALID_ARG;
+  const bool on = m->cfg.act_q8 != 0;
+  *buf = on ? m->s + m->L.xq : nullptr;
+  *slot_bytes = on ? m->L.xq_slot : 0;
+  *slots = on ? 4 * m->cfg.layers + 1 : 0;
   return QD_OK;
 }
 

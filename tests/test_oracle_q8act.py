@@ -200,7 +200,7 @@ def test_teacher_forcing_hooks(act_q8, kv_f16):
     kc2, vc2 = kc.copy(), vc.copy()
     for p, tok in enumerate([9, 250, 1]):
         lg, nxt = om.decode_step(kc, vc, per, p, tok)
-        lg2, nxt2, kv, hx = om.decode_step_tf(kc2, vc2, per, p, tok, kv_given=False)
+        lg2, nxt2, kv, hx, xo = om.decode_step_tf(kc2, vc2, per, p, tok, kv_given=False)
         assert np.array_equal(lg, lg2) and nxt == nxt2
         assert np.array_equal(kc, kc2) and np.array_equal(vc, vc2)
         rnd = _round_f16_vec if kv_f16 else (lambda a: a)
@@ -214,16 +214,42 @@ def test_teacher_forcing_hooks(act_q8, kv_f16):
         else:
             np.testing.assert_allclose(lg, oracle.gemv(cfg["emb_fmt"], head, cfg["vocab"], cfg["dim"], hx)[0],
                                        rtol=0, atol=1e-5 * np.abs(lg).max())
+        if act_q8:
+            # every product's f32 input: the head's is head_x; feeding back each slot's own
+            # quantisation reproduces the step bit for bit
+            slots, cols = om.q8_slots()
+            assert np.array_equal(xo[slots - 1, :cfg["dim"]], hx)
+            qs = np.zeros((slots, cols), np.int8)
+            ds = np.zeros((slots, cols // 32), np.float32)
+            width = [cfg["dim"], cfg["n_heads"] * cfg["head_dim"], cfg["dim"], cfg["ffn"]] * L + [cfg["dim"]]
+            for k in range(slots):
+                q, d, _ = oracle.quantize_q8(xo[k, :width[k]][None, :])
+                qs[k, :width[k]], ds[k, :width[k] // 32] = q[0], d[0]
+            k5, v5 = kc.copy(), vc.copy()
+            lg5, _, _, _, xo5 = om.decode_step_tf(k5, v5, per, p, tok, kv_given=True, q8_codes=qs, q8_d=ds)
+            assert np.array_equal(lg5, lg) and np.array_equal(xo5, xo)
+            # a given code changed in the first layer's attention-output slot: that product uses
+            # it, so the inputs formed after it move (the logits depend on the head's slot only)
+            q1 = qs.copy()
+            q1[1, 3] = q1[1, 3] + (1 if q1[1, 3] < 127 else -1)
+            lg6, _, _, _, xo6 = om.decode_step_tf(kc.copy(), vc.copy(), per, p, tok, kv_given=True, q8_codes=q1,
+                                                  q8_d=ds)
+            assert np.array_equal(xo6[:2], xo[:2]) and not np.array_equal(xo6[2], xo[2])
+            assert np.array_equal(lg6, lg)
+            q8 = qs.copy()
+            q8[slots - 1, 3] = q8[slots - 1, 3] + (1 if q8[slots - 1, 3] < 127 else -1)
+            lg7, _, _, _, _ = om.decode_step_tf(kc.copy(), vc.copy(), per, p, tok, kv_given=True, q8_codes=q8, q8_d=ds)
+            assert not np.array_equal(lg7, lg)
     # kv_given: the same cache gives the same step; other values at pos are read, not replaced
     p, tok = 3, 42
     base_k, base_v = kc.copy(), vc.copy()
     lg, _ = om.decode_step(kc, vc, per, p, tok)
     k3, v3 = kc.copy(), vc.copy()
-    lg3, _, _, _ = om.decode_step_tf(k3, v3, per, p, tok, kv_given=True)
+    lg3, _, _, _, _ = om.decode_step_tf(k3, v3, per, p, tok, kv_given=True)
     assert np.array_equal(lg, lg3) and np.array_equal(k3, kc)
     k4, v4 = kc.copy(), vc.copy()
     k4.reshape(L, hk, ctx, hd)[:, :, p] *= 2.0
-    lg4, _, kv4, _ = om.decode_step_tf(k4, v4, per, p, tok, kv_given=True)
+    lg4, _, kv4, _, _ = om.decode_step_tf(k4, v4, per, p, tok, kv_given=True)
     assert not np.array_equal(lg4, lg)
     assert np.array_equal(k4.reshape(L, hk, ctx, hd)[:, :, p], 2.0 * kc.reshape(L, hk, ctx, hd)[:, :, p])
     assert np.array_equal(base_k.reshape(L, hk, ctx, hd)[:, :, :p], k4.reshape(L, hk, ctx, hd)[:, :, :p])
