@@ -164,13 +164,15 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- our arm
 
-def build_smol135m(qd, torch, seed):
+def build_smol135m(qd, torch, seed, path=None):
     import qdsynth
 
     cfg = qdsynth.SMOL_135M
     host = qdsynth.model_tensors(cfg, seed)
     srcs = [None if t is None else torch.from_numpy(np.ascontiguousarray(t)).cuda() for t in host]
     model = qd.Model(qd.make_config(cfg, PROMPT + GEN, 1), srcs)
+    if path:
+        model.set_step_path(qd.STEP_CLUSTER if path == "cluster" else qd.STEP_KERNEL_CHAIN)
     torch.cuda.synchronize()
     del srcs
     return cfg, model
@@ -233,7 +235,7 @@ def run_ours(args, world, rank, local):
         qd.build()
     qd.load()
     stream = torch.cuda.current_stream()
-    cfg, model = build_smol135m(qd, torch, seed=rank)
+    cfg, model = build_smol135m(qd, torch, seed=rank, path=args.step_path)
     T = PROMPT + GEN
     prompt = qdsynth.tokens(rank, "smol135m.prompt", PROMPT, cfg["vocab"]).astype(np.int32)
     # device-resident token slots: slot t is the input of position t; outputs of prompt
@@ -531,18 +533,26 @@ def bench_1p7b(qd, torch, stream, args, hbm, batches=(1, 16), layers=None, kv_f1
 
 
 def bench_135m_modes(qd, torch, stream, steps=50):
-    """135M-shaped decode, batch 1, in the default mode (f32 activations, f32 cache) and in
-    the pages' ggml-exact mode (Q8_0 activations before every product, binary16 cache):
-    tokens/s over `steps` consecutive steps from position 150 (graph replays)."""
+    """135M-shaped decode, batch 1, in the default mode (f32 activations, f32 cache), in
+    the pages' ggml-exact mode (Q8_0 activations before every product, binary16 cache) and
+    on the optional cluster path (the layers as one thread-block cluster): tokens/s over
+    `steps` consecutive steps from position 150 (graph replays)."""
     import qdsynth
 
     out = {}
-    for name, extra in (("f32", {}), ("ggml_exact", {"act_q8": True, "kv_f16": True})):
+    for name, extra, path in (("f32", {}, None), ("ggml_exact", {"act_q8": True, "kv_f16": True}, None),
+                              ("f32_cluster_path", {}, "cluster")):
         cfg = dict(qdsynth.SMOL_135M, **extra)
         host = qdsynth.model_tensors(cfg, 0)
         srcs = [None if t is None else torch.from_numpy(np.ascontiguousarray(t)).cuda() for t in host]
         m = qd.Model(qd.make_config(cfg, 256, 1), srcs)
         del srcs
+        if path == "cluster":
+            if not m.cluster_available():
+                out[name] = {"unavailable": "the device cannot schedule the cluster"}
+                m.close()
+                continue
+            m.set_step_path(qd.STEP_CLUSTER)
         tok = torch.zeros(1, dtype=torch.int32, device="cuda")
         outt = torch.empty(1, dtype=torch.int32, device="cuda")
         for _ in range(3):
@@ -860,6 +870,8 @@ def main(argv=None):
     ap.add_argument("--q8act", default=None, help="the ggml-exact activation path alone, FMT:ROWSxCOLS:BATCH")
     ap.add_argument("--modes-135m", action="store_true", help="135M decode in the default and ggml-exact modes")
     ap.add_argument("--kv-f16", action="store_true", help="with --decode-1p7b: binary16 KV cache")
+    ap.add_argument("--step-path", choices=["chain", "cluster"], default=None,
+                    help="force the 135M decode step's path (default: the library's choice)")
     args = ap.parse_args(argv)
     if args.gemv:
         run_gemv_only(args.gemv, args.reps)

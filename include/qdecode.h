@@ -441,6 +441,32 @@ qd_status qd_model_check(qd_model* m, qd_stream_t stream);
 /* Number of kernels one decode step launches (for launch accounting). */
 int qd_model_launches_per_step(const qd_model* m);
 
+/* How the decode step runs its layers (no counterpart on the pages; the same step either
+ * way, parity-tested both ways):
+ *  - QD_STEP_KERNEL_CHAIN: a CUDA graph of per-operation kernels over the whole GPU (the
+ *    embedding, five kernels per layer, the head GEMV with the argmax).
+ *  - QD_STEP_CLUSTER: the embedding and all layers in one kernel, one thread-block
+ *    cluster of 8 or 16 CTAs per sequence that keeps each layer's intermediate vectors in
+ *    distributed shared memory, then the head GEMV with the argmax over the whole GPU.
+ *    Available for Q4_0 / Q8_0 layer weights with the f32 cache and f32 activations, when
+ *    the shapes fit its shared memory (per sequence: a weight slice of each product, and
+ *    the cached K/V rows of one attention chunk, max_ctx / (cluster size / n_kv_heads)
+ *    positions) and the device can schedule the cluster.
+ *  - QD_STEP_AUTO (the default): the kernel chain, the faster of the two on GB300 at the
+ *    135M shape (0.45 against 0.65-0.69 ms per token: the cluster's 16 SMs are latency-
+ *    bound on each layer's products, and a handoff through distributed shared memory costs
+ *    about a round trip to L2).
+ * qd_model_set_step_path: QD_ERR_UNSUPPORTED when QD_STEP_CLUSTER is asked for and not
+ * available, QD_ERR_INVALID_ARG for another value.  qd_model_step_path: the path the
+ * next step takes (QD_STEP_KERNEL_CHAIN or QD_STEP_CLUSTER; -1 for a null model).
+ * qd_model_cluster_available: 1 when the model can take QD_STEP_CLUSTER, else 0. */
+#define QD_STEP_AUTO 0
+#define QD_STEP_KERNEL_CHAIN 1
+#define QD_STEP_CLUSTER 2
+qd_status qd_model_set_step_path(qd_model* m, int path);
+int qd_model_step_path(const qd_model* m);
+int qd_model_cluster_available(const qd_model* m);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,9 @@ EXPORTS = ["qd_status_str", "qd_abi_version", "qd_f16_to_f32", "qd_bf16_to_f32",
            "qd_swiglu", "qd_argmax", "qd_embed", "qd_model_weight_bytes", "qd_model_state_bytes",
            "qd_model_create", "qd_model_destroy", "qd_decode_step", "qd_model_reset", "qd_model_set_pos",
            "qd_model_pos", "qd_model_kv_cache", "qd_model_act_q8_buffer", "qd_model_check",
-           "qd_model_launches_per_step"]
+           "qd_model_launches_per_step", "qd_model_set_step_path", "qd_model_step_path",
+           "qd_model_cluster_available"]
+STEP_AUTO, STEP_KERNEL_CHAIN, STEP_CLUSTER = 0, 1, 2
 
 
 class QDError(RuntimeError):
@@ -107,6 +109,9 @@ def load():
         "qd_model_act_q8_buffer": ([p, ctypes.POINTER(p), ctypes.POINTER(sz), ctypes.POINTER(i32)], i32),
         "qd_model_check": ([p, p], i32),
         "qd_model_launches_per_step": ([p], i32),
+        "qd_model_set_step_path": ([p, i32], i32),
+        "qd_model_step_path": ([p], i32),
+        "qd_model_cluster_available": ([p], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -363,6 +368,16 @@ class Model:
 
     def check(self, stream=None) -> int:
         return int(load().qd_model_check(self.handle, _stream(stream)))
+
+    def set_step_path(self, path: int):
+        """STEP_AUTO, STEP_KERNEL_CHAIN or STEP_CLUSTER (see qd_model_set_step_path)."""
+        _check("qd_model_set_step_path", load().qd_model_set_step_path(self.handle, int(path)))
+
+    def step_path(self) -> int:
+        return int(load().qd_model_step_path(self.handle))
+
+    def cluster_available(self) -> bool:
+        return bool(load().qd_model_cluster_available(self.handle))
 
     def launches_per_step(self) -> int:
         return int(load().qd_model_launches_per_step(self.handle))

@@ -421,4 +421,35 @@ qd_status launch_attention_flat(const float* q, int64_t q_stride, const void* kc
                                 const int32_t* pos, int max_ctx, int batch, int ctas, float* ws, unsigned int* cnt,
                                 uint32_t* err, cudaStream_t stream, bool pdl);
 
+// The decode step's layers (embedding to the last residual add) as one thread-block
+// cluster per sequence (qd_step_cluster.cu).  What it needs from the model: formats,
+// shapes, the weight layout (a uniform stride between layers, offsets inside a layer) and
+// the cache.
+struct StepClusterModel {
+  int fmt = QD_Q4_0, emb_fmt = QD_Q8_0;
+  PackedView emb{};
+  const uint8_t* w = nullptr;
+  int64_t layer0 = 0, layer_stride = 0;  // bytes
+  int64_t off_attn_norm = 0, off_ffn_norm = 0, off_qkv = 0, off_wo = 0, off_gu = 0, off_wd = 0;  // in a layer
+  int layers = 0, D = 0, F = 0, n_heads = 0, n_kv = 0, max_ctx = 0, pairing = QD_ROPE_HALF, vocab = 0;
+  float eps = 0.f;
+  float* kc = nullptr;  // f32 caches [layer][batch][kv_head][max_ctx][64]
+  float* vc = nullptr;
+  int64_t cache_layer_stride = 0, cache_batch_stride = 0;  // elements
+  const float* rope = nullptr;
+};
+struct StepClusterPlan {
+  int C = 0, S = 0, kvp = 0, nmax = 0;
+  uint32_t wbuf_bytes = 0, smem = 0;
+  uint32_t off_wbuf = 0, off_kv = 0, off_slot = 0, off_x = 0, off_v = 0, off_rec = 0, off_sc = 0, off_misc = 0,
+           off_bar = 0;
+};
+// False when the model's shapes, formats or cache do not fit the kernel (shared memory,
+// cluster scheduling on this device).
+bool step_cluster_plan(const StepClusterModel& m, StepClusterPlan* plan);
+// Embedding and every layer for `batch` sequences (tokens tok[b] at positions pos[b]); the
+// residual stream after the last layer goes to x_out [batch][D].
+qd_status launch_step_cluster(const StepClusterModel& m, const StepClusterPlan& plan, const int32_t* tok,
+                              const int32_t* pos, float* x_out, uint32_t* err, int batch, cudaStream_t stream);
+
 }  // namespace qd

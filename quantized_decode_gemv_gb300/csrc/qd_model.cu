@@ -145,6 +145,11 @@ struct qd_model {
   Layout L;
   uint8_t* w;  // weight memory (caller-owned)
   uint8_t* s;  // state memory (caller-owned)
+  // the layers as one thread-block cluster per sequence, when the model fits it
+  StepClusterModel scm{};
+  StepClusterPlan plan{};
+  bool cluster_ok = false;
+  int step_path = QD_STEP_AUTO;
   cudaStream_t capture_stream = nullptr;
   cudaGraphExec_t graph[QD_MAX_BATCH + 1] = {};
   int launches = 0;
@@ -174,8 +179,15 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
   float *x = m->f(L.x), *xn = m->f(L.xn), *qkv = m->f(L.qkv), *q = m->f(L.q), *att = m->f(L.att),
         *act = m->f(L.act);
   int n = 0;
-  QD_TRY(launch_embed(c.emb_fmt, m->W(c.emb_fmt, L.emb, c.vocab, D), m->i(L.tok_in), batch, x, err, st));
-  ++n;
+  const bool cluster = m->cluster_ok && m->step_path == QD_STEP_CLUSTER;
+  if (cluster) {
+    // embedding and every layer in one cluster kernel per sequence; x is the head's input
+    QD_TRY(launch_step_cluster(m->scm, m->plan, m->i(L.tok_in), pos, x, err, batch, st));
+    ++n;
+  } else {
+    QD_TRY(launch_embed(c.emb_fmt, m->W(c.emb_fmt, L.emb, c.vocab, D), m->i(L.tok_in), batch, x, err, st));
+    ++n;
+  }
   auto args = [&](int fmt, PackedView W, const float* in, float* y, GemvMode mode) {
     GemvArgs a;
     a.fmt = fmt;
@@ -217,7 +229,7 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
     n += 2;
     return launch_q_gemv(a, st);
   };
-  for (int l = 0; l < c.layers; ++l) {
+  for (int l = 0; l < (cluster ? 0 : c.layers); ++l) {
     const LayerOff& o = L.layer[l];
     const int64_t esz = c.kv_f16 ? 2 : 4;  // bytes per cache element
     void* kc = m->s + L.kc + (int64_t)l * L.cache_layer_stride * esz;
@@ -391,6 +403,45 @@ qd_status qd_model_create(const qd_config* cfg, const void* const* src, void* we
       cudaStreamSynchronize(st) != cudaSuccess)
     return fail(QD_ERR_CUDA);
   if (cudaStreamCreateWithFlags(&m->capture_stream, cudaStreamNonBlocking) != cudaSuccess) return fail(QD_ERR_CUDA);
+  if (!cfg->act_q8 && !cfg->kv_f16) {
+    StepClusterModel& sc = m->scm;
+    sc.fmt = wf;
+    sc.emb_fmt = cfg->emb_fmt;
+    sc.emb = m->W(cfg->emb_fmt, L.emb, cfg->vocab, D);
+    sc.w = m->w;
+    const LayerOff& l0 = L.layer[0];
+    sc.layer0 = (int64_t)l0.attn_norm;
+    sc.layer_stride = cfg->layers > 1 ? (int64_t)(L.layer[1].attn_norm - l0.attn_norm) : 0;
+    bool uniform = true;
+    for (int l = 1; l < cfg->layers; ++l) {
+      const LayerOff& o = L.layer[l];
+      const int64_t base = sc.layer0 + (int64_t)l * sc.layer_stride;
+      uniform = uniform && (int64_t)o.attn_norm == base && o.ffn_norm - o.attn_norm == l0.ffn_norm - l0.attn_norm &&
+                o.wqkv - o.attn_norm == l0.wqkv - l0.attn_norm && o.wo - o.attn_norm == l0.wo - l0.attn_norm &&
+                o.wgu - o.attn_norm == l0.wgu - l0.attn_norm && o.wd - o.attn_norm == l0.wd - l0.attn_norm;
+    }
+    sc.off_attn_norm = 0;
+    sc.off_ffn_norm = (int64_t)(l0.ffn_norm - l0.attn_norm);
+    sc.off_qkv = (int64_t)(l0.wqkv - l0.attn_norm);
+    sc.off_wo = (int64_t)(l0.wo - l0.attn_norm);
+    sc.off_gu = (int64_t)(l0.wgu - l0.attn_norm);
+    sc.off_wd = (int64_t)(l0.wd - l0.attn_norm);
+    sc.layers = cfg->layers;
+    sc.D = (int)D;
+    sc.F = (int)F;
+    sc.n_heads = cfg->n_heads;
+    sc.n_kv = cfg->n_kv_heads;
+    sc.max_ctx = cfg->max_ctx;
+    sc.pairing = cfg->pairing;
+    sc.vocab = cfg->vocab;
+    sc.eps = cfg->eps;
+    sc.kc = reinterpret_cast<float*>(m->s + L.kc);
+    sc.vc = reinterpret_cast<float*>(m->s + L.vc);
+    sc.cache_layer_stride = L.cache_layer_stride;
+    sc.cache_batch_stride = L.cache_batch_stride;
+    sc.rope = reinterpret_cast<const float*>(m->s + L.rope);
+    m->cluster_ok = uniform && step_cluster_plan(sc, &m->plan);
+  }
   *out = m;
   return QD_OK;
 }
@@ -488,5 +539,27 @@ qd_status qd_model_check(qd_model* m, qd_stream_t stream) {
 }
 
 int qd_model_launches_per_step(const qd_model* m) { return m ? m->launches : 0; }
+
+qd_status qd_model_set_step_path(qd_model* m, int path) {
+  if (!m) return QD_ERR_INVALID_ARG;
+  if (path != QD_STEP_AUTO && path != QD_STEP_KERNEL_CHAIN && path != QD_STEP_CLUSTER) return QD_ERR_INVALID_ARG;
+  if (path == QD_STEP_CLUSTER && !m->cluster_ok) return QD_ERR_UNSUPPORTED;
+  if (path != m->step_path) {
+    for (auto& g : m->graph)
+      if (g) {
+        cudaGraphExecDestroy(g);
+        g = nullptr;
+      }
+    m->step_path = path;
+  }
+  return QD_OK;
+}
+
+int qd_model_step_path(const qd_model* m) {
+  if (!m) return -1;
+  return m->cluster_ok && m->step_path == QD_STEP_CLUSTER ? QD_STEP_CLUSTER : QD_STEP_KERNEL_CHAIN;
+}
+
+int qd_model_cluster_available(const qd_model* m) { return m && m->cluster_ok ? 1 : 0; }
 
 }  // extern "C"

@@ -15,10 +15,14 @@ from gpu_helpers import TOL, assert_close, dev
 pytestmark = pytest.mark.gpu
 
 
-def build_model(qd, cfg, seed, max_ctx, max_batch, host=None):
+def build_model(qd, cfg, seed, max_ctx, max_batch, host=None, path=None):
+    """path: None (the library's choice), or "chain" / "cluster" to force the step path."""
     host = qdsynth.model_tensors(cfg, seed) if host is None else host
     srcs = [None if t is None else dev(t.view(np.uint8) if t.dtype != np.float32 else t) for t in host]
     m = qd.Model(qd.make_config(cfg, max_ctx, max_batch), srcs)
+    if path is not None:
+        m.set_step_path(qd.STEP_CLUSTER if path == "cluster" else qd.STEP_KERNEL_CHAIN)
+        assert m.step_path() == (qd.STEP_CLUSTER if path == "cluster" else qd.STEP_KERNEL_CHAIN)
     torch.cuda.synchronize()
     return m, host
 
@@ -31,12 +35,12 @@ def check_token(ora_logits, ora_tok, gpu_tok, tol=TOL):
     return 1
 
 
-def run_teacher_forced(qd, cfg, seed, prompt, n_gen, batch=1, max_ctx=None, tol=TOL):
+def run_teacher_forced(qd, cfg, seed, prompt, n_gen, batch=1, max_ctx=None, tol=TOL, path=None):
     """Feed `prompt` (batch x P ids) then n_gen greedy tokens; compare every step's logits
     (within `tol` of max |oracle|; near-tie tokens within the same gap)."""
     P = prompt.shape[1]
     max_ctx = max_ctx or (P + n_gen)
-    m, host = build_model(qd, cfg, seed, max_ctx, batch)
+    m, host = build_model(qd, cfg, seed, max_ctx, batch, path=path)
     om = oracle.Model(dict(cfg, max_ctx=max_ctx), host)
     L, hk, hd = cfg["layers"], cfg["n_kv_heads"], cfg["head_dim"]
     okc = [np.zeros(L * hk * max_ctx * hd, np.float32) for _ in range(batch)]
@@ -66,13 +70,61 @@ TINY = dict(layers=2, dim=256, ffn=512, n_heads=4, n_kv_heads=2, head_dim=64, vo
             pairing="half", w_fmt="q4_0", emb_fmt="q8_0")
 
 
-@pytest.mark.parametrize("w_fmt,emb_fmt,pairing", [("q4_0", "q8_0", "half"), ("q8_0", "q8_0", "adjacent"),
-                                                   ("i8", "i8", "half"), ("q4_k", "q4_0", "half")])
-def test_tiny_model_teacher_forced(qd, w_fmt, emb_fmt, pairing):
+@pytest.mark.parametrize("w_fmt,emb_fmt,pairing,path", [
+    ("q4_0", "q8_0", "half", "chain"), ("q8_0", "q8_0", "adjacent", "chain"), ("i8", "i8", "half", None),
+    ("q4_k", "q4_0", "half", None), ("q4_0", "q8_0", "half", "cluster"), ("q8_0", "q8_0", "adjacent", "cluster"),
+    ("q4_0", "q4_0", "adjacent", "cluster"), ("q8_0", "q8_0", "half", "cluster")])
+def test_tiny_model_teacher_forced(qd, w_fmt, emb_fmt, pairing, path):
+    """Both step paths (the kernel chain and the cluster kernel) on the same seeded models."""
     cfg = dict(TINY, w_fmt=w_fmt, emb_fmt=emb_fmt, pairing=pairing)
     prompt = qdsynth.tokens(9, "tiny.prompt", 3 * 5, cfg["vocab"]).reshape(3, 5)
-    worst, near = run_teacher_forced(qd, cfg, 9, prompt, n_gen=6, batch=3, max_ctx=16)
-    print(f"tiny {w_fmt}/{emb_fmt}: worst rel err {worst:.2e}, near-tie tokens {near}")
+    worst, near = run_teacher_forced(qd, cfg, 9, prompt, n_gen=6, batch=3, max_ctx=16, path=path)
+    print(f"tiny {w_fmt}/{emb_fmt} {path}: worst rel err {worst:.2e}, near-tie tokens {near}")
+
+
+@pytest.mark.parametrize("n_heads,n_kv,dim,ffn,max_ctx,batch", [(9, 3, 576, 1536, 40, 1), (8, 8, 512, 1024, 24, 2),
+                                                                (16, 2, 256, 768, 70, 3), (6, 1, 320, 640, 33, 1)])
+def test_cluster_step_shapes_teacher_forced(qd, n_heads, n_kv, dim, ffn, max_ctx, batch):
+    """The cluster kernel over ragged splits: head groupings G = 3, 1, 8, 6, one kv head or
+    as many as half the cluster, rows and positions that do not divide by the cluster, a
+    context run to its end (max_ctx positions, so the last chunk holds the last slot)."""
+    cfg = dict(layers=2, dim=dim, ffn=ffn, n_heads=n_heads, n_kv_heads=n_kv, head_dim=64, vocab=300,
+               rope_theta=1e4, eps=1e-5, pairing="half", w_fmt="q4_0", emb_fmt="q8_0")
+    P = max_ctx - 4
+    prompt = qdsynth.tokens(27, "cl.prompt", batch * P, cfg["vocab"]).reshape(batch, P)
+    worst, near = run_teacher_forced(qd, cfg, 27, prompt, n_gen=5, batch=batch, max_ctx=max_ctx, path="cluster")
+    print(f"cluster G={n_heads // n_kv} n_kv={n_kv}: worst rel err {worst:.2e}, near-tie tokens {near}")
+
+
+def test_step_path_choice(qd):
+    """The kernel chain by default; the 135M shape can take the cluster path (two launches
+    per token: the layers, then the head GEMV with the argmax), and switching back and
+    forth gives the same tokens; modes the cluster kernel does not take refuse it."""
+    m, _ = build_model(qd, dict(qdsynth.SMOL_135M, layers=2), 0, 256, 1)
+    assert m.step_path() == qd.STEP_KERNEL_CHAIN and m.cluster_available()
+    toks = {}
+    for path in (qd.STEP_CLUSTER, qd.STEP_KERNEL_CHAIN):
+        m.reset()
+        m.set_step_path(path)
+        assert m.step_path() == path
+        out = torch.empty(1, dtype=torch.int32)
+        seq = []
+        cur = torch.tensor([3], dtype=torch.int32)
+        for _ in range(4):
+            m.decode_step(cur, 1, out)
+            torch.cuda.synchronize()
+            seq.append(int(out.item()))
+            cur = out.clone()
+        assert m.check() == 0
+        assert m.launches_per_step() == (2 if path == qd.STEP_CLUSTER else 152 - 28 * 5)
+        toks[path] = seq
+    assert toks[qd.STEP_CLUSTER] == toks[qd.STEP_KERNEL_CHAIN]
+    m.close()
+    m, _ = build_model(qd, dict(TINY, kv_f16=True), 0, 16, 1)
+    assert m.step_path() == qd.STEP_KERNEL_CHAIN and not m.cluster_available()
+    with pytest.raises(qd.QDError):
+        m.set_step_path(qd.STEP_CLUSTER)
+    m.close()
 
 
 @pytest.mark.parametrize("batch", [12, 16])
@@ -160,12 +212,13 @@ def test_model_reset_and_errors(qd):
 
 
 @pytest.mark.slow
-def test_smol135m_prompt128_gen128_teacher_forced(qd):
+@pytest.mark.parametrize("path", ["cluster", "chain"])
+def test_smol135m_prompt128_gen128_teacher_forced(qd, path):
     """135M-shaped model: 128 prompt ids ~U[0, 49152), then 128 greedy tokens, batch 1."""
     cfg = qdsynth.SMOL_135M
     prompt = qdsynth.tokens(0, "smol135m.prompt", 128, cfg["vocab"]).reshape(1, 128)
-    worst, near = run_teacher_forced(qd, cfg, 0, prompt, n_gen=128, batch=1, max_ctx=256)
-    print(f"135M: worst rel err {worst:.2e}, near-tie tokens {near}/255")
+    worst, near = run_teacher_forced(qd, cfg, 0, prompt, n_gen=128, batch=1, max_ctx=256, path=path)
+    print(f"135M {path}: worst rel err {worst:.2e}, near-tie tokens {near}/255")
 
 
 def fill_cache_normal(m, cfg, seed, max_batch, max_ctx):
