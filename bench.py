@@ -219,6 +219,48 @@ def time_gemv_cold(qd, torch, fmt, rows, cols, batch, stream, reps=None, seed=0,
     return best, len(ptrs)
 
 
+_CEIL_CACHE = {}
+
+
+def time_read_ceiling(qd, torch, nbytes, overlap, reps=None):
+    """The plain-read ceiling for a buffer of nbytes in the same harness as time_gemv_cold
+    (distinct copies, L2 flushed before each replay of back-to-back launches): the best
+    over a few launch shapes of qd_read_ceiling.  Returns (seconds, config)."""
+    key = (nbytes, overlap)
+    if key in _CEIL_CACHE:
+        return _CEIL_CACHE[key]
+    nb = (nbytes + 15) // 16 * 16
+    n = max(8, min(400, (2 * L2_FLUSH_BYTES) // nb + 1)) if reps is None else reps
+    buf = torch.randint(0, 255, (n, nb), dtype=torch.uint8, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flags = qd.GEMV_OVERLAP if overlap else 0
+    best = None
+    for cps, thr in ((1, 512), (2, 512), (2, 256), (4, 256)):
+        ptrs = [buf[i].data_ptr() for i in range(n)]
+        for ptr in ptrs[:3]:
+            qd.read_ceiling(ptr, nb, cps, thr, flags, sink)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for ptr in ptrs:
+                qd.read_ceiling(ptr, nb, cps, thr, flags, sink)
+        for _ in range(3):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) / 1e3 / n
+            if best is None or t < best[0]:
+                best = (t, f"{cps} CTA/SM x {thr} threads")
+        del g
+    del buf, flush
+    _CEIL_CACHE[key] = best
+    return best
+
+
 def algorithmic_bytes(fmt, rows, cols, batch, qd):
     return qd.packed_bytes(fmt, rows, cols) + 4 * batch * (rows + cols)
 
@@ -475,6 +517,11 @@ def gemv_sweep(qd, torch, stream, hbm, args):
                 t, n = time_gemv_cold(qd, torch, fmt, r, c, b, stream, overlap=ov)
                 row[mode] = {"us": round(t * 1e6, 2), "GB/s": round(by / t / 1e9, 1),
                              "frac": round(by / t / 1e9 / hbm, 3)}
+                if fmt != "i8" and (r, c) != (576, 1536) and fmt != "q4_k":
+                    # the same bytes read by a plain read kernel, same harness and mode
+                    tc_, how = time_read_ceiling(qd, torch, qd.packed_bytes(fmt, r, c), ov)
+                    row[mode]["read_ceiling_us"] = round(tc_ * 1e6, 2)
+                    row[mode]["frac_of_read_ceiling"] = round(tc_ / t, 3)
             res[f"{fmt} {r}x{c} b{b}"] = row
     return res
 
@@ -689,7 +736,7 @@ def run_reference(args, world, rank, local):
     }))
 
 
-def run_gemv_only(spec: str, reps: int):
+def run_gemv_only(spec: str, reps: int, ceiling: bool = True):
     """Microbenchmark of one q_gemv shape, e.g. "q4_0:14336x4096:1" (format:rowsxcols:batch):
     `reps` cold-weight passes; prints one JSON line (not the benchmark contract line)."""
     import torch
@@ -714,6 +761,10 @@ def run_gemv_only(spec: str, reps: int):
         t = min(ts)
         out[mode] = {"us": round(t * 1e6, 3), "GB/s": round(by / t / 1e9, 1), "frac": round(by / t / 1e9 / hbm, 4),
                      "launches_per_pass": n}
+        if ceiling:
+            tc_, how = time_read_ceiling(qd, torch, qd.packed_bytes(fmt, r, c), ov)
+            out[mode].update({"read_ceiling_us": round(tc_ * 1e6, 3), "read_ceiling_launch": how,
+                              "frac_of_read_ceiling": round(tc_ / t, 4)})
     print(json.dumps(out))
 
 
@@ -863,6 +914,7 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--gemv", default=None, help="microbenchmark one shape, FMT:ROWSxCOLS:BATCH")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--no-ceiling", action="store_true", help="with --gemv: skip the plain-read ceiling")
     ap.add_argument("--decode-1p7b", default=None, help="the 1.7B-shaped step alone, at batches e.g. 1,16")
     ap.add_argument("--layers", type=int, default=None, help="with --decode-1p7b: fewer layers (profiling)")
     ap.add_argument("--quantize", default=None, help="the BF16 -> INT8 quantiser alone at ROWSxCOLS")
@@ -874,7 +926,7 @@ def main(argv=None):
                     help="force the 135M decode step's path (default: the library's choice)")
     args = ap.parse_args(argv)
     if args.gemv:
-        run_gemv_only(args.gemv, args.reps)
+        run_gemv_only(args.gemv, args.reps, ceiling=not args.no_ceiling)
         return
     if args.decode_1p7b:
         run_1p7b_only(args.decode_1p7b, args.layers, args.kv_f16)

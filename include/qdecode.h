@@ -218,6 +218,17 @@ qd_status qd_q_gemv(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const
  * still be running on `stream` writes W.  No flags: same as qd_q_gemv.  Unknown
  * flag bits: QD_ERR_INVALID_ARG. */
 #define QD_GEMV_OVERLAP 1u
+
+/* Roofline calibration (no counterpart on the pages: measurement support).  Reads every
+ * byte of buf (device, 16-byte aligned, bytes a multiple of 16) once with 16-byte streaming
+ * loads and computes nothing: the bandwidth one launch of a plain read reaches on this GPU
+ * for a buffer of that size, the ceiling a GEMV streaming the same bytes can be compared
+ * with.  Grid: ctas_per_sm (1..8) CTAs per SM of `threads` (128, 256 or 512) threads, each
+ * CTA one contiguous run.  flags: QD_GEMV_OVERLAP launches it as a programmatic dependent
+ * that waits for its predecessor only before its last write, as a GEMV waits before it
+ * reads x.  sink: device word that the kernel writes only on an improbable XOR value. */
+qd_status qd_read_ceiling(const void* buf, size_t bytes, int ctas_per_sm, int threads, unsigned flags,
+                          uint32_t* sink, qd_stream_t stream);
 qd_status qd_q_gemv_ex(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch,
                        unsigned int flags, qd_stream_t stream);
 

@@ -25,7 +25,7 @@ STATUS = {0: "QD_OK", 1: "QD_ERR_INVALID_ARG", 2: "QD_ERR_SHAPE", 3: "QD_ERR_ALI
 EXPORTS = ["qd_status_str", "qd_abi_version", "qd_f16_to_f32", "qd_bf16_to_f32", "qd_src_bytes", "qd_packed_bytes",
            "qd_repack", "qd_unpack", "qd_dequant", "qd_quantize_i8_rows", "qd_quantize_i4_rows",
            "qd_q_gemv_workspace", "qd_q_gemv",
-           "qd_q_gemv_ex", "qd_q_gemm_workspace", "qd_q_gemm", "qd_q8_bytes",
+           "qd_q_gemv_ex", "qd_read_ceiling", "qd_q_gemm_workspace", "qd_q_gemm", "qd_q8_bytes",
            "qd_quantize_q8", "qd_q_gemv_q8", "qd_rmsnorm",
            "qd_rope_table", "qd_rope", "qd_kv_append", "qd_gqa_decode_attn_workspace", "qd_gqa_decode_attn",
            "qd_gqa_decode_attn_noalloc",
@@ -82,6 +82,7 @@ def load():
         "qd_q_gemv_workspace": ([i32, i64, i64, i32], sz),
         "qd_q_gemv": ([i32, p, i64, i64, p, p, i32, p, sz, p], i32),
         "qd_q_gemv_ex": ([i32, p, i64, i64, p, p, i32, ctypes.c_uint, p], i32),
+        "qd_read_ceiling": ([p, sz, i32, i32, ctypes.c_uint, p, p], i32),
         "qd_q_gemm_workspace": ([i32, i64, i64, i32], sz),
         "qd_q_gemm": ([i32, p, i64, i64, p, p, i32, p, sz, p], i32),
         "qd_q8_bytes": ([i32, i64, i32], sz),
@@ -240,6 +241,12 @@ GEMV_OVERLAP = 1
 def q_gemv_ex(fmt, W, rows, cols, x, y, batch, flags=0, stream=None):
     _check("qd_q_gemv_ex", load().qd_q_gemv_ex(FMT[fmt], _ptr(W), rows, cols, _ptr(x), _ptr(y), batch, flags,
                                                _stream(stream)))
+
+
+def read_ceiling(buf, nbytes, ctas_per_sm, threads, flags=0, sink=None, stream=None):
+    """Roofline calibration: one plain read of nbytes of buf (see qd_read_ceiling)."""
+    _check("qd_read_ceiling", load().qd_read_ceiling(_ptr(buf), nbytes, ctas_per_sm, threads, flags, _ptr(sink),
+                                                     _stream(stream)))
 
 
 def rmsnorm(x, g, out, n, batch, eps, stream=None):

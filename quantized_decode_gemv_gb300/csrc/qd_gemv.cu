@@ -540,7 +540,52 @@ qd_status launch_q_gemv(const GemvArgs& a, cudaStream_t stream) {
 
 using namespace qd;
 
+namespace qd {
+namespace calib {
+
+// Roofline calibration: every 16-byte chunk of a buffer read once with streaming loads,
+// eight in flight per thread, nothing computed; each CTA reads one contiguous run.  The
+// sink word is written only by a CTA whose XOR of everything it read is a value that
+// random data does not give, which keeps the loads alive.  With `pdl` the kernel lets its
+// successor launch at once and waits for its predecessor only before that write, as a
+// GEMV waits before it reads x.
+__global__ void __launch_bounds__(512) k_read_ceiling(const uint4* __restrict__ p, int64_t n16, uint32_t* sink,
+                                                     int pdl) {
+  if (pdl) pdl_trigger();
+  const int64_t per = (n16 + gridDim.x - 1) / gridDim.x;
+  const int64_t b0 = (int64_t)blockIdx.x * per;
+  const int64_t b1 = b0 + per < n16 ? b0 + per : n16;
+  uint32_t acc = 0;
+  for (int64_t i = b0 + threadIdx.x; i < b1; i += 8 * (int64_t)blockDim.x) {
+    uint4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int64_t j = i + (int64_t)k * blockDim.x;
+      v[k] = j < b1 ? ld_stream_v4(p + j) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc ^= v[k].x ^ v[k].y ^ v[k].z ^ v[k].w;
+  }
+  if (pdl) pdl_wait();
+  if (acc == 0x9E3779B9u) atomicOr(sink, 1u);
+}
+
+}  // namespace calib
+}  // namespace qd
+
 extern "C" {
+
+qd_status qd_read_ceiling(const void* buf, size_t bytes, int ctas_per_sm, int threads, unsigned flags,
+                          uint32_t* sink, qd_stream_t stream) {
+  if (!buf || !sink || (flags & ~QD_GEMV_OVERLAP)) return QD_ERR_INVALID_ARG;
+  if (!aligned16(buf) || bytes % 16) return QD_ERR_ALIGN;
+  if (ctas_per_sm < 1 || ctas_per_sm > 8 || (threads != 128 && threads != 256 && threads != 512)) return QD_ERR_SHAPE;
+  if (bytes == 0) return QD_OK;
+  const int sms = attn_sm_count();
+  return launch_k(calib::k_read_ceiling, dim3((unsigned)(sms * ctas_per_sm)), dim3((unsigned)threads), 0,
+                  (cudaStream_t)stream, (flags & QD_GEMV_OVERLAP) != 0, static_cast<const uint4*>(buf),
+                  (int64_t)(bytes / 16), sink, (int)((flags & QD_GEMV_OVERLAP) != 0));
+}
 
 size_t qd_q_gemv_workspace(qd_fmt fmt, int64_t rows, int64_t cols, int batch) {
   (void)fmt;

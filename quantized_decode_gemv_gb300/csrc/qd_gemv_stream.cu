@@ -360,8 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
     }
     cp_commit();
   };
-#pragma unroll
-  for (int k = 0; k < kStages - 1; ++k) issue(k);
+  // One stage before the dependency wait (for the decode step's small products that is
+  // all of a warp's weights); the rest after x's first loads, which would otherwise queue
+  // behind the whole ring's copies (measured: ~2.5 us of prologue at 14336x4096 Q8_0).
+  issue(0);
 
   pdl_wait();  // x is the previous kernel's output
   EpiPrefetch pf;
@@ -374,11 +376,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
   float inv[NB];
   {
     const int k = lane & 7;
+    constexpr int kPass = kWarps * 4;  // units per pass of the CTA
+    constexpr int kBatch = 4;          // passes of a warp whose loads are issued together
+    auto load = [&](int b, int u, float4& v, float4& g) {
+      const bool ok = u < units;
+      const int e = k < 4 ? unit_xa<FMT>(u) + 4 * k : unit_xb<FMT>(u) + 4 * (k - 4);
+      const float* xr = p.x + (int64_t)b * cols;
+      v = ok ? __ldcg(reinterpret_cast<const float4*>(xr + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      g = ok && p.norm_g ? __ldg(reinterpret_cast<const float4*>(p.norm_g + e)) : make_float4(1.f, 1.f, 1.f, 1.f);
+    };
+    // this warp's first passes of batch row 0, loaded before the rest of the ring is issued
+    float4 v0[kBatch], g0[kBatch];
+#pragma unroll
+    for (int t = 0; t < kBatch; ++t) load(0, warp * 4 + t * kPass + (lane >> 3), v0[t], g0[t]);
+#pragma unroll
+    for (int s = 1; s < kStages - 1; ++s) issue(s);
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       float ss = 0.f;
       if (b < p.batch) {
-        const float* xr = p.x + (int64_t)b * cols;
         // one unit record from this lane's 4 elements v (gains g)
         auto record = [&](int u, bool ok, float4 v, float4 g) {
           if (p.norm_g) {
@@ -387,33 +403,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
           }
           intdot::write_record<FMT>(xq + ((size_t)b * units + u) * kRecBytes, k, ok, v);
         };
-        auto load = [&](int u, float4& v, float4& g) {
-          const bool ok = u < units;
-          const int e = k < 4 ? unit_xa<FMT>(u) + 4 * k : unit_xb<FMT>(u) + 4 * (k - 4);
-          v = ok ? __ldcg(reinterpret_cast<const float4*>(xr + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
-          g = ok && p.norm_g ? __ldg(reinterpret_cast<const float4*>(p.norm_g + e)) : make_float4(1.f, 1.f, 1.f, 1.f);
-        };
-        constexpr int kPass = kWarps * 4;  // units per pass of the CTA
-        if (units <= kPass) {
-          if (warp * 4 < units) {  // uniform per warp
-            const int u = warp * 4 + (lane >> 3);
-            float4 v, g;
-            load(u, v, g);
-            record(u, u < units, v, g);
-          }
-        } else {
-          // kBatch passes of this warp at once: their loads are issued before any is used
-          constexpr int kBatch = 4;
-          for (int ub0 = warp * 4; ub0 < units; ub0 += kBatch * kPass) {  // uniform per warp
-            float4 vv[kBatch], gg[kBatch];
-#pragma unroll
-            for (int t = 0; t < kBatch; ++t) load(ub0 + t * kPass + (lane >> 3), vv[t], gg[t]);
+        for (int ub0 = warp * 4; ub0 < units; ub0 += kBatch * kPass) {  // uniform per warp
+          float4 vv[kBatch], gg[kBatch];
+          if (b == 0 && ub0 == warp * 4) {
 #pragma unroll
             for (int t = 0; t < kBatch; ++t) {
-              if (ub0 + t * kPass >= units) break;  // uniform per warp
-              const int u = ub0 + t * kPass + (lane >> 3);
-              record(u, u < units, vv[t], gg[t]);
+              vv[t] = v0[t];
+              gg[t] = g0[t];
             }
+          } else {
+#pragma unroll
+            for (int t = 0; t < kBatch; ++t) load(b, ub0 + t * kPass + (lane >> 3), vv[t], gg[t]);
+          }
+#pragma unroll
+          for (int t = 0; t < kBatch; ++t) {
+            if (ub0 + t * kPass >= units) break;  // uniform per warp
+            const int u = ub0 + t * kPass + (lane >> 3);
+            record(u, u < units, vv[t], gg[t]);
           }
         }
       }
