@@ -507,10 +507,16 @@ qd_status launch_fmt(const PackedView& W, const float* x, float* y, int batch, i
 
 }  // namespace
 
+bool gemv_fuses_norm(const GemvArgs& a) { return gemv_mma_supported(a) || gemv_streams(a); }
+
 qd_status launch_q_gemv(const GemvArgs& a, cudaStream_t stream) {
-  // Batch 1-8 and the shapes it supports: the streaming kernel (it also fuses
-  // RMSNorm).  Otherwise the register-path kernel below (RMSNorm must then have been
-  // applied by the caller, see gemv_streams).
+  // Batch 3-8 (Q4_0, Q8_0, INT8 rows): the tensor-core kernel.  Batch 1-8 and the shapes
+  // it supports: the streaming kernel.  Both fuse RMSNorm.  Otherwise the register-path
+  // kernel below (RMSNorm must then have been applied by the caller, see gemv_fuses_norm).
+  {
+    const qd_status st = launch_q_gemv_mma(a, stream);
+    if (st != QD_ERR_UNSUPPORTED) return st;
+  }
   {
     const qd_status st = launch_q_gemv_stream(a, stream);
     if (st != QD_ERR_UNSUPPORTED) return st;

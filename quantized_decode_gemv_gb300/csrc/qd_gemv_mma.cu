@@ -1,0 +1,796 @@
+// q_gemv for batch 3-8 on the tensor cores (mma.sync, f16 inputs, f32 accumulate).
+//
+// y[b][r] = sum_c deq(W)[r][c] * x[b][c] (llmoxide blog s1, s10; dasLLAMA 8.7.1.4 matmul)
+// for a few batch rows is a skinny dense contraction, and on the CUDA cores its cost grows
+// with every batch row (the streaming kernel spends 24 dp4a per 32 weights per batch row:
+// 14336x4096 Q4_0 took 11 / 24 / 48 us at batch 1 / 4 / 8).  Here it runs on the tensor
+// cores without giving up the f32-activation contract:
+//
+//  * Weight codes are exact in binary16 (Q4_0 q - 8 in [-8, 7], Q8_0 / INT8 codes in
+//    [-127, 127]), turned into f16 pairs in registers with the exponent-bias trick (the
+//    code in the mantissa of 1024, then a subtraction).
+//  * x reaches shared memory by bulk copies (one per batch row, counted on an mbarrier),
+//    off the load path that the weight ring fills.  Each stage of 256 elements of every
+//    batch row is then scaled by a power of two s (its largest |x| rounded down to a power
+//    of two, so |x / s| < 2) and split in place into two binary16 parts, hi = f16(x / s)
+//    and lo = f16(x / s - hi): about 22 bits of x, relative error ~2^-22 of the stage's
+//    largest value (the batch-16 tensor-core GEMV uses the same split).  Products of f16
+//    values are exact and sum in f32.
+//  * mma.sync.m16n8k16 multiplies a 16-row tile of one unit's codes by the hi and lo parts
+//    of 8 batch columns, two K halves: four instructions per unit, chained through one
+//    accumulator.  The order of the 32 elements along K is free as long as A and B agree:
+//    lane t takes its A values from code word t (bytes 4t..4t+3) of each row, pairing
+//    bytes (0, 2) and (1, 3), so one 32-bit load and a few bit operations make its
+//    fragments, and x is staged in the same order.  A unit is one quantisation block, so
+//    the block scale d multiplies its f32 sums into a stage accumulator, and the stage's
+//    x scale multiplies that into the tile's (INT8 rows, one scale a row, need neither
+//    until the epilogue).  (GB300's int8 tensor path is ~4x slower than f16 here: 150
+//    against 590 TOPS measured for mma.sync.)
+//  * Weights stream as in the streaming kernel: every warp owns 16-row tiles taken round-
+//    robin over the grid's warps, and copies its stages (16 rows x 8 units of codes and
+//    scales, rows padded so that the fragment loads hit distinct banks) with per-lane
+//    cp.async into a ring in shared memory, no CTA barrier in the main loop; the ring's
+//    first stages are issued before the dependency wait.
+//  * Rows of x wider than the shared memory holds (store and accumulate only) run as
+//    several launches over column ranges, the first storing and the rest accumulating:
+//    the sums still follow one fixed order.
+//  * Epilogues: store, accumulate, SwiGLU over interleaved (gate, up) rows, the QKV
+//    epilogue (RoPE pairs, cache append) and the fused argmax, as the streaming kernel.
+#include "qd_intdot.cuh"
+#include "qd_tc.cuh"
+
+namespace qd {
+namespace mma_gemv {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTileRows = 16;
+constexpr int kStageUnits = 8;  // units (32 columns each) per ring stage and per x scale
+constexpr int kStageCols = kStageUnits * 32;
+constexpr int kXPad = 64;  // bytes after each staged x row: rows 2j, 2j + 1 on disjoint banks
+
+struct Params {
+  PackedView W;  // the column range's codes and scales start at unit u0
+  const float* x;
+  float* y;
+  const float* norm_g;
+  float eps;
+  int batch;
+  int mode;
+  uint32_t* err;
+  QkvEpilogue qkv;
+  ArgmaxEpilogue am;
+  int64_t x_stride;  // floats between batch rows of x
+  int u0;            // first unit (32 columns) of the range
+  int units;         // units in the range
+  int stages;        // ring depth (slots per warp), sized to the shared memory left
+  int ks;            // warps that share one tile, each over a contiguous part of its columns
+  bool accumulate;   // a later column range: y += partial product (store mode's chunks)
+};
+
+template <int FMT>
+constexpr int code_bytes() {
+  return FMT == QD_Q4_0 ? 16 : 32;
+}
+// a ring slot: codes [16 rows][row stride] (8 units a row, padded by 16 bytes so that the
+// 8 rows a fragment load touches fall on different banks), then f16 scales [16][8]
+template <int FMT>
+constexpr int row_stride() {
+  return kStageUnits * code_bytes<FMT>() + 16;
+}
+template <int FMT>
+constexpr int scale_bytes() {
+  return FMT == QD_I8_ROW ? 0 : kTileRows * kStageUnits * 2;
+}
+template <int FMT>
+constexpr int slot_bytes() {
+  return kTileRows * row_stride<FMT>() + scale_bytes<FMT>();
+}
+// per-warp partial accumulators for the column split, two tiles deep
+constexpr int kPartialBytes = 2 * kWarps * 32 * 4 * 4;
+
+// Shared-memory layout of one launch (byte offsets; every part 16-byte aligned).
+struct Layout {
+  size_t ring, xs, gs, sx, ssq, partial, bar, total;
+  int64_t x_row;  // bytes between staged batch rows
+};
+template <int FMT>
+__host__ __device__ inline Layout layout(int units, int batch, bool norm, int stages) {
+  Layout L;
+  const int nst = (units + kStageUnits - 1) / kStageUnits;
+  L.x_row = (int64_t)units * 128 + kXPad;
+  L.ring = 0;
+  L.xs = L.ring + (size_t)kWarps * stages * slot_bytes<FMT>();
+  L.gs = L.xs + (size_t)batch * L.x_row;
+  L.sx = L.gs + (norm ? (size_t)units * 128 : 0);
+  L.ssq = L.sx + (size_t)nst * 8 * 4;
+  L.partial = L.ssq + (size_t)nst * 8 * 4;
+  L.bar = L.partial + kPartialBytes;
+  L.total = L.bar + 16;
+  return L;
+}
+
+template <int N>
+__device__ __forceinline__ void cp_wait_n() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// cp.async.wait_group with a run-time count (the ring depth minus one, 1..7)
+__device__ __forceinline__ void cp_wait_dyn(int n) {
+  switch (n) {
+    case 1: cp_wait_n<1>(); break;
+    case 2: cp_wait_n<2>(); break;
+    case 3: cp_wait_n<3>(); break;
+    case 4: cp_wait_n<4>(); break;
+    case 5: cp_wait_n<5>(); break;
+    case 6: cp_wait_n<6>(); break;
+    default: cp_wait_n<7>(); break;
+  }
+}
+
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// D = A (16x16, row) * B (16x8, col) + D over binary16 into f32.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+               "{%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t w) { return *reinterpret_cast<const __half2*>(&w); }
+
+// One Q4_0 code word (bytes 4t..4t+3 of a block: low nibbles are elements 4t..4t+3, high
+// nibbles elements 16 + 4t..) as f16 pairs q - 8: k0 = elements (4t, 4t + 2), k0b =
+// (4t + 1, 4t + 3); k1, k1b the same for the high nibbles.  A nibble in the low bits of
+// 1024's mantissa gives 1024 + n; one in bits 4-7 gives 1024 + 16n, scaled by 1/16.
+__device__ __forceinline__ void q4_word(uint32_t w, uint32_t& k0, uint32_t& k0b, uint32_t& k1, uint32_t& k1b) {
+  const __half2 c1032 = __floats2half2_rn(1032.f, 1032.f);
+  const __half2 s16 = __floats2half2_rn(0.0625f, 0.0625f), c72 = __floats2half2_rn(-72.f, -72.f);
+  const uint32_t w8 = w >> 8;
+  k0 = h2_bits(__hsub2(bits_h2((w & 0x000F000Fu) | 0x64006400u), c1032));
+  k0b = h2_bits(__hsub2(bits_h2((w8 & 0x000F000Fu) | 0x64006400u), c1032));
+  k1 = h2_bits(__hfma2(bits_h2((w & 0x00F000F0u) | 0x64006400u), s16, c72));
+  k1b = h2_bits(__hfma2(bits_h2((w8 & 0x00F000F0u) | 0x64006400u), s16, c72));
+}
+// One word of signed byte codes (elements 4t..4t+3) as f16 pairs: k = (4t, 4t + 2), kb =
+// (4t + 1, 4t + 3).  q ^ 0x80 is q + 128 in 0..255: 1024 + q + 128, minus 1152.
+__device__ __forceinline__ void i8_word(uint32_t w, uint32_t& k, uint32_t& kb) {
+  const __half2 c1152 = __floats2half2_rn(1152.f, 1152.f);
+  const uint32_t u = w ^ 0x80808080u;
+  k = h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, 0x4240u)), c1152));
+  kb = h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, 0x4341u)), c1152));
+}
+
+// 2^e for e in [-127, 127] (2^-127 is subnormal)
+__device__ __forceinline__ float pow2i(int e) {
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// The QKV epilogue for one (even row r, row r + 1) pair of batch row b: a RoPE pair of q
+// or k (rotated; q to q_out, k to the cache at pos[b]) or two consecutive v values.
+__device__ __forceinline__ void qkv_pair(const Params& p, int64_t r, int b, float a, float bb) {
+  const QkvEpilogue& e = p.qkv;
+  const int pos = __ldcg(e.pos + b);
+  if (pos < 0 || pos >= e.max_ctx) {
+    if (p.err) atomicOr(p.err, kErrPosition);
+    return;
+  }
+  const int hd = e.head_dim, half = hd / 2;
+  if (r < e.q_rows + e.k_rows) {
+    const bool isq = r < e.q_rows;
+    const int64_t local = isq ? r : r - e.q_rows;
+    const int64_t h = local / hd;
+    const int pi = (int)(local % hd) / 2;
+    const int d0 = e.pairing == QD_ROPE_HALF ? pi : 2 * pi;
+    const int d1 = e.pairing == QD_ROPE_HALF ? pi + half : 2 * pi + 1;
+    const float2 cs = __ldg(reinterpret_cast<const float2*>(e.rope + ((int64_t)pos * half + pi) * 2));
+    const float o0 = a * cs.x - bb * cs.y, o1 = a * cs.y + bb * cs.x;
+    if (isq) {
+      float* dst = e.q_out + (int64_t)b * e.q_stride + h * hd;
+      dst[d0] = o0;
+      dst[d1] = o1;
+    } else {
+      const int64_t row = (int64_t)b * e.cache_batch_stride + (h * e.max_ctx + pos) * hd;
+      cache_store(e.kc, e.kv_f16, row + d0, o0);
+      cache_store(e.kc, e.kv_f16, row + d1, o1);
+    }
+  } else {
+    const int64_t local = r - e.q_rows - e.k_rows;
+    const int64_t h = local / hd;
+    const int d = (int)(local % hd);
+    const int64_t row = (int64_t)b * e.cache_batch_stride + (h * e.max_ctx + pos) * hd;
+    cache_store(e.vc, e.kv_f16, row + d, a);
+    cache_store(e.vc, e.kv_f16, row + d + 1, bb);
+  }
+}
+
+// One unit's product on the tensor cores: rows g, g + 8 of the 16-row tile (codes at
+// `row0` and `row8` in the ring slot) times the hi and lo fragments of x at `xu`, the lo
+// parts first; d = the unit's f32 sums for (row g, column 2t), (g, 2t + 1), (g + 8, 2t),
+// (g + 8, 2t + 1).
+template <int FMT>
+__device__ __forceinline__ void unit_mma(float (&d)[4], const uint8_t* row0, const uint8_t* row8, const uint8_t* xu,
+                                         int t) {
+  uint32_t a0[4], a1[4];  // K halves 0 and 1: rows (g, g + 8) x pairs ((4t, 4t+2), (4t+1, 4t+3))
+  if constexpr (FMT == QD_Q4_0) {
+    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(row0 + 4 * t);
+    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(row8 + 4 * t);
+    q4_word(w0, a0[0], a0[2], a1[0], a1[2]);
+    q4_word(w1, a0[1], a0[3], a1[1], a1[3]);
+  } else {
+    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(row0 + 4 * t);
+    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(row8 + 4 * t);
+    const uint32_t x0 = *reinterpret_cast<const uint32_t*>(row0 + 16 + 4 * t);
+    const uint32_t x1 = *reinterpret_cast<const uint32_t*>(row8 + 16 + 4 * t);
+    i8_word(w0, a0[0], a0[2]);
+    i8_word(w1, a0[1], a0[3]);
+    i8_word(x0, a1[0], a1[2]);
+    i8_word(x1, a1[1], a1[3]);
+  }
+  // (hi b0, hi b1, lo b0, lo b1) of the two K halves
+  const uint4 v0 = *reinterpret_cast<const uint4*>(xu + 16 * t);
+  const uint4 v1 = *reinterpret_cast<const uint4*>(xu + 64 + 16 * t);
+  mma_f16(d, a0, v0.z, v0.w);
+  mma_f16(d, a1, v1.z, v1.w);
+  mma_f16(d, a0, v0.x, v0.y);
+  mma_f16(d, a1, v1.x, v1.y);
+}
+
+// The f16 block scale of unit uu (0..7) from a row's 8 scales held as 4 words.
+__device__ __forceinline__ float scale_of(const uint4& s, int uu) {
+  const uint32_t w = (uu >> 1) == 0 ? s.x : (uu >> 1) == 1 ? s.y : (uu >> 1) == 2 ? s.z : s.w;
+  const float2 f = __half22float2(bits_h2(w));
+  return (uu & 1) ? f.y : f.x;
+}
+
+// One ring stage of `NU` units (NU = 8, or 0: `nu` units known at run time) into the
+// stage accumulator `as`: block-scaled formats scale each unit's sums by the rows' block
+// scales d; INT8 rows keep unit-interleaved MMA chains and add them at the end.
+template <int FMT, int NU>
+__device__ __forceinline__ void stage_mma(float (&as)[4], const uint8_t* slot, const uint8_t* xst, int g, int t,
+                                          int nu) {
+  constexpr int CB = code_bytes<FMT>();
+  constexpr int RS = row_stride<FMT>();
+  const uint8_t* row0 = slot + g * RS;
+  const uint8_t* row8 = row0 + 8 * RS;
+  if constexpr (FMT == QD_I8_ROW) {
+    float c[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
+    if constexpr (NU > 0) {
+#pragma unroll
+      for (int uu = 0; uu < NU; ++uu) unit_mma<FMT>(c[uu & 3], row0 + uu * CB, row8 + uu * CB, xst + uu * 128, t);
+    } else {
+      int uu = 0;
+      for (; uu + 1 < nu; uu += 2) {
+        unit_mma<FMT>(c[0], row0 + uu * CB, row8 + uu * CB, xst + uu * 128, t);
+        unit_mma<FMT>(c[1], row0 + (uu + 1) * CB, row8 + (uu + 1) * CB, xst + (uu + 1) * 128, t);
+      }
+      if (uu < nu) unit_mma<FMT>(c[2], row0 + uu * CB, row8 + uu * CB, xst + uu * 128, t);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) as[i] = (c[0][i] + c[1][i]) + (c[2][i] + c[3][i]);
+  } else {
+    // the block scales of rows g and g + 8 for the stage's 8 units (f16, 16 bytes a row)
+    const uint8_t* scs = slot + kTileRows * RS;
+    const uint4 s0 = *reinterpret_cast<const uint4*>(scs + g * 16);
+    const uint4 s8 = *reinterpret_cast<const uint4*>(scs + (g + 8) * 16);
+    auto one = [&](int uu) {
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      unit_mma<FMT>(d, row0 + uu * CB, row8 + uu * CB, xst + uu * 128, t);
+      const float d0 = scale_of(s0, uu), d8 = scale_of(s8, uu);
+      as[0] = fmaf(d0, d[0], as[0]);
+      as[1] = fmaf(d0, d[1], as[1]);
+      as[2] = fmaf(d8, d[2], as[2]);
+      as[3] = fmaf(d8, d[3], as[3]);
+    };
+    if constexpr (NU > 0) {
+#pragma unroll
+      for (int uu = 0; uu < NU; ++uu) one(uu);
+    } else {
+      for (int uu = 0; uu < nu; ++uu) one(uu);  // block formats: nu is even
+    }
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int CB = code_bytes<FMT>();
+  constexpr int RS = row_stride<FMT>();
+  constexpr int kSlot = slot_bytes<FMT>();
+  const int kStages = p.stages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;  // mma fragment: row group, thread in group
+  const PackedView& W = p.W;
+  const int units = p.units;
+  const int nst = (units + kStageUnits - 1) / kStageUnits;  // stages per tile
+  const bool norm = p.norm_g != nullptr;
+  const Layout L = layout<FMT>(units, p.batch, norm, kStages);
+  const int64_t tiles = (W.rows + kTileRows - 1) / kTileRows;
+  // the KS warps of a group share each of the group's tiles; warp ks of the group takes
+  // the tile's stages [st0, st1); groups take tiles round-robin over the grid
+  const int KS = p.ks, grp = warp / KS, ks = warp % KS;
+  const int st0 = ks * nst / KS, st1 = (ks + 1) * nst / KS;
+  const int64_t gslot = (int64_t)grp * gridDim.x + blockIdx.x, ngs = (int64_t)gridDim.x * (kWarps / KS);
+  uint8_t* ring = smem + L.ring + (size_t)warp * kStages * kSlot;
+  const uint32_t ring_s = tc::smem_u32(ring);
+  uint8_t* xs = smem + L.xs;
+  const float* gs = reinterpret_cast<const float*>(smem + L.gs);
+  float* sxs = reinterpret_cast<float*>(smem + L.sx);   // [stage][8] x scales
+  float* ssq = reinterpret_cast<float*>(smem + L.ssq);  // [stage][8] sums of squares
+  float* partial = reinterpret_cast<float*>(smem + L.partial);  // [2][warps][32][4]
+  const uint32_t bar = tc::smem_u32(smem + L.bar);
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  // ---- ring: stage s of a tile = units [8s, 8s + 8) of its 16 rows.  Lane l copies the
+  // 16-byte code chunk l % kPerRow of rows l / kPerRow + i * kRowsPerPass and the 4-byte
+  // scale word (unit pair l % 4) of rows l / 4 and l / 4 + 8; the source rows of a tile are
+  // set up once per tile (clamped to the last row for a ragged tile)
+  constexpr int kPerRow = kStageUnits * CB / 16;  // 16-byte chunks per row and stage
+  constexpr int kRowsPerPass = 32 / kPerRow;
+  constexpr int kChunks = kTileRows / kRowsPerPass;  // code chunks per lane and stage
+  const int crow = lane / kPerRow, crem = lane % kPerRow, cunit = crem / (CB / 16);
+  const int srow = lane >> 2, spr = lane & 3;
+  int64_t lt = gslot;  // tile of the next copy
+  int ls = st0;        // its stage
+  const uint8_t* cptr[kChunks];
+  const uint8_t* sptr[2];
+  auto tile_ptrs = [&]() {
+#pragma unroll
+    for (int i = 0; i < kChunks; ++i) {
+      const int64_t r = min(lt * kTileRows + crow + i * kRowsPerPass, W.rows - 1);
+      cptr[i] = W.codes + r * W.row_code_bytes + (int64_t)p.u0 * CB + 16 * crem;
+    }
+    if constexpr (scale_bytes<FMT>() > 0) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int64_t r = min(lt * kTileRows + srow + 8 * j, W.rows - 1);
+        sptr[j] = W.scales + r * W.row_scale_bytes + (int64_t)(p.u0 + 2 * spr) * 2;
+      }
+    }
+  };
+  if (lt < tiles) tile_ptrs();
+  auto issue = [&](int slot_idx) {
+    if (lt < tiles && st1 > st0) {
+      const uint32_t slot = ring_s + (uint32_t)slot_idx * kSlot;
+      const int u0 = ls * kStageUnits;
+      if (u0 + cunit < units) {
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i)
+          cp16(slot + (uint32_t)((crow + i * kRowsPerPass) * RS + 16 * crem), cptr[i] + (int64_t)u0 * CB);
+      }
+      if constexpr (scale_bytes<FMT>() > 0) {
+        // units come in pairs (even unit counts)
+        if (u0 + 2 * spr < units) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            cp4(slot + (uint32_t)(kTileRows * RS + ((srow + 8 * j) * kStageUnits + 2 * spr) * 2), sptr[j] + u0 * 2);
+        }
+      }
+      if (++ls == st1) {
+        ls = st0;
+        lt += ngs;
+        if (lt < tiles) tile_ptrs();
+      }
+    }
+    cp_commit();
+  };
+
+  // ---- before the dependency wait: the norm gains (a weight) by bulk copy and the
+  // ring's first kStages - 1 stages; neither depends on the previous kernel
+  const uint32_t row_bytes = (uint32_t)units * 128u;
+  if (threadIdx.x == 0) {
+    tc::mbar_arrive_expect_tx(bar, row_bytes * (uint32_t)(p.batch + (norm ? 1 : 0)));
+    if (norm) tc::bulk_copy_g2s(tc::smem_u32(smem + L.gs), p.norm_g + (int64_t)p.u0 * 32, row_bytes, bar);
+  }
+  for (int s = 0; s < kStages - 1; ++s) issue(s);
+
+  pdl_wait();  // x (and y, for accumulation) belong to the previous kernel
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < p.batch; ++b)
+      tc::bulk_copy_g2s(tc::smem_u32(xs + b * L.x_row), p.x + b * p.x_stride + (int64_t)p.u0 * 32, row_bytes, bar);
+  }
+  for (int i = threadIdx.x; i < nst * 8; i += kThreads) {
+    if ((i & 7) >= p.batch) sxs[i] = ssq[i] = 0.f;  // columns without a batch row
+  }
+  if (!__syncthreads_and(tc::mbar_wait_sleep(bar, 0))) {
+    // the copies did not land in time: report it, give them one more bounded wait (they
+    // target this CTA's shared memory), drain the ring and leave
+    if (threadIdx.x == 0 && p.err) atomicOr(p.err, kErrTimeout);
+    tc::mbar_wait_sleep(bar, 0);
+    cp_wait_n<0>();
+    return;
+  }
+
+  // ---- x in place: warp w converts stages w, w + 8, ... for all 8 batch rows at once, as
+  // straight-line code (rows past the batch convert zeros and store nothing), so the rows'
+  // loads and dependency chains overlap.  Lane l holds elements 8l..8l+7 of the stage
+  // (unit l / 4, K half (l % 4) / 2): two 16-byte halves, each the four elements of one
+  // fragment thread (2 (l % 2) and 2 (l % 2) + 1), rewritten in place as that thread's
+  // (hi b0, hi b1, lo b0, lo b1).  Lanes 4-7 of each quarter take their second half
+  // first: the eight lanes of a 128-bit access then cover all 32 banks once.
+  {
+    const int h = (lane >> 2) & 1;
+    for (int s = warp; s < nst; s += kWarps) {
+      const int e0 = s * kStageCols + 8 * lane;
+      const bool in = e0 < units * 32;
+      uint8_t* sbase = xs + (int64_t)s * kStageCols * 4 + 32 * lane;
+      float v[8][8];  // [row][half h's 4 elements, then the other half's]
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0;
+        if (b < p.batch && in) {
+          const float4* px = reinterpret_cast<const float4*>(sbase + b * L.x_row);
+          q0 = px[h];
+          q1 = px[h ^ 1];
+        }
+        v[b][0] = q0.x, v[b][1] = q0.y, v[b][2] = q0.z, v[b][3] = q0.w;
+        v[b][4] = q1.x, v[b][5] = q1.y, v[b][6] = q1.z, v[b][7] = q1.w;
+      }
+      float ss[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (norm) {
+        float gv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (in) {
+          const float4 g0 = *reinterpret_cast<const float4*>(gs + e0 + 4 * h);
+          const float4 g1 = *reinterpret_cast<const float4*>(gs + e0 + 4 * (h ^ 1));
+          gv[0] = g0.x, gv[1] = g0.y, gv[2] = g0.z, gv[3] = g0.w, gv[4] = g1.x, gv[5] = g1.y, gv[6] = g1.z, gv[7] = g1.w;
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+#pragma unroll
+          for (int j2 = 0; j2 < 8; ++j2) {
+            ss[b] = fmaf(v[b][j2], v[b][j2], ss[b]);
+            v[b][j2] *= gv[j2];
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+          for (int b = 0; b < 8; ++b) ss[b] += __shfl_xor_sync(0xffffffffu, ss[b], o);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        // the stage scale: 2^e with the largest |x| in [2^e, 2^(e+1)); magnitude bits
+        // order like the values, and inf / NaN sit above every finite one
+        uint32_t mb = 0;
+#pragma unroll
+        for (int j2 = 0; j2 < 8; ++j2) mb = max(mb, __float_as_uint(v[b][j2]) & 0x7FFFFFFFu);
+        mb = __reduce_max_sync(0xffffffffu, mb);
+        const bool bad = mb >= 0x7F800000u, live = mb != 0u;
+        const int e = (int)(mb >> 23) - 127;
+        const float rs = live && !bad ? pow2i(-e) : 0.f;
+        float4 fr[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {  // the two halves, each one fragment thread's elements
+          const float y0 = v[b][4 * k] * rs, y1 = v[b][4 * k + 1] * rs;
+          const float y2 = v[b][4 * k + 2] * rs, y3 = v[b][4 * k + 3] * rs;
+          const __half2 h0 = __floats2half2_rn(y0, y2), h1 = __floats2half2_rn(y1, y3);
+          const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+          const __half2 l0 = __floats2half2_rn(y0 - f0.x, y2 - f0.y), l1 = __floats2half2_rn(y1 - f1.x, y3 - f1.y);
+          fr[k] = make_float4(__uint_as_float(h2_bits(h0)), __uint_as_float(h2_bits(h1)), __uint_as_float(h2_bits(l0)),
+                              __uint_as_float(h2_bits(l1)));
+        }
+        if (b < p.batch) {
+          if (in) {
+            float4* px = reinterpret_cast<float4*>(sbase + b * L.x_row);
+            px[h] = fr[0];
+            px[h ^ 1] = fr[1];
+          }
+          if (lane == 0) {
+            sxs[s * 8 + b] = bad ? __uint_as_float(0x7FC00000u) : live ? pow2i(e) : 0.f;
+            ssq[s * 8 + b] = ss[b];
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // RMSNorm factors of this lane's columns 2t, 2t + 1 (stage sums in stage order: every
+  // CTA forms the same value)
+  float inv[2] = {1.f, 1.f};
+  if (norm) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float tt = 0.f;
+      for (int s = 0; s < nst; ++s) tt += ssq[s * 8 + 2 * t + j];
+      inv[j] = 1.0f / sqrtf(tt / (float)(units * 32) + p.eps);
+    }
+  }
+  pdl_trigger();
+
+  // this lane's B column: batch row g, or (no such row) the last staged one, whose sums
+  // land in a column the epilogue never stores
+  const uint8_t* xrow = xs + min(g, p.batch - 1) * L.x_row;
+  unsigned long long best[2] = {0ull, 0ull};  // argmax keys of columns 2t, 2t + 1
+  float acc[4];
+  int cs = 0, it = 0;
+  for (int64_t tl = gslot; tl < tiles; tl += ngs, ++it) {  // uniform over the group
+    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    for (int st = st0; st < st1; ++st) {
+      __syncwarp();
+      issue(cs == 0 ? kStages - 1 : cs - 1);
+      cp_wait_dyn(kStages - 1);
+      __syncwarp();
+      const uint8_t* slot = ring + (size_t)cs * kSlot;
+      const uint8_t* xst = xrow + (size_t)st * kStageCols * 4;
+      const int nu = min(kStageUnits, units - st * kStageUnits);
+      float as[4] = {0.f, 0.f, 0.f, 0.f};
+      if (nu == kStageUnits) stage_mma<FMT, kStageUnits>(as, slot, xst, g, t, nu);
+      else stage_mma<FMT, 0>(as, slot, xst, g, t, nu);
+      // the stage's x scales of columns 2t, 2t + 1
+      const float2 sx = *reinterpret_cast<const float2*>(sxs + st * 8 + 2 * t);
+      acc[0] = fmaf(sx.x, as[0], acc[0]);
+      acc[1] = fmaf(sx.y, as[1], acc[1]);
+      acc[2] = fmaf(sx.x, as[2], acc[2]);
+      acc[3] = fmaf(sx.y, as[3], acc[3]);
+      cs = (cs + 1 == kStages) ? 0 : cs + 1;
+    }
+    if (KS > 1) {
+      // the group's column parts, summed in part order by its first warp
+      float* pt = partial + (size_t)(it & 1) * kWarps * 128;
+      *reinterpret_cast<float4*>(pt + (warp * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(KS * 32) : "memory");
+      if (ks != 0) continue;  // uniform per warp
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+      for (int k = 0; k < KS; ++k) {
+        const float4 q = *reinterpret_cast<const float4*>(pt + ((grp * KS + k) * 32 + lane) * 4);
+        acc[0] += q.x;
+        acc[1] += q.y;
+        acc[2] += q.z;
+        acc[3] += q.w;
+      }
+    }
+    // ---- end of a tile (first warp of the group): rows tile + g, + 8; columns 2t, 2t + 1
+    const int64_t rbase = tl * kTileRows;
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t r = rbase + g + (i >= 2 ? 8 : 0);
+      float s = inv[i & 1];
+      if constexpr (FMT == QD_I8_ROW)
+        s *= __ldg(reinterpret_cast<const float*>(W.scales + min(r, W.rows - 1) * W.row_scale_bytes));
+      v[i] = acc[i] * s;
+    }
+    // the next row's values (row g + 1 is lane + 4) for the pair epilogues
+    float nx[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) nx[i] = __shfl_down_sync(0xffffffffu, v[i], 4);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t r = rbase + g + (i >= 2 ? 8 : 0);
+      const int b = 2 * t + (i & 1);
+      if (b >= p.batch || r >= W.rows) continue;
+      if (p.mode == kGemvSwiGLU) {
+        if ((g & 1) == 0 && r + 1 < W.rows) p.y[(int64_t)b * (W.rows / 2) + r / 2] = v[i] / (1.0f + expf(-v[i])) * nx[i];
+      } else if (p.mode == kGemvQKV) {
+        if ((g & 1) == 0 && r + 1 < W.rows) qkv_pair(p, r, b, v[i], nx[i]);
+      } else {
+        float* dst = p.y + (int64_t)b * W.rows + r;
+        if (p.mode == kGemvAccumulate || p.accumulate) *dst = __ldcg(dst) + v[i];
+        else *dst = v[i];
+        if (p.mode == kGemvArgmax) {
+          const unsigned long long key = argmax_key(v[i], (uint32_t)r);
+          best[i & 1] = key > best[i & 1] ? key : best[i & 1];
+        }
+      }
+    }
+  }
+  cp_wait_n<0>();  // no copy may still target this CTA's shared memory at exit
+  if (p.mode == kGemvArgmax) {
+    // per batch column: max over the lanes holding it (same t), one atomicMax per warp;
+    // the last CTA to arrive finalises the tokens and re-arms keys and counter
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      unsigned long long kk = best[j];
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, kk, off);
+        kk = o > kk ? o : kk;
+      }
+      const int b = 2 * t + j;
+      if (g == 0 && kk != 0 && b < p.batch) atomicMax(p.am.key + b, kk);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned int old;
+      asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.am.counter) : "memory");
+      if (old == gridDim.x - 1) {
+        for (int b = 0; b < p.batch; ++b) {
+          const unsigned long long kk = atomicExch(p.am.key + b, 0ull);
+          p.am.tok_out[b] = (int32_t)argmax_key_index(kk);
+          p.am.pos[b] += 1;
+        }
+        *p.am.counter = 0u;
+      }
+    }
+  }
+}
+
+
+constexpr size_t kSmemCap = 220 * 1024;
+
+int sm_count() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      v <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  return v;
+}
+
+template <int FMT>
+bool smem_attr_set() {
+  static bool done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (!done[dev]) {
+    if (cudaFuncSetAttribute(k_gemv_mma<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    done[dev] = true;
+  }
+  return true;
+}
+
+bool fmt_taken(int fmt) { return fmt == QD_Q4_0 || fmt == QD_Q8_0 || fmt == QD_I8_ROW; }
+
+size_t smem_for(int fmt, int units, int batch, bool norm, int stages) {
+  switch (fmt) {
+    case QD_Q4_0: return layout<QD_Q4_0>(units, batch, norm, stages).total;
+    case QD_Q8_0: return layout<QD_Q8_0>(units, batch, norm, stages).total;
+    default: return layout<QD_I8_ROW>(units, batch, norm, stages).total;
+  }
+}
+
+// Ring depth: the deepest (up to 8 slots a warp) that fits the shared memory; 0: none does.
+int stages_for(int fmt, int units, int batch, bool norm) {
+  for (int s = 8; s >= 2; --s)
+    if (smem_for(fmt, units, batch, norm, s) <= kSmemCap) return s;
+  return 0;
+}
+
+// Ring stages a column range is sized for: about 64 KB of weights in flight per SM.
+int ring_floor(int fmt) {
+  const int slot = fmt == QD_Q4_0 ? slot_bytes<QD_Q4_0>() : fmt == QD_Q8_0 ? slot_bytes<QD_Q8_0>() : slot_bytes<QD_I8_ROW>();
+  return max(2, (65536 + kWarps * slot - 1) / (kWarps * slot));
+}
+
+// Units per column range: all of them when x fits beside a ring of two stages or more;
+// otherwise the widest multiple of a stage that leaves room for ring_floor stages.
+int range_units(int fmt, int units, int batch, bool norm) {
+  if (stages_for(fmt, units, batch, norm) >= 2) return units;
+  const int floor_st = ring_floor(fmt);
+  int ru = (units / kStageUnits) * kStageUnits;
+  while (ru > kStageUnits && smem_for(fmt, ru, batch, norm, floor_st) > kSmemCap) ru -= kStageUnits;
+  return smem_for(fmt, ru, batch, norm, floor_st) <= kSmemCap ? ru : 0;
+}
+
+// Warps per tile (1, 2 or 4): the fewest rounds of stages on the busiest warp, counting the
+// CTAs the grid can hold (a small extra cost per split for the partial sums).
+int ks_for(int64_t tiles, int nst, int sms) {
+  int best = 1;
+  double best_cost = 1e30;
+  for (int ks : {1, 2, 4}) {
+    const int64_t groups_per_cta = kWarps / ks;
+    int64_t ctas = (tiles + groups_per_cta - 1) / groups_per_cta;
+    if (ctas > sms) ctas = sms;
+    const int64_t rounds = (tiles + ctas * groups_per_cta - 1) / (ctas * groups_per_cta);
+    const double cost = (double)rounds * ((nst + ks - 1) / ks) * (1.0 + 0.05 * (ks - 1));
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = ks;
+    }
+  }
+  return best;
+}
+
+// One launch over the column range [p.u0, p.u0 + p.units).
+template <int FMT>
+qd_status launch_range(Params p, bool pdl, cudaStream_t stream) {
+  const int64_t tiles = (p.W.rows + kTileRows - 1) / kTileRows;
+  const int nst = (p.units + kStageUnits - 1) / kStageUnits;
+  const int sms = sm_count();
+  const bool norm = p.norm_g != nullptr;
+  p.stages = stages_for(FMT, p.units, p.batch, norm);
+  if (p.stages < 2) return QD_ERR_UNSUPPORTED;
+  p.ks = ks_for(tiles, nst, sms);
+  const int64_t groups_per_cta = kWarps / p.ks;
+  int64_t ctas = (tiles + groups_per_cta - 1) / groups_per_cta;
+  if (ctas > sms) ctas = sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = layout<FMT>(p.units, p.batch, norm, p.stages).total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_gemv_mma<FMT>, p) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
+}
+
+// All column ranges in order: the first stores (or accumulates, in accumulate mode), the
+// rest accumulate, each a programmatic dependent of the one before.
+template <int FMT>
+qd_status launch(Params p, bool pdl, cudaStream_t stream) {
+  if (!smem_attr_set<FMT>()) return QD_ERR_CUDA;
+  const int units = (int)(p.W.cols / 32);
+  const int ru = range_units(FMT, units, p.batch, p.norm_g != nullptr);
+  if (ru <= 0) return QD_ERR_UNSUPPORTED;
+  for (int u0 = 0; u0 < units; u0 += ru) {
+    p.u0 = u0;
+    p.units = min(ru, units - u0);
+    p.accumulate = u0 > 0;
+    const qd_status st = launch_range<FMT>(p, u0 > 0 || pdl, stream);
+    if (st != QD_OK) return st;
+  }
+  return QD_OK;
+}
+
+}  // namespace mma_gemv
+
+// Batch 3-8, Q4_0 / Q8_0 / INT8 rows, even unit counts for the block formats (4-byte scale
+// copies), x and norm_g on 16-byte boundaries (bulk copies); x of every batch row beside a
+// ring of two stages in shared memory, or (store and accumulate without RMSNorm) split
+// into column ranges that fit.
+bool gemv_mma_supported(const GemvArgs& a) {
+  using namespace mma_gemv;
+  if (!fmt_taken(a.fmt) || a.batch < 3 || a.batch > 8 || a.W.cols % 32 || a.W.cols > (1 << 22)) return false;
+  if (reinterpret_cast<uintptr_t>(a.x) & 15) return false;
+  if (a.norm_g && (reinterpret_cast<uintptr_t>(a.norm_g) & 15)) return false;
+  const int units = (int)(a.W.cols / 32);
+  if ((a.fmt == QD_Q4_0 || a.fmt == QD_Q8_0) && (units & 1)) return false;
+  if (a.mode == kGemvSwiGLU || a.mode == kGemvQKV) {
+    if (a.W.rows & 1) return false;
+  }
+  if (stages_for(a.fmt, units, a.batch, a.norm_g != nullptr) >= 2) return true;
+  const bool splits = (a.mode == kGemvStore || a.mode == kGemvAccumulate) && !a.norm_g;
+  return splits && range_units(a.fmt, units, a.batch, false) > 0;
+}
+
+qd_status launch_q_gemv_mma(const GemvArgs& a, cudaStream_t stream) {
+  using namespace mma_gemv;
+  if (!gemv_mma_supported(a)) return QD_ERR_UNSUPPORTED;
+  Params p;
+  p.W = a.W;
+  p.x = a.x;
+  p.y = a.y;
+  p.norm_g = a.norm_g;
+  p.eps = a.eps;
+  p.batch = a.batch;
+  p.mode = a.mode;
+  p.err = a.err;
+  p.qkv = a.qkv;
+  p.am = a.am;
+  p.x_stride = a.W.cols;
+  p.u0 = 0;
+  p.units = (int)(a.W.cols / 32);
+  p.stages = 0;
+  p.ks = 1;
+  p.accumulate = false;
+  switch (a.fmt) {
+    case QD_Q4_0: return launch<QD_Q4_0>(p, a.pdl, stream);
+    case QD_Q8_0: return launch<QD_Q8_0>(p, a.pdl, stream);
+    default: return launch<QD_I8_ROW>(p, a.pdl, stream);
+  }
+}
+
+}  // namespace qd

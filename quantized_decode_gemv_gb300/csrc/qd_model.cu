@@ -218,7 +218,7 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
   // GEMV with RMSNorm fused into its prologue when the streaming kernel runs; a
   // separate norm kernel (into xn) otherwise.
   auto normed = [&](GemvArgs a, const float* gains) -> qd_status {
-    if (gemv_streams(a)) {
+    if (gemv_fuses_norm(a)) {
       a.norm_g = gains;
       a.eps = c.eps;
       ++n;
@@ -255,7 +255,7 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
       QD_TRY(q8prod(4 * l, c.w_fmt, qa.W, x, attn_norm, qkv, kGemvStore));
       QD_TRY(launch_qkv_post(qkv, L.qkv_rows, batch, e, err, st, true));
       ++n;
-    } else if (gemv_streams(qa)) {
+    } else if (gemv_fuses_norm(qa)) {
       QD_TRY(normed(qa, attn_norm));
     } else {
       GemvArgs raw = qa;
@@ -298,7 +298,7 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
     QD_TRY(q8prod(4 * c.layers, c.emb_fmt, ha.W, x, out_norm, m->f(L.logits), kGemvStore));
     QD_TRY(launch_argmax(m->f(L.logits), c.vocab, batch, m->i(L.tok_out), pos, st));
     ++n;
-  } else if (gemv_streams(ha)) {
+  } else if (gemv_fuses_norm(ha)) {
     QD_TRY(normed(ha, out_norm));
   } else {
     ha.mode = kGemvStore;

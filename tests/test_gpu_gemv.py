@@ -83,9 +83,11 @@ def test_q_gemv_small_ragged_shapes(qd, fmt, batch):
 
 
 @pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "i8", "q4_k"])
-def test_q_gemv_exact_case_bit_exact(qd, fmt):
+@pytest.mark.parametrize("batch", [3, 8])
+def test_q_gemv_exact_case_bit_exact(qd, fmt, batch):
     """Power-of-two scales and integer x: every partial sum is exact in f32, so the GPU must
-    equal the oracle exactly whatever its summation order."""
+    equal the oracle exactly whatever its summation order (batch 3 and 8 take the tensor-core
+    kernel for Q4_0, Q8_0 and INT8 rows)."""
     rows, cols = 70, 2048
     src = qdsynth.weight_src(fmt, 4, "ex", rows, cols).copy()
     if fmt in ("q4_0", "q8_0"):
@@ -98,7 +100,7 @@ def test_q_gemv_exact_case_bit_exact(qd, fmt):
     else:
         src[rows * cols:] = np.full(rows, 2.0 ** -3, np.float32).view(np.uint8)
     p = packed(qd, fmt, src, rows, cols)
-    x = qdsynth.ints_i32(4, "xi", 3 * cols, -4, 4).reshape(3, cols).astype(np.float32)
+    x = qdsynth.ints_i32(4, "xi", batch * cols, -4, 4).reshape(batch, cols).astype(np.float32)
     got = _gemv(qd, fmt, p, rows, cols, x)
     want = oracle.gemv(fmt, src, rows, cols, x)
     assert np.array_equal(got.astype(np.float64), want)
@@ -183,14 +185,60 @@ def test_q_gemv_activation_planes_precision(qd, fmt, batch):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-def test_q_gemv_non_finite_x_propagates(qd, fmt):
+@pytest.mark.parametrize("batch", [2, 5])
+def test_q_gemv_non_finite_x_propagates(qd, fmt, batch):
+    """A non-finite x value makes its batch row's outputs non-finite; the other rows stay
+    finite and correct."""
     rows, cols = 40, 512
     src, p = weights(qd, fmt, 6, "nf", rows, cols)
-    x = qdsynth.activations(6, "xnf", 2, cols)
+    x = qdsynth.activations(6, "xnf", batch, cols)
     x[0, 37] = np.inf
     x[1, 300] = np.nan
     got = _gemv(qd, fmt, p, rows, cols, x)
-    assert not np.isfinite(got).any()
+    assert not np.isfinite(got[:2]).any()
+    if batch > 2:
+        assert_close(got[2:], oracle.gemv(fmt, src, rows, cols, x[2:]), what=f"{fmt} finite rows")
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "i8"])
+@pytest.mark.parametrize("batch", [3, 4, 6, 8])
+def test_q_gemv_tensor_core_batches_full(qd, fmt, batch):
+    """Batch 3-8 on the tensor-core kernel: 16-row tiles with a ragged last tile (rows 1000
+    = 62 tiles + 8), every output row, the 2e-5 bound of the integer planes."""
+    rows, cols = 1000, 1536
+    src, p = weights(qd, fmt, 12, f"tcb.{fmt}", rows, cols)
+    x = qdsynth.activations(12, "tcb.x", batch, cols)
+    got = _gemv(qd, fmt, p, rows, cols, x)
+    assert_close(got, oracle.gemv(fmt, src, rows, cols, x), tol=2e-5, what=f"{fmt} b{batch}")
+
+
+@pytest.mark.parametrize("fmt,cols", [("q4_0", 1600), ("q8_0", 1600), ("i8", 1504)])
+@pytest.mark.parametrize("batch", [3, 7])
+def test_q_gemv_tensor_core_partial_stage(qd, fmt, cols, batch):
+    """Rows whose last 256-column stage is partial (1600 = 6 stages + 2 units; INT8 1504 =
+    5 stages + 7 units, an odd count): the stage loop's run-time tail and the x scale of a
+    short stage, every output row."""
+    rows = 1000
+    src, p = weights(qd, fmt, 13, f"tcp.{fmt}", rows, cols)
+    x = qdsynth.activations(13, "tcp.x", batch, cols)
+    got = _gemv(qd, fmt, p, rows, cols, x)
+    assert_close(got, oracle.gemv(fmt, src, rows, cols, x), tol=2e-5, what=f"{fmt} {cols} b{batch}")
+
+
+@pytest.mark.parametrize("fmt,cols", [("q4_0", 11008), ("q8_0", 11008), ("i8", 11040)])
+@pytest.mark.parametrize("batch", [5, 8])
+def test_q_gemv_tensor_core_column_ranges(qd, fmt, cols, batch):
+    """x rows too wide for the shared memory beside the weight ring (11008 columns at batch
+    5 or 8: over 220 KB of x) run as consecutive launches over column ranges, the first
+    storing and the rest adding; INT8 11040 = 345 units leaves an odd, partial last range.
+    Every output row against the oracle, and two runs give the same bits."""
+    rows = 300
+    src, p = weights(qd, fmt, 14, f"tcr.{fmt}", rows, cols)
+    x = qdsynth.activations(14, "tcr.x", batch, cols)
+    got = _gemv(qd, fmt, p, rows, cols, x)
+    assert_close(got, oracle.gemv(fmt, src, rows, cols, x), tol=2e-5, what=f"{fmt} {cols} b{batch}")
+    again = _gemv(qd, fmt, p, rows, cols, x)
+    assert np.array_equal(got.view(np.uint32), again.view(np.uint32))
 
 
 def test_q_gemv_overlap_chain_matches_plain_launches(qd):

@@ -96,6 +96,19 @@ def test_cluster_step_shapes_teacher_forced(qd, n_heads, n_kv, dim, ffn, max_ctx
     print(f"cluster G={n_heads // n_kv} n_kv={n_kv}: worst rel err {worst:.2e}, near-tie tokens {near}")
 
 
+@pytest.mark.parametrize("w_fmt,batch", [("q4_0", 6), ("q8_0", 8)])
+def test_wide_ffn_model_column_ranges(qd, w_fmt, batch):
+    """A 7B-wide FFN (11008) under a narrow model (dim 320, one stage and a partial one):
+    at batch 6 and 8 the down projection's x is too wide for one launch, so it runs as
+    column ranges that add into the residual, and the fused RMSNorm of the QKV and gate/up
+    products spans a partial stage."""
+    cfg = dict(layers=1, dim=320, ffn=11008, n_heads=5, n_kv_heads=1, head_dim=64, vocab=300, rope_theta=1e4,
+               eps=1e-5, pairing="half", w_fmt=w_fmt, emb_fmt="q8_0")
+    prompt = qdsynth.tokens(28, "wide.prompt", batch * 3, cfg["vocab"]).reshape(batch, 3)
+    worst, near = run_teacher_forced(qd, cfg, 28, prompt, n_gen=3, batch=batch, max_ctx=8)
+    print(f"wide ffn {w_fmt} batch {batch}: worst rel err {worst:.2e}, near-tie tokens {near}")
+
+
 def test_step_path_choice(qd):
     """The kernel chain by default; the 135M shape can take the cluster path (two launches
     per token: the layers, then the head GEMV with the argmax), and switching back and
