@@ -211,14 +211,13 @@ __device__ __forceinline__ void qkv_pair(const Params& p, int64_t r, int b, floa
   }
 }
 
-// One unit's product on the tensor cores: rows g, g + 8 of the 16-row tile (codes at
-// `row0` and `row8` in the ring slot) times the hi and lo fragments of x at `xu`, the lo
-// parts first; d = the unit's f32 sums for (row g, column 2t), (g, 2t + 1), (g + 8, 2t),
-// (g + 8, 2t + 1).
+// One unit's fragments: A for rows g, g + 8 of the 16-row tile (codes at `row0` and
+// `row8` in the ring slot; a0 = K half 0, a1 = K half 1, each rows (g, g + 8) x pairs
+// ((4t, 4t+2), (4t+1, 4t+3))) and B for column g (x at `xu`: v0, v1 = the two K halves'
+// (hi b0, hi b1, lo b0, lo b1)).
 template <int FMT>
-__device__ __forceinline__ void unit_mma(float (&d)[4], const uint8_t* row0, const uint8_t* row8, const uint8_t* xu,
-                                         int t) {
-  uint32_t a0[4], a1[4];  // K halves 0 and 1: rows (g, g + 8) x pairs ((4t, 4t+2), (4t+1, 4t+3))
+__device__ __forceinline__ void unit_frags(const uint8_t* row0, const uint8_t* row8, const uint8_t* xu, int t,
+                                           uint32_t (&a0)[4], uint32_t (&a1)[4], uint4& v0, uint4& v1) {
   if constexpr (FMT == QD_Q4_0) {
     const uint32_t w0 = *reinterpret_cast<const uint32_t*>(row0 + 4 * t);
     const uint32_t w1 = *reinterpret_cast<const uint32_t*>(row8 + 4 * t);
@@ -234,13 +233,25 @@ __device__ __forceinline__ void unit_mma(float (&d)[4], const uint8_t* row0, con
     i8_word(x0, a1[0], a1[2]);
     i8_word(x1, a1[1], a1[3]);
   }
-  // (hi b0, hi b1, lo b0, lo b1) of the two K halves
-  const uint4 v0 = *reinterpret_cast<const uint4*>(xu + 16 * t);
-  const uint4 v1 = *reinterpret_cast<const uint4*>(xu + 64 + 16 * t);
+  v0 = *reinterpret_cast<const uint4*>(xu + 16 * t);
+  v1 = *reinterpret_cast<const uint4*>(xu + 64 + 16 * t);
+}
+
+// One unit's product: d += the unit's f32 sums for (row g, column 2t), (g, 2t + 1),
+// (g + 8, 2t), (g + 8, 2t + 1), two chains of two MMAs (one per K half, lo part first).
+template <int FMT>
+__device__ __forceinline__ void unit_mma(float (&d)[4], const uint8_t* row0, const uint8_t* row8, const uint8_t* xu,
+                                         int t) {
+  uint32_t a0[4], a1[4];
+  uint4 v0, v1;
+  unit_frags<FMT>(row0, row8, xu, t, a0, a1, v0, v1);
+  float e[4] = {0.f, 0.f, 0.f, 0.f};
   mma_f16(d, a0, v0.z, v0.w);
-  mma_f16(d, a1, v1.z, v1.w);
+  mma_f16(e, a1, v1.z, v1.w);
   mma_f16(d, a0, v0.x, v0.y);
-  mma_f16(d, a1, v1.x, v1.y);
+  mma_f16(e, a1, v1.x, v1.y);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] += e[i];
 }
 
 // The f16 block scale of unit uu (0..7) from a row's 8 scales held as 4 words.
@@ -265,8 +276,34 @@ __device__ __forceinline__ void stage_mma(float (&as)[4], const uint8_t* slot, c
 #pragma unroll
     for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
     if constexpr (NU > 0) {
+      // groups of 4 units: fragments first, then the MMAs round-robin over the units, so
+      // 8 independent accumulator chains are in flight (K half 0 in c[u], half 1 in c2[u])
+      float c2[4][4];
 #pragma unroll
-      for (int uu = 0; uu < NU; ++uu) unit_mma<FMT>(c[uu & 3], row0 + uu * CB, row8 + uu * CB, xst + uu * 128, t);
+      for (int j = 0; j < 4; ++j) c2[j][0] = c2[j][1] = c2[j][2] = c2[j][3] = 0.f;
+#pragma unroll
+      for (int q = 0; q < NU / 4; ++q) {
+        uint32_t A0[4][4], A1[4][4];
+        uint4 V0[4], V1[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          unit_frags<FMT>(row0 + (4 * q + u) * CB, row8 + (4 * q + u) * CB, xst + (4 * q + u) * 128, t, A0[u], A1[u],
+                          V0[u], V1[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          mma_f16(c[u], A0[u], V0[u].z, V0[u].w);
+          mma_f16(c2[u], A1[u], V1[u].z, V1[u].w);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          mma_f16(c[u], A0[u], V0[u].x, V0[u].y);
+          mma_f16(c2[u], A1[u], V1[u].x, V1[u].y);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[j][i] += c2[j][i];
     } else {
       int uu = 0;
       for (; uu + 1 < nu; uu += 2) {
@@ -292,10 +329,129 @@ __device__ __forceinline__ void stage_mma(float (&as)[4], const uint8_t* slot, c
       as[3] = fmaf(d8, d[3], as[3]);
     };
     if constexpr (NU > 0) {
+      // groups of 4 units: fragments first, then the MMAs round-robin over the units (8
+      // independent accumulator chains in flight), then the block scales
 #pragma unroll
-      for (int uu = 0; uu < NU; ++uu) one(uu);
+      for (int q = 0; q < NU / 4; ++q) {
+        uint32_t A0[4][4], A1[4][4];
+        uint4 V0[4], V1[4];
+        float D[4][4], E[4][4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          unit_frags<FMT>(row0 + (4 * q + u) * CB, row8 + (4 * q + u) * CB, xst + (4 * q + u) * 128, t, A0[u], A1[u],
+                          V0[u], V1[u]);
+          D[u][0] = D[u][1] = D[u][2] = D[u][3] = 0.f;
+          E[u][0] = E[u][1] = E[u][2] = E[u][3] = 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          mma_f16(D[u], A0[u], V0[u].z, V0[u].w);
+          mma_f16(E[u], A1[u], V1[u].z, V1[u].w);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          mma_f16(D[u], A0[u], V0[u].x, V0[u].y);
+          mma_f16(E[u], A1[u], V1[u].x, V1[u].y);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float d0 = scale_of(s0, 4 * q + u), d8 = scale_of(s8, 4 * q + u);
+          as[0] = fmaf(d0, D[u][0] + E[u][0], as[0]);
+          as[1] = fmaf(d0, D[u][1] + E[u][1], as[1]);
+          as[2] = fmaf(d8, D[u][2] + E[u][2], as[2]);
+          as[3] = fmaf(d8, D[u][3] + E[u][3], as[3]);
+        }
+      }
     } else {
       for (int uu = 0; uu < nu; ++uu) one(uu);  // block formats: nu is even
+    }
+  }
+}
+
+// x in place: warp w converts stages w, w + 8, ... for R batch rows at once (R = 4 or 8),
+// as straight-line code (rows past the batch convert zeros and store nothing), so the rows'
+// loads and dependency chains overlap.  Lane l holds elements 8l..8l+7 of the stage
+// (unit l / 4, K half (l % 4) / 2): two 16-byte halves, each the four elements of one
+// fragment thread (2 (l % 2) and 2 (l % 2) + 1), rewritten in place as that thread's
+// (hi b0, hi b1, lo b0, lo b1).  Lanes 4-7 of each quarter take their second half
+// first: the eight lanes of a 128-bit access then cover all 32 banks once.
+template <int R>
+__device__ __forceinline__ void convert_x(uint8_t* xs, int64_t x_row, const float* gs, float* sxs, float* ssq, int units,
+                                          int nst, int batch, bool norm, int warp, int lane) {
+  const int h = (lane >> 2) & 1;
+  for (int s = warp; s < nst; s += kWarps) {
+    const int e0 = s * kStageCols + 8 * lane;
+    const bool in = e0 < units * 32;
+    uint8_t* sbase = xs + (int64_t)s * kStageCols * 4 + 32 * lane;
+    float v[R][8];  // [row][half h's 4 elements, then the other half's]
+#pragma unroll
+    for (int b = 0; b < R; ++b) {
+      float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0;
+      if (b < batch && in) {
+        const float4* px = reinterpret_cast<const float4*>(sbase + b * x_row);
+        q0 = px[h];
+        q1 = px[h ^ 1];
+      }
+      v[b][0] = q0.x, v[b][1] = q0.y, v[b][2] = q0.z, v[b][3] = q0.w;
+      v[b][4] = q1.x, v[b][5] = q1.y, v[b][6] = q1.z, v[b][7] = q1.w;
+    }
+    float ss[R];
+#pragma unroll
+    for (int b = 0; b < R; ++b) ss[b] = 0.f;
+    if (norm) {
+      float gv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (in) {
+        const float4 g0 = *reinterpret_cast<const float4*>(gs + e0 + 4 * h);
+        const float4 g1 = *reinterpret_cast<const float4*>(gs + e0 + 4 * (h ^ 1));
+        gv[0] = g0.x, gv[1] = g0.y, gv[2] = g0.z, gv[3] = g0.w, gv[4] = g1.x, gv[5] = g1.y, gv[6] = g1.z, gv[7] = g1.w;
+      }
+#pragma unroll
+      for (int b = 0; b < R; ++b) {
+#pragma unroll
+        for (int j2 = 0; j2 < 8; ++j2) {
+          ss[b] = fmaf(v[b][j2], v[b][j2], ss[b]);
+          v[b][j2] *= gv[j2];
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int b = 0; b < R; ++b) ss[b] += __shfl_xor_sync(0xffffffffu, ss[b], o);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < R; ++b) {
+      // the stage scale: 2^e with the largest |x| in [2^e, 2^(e+1)); magnitude bits
+      // order like the values, and inf / NaN sit above every finite one
+      uint32_t mb = 0;
+#pragma unroll
+      for (int j2 = 0; j2 < 8; ++j2) mb = max(mb, __float_as_uint(v[b][j2]) & 0x7FFFFFFFu);
+      mb = __reduce_max_sync(0xffffffffu, mb);
+      const bool bad = mb >= 0x7F800000u, live = mb != 0u;
+      const int e = (int)(mb >> 23) - 127;
+      const float rs = live && !bad ? pow2i(-e) : 0.f;
+      float4 fr[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {  // the two halves, each one fragment thread's elements
+        const float y0 = v[b][4 * k] * rs, y1 = v[b][4 * k + 1] * rs;
+        const float y2 = v[b][4 * k + 2] * rs, y3 = v[b][4 * k + 3] * rs;
+        const __half2 h0 = __floats2half2_rn(y0, y2), h1 = __floats2half2_rn(y1, y3);
+        const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+        const __half2 l0 = __floats2half2_rn(y0 - f0.x, y2 - f0.y), l1 = __floats2half2_rn(y1 - f1.x, y3 - f1.y);
+        fr[k] = make_float4(__uint_as_float(h2_bits(h0)), __uint_as_float(h2_bits(h1)), __uint_as_float(h2_bits(l0)),
+                            __uint_as_float(h2_bits(l1)));
+      }
+      if (b < batch) {
+        if (in) {
+          float4* px = reinterpret_cast<float4*>(sbase + b * x_row);
+          px[h] = fr[0];
+          px[h ^ 1] = fr[1];
+        }
+        if (lane == 0) {
+          sxs[s * 8 + b] = bad ? __uint_as_float(0x7FC00000u) : live ? pow2i(e) : 0.f;
+          ssq[s * 8 + b] = ss[b];
+        }
+      }
     }
   }
 }
@@ -415,89 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
     return;
   }
 
-  // ---- x in place: warp w converts stages w, w + 8, ... for all 8 batch rows at once, as
-  // straight-line code (rows past the batch convert zeros and store nothing), so the rows'
-  // loads and dependency chains overlap.  Lane l holds elements 8l..8l+7 of the stage
-  // (unit l / 4, K half (l % 4) / 2): two 16-byte halves, each the four elements of one
-  // fragment thread (2 (l % 2) and 2 (l % 2) + 1), rewritten in place as that thread's
-  // (hi b0, hi b1, lo b0, lo b1).  Lanes 4-7 of each quarter take their second half
-  // first: the eight lanes of a 128-bit access then cover all 32 banks once.
-  {
-    const int h = (lane >> 2) & 1;
-    for (int s = warp; s < nst; s += kWarps) {
-      const int e0 = s * kStageCols + 8 * lane;
-      const bool in = e0 < units * 32;
-      uint8_t* sbase = xs + (int64_t)s * kStageCols * 4 + 32 * lane;
-      float v[8][8];  // [row][half h's 4 elements, then the other half's]
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0;
-        if (b < p.batch && in) {
-          const float4* px = reinterpret_cast<const float4*>(sbase + b * L.x_row);
-          q0 = px[h];
-          q1 = px[h ^ 1];
-        }
-        v[b][0] = q0.x, v[b][1] = q0.y, v[b][2] = q0.z, v[b][3] = q0.w;
-        v[b][4] = q1.x, v[b][5] = q1.y, v[b][6] = q1.z, v[b][7] = q1.w;
-      }
-      float ss[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (norm) {
-        float gv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (in) {
-          const float4 g0 = *reinterpret_cast<const float4*>(gs + e0 + 4 * h);
-          const float4 g1 = *reinterpret_cast<const float4*>(gs + e0 + 4 * (h ^ 1));
-          gv[0] = g0.x, gv[1] = g0.y, gv[2] = g0.z, gv[3] = g0.w, gv[4] = g1.x, gv[5] = g1.y, gv[6] = g1.z, gv[7] = g1.w;
-        }
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-#pragma unroll
-          for (int j2 = 0; j2 < 8; ++j2) {
-            ss[b] = fmaf(v[b][j2], v[b][j2], ss[b]);
-            v[b][j2] *= gv[j2];
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-          for (int b = 0; b < 8; ++b) ss[b] += __shfl_xor_sync(0xffffffffu, ss[b], o);
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        // the stage scale: 2^e with the largest |x| in [2^e, 2^(e+1)); magnitude bits
-        // order like the values, and inf / NaN sit above every finite one
-        uint32_t mb = 0;
-#pragma unroll
-        for (int j2 = 0; j2 < 8; ++j2) mb = max(mb, __float_as_uint(v[b][j2]) & 0x7FFFFFFFu);
-        mb = __reduce_max_sync(0xffffffffu, mb);
-        const bool bad = mb >= 0x7F800000u, live = mb != 0u;
-        const int e = (int)(mb >> 23) - 127;
-        const float rs = live && !bad ? pow2i(-e) : 0.f;
-        float4 fr[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {  // the two halves, each one fragment thread's elements
-          const float y0 = v[b][4 * k] * rs, y1 = v[b][4 * k + 1] * rs;
-          const float y2 = v[b][4 * k + 2] * rs, y3 = v[b][4 * k + 3] * rs;
-          const __half2 h0 = __floats2half2_rn(y0, y2), h1 = __floats2half2_rn(y1, y3);
-          const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
-          const __half2 l0 = __floats2half2_rn(y0 - f0.x, y2 - f0.y), l1 = __floats2half2_rn(y1 - f1.x, y3 - f1.y);
-          fr[k] = make_float4(__uint_as_float(h2_bits(h0)), __uint_as_float(h2_bits(h1)), __uint_as_float(h2_bits(l0)),
-                              __uint_as_float(h2_bits(l1)));
-        }
-        if (b < p.batch) {
-          if (in) {
-            float4* px = reinterpret_cast<float4*>(sbase + b * L.x_row);
-            px[h] = fr[0];
-            px[h ^ 1] = fr[1];
-          }
-          if (lane == 0) {
-            sxs[s * 8 + b] = bad ? __uint_as_float(0x7FC00000u) : live ? pow2i(e) : 0.f;
-            ssq[s * 8 + b] = ss[b];
-          }
-        }
-      }
-    }
-  }
+  if (p.batch <= 4) convert_x<4>(xs, L.x_row, gs, sxs, ssq, units, nst, p.batch, norm, warp, lane);
+  else convert_x<8>(xs, L.x_row, gs, sxs, ssq, units, nst, p.batch, norm, warp, lane);
   __syncthreads();
   // RMSNorm factors of this lane's columns 2t, 2t + 1 (stage sums in stage order: every
   // CTA forms the same value)
