@@ -398,6 +398,7 @@ def run_ours(args, world, rank, local):
         del model
         torch.cuda.empty_cache()
         out["decode_135m_modes"] = bench_135m_modes(qd, torch, stream)
+        out["prefill_135m"] = bench_prefill_135m(qd, torch, stream)
         if not args.no_1p7b:
             out["decode_1p7b"] = bench_1p7b(qd, torch, stream, args, hbm)
             out["decode_1p7b"].update(bench_1p7b(qd, torch, stream, args, hbm, kv_f16=True))
@@ -620,6 +621,58 @@ def bench_135m_modes(qd, torch, stream, steps=50):
         del m
         torch.cuda.empty_cache()
     return out
+
+
+def bench_prefill_135m(qd, torch, stream, reps=10):
+    """The 135M-shaped model's 128-token prompt in one qd_prefill call (batched prefill), on
+    the tensor-core GEMM (flags 0) and on the batched GEMV (QD_PREFILL_EXACT), against the
+    same prompt as 128 decode steps: prompt tokens/s, CUDA events around the prefill call
+    only (the cache reset before each is outside them); L2 flushed before each rep."""
+    import qdsynth
+
+    cfg = qdsynth.SMOL_135M
+    host = qdsynth.model_tensors(cfg, 0)
+    srcs = [None if t is None else torch.from_numpy(np.ascontiguousarray(t)).cuda() for t in host]
+    m = qd.Model(qd.make_config(cfg, PROMPT + GEN, 1), srcs)
+    del srcs
+    prompt = torch.from_numpy(qdsynth.tokens(0, "smol135m.prompt", PROMPT, cfg["vocab"]).astype(np.int32)).cuda()
+    ws = torch.empty(m.prefill_workspace(PROMPT), dtype=torch.uint8, device="cuda")
+    outt = torch.empty(1, dtype=torch.int32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    res = {"tokens": PROMPT, "model": "135M-shaped, q4_0 layers, q8_0 tied head"}
+    toks = {}
+    for name, flags in (("gemm", 0), ("exact", qd.PREFILL_EXACT), ("decode_steps", None)):
+        def once(flags=flags):
+            if flags is None:
+                for i in range(PROMPT):
+                    m.decode_step(prompt.data_ptr() + 4 * i, 1, outt, None, stream)
+            else:
+                m.prefill(0, prompt, PROMPT, outt, None, flags=flags, workspace=ws, stream=stream)
+        for _ in range(3):
+            m.reset(stream)
+            once()
+        ts = []
+        for _ in range(reps):
+            flush.fill_(0)
+            m.reset(stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            once()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / 1e3)
+        assert m.check() == 0
+        toks[name] = int(outt.item())
+        t = statistics.median(ts)
+        res[name] = {"ms": round(t * 1e3, 3), "prompt_tokens/s": round(PROMPT / t, 1)}
+    # the token after the prompt: the exact path and the decode steps agree (same products);
+    # the GEMM's binary16 weights may move a near-tie
+    res["next_token"] = toks
+    res["speedup_vs_decode_steps"] = {k: round(res["decode_steps"]["ms"] / res[k]["ms"], 2) for k in ("gemm", "exact")}
+    m.close()
+    del m
+    torch.cuda.empty_cache()
+    return res
 
 
 def cpu_baseline(cfg, seconds=15.0, max_tokens=64):
@@ -921,6 +974,7 @@ def main(argv=None):
     ap.add_argument("--gemm", default=None, help="the prefill product alone, FMT:ROWSxCOLS:TOKENS")
     ap.add_argument("--q8act", default=None, help="the ggml-exact activation path alone, FMT:ROWSxCOLS:BATCH")
     ap.add_argument("--modes-135m", action="store_true", help="135M decode in the default and ggml-exact modes")
+    ap.add_argument("--prefill-135m", action="store_true", help="the 135M prompt through qd_prefill alone")
     ap.add_argument("--kv-f16", action="store_true", help="with --decode-1p7b: binary16 KV cache")
     ap.add_argument("--step-path", choices=["chain", "cluster"], default=None,
                     help="force the 135M decode step's path (default: the library's choice)")
@@ -939,6 +993,14 @@ def main(argv=None):
         return
     if args.q8act:
         run_q8act_only(args.q8act, args.reps)
+        return
+    if args.prefill_135m:
+        import torch
+
+        import quantized_decode_gemv_gb300 as qd
+
+        qd.load()
+        print(json.dumps({"prefill_135m": bench_prefill_135m(qd, torch, torch.cuda.current_stream())}))
         return
     if args.modes_135m:
         import torch

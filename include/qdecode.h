@@ -428,10 +428,38 @@ void qd_model_destroy(qd_model* m);
  * or device pointers (int32 [batch]); logits_out (f32 [batch][vocab], host or
  * device) may be NULL.  The step is one CUDA graph replay on `stream` (captured on
  * the first step of each batch size); host pointers make the call wait for the
- * copies.  Prefill is this call once per prompt token: the Go package's "Results"
- * section runs its prompt the same way, one decode pass per token. */
+ * copies.  A prompt can run as this call once per token (the Go package's "Results"
+ * section runs its prompt that way, one decode pass per token) or through qd_prefill. */
 qd_status qd_decode_step(qd_model* m, const int32_t* tokens, int batch, int32_t* out_tokens, float* logits_out,
                          qd_stream_t stream);
+
+/* Batched prefill ([llmoxide] 11 "Prefill and decode": the prompt's t tokens go through
+ * every product as one t-row matrix, so each weight tile is read once for all of them).
+ * Runs the t prompt tokens of sequence `seq` (0 <= seq < max_batch) at positions
+ * pos[seq] .. pos[seq] + t - 1: embeds them, runs every layer over the t rows (RMSNorm,
+ * QKV product, RoPE and the cache append at each token's position, causal attention of
+ * token i over positions 0 .. pos[seq] + i, output projection and residual, SwiGLU
+ * feed-forward and residual), then the output head on the last token: its greedy token
+ * to *out_token and, if logits_out is not NULL, its logits (f32 [vocab]).  pos[seq]
+ * advances by t.  The cache and the returned values equal those of t decode steps of that
+ * sequence, up to the products' arithmetic:
+ *  - flags 0: with Q4_0, Q8_0 or INT8 layer weights, column counts (dim, heads * 64, ffn)
+ *    that are multiples of 64 and t > 16, the layer products run on qd_q_gemm's tensor-core
+ *    GEMM (Q4_0 / Q8_0 weights rounded to binary16, see qd_q_gemm); otherwise as below.
+ *  - QD_PREFILL_EXACT: the layer products run on the batched GEMV (qd_q_gemv's arithmetic,
+ *    as the decode step), 8 tokens a launch.
+ * The head always runs the decode step's GEMV.  tokens: host or device int32 [t]; ids
+ * outside [0, vocab) embed zeros and set the device flag (qd_model_check), as do
+ * positions past max_ctx.  out_token (int32) and logits_out: host or device.
+ * workspace: device, 256-byte aligned, >= qd_prefill_workspace(cfg, t) bytes (smaller:
+ * QD_ERR_NOMEM); it may be reused once the call has completed on `stream`.
+ * 1 <= t <= min(max_ctx, QD_MAX_GEMM_TOKENS) (else QD_ERR_SHAPE); models with act_q8 = 1:
+ * QD_ERR_UNSUPPORTED; unknown flag bits: QD_ERR_INVALID_ARG.  Kernels are launched
+ * directly on `stream` (no graph). */
+#define QD_PREFILL_EXACT 1u
+size_t qd_prefill_workspace(const qd_config* cfg, int t);
+qd_status qd_prefill(qd_model* m, int seq, const int32_t* tokens, int t, unsigned flags, void* workspace,
+                     size_t workspace_bytes, int32_t* out_token, float* logits_out, qd_stream_t stream);
 
 /* Zero the KV cache and set every position to 0 ([go-llm] CPU.Reset). */
 qd_status qd_model_reset(qd_model* m, qd_stream_t stream);

@@ -30,11 +30,13 @@ EXPORTS = ["qd_status_str", "qd_abi_version", "qd_f16_to_f32", "qd_bf16_to_f32",
            "qd_rope_table", "qd_rope", "qd_kv_append", "qd_gqa_decode_attn_workspace", "qd_gqa_decode_attn",
            "qd_gqa_decode_attn_noalloc",
            "qd_swiglu", "qd_argmax", "qd_embed", "qd_model_weight_bytes", "qd_model_state_bytes",
-           "qd_model_create", "qd_model_destroy", "qd_decode_step", "qd_model_reset", "qd_model_set_pos",
+           "qd_model_create", "qd_model_destroy", "qd_decode_step", "qd_prefill_workspace", "qd_prefill",
+           "qd_model_reset", "qd_model_set_pos",
            "qd_model_pos", "qd_model_kv_cache", "qd_model_act_q8_buffer", "qd_model_check",
            "qd_model_launches_per_step", "qd_model_set_step_path", "qd_model_step_path",
            "qd_model_cluster_available"]
 STEP_AUTO, STEP_KERNEL_CHAIN, STEP_CLUSTER = 0, 1, 2
+PREFILL_EXACT = 1
 
 
 class QDError(RuntimeError):
@@ -103,6 +105,8 @@ def load():
         "qd_model_create": ([ctypes.POINTER(Config), p, p, sz, p, sz, p, ctypes.POINTER(p)], i32),
         "qd_model_destroy": ([p], None),
         "qd_decode_step": ([p, p, i32, p, p, p], i32),
+        "qd_prefill_workspace": ([ctypes.POINTER(Config), i32], sz),
+        "qd_prefill": ([p, i32, p, i32, ctypes.c_uint, p, sz, p, p, p], i32),
         "qd_model_reset": ([p, p], i32),
         "qd_model_set_pos": ([p, p, i32, p], i32),
         "qd_model_pos": ([p, p, i32, p], i32),
@@ -347,6 +351,23 @@ class Model:
         """tokens / out_tokens / logits_out: torch tensors (host or device) or raw pointers."""
         _check("qd_decode_step", load().qd_decode_step(self.handle, _ptr(tokens), batch, _ptr(out_tokens),
                                                        _ptr(logits_out), _stream(stream)))
+
+    def prefill_workspace(self, t):
+        """Bytes of the workspace qd_prefill needs for t tokens (0: not available)."""
+        return load().qd_prefill_workspace(ctypes.byref(self.cfg), t)
+
+    def prefill(self, seq, tokens, t, out_token, logits_out=None, flags=0, workspace=None, stream=None):
+        """Run t prompt tokens of sequence seq in one call (qd_prefill).  tokens, out_token,
+        logits_out: torch tensors (host or device) or raw pointers; workspace: a device
+        tensor of at least prefill_workspace(t) bytes (allocated here when None)."""
+        import torch
+
+        need = self.prefill_workspace(t)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+        nbytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else need
+        _check("qd_prefill", load().qd_prefill(self.handle, seq, _ptr(tokens), t, flags, _ptr(workspace), nbytes,
+                                               _ptr(out_token), _ptr(logits_out), _stream(stream)))
 
     def reset(self, stream=None):
         _check("qd_model_reset", load().qd_model_reset(self.handle, _stream(stream)))

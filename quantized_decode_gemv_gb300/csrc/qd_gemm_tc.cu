@@ -81,8 +81,9 @@ struct Params {
   int64_t tiles;
   const uint8_t* bimg;    // [token tile][stage] B images
   const float* unscale;   // [token tiles * 64]
-  float* y;               // [t][rows]
+  float* y;               // [t][rows] ([t][rows / 2] for SwiGLU)
   uint32_t* err;
+  int mode;               // kGemmStore, kGemmAccumulate (y += product), kGemmSwiGLU
 };
 
 // ---- the prologue: x -> scaled f16 high / low parts in B-image layout
@@ -296,11 +297,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const Params p) {
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(drained);  // the accumulators may be overwritten
-      if (row < p.rows) {
+      if (p.mode == kGemmSwiGLU) {
+        // rows (2i, 2i + 1) = (gate_i, up_i) sit in lanes (2j, 2j + 1): y[n][i] = silu(gate) * up
 #pragma unroll
         for (int k = 0; k < kTN; ++k) {
           const int n = n0 + k;
-          if (n < p.t) p.y[(int64_t)n * p.rows + row] = bad ? 0.f : v[k] * __ldg(p.unscale + n) * rs;
+          const float val = (row < p.rows && n < p.t && !bad) ? v[k] * __ldg(p.unscale + n) * rs : 0.f;
+          const float up = __shfl_down_sync(0xffffffffu, val, 1);
+          if ((tid & 1) == 0 && row + 1 < p.rows && n < p.t)
+            p.y[(int64_t)n * (p.rows / 2) + row / 2] = val / (1.0f + expf(-val)) * up;
+        }
+      } else if (row < p.rows) {
+#pragma unroll
+        for (int k = 0; k < kTN; ++k) {
+          const int n = n0 + k;
+          if (n < p.t) {
+            const float val = bad ? 0.f : v[k] * __ldg(p.unscale + n) * rs;
+            float* dst = p.y + (int64_t)n * p.rows + row;
+            *dst = p.mode == kGemmAccumulate ? *dst + val : val;
+          }
         }
       }
     };
@@ -459,9 +474,12 @@ size_t gemm_workspace_bytes(int64_t cols, int t) {
 }
 
 qd_status launch_q_gemm(int fmt, const PackedView& W, const float* x, float* y, int t, void* ws, uint32_t* err,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, int mode) {
   using namespace tc_gemm;
+  if (mode != kGemmStore && mode != kGemmAccumulate && mode != kGemmSwiGLU) return QD_ERR_INVALID_ARG;
+  if (mode == kGemmSwiGLU && (W.rows & 1)) return QD_ERR_SHAPE;
   Params p;
+  p.mode = mode;
   p.codes = W.codes;
   p.scales = W.scales;
   p.row_code_bytes = W.row_code_bytes;

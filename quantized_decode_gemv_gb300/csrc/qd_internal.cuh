@@ -360,10 +360,14 @@ bool gemv_tc_supported(const GemvArgs& a);
 qd_status launch_q_gemv_tc(const GemvArgs& a, cudaStream_t stream);
 
 // Batched prefill product on the tensor cores (Q4_0, Q8_0, INT8 rows; cols % 64 == 0):
-// y[n][r] = sum_c deq(W)[r][c] x[n][c] for n < t; ws holds gemm_workspace_bytes(cols, t).
+// y[n][r] = sum_c deq(W)[r][c] x[n][c] for n < t (kGemmStore), y[n][r] += that
+// (kGemmAccumulate), or for rows interleaved as (gate_i, up_i) pairs y[n][i] =
+// silu(gate_i . x[n]) * (up_i . x[n]) (kGemmSwiGLU; y has rows / 2 columns); ws holds
+// gemm_workspace_bytes(cols, t).
+constexpr int kGemmStore = 0, kGemmAccumulate = 1, kGemmSwiGLU = 2;
 size_t gemm_workspace_bytes(int64_t cols, int t);
 qd_status launch_q_gemm(int fmt, const PackedView& W, const float* x, float* y, int t, void* ws, uint32_t* err,
-                        cudaStream_t stream);
+                        cudaStream_t stream, int mode = kGemmStore);
 
 // ggml-exact activations: Q8_0 (Q8_1 with with_sum) quantisation of x [batch][cols] into
 // out (codes, then f16 d, then f16 s; q8_buffer_bytes), and the product over them with the

@@ -334,6 +334,178 @@ qd_status get_graph(qd_model* m, int batch, cudaGraphExec_t* out) {
   return QD_OK;
 }
 
+
+// ---- batched prefill (llmoxide blog s11 "Prefill and decode": the prompt's t tokens go
+// through every product as one t-row matrix, one read of each weight tile for all of them)
+
+// ppos[i] = pos[seq] + i: each prompt token's position.
+__global__ void k_prefill_pos(const int32_t* __restrict__ pos_seq, int32_t* __restrict__ ppos, int t) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < t; i += gridDim.x * blockDim.x) ppos[i] = *pos_seq + i;
+}
+// pos[seq] += n (the head's argmax adds the last one).
+__global__ void k_pos_add(int32_t* pos_seq, int n) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) *pos_seq += n;
+}
+
+struct PrefillLayout {
+  size_t tok, ppos, x, xn, qkv, q, att, act, gemm_ws, attn_ws, attn_cnt, total;
+};
+
+constexpr int kPrefillChunk = 16;  // tokens per flat-attention launch (binary16 cache)
+constexpr int kPrefillRows = 8;    // tokens per batched-GEMV launch (the tensor-core GEMV)
+
+PrefillLayout prefill_layout(const qd_config& c, int64_t qkv_rows, int t) {
+  PrefillLayout P{};
+  const int64_t D = c.dim, F = c.ffn, QD = (int64_t)c.n_heads * c.head_dim;
+  size_t off = 0;
+  auto take = [&off](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  P.tok = take(4 * (size_t)t);
+  P.ppos = take(4 * (size_t)t);
+  P.x = take(4 * (size_t)t * D);
+  P.xn = take(4 * (size_t)t * D);
+  P.qkv = take(4 * (size_t)t * qkv_rows);
+  P.q = take(4 * (size_t)t * QD);
+  P.att = take(4 * (size_t)t * QD);
+  P.act = take(4 * (size_t)t * F);
+  P.gemm_ws = take(std::max(gemm_workspace_bytes(D, t), std::max(gemm_workspace_bytes(QD, t), gemm_workspace_bytes(F, t))));
+  if (c.kv_f16) {
+    P.attn_ws = take(4 * attn_flat_ws_floats(c.n_heads, c.n_kv_heads, kPrefillChunk, attn_flat_ctas()));
+    P.attn_cnt = take(4 * (size_t)kPrefillChunk * c.n_kv_heads);
+  } else {
+    P.attn_ws = take(attn_workspace_bytes(c.n_heads, c.head_dim, c.max_ctx, t));
+    P.attn_cnt = 0;
+  }
+  P.total = off;
+  return P;
+}
+
+// Whether the prefill products run on the tensor-core GEMM (binary16 weights) rather than
+// the batched GEMVs (the decode step's arithmetic).
+bool prefill_uses_gemm(const qd_config& c, int t, unsigned flags) {
+  if (flags & QD_PREFILL_EXACT) return false;
+  if (t <= 2 * kPrefillRows) return false;  // two GEMV launches per product are as fast
+  if (c.w_fmt != QD_Q4_0 && c.w_fmt != QD_Q8_0 && c.w_fmt != QD_I8_ROW) return false;
+  const int64_t QD = (int64_t)c.n_heads * c.head_dim;
+  return c.dim % 64 == 0 && QD % 64 == 0 && c.ffn % 64 == 0;
+}
+
+qd_status enqueue_prefill(qd_model* m, int seq, int t, unsigned flags, uint8_t* ws, cudaStream_t st) {
+  const qd_config& c = m->cfg;
+  const Layout& L = m->L;
+  const PrefillLayout P = prefill_layout(c, L.qkv_rows, t);
+  const int64_t D = c.dim, F = c.ffn, QD = (int64_t)c.n_heads * c.head_dim, KD = (int64_t)c.n_kv_heads * c.head_dim;
+  uint32_t* err = reinterpret_cast<uint32_t*>(m->s + L.err);
+  int32_t* pos_seq = m->i(L.pos) + seq;
+  int32_t* ppos = reinterpret_cast<int32_t*>(ws + P.ppos);
+  float* x = reinterpret_cast<float*>(ws + P.x);
+  float* xn = reinterpret_cast<float*>(ws + P.xn);
+  float* qkv = reinterpret_cast<float*>(ws + P.qkv);
+  float* q = reinterpret_cast<float*>(ws + P.q);
+  float* att = reinterpret_cast<float*>(ws + P.att);
+  float* act = reinterpret_cast<float*>(ws + P.act);
+  const bool gemm = prefill_uses_gemm(c, t, flags);
+
+  k_prefill_pos<<<(t + 255) / 256, 256, 0, st>>>(pos_seq, ppos, t);
+  QD_TRY(launch_status());
+  QD_TRY(launch_embed(c.emb_fmt, m->W(c.emb_fmt, L.emb, c.vocab, D), reinterpret_cast<int32_t*>(ws + P.tok), t, x,
+                      err, st));
+  if (c.kv_f16) QD_TRY(zero_region(ws + P.attn_cnt, align_up(4 * (size_t)kPrefillChunk * c.n_kv_heads, 16), st));
+
+  // one product over the t rows of `in`: the GEMM, or batched GEMVs of up to 8 rows
+  auto product = [&](PackedView W, const float* in, float* y, GemvMode mode) -> qd_status {
+    if (gemm) {
+      const int gm = mode == kGemvAccumulate ? kGemmAccumulate : mode == kGemvSwiGLU ? kGemmSwiGLU : kGemmStore;
+      return launch_q_gemm(c.w_fmt, W, in, y, t, ws + P.gemm_ws, err, st, gm);
+    }
+    const int64_t ycols = mode == kGemvSwiGLU ? W.rows / 2 : W.rows;
+    for (int c0 = 0; c0 < t; c0 += kPrefillRows) {
+      GemvArgs a;
+      a.fmt = c.w_fmt;
+      a.W = W;
+      a.x = in + (int64_t)c0 * W.cols;
+      a.y = y + (int64_t)c0 * ycols;
+      a.batch = std::min(kPrefillRows, t - c0);
+      a.mode = mode;
+      a.err = err;
+      QD_TRY(launch_q_gemv(a, st));
+    }
+    return QD_OK;
+  };
+
+  for (int l = 0; l < c.layers; ++l) {
+    const LayerOff& o = L.layer[l];
+    const int64_t esz = c.kv_f16 ? 2 : 4;
+    // this sequence's cache rows of layer l; every prompt token appends into the same one
+    uint8_t* kc = m->s + L.kc + ((int64_t)l * L.cache_layer_stride + (int64_t)seq * L.cache_batch_stride) * esz;
+    uint8_t* vc = m->s + L.vc + ((int64_t)l * L.cache_layer_stride + (int64_t)seq * L.cache_batch_stride) * esz;
+    QD_TRY(launch_rmsnorm(x, reinterpret_cast<const float*>(m->w + o.attn_norm), xn, (int)D, t, c.eps, st));
+    QD_TRY(product(m->W(c.w_fmt, o.wqkv, L.qkv_rows, D), xn, qkv, kGemvStore));
+    QkvEpilogue e;
+    e.q_rows = (int)QD;
+    e.k_rows = (int)KD;
+    e.head_dim = c.head_dim;
+    e.pairing = c.pairing;
+    e.pos = ppos;
+    e.rope = m->f(L.rope);
+    e.q_out = q;
+    e.q_stride = QD;
+    e.kc = kc;
+    e.vc = vc;
+    e.kv_f16 = c.kv_f16 != 0;
+    e.cache_batch_stride = 0;
+    e.max_ctx = c.max_ctx;
+    QD_TRY(launch_qkv_post(qkv, L.qkv_rows, t, e, err, st, false));
+    // causal attention: token i over positions 0 .. ppos[i] of the one cache
+    if (c.kv_f16) {
+      for (int c0 = 0; c0 < t; c0 += kPrefillChunk)
+        QD_TRY(launch_attention_flat(q + (int64_t)c0 * QD, QD, kc, vc, true, 0, att + (int64_t)c0 * QD, c.n_heads,
+                                     c.n_kv_heads, c.head_dim, ppos + c0, c.max_ctx, std::min(kPrefillChunk, t - c0),
+                                     attn_flat_ctas(), reinterpret_cast<float*>(ws + P.attn_ws),
+                                     reinterpret_cast<unsigned int*>(ws + P.attn_cnt), err, st, false));
+    } else {
+      QD_TRY(launch_attention(q, QD, reinterpret_cast<const float*>(kc), reinterpret_cast<const float*>(vc), 0, att,
+                              c.n_heads, c.n_kv_heads, c.head_dim, ppos, c.max_ctx, t, ws + P.attn_ws, err, st));
+    }
+    QD_TRY(product(m->W(c.w_fmt, o.wo, D, QD), att, x, kGemvAccumulate));
+    QD_TRY(launch_rmsnorm(x, reinterpret_cast<const float*>(m->w + o.ffn_norm), xn, (int)D, t, c.eps, st));
+    QD_TRY(product(m->W(c.w_fmt, o.wgu, 2 * F, D), xn, act, kGemvSwiGLU));
+    QD_TRY(product(m->W(c.w_fmt, o.wd, D, F), act, x, kGemvAccumulate));
+  }
+
+  // the last token's logits and greedy token, as the decode step's head; the position
+  // ends at pos[seq] + t (the argmax adds the last one)
+  k_pos_add<<<1, 32, 0, st>>>(pos_seq, t - 1);
+  QD_TRY(launch_status());
+  float* logits = m->f(L.logits) + (int64_t)seq * c.vocab;
+  GemvArgs ha;
+  ha.fmt = c.emb_fmt;
+  ha.W = m->W(c.emb_fmt, L.head, c.vocab, D);
+  ha.x = x + (int64_t)(t - 1) * D;
+  ha.y = logits;
+  ha.batch = 1;
+  ha.mode = kGemvArgmax;
+  ha.err = err;
+  ha.am.key = reinterpret_cast<unsigned long long*>(m->s + L.am_key) + seq;
+  ha.am.counter = reinterpret_cast<unsigned int*>(m->s + L.am_cnt);
+  ha.am.tok_out = m->i(L.tok_out) + seq;
+  ha.am.pos = pos_seq;
+  const float* out_norm = reinterpret_cast<const float*>(m->w + L.out_norm);
+  if (gemv_fuses_norm(ha)) {
+    ha.norm_g = out_norm;
+    ha.eps = c.eps;
+    return launch_q_gemv(ha, st);
+  }
+  QD_TRY(launch_rmsnorm(ha.x, out_norm, xn, (int)D, 1, c.eps, st));
+  ha.x = xn;
+  ha.mode = kGemvStore;
+  QD_TRY(launch_q_gemv(ha, st));
+  return launch_argmax(logits, c.vocab, 1, m->i(L.tok_out) + seq, pos_seq, st);
+}
+
 }  // namespace
 
 extern "C" {
@@ -469,6 +641,36 @@ qd_status qd_decode_step(qd_model* m, const int32_t* tokens, int batch, int32_t*
   if (logits_out &&
       cudaMemcpyAsync(logits_out, m->s + m->L.logits, 4 * (size_t)batch * m->cfg.vocab, cudaMemcpyDefault, st) !=
           cudaSuccess)
+    return QD_ERR_CUDA;
+  return QD_OK;
+}
+
+size_t qd_prefill_workspace(const qd_config* cfg, int t) {
+  if (!config_ok(cfg) || cfg->act_q8 || t < 1 || t > QD_MAX_GEMM_TOKENS || t > cfg->max_ctx) return 0;
+  const Layout L = make_layout(cfg);
+  return prefill_layout(*cfg, L.qkv_rows, t).total;
+}
+
+qd_status qd_prefill(qd_model* m, int seq, const int32_t* tokens, int t, unsigned flags, void* workspace,
+                     size_t workspace_bytes, int32_t* out_token, float* logits_out, qd_stream_t stream) {
+  if (!m || !tokens || !out_token || !workspace) return QD_ERR_INVALID_ARG;
+  if (flags & ~QD_PREFILL_EXACT) return QD_ERR_INVALID_ARG;
+  if (m->cfg.act_q8) return QD_ERR_UNSUPPORTED;
+  if (seq < 0 || seq >= m->cfg.max_batch || t < 1 || t > QD_MAX_GEMM_TOKENS || t > m->cfg.max_ctx)
+    return QD_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return QD_ERR_INVALID_ARG;
+  const size_t need = prefill_layout(m->cfg, m->L.qkv_rows, t).total;
+  if (workspace_bytes < need) return QD_ERR_NOMEM;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemcpyAsync(ws + prefill_layout(m->cfg, m->L.qkv_rows, t).tok, tokens, 4 * (size_t)t, cudaMemcpyDefault,
+                      st) != cudaSuccess)
+    return QD_ERR_CUDA;
+  QD_TRY(enqueue_prefill(m, seq, t, flags, ws, st));
+  if (cudaMemcpyAsync(out_token, m->s + m->L.tok_out + 4 * (size_t)seq, 4, cudaMemcpyDefault, st) != cudaSuccess)
+    return QD_ERR_CUDA;
+  if (logits_out && cudaMemcpyAsync(logits_out, m->f(m->L.logits) + (int64_t)seq * m->cfg.vocab,
+                                    4 * (size_t)m->cfg.vocab, cudaMemcpyDefault, st) != cudaSuccess)
     return QD_ERR_CUDA;
   return QD_OK;
 }

@@ -204,3 +204,22 @@ def test_rope_table_host_matches_oracle(lib):
     qd.rope_table(theta, hd, ctx, got.ctypes.data)
     want = oracle.rope_table(theta, hd, ctx)
     assert np.array_equal(got, want)
+
+
+def test_prefill_workspace_sizes(lib):
+    """qd_prefill_workspace: host arithmetic only (no device work); 0 where qd_prefill refuses."""
+    import qdsynth
+
+    cfg = qdsynth.SMOL_135M
+    c = qd.make_config(cfg, max_ctx=256, max_batch=1)
+    w128 = lib.qd_prefill_workspace(ctypes.byref(c), 128)
+    w16 = lib.qd_prefill_workspace(ctypes.byref(c), 16)
+    # at least the t-row activations: x, xn (dim), qkv (dim + 2 kv), q and attention out, act (ffn)
+    per_tok = 4 * (2 * 576 + (576 + 2 * 192) + 2 * 576 + 1536)
+    assert w128 >= 128 * per_tok and w16 >= 16 * per_tok and w128 > w16
+    assert lib.qd_prefill_workspace(ctypes.byref(c), 0) == 0
+    assert lib.qd_prefill_workspace(ctypes.byref(c), 257) == 0  # beyond max_ctx
+    q8 = qd.make_config(cfg, max_ctx=256, max_batch=1, act_q8=True)
+    assert lib.qd_prefill_workspace(ctypes.byref(q8), 16) == 0  # ggml-exact models: refused
+    h = qd.make_config(cfg, max_ctx=256, max_batch=1, kv_f16=True)
+    assert lib.qd_prefill_workspace(ctypes.byref(h), 128) >= 128 * per_tok
