@@ -72,7 +72,22 @@ struct Params {
   uint32_t* err;
   QkvEpilogue qkv;
   ArgmaxEpilogue am;
+  int ksplit;  // CTAs per cluster sharing each row group, each over its own unit steps
+  int maxk;    // row groups per warp at most (the partial-sum slots, ksplit > 1)
 };
+
+// Distributed shared memory (thread-block clusters): store v at this CTA's shared address
+// `addr` as mapped into CTA `rank` of the cluster; and the cluster-wide barrier.
+__device__ __forceinline__ void st_cluster(uint32_t addr, int rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // kGemvQKV: rows r (even) and r+1 of batch b hold a RoPE pair (q or k) or two
 // consecutive v values; rotate and scatter them (see QkvEpilogue).
@@ -332,11 +347,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
   const PackedView& W = p.W;
   const int cols = (int)W.cols;
   const int units = cols / 32;
-  const int iters = (units + 31) / 32;  // unit steps per row group
   const int64_t groups = (W.rows + RW - 1) / RW;
-  // Global warp ids interleave the CTAs (warp-major), so the groups left over after
-  // an even split land on warps spread over every CTA rather than on the first CTAs.
-  const int64_t gw = (int64_t)warp * gridDim.x + blockIdx.x, nw = (int64_t)gridDim.x * kWarps;
+  // Split-K over a cluster of C CTAs: each takes the same row groups over its own
+  // contiguous unit steps [j0, j1) (and builds only those units' x records); the partial
+  // row sums meet in the first CTA, which adds them in CTA order and writes the rows.
+  const int C = p.ksplit;
+  const int rank = C > 1 ? (int)(blockIdx.x % C) : 0;
+  const int64_t ncl = gridDim.x / C, cid = blockIdx.x / C;
+  const int steps_all = (units + 31) / 32;  // unit steps per row group
+  const int j0 = rank * steps_all / C, j1 = (rank + 1) * steps_all / C;
+  const int ua = 32 * j0, ub = min(32 * j1, units);  // this CTA's units
+  if (C > 1) cluster_arrive_relaxed();  // every CTA of the cluster has started (waited below)
+  // Global warp ids interleave the clusters (warp-major), so the groups left over after
+  // an even split land on warps spread over every SM rather than on the first ones.
+  const int64_t gw = (int64_t)warp * ncl + cid, nw = ncl * kWarps;
   constexpr uint32_t SB = slot_bytes<FMT, RW>();
   constexpr int kStages = stages<FMT, RW>();
   uint8_t* ring = smem + (size_t)warp * kStages * SB;
@@ -345,15 +369,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
 
   // ---- start streaming the first steps (weights never depend on the previous kernel)
   int64_t lg = gw;  // group of the next copy
-  int lj = 0;       // its unit step
+  int lj = j0;      // its unit step
   RowPtrs<RW> lrp;
   if (lg < groups) row_ptrs<RW>(lrp, W, lg * RW);
   auto issue = [&](int slot_idx) {
     if (lg < groups) {
       const int u = lane + 32 * lj;
       if (u < units) stage_step<FMT, RW>(ring_s + (uint32_t)slot_idx * SB, lrp, u, lane);
-      if (++lj == iters) {
-        lj = 0;
+      if (++lj == j1) {
+        lj = j0;
         lg += nw;
         if (lg < groups) row_ptrs<RW>(lrp, W, lg * RW);
       }
@@ -379,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
     constexpr int kPass = kWarps * 4;  // units per pass of the CTA
     constexpr int kBatch = 4;          // passes of a warp whose loads are issued together
     auto load = [&](int b, int u, float4& v, float4& g) {
-      const bool ok = u < units;
+      const bool ok = u < ub;
       const int e = k < 4 ? unit_xa<FMT>(u) + 4 * k : unit_xb<FMT>(u) + 4 * (k - 4);
       const float* xr = p.x + (int64_t)b * cols;
       v = ok ? __ldcg(reinterpret_cast<const float4*>(xr + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -388,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
     // this warp's first passes of batch row 0, loaded before the rest of the ring is issued
     float4 v0[kBatch], g0[kBatch];
 #pragma unroll
-    for (int t = 0; t < kBatch; ++t) load(0, warp * 4 + t * kPass + (lane >> 3), v0[t], g0[t]);
+    for (int t = 0; t < kBatch; ++t) load(0, ua + warp * 4 + t * kPass + (lane >> 3), v0[t], g0[t]);
 #pragma unroll
     for (int s = 1; s < kStages - 1; ++s) issue(s);
 #pragma unroll
@@ -403,9 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
           }
           intdot::write_record<FMT>(xq + ((size_t)b * units + u) * kRecBytes, k, ok, v);
         };
-        for (int ub0 = warp * 4; ub0 < units; ub0 += kBatch * kPass) {  // uniform per warp
+        for (int ub0 = ua + warp * 4; ub0 < ub; ub0 += kBatch * kPass) {  // uniform per warp
           float4 vv[kBatch], gg[kBatch];
-          if (b == 0 && ub0 == warp * 4) {
+          if (b == 0 && ub0 == ua + warp * 4) {
 #pragma unroll
             for (int t = 0; t < kBatch; ++t) {
               vv[t] = v0[t];
@@ -417,9 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
           }
 #pragma unroll
           for (int t = 0; t < kBatch; ++t) {
-            if (ub0 + t * kPass >= units) break;  // uniform per warp
+            if (ub0 + t * kPass >= ub) break;  // uniform per warp
             const int u = ub0 + t * kPass + (lane >> 3);
-            record(u, u < units, vv[t], gg[t]);
+            record(u, u < ub, vv[t], gg[t]);
           }
         }
       }
@@ -447,14 +471,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
 #pragma unroll
   for (int b = 0; b < NB; ++b) best[b] = 0ull;
   Acc<NB, RW> acc;
+  constexpr int V = RW * NB, GRP = 32 / V;
+  static_assert(V <= 32, "one reduce-scatter per group");
+  // split-K partial sums, in the first CTA of the cluster: [rank][warp][maxk][V]
+  float* part = reinterpret_cast<float*>(xq + (size_t)NB * units * kRecBytes);
+  const uint32_t part_s = (uint32_t)__cvta_generic_to_shared(part);
+  // Write (or, split, hand over) the V row sums of a finished group: lanes with
+  // lane % GRP == 0 write value kk = lane / GRP (row row0 + kk / NB, batch row kk % NB);
+  // `partner` is the next row's value (same batch row) for the pair epilogues.
+  auto emit = [&](int64_t row0, float tot, float partner, const EpiPrefetch& pf_) {
+    if ((lane % GRP) != 0) return;
+    const int kk = lane / GRP, rr = kk / NB, b = kk % NB;
+    const int64_t r = row0 + rr;
+    if (b >= p.batch || r >= W.rows) return;
+    if (p.mode == kGemvSwiGLU) {
+      if ((rr & 1) == 0 && r + 1 < W.rows) p.y[(int64_t)b * (W.rows / 2) + r / 2] = tot / (1.0f + expf(-tot)) * partner;
+    } else if (p.mode == kGemvQKV) {
+      if ((rr & 1) == 0 && r + 1 < W.rows) qkv_pair_out(p, r, b, tot, partner, pf_);
+    } else {
+      if (p.mode == kGemvArgmax) {
+        const unsigned long long key = argmax_key(tot, (uint32_t)r);
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb)
+          if (bb == b) best[bb] = key > best[bb] ? key : best[bb];
+      }
+      float* dst = p.y + (int64_t)b * W.rows + r;
+      *dst = p.mode == kGemvAccumulate ? pf_.y_old + tot : tot;
+    }
+  };
+  if (C > 1) cluster_wait();  // the partial-sum slots of the first CTA exist from here on
   int cs = 0;  // slot of the step being computed
-  int j = 0;
+  int j = j0;
+  int kg = 0;  // this warp's finished groups
   for (int64_t g = gw; g < groups;) {
     __syncwarp();  // every lane is done with the slot about to be refilled
     issue(cs == 0 ? kStages - 1 : cs - 1);
     cp_wait<kStages - 1>();  // this step's group of copies has landed
     __syncwarp();            // ...for every lane (scales are shared across lanes)
-    if (j == 0) {
+    if (j == j0) {
 #pragma unroll
       for (int rr = 0; rr < RW; ++rr)
 #pragma unroll
@@ -469,8 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
       for (int rr = 0; rr < RW; ++rr) rsc[rr] = *reinterpret_cast<const float*>(slot + slot_code_bytes<FMT, RW>() + rr * 64);
     }
     cs = (cs + 1 == kStages) ? 0 : cs + 1;
-    if (++j < iters) continue;
-    j = 0;
+    if (++j < j1) continue;
+    j = j0;
 
     // ---- end of a group: reduce and write its RW rows
     const int64_t row0 = g * RW;
@@ -480,8 +534,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
 #pragma unroll
         for (int b = 0; b < NB; ++b) acc.v[rr][b] *= rsc[rr];
     }
-    constexpr int V = RW * NB, GRP = 32 / V;
-    static_assert(V <= 32, "one reduce-scatter per group");
     float v[V];
 #pragma unroll
     for (int rr = 0; rr < RW; ++rr)
@@ -492,30 +544,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
 #pragma unroll
     for (int b = 1; b < NB; ++b) iv = kb == b ? inv[b] : iv;
     const float tot = reduce_scatter<V>(v, lane) * iv;
-    const float partner = __shfl_down_sync(0xffffffffu, tot, (NB * GRP) & 31);  // row +1, same batch
-    if ((lane % GRP) == 0) {
-      const int kk = lane / GRP, rr = kk / NB, b = kk % NB;
-      const int64_t r = row0 + rr;
-      if (b < p.batch && r < W.rows) {
-        if (p.mode == kGemvSwiGLU) {
-          if ((rr & 1) == 0 && r + 1 < W.rows)
-            p.y[(int64_t)b * (W.rows / 2) + r / 2] = tot / (1.0f + expf(-tot)) * partner;
-        } else if (p.mode == kGemvQKV) {
-          if ((rr & 1) == 0 && r + 1 < W.rows) qkv_pair_out(p, r, b, tot, partner, pf);
-        } else {
-          if (p.mode == kGemvArgmax) {
-            const unsigned long long key = argmax_key(tot, (uint32_t)r);
-#pragma unroll
-            for (int bb = 0; bb < NB; ++bb)
-              if (bb == b) best[bb] = key > best[bb] ? key : best[bb];
-          }
-          float* dst = p.y + (int64_t)b * W.rows + r;
-          *dst = p.mode == kGemvAccumulate ? pf.y_old + tot : tot;
-        }
-      }
+    if (C > 1) {
+      // this CTA's part of the group, to slot [rank][warp][kg] of the first CTA
+      if ((lane % GRP) == 0)
+        st_cluster(part_s + 4u * (uint32_t)(((rank * kWarps + warp) * p.maxk + kg) * V + lane / GRP), 0, tot);
+      ++kg;
+      g += nw;
+      continue;
     }
+    const float partner = __shfl_down_sync(0xffffffffu, tot, (NB * GRP) & 31);  // row +1, same batch
+    emit(row0, tot, partner, pf);
     g += nw;
     if (g < groups) pf = epi_prefetch<NB, RW>(p, g, lane);
+  }
+  if (C > 1) {
+    // every part has landed in the first CTA, which adds them in CTA order and writes
+    cp_wait<0>();
+    cluster_arrive();
+    cluster_wait();
+    if (rank == 0) {
+      int k = 0;
+      for (int64_t g = gw; g < groups; g += nw, ++k) {
+        const EpiPrefetch pf2 = epi_prefetch<NB, RW>(p, g, lane);
+        float tot = 0.f;
+        for (int r = 0; r < C; ++r) tot += part[((r * kWarps + warp) * p.maxk + k) * V + lane / GRP];
+        const float partner = __shfl_down_sync(0xffffffffu, tot, (NB * GRP) & 31);
+        emit(g * RW, tot, partner, pf2);
+      }
+    }
   }
   cp_wait<0>();  // no copy may still target this CTA's shared memory at exit
   if (p.mode == kGemvArgmax) {
@@ -586,9 +642,10 @@ int resident_ctas(K kern, size_t smem) {
 }
 
 template <int FMT, int NB, int RW>
-size_t smem_bytes_t(int64_t cols) {
+size_t smem_bytes_t(int64_t cols, int ksplit = 1, int maxk = 0) {
   const size_t units = (size_t)cols / 32;
-  return (size_t)kWarps * stages<FMT, RW>() * slot_bytes<FMT, RW>() + (size_t)NB * units * kRecBytes;
+  const size_t part = ksplit > 1 ? (size_t)ksplit * kWarps * maxk * RW * NB * 4 : 0;
+  return (size_t)kWarps * stages<FMT, RW>() * slot_bytes<FMT, RW>() + (size_t)NB * units * kRecBytes + part;
 }
 
 // Rows per group available for NB batch rows (more rows would spill registers).
@@ -645,65 +702,117 @@ bool smem_attr_set() {
 template <int FMT, int NB, int RW>
 qd_status launch_rw(const Params& p, bool pdl, cudaStream_t stream, int64_t ctas) {
   auto kern = k_gemv_warp<FMT, NB, RW>;
-  const size_t smem = smem_bytes_t<FMT, NB, RW>(p.W.cols);
+  const size_t smem = smem_bytes_t<FMT, NB, RW>(p.W.cols, p.ksplit, p.maxk);
+  if (smem > kSmemCap) return QD_ERR_UNSUPPORTED;
   if (!smem_attr_set<FMT, NB, RW>()) return QD_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (p.ksplit > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)p.ksplit;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return QD_ERR_CUDA;
+  cfg.numAttrs = na;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) {
+    cudaGetLastError();
+    return QD_ERR_CUDA;
+  }
   return QD_OK;
 }
 
-// CTAs for RW rows per group: one wave of at most kCtasPerSm CTAs per SM (0 when the
-// shared memory does not fit).  One CTA (8 warps) per SM measured as fast as two on
-// the large shapes and faster on several (the streams already fill the DRAM queues),
-// and it leaves room for the next kernel's CTAs to start their weight copies early.
+// At most kCtasPerSm CTAs per SM, one wave.  One CTA (8 warps) per SM measured as fast as
+// two on the large shapes and faster on several (the streams already fill the DRAM
+// queues), and it leaves room for the next kernel's CTAs to start their weight copies early.
 #ifndef QD_GEMV_CTAS_PER_SM
 #define QD_GEMV_CTAS_PER_SM 1
 #endif
 constexpr int kCtasPerSm = QD_GEMV_CTAS_PER_SM;
+
+// Launch geometry of one candidate: rows per group, CTAs per cluster (split-K), CTAs and
+// the partial-sum slots per warp.
+struct Geometry {
+  int rw = 0, ksplit = 1, maxk = 0;
+  int64_t ctas = 0;
+};
+
+// CTAs for RW rows per group split over `ksplit` CTAs per cluster: one warp per group up to
+// one wave of at most kCtasPerSm CTAs per SM, whole clusters (ctas 0 when the shared memory
+// does not fit).
 template <int FMT, int NB, int RW>
-int64_t ctas_for(int64_t rows, int64_t cols) {
-  const size_t smem = smem_bytes_t<FMT, NB, RW>(cols);
-  if (smem > kSmemCap || !smem_attr_set<FMT, NB, RW>()) return 0;
+Geometry geometry_for(int64_t rows, int64_t cols, int ksplit) {
+  Geometry gm;
+  gm.rw = RW;
+  gm.ksplit = ksplit;
+  if (smem_bytes_t<FMT, NB, RW>(cols) > kSmemCap || !smem_attr_set<FMT, NB, RW>()) return gm;
   const int64_t groups = (rows + RW - 1) / RW;
-  const int64_t want = (groups + kWarps - 1) / kWarps;
-  int per_sm = resident_ctas(k_gemv_warp<FMT, NB, RW>, smem);
+  int per_sm = resident_ctas(k_gemv_warp<FMT, NB, RW>, smem_bytes_t<FMT, NB, RW>(cols));
   if (per_sm > kCtasPerSm) per_sm = kCtasPerSm;
-  const int64_t cap = (int64_t)sm_count() * per_sm;
-  return want < cap ? want : cap;
+  const int64_t cap_cl = (int64_t)sm_count() * per_sm / ksplit;
+  int64_t cl = (groups + kWarps - 1) / kWarps;
+  if (cl > cap_cl) cl = cap_cl;
+  if (cl < 1) return gm;
+  gm.maxk = ksplit > 1 ? (int)((groups + cl * kWarps - 1) / (cl * kWarps)) : 0;
+  if (smem_bytes_t<FMT, NB, RW>(cols, ksplit, gm.maxk) > kSmemCap) return gm;
+  gm.ctas = cl * ksplit;
+  return gm;
+}
+
+// Split-K across CTAs (a cluster of two sharing each row group) for the tall-and-thin
+// products where it measured faster: store and accumulate without the fused norm (whose
+// sum of squares spans all columns), 1024 rows or more and at least twice as many
+// columns, at batch 2 or more (4096x11008 Q4_0 at batch 2: 17.7 -> 16.5 us; 2048x8192
+// INT8: 10.0 -> 9.1 us) or with 8-bit weights (Q8_0 4096x11008: 12.8 -> 12.5 us).  At
+// batch 1 with 4-bit weights, on the small decode shapes (576x1536: 3.1 -> 3.3 us), and
+// with clusters of four it measured slower: clusters wait for groups of free SMs while
+// the previous kernel still holds them.
+int choose_ksplit(const Params& p, int fmt, int nb) {
+  if (p.norm_g || (p.mode != kGemvStore && p.mode != kGemvAccumulate)) return 1;
+  const int64_t rows = p.W.rows, cols = p.W.cols;
+  if (rows < 1024 || cols < 2 * rows) return 1;
+  if (nb >= 2 || fmt == QD_Q8_0 || fmt == QD_I8_ROW) return 2;
+  return 1;
 }
 
 // Rows per group: the choice whose groups split most evenly over the warps (the kernel
-// lasts as long as its busiest warp), preferring more rows (more reuse of staged x).
+// lasts as long as its busiest warp), preferring more rows (more reuse of staged x); then
+// the split over a cluster (choose_ksplit).
 template <int FMT, int NB>
-qd_status launch_inst(const Params& p, bool pdl, cudaStream_t stream) {
+qd_status launch_inst(Params p, bool pdl, cudaStream_t stream) {
   const int64_t rows = p.W.rows, cols = p.W.cols;
   constexpr int kMax = max_rw<NB>(), kMin = min_rw<NB>();
   const bool pairs = p.mode == kGemvSwiGLU || p.mode == kGemvQKV;  // need even rows per group
+  auto geo = [&](int rw, int ks) {
+    Geometry g;
+    if constexpr (kMax >= 4) {
+      if (rw == 4) g = geometry_for<FMT, NB, 4>(rows, cols, ks);
+    }
+    if (rw == 2) g = geometry_for<FMT, NB, 2>(rows, cols, ks);
+    if constexpr (kMin <= 1) {
+      if (rw == 1) g = geometry_for<FMT, NB, 1>(rows, cols, ks);
+    }
+    return g;
+  };
   double best = -1.0;
-  int brw = 0;
-  int64_t bctas = 0;
+  Geometry bg;
   for (int rw : {4, 2, 1}) {
     if (rw > kMax || rw < kMin || (pairs && rw == 1)) continue;
-    int64_t ctas = 0;
-    if constexpr (kMax >= 4) {
-      if (rw == 4) ctas = ctas_for<FMT, NB, 4>(rows, cols);
-    }
-    if (rw == 2) ctas = ctas_for<FMT, NB, 2>(rows, cols);
-    if constexpr (kMin <= 1) {
-      if (rw == 1) ctas = ctas_for<FMT, NB, 1>(rows, cols);
-    }
-    if (ctas <= 0) continue;
+    const Geometry g = geo(rw, 1);
+    if (g.ctas <= 0) continue;
     const int64_t groups = (rows + rw - 1) / rw;
-    const int64_t slots = ctas * kWarps;
+    const int64_t slots = g.ctas * kWarps;
     const int64_t rounds = (groups + slots - 1) / slots;
     double score;
     if (rounds <= 1) {
@@ -716,16 +825,24 @@ qd_status launch_inst(const Params& p, bool pdl, cudaStream_t stream) {
     }
     if (score > best) {
       best = score;
-      brw = rw;
-      bctas = ctas;
+      bg = g;
     }
   }
-  if constexpr (kMax >= 4) {
-    if (brw == 4) return launch_rw<FMT, NB, 4>(p, pdl, stream, bctas);
+  if (bg.ctas <= 0) return QD_ERR_UNSUPPORTED;
+  const int steps_all = (int)((cols / 32 + 31) / 32);
+  const int ks = choose_ksplit(p, FMT, NB);
+  if (ks > 1 && ks <= steps_all) {
+    const Geometry g = geo(bg.rw, ks);
+    if (g.ctas > 0) bg = g;
   }
-  if (brw == 2) return launch_rw<FMT, NB, 2>(p, pdl, stream, bctas);
+  p.ksplit = bg.ksplit;
+  p.maxk = bg.maxk;
+  if constexpr (kMax >= 4) {
+    if (bg.rw == 4) return launch_rw<FMT, NB, 4>(p, pdl, stream, bg.ctas);
+  }
+  if (bg.rw == 2) return launch_rw<FMT, NB, 2>(p, pdl, stream, bg.ctas);
   if constexpr (kMin <= 1) {
-    if (brw == 1) return launch_rw<FMT, NB, 1>(p, pdl, stream, bctas);
+    if (bg.rw == 1) return launch_rw<FMT, NB, 1>(p, pdl, stream, bg.ctas);
   }
   return QD_ERR_UNSUPPORTED;
 }
@@ -762,6 +879,8 @@ qd_status launch_q_gemv_stream(const GemvArgs& a, cudaStream_t stream) {
   p.err = a.err;
   p.qkv = a.qkv;
   p.am = a.am;
+  p.ksplit = 1;
+  p.maxk = 0;
   const int nb = nb_for(a.batch);
 #define QD_NB_SWITCH(F)                                      \
   switch (nb) {                                              \

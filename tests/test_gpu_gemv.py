@@ -172,6 +172,23 @@ def test_q_gemv_is_deterministic(qd):
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("fmt,rows,cols,batch", [("q4_0", 1024, 3072, 2), ("q4_0", 2048, 8192, 2),
+                                                 ("q8_0", 2048, 8192, 1), ("i8", 2048, 8192, 1), ("i8", 2048, 8192, 2),
+                                                 ("q4_k", 1024, 4096, 2), ("q8_0", 1042, 4160, 2)])
+def test_q_gemv_split_k_tall_thin(qd, fmt, rows, cols, batch):
+    """Tall-and-thin products (1024 rows or more, at least twice as many columns) at batch
+    2, or with 8-bit weights, split their columns over a cluster of two CTAs whose partial
+    row sums meet in the first one and are added in CTA order: every row against the
+    oracle, and two runs give the same bits (1042x4160: ragged row groups and an odd
+    number of 32-unit steps)."""
+    src, p = weights(qd, fmt, 15, f"sk.{fmt}.{rows}x{cols}", rows, cols)
+    x = qdsynth.activations(15, f"sk.x{cols}", batch, cols)
+    got = _gemv(qd, fmt, p, rows, cols, x)
+    assert_close(got, oracle.gemv(fmt, src, rows, cols, x), tol=2e-5, what=f"{fmt} {rows}x{cols} b{batch}")
+    again = _gemv(qd, fmt, p, rows, cols, x)
+    assert np.array_equal(got.view(np.uint32), again.view(np.uint32))
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("batch", [1, 2, 8])
 def test_q_gemv_activation_planes_precision(qd, fmt, batch):
