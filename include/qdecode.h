@@ -104,8 +104,8 @@ typedef enum {
  *            value q*s_row.
  * The "source" layout of a tensor is the model-file layout above, rows in order
  * (for QD_I8_ROW: all codes, then all scales, in one buffer).  The decode step
- * (qd_model_*) takes QD_Q4_0, QD_Q8_0, QD_Q4_K and QD_I8_ROW; the layout calls,
- * qd_dequant, qd_embed and qd_q_gemv take every format. */
+ * (qd_model_*) takes every format but QD_I4_ROW, for each class of layer matrix and for
+ * the embedding; the layout calls, qd_dequant, qd_embed and qd_q_gemv take every format. */
 typedef enum {
     QD_Q4_0 = 0,
     QD_Q8_0 = 1,
@@ -392,9 +392,17 @@ typedef struct {
                     /* read back exactly; half the cache bytes)                   */
     int act_q8;     /* 0: products over f32 activations; 1: every quantised       */
                     /* product over Q8_0 activations (qd_quantize_q8 rule) in     */
-                    /* integers (go-llm's ggml-exact products); w_fmt and emb_fmt */
-                    /* must then be QD_Q4_0 or QD_Q8_0.  With kv_f16 = 1 this is  */
-                    /* the pages' whole ggml-exact mode.                           */
+                    /* integers (go-llm's ggml-exact products); the layer formats */
+                    /* and emb_fmt must then be QD_Q4_0 or QD_Q8_0.  With kv_f16 = */
+                    /* 1 this is the pages' whole ggml-exact mode.                 */
+    int mixed_fmt;  /* 0: every layer matrix takes w_fmt; 1: each class takes its  */
+                    /* own format below and w_fmt is unused (model files mix      */
+                    /* formats by tensor, e.g. Q4_K with Q6_K: [llamini] "Quants", */
+                    /* [go-llm] package overview)                                  */
+    qd_fmt qkv_fmt;     /* wq, wk, wv (one fused matrix)                           */
+    qd_fmt wo_fmt;      /* attention output                                       */
+    qd_fmt gate_up_fmt; /* wg, wu (one fused matrix)                              */
+    qd_fmt down_fmt;    /* wd                                                     */
 } qd_config;
 
 typedef struct qd_model qd_model;

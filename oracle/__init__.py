@@ -51,7 +51,9 @@ class _Config(ctypes.Structure):
                 ("n_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("vocab", ctypes.c_int), ("max_ctx", ctypes.c_int), ("rope_theta", ctypes.c_double),
                 ("eps", ctypes.c_double), ("pairing", ctypes.c_int), ("w_fmt", ctypes.c_int),
-                ("emb_fmt", ctypes.c_int), ("kv_f16", ctypes.c_int), ("act_q8", ctypes.c_int)]
+                ("emb_fmt", ctypes.c_int), ("kv_f16", ctypes.c_int), ("act_q8", ctypes.c_int),
+                ("qkv_fmt", ctypes.c_int), ("wo_fmt", ctypes.c_int), ("gate_up_fmt", ctypes.c_int),
+                ("down_fmt", ctypes.c_int)]
 
 
 class _Q8TF(ctypes.Structure):
@@ -370,7 +372,8 @@ class Model:
         self._c = _Config(cfg["layers"], cfg["dim"], cfg["ffn"], cfg["n_heads"], cfg["n_kv_heads"],
                           cfg["head_dim"], cfg["vocab"], cfg["max_ctx"], cfg["rope_theta"], cfg["eps"],
                           PAIRING[cfg["pairing"]], FMT[cfg["w_fmt"]], FMT[cfg["emb_fmt"]],
-                          1 if cfg.get("kv_f16") else 0, 1 if cfg.get("act_q8") else 0)
+                          1 if cfg.get("kv_f16") else 0, 1 if cfg.get("act_q8") else 0,
+                          *[FMT[cfg.get(k, cfg["w_fmt"])] for k in ("qkv_fmt", "wo_fmt", "gate_up_fmt", "down_fmt")])
 
     def decode_step(self, k_cache: np.ndarray, v_cache: np.ndarray, layer_stride: int, pos: int,
                     token: int, seq_offset: int = 0):

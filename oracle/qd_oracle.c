@@ -706,6 +706,10 @@ typedef struct {
     int act_q8; /* 1: every quantised product takes its activations (rounded to f32) as Q8_0
                  * -- Q8_1 for Q4_1 weights -- and multiplies in integers ([go-llm]
                  * "ExactGGML"; or_quantize_q8, or_gemv_q8act) */
+    /* the format of each class of layer matrix: wq, wk, wv; wo; wg, wu; wd (model files
+     * mix formats by tensor: [llamini] "Quants", [go-llm] package overview).  w_fmt is the
+     * format of a model that does not mix; the caller sets all four to it then. */
+    int qkv_fmt, wo_fmt, gate_up_fmt, down_fmt;
 } or_config;
 
 int or_quantize_q8(const float* x, int64_t n, int8_t* q, float* d16, float* s16);
@@ -797,9 +801,9 @@ int or_decode_step_tf(const or_config* c, const void* const* tensors, float* k_c
         float* vl = v_cache + (int64_t)l * layer_stride;
         /* attention block */
         or_rmsnorm_d(x, (const float*)L[0], D, c->eps, xn);
-        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[1], QD, D, xn, q, tf, 4 * l)) ||
-            (rc = product(c, c->w_fmt, (const uint8_t*)L[2], KD, D, xn, k, tf, 4 * l)) ||
-            (rc = product(c, c->w_fmt, (const uint8_t*)L[3], KD, D, xn, v, tf, 4 * l)))
+        if ((rc = product(c, c->qkv_fmt, (const uint8_t*)L[1], QD, D, xn, q, tf, 4 * l)) ||
+            (rc = product(c, c->qkv_fmt, (const uint8_t*)L[2], KD, D, xn, k, tf, 4 * l)) ||
+            (rc = product(c, c->qkv_fmt, (const uint8_t*)L[3], KD, D, xn, v, tf, 4 * l)))
             goto done;
         for (int h = 0; h < hq; ++h) or_rope_head_d(q + (int64_t)h * hd, hd, pos, c->pairing, c->rope_theta);
         for (int h = 0; h < hk; ++h) or_rope_head_d(k + (int64_t)h * hd, hd, pos, c->pairing, c->rope_theta);
@@ -820,15 +824,15 @@ int or_decode_step_tf(const or_config* c, const void* const* tensors, float* k_c
                 }
             }
         or_attention_d(q, kl, vl, hq, hk, hd, pos + 1, c->max_ctx, att);
-        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[4], D, QD, att, t, tf, 4 * l + 1))) goto done;
+        if ((rc = product(c, c->wo_fmt, (const uint8_t*)L[4], D, QD, att, t, tf, 4 * l + 1))) goto done;
         for (int i = 0; i < D; ++i) x[i] += t[i];
         /* feed-forward block */
         or_rmsnorm_d(x, (const float*)L[5], D, c->eps, xn);
-        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[6], F, D, xn, g, tf, 4 * l + 2)) ||
-            (rc = product(c, c->w_fmt, (const uint8_t*)L[7], F, D, xn, u, tf, 4 * l + 2)))
+        if ((rc = product(c, c->gate_up_fmt, (const uint8_t*)L[6], F, D, xn, g, tf, 4 * l + 2)) ||
+            (rc = product(c, c->gate_up_fmt, (const uint8_t*)L[7], F, D, xn, u, tf, 4 * l + 2)))
             goto done;
         for (int i = 0; i < F; ++i) g[i] = or_silu(g[i]) * u[i];
-        if ((rc = product(c, c->w_fmt, (const uint8_t*)L[8], D, F, g, t, tf, 4 * l + 3))) goto done;
+        if ((rc = product(c, c->down_fmt, (const uint8_t*)L[8], D, F, g, t, tf, 4 * l + 3))) goto done;
         for (int i = 0; i < D; ++i) x[i] += t[i];
     }
     or_rmsnorm_d(x, (const float*)tensors[1], D, c->eps, xn);

@@ -334,6 +334,17 @@ def layer_shapes(cfg: dict):
             ("wg", F, D), ("wu", F, D), ("wd", D, F)]
 
 
+# The class of each layer matrix and the config key of its format (a mixed model names
+# them; otherwise every matrix takes w_fmt).
+MATRIX_CLASS = {"wq": "qkv_fmt", "wk": "qkv_fmt", "wv": "qkv_fmt", "wo": "wo_fmt", "wg": "gate_up_fmt",
+                "wu": "gate_up_fmt", "wd": "down_fmt"}
+
+
+def matrix_fmt(cfg: dict, name: str) -> str:
+    """The format of layer matrix `name` (wq .. wd) in a model config."""
+    return cfg.get(MATRIX_CLASS[name], cfg["w_fmt"])
+
+
 def model_tensors(cfg: dict, seed: int, tied: bool = True) -> list:
     """All tensors of a synthetic model as flat numpy arrays, in the order above."""
     D = cfg["dim"]
@@ -348,7 +359,7 @@ def model_tensors(cfg: dict, seed: int, tied: bool = True) -> list:
                 t.append(norm_gains(seed, p + name, D))
             else:
                 r, c = shapes[name]
-                t.append(weight_src(cfg["w_fmt"], seed, p + name, r, c))
+                t.append(weight_src(matrix_fmt(cfg, name), seed, p + name, r, c))
     return t
 
 
@@ -356,5 +367,5 @@ def model_weight_src_bytes(cfg: dict, tied: bool = True) -> int:
     """Bytes of all model-file-layout weight tensors (norm gains included)."""
     D = cfg["dim"]
     n = src_bytes(cfg["emb_fmt"], cfg["vocab"], D) * (1 if tied else 2) + 4 * D
-    per = sum(src_bytes(cfg["w_fmt"], r, c) for _, r, c in layer_shapes(cfg)) + 8 * D
+    per = sum(src_bytes(matrix_fmt(cfg, n), r, c) for n, r, c in layer_shapes(cfg)) + 8 * D
     return n + cfg["layers"] * per

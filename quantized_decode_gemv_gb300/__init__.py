@@ -51,7 +51,9 @@ class Config(ctypes.Structure):
                 ("vocab", ctypes.c_int), ("max_ctx", ctypes.c_int), ("max_batch", ctypes.c_int),
                 ("rope_theta", ctypes.c_float), ("eps", ctypes.c_float), ("pairing", ctypes.c_int),
                 ("w_fmt", ctypes.c_int), ("emb_fmt", ctypes.c_int), ("tied", ctypes.c_int),
-                ("kv_f16", ctypes.c_int), ("act_q8", ctypes.c_int)]
+                ("kv_f16", ctypes.c_int), ("act_q8", ctypes.c_int), ("mixed_fmt", ctypes.c_int),
+                ("qkv_fmt", ctypes.c_int), ("wo_fmt", ctypes.c_int), ("gate_up_fmt", ctypes.c_int),
+                ("down_fmt", ctypes.c_int)]
 
 
 def build(force: bool = False) -> str:
@@ -308,12 +310,18 @@ def embed(fmt, E, vocab, dim, tokens, batch, x, stream=None):
 def make_config(cfg: dict, max_ctx: int, max_batch: int, tied: bool = True, kv_f16: bool | None = None,
                 act_q8: bool | None = None) -> Config:
     """kv_f16: binary16 KV cache (default: cfg.get("kv_f16", False)); act_q8: products over
-    Q8_0 activations (default: cfg.get("act_q8", False))."""
+    Q8_0 activations (default: cfg.get("act_q8", False)).  A config naming any of qkv_fmt,
+    wo_fmt, gate_up_fmt or down_fmt is a mixed-format model (the classes it does not name
+    take w_fmt)."""
     f16 = cfg.get("kv_f16", False) if kv_f16 is None else kv_f16
     q8 = cfg.get("act_q8", False) if act_q8 is None else act_q8
+    classes = ("qkv_fmt", "wo_fmt", "gate_up_fmt", "down_fmt")
+    mixed = any(k in cfg for k in classes)
+    per = [FMT[cfg.get(k, cfg["w_fmt"])] for k in classes]
     return Config(cfg["layers"], cfg["dim"], cfg["ffn"], cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"],
                   cfg["vocab"], max_ctx, max_batch, cfg["rope_theta"], cfg["eps"], PAIRING[cfg["pairing"]],
-                  FMT[cfg["w_fmt"]], FMT[cfg["emb_fmt"]], 1 if tied else 0, 1 if f16 else 0, 1 if q8 else 0)
+                  FMT[cfg["w_fmt"]], FMT[cfg["emb_fmt"]], 1 if tied else 0, 1 if f16 else 0, 1 if q8 else 0,
+                  1 if mixed else 0, *per)
 
 
 class Model:

@@ -225,7 +225,7 @@ const char* qd_status_str(qd_status s) {
   }
 }
 
-int qd_abi_version(void) { return 3; }
+int qd_abi_version(void) { return 4; }
 
 size_t qd_src_bytes(qd_fmt fmt, int64_t rows, int64_t cols) { return src_bytes(fmt, rows, cols); }
 size_t qd_packed_bytes(qd_fmt fmt, int64_t rows, int64_t cols) { return packed_bytes(fmt, rows, cols); }

@@ -44,6 +44,20 @@ struct Layout {
   int64_t qkv_rows, cache_batch_stride, cache_layer_stride;
 };
 
+// The format of each class of layer matrix (w_fmt for all of them unless mixed_fmt).
+inline int fmt_qkv(const qd_config& c) { return c.mixed_fmt ? c.qkv_fmt : c.w_fmt; }
+inline int fmt_wo(const qd_config& c) { return c.mixed_fmt ? c.wo_fmt : c.w_fmt; }
+inline int fmt_gu(const qd_config& c) { return c.mixed_fmt ? c.gate_up_fmt : c.w_fmt; }
+inline int fmt_down(const qd_config& c) { return c.mixed_fmt ? c.down_fmt : c.w_fmt; }
+inline bool uniform_fmt(const qd_config& c) {
+  return fmt_qkv(c) == fmt_wo(c) && fmt_wo(c) == fmt_gu(c) && fmt_gu(c) == fmt_down(c);
+}
+// Formats the decode step takes: every one but per-row INT4.  The streaming and tensor-
+// core GEMVs fuse the norm and the epilogues for theirs; for the others the step runs the
+// norm, the QKV epilogue and the argmax as separate kernels.
+inline bool step_fmt_ok(int fmt) { return fmt_ok(fmt) && fmt != QD_I4_ROW; }
+inline bool q8_fmt(int fmt) { return fmt == QD_Q4_0 || fmt == QD_Q8_0; }
+
 bool config_ok(const qd_config* c) {
   if (!c) return false;
   if (c->layers < 1 || c->dim < 1 || c->ffn < 1 || c->n_heads < 1 || c->n_kv_heads < 1 || c->vocab < 1) return false;
@@ -53,14 +67,16 @@ bool config_ok(const qd_config* c) {
   if (c->pairing != QD_ROPE_ADJACENT && c->pairing != QD_ROPE_HALF) return false;
   if (c->kv_f16 != 0 && c->kv_f16 != 1) return false;
   if (c->act_q8 != 0 && c->act_q8 != 1) return false;
-  // the integer products over Q8_0 activations take Q4_0 and Q8_0 weights
-  if (c->act_q8 && ((c->w_fmt != QD_Q4_0 && c->w_fmt != QD_Q8_0) || (c->emb_fmt != QD_Q4_0 && c->emb_fmt != QD_Q8_0)))
+  if (c->mixed_fmt != 0 && c->mixed_fmt != 1) return false;
+  const int fq = fmt_qkv(*c), fo = fmt_wo(*c), fg = fmt_gu(*c), fd = fmt_down(*c);
+  if (!step_fmt_ok(fq) || !step_fmt_ok(fo) || !step_fmt_ok(fg) || !step_fmt_ok(fd) || !step_fmt_ok(c->emb_fmt))
     return false;
-  if (!model_fmt_ok(c->w_fmt) || !model_fmt_ok(c->emb_fmt)) return false;
+  // the integer products over Q8_0 activations take Q4_0 and Q8_0 weights
+  if (c->act_q8 && !(q8_fmt(fq) && q8_fmt(fo) && q8_fmt(fg) && q8_fmt(fd) && q8_fmt(c->emb_fmt))) return false;
   if (!(c->eps >= 0.f) || !(c->rope_theta > 0.f)) return false;
   const int64_t QD = (int64_t)c->n_heads * c->head_dim, KD = (int64_t)c->n_kv_heads * c->head_dim;
-  if (!shape_ok(c->w_fmt, QD + 2 * KD, c->dim) || !shape_ok(c->w_fmt, c->dim, QD) ||
-      !shape_ok(c->w_fmt, 2 * (int64_t)c->ffn, c->dim) || !shape_ok(c->w_fmt, c->dim, c->ffn))
+  if (!shape_ok(fq, QD + 2 * KD, c->dim) || !shape_ok(fo, c->dim, QD) || !shape_ok(fg, 2 * (int64_t)c->ffn, c->dim) ||
+      !shape_ok(fd, c->dim, c->ffn))
     return false;
   if (!shape_ok(c->emb_fmt, c->vocab, c->dim)) return false;
   return true;
@@ -85,10 +101,10 @@ Layout make_layout(const qd_config* c) {
     LayerOff& o = L.layer[l];
     o.attn_norm = take(4 * D);
     o.ffn_norm = take(4 * D);
-    o.wqkv = take(packed_bytes(c->w_fmt, L.qkv_rows, D));
-    o.wo = take(packed_bytes(c->w_fmt, D, QD));
-    o.wgu = take(packed_bytes(c->w_fmt, 2 * F, D));
-    o.wd = take(packed_bytes(c->w_fmt, D, F));
+    o.wqkv = take(packed_bytes(fmt_qkv(*c), L.qkv_rows, D));
+    o.wo = take(packed_bytes(fmt_wo(*c), D, QD));
+    o.wgu = take(packed_bytes(fmt_gu(*c), 2 * F, D));
+    o.wd = take(packed_bytes(fmt_down(*c), D, F));
   }
   L.weight_bytes = off;
 
@@ -235,7 +251,8 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
     void* kc = m->s + L.kc + (int64_t)l * L.cache_layer_stride * esz;
     void* vc = m->s + L.vc + (int64_t)l * L.cache_layer_stride * esz;
     // QKV projection with RoPE and the cache append fused into its epilogue
-    GemvArgs qa = args(c.w_fmt, m->W(c.w_fmt, o.wqkv, L.qkv_rows, D), x, qkv, kGemvQKV);
+    const int fq = fmt_qkv(c), fo = fmt_wo(c), fg = fmt_gu(c), fd = fmt_down(c);
+    GemvArgs qa = args(fq, m->W(fq, o.wqkv, L.qkv_rows, D), x, qkv, kGemvQKV);
     QkvEpilogue& e = qa.qkv;
     e.q_rows = (int)QD;
     e.k_rows = (int)KD;
@@ -252,7 +269,7 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
     e.max_ctx = c.max_ctx;
     const float* attn_norm = reinterpret_cast<const float*>(m->w + o.attn_norm);
     if (c.act_q8) {
-      QD_TRY(q8prod(4 * l, c.w_fmt, qa.W, x, attn_norm, qkv, kGemvStore));
+      QD_TRY(q8prod(4 * l, fq, qa.W, x, attn_norm, qkv, kGemvStore));
       QD_TRY(launch_qkv_post(qkv, L.qkv_rows, batch, e, err, st, true));
       ++n;
     } else if (gemv_fuses_norm(qa)) {
@@ -274,17 +291,17 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
                                       c.head_dim, pos, c.max_ctx, batch, err, st, true));
     ++n;
     if (c.act_q8) {
-      QD_TRY(q8prod(4 * l + 1, c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, nullptr, x, kGemvAccumulate));
-      QD_TRY(q8prod(4 * l + 2, c.w_fmt, m->W(c.w_fmt, o.wgu, 2 * F, D), x, reinterpret_cast<const float*>(m->w + o.ffn_norm),
+      QD_TRY(q8prod(4 * l + 1, fo, m->W(fo, o.wo, D, QD), att, nullptr, x, kGemvAccumulate));
+      QD_TRY(q8prod(4 * l + 2, fg, m->W(fg, o.wgu, 2 * F, D), x, reinterpret_cast<const float*>(m->w + o.ffn_norm),
                     act, kGemvSwiGLU));
-      QD_TRY(q8prod(4 * l + 3, c.w_fmt, m->W(c.w_fmt, o.wd, D, F), act, nullptr, x, kGemvAccumulate));
+      QD_TRY(q8prod(4 * l + 3, fd, m->W(fd, o.wd, D, F), act, nullptr, x, kGemvAccumulate));
       continue;
     }
-    QD_TRY(launch_q_gemv(args(c.w_fmt, m->W(c.w_fmt, o.wo, D, QD), att, x, kGemvAccumulate), st));
+    QD_TRY(launch_q_gemv(args(fo, m->W(fo, o.wo, D, QD), att, x, kGemvAccumulate), st));
     ++n;
-    QD_TRY(normed(args(c.w_fmt, m->W(c.w_fmt, o.wgu, 2 * F, D), x, act, kGemvSwiGLU),
+    QD_TRY(normed(args(fg, m->W(fg, o.wgu, 2 * F, D), x, act, kGemvSwiGLU),
                   reinterpret_cast<const float*>(m->w + o.ffn_norm)));
-    QD_TRY(launch_q_gemv(args(c.w_fmt, m->W(c.w_fmt, o.wd, D, F), act, x, kGemvAccumulate), st));
+    QD_TRY(launch_q_gemv(args(fd, m->W(fd, o.wd, D, F), act, x, kGemvAccumulate), st));
     ++n;
   }
   // output head with the greedy argmax (and the position advance) fused in
@@ -383,15 +400,16 @@ PrefillLayout prefill_layout(const qd_config& c, int64_t qkv_rows, int t) {
   return P;
 }
 
-// Whether the prefill products run on the tensor-core GEMM (binary16 weights) rather than
-// the batched GEMVs (the decode step's arithmetic).
+// Whether the prefill products may run on the tensor-core GEMM (binary16 weights) rather
+// than the batched GEMVs (the decode step's arithmetic); each product also needs a format
+// the GEMM takes (Q4_0, Q8_0, INT8 rows).
 bool prefill_uses_gemm(const qd_config& c, int t, unsigned flags) {
   if (flags & QD_PREFILL_EXACT) return false;
   if (t <= 2 * kPrefillRows) return false;  // two GEMV launches per product are as fast
-  if (c.w_fmt != QD_Q4_0 && c.w_fmt != QD_Q8_0 && c.w_fmt != QD_I8_ROW) return false;
   const int64_t QD = (int64_t)c.n_heads * c.head_dim;
   return c.dim % 64 == 0 && QD % 64 == 0 && c.ffn % 64 == 0;
 }
+inline bool gemm_fmt(int fmt) { return fmt == QD_Q4_0 || fmt == QD_Q8_0 || fmt == QD_I8_ROW; }
 
 qd_status enqueue_prefill(qd_model* m, int seq, int t, unsigned flags, uint8_t* ws, cudaStream_t st) {
   const qd_config& c = m->cfg;
@@ -416,15 +434,15 @@ qd_status enqueue_prefill(qd_model* m, int seq, int t, unsigned flags, uint8_t* 
   if (c.kv_f16) QD_TRY(zero_region(ws + P.attn_cnt, align_up(4 * (size_t)kPrefillChunk * c.n_kv_heads, 16), st));
 
   // one product over the t rows of `in`: the GEMM, or batched GEMVs of up to 8 rows
-  auto product = [&](PackedView W, const float* in, float* y, GemvMode mode) -> qd_status {
-    if (gemm) {
+  auto product = [&](int fmt, PackedView W, const float* in, float* y, GemvMode mode) -> qd_status {
+    if (gemm && gemm_fmt(fmt)) {
       const int gm = mode == kGemvAccumulate ? kGemmAccumulate : mode == kGemvSwiGLU ? kGemmSwiGLU : kGemmStore;
-      return launch_q_gemm(c.w_fmt, W, in, y, t, ws + P.gemm_ws, err, st, gm);
+      return launch_q_gemm(fmt, W, in, y, t, ws + P.gemm_ws, err, st, gm);
     }
     const int64_t ycols = mode == kGemvSwiGLU ? W.rows / 2 : W.rows;
     for (int c0 = 0; c0 < t; c0 += kPrefillRows) {
       GemvArgs a;
-      a.fmt = c.w_fmt;
+      a.fmt = fmt;
       a.W = W;
       a.x = in + (int64_t)c0 * W.cols;
       a.y = y + (int64_t)c0 * ycols;
@@ -443,7 +461,8 @@ qd_status enqueue_prefill(qd_model* m, int seq, int t, unsigned flags, uint8_t* 
     uint8_t* kc = m->s + L.kc + ((int64_t)l * L.cache_layer_stride + (int64_t)seq * L.cache_batch_stride) * esz;
     uint8_t* vc = m->s + L.vc + ((int64_t)l * L.cache_layer_stride + (int64_t)seq * L.cache_batch_stride) * esz;
     QD_TRY(launch_rmsnorm(x, reinterpret_cast<const float*>(m->w + o.attn_norm), xn, (int)D, t, c.eps, st));
-    QD_TRY(product(m->W(c.w_fmt, o.wqkv, L.qkv_rows, D), xn, qkv, kGemvStore));
+    const int fq = fmt_qkv(c), fo = fmt_wo(c), fg = fmt_gu(c), fd = fmt_down(c);
+    QD_TRY(product(fq, m->W(fq, o.wqkv, L.qkv_rows, D), xn, qkv, kGemvStore));
     QkvEpilogue e;
     e.q_rows = (int)QD;
     e.k_rows = (int)KD;
@@ -470,10 +489,10 @@ qd_status enqueue_prefill(qd_model* m, int seq, int t, unsigned flags, uint8_t* 
       QD_TRY(launch_attention(q, QD, reinterpret_cast<const float*>(kc), reinterpret_cast<const float*>(vc), 0, att,
                               c.n_heads, c.n_kv_heads, c.head_dim, ppos, c.max_ctx, t, ws + P.attn_ws, err, st));
     }
-    QD_TRY(product(m->W(c.w_fmt, o.wo, D, QD), att, x, kGemvAccumulate));
+    QD_TRY(product(fo, m->W(fo, o.wo, D, QD), att, x, kGemvAccumulate));
     QD_TRY(launch_rmsnorm(x, reinterpret_cast<const float*>(m->w + o.ffn_norm), xn, (int)D, t, c.eps, st));
-    QD_TRY(product(m->W(c.w_fmt, o.wgu, 2 * F, D), xn, act, kGemvSwiGLU));
-    QD_TRY(product(m->W(c.w_fmt, o.wd, D, F), act, x, kGemvAccumulate));
+    QD_TRY(product(fg, m->W(fg, o.wgu, 2 * F, D), xn, act, kGemvSwiGLU));
+    QD_TRY(product(fd, m->W(fd, o.wd, D, F), act, x, kGemvAccumulate));
   }
 
   // the last token's logits and greedy token, as the decode step's head; the position
@@ -550,7 +569,7 @@ qd_status qd_model_create(const qd_config* cfg, const void* const* src, void* we
       (s = launch_repack_rows(cfg->emb_fmt, src[2], cfg->vocab, D, m->w + L.head, cfg->vocab, 0, 1, st)))
     return fail(s);
   if ((s = copy_f32(L.out_norm, src[1], D))) return fail(s);
-  const int wf = cfg->w_fmt;
+  const int fq = fmt_qkv(*cfg), fo = fmt_wo(*cfg), fg = fmt_gu(*cfg), fd = fmt_down(*cfg);
   for (int l = 0; l < cfg->layers; ++l) {
     const void* const* T = src + 3 + 9 * l;
     const LayerOff& o = L.layer[l];
@@ -559,14 +578,14 @@ qd_status qd_model_create(const qd_config* cfg, const void* const* src, void* we
     // fused QKV: q rows, then k rows, then v rows; with half pairing the rows of each
     // RoPE pair (i, i + head_dim/2) are made adjacent for the projection's epilogue
     const int pair_hd = cfg->pairing == QD_ROPE_HALF ? cfg->head_dim : 0;
-    if ((s = launch_repack_rows(wf, T[1], QD, D, m->w + o.wqkv, L.qkv_rows, 0, 1, st, pair_hd))) return fail(s);
-    if ((s = launch_repack_rows(wf, T[2], KD, D, m->w + o.wqkv, L.qkv_rows, QD, 1, st, pair_hd))) return fail(s);
-    if ((s = launch_repack_rows(wf, T[3], KD, D, m->w + o.wqkv, L.qkv_rows, QD + KD, 1, st))) return fail(s);
-    if ((s = launch_repack_rows(wf, T[4], D, QD, m->w + o.wo, D, 0, 1, st))) return fail(s);
+    if ((s = launch_repack_rows(fq, T[1], QD, D, m->w + o.wqkv, L.qkv_rows, 0, 1, st, pair_hd))) return fail(s);
+    if ((s = launch_repack_rows(fq, T[2], KD, D, m->w + o.wqkv, L.qkv_rows, QD, 1, st, pair_hd))) return fail(s);
+    if ((s = launch_repack_rows(fq, T[3], KD, D, m->w + o.wqkv, L.qkv_rows, QD + KD, 1, st))) return fail(s);
+    if ((s = launch_repack_rows(fo, T[4], D, QD, m->w + o.wo, D, 0, 1, st))) return fail(s);
     // gate/up interleaved: row 2i = gate row i, row 2i+1 = up row i
-    if ((s = launch_repack_rows(wf, T[6], F, D, m->w + o.wgu, 2 * F, 0, 2, st))) return fail(s);
-    if ((s = launch_repack_rows(wf, T[7], F, D, m->w + o.wgu, 2 * F, 1, 2, st))) return fail(s);
-    if ((s = launch_repack_rows(wf, T[8], D, F, m->w + o.wd, D, 0, 1, st))) return fail(s);
+    if ((s = launch_repack_rows(fg, T[6], F, D, m->w + o.wgu, 2 * F, 0, 2, st))) return fail(s);
+    if ((s = launch_repack_rows(fg, T[7], F, D, m->w + o.wgu, 2 * F, 1, 2, st))) return fail(s);
+    if ((s = launch_repack_rows(fd, T[8], D, F, m->w + o.wd, D, 0, 1, st))) return fail(s);
   }
   if ((s = zero_region(m->s, L.state_bytes, st))) return fail(s);
   std::vector<float> table((size_t)cfg->max_ctx * cfg->head_dim);
@@ -575,9 +594,9 @@ qd_status qd_model_create(const qd_config* cfg, const void* const* src, void* we
       cudaStreamSynchronize(st) != cudaSuccess)
     return fail(QD_ERR_CUDA);
   if (cudaStreamCreateWithFlags(&m->capture_stream, cudaStreamNonBlocking) != cudaSuccess) return fail(QD_ERR_CUDA);
-  if (!cfg->act_q8 && !cfg->kv_f16) {
+  if (!cfg->act_q8 && !cfg->kv_f16 && uniform_fmt(*cfg)) {
     StepClusterModel& sc = m->scm;
-    sc.fmt = wf;
+    sc.fmt = fq;
     sc.emb_fmt = cfg->emb_fmt;
     sc.emb = m->W(cfg->emb_fmt, L.emb, cfg->vocab, D);
     sc.w = m->w;

@@ -41,7 +41,7 @@ def test_status_strings(lib):
     assert qd.status_str(0) == "ok"
     for s in range(1, 8):
         assert qd.status_str(s) != "unknown status"
-    assert lib.qd_abi_version() == 3
+    assert lib.qd_abi_version() == 4
 
 
 @pytest.mark.parametrize("fmt,rows,cols,src,packed", [
@@ -176,12 +176,37 @@ def test_model_sizes_and_config_refusals(lib):
     bad = qd.make_config(qdsynth.SMOL_135M, max_ctx=256, max_batch=1)
     bad.kv_f16 = 2
     assert lib.qd_model_state_bytes(ctypes.byref(bad)) == 0
-    # the decode step's fused kernels take Q4_0, Q8_0, Q4_K and INT8 rows only
-    for f in ("q4_1", "q5_0", "q5_k", "q6_k", "f16"):
+    # the decode step takes every format but per-row INT4, where its block fits the shapes:
+    # 576 columns take the 32-wide blocks, not the 256-wide K super-blocks
+    for f in ("q4_1", "q5_0", "f16"):
+        ok = qd.make_config(dict(qdsynth.SMOL_135M, w_fmt=f), max_ctx=256, max_batch=1)
+        assert lib.qd_model_weight_bytes(ctypes.byref(ok)) > 0, f
+        ok = qd.make_config(dict(qdsynth.SMOL_135M, emb_fmt=f), max_ctx=256, max_batch=1)
+        assert lib.qd_model_state_bytes(ctypes.byref(ok)) > 0, f
+    for f in ("q5_k", "q6_k", "q4_k"):
         bad = qd.make_config(dict(qdsynth.SMOL_135M, w_fmt=f), max_ctx=256, max_batch=1)
         assert lib.qd_model_weight_bytes(ctypes.byref(bad)) == 0, f
-        bad = qd.make_config(dict(qdsynth.SMOL_135M, emb_fmt=f), max_ctx=256, max_batch=1)
-        assert lib.qd_model_state_bytes(ctypes.byref(bad)) == 0, f
+    bad = qd.make_config(dict(qdsynth.SMOL_135M, w_fmt="i4"), max_ctx=256, max_batch=1)
+    assert lib.qd_model_weight_bytes(ctypes.byref(bad)) == 0
+    # per-class formats: each class checked on its own shapes; sizes follow the classes
+    wide = dict(qdsynth.SMOL_135M, dim=512, ffn=1024, n_heads=8, n_kv_heads=4)  # 256-divisible widths
+    uni = qd.make_config(dict(wide, w_fmt="q4_k"), max_ctx=256, max_batch=1)
+    mix = qd.make_config(dict(wide, w_fmt="q4_k", down_fmt="q6_k"), max_ctx=256, max_batch=1)
+    assert mix.mixed_fmt == 1 and uni.mixed_fmt == 0
+    wu, wm = lib.qd_model_weight_bytes(ctypes.byref(uni)), lib.qd_model_weight_bytes(ctypes.byref(mix))
+    # Q6_K in place of Q4_K for wd (512 x 1024) in each of 30 layers, regions 256-aligned
+    r256 = lambda n: (n + 255) // 256 * 256
+    pb = lambda f: lib.qd_packed_bytes(qd.FMT[f], 512, 1024)
+    assert wm - wu == 30 * (r256(pb("q6_k")) - r256(pb("q4_k"))) > 0
+    bad = qd.make_config(dict(qdsynth.SMOL_135M, down_fmt="q6_k"), max_ctx=256, max_batch=1)  # 1536 ok, 576 rows
+    assert lib.qd_model_weight_bytes(ctypes.byref(bad)) > 0  # wd is 576 x 1536: 1536 = 6 x 256 columns
+    bad = qd.make_config(dict(qdsynth.SMOL_135M, wo_fmt="q6_k"), max_ctx=256, max_batch=1)  # 576 columns
+    assert lib.qd_model_weight_bytes(ctypes.byref(bad)) == 0
+    bad = qd.make_config(dict(qdsynth.SMOL_135M, down_fmt="q4_k"), max_ctx=256, max_batch=1, act_q8=True)
+    assert lib.qd_model_state_bytes(ctypes.byref(bad)) == 0  # ggml-exact products: Q4_0 / Q8_0 only
+    bad = qd.make_config(qdsynth.SMOL_135M, max_ctx=256, max_batch=1)
+    bad.mixed_fmt = 2
+    assert lib.qd_model_weight_bytes(ctypes.byref(bad)) == 0
     # ggml-exact products take Q4_0 / Q8_0 weights only, and act_q8 is a flag
     ok = qd.make_config(qdsynth.SMOL_135M, max_ctx=256, max_batch=1, act_q8=True)
     assert lib.qd_model_state_bytes(ctypes.byref(ok)) > sb  # plus the quantised-activation buffer

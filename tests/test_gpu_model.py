@@ -96,6 +96,20 @@ def test_cluster_step_shapes_teacher_forced(qd, n_heads, n_kv, dim, ffn, max_ctx
     print(f"cluster G={n_heads // n_kv} n_kv={n_kv}: worst rel err {worst:.2e}, near-tie tokens {near}")
 
 
+@pytest.mark.parametrize("mix,emb_fmt,batch", [
+    (dict(w_fmt="q4_k", down_fmt="q6_k"), "q6_k", 1),  # Q4_K_M-like: Q4_K, Q6_K down and head
+    (dict(qkv_fmt="q8_0", wo_fmt="q5_0", gate_up_fmt="q5_k", down_fmt="q6_k"), "q4_1", 3),
+    (dict(w_fmt="q8_0", gate_up_fmt="f16", down_fmt="q4_1"), "q8_0", 2)])
+def test_mixed_format_model_teacher_forced(qd, mix, emb_fmt, batch):
+    """Models whose matrix classes take different formats (model files mix them by tensor):
+    the streaming and tensor-core GEMVs for the formats they take, the register-path GEMV
+    with a separate norm, QKV epilogue and argmax for the others, in one step."""
+    cfg = dict(TINY, emb_fmt=emb_fmt, **mix)
+    prompt = qdsynth.tokens(29, "mix.prompt", batch * 4, cfg["vocab"]).reshape(batch, 4)
+    worst, near = run_teacher_forced(qd, cfg, 29, prompt, n_gen=4, batch=batch, max_ctx=12)
+    print(f"mixed {mix} emb {emb_fmt} batch {batch}: worst rel err {worst:.2e}, near-tie tokens {near}")
+
+
 @pytest.mark.parametrize("w_fmt,batch", [("q4_0", 6), ("q8_0", 8)])
 def test_wide_ffn_model_column_ranges(qd, w_fmt, batch):
     """A 7B-wide FFN (11008) under a narrow model (dim 320, one stage and a partial one):

@@ -112,6 +112,7 @@ CASES = [
     ("q4_0", "q8_0", True, 0, 37, 0, 1),       # binary16 cache (attention in chunks of 16)
     ("q4_k", "q4_0", False, 0, 20, 0, 1),      # a format the GEMM does not take: batched GEMV
     ("q4_0", "q8_0", False, 0, 5, 0, 1),       # t <= 16: batched GEMV
+    ("mixed", "q6_k", False, 1, 24, 0, 1),     # a mixed-format model (Q4_K with Q6_K down), exact
 ]
 
 
@@ -145,7 +146,8 @@ def _check_prompt(m, cfg, host, max_ctx, max_batch, seq, prompt, flags, tok, log
 
 @pytest.mark.parametrize("w_fmt,emb_fmt,kv_f16,flags,t,seq,max_batch", CASES)
 def test_prefill_matches_decode_steps(qd, w_fmt, emb_fmt, kv_f16, flags, t, seq, max_batch):
-    cfg = dict(TINY, w_fmt=w_fmt, emb_fmt=emb_fmt, kv_f16=kv_f16)
+    mix = dict(w_fmt="q4_k", down_fmt="q6_k") if w_fmt == "mixed" else dict(w_fmt=w_fmt)
+    cfg = dict(TINY, emb_fmt=emb_fmt, kv_f16=kv_f16, **mix)
     max_ctx = t + 8
     m, host = build_model(qd, cfg, 31, max_ctx, max_batch)
     prompt = qdsynth.tokens(31, f"pf.{w_fmt}.{t}", t, cfg["vocab"])

@@ -20,36 +20,47 @@ TINY = dict(layers=2, dim=64, ffn=96, n_heads=4, n_kv_heads=2, head_dim=16, voca
 def _composed_step(cfg, T, kc, vc, pos, tok):
     D, F, hd = cfg["dim"], cfg["ffn"], cfg["head_dim"]
     hq, hk, ctx = cfg["n_heads"], cfg["n_kv_heads"], cfg["max_ctx"]
-    wf, ef = cfg["w_fmt"], cfg["emb_fmt"]
+    ef = cfg["emb_fmt"]
+    # a mixed model names the format of each class of matrix; the others take w_fmt
+    fq, fo = cfg.get("qkv_fmt", cfg["w_fmt"]), cfg.get("wo_fmt", cfg["w_fmt"])
+    fg, fd = cfg.get("gate_up_fmt", cfg["w_fmt"]), cfg.get("down_fmt", cfg["w_fmt"])
     f32 = lambda a: np.asarray(a, dtype=np.float32)
     x = oracle.dequant(ef, T[0], cfg["vocab"], D, row0=tok, nrows=1)[0].astype(np.float64)
     for l in range(cfg["layers"]):
         an, wq, wk, wv, wo, fn, wg, wu, wd = T[3 + 9 * l:12 + 9 * l]
         xn = f32(oracle.rmsnorm(f32(x), an, cfg["eps"]))
-        q = oracle.gemv(wf, wq, hq * hd, D, xn)[0]
-        k = oracle.gemv(wf, wk, hk * hd, D, xn)[0]
-        v = oracle.gemv(wf, wv, hk * hd, D, xn)[0]
+        q = oracle.gemv(fq, wq, hq * hd, D, xn)[0]
+        k = oracle.gemv(fq, wk, hk * hd, D, xn)[0]
+        v = oracle.gemv(fq, wv, hk * hd, D, xn)[0]
         q = oracle.rope(f32(q), hq, hd, pos, cfg["pairing"], cfg["rope_theta"])
         k = oracle.rope(f32(k), hk, hd, pos, cfg["pairing"], cfg["rope_theta"])
         kc[l][:, pos, :] = f32(k).reshape(hk, hd)
         vc[l][:, pos, :] = f32(v).reshape(hk, hd)
         att = oracle.attention(f32(q), kc[l], vc[l], hq, hk, hd, pos + 1, ctx)
-        x = x + oracle.gemv(wf, wo, D, hq * hd, f32(att))[0]
+        x = x + oracle.gemv(fo, wo, D, hq * hd, f32(att))[0]
         xn = f32(oracle.rmsnorm(f32(x), fn, cfg["eps"]))
-        g = oracle.gemv(wf, wg, F, D, xn)[0]
-        u = oracle.gemv(wf, wu, F, D, xn)[0]
+        g = oracle.gemv(fg, wg, F, D, xn)[0]
+        u = oracle.gemv(fg, wu, F, D, xn)[0]
         a = oracle.swiglu(f32(g), f32(u))
-        x = x + oracle.gemv(wf, wd, D, F, f32(a))[0]
+        x = x + oracle.gemv(fd, wd, D, F, f32(a))[0]
     xn = f32(oracle.rmsnorm(f32(x), T[1], cfg["eps"]))
     logits = oracle.gemv(ef, T[0], cfg["vocab"], D, xn)[0]
     return logits
 
 
-@pytest.mark.parametrize("pairing,w_fmt,emb_fmt", [("half", "q4_0", "q8_0"), ("adjacent", "q8_0", "q8_0"),
-                                                   ("half", "i8", "i8"), ("half", "q4_k", "q8_0")])
-def test_decode_step_equals_composition(pairing, w_fmt, emb_fmt):
-    cfg = dict(TINY, pairing=pairing, w_fmt=w_fmt, emb_fmt=emb_fmt)
-    if w_fmt == "q4_k":
+# mixed-format models (a Q4_K_M-like mix, and one with a different format in every class,
+# so a matrix read in another class's format fails by O(1))
+MIXED_A = dict(down_fmt="q6_k")  # with w_fmt q4_k
+MIXED_B = dict(qkv_fmt="q8_0", wo_fmt="q5_0", gate_up_fmt="q5_k", down_fmt="q6_k")
+
+
+@pytest.mark.parametrize("pairing,w_fmt,emb_fmt,mix", [("half", "q4_0", "q8_0", {}), ("adjacent", "q8_0", "q8_0", {}),
+                                                       ("half", "i8", "i8", {}), ("half", "q4_k", "q8_0", {}),
+                                                       ("half", "q4_k", "q6_k", MIXED_A),
+                                                       ("adjacent", "q4_0", "q4_1", MIXED_B)])
+def test_decode_step_equals_composition(pairing, w_fmt, emb_fmt, mix):
+    cfg = dict(TINY, pairing=pairing, w_fmt=w_fmt, emb_fmt=emb_fmt, **mix)
+    if "q4_k" in (w_fmt,) or mix:
         cfg.update(dim=256, ffn=512, n_heads=4, n_kv_heads=1, head_dim=64)
     T = qdsynth.model_tensors(cfg, seed=11)
     m = oracle.Model(cfg, T)
