@@ -195,14 +195,18 @@ __device__ __forceinline__ void cp_wait() {
 // each lane reads back only what it copied) and then the scale data of each row: 64
 // bytes (Q4_0/Q8_0 the 32 lanes' f16 scales, Q4_K the 4 super-block headers the 32 units
 // span, INT8 / INT4 the row scale) or, for Q4_1, 128 (the 32 lanes' (d, m) pairs).
+// Q6_K takes its step's four super-blocks whole instead (768 bytes of ql and qh per row, the
+// lanes of a super-block reading the bytes they share; 72 bytes of scales and d).
+constexpr int kQ6Step = 4 * 192;
 template <int FMT, int RW>
 constexpr int slot_code_bytes() {
-  return RW * 32 * code_bytes<FMT>();
+  return FMT == QD_Q6_K ? RW * kQ6Step : RW * 32 * code_bytes<FMT>();
 }
-// scale bytes per row of a slot: Q4_1 one (d, m) pair per lane's unit, the others 64
+// scale bytes per row of a slot: Q4_1 one (d, m) pair per lane's unit, Q6_K its 4
+// super-blocks' 18-byte records, the others 64
 template <int FMT>
 constexpr int slot_scale_bytes() {
-  return FMT == QD_Q4_1 ? 128 : 64;
+  return FMT == QD_Q4_1 ? 128 : FMT == QD_Q6_K ? 80 : 64;
 }
 template <int FMT, int RW>
 constexpr int slot_bytes() {
@@ -223,23 +227,38 @@ constexpr int stages() {
 
 // Issue the copies of one unit step (unit u of the rows in rp) into the slot at `slot`.
 template <int FMT, int RW>
-__device__ __forceinline__ void stage_step(uint32_t slot, const RowPtrs<RW>& rp, int u, int lane) {
+__device__ __forceinline__ void stage_step(uint32_t slot, const RowPtrs<RW>& rp, int u, int lane, int units) {
   constexpr int CB = code_bytes<FMT>();
+  if constexpr (FMT == QD_Q6_K) {
+    // the step's super-blocks (an even count: rows hold an even number of them), chunk c of
+    // their codes by lane c and c - 32, word w of their scale records by lane w
+    const int sb0 = (u - lane) >> 3, nsb = min(4, units / 8 - sb0);
 #pragma unroll
-  for (int rr = 0; rr < RW; ++rr) {
-    const uint8_t* c = rp.c[rr] + (uint32_t)u * (uint32_t)CB;
-    const uint32_t dst = slot + (uint32_t)(rr * 32 + lane) * CB;
+    for (int rr = 0; rr < RW; ++rr) {
+      const uint8_t* c = rp.c[rr] + (uint32_t)sb0 * 192u;
+      const uint32_t dst = slot + (uint32_t)(rr * kQ6Step);
+      if (lane < nsb * 12) cp16(dst + 16 * lane, c + 16 * lane);
+      if (lane + 32 < nsb * 12) cp16(dst + 16 * (lane + 32), c + 16 * (lane + 32));
+      const uint32_t sdst = slot + slot_code_bytes<FMT, RW>() + rr * slot_scale_bytes<FMT>();
+      if (lane < nsb * 18 / 4) cp4(sdst + 4 * lane, rp.s[rr] + (uint32_t)sb0 * 18u + 4 * lane);
+    }
+  } else {
 #pragma unroll
-    for (int k = 0; k < CB / 16; ++k) cp16(dst + 16 * k, c + 16 * k);
-    const uint32_t sdst = slot + slot_code_bytes<FMT, RW>() + rr * slot_scale_bytes<FMT>();
-    if constexpr (FMT == QD_Q4_1) {
-      cp4(sdst + 4 * lane, rp.s[rr] + 4 * (uint32_t)u);  // (d, m) of this lane's unit
-    } else if constexpr (FMT == QD_Q4_0 || FMT == QD_Q8_0) {
-      if ((lane & 1) == 0) cp4(sdst + 2 * lane, rp.s[rr] + 2 * (uint32_t)u);  // d of units u, u+1
-    } else if constexpr (FMT == QD_Q4_K) {
-      if ((lane & 7) == 0) cp16(sdst + 2 * lane, rp.s[rr] + (uint32_t)(u >> 3) * 16u);  // header
-    } else {
-      if (lane == 0) cp4(sdst, rp.s[rr]);  // row scale
+    for (int rr = 0; rr < RW; ++rr) {
+      const uint8_t* c = rp.c[rr] + (uint32_t)u * (uint32_t)CB;
+      const uint32_t dst = slot + (uint32_t)(rr * 32 + lane) * CB;
+#pragma unroll
+      for (int k = 0; k < CB / 16; ++k) cp16(dst + 16 * k, c + 16 * k);
+      const uint32_t sdst = slot + slot_code_bytes<FMT, RW>() + rr * slot_scale_bytes<FMT>();
+      if constexpr (FMT == QD_Q4_1) {
+        cp4(sdst + 4 * lane, rp.s[rr] + 4 * (uint32_t)u);  // (d, m) of this lane's unit
+      } else if constexpr (FMT == QD_Q4_0 || FMT == QD_Q8_0) {
+        if ((lane & 1) == 0) cp4(sdst + 2 * lane, rp.s[rr] + 2 * (uint32_t)u);  // d of units u, u+1
+      } else if constexpr (FMT == QD_Q4_K) {
+        if ((lane & 7) == 0) cp16(sdst + 2 * lane, rp.s[rr] + (uint32_t)(u >> 3) * 16u);  // header
+      } else {
+        if (lane == 0) cp4(sdst, rp.s[rr]);  // row scale
+      }
     }
   }
 }
@@ -255,84 +274,131 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
                                              int u, int lane, int batch) {
   constexpr int CB = code_bytes<FMT>();
   const uint8_t* sc = slot + slot_code_bytes<FMT, RW>();
-  // codes: Q4_0 / Q4_K word t < 4 = low nibbles of code bytes 4t..4t+3 (half A),
-  // t >= 4 = their high nibbles (half B); Q8_0 / INT8 the 32 code bytes in order
-  uint32_t w[RW][8];
-  float dq[RW], dm[RW];
-  int s0[RW], s1[RW], m0[RW], m1[RW];
-#pragma unroll
-  for (int rr = 0; rr < RW; ++rr) {
-    const uint8_t* cp = slot + (rr * 32 + lane) * CB;
-    if constexpr (FMT == QD_Q4_0 || FMT == QD_Q4_K || FMT == QD_I4_ROW || FMT == QD_Q4_1) {
-      const uint4 q = *reinterpret_cast<const uint4*>(cp);
-      const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        w[rr][t] = wv[t] & 0x0F0F0F0Fu;
-        w[rr][t + 4] = (wv[t] >> 4) & 0x0F0F0F0Fu;
-      }
-    } else {
-      const uint4 q0 = *reinterpret_cast<const uint4*>(cp);
-      const uint4 q1 = *reinterpret_cast<const uint4*>(cp + 16);
-      w[rr][0] = q0.x; w[rr][1] = q0.y; w[rr][2] = q0.z; w[rr][3] = q0.w;
-      w[rr][4] = q1.x; w[rr][5] = q1.y; w[rr][6] = q1.z; w[rr][7] = q1.w;
-    }
-    dm[rr] = 0.f;
-    s0[rr] = s1[rr] = m0[rr] = m1[rr] = 0;
-    if constexpr (FMT == QD_Q4_1) {
-      const uint32_t dmv = *reinterpret_cast<const uint32_t*>(sc + rr * slot_scale_bytes<FMT>() + 4 * lane);
-      dq[rr] = f16_bits_to_f32(dmv & 0xFFFFu);
-      dm[rr] = f16_bits_to_f32(dmv >> 16);
-    } else if constexpr (FMT == QD_Q4_0 || FMT == QD_Q8_0) {
-      dq[rr] = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sc + rr * 64 + 2 * lane));
-    } else if constexpr (FMT == QD_Q4_K) {
-      const uint4 hdr = *reinterpret_cast<const uint4*>(sc + rr * 64 + (lane >> 3) * 16);
-      const int j0 = 2 * ((u >> 1) & 3);
-      q4k_sm_words(hdr.y, hdr.z, hdr.w, j0, s0[rr], m0[rr]);
-      q4k_sm_words(hdr.y, hdr.z, hdr.w, j0 + 1, s1[rr], m1[rr]);
-      dq[rr] = f16_bits_to_f32(hdr.x & 0xFFFFu);
-      dm[rr] = f16_bits_to_f32(hdr.x >> 16);
-    } else {
-      dq[rr] = 1.f;  // INT8 / INT4 rows: the row scale multiplies the finished row sum
-    }
-  }
-#pragma unroll
-  for (int b = 0; b < NB; ++b) {
-    if (NB > 1 && b >= batch) break;
-    const uint8_t* rec = xq + ((size_t)b * units + u) * kRecBytes;
-    const uint4 hA = *reinterpret_cast<const uint4*>(rec + 0), hB = *reinterpret_cast<const uint4*>(rec + 16);
-    const uint4 mA = *reinterpret_cast<const uint4*>(rec + 32), mB = *reinterpret_cast<const uint4*>(rec + 48);
-    const uint4 lA = *reinterpret_cast<const uint4*>(rec + 64), lB = *reinterpret_cast<const uint4*>(rec + 80);
-    const float4 mt = *reinterpret_cast<const float4*>(rec + 96);
+  if constexpr (FMT == QD_Q6_K) {
+    // unit v = u % 8 of super-block u / 8 (the step's lsb-th): elements 32v..32v+31 take the
+    // low (k < 2) or high nibbles of ql bytes 64h + 32(k & 1) + l and bits 2k, 2k+1 of qh
+    // bytes 128 + 32h + l (h = v / 4, k = v % 4), as signed q - 32 (bytes: (q | 0x80) - 0x20
+    // cannot borrow, then ^ 0x80); halves A, B are sub-blocks 8h + 2k and 8h + 2k + 1
+    const int v = u & 7, h = v >> 2, k = v & 3, lsb = (u & 31) >> 3;
+    const int sh = (k >> 1) * 4, hs = 2 * k;
+    uint32_t w[RW][8];
+    float c0[RW], c1[RW];
 #pragma unroll
     for (int rr = 0; rr < RW; ++rr) {
-      if constexpr (FMT == QD_Q4_0 || FMT == QD_I4_ROW) {
-        // planes start at -8 * their element sums: sum (q - 8) xq, plane by plane (INT4
-        // rows are packed as Q4_0 codes in offset binary, q + 8)
-        const int h = plane_dot<false, true>(w[rr], hA, hB, __float_as_int(mt.y));
-        const int m = plane_dot<false, false>(w[rr], mA, mB, __float_as_int(mt.z));
-        const int l = plane_dot<false, false>(w[rr], lA, lB, __float_as_int(mt.w));
-        acc.v[rr][b] = fmaf(dq[rr] * mt.x, planes_value(h, m, l), acc.v[rr][b]);
-      } else if constexpr (FMT == QD_Q4_1) {
-        // value d q + m: d sum q xq (plane by plane) + m sum x (the record's half sums)
-        const int h = plane_dot<false, true>(w[rr], hA, hB, 0);
-        const int m = plane_dot<false, false>(w[rr], mA, mB, 0);
-        const int l = plane_dot<false, false>(w[rr], lA, lB, 0);
-        acc.v[rr][b] = fmaf(dq[rr] * mt.x, planes_value(h, m, l), fmaf(dm[rr], mt.y + mt.z, acc.v[rr][b]));
-      } else if constexpr (FMT == QD_Q4_K) {
-        // value d sc q - dmin m, summed over halves A (sub-block 2c) and B (2c + 1)
-        const float va = planes_value(half_dot<true>(w[rr], hA, 0), half_dot<false>(w[rr], mA, 0),
-                                      half_dot<false>(w[rr], lA, 0));
-        const float vb = planes_value(half_dot<true>(w[rr] + 4, hB, 0), half_dot<false>(w[rr] + 4, mB, 0),
-                                      half_dot<false>(w[rr] + 4, lB, 0));
-        const float q = fmaf((float)s0[rr], va, (float)s1[rr] * vb);
-        const float mins = fmaf((float)m0[rr], mt.y, (float)m1[rr] * mt.z);
-        acc.v[rr][b] = fmaf(dq[rr] * mt.x, q, fmaf(-dm[rr], mins, acc.v[rr][b]));
+      const uint8_t* blk = slot + rr * kQ6Step + lsb * 192;
+      const uint4 l0 = *reinterpret_cast<const uint4*>(blk + 64 * h + 32 * (k & 1));
+      const uint4 l1 = *reinterpret_cast<const uint4*>(blk + 64 * h + 32 * (k & 1) + 16);
+      const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 128 + 32 * h);
+      const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 128 + 32 * h + 16);
+      const uint32_t lw[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+      const uint32_t hw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const uint32_t q = ((lw[t] >> sh) & 0x0F0F0F0Fu) | (((hw[t] >> hs) & 0x03030303u) << 4);
+        w[rr][t] = ((q | 0x80808080u) - 0x20202020u) ^ 0x80808080u;
+      }
+      const uint8_t* sr = sc + rr * slot_scale_bytes<FMT>() + lsb * 18;
+      const float d = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sr + 16));
+      c0[rr] = d * (float)(int8_t)sr[8 * h + 2 * k];
+      c1[rr] = d * (float)(int8_t)sr[8 * h + 2 * k + 1];
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      if (NB > 1 && b >= batch) break;
+      const uint8_t* rec = xq + ((size_t)b * units + u) * kRecBytes;
+      const uint4 hA = *reinterpret_cast<const uint4*>(rec + 0), hB = *reinterpret_cast<const uint4*>(rec + 16);
+      const uint4 mA = *reinterpret_cast<const uint4*>(rec + 32), mB = *reinterpret_cast<const uint4*>(rec + 48);
+      const uint4 lA = *reinterpret_cast<const uint4*>(rec + 64), lB = *reinterpret_cast<const uint4*>(rec + 80);
+      const float xs = *reinterpret_cast<const float*>(rec + 96);
+#pragma unroll
+      for (int rr = 0; rr < RW; ++rr) {
+        const float va = planes_value(half_dot_s<true>(w[rr], hA, 0), half_dot_s<false>(w[rr], mA, 0),
+                                      half_dot_s<false>(w[rr], lA, 0));
+        const float vb = planes_value(half_dot_s<true>(w[rr] + 4, hB, 0), half_dot_s<false>(w[rr] + 4, mB, 0),
+                                      half_dot_s<false>(w[rr] + 4, lB, 0));
+        acc.v[rr][b] = fmaf(xs, fmaf(c0[rr], va, c1[rr] * vb), acc.v[rr][b]);
+      }
+    }
+  } else {
+    // codes: Q4_0 / Q4_K word t < 4 = low nibbles of code bytes 4t..4t+3 (half A),
+    // t >= 4 = their high nibbles (half B); Q8_0 / INT8 the 32 code bytes in order
+    uint32_t w[RW][8];
+    float dq[RW], dm[RW];
+    int s0[RW], s1[RW], m0[RW], m1[RW];
+#pragma unroll
+    for (int rr = 0; rr < RW; ++rr) {
+      const uint8_t* cp = slot + (rr * 32 + lane) * CB;
+      if constexpr (FMT == QD_Q4_0 || FMT == QD_Q4_K || FMT == QD_I4_ROW || FMT == QD_Q4_1) {
+        const uint4 q = *reinterpret_cast<const uint4*>(cp);
+        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          w[rr][t] = wv[t] & 0x0F0F0F0Fu;
+          w[rr][t + 4] = (wv[t] >> 4) & 0x0F0F0F0Fu;
+        }
       } else {
-        const int h = plane_dot<true, true>(w[rr], hA, hB, 0);
-        const int m = plane_dot<true, false>(w[rr], mA, mB, 0);
-        const int l = plane_dot<true, false>(w[rr], lA, lB, 0);
-        acc.v[rr][b] = fmaf(dq[rr] * mt.x, planes_value(h, m, l), acc.v[rr][b]);
+        const uint4 q0 = *reinterpret_cast<const uint4*>(cp);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(cp + 16);
+        w[rr][0] = q0.x; w[rr][1] = q0.y; w[rr][2] = q0.z; w[rr][3] = q0.w;
+        w[rr][4] = q1.x; w[rr][5] = q1.y; w[rr][6] = q1.z; w[rr][7] = q1.w;
+      }
+      dm[rr] = 0.f;
+      s0[rr] = s1[rr] = m0[rr] = m1[rr] = 0;
+      if constexpr (FMT == QD_Q4_1) {
+        const uint32_t dmv = *reinterpret_cast<const uint32_t*>(sc + rr * slot_scale_bytes<FMT>() + 4 * lane);
+        dq[rr] = f16_bits_to_f32(dmv & 0xFFFFu);
+        dm[rr] = f16_bits_to_f32(dmv >> 16);
+      } else if constexpr (FMT == QD_Q4_0 || FMT == QD_Q8_0) {
+        dq[rr] = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sc + rr * 64 + 2 * lane));
+      } else if constexpr (FMT == QD_Q4_K) {
+        const uint4 hdr = *reinterpret_cast<const uint4*>(sc + rr * 64 + (lane >> 3) * 16);
+        const int j0 = 2 * ((u >> 1) & 3);
+        q4k_sm_words(hdr.y, hdr.z, hdr.w, j0, s0[rr], m0[rr]);
+        q4k_sm_words(hdr.y, hdr.z, hdr.w, j0 + 1, s1[rr], m1[rr]);
+        dq[rr] = f16_bits_to_f32(hdr.x & 0xFFFFu);
+        dm[rr] = f16_bits_to_f32(hdr.x >> 16);
+      } else {
+        dq[rr] = 1.f;  // INT8 / INT4 rows: the row scale multiplies the finished row sum
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      if (NB > 1 && b >= batch) break;
+      const uint8_t* rec = xq + ((size_t)b * units + u) * kRecBytes;
+      const uint4 hA = *reinterpret_cast<const uint4*>(rec + 0), hB = *reinterpret_cast<const uint4*>(rec + 16);
+      const uint4 mA = *reinterpret_cast<const uint4*>(rec + 32), mB = *reinterpret_cast<const uint4*>(rec + 48);
+      const uint4 lA = *reinterpret_cast<const uint4*>(rec + 64), lB = *reinterpret_cast<const uint4*>(rec + 80);
+      const float4 mt = *reinterpret_cast<const float4*>(rec + 96);
+#pragma unroll
+      for (int rr = 0; rr < RW; ++rr) {
+        if constexpr (FMT == QD_Q4_0 || FMT == QD_I4_ROW) {
+          // planes start at -8 * their element sums: sum (q - 8) xq, plane by plane (INT4
+          // rows are packed as Q4_0 codes in offset binary, q + 8)
+          const int h = plane_dot<false, true>(w[rr], hA, hB, __float_as_int(mt.y));
+          const int m = plane_dot<false, false>(w[rr], mA, mB, __float_as_int(mt.z));
+          const int l = plane_dot<false, false>(w[rr], lA, lB, __float_as_int(mt.w));
+          acc.v[rr][b] = fmaf(dq[rr] * mt.x, planes_value(h, m, l), acc.v[rr][b]);
+        } else if constexpr (FMT == QD_Q4_1) {
+          // value d q + m: d sum q xq (plane by plane) + m sum x (the record's half sums)
+          const int h = plane_dot<false, true>(w[rr], hA, hB, 0);
+          const int m = plane_dot<false, false>(w[rr], mA, mB, 0);
+          const int l = plane_dot<false, false>(w[rr], lA, lB, 0);
+          acc.v[rr][b] = fmaf(dq[rr] * mt.x, planes_value(h, m, l), fmaf(dm[rr], mt.y + mt.z, acc.v[rr][b]));
+        } else if constexpr (FMT == QD_Q4_K) {
+          // value d sc q - dmin m, summed over halves A (sub-block 2c) and B (2c + 1)
+          const float va = planes_value(half_dot<true>(w[rr], hA, 0), half_dot<false>(w[rr], mA, 0),
+                                        half_dot<false>(w[rr], lA, 0));
+          const float vb = planes_value(half_dot<true>(w[rr] + 4, hB, 0), half_dot<false>(w[rr] + 4, mB, 0),
+                                        half_dot<false>(w[rr] + 4, lB, 0));
+          const float q = fmaf((float)s0[rr], va, (float)s1[rr] * vb);
+          const float mins = fmaf((float)m0[rr], mt.y, (float)m1[rr] * mt.z);
+          acc.v[rr][b] = fmaf(dq[rr] * mt.x, q, fmaf(-dm[rr], mins, acc.v[rr][b]));
+        } else {
+          const int h = plane_dot<true, true>(w[rr], hA, hB, 0);
+          const int m = plane_dot<true, false>(w[rr], mA, mB, 0);
+          const int l = plane_dot<true, false>(w[rr], lA, lB, 0);
+          acc.v[rr][b] = fmaf(dq[rr] * mt.x, planes_value(h, m, l), acc.v[rr][b]);
+        }
       }
     }
   }
@@ -375,7 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
   auto issue = [&](int slot_idx) {
     if (lg < groups) {
       const int u = lane + 32 * lj;
-      if (u < units) stage_step<FMT, RW>(ring_s + (uint32_t)slot_idx * SB, lrp, u, lane);
+      // (Q6_K: copies by chunk, not by unit, so every lane takes part in a short last step)
+      if (u < units || FMT == QD_Q6_K) stage_step<FMT, RW>(ring_s + (uint32_t)slot_idx * SB, lrp, u, lane, units);
       if (++lj == j1) {
         lj = j0;
         lg += nw;
@@ -675,6 +742,7 @@ size_t smem_bytes(int fmt, int64_t cols, int nb) {
     QD_SMEM_CASE(QD_I8_ROW)
     QD_SMEM_CASE(QD_I4_ROW)
     QD_SMEM_CASE(QD_Q4_1)
+    QD_SMEM_CASE(QD_Q6_K)
 #undef QD_SMEM_CASE
     default: return ~(size_t)0;
   }
@@ -850,7 +918,9 @@ qd_status launch_inst(Params p, bool pdl, cudaStream_t stream) {
 int nb_for(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8; }
 
 bool supported(const GemvArgs& a) {
-  if (!model_fmt_ok(a.fmt) && a.fmt != QD_I4_ROW && a.fmt != QD_Q4_1) return false;  // + INT4 rows, Q4_1
+  // + INT4 rows, Q4_1, Q6_K (an even number of super-blocks per row: 4-byte scale copies)
+  if (!model_fmt_ok(a.fmt) && a.fmt != QD_I4_ROW && a.fmt != QD_Q4_1 && a.fmt != QD_Q6_K) return false;
+  if (a.fmt == QD_Q6_K && a.W.cols % 512) return false;
   if (a.batch < 1 || a.batch > 8 || a.W.cols % 32) return false;
   if (a.W.cols > (1 << 24)) return false;
   if (smem_bytes(a.fmt, a.W.cols, nb_for(a.batch)) > kSmemCap) return false;
@@ -896,6 +966,7 @@ qd_status launch_q_gemv_stream(const GemvArgs& a, cudaStream_t stream) {
     case QD_I8_ROW: QD_NB_SWITCH(QD_I8_ROW)
     case QD_I4_ROW: QD_NB_SWITCH(QD_I4_ROW)
     case QD_Q4_1: QD_NB_SWITCH(QD_Q4_1)
+    case QD_Q6_K: QD_NB_SWITCH(QD_Q6_K)
     default: return QD_ERR_UNSUPPORTED;
   }
 #undef QD_NB_SWITCH

@@ -95,6 +95,14 @@ __device__ __forceinline__ int half_dot(const uint32_t* w, uint4 p, int c) {
   for (int t = 0; t < 4; ++t) c = PLANE_SIGNED ? dp4a_us(w[t], xv[t], c) : dp4a_uu(w[t], xv[t], c);
   return c;
 }
+// Same over 4 signed code words (Q6_K's q - 32).
+template <bool PLANE_SIGNED>
+__device__ __forceinline__ int half_dot_s(const uint32_t* w, uint4 p, int c) {
+  const uint32_t xv[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) c = PLANE_SIGNED ? dp4a_ss(w[t], xv[t], c) : dp4a_su(w[t], xv[t], c);
+  return c;
+}
 // 65536 h + 256 m + l as a float (h exact; the rest rounded once).
 __device__ __forceinline__ float planes_value(int h, int m, int l) {
   return fmaf((float)h, 65536.f, (float)(m * 256 + l));

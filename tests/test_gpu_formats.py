@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 
 NEW = ["q4_1", "q5_0", "q5_k", "q6_k", "f16", "i4"]
 SHAPES = {"q4_1": [(1, 32), (67, 1056), (130, 4128)], "q5_0": [(1, 32), (67, 1056), (33, 4128)],
-          "q5_k": [(1, 256), (37, 2304), (19, 4352)], "q6_k": [(1, 256), (37, 2304), (19, 4352)],
+          "q5_k": [(1, 256), (37, 2304), (19, 4352)], "q6_k": [(1, 256), (37, 2304), (19, 4352), (37, 2048), (19, 3584)],
           "f16": [(1, 32), (67, 1056), (41, 4128)], "i4": [(1, 32), (67, 1056), (41, 4128)]}
 
 
@@ -68,6 +68,19 @@ def test_q_gemv_parity(qd, fmt, batch):
         x = qdsynth.activations(44, f"gvx{cols}", batch, cols)
         got = _gemv(qd, fmt, p, rows, cols, x)
         assert_close(got, oracle.gemv(fmt, src, rows, cols, x), what=f"{fmt} {rows}x{cols} b{batch}")
+
+
+def test_q_gemv_q6k_streaming_precision(qd):
+    """Q6_K rows with an even number of super-blocks take the streaming kernel's integer
+    dot (signed 6-bit codes against x's 24-bit planes): at batch 1, 2, 5 and 8, over 2048
+    columns (two full steps) and 3584 (a last step of two super-blocks), every row within
+    2e-5 of the oracle (the planes' bound), not just 1e-3."""
+    for rows, cols in ((37, 2048), (19, 3584), (300, 7168)):
+        src, p = weights(qd, "q6_k", 46, f"q6s{rows}", rows, cols)
+        for batch in (1, 2, 5, 8):
+            x = qdsynth.activations(46, f"q6sx{cols}", batch, cols)
+            got = _gemv(qd, "q6_k", p, rows, cols, x)
+            assert_close(got, oracle.gemv("q6_k", src, rows, cols, x), tol=2e-5, what=f"q6_k {rows}x{cols} b{batch}")
 
 
 @pytest.mark.parametrize("fmt", NEW)
