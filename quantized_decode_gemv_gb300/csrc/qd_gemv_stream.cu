@@ -202,11 +202,11 @@ template <int FMT, int RW>
 constexpr int slot_code_bytes() {
   return FMT == QD_Q6_K ? RW * kQ6Step : RW * 32 * code_bytes<FMT>();
 }
-// scale bytes per row of a slot: Q4_1 one (d, m) pair per lane's unit, Q6_K its 4
-// super-blocks' 18-byte records, the others 64
+// scale bytes per row of a slot: Q4_1 one (d, m) pair per lane's unit, Q5_0 one (d, qh)
+// record (6 bytes) per lane's unit, Q6_K its 4 super-blocks' 18-byte records, the others 64
 template <int FMT>
 constexpr int slot_scale_bytes() {
-  return FMT == QD_Q4_1 ? 128 : FMT == QD_Q6_K ? 80 : 64;
+  return FMT == QD_Q4_1 ? 128 : FMT == QD_Q5_0 ? 192 : FMT == QD_Q6_K ? 80 : 64;
 }
 template <int FMT, int RW>
 constexpr int slot_bytes() {
@@ -245,16 +245,29 @@ __device__ __forceinline__ void stage_step(uint32_t slot, const RowPtrs<RW>& rp,
   } else {
 #pragma unroll
     for (int rr = 0; rr < RW; ++rr) {
-      const uint8_t* c = rp.c[rr] + (uint32_t)u * (uint32_t)CB;
       const uint32_t dst = slot + (uint32_t)(rr * 32 + lane) * CB;
+      if constexpr (FMT == QD_Q5_K) {
+        // unit u = 8s + 2c + h of a 160-byte super-block: nibbles at 32 + 32c + 16h, fifth
+        // bits at 16h (bit 2c for the low nibbles, 2c + 1 for the high ones)
+        const uint8_t* b = rp.c[rr] + (uint32_t)(u >> 3) * 160u;
+        cp16(dst, b + 32 + 32 * ((u >> 1) & 3) + 16 * (u & 1));
+        cp16(dst + 16, b + 16 * (u & 1));
+      } else {
+        const uint8_t* c = rp.c[rr] + (uint32_t)u * (uint32_t)CB;
 #pragma unroll
-      for (int k = 0; k < CB / 16; ++k) cp16(dst + 16 * k, c + 16 * k);
+        for (int k = 0; k < CB / 16; ++k) cp16(dst + 16 * k, c + 16 * k);
+      }
       const uint32_t sdst = slot + slot_code_bytes<FMT, RW>() + rr * slot_scale_bytes<FMT>();
       if constexpr (FMT == QD_Q4_1) {
         cp4(sdst + 4 * lane, rp.s[rr] + 4 * (uint32_t)u);  // (d, m) of this lane's unit
       } else if constexpr (FMT == QD_Q4_0 || FMT == QD_Q8_0) {
         if ((lane & 1) == 0) cp4(sdst + 2 * lane, rp.s[rr] + 2 * (uint32_t)u);  // d of units u, u+1
-      } else if constexpr (FMT == QD_Q4_K) {
+      } else if constexpr (FMT == QD_Q5_0) {
+        if ((lane & 1) == 0) {  // (d, qh) of units u, u+1: 12 bytes
+#pragma unroll
+          for (int k = 0; k < 3; ++k) cp4(sdst + 6 * lane + 4 * k, rp.s[rr] + 6 * (uint32_t)u + 4 * k);
+        }
+      } else if constexpr (FMT == QD_Q4_K || FMT == QD_Q5_K) {
         if ((lane & 7) == 0) cp16(sdst + 2 * lane, rp.s[rr] + (uint32_t)(u >> 3) * 16u);  // header
       } else {
         if (lane == 0) cp4(sdst, rp.s[rr]);  // row scale
@@ -336,6 +349,32 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
           w[rr][t] = wv[t] & 0x0F0F0F0Fu;
           w[rr][t + 4] = (wv[t] >> 4) & 0x0F0F0F0Fu;
         }
+      } else if constexpr (FMT == QD_Q5_0) {
+        // Q4_0's nibbles plus fifth bit j of qh for element j, spread to bit 4 of each byte
+        // (x * 0x00204081 moves bit i of a 4-bit x to bit 8i, no carries), as signed q - 16
+        const uint4 q = *reinterpret_cast<const uint4*>(cp);
+        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+        const unsigned short* rec = reinterpret_cast<const unsigned short*>(sc + rr * slot_scale_bytes<FMT>() + 6 * lane);
+        const uint32_t qh = (uint32_t)rec[1] | ((uint32_t)rec[2] << 16);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const uint32_t fa = (((qh >> (4 * t)) & 15u) * 0x00204081u) & 0x01010101u;
+          const uint32_t fb = (((qh >> (16 + 4 * t)) & 15u) * 0x00204081u) & 0x01010101u;
+          const uint32_t qa = (wv[t] & 0x0F0F0F0Fu) | (fa << 4), qb = ((wv[t] >> 4) & 0x0F0F0F0Fu) | (fb << 4);
+          w[rr][t] = ((qa | 0x80808080u) - 0x10101010u) ^ 0x80808080u;
+          w[rr][t + 4] = ((qb | 0x80808080u) - 0x10101010u) ^ 0x80808080u;
+        }
+      } else if constexpr (FMT == QD_Q5_K) {
+        // Q4_K's nibbles plus the fifth bit: unsigned 5-bit codes through Q4_K's dot
+        const uint4 q = *reinterpret_cast<const uint4*>(cp);
+        const uint4 hq = *reinterpret_cast<const uint4*>(cp + 16);
+        const uint32_t wv[4] = {q.x, q.y, q.z, q.w}, hv[4] = {hq.x, hq.y, hq.z, hq.w};
+        const int b0 = 2 * ((u >> 1) & 3);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          w[rr][t] = (wv[t] & 0x0F0F0F0Fu) | (((hv[t] >> b0) & 0x01010101u) << 4);
+          w[rr][t + 4] = ((wv[t] >> 4) & 0x0F0F0F0Fu) | (((hv[t] >> (b0 + 1)) & 0x01010101u) << 4);
+        }
       } else {
         const uint4 q0 = *reinterpret_cast<const uint4*>(cp);
         const uint4 q1 = *reinterpret_cast<const uint4*>(cp + 16);
@@ -350,7 +389,9 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
         dm[rr] = f16_bits_to_f32(dmv >> 16);
       } else if constexpr (FMT == QD_Q4_0 || FMT == QD_Q8_0) {
         dq[rr] = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sc + rr * 64 + 2 * lane));
-      } else if constexpr (FMT == QD_Q4_K) {
+      } else if constexpr (FMT == QD_Q5_0) {
+        dq[rr] = f16_bits_to_f32(*reinterpret_cast<const unsigned short*>(sc + rr * slot_scale_bytes<FMT>() + 6 * lane));
+      } else if constexpr (FMT == QD_Q4_K || FMT == QD_Q5_K) {
         const uint4 hdr = *reinterpret_cast<const uint4*>(sc + rr * 64 + (lane >> 3) * 16);
         const int j0 = 2 * ((u >> 1) & 3);
         q4k_sm_words(hdr.y, hdr.z, hdr.w, j0, s0[rr], m0[rr]);
@@ -384,7 +425,7 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
           const int m = plane_dot<false, false>(w[rr], mA, mB, 0);
           const int l = plane_dot<false, false>(w[rr], lA, lB, 0);
           acc.v[rr][b] = fmaf(dq[rr] * mt.x, planes_value(h, m, l), fmaf(dm[rr], mt.y + mt.z, acc.v[rr][b]));
-        } else if constexpr (FMT == QD_Q4_K) {
+        } else if constexpr (FMT == QD_Q4_K || FMT == QD_Q5_K) {
           // value d sc q - dmin m, summed over halves A (sub-block 2c) and B (2c + 1)
           const float va = planes_value(half_dot<true>(w[rr], hA, 0), half_dot<false>(w[rr], mA, 0),
                                         half_dot<false>(w[rr], lA, 0));
@@ -742,6 +783,8 @@ size_t smem_bytes(int fmt, int64_t cols, int nb) {
     QD_SMEM_CASE(QD_I8_ROW)
     QD_SMEM_CASE(QD_I4_ROW)
     QD_SMEM_CASE(QD_Q4_1)
+    QD_SMEM_CASE(QD_Q5_0)
+    QD_SMEM_CASE(QD_Q5_K)
     QD_SMEM_CASE(QD_Q6_K)
 #undef QD_SMEM_CASE
     default: return ~(size_t)0;
@@ -918,14 +961,17 @@ qd_status launch_inst(Params p, bool pdl, cudaStream_t stream) {
 int nb_for(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8; }
 
 bool supported(const GemvArgs& a) {
-  // + INT4 rows, Q4_1, Q6_K (an even number of super-blocks per row: 4-byte scale copies)
-  if (!model_fmt_ok(a.fmt) && a.fmt != QD_I4_ROW && a.fmt != QD_Q4_1 && a.fmt != QD_Q6_K) return false;
+  // + INT4 rows, Q4_1, Q5_0, Q5_K, Q6_K (an even number of super-blocks per row: 4-byte
+  // scale copies)
+  if (!model_fmt_ok(a.fmt) && a.fmt != QD_I4_ROW && a.fmt != QD_Q4_1 && a.fmt != QD_Q5_0 && a.fmt != QD_Q5_K &&
+      a.fmt != QD_Q6_K)
+    return false;
   if (a.fmt == QD_Q6_K && a.W.cols % 512) return false;
   if (a.batch < 1 || a.batch > 8 || a.W.cols % 32) return false;
   if (a.W.cols > (1 << 24)) return false;
   if (smem_bytes(a.fmt, a.W.cols, nb_for(a.batch)) > kSmemCap) return false;
   // 4-byte scale copies need an even number of blocks per row
-  if ((a.fmt == QD_Q4_0 || a.fmt == QD_Q8_0) && ((a.W.cols / 32) & 1)) return false;
+  if ((a.fmt == QD_Q4_0 || a.fmt == QD_Q8_0 || a.fmt == QD_Q5_0) && ((a.W.cols / 32) & 1)) return false;
   return true;
 }
 
@@ -966,6 +1012,8 @@ qd_status launch_q_gemv_stream(const GemvArgs& a, cudaStream_t stream) {
     case QD_I8_ROW: QD_NB_SWITCH(QD_I8_ROW)
     case QD_I4_ROW: QD_NB_SWITCH(QD_I4_ROW)
     case QD_Q4_1: QD_NB_SWITCH(QD_Q4_1)
+    case QD_Q5_0: QD_NB_SWITCH(QD_Q5_0)
+    case QD_Q5_K: QD_NB_SWITCH(QD_Q5_K)
     case QD_Q6_K: QD_NB_SWITCH(QD_Q6_K)
     default: return QD_ERR_UNSUPPORTED;
   }

@@ -37,20 +37,22 @@ __device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c) {  // a si
 
 // Element offsets (in x) of the two 16-element halves A, B of unit u:
 //  Q4_0: A = [32u, 32u+16), B = [32u+16, 32u+32); code byte i: low nibble -> A[i], high -> B[i]
-//  Q4_K: u = 8s + 2c + h, A = [256s+64c+16h, +16), B = A + 32; same nibble rule
+//  Q4_K, Q5_K: u = 8s + 2c + h, A = [256s+64c+16h, +16), B = A + 32; same nibble rule
 //  Q8_0 / INT8: A <- code bytes 0..15, B <- bytes 16..31
 template <int FMT>
 __device__ __forceinline__ int unit_xa(int u) {
-  if constexpr (FMT == QD_Q4_K) return (u >> 3) * 256 + ((u >> 1) & 3) * 64 + (u & 1) * 16;
+  if constexpr (FMT == QD_Q4_K || FMT == QD_Q5_K) return (u >> 3) * 256 + ((u >> 1) & 3) * 64 + (u & 1) * 16;
   return u * 32;
 }
 template <int FMT>
 __device__ __forceinline__ int unit_xb(int u) {
-  return unit_xa<FMT>(u) + ((FMT == QD_Q4_K) ? 32 : 16);
+  return unit_xa<FMT>(u) + ((FMT == QD_Q4_K || FMT == QD_Q5_K) ? 32 : 16);
 }
+// code bytes a lane stages per unit: Q5_K its 16 nibble bytes, then the 16 bytes of fifth
+// bits of the same element positions
 template <int FMT>
 constexpr int code_bytes() {
-  return (FMT == QD_Q8_0 || FMT == QD_I8_ROW) ? 32 : 16;
+  return (FMT == QD_Q8_0 || FMT == QD_I8_ROW || FMT == QD_Q5_K) ? 32 : 16;
 }
 
 // Shared-memory x records: per batch row and unit, 112 bytes in seven 16-byte chunks:
@@ -153,7 +155,7 @@ __device__ __forceinline__ void write_record(uint8_t* rec, int k, bool ok, float
       s0 += __shfl_xor_sync(0xffffffffu, s0, o);
     }
     meta = make_float4(sc, __int_as_float(-8 * s2), __int_as_float(-8 * s1), __int_as_float(-8 * s0));
-  } else if constexpr (FMT == QD_Q4_K || FMT == QD_Q4_1) {
+  } else if constexpr (FMT == QD_Q4_K || FMT == QD_Q5_K || FMT == QD_Q4_1) {
     float sv = (v.x + v.y) + (v.z + v.w);
     sv += __shfl_xor_sync(0xffffffffu, sv, 1);
     sv += __shfl_xor_sync(0xffffffffu, sv, 2);  // lanes 0-3: sum over A, 4-7: over B

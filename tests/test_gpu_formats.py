@@ -14,7 +14,7 @@ from gpu_helpers import assert_close, dev, packed, weights
 pytestmark = pytest.mark.gpu
 
 NEW = ["q4_1", "q5_0", "q5_k", "q6_k", "f16", "i4"]
-SHAPES = {"q4_1": [(1, 32), (67, 1056), (130, 4128)], "q5_0": [(1, 32), (67, 1056), (33, 4128)],
+SHAPES = {"q4_1": [(1, 32), (67, 1056), (130, 4128)], "q5_0": [(1, 32), (67, 1056), (33, 4128), (67, 1024), (33, 4160)],
           "q5_k": [(1, 256), (37, 2304), (19, 4352)], "q6_k": [(1, 256), (37, 2304), (19, 4352), (37, 2048), (19, 3584)],
           "f16": [(1, 32), (67, 1056), (41, 4128)], "i4": [(1, 32), (67, 1056), (41, 4128)]}
 
@@ -70,17 +70,23 @@ def test_q_gemv_parity(qd, fmt, batch):
         assert_close(got, oracle.gemv(fmt, src, rows, cols, x), what=f"{fmt} {rows}x{cols} b{batch}")
 
 
-def test_q_gemv_q6k_streaming_precision(qd):
-    """Q6_K rows with an even number of super-blocks take the streaming kernel's integer
-    dot (signed 6-bit codes against x's 24-bit planes): at batch 1, 2, 5 and 8, over 2048
-    columns (two full steps) and 3584 (a last step of two super-blocks), every row within
-    2e-5 of the oracle (the planes' bound), not just 1e-3."""
-    for rows, cols in ((37, 2048), (19, 3584), (300, 7168)):
-        src, p = weights(qd, "q6_k", 46, f"q6s{rows}", rows, cols)
+STREAMED = {"q6_k": [(37, 2048), (19, 3584), (300, 7168)],   # even super-block counts
+            "q5_k": [(37, 2304), (19, 4352), (300, 7168)],
+            "q5_0": [(67, 1024), (33, 4160), (300, 7168)]}     # even block counts
+
+
+@pytest.mark.parametrize("fmt", ["q6_k", "q5_k", "q5_0"])
+def test_q_gemv_streaming_integer_precision(qd, fmt):
+    """Q6_K, Q5_K and Q5_0 on the streaming kernel's integer dot (Q6_K and Q5_0 as signed
+    codes, Q5_K as Q4_K's unsigned codes with the fifth bit) against x's 24-bit planes: at
+    batch 1, 2, 5 and 8, over full and short last steps, every row within 2e-5 of the
+    oracle (the planes' bound), not just 1e-3."""
+    for rows, cols in STREAMED[fmt]:
+        src, p = weights(qd, fmt, 46, f"st{fmt}{rows}", rows, cols)
         for batch in (1, 2, 5, 8):
-            x = qdsynth.activations(46, f"q6sx{cols}", batch, cols)
-            got = _gemv(qd, "q6_k", p, rows, cols, x)
-            assert_close(got, oracle.gemv("q6_k", src, rows, cols, x), tol=2e-5, what=f"q6_k {rows}x{cols} b{batch}")
+            x = qdsynth.activations(46, f"stx{cols}", batch, cols)
+            got = _gemv(qd, fmt, p, rows, cols, x)
+            assert_close(got, oracle.gemv(fmt, src, rows, cols, x), tol=2e-5, what=f"{fmt} {rows}x{cols} b{batch}")
 
 
 @pytest.mark.parametrize("fmt", NEW)
