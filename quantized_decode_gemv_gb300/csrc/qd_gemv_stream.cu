@@ -195,12 +195,17 @@ __device__ __forceinline__ void cp_wait() {
 // each lane reads back only what it copied) and then the scale data of each row: 64
 // bytes (Q4_0/Q8_0 the 32 lanes' f16 scales, Q4_K the 4 super-block headers the 32 units
 // span, INT8 / INT4 the row scale) or, for Q4_1, 128 (the 32 lanes' (d, m) pairs).
-// Q6_K takes its step's four super-blocks whole instead (768 bytes of ql and qh per row, the
-// lanes of a super-block reading the bytes they share; 72 bytes of scales and d).
-constexpr int kQ6Step = 4 * 192;
+// Q6_K and Q5_K take their step's four super-blocks whole instead (Q6_K 768 bytes of ql
+// and qh per row and 72 bytes of scale records; Q5_K 640 bytes of fifth bits and nibbles
+// and 64 bytes of headers), the lanes of a super-block reading the bytes they share.
+constexpr int kQ6Step = 4 * 192, kQ5KStep = 4 * 160;
+template <int FMT>
+constexpr bool whole_blocks() {
+  return FMT == QD_Q6_K || FMT == QD_Q5_K;
+}
 template <int FMT, int RW>
 constexpr int slot_code_bytes() {
-  return FMT == QD_Q6_K ? RW * kQ6Step : RW * 32 * code_bytes<FMT>();
+  return FMT == QD_Q6_K ? RW * kQ6Step : FMT == QD_Q5_K ? RW * kQ5KStep : RW * 32 * code_bytes<FMT>();
 }
 // scale bytes per row of a slot: Q4_1 one (d, m) pair per lane's unit, Q5_0 one (d, qh)
 // record (6 bytes) per lane's unit, Q6_K its 4 super-blocks' 18-byte records, the others 64
@@ -229,34 +234,33 @@ constexpr int stages() {
 template <int FMT, int RW>
 __device__ __forceinline__ void stage_step(uint32_t slot, const RowPtrs<RW>& rp, int u, int lane, int units) {
   constexpr int CB = code_bytes<FMT>();
-  if constexpr (FMT == QD_Q6_K) {
-    // the step's super-blocks (an even count: rows hold an even number of them), chunk c of
-    // their codes by lane c and c - 32, word w of their scale records by lane w
+  if constexpr (whole_blocks<FMT>()) {
+    // the step's super-blocks, chunk c of their codes by lane c and c - 32; Q6_K's scale
+    // records (an even number of super-blocks a row: whole words) word w by lane w, Q5_K's
+    // 16-byte headers header k by lane k
+    constexpr int kBlk = FMT == QD_Q6_K ? 192 : 160, kStep = 4 * kBlk;
     const int sb0 = (u - lane) >> 3, nsb = min(4, units / 8 - sb0);
 #pragma unroll
     for (int rr = 0; rr < RW; ++rr) {
-      const uint8_t* c = rp.c[rr] + (uint32_t)sb0 * 192u;
-      const uint32_t dst = slot + (uint32_t)(rr * kQ6Step);
-      if (lane < nsb * 12) cp16(dst + 16 * lane, c + 16 * lane);
-      if (lane + 32 < nsb * 12) cp16(dst + 16 * (lane + 32), c + 16 * (lane + 32));
+      const uint8_t* c = rp.c[rr] + (uint32_t)sb0 * (uint32_t)kBlk;
+      const uint32_t dst = slot + (uint32_t)(rr * kStep);
+      const int chunks = nsb * kBlk / 16;
+      if (lane < chunks) cp16(dst + 16 * lane, c + 16 * lane);
+      if (lane + 32 < chunks) cp16(dst + 16 * (lane + 32), c + 16 * (lane + 32));
       const uint32_t sdst = slot + slot_code_bytes<FMT, RW>() + rr * slot_scale_bytes<FMT>();
-      if (lane < nsb * 18 / 4) cp4(sdst + 4 * lane, rp.s[rr] + (uint32_t)sb0 * 18u + 4 * lane);
+      if constexpr (FMT == QD_Q6_K) {
+        if (lane < nsb * 18 / 4) cp4(sdst + 4 * lane, rp.s[rr] + (uint32_t)sb0 * 18u + 4 * lane);
+      } else {
+        if (lane < nsb) cp16(sdst + 16 * lane, rp.s[rr] + (uint32_t)(sb0 + lane) * 16u);
+      }
     }
   } else {
 #pragma unroll
     for (int rr = 0; rr < RW; ++rr) {
       const uint32_t dst = slot + (uint32_t)(rr * 32 + lane) * CB;
-      if constexpr (FMT == QD_Q5_K) {
-        // unit u = 8s + 2c + h of a 160-byte super-block: nibbles at 32 + 32c + 16h, fifth
-        // bits at 16h (bit 2c for the low nibbles, 2c + 1 for the high ones)
-        const uint8_t* b = rp.c[rr] + (uint32_t)(u >> 3) * 160u;
-        cp16(dst, b + 32 + 32 * ((u >> 1) & 3) + 16 * (u & 1));
-        cp16(dst + 16, b + 16 * (u & 1));
-      } else {
-        const uint8_t* c = rp.c[rr] + (uint32_t)u * (uint32_t)CB;
+      const uint8_t* c = rp.c[rr] + (uint32_t)u * (uint32_t)CB;
 #pragma unroll
-        for (int k = 0; k < CB / 16; ++k) cp16(dst + 16 * k, c + 16 * k);
-      }
+      for (int k = 0; k < CB / 16; ++k) cp16(dst + 16 * k, c + 16 * k);
       const uint32_t sdst = slot + slot_code_bytes<FMT, RW>() + rr * slot_scale_bytes<FMT>();
       if constexpr (FMT == QD_Q4_1) {
         cp4(sdst + 4 * lane, rp.s[rr] + 4 * (uint32_t)u);  // (d, m) of this lane's unit
@@ -267,7 +271,7 @@ __device__ __forceinline__ void stage_step(uint32_t slot, const RowPtrs<RW>& rp,
 #pragma unroll
           for (int k = 0; k < 3; ++k) cp4(sdst + 6 * lane + 4 * k, rp.s[rr] + 6 * (uint32_t)u + 4 * k);
         }
-      } else if constexpr (FMT == QD_Q4_K || FMT == QD_Q5_K) {
+      } else if constexpr (FMT == QD_Q4_K) {
         if ((lane & 7) == 0) cp16(sdst + 2 * lane, rp.s[rr] + (uint32_t)(u >> 3) * 16u);  // header
       } else {
         if (lane == 0) cp4(sdst, rp.s[rr]);  // row scale
@@ -365,9 +369,12 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
           w[rr][t + 4] = ((qb | 0x80808080u) - 0x10101010u) ^ 0x80808080u;
         }
       } else if constexpr (FMT == QD_Q5_K) {
-        // Q4_K's nibbles plus the fifth bit: unsigned 5-bit codes through Q4_K's dot
-        const uint4 q = *reinterpret_cast<const uint4*>(cp);
-        const uint4 hq = *reinterpret_cast<const uint4*>(cp + 16);
+        // Q4_K's nibbles plus the fifth bit: unsigned 5-bit codes through Q4_K's dot.  Unit
+        // u = 8s + 2c + h of its 160-byte super-block (the step's lane / 8-th): nibbles at
+        // 32 + 32c + 16h, fifth bits at 16h (bit 2c for the low nibbles, 2c + 1 the high)
+        const uint8_t* blk = slot + rr * kQ5KStep + (lane >> 3) * 160;
+        const uint4 q = *reinterpret_cast<const uint4*>(blk + 32 + 32 * ((u >> 1) & 3) + 16 * (u & 1));
+        const uint4 hq = *reinterpret_cast<const uint4*>(blk + 16 * (u & 1));
         const uint32_t wv[4] = {q.x, q.y, q.z, q.w}, hv[4] = {hq.x, hq.y, hq.z, hq.w};
         const int b0 = 2 * ((u >> 1) & 3);
 #pragma unroll
@@ -483,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
     if (lg < groups) {
       const int u = lane + 32 * lj;
       // (Q6_K: copies by chunk, not by unit, so every lane takes part in a short last step)
-      if (u < units || FMT == QD_Q6_K) stage_step<FMT, RW>(ring_s + (uint32_t)slot_idx * SB, lrp, u, lane, units);
+      if (u < units || whole_blocks<FMT>()) stage_step<FMT, RW>(ring_s + (uint32_t)slot_idx * SB, lrp, u, lane, units);
       if (++lj == j1) {
         lj = j0;
         lg += nw;

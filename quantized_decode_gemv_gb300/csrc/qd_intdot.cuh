@@ -48,11 +48,9 @@ template <int FMT>
 __device__ __forceinline__ int unit_xb(int u) {
   return unit_xa<FMT>(u) + ((FMT == QD_Q4_K || FMT == QD_Q5_K) ? 32 : 16);
 }
-// code bytes a lane stages per unit: Q5_K its 16 nibble bytes, then the 16 bytes of fifth
-// bits of the same element positions
 template <int FMT>
 constexpr int code_bytes() {
-  return (FMT == QD_Q8_0 || FMT == QD_I8_ROW || FMT == QD_Q5_K) ? 32 : 16;
+  return (FMT == QD_Q8_0 || FMT == QD_I8_ROW) ? 32 : 16;
 }
 
 // Shared-memory x records: per batch row and unit, 112 bytes in seven 16-byte chunks:
