@@ -507,10 +507,14 @@ qd_status launch_fmt(const PackedView& W, const float* x, float* y, int batch, i
 
 }  // namespace
 
-bool gemv_fuses_norm(const GemvArgs& a) { return gemv_mma_supported(a) || gemv_streams(a); }
+bool gemv_fuses_norm(const GemvArgs& a, const float* gains) {
+  GemvArgs n = a;  // decided with the gains in place: they take shared memory too
+  n.norm_g = gains;
+  return gains && (gemv_mma_supported(n) || gemv_streams(n));
+}
 
 qd_status launch_q_gemv(const GemvArgs& a, cudaStream_t stream) {
-  // Batch 3-8 (Q4_0, Q8_0, INT8 rows): the tensor-core kernel.  Batch 1-8 and the shapes
+  // Batch 3-16 (Q4_0, Q8_0, INT8 rows): the mma.sync tensor-core kernel.  Batch 1-8 and the shapes
   // it supports: the streaming kernel.  Both fuse RMSNorm.  Otherwise the register-path
   // kernel below (RMSNorm must then have been applied by the caller, see gemv_fuses_norm).
   {
@@ -521,7 +525,7 @@ qd_status launch_q_gemv(const GemvArgs& a, cudaStream_t stream) {
     const qd_status st = launch_q_gemv_stream(a, stream);
     if (st != QD_ERR_UNSUPPORTED) return st;
   }
-  // Batch 9-16 INT8 rows: tensor cores.
+  // Batch 9-16 INT8 rows the mma kernel does not take (x too wide): tcgen05 tensor cores.
   {
     const qd_status st = launch_q_gemv_tc(a, stream);
     if (st != QD_ERR_UNSUPPORTED) return st;

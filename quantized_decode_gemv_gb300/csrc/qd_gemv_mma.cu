@@ -1,4 +1,4 @@
-// q_gemv for batch 3-8 on the tensor cores (mma.sync, f16 inputs, f32 accumulate).
+// q_gemv for batch 3-16 on the tensor cores (mma.sync, f16 inputs, f32 accumulate).
 //
 // y[b][r] = sum_c deq(W)[r][c] * x[b][c] (llmoxide blog s1, s10; dasLLAMA 8.7.1.4 matmul)
 // for a few batch rows is a skinny dense contraction, and on the CUDA cores its cost grows
@@ -17,8 +17,8 @@
 //    largest value (the batch-16 tensor-core GEMV uses the same split).  Products of f16
 //    values are exact and sum in f32.
 //  * mma.sync.m16n8k16 multiplies a 16-row tile of one unit's codes by the hi and lo parts
-//    of 8 batch columns, two K halves: four instructions per unit, chained through one
-//    accumulator.  The order of the 32 elements along K is free as long as A and B agree:
+//    of 8 batch columns, two K halves: four instructions per unit and block of 8 columns
+//    (batch 9-16: two blocks sharing the unit's A fragments).  The order of the 32 elements along K is free as long as A and B agree:
 //    lane t takes its A values from code word t (bytes 4t..4t+3) of each row, pairing
 //    bytes (0, 2) and (1, 3), so one 32-bit load and a few bit operations make its
 //    fragments, and x is staged in the same order.  A unit is one quantisation block, so
@@ -86,8 +86,11 @@ template <int FMT>
 constexpr int slot_bytes() {
   return kTileRows * row_stride<FMT>() + scale_bytes<FMT>();
 }
+// batch columns: one or two blocks of 8 (the MMA's N); scale and norm arrays keep 16 a stage
+constexpr int kMaxCols = 16;
+__host__ __device__ constexpr int col_blocks(int batch) { return batch > 8 ? 2 : 1; }
 // per-warp partial accumulators for the column split, two tiles deep
-constexpr int kPartialBytes = 2 * kWarps * 32 * 4 * 4;
+__host__ __device__ constexpr size_t partial_bytes(int nc) { return (size_t)2 * kWarps * 32 * 4 * nc * 4; }
 
 // Shared-memory layout of one launch (byte offsets; every part 16-byte aligned).
 struct Layout {
@@ -103,9 +106,9 @@ __host__ __device__ inline Layout layout(int units, int batch, bool norm, int st
   L.xs = L.ring + (size_t)kWarps * stages * slot_bytes<FMT>();
   L.gs = L.xs + (size_t)batch * L.x_row;
   L.sx = L.gs + (norm ? (size_t)units * 128 : 0);
-  L.ssq = L.sx + (size_t)nst * 8 * 4;
-  L.partial = L.ssq + (size_t)nst * 8 * 4;
-  L.bar = L.partial + kPartialBytes;
+  L.ssq = L.sx + (size_t)nst * kMaxCols * 4;
+  L.partial = L.ssq + (size_t)nst * kMaxCols * 4;
+  L.bar = L.partial + partial_bytes(col_blocks(batch));
   L.total = L.bar + 16;
   return L;
 }
@@ -211,13 +214,12 @@ __device__ __forceinline__ void qkv_pair(const Params& p, int64_t r, int b, floa
   }
 }
 
-// One unit's fragments: A for rows g, g + 8 of the 16-row tile (codes at `row0` and
-// `row8` in the ring slot; a0 = K half 0, a1 = K half 1, each rows (g, g + 8) x pairs
-// ((4t, 4t+2), (4t+1, 4t+3))) and B for column g (x at `xu`: v0, v1 = the two K halves'
-// (hi b0, hi b1, lo b0, lo b1)).
+// One unit's A fragments: rows g, g + 8 of the 16-row tile (codes at `row0` and `row8` in
+// the ring slot; a0 = K half 0, a1 = K half 1, each rows (g, g + 8) x pairs
+// ((4t, 4t+2), (4t+1, 4t+3))).
 template <int FMT>
-__device__ __forceinline__ void unit_frags(const uint8_t* row0, const uint8_t* row8, const uint8_t* xu, int t,
-                                           uint32_t (&a0)[4], uint32_t (&a1)[4], uint4& v0, uint4& v1) {
+__device__ __forceinline__ void unit_a(const uint8_t* row0, const uint8_t* row8, int t, uint32_t (&a0)[4],
+                                       uint32_t (&a1)[4]) {
   if constexpr (FMT == QD_Q4_0) {
     const uint32_t w0 = *reinterpret_cast<const uint32_t*>(row0 + 4 * t);
     const uint32_t w1 = *reinterpret_cast<const uint32_t*>(row8 + 4 * t);
@@ -233,18 +235,16 @@ __device__ __forceinline__ void unit_frags(const uint8_t* row0, const uint8_t* r
     i8_word(x0, a1[0], a1[2]);
     i8_word(x1, a1[1], a1[3]);
   }
+}
+// One unit's B fragments for column g of a block (x at `xu`): v0, v1 = the two K halves'
+// (hi b0, hi b1, lo b0, lo b1).
+__device__ __forceinline__ void unit_b(const uint8_t* xu, int t, uint4& v0, uint4& v1) {
   v0 = *reinterpret_cast<const uint4*>(xu + 16 * t);
   v1 = *reinterpret_cast<const uint4*>(xu + 64 + 16 * t);
 }
-
-// One unit's product: d += the unit's f32 sums for (row g, column 2t), (g, 2t + 1),
-// (g + 8, 2t), (g + 8, 2t + 1), two chains of two MMAs (one per K half, lo part first).
-template <int FMT>
-__device__ __forceinline__ void unit_mma(float (&d)[4], const uint8_t* row0, const uint8_t* row8, const uint8_t* xu,
-                                         int t) {
-  uint32_t a0[4], a1[4];
-  uint4 v0, v1;
-  unit_frags<FMT>(row0, row8, xu, t, a0, a1, v0, v1);
+// d += A x B over the unit's two K halves, two chains of two MMAs (lo parts first), added.
+__device__ __forceinline__ void unit_mma(float (&d)[4], const uint32_t (&a0)[4], const uint32_t (&a1)[4], uint4 v0,
+                                         uint4 v1) {
   float e[4] = {0.f, 0.f, 0.f, 0.f};
   mma_f16(d, a0, v0.z, v0.w);
   mma_f16(e, a1, v1.z, v1.w);
@@ -261,109 +261,99 @@ __device__ __forceinline__ float scale_of(const uint4& s, int uu) {
   return (uu & 1) ? f.y : f.x;
 }
 
-// One ring stage of `NU` units (NU = 8, or 0: `nu` units known at run time) into the
-// stage accumulator `as`: block-scaled formats scale each unit's sums by the rows' block
-// scales d; INT8 rows keep unit-interleaved MMA chains and add them at the end.
-template <int FMT, int NU>
-__device__ __forceinline__ void stage_mma(float (&as)[4], const uint8_t* slot, const uint8_t* xst, int g, int t,
-                                          int nu) {
+// One ring stage of `NU` units (NU = 8, or 0: `nu` units known at run time) for NC blocks of
+// 8 batch columns (x of block c at xst[c]) into the stage accumulators as[c]: block-scaled
+// formats scale each unit's sums by the rows' block scales d; INT8 rows keep unit-
+// interleaved MMA chains and add them at the end.  Each unit's A fragments serve every
+// block.  Full stages run as groups of units: fragments first, then the MMAs round-robin
+// over the group's units, so independent accumulator chains are in flight.
+template <int FMT, int NU, int NC>
+__device__ __forceinline__ void stage_mma(float (&as)[NC][4], const uint8_t* slot, const uint8_t* const (&xst)[NC],
+                                          int g, int t, int nu) {
   constexpr int CB = code_bytes<FMT>();
   constexpr int RS = row_stride<FMT>();
+  constexpr int G = NC == 1 ? 4 : 2;  // units per group
   const uint8_t* row0 = slot + g * RS;
   const uint8_t* row8 = row0 + 8 * RS;
   if constexpr (FMT == QD_I8_ROW) {
-    float c[4][4];
+    float c[NC][2][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
+    for (int b = 0; b < NC; ++b)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) c[b][j][0] = c[b][j][1] = c[b][j][2] = c[b][j][3] = 0.f;
+    auto one = [&](int uu, int j) {
+      uint32_t a0[4], a1[4];
+      unit_a<FMT>(row0 + uu * CB, row8 + uu * CB, t, a0, a1);
+#pragma unroll
+      for (int b = 0; b < NC; ++b) {
+        uint4 v0, v1;
+        unit_b(xst[b] + uu * 128, t, v0, v1);
+        unit_mma(c[b][j], a0, a1, v0, v1);
+      }
+    };
     if constexpr (NU > 0) {
-      // groups of 4 units: fragments first, then the MMAs round-robin over the units, so
-      // 8 independent accumulator chains are in flight (K half 0 in c[u], half 1 in c2[u])
-      float c2[4][4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) c2[j][0] = c2[j][1] = c2[j][2] = c2[j][3] = 0.f;
-#pragma unroll
-      for (int q = 0; q < NU / 4; ++q) {
-        uint32_t A0[4][4], A1[4][4];
-        uint4 V0[4], V1[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          unit_frags<FMT>(row0 + (4 * q + u) * CB, row8 + (4 * q + u) * CB, xst + (4 * q + u) * 128, t, A0[u], A1[u],
-                          V0[u], V1[u]);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          mma_f16(c[u], A0[u], V0[u].z, V0[u].w);
-          mma_f16(c2[u], A1[u], V1[u].z, V1[u].w);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          mma_f16(c[u], A0[u], V0[u].x, V0[u].y);
-          mma_f16(c2[u], A1[u], V1[u].x, V1[u].y);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) c[j][i] += c2[j][i];
+      for (int uu = 0; uu < NU; ++uu) one(uu, uu & 1);
     } else {
-      int uu = 0;
-      for (; uu + 1 < nu; uu += 2) {
-        unit_mma<FMT>(c[0], row0 + uu * CB, row8 + uu * CB, xst + uu * 128, t);
-        unit_mma<FMT>(c[1], row0 + (uu + 1) * CB, row8 + (uu + 1) * CB, xst + (uu + 1) * 128, t);
-      }
-      if (uu < nu) unit_mma<FMT>(c[2], row0 + uu * CB, row8 + uu * CB, xst + uu * 128, t);
+      for (int uu = 0; uu < nu; ++uu) one(uu, 0);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) as[i] = (c[0][i] + c[1][i]) + (c[2][i] + c[3][i]);
+    for (int b = 0; b < NC; ++b)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) as[b][i] = c[b][0][i] + c[b][1][i];
   } else {
     // the block scales of rows g and g + 8 for the stage's 8 units (f16, 16 bytes a row)
     const uint8_t* scs = slot + kTileRows * RS;
     const uint4 s0 = *reinterpret_cast<const uint4*>(scs + g * 16);
     const uint4 s8 = *reinterpret_cast<const uint4*>(scs + (g + 8) * 16);
-    auto one = [&](int uu) {
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      unit_mma<FMT>(d, row0 + uu * CB, row8 + uu * CB, xst + uu * 128, t);
-      const float d0 = scale_of(s0, uu), d8 = scale_of(s8, uu);
-      as[0] = fmaf(d0, d[0], as[0]);
-      as[1] = fmaf(d0, d[1], as[1]);
-      as[2] = fmaf(d8, d[2], as[2]);
-      as[3] = fmaf(d8, d[3], as[3]);
-    };
     if constexpr (NU > 0) {
-      // groups of 4 units: fragments first, then the MMAs round-robin over the units (8
-      // independent accumulator chains in flight), then the block scales
 #pragma unroll
-      for (int q = 0; q < NU / 4; ++q) {
-        uint32_t A0[4][4], A1[4][4];
-        uint4 V0[4], V1[4];
-        float D[4][4], E[4][4];
+      for (int q = 0; q < NU / G; ++q) {
+        uint32_t A0[G][4], A1[G][4];
+        uint4 V0[NC][G], V1[NC][G];
+        float D[NC][G][4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          unit_frags<FMT>(row0 + (4 * q + u) * CB, row8 + (4 * q + u) * CB, xst + (4 * q + u) * 128, t, A0[u], A1[u],
-                          V0[u], V1[u]);
-          D[u][0] = D[u][1] = D[u][2] = D[u][3] = 0.f;
-          E[u][0] = E[u][1] = E[u][2] = E[u][3] = 0.f;
+        for (int u = 0; u < G; ++u) {
+          unit_a<FMT>(row0 + (G * q + u) * CB, row8 + (G * q + u) * CB, t, A0[u], A1[u]);
+#pragma unroll
+          for (int b = 0; b < NC; ++b) {
+            unit_b(xst[b] + (G * q + u) * 128, t, V0[b][u], V1[b][u]);
+            D[b][u][0] = D[b][u][1] = D[b][u][2] = D[b][u][3] = 0.f;
+          }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          mma_f16(D[u], A0[u], V0[u].z, V0[u].w);
-          mma_f16(E[u], A1[u], V1[u].z, V1[u].w);
-        }
+        for (int b = 0; b < NC; ++b)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          mma_f16(D[u], A0[u], V0[u].x, V0[u].y);
-          mma_f16(E[u], A1[u], V1[u].x, V1[u].y);
-        }
+          for (int u = 0; u < G; ++u) unit_mma(D[b][u], A0[u], A1[u], V0[b][u], V1[b][u]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float d0 = scale_of(s0, 4 * q + u), d8 = scale_of(s8, 4 * q + u);
-          as[0] = fmaf(d0, D[u][0] + E[u][0], as[0]);
-          as[1] = fmaf(d0, D[u][1] + E[u][1], as[1]);
-          as[2] = fmaf(d8, D[u][2] + E[u][2], as[2]);
-          as[3] = fmaf(d8, D[u][3] + E[u][3], as[3]);
+        for (int u = 0; u < G; ++u) {
+          const float d0 = scale_of(s0, G * q + u), d8 = scale_of(s8, G * q + u);
+#pragma unroll
+          for (int b = 0; b < NC; ++b) {
+            as[b][0] = fmaf(d0, D[b][u][0], as[b][0]);
+            as[b][1] = fmaf(d0, D[b][u][1], as[b][1]);
+            as[b][2] = fmaf(d8, D[b][u][2], as[b][2]);
+            as[b][3] = fmaf(d8, D[b][u][3], as[b][3]);
+          }
         }
       }
     } else {
-      for (int uu = 0; uu < nu; ++uu) one(uu);  // block formats: nu is even
+      for (int uu = 0; uu < nu; ++uu) {  // block formats: nu is even
+        uint32_t a0[4], a1[4];
+        unit_a<FMT>(row0 + uu * CB, row8 + uu * CB, t, a0, a1);
+        const float d0 = scale_of(s0, uu), d8 = scale_of(s8, uu);
+#pragma unroll
+        for (int b = 0; b < NC; ++b) {
+          uint4 v0, v1;
+          unit_b(xst[b] + uu * 128, t, v0, v1);
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          unit_mma(d, a0, a1, v0, v1);
+          as[b][0] = fmaf(d0, d[0], as[b][0]);
+          as[b][1] = fmaf(d0, d[1], as[b][1]);
+          as[b][2] = fmaf(d8, d[2], as[b][2]);
+          as[b][3] = fmaf(d8, d[3], as[b][3]);
+        }
+      }
     }
   }
 }
@@ -448,15 +438,15 @@ __device__ __forceinline__ void convert_x(uint8_t* xs, int64_t x_row, const floa
           px[h ^ 1] = fr[1];
         }
         if (lane == 0) {
-          sxs[s * 8 + b] = bad ? __uint_as_float(0x7FC00000u) : live ? pow2i(e) : 0.f;
-          ssq[s * 8 + b] = ss[b];
+          sxs[s * kMaxCols + b] = bad ? __uint_as_float(0x7FC00000u) : live ? pow2i(e) : 0.f;
+          ssq[s * kMaxCols + b] = ss[b];
         }
       }
     }
   }
 }
 
-template <int FMT>
+template <int FMT, int NC>
 __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int CB = code_bytes<FMT>();
@@ -559,8 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
     for (int b = 0; b < p.batch; ++b)
       tc::bulk_copy_g2s(tc::smem_u32(xs + b * L.x_row), p.x + b * p.x_stride + (int64_t)p.u0 * 32, row_bytes, bar);
   }
-  for (int i = threadIdx.x; i < nst * 8; i += kThreads) {
-    if ((i & 7) >= p.batch) sxs[i] = ssq[i] = 0.f;  // columns without a batch row
+  for (int i = threadIdx.x; i < nst * kMaxCols; i += kThreads) {
+    if ((i % kMaxCols) >= p.batch) sxs[i] = ssq[i] = 0.f;  // columns without a batch row
   }
   if (!__syncthreads_and(tc::mbar_wait_sleep(bar, 0))) {
     // the copies did not land in time: report it, give them one more bounded wait (they
@@ -571,95 +561,126 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
     return;
   }
 
+  // x in place, 8 batch rows a pass (rows 8-15 with their scale and norm columns offset)
   if (p.batch <= 4) convert_x<4>(xs, L.x_row, gs, sxs, ssq, units, nst, p.batch, norm, warp, lane);
-  else convert_x<8>(xs, L.x_row, gs, sxs, ssq, units, nst, p.batch, norm, warp, lane);
+  else convert_x<8>(xs, L.x_row, gs, sxs, ssq, units, nst, min(p.batch, 8), norm, warp, lane);
+  if constexpr (NC > 1) {
+    if (p.batch > 8)
+      convert_x<8>(xs + 8 * L.x_row, L.x_row, gs, sxs + 8, ssq + 8, units, nst, p.batch - 8, norm, warp, lane);
+  }
   __syncthreads();
-  // RMSNorm factors of this lane's columns 2t, 2t + 1 (stage sums in stage order: every
-  // CTA forms the same value)
-  float inv[2] = {1.f, 1.f};
-  if (norm) {
+  // RMSNorm factors of this lane's columns 8c + 2t, 8c + 2t + 1 (stage sums in stage order:
+  // every CTA forms the same value)
+  float inv[NC][2];
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      float tt = 0.f;
-      for (int s = 0; s < nst; ++s) tt += ssq[s * 8 + 2 * t + j];
-      inv[j] = 1.0f / sqrtf(tt / (float)(units * 32) + p.eps);
+      inv[c][j] = 1.f;
+      if (norm) {
+        float tt = 0.f;
+        for (int s = 0; s < nst; ++s) tt += ssq[s * kMaxCols + 8 * c + 2 * t + j];
+        inv[c][j] = 1.0f / sqrtf(tt / (float)(units * 32) + p.eps);
+      }
     }
-  }
   pdl_trigger();
 
-  // this lane's B column: batch row g, or (no such row) the last staged one, whose sums
-  // land in a column the epilogue never stores
-  const uint8_t* xrow = xs + min(g, p.batch - 1) * L.x_row;
-  unsigned long long best[2] = {0ull, 0ull};  // argmax keys of columns 2t, 2t + 1
-  float acc[4];
+  // this lane's B column of block c: batch row 8c + g, or (no such row) the last staged
+  // one, whose sums land in a column the epilogue never stores
+  const uint8_t* xrow[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) xrow[c] = xs + min(8 * c + g, p.batch - 1) * L.x_row;
+  unsigned long long best[NC][2];  // argmax keys of columns 8c + 2t, 8c + 2t + 1
+#pragma unroll
+  for (int c = 0; c < NC; ++c) best[c][0] = best[c][1] = 0ull;
+  float acc[NC][4];
   int cs = 0, it = 0;
   for (int64_t tl = gslot; tl < tiles; tl += ngs, ++it) {  // uniform over the group
-    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
     for (int st = st0; st < st1; ++st) {
       __syncwarp();
       issue(cs == 0 ? kStages - 1 : cs - 1);
       cp_wait_dyn(kStages - 1);
       __syncwarp();
       const uint8_t* slot = ring + (size_t)cs * kSlot;
-      const uint8_t* xst = xrow + (size_t)st * kStageCols * 4;
+      const uint8_t* xst[NC];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) xst[c] = xrow[c] + (size_t)st * kStageCols * 4;
       const int nu = min(kStageUnits, units - st * kStageUnits);
-      float as[4] = {0.f, 0.f, 0.f, 0.f};
-      if (nu == kStageUnits) stage_mma<FMT, kStageUnits>(as, slot, xst, g, t, nu);
-      else stage_mma<FMT, 0>(as, slot, xst, g, t, nu);
-      // the stage's x scales of columns 2t, 2t + 1
-      const float2 sx = *reinterpret_cast<const float2*>(sxs + st * 8 + 2 * t);
-      acc[0] = fmaf(sx.x, as[0], acc[0]);
-      acc[1] = fmaf(sx.y, as[1], acc[1]);
-      acc[2] = fmaf(sx.x, as[2], acc[2]);
-      acc[3] = fmaf(sx.y, as[3], acc[3]);
+      float as[NC][4];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) as[c][0] = as[c][1] = as[c][2] = as[c][3] = 0.f;
+      if (nu == kStageUnits) stage_mma<FMT, kStageUnits, NC>(as, slot, xst, g, t, nu);
+      else stage_mma<FMT, 0, NC>(as, slot, xst, g, t, nu);
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        // the stage's x scales of columns 8c + 2t, 8c + 2t + 1
+        const float2 sx = *reinterpret_cast<const float2*>(sxs + st * kMaxCols + 8 * c + 2 * t);
+        acc[c][0] = fmaf(sx.x, as[c][0], acc[c][0]);
+        acc[c][1] = fmaf(sx.y, as[c][1], acc[c][1]);
+        acc[c][2] = fmaf(sx.x, as[c][2], acc[c][2]);
+        acc[c][3] = fmaf(sx.y, as[c][3], acc[c][3]);
+      }
       cs = (cs + 1 == kStages) ? 0 : cs + 1;
     }
     if (KS > 1) {
       // the group's column parts, summed in part order by its first warp
-      float* pt = partial + (size_t)(it & 1) * kWarps * 128;
-      *reinterpret_cast<float4*>(pt + (warp * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      float* pt = partial + (size_t)(it & 1) * kWarps * 32 * 4 * NC;
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+        *reinterpret_cast<float4*>(pt + ((warp * 32 + lane) * NC + c) * 4) =
+            make_float4(acc[c][0], acc[c][1], acc[c][2], acc[c][3]);
       asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(KS * 32) : "memory");
       if (ks != 0) continue;  // uniform per warp
-      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-      for (int k = 0; k < KS; ++k) {
-        const float4 q = *reinterpret_cast<const float4*>(pt + ((grp * KS + k) * 32 + lane) * 4);
-        acc[0] += q.x;
-        acc[1] += q.y;
-        acc[2] += q.z;
-        acc[3] += q.w;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+        for (int k = 0; k < KS; ++k) {
+          const float4 q = *reinterpret_cast<const float4*>(pt + (((grp * KS + k) * 32 + lane) * NC + c) * 4);
+          acc[c][0] += q.x;
+          acc[c][1] += q.y;
+          acc[c][2] += q.z;
+          acc[c][3] += q.w;
+        }
       }
     }
-    // ---- end of a tile (first warp of the group): rows tile + g, + 8; columns 2t, 2t + 1
+    // ---- end of a tile (first warp of the group): rows tile + g, + 8; columns 8c + 2t,
+    // 8c + 2t + 1
     const int64_t rbase = tl * kTileRows;
-    float v[4];
+    float rsc[2] = {1.f, 1.f};  // INT8 row scales of rows g, g + 8
+    if constexpr (FMT == QD_I8_ROW) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t r = rbase + g + (i >= 2 ? 8 : 0);
-      float s = inv[i & 1];
-      if constexpr (FMT == QD_I8_ROW)
-        s *= __ldg(reinterpret_cast<const float*>(W.scales + min(r, W.rows - 1) * W.row_scale_bytes));
-      v[i] = acc[i] * s;
+      for (int h = 0; h < 2; ++h)
+        rsc[h] = __ldg(reinterpret_cast<const float*>(W.scales + min(rbase + g + 8 * h, W.rows - 1) * W.row_scale_bytes));
     }
-    // the next row's values (row g + 1 is lane + 4) for the pair epilogues
-    float nx[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) nx[i] = __shfl_down_sync(0xffffffffu, v[i], 4);
+    for (int c = 0; c < NC; ++c) {
+      float v[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t r = rbase + g + (i >= 2 ? 8 : 0);
-      const int b = 2 * t + (i & 1);
-      if (b >= p.batch || r >= W.rows) continue;
-      if (p.mode == kGemvSwiGLU) {
-        if ((g & 1) == 0 && r + 1 < W.rows) p.y[(int64_t)b * (W.rows / 2) + r / 2] = v[i] / (1.0f + expf(-v[i])) * nx[i];
-      } else if (p.mode == kGemvQKV) {
-        if ((g & 1) == 0 && r + 1 < W.rows) qkv_pair(p, r, b, v[i], nx[i]);
-      } else {
-        float* dst = p.y + (int64_t)b * W.rows + r;
-        if (p.mode == kGemvAccumulate || p.accumulate) *dst = __ldcg(dst) + v[i];
-        else *dst = v[i];
-        if (p.mode == kGemvArgmax) {
-          const unsigned long long key = argmax_key(v[i], (uint32_t)r);
-          best[i & 1] = key > best[i & 1] ? key : best[i & 1];
+      for (int i = 0; i < 4; ++i) v[i] = acc[c][i] * inv[c][i & 1] * rsc[i >> 1];
+      // the next row's values (row g + 1 is lane + 4) for the pair epilogues
+      float nx[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) nx[i] = __shfl_down_sync(0xffffffffu, v[i], 4);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t r = rbase + g + (i >= 2 ? 8 : 0);
+        const int b = 8 * c + 2 * t + (i & 1);
+        if (b >= p.batch || r >= W.rows) continue;
+        if (p.mode == kGemvSwiGLU) {
+          if ((g & 1) == 0 && r + 1 < W.rows)
+            p.y[(int64_t)b * (W.rows / 2) + r / 2] = v[i] / (1.0f + expf(-v[i])) * nx[i];
+        } else if (p.mode == kGemvQKV) {
+          if ((g & 1) == 0 && r + 1 < W.rows) qkv_pair(p, r, b, v[i], nx[i]);
+        } else {
+          float* dst = p.y + (int64_t)b * W.rows + r;
+          if (p.mode == kGemvAccumulate || p.accumulate) *dst = __ldcg(dst) + v[i];
+          else *dst = v[i];
+          if (p.mode == kGemvArgmax) {
+            const unsigned long long key = argmax_key(v[i], (uint32_t)r);
+            best[c][i & 1] = key > best[c][i & 1] ? key : best[c][i & 1];
+          }
         }
       }
     }
@@ -669,16 +690,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
     // per batch column: max over the lanes holding it (same t), one atomicMax per warp;
     // the last CTA to arrive finalises the tokens and re-arms keys and counter
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      unsigned long long kk = best[j];
+    for (int c = 0; c < NC; ++c)
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        const unsigned long long o = __shfl_xor_sync(0xffffffffu, kk, off);
-        kk = o > kk ? o : kk;
+      for (int j = 0; j < 2; ++j) {
+        unsigned long long kk = best[c][j];
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          const unsigned long long o = __shfl_xor_sync(0xffffffffu, kk, off);
+          kk = o > kk ? o : kk;
+        }
+        const int b = 8 * c + 2 * t + j;
+        if (g == 0 && kk != 0 && b < p.batch) atomicMax(p.am.key + b, kk);
       }
-      const int b = 2 * t + j;
-      if (g == 0 && kk != 0 && b < p.batch) atomicMax(p.am.key + b, kk);
-    }
     __syncthreads();
     if (threadIdx.x == 0) {
       unsigned int old;
@@ -708,13 +731,13 @@ int sm_count() {
   return v;
 }
 
-template <int FMT>
+template <int FMT, int NC>
 bool smem_attr_set() {
   static bool done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (!done[dev]) {
-    if (cudaFuncSetAttribute(k_gemv_mma<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) !=
+    if (cudaFuncSetAttribute(k_gemv_mma<FMT, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) !=
         cudaSuccess) {
       cudaGetLastError();
       return false;
@@ -799,14 +822,16 @@ qd_status launch_range(Params p, bool pdl, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_gemv_mma<FMT>, p) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
+  if (col_blocks(p.batch) == 2)
+    return cudaLaunchKernelEx(&cfg, k_gemv_mma<FMT, 2>, p) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, k_gemv_mma<FMT, 1>, p) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
 }
 
 // All column ranges in order: the first stores (or accumulates, in accumulate mode), the
 // rest accumulate, each a programmatic dependent of the one before.
 template <int FMT>
 qd_status launch(Params p, bool pdl, cudaStream_t stream) {
-  if (!smem_attr_set<FMT>()) return QD_ERR_CUDA;
+  if (!(col_blocks(p.batch) == 2 ? smem_attr_set<FMT, 2>() : smem_attr_set<FMT, 1>())) return QD_ERR_CUDA;
   const int units = (int)(p.W.cols / 32);
   const int ru = range_units(FMT, units, p.batch, p.norm_g != nullptr);
   if (ru <= 0) return QD_ERR_UNSUPPORTED;
@@ -822,28 +847,43 @@ qd_status launch(Params p, bool pdl, cudaStream_t stream) {
 
 }  // namespace mma_gemv
 
-// Batch 3-8, Q4_0 / Q8_0 / INT8 rows, even unit counts for the block formats (4-byte scale
-// copies), x and norm_g on 16-byte boundaries (bulk copies); x of every batch row beside a
-// ring of two stages in shared memory, or (store and accumulate without RMSNorm) split
-// into column ranges that fit.
-bool gemv_mma_supported(const GemvArgs& a) {
-  using namespace mma_gemv;
-  if (!fmt_taken(a.fmt) || a.batch < 3 || a.batch > 8 || a.W.cols % 32 || a.W.cols > (1 << 22)) return false;
-  if (reinterpret_cast<uintptr_t>(a.x) & 15) return false;
-  if (a.norm_g && (reinterpret_cast<uintptr_t>(a.norm_g) & 15)) return false;
+namespace mma_gemv {
+
+// Whether one launch sequence (a single launch, or column ranges) takes these arguments:
+// x of every batch row beside a ring of two stages, or (store and accumulate without the
+// fused norm) column ranges that fit.
+bool one_pass_fits(const GemvArgs& a) {
   const int units = (int)(a.W.cols / 32);
-  if ((a.fmt == QD_Q4_0 || a.fmt == QD_Q8_0) && (units & 1)) return false;
-  if (a.mode == kGemvSwiGLU || a.mode == kGemvQKV) {
-    if (a.W.rows & 1) return false;
-  }
   if (stages_for(a.fmt, units, a.batch, a.norm_g != nullptr) >= 2) return true;
   const bool splits = (a.mode == kGemvStore || a.mode == kGemvAccumulate) && !a.norm_g;
   return splits && range_units(a.fmt, units, a.batch, false) > 0;
 }
 
-qd_status launch_q_gemv_mma(const GemvArgs& a, cudaStream_t stream) {
-  using namespace mma_gemv;
-  if (!gemv_mma_supported(a)) return QD_ERR_UNSUPPORTED;
+// Batch rows [b0, b0 + nb) of `a` as arguments of their own: x, y and every epilogue
+// pointer moved to row b0.
+GemvArgs row_slice(const GemvArgs& a, int b0, int nb) {
+  GemvArgs s = a;
+  s.batch = nb;
+  s.x = a.x + (int64_t)b0 * a.W.cols;
+  const int64_t ycols = a.mode == kGemvSwiGLU ? a.W.rows / 2 : a.W.rows;
+  if (a.y) s.y = a.y + (int64_t)b0 * ycols;
+  if (a.mode == kGemvQKV) {
+    QkvEpilogue& e = s.qkv;
+    e.pos = a.qkv.pos + b0;
+    e.q_out = a.qkv.q_out + (int64_t)b0 * a.qkv.q_stride;
+    const int64_t esz = a.qkv.kv_f16 ? 2 : 4;
+    e.kc = static_cast<uint8_t*>(a.qkv.kc) + (int64_t)b0 * a.qkv.cache_batch_stride * esz;
+    e.vc = static_cast<uint8_t*>(a.qkv.vc) + (int64_t)b0 * a.qkv.cache_batch_stride * esz;
+  }
+  if (a.mode == kGemvArgmax) {
+    s.am.key = a.am.key + b0;
+    s.am.tok_out = a.am.tok_out + b0;
+    s.am.pos = a.am.pos + b0;
+  }
+  return s;
+}
+
+qd_status launch_args(const GemvArgs& a, cudaStream_t stream) {
   Params p;
   p.W = a.W;
   p.x = a.x;
@@ -866,6 +906,45 @@ qd_status launch_q_gemv_mma(const GemvArgs& a, cudaStream_t stream) {
     case QD_Q8_0: return launch<QD_Q8_0>(p, a.pdl, stream);
     default: return launch<QD_I8_ROW>(p, a.pdl, stream);
   }
+}
+
+}  // namespace mma_gemv
+
+// Batch 3-16, Q4_0 / Q8_0 / INT8 rows, even unit counts for the block formats (4-byte scale
+// copies), x and norm_g on 16-byte boundaries (bulk copies).  One pass over the weights when
+// x of every batch row fits beside a ring of two stages (or, store and accumulate without
+// RMSNorm, in column ranges that fit).  At batch 9-16 otherwise two passes of up to 8 rows
+// for Q4_0 and Q8_0 (measured faster than column ranges: the second pass finds much of
+// the weights in L2); INT8 rows then go to the batch-16 tcgen05 kernel, which measured
+// faster there.
+bool gemv_mma_supported(const GemvArgs& a) {
+  using namespace mma_gemv;
+  if (!fmt_taken(a.fmt) || a.batch < 3 || a.batch > kMaxCols || a.W.cols % 32 || a.W.cols > (1 << 22)) return false;
+  if (reinterpret_cast<uintptr_t>(a.x) & 15) return false;
+  if (a.norm_g && (reinterpret_cast<uintptr_t>(a.norm_g) & 15)) return false;
+  const int units = (int)(a.W.cols / 32);
+  if ((a.fmt == QD_Q4_0 || a.fmt == QD_Q8_0) && (units & 1)) return false;
+  if (a.mode == kGemvSwiGLU || a.mode == kGemvQKV) {
+    if (a.W.rows & 1) return false;
+  }
+  if (a.batch <= 8) return one_pass_fits(a);
+  const int units_ok = stages_for(a.fmt, units, a.batch, a.norm_g != nullptr) >= 2;
+  if (units_ok) return true;
+  if (a.fmt == QD_I8_ROW) return false;
+  return one_pass_fits(row_slice(a, 0, 8)) && one_pass_fits(row_slice(a, 8, a.batch - 8));
+}
+
+qd_status launch_q_gemv_mma(const GemvArgs& a, cudaStream_t stream) {
+  using namespace mma_gemv;
+  if (!gemv_mma_supported(a)) return QD_ERR_UNSUPPORTED;
+  const int units = (int)(a.W.cols / 32);
+  if (a.batch <= 8 || stages_for(a.fmt, units, a.batch, a.norm_g != nullptr) >= 2) return launch_args(a, stream);
+  // two passes of up to 8 batch rows, the second a programmatic dependent of the first
+  const qd_status st = launch_args(row_slice(a, 0, 8), stream);
+  if (st != QD_OK) return st;
+  GemvArgs hi = row_slice(a, 8, a.batch - 8);
+  hi.pdl = true;
+  return launch_args(hi, stream);
 }
 
 }  // namespace qd

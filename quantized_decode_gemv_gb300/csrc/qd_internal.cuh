@@ -348,13 +348,13 @@ qd_status launch_q_gemv_stream(const GemvArgs& a, cudaStream_t stream);
 // Whether launch_q_gemv runs the streaming kernel for these arguments (and so can
 // take norm_g and the pdl flag).
 bool gemv_streams(const GemvArgs& a);
-// Batch 3-8 on the tensor cores (mma.sync, binary16 codes times x split into two binary16
+// Batch 3-16 on the tensor cores (mma.sync, binary16 codes times x split into two binary16
 // parts; Q4_0, Q8_0, INT8 rows; every epilogue and the fused RMSNorm; store and accumulate
 // over column ranges when x is wider than the shared memory holds).
 bool gemv_mma_supported(const GemvArgs& a);
 qd_status launch_q_gemv_mma(const GemvArgs& a, cudaStream_t stream);
-// Whether launch_q_gemv fuses RMSNorm (norm_g) for these arguments.
-bool gemv_fuses_norm(const GemvArgs& a);
+// Whether launch_q_gemv fuses RMSNorm for these arguments with norm_g = gains.
+bool gemv_fuses_norm(const GemvArgs& a, const float* gains);
 // Batch 9-16 per-row INT8 on the tensor cores (store, accumulate or SwiGLU; no fused norm).
 bool gemv_tc_supported(const GemvArgs& a);
 qd_status launch_q_gemv_tc(const GemvArgs& a, cudaStream_t stream);

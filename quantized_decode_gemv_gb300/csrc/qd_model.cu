@@ -234,7 +234,7 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
   // GEMV with RMSNorm fused into its prologue when the streaming kernel runs; a
   // separate norm kernel (into xn) otherwise.
   auto normed = [&](GemvArgs a, const float* gains) -> qd_status {
-    if (gemv_fuses_norm(a)) {
+    if (gemv_fuses_norm(a, gains)) {
       a.norm_g = gains;
       a.eps = c.eps;
       ++n;
@@ -272,7 +272,7 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
       QD_TRY(q8prod(4 * l, fq, qa.W, x, attn_norm, qkv, kGemvStore));
       QD_TRY(launch_qkv_post(qkv, L.qkv_rows, batch, e, err, st, true));
       ++n;
-    } else if (gemv_fuses_norm(qa)) {
+    } else if (gemv_fuses_norm(qa, attn_norm)) {
       QD_TRY(normed(qa, attn_norm));
     } else {
       GemvArgs raw = qa;
@@ -315,7 +315,7 @@ qd_status enqueue_step(qd_model* m, int batch, cudaStream_t st) {
     QD_TRY(q8prod(4 * c.layers, c.emb_fmt, ha.W, x, out_norm, m->f(L.logits), kGemvStore));
     QD_TRY(launch_argmax(m->f(L.logits), c.vocab, batch, m->i(L.tok_out), pos, st));
     ++n;
-  } else if (gemv_fuses_norm(ha)) {
+  } else if (gemv_fuses_norm(ha, out_norm)) {
     QD_TRY(normed(ha, out_norm));
   } else {
     ha.mode = kGemvStore;
@@ -513,7 +513,7 @@ qd_status enqueue_prefill(qd_model* m, int seq, int t, unsigned flags, uint8_t* 
   ha.am.tok_out = m->i(L.tok_out) + seq;
   ha.am.pos = pos_seq;
   const float* out_norm = reinterpret_cast<const float*>(m->w + L.out_norm);
-  if (gemv_fuses_norm(ha)) {
+  if (gemv_fuses_norm(ha, out_norm)) {
     ha.norm_g = out_norm;
     ha.eps = c.eps;
     return launch_q_gemv(ha, st);

@@ -218,9 +218,9 @@ def test_q_gemv_non_finite_x_propagates(qd, fmt, batch):
 
 
 @pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "i8"])
-@pytest.mark.parametrize("batch", [3, 4, 6, 8])
+@pytest.mark.parametrize("batch", [3, 4, 6, 8, 9, 13, 16])
 def test_q_gemv_tensor_core_batches_full(qd, fmt, batch):
-    """Batch 3-8 on the tensor-core kernel: 16-row tiles with a ragged last tile (rows 1000
+    """Batch 3-16 on the tensor-core kernel: 16-row tiles with a ragged last tile (rows 1000
     = 62 tiles + 8), every output row, the 2e-5 bound of the integer planes."""
     rows, cols = 1000, 1536
     src, p = weights(qd, fmt, 12, f"tcb.{fmt}", rows, cols)
@@ -230,7 +230,7 @@ def test_q_gemv_tensor_core_batches_full(qd, fmt, batch):
 
 
 @pytest.mark.parametrize("fmt,cols", [("q4_0", 1600), ("q8_0", 1600), ("i8", 1504)])
-@pytest.mark.parametrize("batch", [3, 7])
+@pytest.mark.parametrize("batch", [3, 7, 11])
 def test_q_gemv_tensor_core_partial_stage(qd, fmt, cols, batch):
     """Rows whose last 256-column stage is partial (1600 = 6 stages + 2 units; INT8 1504 =
     5 stages + 7 units, an odd count): the stage loop's run-time tail and the x scale of a
@@ -243,7 +243,7 @@ def test_q_gemv_tensor_core_partial_stage(qd, fmt, cols, batch):
 
 
 @pytest.mark.parametrize("fmt,cols", [("q4_0", 11008), ("q8_0", 11008), ("i8", 11040)])
-@pytest.mark.parametrize("batch", [5, 8])
+@pytest.mark.parametrize("batch", [5, 8, 16])
 def test_q_gemv_tensor_core_column_ranges(qd, fmt, cols, batch):
     """x rows too wide for the shared memory beside the weight ring (11008 columns at batch
     5 or 8: over 220 KB of x) run as consecutive launches over column ranges, the first
