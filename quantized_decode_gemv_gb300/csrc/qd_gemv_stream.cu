@@ -452,7 +452,7 @@ __device__ __forceinline__ void compute_step(Acc<NB, RW>& acc, const uint8_t* sl
   }
 }
 
-template <int FMT, int NB, int RW>
+template <int FMT, int NB, int RW, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
   // dynamic shared memory: [warps][stages] ring slots, then the x records [NB][units]
   extern __shared__ __align__(128) uint8_t smem[];
@@ -465,13 +465,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
   // Split-K over a cluster of C CTAs: each takes the same row groups over its own
   // contiguous unit steps [j0, j1) (and builds only those units' x records); the partial
   // row sums meet in the first CTA, which adds them in CTA order and writes the rows.
-  const int C = p.ksplit;
+  // (a kernel that can split carries cluster instructions, which measured ~0.3 us slower to
+  // launch even at C = 1: the split is a separate instantiation)
+  const int C = SPLIT ? p.ksplit : 1;
   const int rank = C > 1 ? (int)(blockIdx.x % C) : 0;
   const int64_t ncl = gridDim.x / C, cid = blockIdx.x / C;
   const int steps_all = (units + 31) / 32;  // unit steps per row group
   const int j0 = rank * steps_all / C, j1 = (rank + 1) * steps_all / C;
   const int ua = 32 * j0, ub = min(32 * j1, units);  // this CTA's units
-  if (C > 1) cluster_arrive_relaxed();  // every CTA of the cluster has started (waited below)
+  if constexpr (SPLIT) cluster_arrive_relaxed();  // every CTA of the cluster has started (waited below)
   // Global warp ids interleave the clusters (warp-major), so the groups left over after
   // an even split land on warps spread over every SM rather than on the first ones.
   const int64_t gw = (int64_t)warp * ncl + cid, nw = ncl * kWarps;
@@ -614,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
       *dst = p.mode == kGemvAccumulate ? pf_.y_old + tot : tot;
     }
   };
-  if (C > 1) cluster_wait();  // the partial-sum slots of the first CTA exist from here on
+  if constexpr (SPLIT) cluster_wait();  // the partial-sum slots of the first CTA exist from here on
   int cs = 0;  // slot of the step being computed
   int j = j0;
   int kg = 0;  // this warp's finished groups
@@ -659,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
 #pragma unroll
     for (int b = 1; b < NB; ++b) iv = kb == b ? inv[b] : iv;
     const float tot = reduce_scatter<V>(v, lane) * iv;
-    if (C > 1) {
+    if constexpr (SPLIT) {
       // this CTA's part of the group, to slot [rank][warp][kg] of the first CTA
       if ((lane % GRP) == 0)
         st_cluster(part_s + 4u * (uint32_t)(((rank * kWarps + warp) * p.maxk + kg) * V + lane / GRP), 0, tot);
@@ -672,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_warp(const Params p) {
     g += nw;
     if (g < groups) pf = epi_prefetch<NB, RW>(p, g, lane);
   }
-  if (C > 1) {
+  if constexpr (SPLIT) {
     // every part has landed in the first CTA, which adds them in CTA order and writes
     cp_wait<0>();
     cluster_arrive();
@@ -800,17 +802,24 @@ size_t smem_bytes(int fmt, int64_t cols, int nb) {
 
 constexpr size_t kSmemCap = 200 * 1024;
 
+// The formats and batch widths that have a split-K instantiation (the split runs where it
+// measured faster: batch 1-2; the tensor-core kernel takes these formats at batch 3-16).
+template <int FMT, int NB>
+constexpr bool split_built() {
+  return NB <= 2 && (FMT == QD_Q4_0 || FMT == QD_Q8_0 || FMT == QD_I8_ROW || FMT == QD_Q4_K);
+}
+
 // Raise the kernel's dynamic shared-memory limit to kSmemCap once per device; the
 // occupancy query and the launch both depend on it.
-template <int FMT, int NB, int RW>
+template <int FMT, int NB, int RW, bool SPLIT = false>
 bool smem_attr_set() {
   static bool done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return false;
   if (!done[dev]) {
-    if (cudaFuncSetAttribute(k_gemv_warp<FMT, NB, RW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(k_gemv_warp<FMT, NB, RW, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemCap) != cudaSuccess)
       return false;
     done[dev] = true;
   }
@@ -819,7 +828,14 @@ bool smem_attr_set() {
 
 template <int FMT, int NB, int RW>
 qd_status launch_rw(const Params& p, bool pdl, cudaStream_t stream, int64_t ctas) {
-  auto kern = k_gemv_warp<FMT, NB, RW>;
+  auto kern = k_gemv_warp<FMT, NB, RW, false>;
+  if constexpr (split_built<FMT, NB>()) {
+    if (p.ksplit > 1) {
+      if (!smem_attr_set<FMT, NB, RW, true>()) return QD_ERR_CUDA;
+      kern = k_gemv_warp<FMT, NB, RW, true>;
+    }
+  }
+  if (p.ksplit > 1 && !split_built<FMT, NB>()) return QD_ERR_UNSUPPORTED;
   const size_t smem = smem_bytes_t<FMT, NB, RW>(p.W.cols, p.ksplit, p.maxk);
   if (smem > kSmemCap) return QD_ERR_UNSUPPORTED;
   if (!smem_attr_set<FMT, NB, RW>()) return QD_ERR_CUDA;
@@ -876,7 +892,7 @@ Geometry geometry_for(int64_t rows, int64_t cols, int ksplit) {
   gm.ksplit = ksplit;
   if (smem_bytes_t<FMT, NB, RW>(cols) > kSmemCap || !smem_attr_set<FMT, NB, RW>()) return gm;
   const int64_t groups = (rows + RW - 1) / RW;
-  int per_sm = resident_ctas(k_gemv_warp<FMT, NB, RW>, smem_bytes_t<FMT, NB, RW>(cols));
+  int per_sm = resident_ctas(k_gemv_warp<FMT, NB, RW, false>, smem_bytes_t<FMT, NB, RW>(cols));
   if (per_sm > kCtasPerSm) per_sm = kCtasPerSm;
   const int64_t cap_cl = (int64_t)sm_count() * per_sm / ksplit;
   int64_t cl = (groups + kWarps - 1) / kWarps;
@@ -948,7 +964,7 @@ qd_status launch_inst(Params p, bool pdl, cudaStream_t stream) {
   }
   if (bg.ctas <= 0) return QD_ERR_UNSUPPORTED;
   const int steps_all = (int)((cols / 32 + 31) / 32);
-  const int ks = choose_ksplit(p, FMT, NB);
+  const int ks = split_built<FMT, NB>() ? choose_ksplit(p, FMT, NB) : 1;
   if (ks > 1 && ks <= steps_all) {
     const Geometry g = geo(bg.rw, ks);
     if (g.ctas > 0) bg = g;
