@@ -457,7 +457,7 @@ qd_status qd_decode_step(qd_model* m, const int32_t* tokens, int batch, int32_t*
  *    that are multiples of 64 and t > 16, the layer products run on qd_q_gemm's tensor-core
  *    GEMM (Q4_0 / Q8_0 weights rounded to binary16, see qd_q_gemm); otherwise as below.
  *  - QD_PREFILL_EXACT: the layer products run on the batched GEMV (qd_q_gemv's arithmetic,
- *    as the decode step), 8 tokens a launch.
+ *    as the decode step), 16 tokens a launch.
  * The head always runs the decode step's GEMV.  tokens: host or device int32 [t]; ids
  * outside [0, vocab) embed zeros and set the device flag (qd_model_check), as do
  * positions past max_ctx.  out_token (int32) and logits_out: host or device.

@@ -369,7 +369,7 @@ struct PrefillLayout {
 };
 
 constexpr int kPrefillChunk = 16;  // tokens per flat-attention launch (binary16 cache)
-constexpr int kPrefillRows = 8;    // tokens per batched-GEMV launch (the tensor-core GEMV)
+constexpr int kPrefillRows = 16;   // tokens per batched-GEMV launch (the tensor-core GEMV's widest)
 
 PrefillLayout prefill_layout(const qd_config& c, int64_t qkv_rows, int t) {
   PrefillLayout P{};
@@ -405,7 +405,7 @@ PrefillLayout prefill_layout(const qd_config& c, int64_t qkv_rows, int t) {
 // the GEMM takes (Q4_0, Q8_0, INT8 rows).
 bool prefill_uses_gemm(const qd_config& c, int t, unsigned flags) {
   if (flags & QD_PREFILL_EXACT) return false;
-  if (t <= 2 * kPrefillRows) return false;  // two GEMV launches per product are as fast
+  if (t <= kPrefillRows) return false;  // one GEMV launch per product is as fast
   const int64_t QD = (int64_t)c.n_heads * c.head_dim;
   return c.dim % 64 == 0 && QD % 64 == 0 && c.ffn % 64 == 0;
 }
@@ -433,7 +433,7 @@ qd_status enqueue_prefill(qd_model* m, int seq, int t, unsigned flags, uint8_t* 
                       err, st));
   if (c.kv_f16) QD_TRY(zero_region(ws + P.attn_cnt, align_up(4 * (size_t)kPrefillChunk * c.n_kv_heads, 16), st));
 
-  // one product over the t rows of `in`: the GEMM, or batched GEMVs of up to 8 rows
+  // one product over the t rows of `in`: the GEMM, or batched GEMVs of up to 16 rows
   auto product = [&](int fmt, PackedView W, const float* in, float* y, GemvMode mode) -> qd_status {
     if (gemm && gemm_fmt(fmt)) {
       const int gm = mode == kGemvAccumulate ? kGemmAccumulate : mode == kGemvSwiGLU ? kGemmSwiGLU : kGemmStore;
