@@ -110,6 +110,19 @@ def test_mixed_format_model_teacher_forced(qd, mix, emb_fmt, batch):
     print(f"mixed {mix} emb {emb_fmt} batch {batch}: worst rel err {worst:.2e}, near-tie tokens {near}")
 
 
+@pytest.mark.parametrize("w_fmt,emb_fmt,batch", [("q4_0", "q8_0", 12), ("q8_0", "q4_0", 9)])
+def test_wide_model_batch_over_8_row_passes(qd, w_fmt, emb_fmt, batch):
+    """4096-wide activations at batch 9-16: 16 rows of x do not fit beside the weight ring,
+    so the tensor-core GEMV runs two passes of up to 8 batch rows, each with its own x, y,
+    positions, cache rows and argmax keys (the fused RMSNorm, the QKV epilogue, the
+    residual adds and the head's argmax over both passes)."""
+    cfg = dict(layers=1, dim=4096, ffn=512, n_heads=64, n_kv_heads=8, head_dim=64, vocab=300, rope_theta=1e4,
+               eps=1e-5, pairing="half", w_fmt=w_fmt, emb_fmt=emb_fmt)
+    prompt = qdsynth.tokens(30, "rowpass.prompt", batch * 3, cfg["vocab"]).reshape(batch, 3)
+    worst, near = run_teacher_forced(qd, cfg, 30, prompt, n_gen=3, batch=batch, max_ctx=8)
+    print(f"wide model {w_fmt} batch {batch}: worst rel err {worst:.2e}, near-tie tokens {near}")
+
+
 @pytest.mark.parametrize("w_fmt,batch", [("q4_0", 6), ("q8_0", 8)])
 def test_wide_ffn_model_column_ranges(qd, w_fmt, batch):
     """A 7B-wide FFN (11008) under a narrow model (dim 320, one stage and a partial one):
