@@ -27,10 +27,12 @@
 //    until the epilogue).  (GB300's int8 tensor path is ~4x slower than f16 here: 150
 //    against 590 TOPS measured for mma.sync.)
 //  * Weights stream as in the streaming kernel: every warp owns 16-row tiles taken round-
-//    robin over the grid's warps, and copies its stages (16 rows x 8 units of codes and
-//    scales, rows padded so that the fragment loads hit distinct banks) with per-lane
+//    robin over the grid's warps, and copies its stages (16 rows x 8 or 4 units of codes
+//    and scales, rows padded so that the fragment loads hit distinct banks) with per-lane
 //    cp.async into a ring in shared memory, no CTA barrier in the main loop; the ring's
-//    first stages are issued before the dependency wait.
+//    first stages are issued before the dependency wait.  A CTA has 16 warps with 4-unit
+//    stages where x leaves room for a ring three stages deep (more warps hide more of the
+//    fragment-building latency), otherwise 8 warps with 8-unit stages.
 //  * Rows of x wider than the shared memory holds (store and accumulate only) run as
 //    several launches over column ranges, the first storing and the rest accumulating:
 //    the sums still follow one fixed order.
@@ -42,11 +44,14 @@
 namespace qd {
 namespace mma_gemv {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
 constexpr int kTileRows = 16;
-constexpr int kStageUnits = 8;  // units (32 columns each) per ring stage and per x scale
-constexpr int kStageCols = kStageUnits * 32;
+constexpr int kXUnits = 8;  // units per x scale (one power of two per 256 columns and batch row)
+constexpr int kXCols = kXUnits * 32;
+// units (32 columns each) per ring stage of a CTA of W warps
+template <int W>
+__host__ __device__ constexpr int stage_units() {
+  return W == 16 ? 4 : 8;
+}
 constexpr int kXPad = 64;  // bytes after each staged x row: rows 2j, 2j + 1 on disjoint banks
 
 struct Params {
@@ -72,43 +77,43 @@ template <int FMT>
 constexpr int code_bytes() {
   return FMT == QD_Q4_0 ? 16 : 32;
 }
-// a ring slot: codes [16 rows][row stride] (8 units a row, padded by 16 bytes so that the
-// 8 rows a fragment load touches fall on different banks), then f16 scales [16][8]
-template <int FMT>
+// a ring slot: codes [16 rows][row stride] (SU units a row, padded by 16 bytes so that the
+// 8 rows a fragment load touches fall on different banks), then f16 scales [16][SU]
+template <int FMT, int SU>
 constexpr int row_stride() {
-  return kStageUnits * code_bytes<FMT>() + 16;
+  return SU * code_bytes<FMT>() + 16;
 }
-template <int FMT>
+template <int FMT, int SU>
 constexpr int scale_bytes() {
-  return FMT == QD_I8_ROW ? 0 : kTileRows * kStageUnits * 2;
+  return FMT == QD_I8_ROW ? 0 : kTileRows * SU * 2;
 }
-template <int FMT>
+template <int FMT, int SU>
 constexpr int slot_bytes() {
-  return kTileRows * row_stride<FMT>() + scale_bytes<FMT>();
+  return kTileRows * row_stride<FMT, SU>() + scale_bytes<FMT, SU>();
 }
 // batch columns: one or two blocks of 8 (the MMA's N); scale and norm arrays keep 16 a stage
 constexpr int kMaxCols = 16;
 __host__ __device__ constexpr int col_blocks(int batch) { return batch > 8 ? 2 : 1; }
 // per-warp partial accumulators for the column split, two tiles deep
-__host__ __device__ constexpr size_t partial_bytes(int nc) { return (size_t)2 * kWarps * 32 * 4 * nc * 4; }
+__host__ __device__ constexpr size_t partial_bytes(int nc, int warps) { return (size_t)2 * warps * 32 * 4 * nc * 4; }
 
 // Shared-memory layout of one launch (byte offsets; every part 16-byte aligned).
 struct Layout {
   size_t ring, xs, gs, sx, ssq, partial, bar, total;
   int64_t x_row;  // bytes between staged batch rows
 };
-template <int FMT>
+template <int FMT, int W>
 __host__ __device__ inline Layout layout(int units, int batch, bool norm, int stages) {
   Layout L;
-  const int nst = (units + kStageUnits - 1) / kStageUnits;
+  const int nxg = (units + kXUnits - 1) / kXUnits;
   L.x_row = (int64_t)units * 128 + kXPad;
   L.ring = 0;
-  L.xs = L.ring + (size_t)kWarps * stages * slot_bytes<FMT>();
+  L.xs = L.ring + (size_t)W * stages * slot_bytes<FMT, stage_units<W>()>();
   L.gs = L.xs + (size_t)batch * L.x_row;
   L.sx = L.gs + (norm ? (size_t)units * 128 : 0);
-  L.ssq = L.sx + (size_t)nst * kMaxCols * 4;
-  L.partial = L.ssq + (size_t)nst * kMaxCols * 4;
-  L.bar = L.partial + partial_bytes(col_blocks(batch));
+  L.ssq = L.sx + (size_t)nxg * kMaxCols * 4;
+  L.partial = L.ssq + (size_t)nxg * kMaxCols * 4;
+  L.bar = L.partial + partial_bytes(col_blocks(batch), W);
   L.total = L.bar + 16;
   return L;
 }
@@ -254,24 +259,27 @@ __device__ __forceinline__ void unit_mma(float (&d)[4], const uint32_t (&a0)[4],
   for (int i = 0; i < 4; ++i) d[i] += e[i];
 }
 
-// The f16 block scale of unit uu (0..7) from a row's 8 scales held as 4 words.
-__device__ __forceinline__ float scale_of(const uint4& s, int uu) {
-  const uint32_t w = (uu >> 1) == 0 ? s.x : (uu >> 1) == 1 ? s.y : (uu >> 1) == 2 ? s.z : s.w;
+// The f16 block scale of unit uu (0..2N-1) from a row's 2N scales held as N words.
+template <int N>
+__device__ __forceinline__ float scale_of(const uint32_t (&s)[N], int uu) {
+  uint32_t w = s[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i) w = (uu >> 1) == i ? s[i] : w;
   const float2 f = __half22float2(bits_h2(w));
   return (uu & 1) ? f.y : f.x;
 }
 
-// One ring stage of `NU` units (NU = 8, or 0: `nu` units known at run time) for NC blocks of
+// One ring stage of `NU` units (NU = SU, or 0: `nu` units known at run time) for NC blocks of
 // 8 batch columns (x of block c at xst[c]) into the stage accumulators as[c]: block-scaled
 // formats scale each unit's sums by the rows' block scales d; INT8 rows keep unit-
 // interleaved MMA chains and add them at the end.  Each unit's A fragments serve every
 // block.  Full stages run as groups of units: fragments first, then the MMAs round-robin
 // over the group's units, so independent accumulator chains are in flight.
-template <int FMT, int NU, int NC>
+template <int FMT, int SU, int NU, int NC>
 __device__ __forceinline__ void stage_mma(float (&as)[NC][4], const uint8_t* slot, const uint8_t* const (&xst)[NC],
                                           int g, int t, int nu) {
   constexpr int CB = code_bytes<FMT>();
-  constexpr int RS = row_stride<FMT>();
+  constexpr int RS = row_stride<FMT, SU>();
   constexpr int G = NC == 1 ? 4 : 2;  // units per group
   const uint8_t* row0 = slot + g * RS;
   const uint8_t* row8 = row0 + 8 * RS;
@@ -302,10 +310,20 @@ __device__ __forceinline__ void stage_mma(float (&as)[NC][4], const uint8_t* slo
 #pragma unroll
       for (int i = 0; i < 4; ++i) as[b][i] = c[b][0][i] + c[b][1][i];
   } else {
-    // the block scales of rows g and g + 8 for the stage's 8 units (f16, 16 bytes a row)
+    // the block scales of rows g and g + 8 for the stage's SU units (f16, 2 SU bytes a row)
     const uint8_t* scs = slot + kTileRows * RS;
-    const uint4 s0 = *reinterpret_cast<const uint4*>(scs + g * 16);
-    const uint4 s8 = *reinterpret_cast<const uint4*>(scs + (g + 8) * 16);
+    uint32_t s0[SU / 2], s8[SU / 2];
+    if constexpr (SU == 8) {
+      const uint4 a = *reinterpret_cast<const uint4*>(scs + g * 16);
+      const uint4 b = *reinterpret_cast<const uint4*>(scs + (g + 8) * 16);
+      s0[0] = a.x, s0[1] = a.y, s0[2] = a.z, s0[3] = a.w;
+      s8[0] = b.x, s8[1] = b.y, s8[2] = b.z, s8[3] = b.w;
+    } else {
+      const uint2 a = *reinterpret_cast<const uint2*>(scs + g * 8);
+      const uint2 b = *reinterpret_cast<const uint2*>(scs + (g + 8) * 8);
+      s0[0] = a.x, s0[1] = a.y;
+      s8[0] = b.x, s8[1] = b.y;
+    }
     if constexpr (NU > 0) {
 #pragma unroll
       for (int q = 0; q < NU / G; ++q) {
@@ -358,21 +376,21 @@ __device__ __forceinline__ void stage_mma(float (&as)[NC][4], const uint8_t* slo
   }
 }
 
-// x in place: warp w converts stages w, w + 8, ... for R batch rows at once (R = 4 or 8),
-// as straight-line code (rows past the batch convert zeros and store nothing), so the rows'
-// loads and dependency chains overlap.  Lane l holds elements 8l..8l+7 of the stage
-// (unit l / 4, K half (l % 4) / 2): two 16-byte halves, each the four elements of one
+// x in place: warp w converts the 256-column scale groups w, w + W, ... for R batch rows
+// at once (R = 4 or 8), as straight-line code (rows past the batch convert zeros and store
+// nothing), so the rows' loads and dependency chains overlap.  Lane l holds elements
+// 8l..8l+7 of the group (unit l / 4, K half (l % 4) / 2): two 16-byte halves, each the four elements of one
 // fragment thread (2 (l % 2) and 2 (l % 2) + 1), rewritten in place as that thread's
 // (hi b0, hi b1, lo b0, lo b1).  Lanes 4-7 of each quarter take their second half
 // first: the eight lanes of a 128-bit access then cover all 32 banks once.
-template <int R>
+template <int R, int W>
 __device__ __forceinline__ void convert_x(uint8_t* xs, int64_t x_row, const float* gs, float* sxs, float* ssq, int units,
-                                          int nst, int batch, bool norm, int warp, int lane) {
+                                          int nxg, int batch, bool norm, int warp, int lane) {
   const int h = (lane >> 2) & 1;
-  for (int s = warp; s < nst; s += kWarps) {
-    const int e0 = s * kStageCols + 8 * lane;
+  for (int s = warp; s < nxg; s += W) {
+    const int e0 = s * kXCols + 8 * lane;
     const bool in = e0 < units * 32;
-    uint8_t* sbase = xs + (int64_t)s * kStageCols * 4 + 32 * lane;
+    uint8_t* sbase = xs + (int64_t)s * kXCols * 4 + 32 * lane;
     float v[R][8];  // [row][half h's 4 elements, then the other half's]
 #pragma unroll
     for (int b = 0; b < R; ++b) {
@@ -411,7 +429,7 @@ __device__ __forceinline__ void convert_x(uint8_t* xs, int64_t x_row, const floa
     }
 #pragma unroll
     for (int b = 0; b < R; ++b) {
-      // the stage scale: 2^e with the largest |x| in [2^e, 2^(e+1)); magnitude bits
+      // the group's scale: 2^e with the largest |x| in [2^e, 2^(e+1)); magnitude bits
       // order like the values, and inf / NaN sit above every finite one
       uint32_t mb = 0;
 #pragma unroll
@@ -446,32 +464,34 @@ __device__ __forceinline__ void convert_x(uint8_t* xs, int64_t x_row, const floa
   }
 }
 
-template <int FMT, int NC>
-__global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
+template <int FMT, int NC, int W>
+__global__ void __launch_bounds__(W * 32, 1) k_gemv_mma(const Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int CB = code_bytes<FMT>();
-  constexpr int RS = row_stride<FMT>();
-  constexpr int kSlot = slot_bytes<FMT>();
+  constexpr int SU = stage_units<W>();  // units per ring stage
+  constexpr int RS = row_stride<FMT, SU>();
+  constexpr int kSlot = slot_bytes<FMT, SU>();
   const int kStages = p.stages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;  // mma fragment: row group, thread in group
-  const PackedView& W = p.W;
+  const PackedView& Wm = p.W;
   const int units = p.units;
-  const int nst = (units + kStageUnits - 1) / kStageUnits;  // stages per tile
+  const int nst = (units + SU - 1) / SU;                     // stages per tile
+  const int nxg = (units + kXUnits - 1) / kXUnits;           // x scale groups
   const bool norm = p.norm_g != nullptr;
-  const Layout L = layout<FMT>(units, p.batch, norm, kStages);
-  const int64_t tiles = (W.rows + kTileRows - 1) / kTileRows;
+  const Layout L = layout<FMT, W>(units, p.batch, norm, kStages);
+  const int64_t tiles = (Wm.rows + kTileRows - 1) / kTileRows;
   // the KS warps of a group share each of the group's tiles; warp ks of the group takes
   // the tile's stages [st0, st1); groups take tiles round-robin over the grid
   const int KS = p.ks, grp = warp / KS, ks = warp % KS;
   const int st0 = ks * nst / KS, st1 = (ks + 1) * nst / KS;
-  const int64_t gslot = (int64_t)grp * gridDim.x + blockIdx.x, ngs = (int64_t)gridDim.x * (kWarps / KS);
+  const int64_t gslot = (int64_t)grp * gridDim.x + blockIdx.x, ngs = (int64_t)gridDim.x * (W / KS);
   uint8_t* ring = smem + L.ring + (size_t)warp * kStages * kSlot;
   const uint32_t ring_s = tc::smem_u32(ring);
   uint8_t* xs = smem + L.xs;
   const float* gs = reinterpret_cast<const float*>(smem + L.gs);
-  float* sxs = reinterpret_cast<float*>(smem + L.sx);   // [stage][8] x scales
-  float* ssq = reinterpret_cast<float*>(smem + L.ssq);  // [stage][8] sums of squares
+  float* sxs = reinterpret_cast<float*>(smem + L.sx);   // [x group][16] x scales
+  float* ssq = reinterpret_cast<float*>(smem + L.ssq);  // [x group][16] sums of squares
   float* partial = reinterpret_cast<float*>(smem + L.partial);  // [2][warps][32][4]
   const uint32_t bar = tc::smem_u32(smem + L.bar);
 
@@ -481,30 +501,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
   }
   __syncthreads();
 
-  // ---- ring: stage s of a tile = units [8s, 8s + 8) of its 16 rows.  Lane l copies the
-  // 16-byte code chunk l % kPerRow of rows l / kPerRow + i * kRowsPerPass and the 4-byte
-  // scale word (unit pair l % 4) of rows l / 4 and l / 4 + 8; the source rows of a tile are
-  // set up once per tile (clamped to the last row for a ragged tile)
-  constexpr int kPerRow = kStageUnits * CB / 16;  // 16-byte chunks per row and stage
+  // ---- ring: stage s of a tile = units [SU s, SU s + SU) of its 16 rows.  Lane l copies
+  // the 16-byte code chunk l % kPerRow of rows l / kPerRow + i * kRowsPerPass and the
+  // 4-byte scale words l + 32 j (unit pair l % (SU / 2) of rows l / (SU / 2) + j 64 / SU);
+  // the source rows of a tile are set up once per tile (clamped to the last row for a
+  // ragged tile)
+  constexpr int kPerRow = SU * CB / 16;  // 16-byte chunks per row and stage
   constexpr int kRowsPerPass = 32 / kPerRow;
   constexpr int kChunks = kTileRows / kRowsPerPass;  // code chunks per lane and stage
   const int crow = lane / kPerRow, crem = lane % kPerRow, cunit = crem / (CB / 16);
-  const int srow = lane >> 2, spr = lane & 3;
+  constexpr int kScaleWords = SU / 4;  // scale words per lane and stage
+  const int srow = lane / (SU / 2), spr = lane % (SU / 2);
   int64_t lt = gslot;  // tile of the next copy
   int ls = st0;        // its stage
   const uint8_t* cptr[kChunks];
-  const uint8_t* sptr[2];
+  const uint8_t* sptr[kScaleWords];
   auto tile_ptrs = [&]() {
 #pragma unroll
     for (int i = 0; i < kChunks; ++i) {
-      const int64_t r = min(lt * kTileRows + crow + i * kRowsPerPass, W.rows - 1);
-      cptr[i] = W.codes + r * W.row_code_bytes + (int64_t)p.u0 * CB + 16 * crem;
+      const int64_t r = min(lt * kTileRows + crow + i * kRowsPerPass, Wm.rows - 1);
+      cptr[i] = Wm.codes + r * Wm.row_code_bytes + (int64_t)p.u0 * CB + 16 * crem;
     }
-    if constexpr (scale_bytes<FMT>() > 0) {
+    if constexpr (scale_bytes<FMT, SU>() > 0) {
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int64_t r = min(lt * kTileRows + srow + 8 * j, W.rows - 1);
-        sptr[j] = W.scales + r * W.row_scale_bytes + (int64_t)(p.u0 + 2 * spr) * 2;
+      for (int j = 0; j < kScaleWords; ++j) {
+        const int64_t r = min(lt * kTileRows + srow + j * (64 / SU), Wm.rows - 1);
+        sptr[j] = Wm.scales + r * Wm.row_scale_bytes + (int64_t)(p.u0 + 2 * spr) * 2;
       }
     }
   };
@@ -512,18 +534,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
   auto issue = [&](int slot_idx) {
     if (lt < tiles && st1 > st0) {
       const uint32_t slot = ring_s + (uint32_t)slot_idx * kSlot;
-      const int u0 = ls * kStageUnits;
+      const int u0 = ls * SU;
       if (u0 + cunit < units) {
 #pragma unroll
         for (int i = 0; i < kChunks; ++i)
           cp16(slot + (uint32_t)((crow + i * kRowsPerPass) * RS + 16 * crem), cptr[i] + (int64_t)u0 * CB);
       }
-      if constexpr (scale_bytes<FMT>() > 0) {
+      if constexpr (scale_bytes<FMT, SU>() > 0) {
         // units come in pairs (even unit counts)
         if (u0 + 2 * spr < units) {
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
-            cp4(slot + (uint32_t)(kTileRows * RS + ((srow + 8 * j) * kStageUnits + 2 * spr) * 2), sptr[j] + u0 * 2);
+          for (int j = 0; j < kScaleWords; ++j)
+            cp4(slot + (uint32_t)(kTileRows * RS + ((srow + j * (64 / SU)) * SU + 2 * spr) * 2), sptr[j] + u0 * 2);
         }
       }
       if (++ls == st1) {
@@ -549,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
     for (int b = 0; b < p.batch; ++b)
       tc::bulk_copy_g2s(tc::smem_u32(xs + b * L.x_row), p.x + b * p.x_stride + (int64_t)p.u0 * 32, row_bytes, bar);
   }
-  for (int i = threadIdx.x; i < nst * kMaxCols; i += kThreads) {
+  for (int i = threadIdx.x; i < nxg * kMaxCols; i += W * 32) {
     if ((i % kMaxCols) >= p.batch) sxs[i] = ssq[i] = 0.f;  // columns without a batch row
   }
   if (!__syncthreads_and(tc::mbar_wait_sleep(bar, 0))) {
@@ -562,14 +584,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
   }
 
   // x in place, 8 batch rows a pass (rows 8-15 with their scale and norm columns offset)
-  if (p.batch <= 4) convert_x<4>(xs, L.x_row, gs, sxs, ssq, units, nst, p.batch, norm, warp, lane);
-  else convert_x<8>(xs, L.x_row, gs, sxs, ssq, units, nst, min(p.batch, 8), norm, warp, lane);
+  if (p.batch <= 4) convert_x<4, W>(xs, L.x_row, gs, sxs, ssq, units, nxg, p.batch, norm, warp, lane);
+  else convert_x<8, W>(xs, L.x_row, gs, sxs, ssq, units, nxg, min(p.batch, 8), norm, warp, lane);
   if constexpr (NC > 1) {
     if (p.batch > 8)
-      convert_x<8>(xs + 8 * L.x_row, L.x_row, gs, sxs + 8, ssq + 8, units, nst, p.batch - 8, norm, warp, lane);
+      convert_x<8, W>(xs + 8 * L.x_row, L.x_row, gs, sxs + 8, ssq + 8, units, nxg, p.batch - 8, norm, warp, lane);
   }
   __syncthreads();
-  // RMSNorm factors of this lane's columns 8c + 2t, 8c + 2t + 1 (stage sums in stage order:
+  // RMSNorm factors of this lane's columns 8c + 2t, 8c + 2t + 1 (group sums in group order:
   // every CTA forms the same value)
   float inv[NC][2];
 #pragma unroll
@@ -579,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
       inv[c][j] = 1.f;
       if (norm) {
         float tt = 0.f;
-        for (int s = 0; s < nst; ++s) tt += ssq[s * kMaxCols + 8 * c + 2 * t + j];
+        for (int s = 0; s < nxg; ++s) tt += ssq[s * kMaxCols + 8 * c + 2 * t + j];
         inv[c][j] = 1.0f / sqrtf(tt / (float)(units * 32) + p.eps);
       }
     }
@@ -606,17 +628,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
       const uint8_t* slot = ring + (size_t)cs * kSlot;
       const uint8_t* xst[NC];
 #pragma unroll
-      for (int c = 0; c < NC; ++c) xst[c] = xrow[c] + (size_t)st * kStageCols * 4;
-      const int nu = min(kStageUnits, units - st * kStageUnits);
+      for (int c = 0; c < NC; ++c) xst[c] = xrow[c] + (size_t)st * SU * 128;
+      const int nu = min(SU, units - st * SU);
       float as[NC][4];
 #pragma unroll
       for (int c = 0; c < NC; ++c) as[c][0] = as[c][1] = as[c][2] = as[c][3] = 0.f;
-      if (nu == kStageUnits) stage_mma<FMT, kStageUnits, NC>(as, slot, xst, g, t, nu);
-      else stage_mma<FMT, 0, NC>(as, slot, xst, g, t, nu);
+      if (nu == SU) stage_mma<FMT, SU, SU, NC>(as, slot, xst, g, t, nu);
+      else stage_mma<FMT, SU, 0, NC>(as, slot, xst, g, t, nu);
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        // the stage's x scales of columns 8c + 2t, 8c + 2t + 1
-        const float2 sx = *reinterpret_cast<const float2*>(sxs + st * kMaxCols + 8 * c + 2 * t);
+        // the x scales of columns 8c + 2t, 8c + 2t + 1 in the stage's scale group
+        const float2 sx = *reinterpret_cast<const float2*>(sxs + (st / (kXUnits / SU)) * kMaxCols + 8 * c + 2 * t);
         acc[c][0] = fmaf(sx.x, as[c][0], acc[c][0]);
         acc[c][1] = fmaf(sx.y, as[c][1], acc[c][1]);
         acc[c][2] = fmaf(sx.x, as[c][2], acc[c][2]);
@@ -626,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
     }
     if (KS > 1) {
       // the group's column parts, summed in part order by its first warp
-      float* pt = partial + (size_t)(it & 1) * kWarps * 32 * 4 * NC;
+      float* pt = partial + (size_t)(it & 1) * W * 32 * 4 * NC;
 #pragma unroll
       for (int c = 0; c < NC; ++c)
         *reinterpret_cast<float4*>(pt + ((warp * 32 + lane) * NC + c) * 4) =
@@ -652,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
     if constexpr (FMT == QD_I8_ROW) {
 #pragma unroll
       for (int h = 0; h < 2; ++h)
-        rsc[h] = __ldg(reinterpret_cast<const float*>(W.scales + min(rbase + g + 8 * h, W.rows - 1) * W.row_scale_bytes));
+        rsc[h] = __ldg(reinterpret_cast<const float*>(Wm.scales + min(rbase + g + 8 * h, Wm.rows - 1) * Wm.row_scale_bytes));
     }
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
@@ -667,14 +689,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_mma(const Params p) {
       for (int i = 0; i < 4; ++i) {
         const int64_t r = rbase + g + (i >= 2 ? 8 : 0);
         const int b = 8 * c + 2 * t + (i & 1);
-        if (b >= p.batch || r >= W.rows) continue;
+        if (b >= p.batch || r >= Wm.rows) continue;
         if (p.mode == kGemvSwiGLU) {
-          if ((g & 1) == 0 && r + 1 < W.rows)
-            p.y[(int64_t)b * (W.rows / 2) + r / 2] = v[i] / (1.0f + expf(-v[i])) * nx[i];
+          if ((g & 1) == 0 && r + 1 < Wm.rows)
+            p.y[(int64_t)b * (Wm.rows / 2) + r / 2] = v[i] / (1.0f + expf(-v[i])) * nx[i];
         } else if (p.mode == kGemvQKV) {
-          if ((g & 1) == 0 && r + 1 < W.rows) qkv_pair(p, r, b, v[i], nx[i]);
+          if ((g & 1) == 0 && r + 1 < Wm.rows) qkv_pair(p, r, b, v[i], nx[i]);
         } else {
-          float* dst = p.y + (int64_t)b * W.rows + r;
+          float* dst = p.y + (int64_t)b * Wm.rows + r;
           if (p.mode == kGemvAccumulate || p.accumulate) *dst = __ldcg(dst) + v[i];
           else *dst = v[i];
           if (p.mode == kGemvArgmax) {
@@ -731,13 +753,13 @@ int sm_count() {
   return v;
 }
 
-template <int FMT, int NC>
+template <int FMT, int NC, int W>
 bool smem_attr_set() {
   static bool done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (!done[dev]) {
-    if (cudaFuncSetAttribute(k_gemv_mma<FMT, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) !=
+    if (cudaFuncSetAttribute(k_gemv_mma<FMT, NC, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) !=
         cudaSuccess) {
       cudaGetLastError();
       return false;
@@ -749,44 +771,57 @@ bool smem_attr_set() {
 
 bool fmt_taken(int fmt) { return fmt == QD_Q4_0 || fmt == QD_Q8_0 || fmt == QD_I8_ROW; }
 
-size_t smem_for(int fmt, int units, int batch, bool norm, int stages) {
+template <int W>
+size_t smem_for_w(int fmt, int units, int batch, bool norm, int stages) {
   switch (fmt) {
-    case QD_Q4_0: return layout<QD_Q4_0>(units, batch, norm, stages).total;
-    case QD_Q8_0: return layout<QD_Q8_0>(units, batch, norm, stages).total;
-    default: return layout<QD_I8_ROW>(units, batch, norm, stages).total;
+    case QD_Q4_0: return layout<QD_Q4_0, W>(units, batch, norm, stages).total;
+    case QD_Q8_0: return layout<QD_Q8_0, W>(units, batch, norm, stages).total;
+    default: return layout<QD_I8_ROW, W>(units, batch, norm, stages).total;
   }
+}
+size_t smem_for(int fmt, int warps, int units, int batch, bool norm, int stages) {
+  return warps == 16 ? smem_for_w<16>(fmt, units, batch, norm, stages) : smem_for_w<8>(fmt, units, batch, norm, stages);
 }
 
 // Ring depth: the deepest (up to 8 slots a warp) that fits the shared memory; 0: none does.
-int stages_for(int fmt, int units, int batch, bool norm) {
+int stages_for(int fmt, int warps, int units, int batch, bool norm) {
   for (int s = 8; s >= 2; --s)
-    if (smem_for(fmt, units, batch, norm, s) <= kSmemCap) return s;
+    if (smem_for(fmt, warps, units, batch, norm, s) <= kSmemCap) return s;
   return 0;
 }
 
-// Ring stages a column range is sized for: about 64 KB of weights in flight per SM.
+// Warps per CTA for a launch over `units` columns: 16 (4-unit stages) where their ring
+// can be three stages deep, otherwise 8 (8-unit stages).
+int warps_for(int fmt, int units, int batch, bool norm) {
+  return stages_for(fmt, 16, units, batch, norm) >= 3 ? 16 : 8;
+}
+
+// Ring stages a column range is sized for: about 64 KB of weights in flight per SM (8 warps).
 int ring_floor(int fmt) {
-  const int slot = fmt == QD_Q4_0 ? slot_bytes<QD_Q4_0>() : fmt == QD_Q8_0 ? slot_bytes<QD_Q8_0>() : slot_bytes<QD_I8_ROW>();
-  return max(2, (65536 + kWarps * slot - 1) / (kWarps * slot));
+  const int slot = fmt == QD_Q4_0 ? slot_bytes<QD_Q4_0, 8>() : fmt == QD_Q8_0 ? slot_bytes<QD_Q8_0, 8>() : slot_bytes<QD_I8_ROW, 8>();
+  return max(2, (65536 + 8 * slot - 1) / (8 * slot));
 }
 
 // Units per column range: all of them when x fits beside a ring of two stages or more;
-// otherwise the widest multiple of a stage that leaves room for ring_floor stages.
+// otherwise the widest multiple of an x scale group that leaves room for ring_floor stages
+// of the 8-warp CTA.
 int range_units(int fmt, int units, int batch, bool norm) {
-  if (stages_for(fmt, units, batch, norm) >= 2) return units;
+  if (stages_for(fmt, 8, units, batch, norm) >= 2) return units;
   const int floor_st = ring_floor(fmt);
-  int ru = (units / kStageUnits) * kStageUnits;
-  while (ru > kStageUnits && smem_for(fmt, ru, batch, norm, floor_st) > kSmemCap) ru -= kStageUnits;
-  return smem_for(fmt, ru, batch, norm, floor_st) <= kSmemCap ? ru : 0;
+  int ru = (units / kXUnits) * kXUnits;
+  while (ru > kXUnits && smem_for(fmt, 8, ru, batch, norm, floor_st) > kSmemCap) ru -= kXUnits;
+  return smem_for(fmt, 8, ru, batch, norm, floor_st) <= kSmemCap ? ru : 0;
 }
 
-// Warps per tile (1, 2 or 4): the fewest rounds of stages on the busiest warp, counting the
-// CTAs the grid can hold (a small extra cost per split for the partial sums).
-int ks_for(int64_t tiles, int nst, int sms) {
+// Warps per tile (1, 2, 4, or 8 in a 16-warp CTA): the fewest rounds of stages on the
+// busiest warp, counting the CTAs the grid can hold (a small extra cost per split for the
+// partial sums).
+int ks_for(int64_t tiles, int nst, int sms, int warps) {
   int best = 1;
   double best_cost = 1e30;
-  for (int ks : {1, 2, 4}) {
-    const int64_t groups_per_cta = kWarps / ks;
+  for (int ks : {1, 2, 4, 8}) {
+    if (ks == 8 && warps < 16) break;
+    const int64_t groups_per_cta = warps / ks;
     int64_t ctas = (tiles + groups_per_cta - 1) / groups_per_cta;
     if (ctas > sms) ctas = sms;
     const int64_t rounds = (tiles + ctas * groups_per_cta - 1) / (ctas * groups_per_cta);
@@ -799,23 +834,24 @@ int ks_for(int64_t tiles, int nst, int sms) {
   return best;
 }
 
-// One launch over the column range [p.u0, p.u0 + p.units).
-template <int FMT>
+// One launch over the column range [p.u0, p.u0 + p.units) with CTAs of W warps.
+template <int FMT, int W>
 qd_status launch_range(Params p, bool pdl, cudaStream_t stream) {
+  if (!(col_blocks(p.batch) == 2 ? smem_attr_set<FMT, 2, W>() : smem_attr_set<FMT, 1, W>())) return QD_ERR_CUDA;
   const int64_t tiles = (p.W.rows + kTileRows - 1) / kTileRows;
-  const int nst = (p.units + kStageUnits - 1) / kStageUnits;
+  const int nst = (p.units + stage_units<W>() - 1) / stage_units<W>();
   const int sms = sm_count();
   const bool norm = p.norm_g != nullptr;
-  p.stages = stages_for(FMT, p.units, p.batch, norm);
+  p.stages = stages_for(FMT, W, p.units, p.batch, norm);
   if (p.stages < 2) return QD_ERR_UNSUPPORTED;
-  p.ks = ks_for(tiles, nst, sms);
-  const int64_t groups_per_cta = kWarps / p.ks;
+  p.ks = ks_for(tiles, nst, sms, W);
+  const int64_t groups_per_cta = W / p.ks;
   int64_t ctas = (tiles + groups_per_cta - 1) / groups_per_cta;
   if (ctas > sms) ctas = sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = layout<FMT>(p.units, p.batch, norm, p.stages).total;
+  cfg.blockDim = dim3(W * 32);
+  cfg.dynamicSmemBytes = layout<FMT, W>(p.units, p.batch, norm, p.stages).total;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -823,23 +859,25 @@ qd_status launch_range(Params p, bool pdl, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   if (col_blocks(p.batch) == 2)
-    return cudaLaunchKernelEx(&cfg, k_gemv_mma<FMT, 2>, p) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
-  return cudaLaunchKernelEx(&cfg, k_gemv_mma<FMT, 1>, p) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, k_gemv_mma<FMT, 2, W>, p) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, k_gemv_mma<FMT, 1, W>, p) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
 }
 
-// All column ranges in order: the first stores (or accumulates, in accumulate mode), the
-// rest accumulate, each a programmatic dependent of the one before.
+// One launch with 16-warp CTAs where their ring fits three stages deep; otherwise 8-warp
+// CTAs over all column ranges in order: the first stores (or accumulates, in accumulate
+// mode), the rest accumulate, each a programmatic dependent of the one before.
 template <int FMT>
 qd_status launch(Params p, bool pdl, cudaStream_t stream) {
-  if (!(col_blocks(p.batch) == 2 ? smem_attr_set<FMT, 2>() : smem_attr_set<FMT, 1>())) return QD_ERR_CUDA;
   const int units = (int)(p.W.cols / 32);
-  const int ru = range_units(FMT, units, p.batch, p.norm_g != nullptr);
+  const bool norm = p.norm_g != nullptr;
+  if (warps_for(FMT, units, p.batch, norm) == 16) return launch_range<FMT, 16>(p, pdl, stream);
+  const int ru = range_units(FMT, units, p.batch, norm);
   if (ru <= 0) return QD_ERR_UNSUPPORTED;
   for (int u0 = 0; u0 < units; u0 += ru) {
     p.u0 = u0;
     p.units = min(ru, units - u0);
     p.accumulate = u0 > 0;
-    const qd_status st = launch_range<FMT>(p, u0 > 0 || pdl, stream);
+    const qd_status st = launch_range<FMT, 8>(p, u0 > 0 || pdl, stream);
     if (st != QD_OK) return st;
   }
   return QD_OK;
@@ -854,7 +892,7 @@ namespace mma_gemv {
 // fused norm) column ranges that fit.
 bool one_pass_fits(const GemvArgs& a) {
   const int units = (int)(a.W.cols / 32);
-  if (stages_for(a.fmt, units, a.batch, a.norm_g != nullptr) >= 2) return true;
+  if (stages_for(a.fmt, 8, units, a.batch, a.norm_g != nullptr) >= 2) return true;
   const bool splits = (a.mode == kGemvStore || a.mode == kGemvAccumulate) && !a.norm_g;
   return splits && range_units(a.fmt, units, a.batch, false) > 0;
 }
@@ -928,7 +966,7 @@ bool gemv_mma_supported(const GemvArgs& a) {
     if (a.W.rows & 1) return false;
   }
   if (a.batch <= 8) return one_pass_fits(a);
-  const int units_ok = stages_for(a.fmt, units, a.batch, a.norm_g != nullptr) >= 2;
+  const int units_ok = stages_for(a.fmt, 8, units, a.batch, a.norm_g != nullptr) >= 2;
   if (units_ok) return true;
   if (a.fmt == QD_I8_ROW) return false;
   return one_pass_fits(row_slice(a, 0, 8)) && one_pass_fits(row_slice(a, 8, a.batch - 8));
@@ -938,7 +976,7 @@ qd_status launch_q_gemv_mma(const GemvArgs& a, cudaStream_t stream) {
   using namespace mma_gemv;
   if (!gemv_mma_supported(a)) return QD_ERR_UNSUPPORTED;
   const int units = (int)(a.W.cols / 32);
-  if (a.batch <= 8 || stages_for(a.fmt, units, a.batch, a.norm_g != nullptr) >= 2) return launch_args(a, stream);
+  if (a.batch <= 8 || stages_for(a.fmt, 8, units, a.batch, a.norm_g != nullptr) >= 2) return launch_args(a, stream);
   // two passes of up to 8 batch rows, the second a programmatic dependent of the first
   const qd_status st = launch_args(row_slice(a, 0, 8), stream);
   if (st != QD_OK) return st;
