@@ -33,9 +33,14 @@
 //    first stages are issued before the dependency wait.  A CTA has 16 warps with 4-unit
 //    stages where x leaves room for a ring three stages deep (more warps hide more of the
 //    fragment-building latency), otherwise 8 warps with 8-unit stages.
-//  * Rows of x wider than the shared memory holds (store and accumulate only) run as
-//    several launches over column ranges, the first storing and the rest accumulating:
-//    the sums still follow one fixed order.
+//  * Rows of x wider than the shared memory holds (store and accumulate only) split over
+//    a thread-block cluster of 2 or 4 CTAs where every warp group of the grid then takes
+//    one tile: each CTA stages, converts and multiplies only its share of the columns,
+//    the others store their tile sums into the first CTA's shared memory (distributed
+//    shared memory), and after one cluster barrier the first CTA adds them in CTA order
+//    and runs the epilogue.  Otherwise they run as several launches over column ranges,
+//    the first storing and the rest accumulating.  Either way the sums follow one fixed
+//    order.
 //  * Epilogues: store, accumulate, SwiGLU over interleaved (gate, up) rows, the QKV
 //    epilogue (RoPE pairs, cache append) and the fused argmax, as the streaming kernel.
 #include "qd_intdot.cuh"
@@ -70,6 +75,7 @@ struct Params {
   int units;         // units in the range
   int stages;        // ring depth (slots per warp), sized to the shared memory left
   int ks;            // warps that share one tile, each over a contiguous part of its columns
+  int ksplit;        // CTAs per cluster splitting the columns (split launches; 1 otherwise)
   bool accumulate;   // a later column range: y += partial product (store mode's chunks)
 };
 
@@ -99,11 +105,11 @@ __host__ __device__ constexpr size_t partial_bytes(int nc, int warps) { return (
 
 // Shared-memory layout of one launch (byte offsets; every part 16-byte aligned).
 struct Layout {
-  size_t ring, xs, gs, sx, ssq, partial, bar, total;
+  size_t ring, xs, gs, sx, ssq, partial, bar, spl, total;
   int64_t x_row;  // bytes between staged batch rows
 };
 template <int FMT, int W>
-__host__ __device__ inline Layout layout(int units, int batch, bool norm, int stages) {
+__host__ __device__ inline Layout layout(int units, int batch, bool norm, int stages, size_t split_bytes = 0) {
   Layout L;
   const int nxg = (units + kXUnits - 1) / kXUnits;
   L.x_row = (int64_t)units * 128 + kXPad;
@@ -114,8 +120,22 @@ __host__ __device__ inline Layout layout(int units, int batch, bool norm, int st
   L.ssq = L.sx + (size_t)nxg * kMaxCols * 4;
   L.partial = L.ssq + (size_t)nxg * kMaxCols * 4;
   L.bar = L.partial + partial_bytes(col_blocks(batch), W);
-  L.total = L.bar + 16;
+  L.spl = L.bar + 16;
+  L.total = L.spl + split_bytes;
   return L;
+}
+
+// Split launches: a cluster of C CTAs shares each tile, CTA r over the 256-column x groups
+// [r G / C, (r + 1) G / C) of the G in the range, so each stages and converts only its
+// share of x.  The widest share in units (the shared-memory layout is sized for it):
+__host__ __device__ inline int split_units_cap(int units, int c) {
+  const int nxg = (units + kXUnits - 1) / kXUnits;
+  const int cap = (nxg + c - 1) / c * kXUnits;
+  return cap < units ? cap : units;
+}
+// the first CTA's slots for the other CTAs' tile sums: [C - 1][groups][32 lanes][NC][4]
+__host__ __device__ constexpr size_t split_slot_bytes(int c, int groups, int nc) {
+  return (size_t)(c - 1) * groups * 32 * nc * 16;
 }
 
 template <int N>
@@ -142,6 +162,18 @@ __device__ __forceinline__ void cp4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Thread-block clusters: store four floats at this CTA's shared address `addr` as mapped
+// into CTA `rank` of the cluster, and the cluster-wide barrier's arrive / wait.
+__device__ __forceinline__ void st_cluster4(uint32_t addr, int rank, float a, float b, float c, float d) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // D = A (16x16, row) * B (16x8, col) + D over binary16 into f32.
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -464,7 +496,7 @@ __device__ __forceinline__ void convert_x(uint8_t* xs, int64_t x_row, const floa
   }
 }
 
-template <int FMT, int NC, int W>
+template <int FMT, int NC, int W, bool SPLIT>
 __global__ void __launch_bounds__(W * 32, 1) k_gemv_mma(const Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int CB = code_bytes<FMT>();
@@ -475,17 +507,30 @@ __global__ void __launch_bounds__(W * 32, 1) k_gemv_mma(const Params p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;  // mma fragment: row group, thread in group
   const PackedView& Wm = p.W;
-  const int units = p.units;
+  // split launches: CTA `rank` of each cluster of C takes its share [ua, ub) of the range's
+  // units (whole x groups); the clusters take tiles as CTAs do otherwise
+  const int C = SPLIT ? p.ksplit : 1;
+  const int rank = SPLIT ? (int)(blockIdx.x % C) : 0;
+  const int64_t ncl = gridDim.x / C, cid = blockIdx.x / C;
+  const int nxg_all = (p.units + kXUnits - 1) / kXUnits;
+  const int ua = SPLIT ? rank * nxg_all / C * kXUnits : 0;
+  const int ub = SPLIT ? min((rank + 1) * nxg_all / C * kXUnits, p.units) : p.units;
+  const int units = ub - ua;             // this CTA's units
+  const int64_t uoff = (int64_t)p.u0 + ua;  // the first of them in a row
+  if constexpr (SPLIT) cluster_arrive_relaxed();  // every CTA of the cluster has started (waited below)
   const int nst = (units + SU - 1) / SU;                     // stages per tile
   const int nxg = (units + kXUnits - 1) / kXUnits;           // x scale groups
   const bool norm = p.norm_g != nullptr;
-  const Layout L = layout<FMT, W>(units, p.batch, norm, kStages);
+  const int KS = p.ks, grp = warp / KS, ks = warp % KS;
+  const Layout L = layout<FMT, W>(SPLIT ? split_units_cap(p.units, C) : units, p.batch, norm, kStages,
+                                  SPLIT ? split_slot_bytes(C, W / KS, NC) : 0);
   const int64_t tiles = (Wm.rows + kTileRows - 1) / kTileRows;
   // the KS warps of a group share each of the group's tiles; warp ks of the group takes
-  // the tile's stages [st0, st1); groups take tiles round-robin over the grid
-  const int KS = p.ks, grp = warp / KS, ks = warp % KS;
+  // the tile's stages [st0, st1); groups take tiles round-robin over the grid (a split
+  // launch gives every group one tile at most)
   const int st0 = ks * nst / KS, st1 = (ks + 1) * nst / KS;
-  const int64_t gslot = (int64_t)grp * gridDim.x + blockIdx.x, ngs = (int64_t)gridDim.x * (W / KS);
+  const int64_t gslot = (int64_t)grp * ncl + cid, ngs = ncl * (W / KS);
+  const int64_t tiles_end = SPLIT ? min(tiles, gslot + 1) : tiles;
   uint8_t* ring = smem + L.ring + (size_t)warp * kStages * kSlot;
   const uint32_t ring_s = tc::smem_u32(ring);
   uint8_t* xs = smem + L.xs;
@@ -520,19 +565,19 @@ __global__ void __launch_bounds__(W * 32, 1) k_gemv_mma(const Params p) {
 #pragma unroll
     for (int i = 0; i < kChunks; ++i) {
       const int64_t r = min(lt * kTileRows + crow + i * kRowsPerPass, Wm.rows - 1);
-      cptr[i] = Wm.codes + r * Wm.row_code_bytes + (int64_t)p.u0 * CB + 16 * crem;
+      cptr[i] = Wm.codes + r * Wm.row_code_bytes + uoff * CB + 16 * crem;
     }
     if constexpr (scale_bytes<FMT, SU>() > 0) {
 #pragma unroll
       for (int j = 0; j < kScaleWords; ++j) {
         const int64_t r = min(lt * kTileRows + srow + j * (64 / SU), Wm.rows - 1);
-        sptr[j] = Wm.scales + r * Wm.row_scale_bytes + (int64_t)(p.u0 + 2 * spr) * 2;
+        sptr[j] = Wm.scales + r * Wm.row_scale_bytes + (uoff + 2 * spr) * 2;
       }
     }
   };
-  if (lt < tiles) tile_ptrs();
+  if (lt < tiles_end) tile_ptrs();
   auto issue = [&](int slot_idx) {
-    if (lt < tiles && st1 > st0) {
+    if (lt < tiles_end && st1 > st0) {
       const uint32_t slot = ring_s + (uint32_t)slot_idx * kSlot;
       const int u0 = ls * SU;
       if (u0 + cunit < units) {
@@ -551,7 +596,7 @@ __global__ void __launch_bounds__(W * 32, 1) k_gemv_mma(const Params p) {
       if (++ls == st1) {
         ls = st0;
         lt += ngs;
-        if (lt < tiles) tile_ptrs();
+        if (lt < tiles_end) tile_ptrs();
       }
     }
     cp_commit();
@@ -562,14 +607,14 @@ __global__ void __launch_bounds__(W * 32, 1) k_gemv_mma(const Params p) {
   const uint32_t row_bytes = (uint32_t)units * 128u;
   if (threadIdx.x == 0) {
     tc::mbar_arrive_expect_tx(bar, row_bytes * (uint32_t)(p.batch + (norm ? 1 : 0)));
-    if (norm) tc::bulk_copy_g2s(tc::smem_u32(smem + L.gs), p.norm_g + (int64_t)p.u0 * 32, row_bytes, bar);
+    if (norm) tc::bulk_copy_g2s(tc::smem_u32(smem + L.gs), p.norm_g + uoff * 32, row_bytes, bar);
   }
   for (int s = 0; s < kStages - 1; ++s) issue(s);
 
   pdl_wait();  // x (and y, for accumulation) belong to the previous kernel
   if (threadIdx.x == 0) {
     for (int b = 0; b < p.batch; ++b)
-      tc::bulk_copy_g2s(tc::smem_u32(xs + b * L.x_row), p.x + b * p.x_stride + (int64_t)p.u0 * 32, row_bytes, bar);
+      tc::bulk_copy_g2s(tc::smem_u32(xs + b * L.x_row), p.x + b * p.x_stride + uoff * 32, row_bytes, bar);
   }
   for (int i = threadIdx.x; i < nxg * kMaxCols; i += W * 32) {
     if ((i % kMaxCols) >= p.batch) sxs[i] = ssq[i] = 0.f;  // columns without a batch row
@@ -580,6 +625,11 @@ __global__ void __launch_bounds__(W * 32, 1) k_gemv_mma(const Params p) {
     if (threadIdx.x == 0 && p.err) atomicOr(p.err, kErrTimeout);
     tc::mbar_wait_sleep(bar, 0);
     cp_wait_n<0>();
+    if constexpr (SPLIT) {  // the cluster barrier's phases as the other CTAs go through them
+      cluster_wait();
+      cluster_arrive();
+      cluster_wait();
+    }
     return;
   }
 
@@ -617,7 +667,49 @@ __global__ void __launch_bounds__(W * 32, 1) k_gemv_mma(const Params p) {
   for (int c = 0; c < NC; ++c) best[c][0] = best[c][1] = 0ull;
   float acc[NC][4];
   int cs = 0, it = 0;
-  for (int64_t tl = gslot; tl < tiles; tl += ngs, ++it) {  // uniform over the group
+  // ---- end of a tile (first warp of the group): rows tile + g, + 8; columns 8c + 2t,
+  // 8c + 2t + 1
+  auto finish = [&](int64_t tl) {
+    const int64_t rbase = tl * kTileRows;
+    float rsc[2] = {1.f, 1.f};  // INT8 row scales of rows g, g + 8
+    if constexpr (FMT == QD_I8_ROW) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        rsc[h] = __ldg(reinterpret_cast<const float*>(Wm.scales + min(rbase + g + 8 * h, Wm.rows - 1) * Wm.row_scale_bytes));
+    }
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = acc[c][i] * inv[c][i & 1] * rsc[i >> 1];
+      // the next row's values (row g + 1 is lane + 4) for the pair epilogues
+      float nx[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) nx[i] = __shfl_down_sync(0xffffffffu, v[i], 4);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t r = rbase + g + (i >= 2 ? 8 : 0);
+        const int b = 8 * c + 2 * t + (i & 1);
+        if (b >= p.batch || r >= Wm.rows) continue;
+        if (p.mode == kGemvSwiGLU) {
+          if ((g & 1) == 0 && r + 1 < Wm.rows)
+            p.y[(int64_t)b * (Wm.rows / 2) + r / 2] = v[i] / (1.0f + expf(-v[i])) * nx[i];
+        } else if (p.mode == kGemvQKV) {
+          if ((g & 1) == 0 && r + 1 < Wm.rows) qkv_pair(p, r, b, v[i], nx[i]);
+        } else {
+          float* dst = p.y + (int64_t)b * Wm.rows + r;
+          if (p.mode == kGemvAccumulate || p.accumulate) *dst = __ldcg(dst) + v[i];
+          else *dst = v[i];
+          if (p.mode == kGemvArgmax) {
+            const unsigned long long key = argmax_key(v[i], (uint32_t)r);
+            best[c][i & 1] = key > best[c][i & 1] ? key : best[c][i & 1];
+          }
+        }
+      }
+    }
+  };
+  int64_t split_tile = -1;  // split launches: the group's tile, finished after the exchange
+  for (int64_t tl = gslot; tl < tiles_end; tl += ngs, ++it) {  // uniform over the group
 #pragma unroll
     for (int c = 0; c < NC; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
     for (int st = st0; st < st1; ++st) {
@@ -667,47 +759,40 @@ __global__ void __launch_bounds__(W * 32, 1) k_gemv_mma(const Params p) {
         }
       }
     }
-    // ---- end of a tile (first warp of the group): rows tile + g, + 8; columns 8c + 2t,
-    // 8c + 2t + 1
-    const int64_t rbase = tl * kTileRows;
-    float rsc[2] = {1.f, 1.f};  // INT8 row scales of rows g, g + 8
-    if constexpr (FMT == QD_I8_ROW) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        rsc[h] = __ldg(reinterpret_cast<const float*>(Wm.scales + min(rbase + g + 8 * h, Wm.rows - 1) * Wm.row_scale_bytes));
-    }
-#pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      float v[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = acc[c][i] * inv[c][i & 1] * rsc[i >> 1];
-      // the next row's values (row g + 1 is lane + 4) for the pair epilogues
-      float nx[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) nx[i] = __shfl_down_sync(0xffffffffu, v[i], 4);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int64_t r = rbase + g + (i >= 2 ? 8 : 0);
-        const int b = 8 * c + 2 * t + (i & 1);
-        if (b >= p.batch || r >= Wm.rows) continue;
-        if (p.mode == kGemvSwiGLU) {
-          if ((g & 1) == 0 && r + 1 < Wm.rows)
-            p.y[(int64_t)b * (Wm.rows / 2) + r / 2] = v[i] / (1.0f + expf(-v[i])) * nx[i];
-        } else if (p.mode == kGemvQKV) {
-          if ((g & 1) == 0 && r + 1 < Wm.rows) qkv_pair(p, r, b, v[i], nx[i]);
-        } else {
-          float* dst = p.y + (int64_t)b * Wm.rows + r;
-          if (p.mode == kGemvAccumulate || p.accumulate) *dst = __ldcg(dst) + v[i];
-          else *dst = v[i];
-          if (p.mode == kGemvArgmax) {
-            const unsigned long long key = argmax_key(v[i], (uint32_t)r);
-            best[c][i & 1] = key > best[c][i & 1] ? key : best[c][i & 1];
-          }
-        }
-      }
-    }
+    if constexpr (SPLIT) split_tile = tl;
+    else finish(tl);
   }
   cp_wait_n<0>();  // no copy may still target this CTA's shared memory at exit
+  if constexpr (SPLIT) {
+    // the other CTAs' tile sums into the first CTA's slots, one cluster barrier, then the
+    // first CTA adds them in CTA order and runs the epilogue
+    const int groups = W / KS;
+    const uint32_t spl = tc::smem_u32(smem + L.spl);
+    cluster_wait();  // the first CTA has started: its slots exist
+    if (rank != 0 && ks == 0 && split_tile >= 0) {
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+        st_cluster4(spl + (uint32_t)(((((rank - 1) * groups + grp) * 32 + lane) * NC + c) * 16), 0, acc[c][0], acc[c][1],
+                    acc[c][2], acc[c][3]);
+    }
+    cluster_arrive();
+    cluster_wait();
+    if (rank != 0) return;
+    if (ks == 0 && split_tile >= 0) {
+      const float* sp = reinterpret_cast<const float*>(smem + L.spl);
+      for (int r = 1; r < C; ++r) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const float4 q = *reinterpret_cast<const float4*>(sp + ((((r - 1) * groups + grp) * 32 + lane) * NC + c) * 4);
+          acc[c][0] += q.x;
+          acc[c][1] += q.y;
+          acc[c][2] += q.z;
+          acc[c][3] += q.w;
+        }
+      }
+      finish(split_tile);
+    }
+  }
   if (p.mode == kGemvArgmax) {
     // per batch column: max over the lanes holding it (same t), one atomicMax per warp;
     // the last CTA to arrive finalises the tokens and re-arms keys and counter
@@ -753,13 +838,13 @@ int sm_count() {
   return v;
 }
 
-template <int FMT, int NC, int W>
+template <int FMT, int NC, int W, bool SPLIT = false>
 bool smem_attr_set() {
   static bool done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (!done[dev]) {
-    if (cudaFuncSetAttribute(k_gemv_mma<FMT, NC, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) !=
+    if (cudaFuncSetAttribute(k_gemv_mma<FMT, NC, W, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) !=
         cudaSuccess) {
       cudaGetLastError();
       return false;
@@ -772,11 +857,11 @@ bool smem_attr_set() {
 bool fmt_taken(int fmt) { return fmt == QD_Q4_0 || fmt == QD_Q8_0 || fmt == QD_I8_ROW; }
 
 template <int W>
-size_t smem_for_w(int fmt, int units, int batch, bool norm, int stages) {
+size_t smem_for_w(int fmt, int units, int batch, bool norm, int stages, size_t split_bytes = 0) {
   switch (fmt) {
-    case QD_Q4_0: return layout<QD_Q4_0, W>(units, batch, norm, stages).total;
-    case QD_Q8_0: return layout<QD_Q8_0, W>(units, batch, norm, stages).total;
-    default: return layout<QD_I8_ROW, W>(units, batch, norm, stages).total;
+    case QD_Q4_0: return layout<QD_Q4_0, W>(units, batch, norm, stages, split_bytes).total;
+    case QD_Q8_0: return layout<QD_Q8_0, W>(units, batch, norm, stages, split_bytes).total;
+    default: return layout<QD_I8_ROW, W>(units, batch, norm, stages, split_bytes).total;
   }
 }
 size_t smem_for(int fmt, int warps, int units, int batch, bool norm, int stages) {
@@ -859,8 +944,113 @@ qd_status launch_range(Params p, bool pdl, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   if (col_blocks(p.batch) == 2)
-    return cudaLaunchKernelEx(&cfg, k_gemv_mma<FMT, 2, W>, p) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
-  return cudaLaunchKernelEx(&cfg, k_gemv_mma<FMT, 1, W>, p) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, k_gemv_mma<FMT, 2, W, false>, p) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, k_gemv_mma<FMT, 1, W, false>, p) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
+}
+
+// ---- split launches (8-warp CTAs in clusters of 2 or 4 over the columns)
+struct SplitPlan {
+  int c = 0;       // CTAs per cluster; 0: no split fits
+  int ks = 1;      // warps per tile
+  int stages = 0;  // ring depth
+  int64_t clusters = 0;
+};
+
+// Clusters of `c` CTAs with `smem` bytes each that the GPU holds at once (the grid must
+// not run in waves: every CTA takes its tile up front); 0 on error.
+template <int FMT, int NC>
+int max_active_clusters(int c, size_t smem) {
+  struct Entry {
+    int dev, c;
+    size_t smem;
+    int n;
+  };
+  static Entry cache[32];
+  static int used = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  for (int i = 0; i < used; ++i)
+    if (cache[i].dev == dev && cache[i].c == c && cache[i].smem == smem) return cache[i].n;
+  if (!smem_attr_set<FMT, NC, 8, true>()) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)c);
+  cfg.blockDim = dim3(8 * 32);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeClusterDimension;
+  a[0].val.clusterDim.x = (unsigned)c;
+  a[0].val.clusterDim.y = 1;
+  a[0].val.clusterDim.z = 1;
+  cfg.attrs = a;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, (void*)k_gemv_mma<FMT, NC, 8, true>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (used < 32) cache[used++] = Entry{dev, c, smem, n};
+  return n;
+}
+
+// The split with the fewest ring stages on the busiest warp (a shallow ring costs a
+// quarter more) among clusters of 2 or 4 whose CTAs each hold their share of x beside a
+// ring of two stages or more and whose groups take one tile each.
+template <int FMT>
+SplitPlan split_plan(int64_t rows, int units, int batch) {
+  SplitPlan best;
+  double best_cost = 1e30;
+  const int64_t tiles = (rows + kTileRows - 1) / kTileRows;
+  const int nxg = (units + kXUnits - 1) / kXUnits;
+  const int nc = col_blocks(batch);
+  for (int c : {2, 4}) {
+    if (nxg < 2 * c) continue;
+    const int cap = split_units_cap(units, c);
+    const int nst = (cap + stage_units<8>() - 1) / stage_units<8>();
+    for (int ks : {1, 2, 4}) {
+      const size_t sb = split_slot_bytes(c, 8 / ks, nc);
+      int st = 0;
+      for (int s2 = 8; s2 >= 2 && !st; --s2)
+        if (layout<FMT, 8>(cap, batch, false, s2, sb).total <= kSmemCap) st = s2;
+      if (st < 2) continue;
+      const int64_t need = (tiles + 8 / ks - 1) / (8 / ks);  // clusters for one tile per group
+      const int64_t fit = nc == 2 ? max_active_clusters<FMT, 2>(c, layout<FMT, 8>(cap, batch, false, st, sb).total)
+                                  : max_active_clusters<FMT, 1>(c, layout<FMT, 8>(cap, batch, false, st, sb).total);
+      if (need > fit) continue;
+      const double cost = (double)((nst + ks - 1) / ks) * (1.0 + 0.05 * (ks - 1)) * (st >= 3 ? 1.0 : 1.25);
+      if (cost < best_cost) {
+        best_cost = cost;
+        best.c = c;
+        best.ks = ks;
+        best.stages = st;
+        best.clusters = need;
+      }
+    }
+  }
+  return best;
+}
+
+template <int FMT, int NC>
+qd_status launch_split_nc(Params p, const SplitPlan& sp, bool pdl, cudaStream_t stream) {
+  if (!smem_attr_set<FMT, NC, 8, true>()) return QD_ERR_CUDA;
+  p.ks = sp.ks;
+  p.stages = sp.stages;
+  p.ksplit = sp.c;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(sp.clusters * sp.c));
+  cfg.blockDim = dim3(8 * 32);
+  cfg.dynamicSmemBytes =
+      layout<FMT, 8>(split_units_cap(p.units, sp.c), p.batch, false, sp.stages, split_slot_bytes(sp.c, 8 / sp.ks, NC)).total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)sp.c;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, k_gemv_mma<FMT, NC, 8, true>, p) == cudaSuccess ? QD_OK : QD_ERR_CUDA;
 }
 
 // One launch with 16-warp CTAs where their ring fits three stages deep; otherwise 8-warp
@@ -872,6 +1062,13 @@ qd_status launch(Params p, bool pdl, cudaStream_t stream) {
   const bool norm = p.norm_g != nullptr;
   if (warps_for(FMT, units, p.batch, norm) == 16) return launch_range<FMT, 16>(p, pdl, stream);
   const int ru = range_units(FMT, units, p.batch, norm);
+  if (ru < units && !norm && (p.mode == kGemvStore || p.mode == kGemvAccumulate)) {
+    // x too wide for one CTA: split the columns over a cluster where that fits
+    const SplitPlan sp = split_plan<FMT>(p.W.rows, units, p.batch);
+    if (sp.c > 0)
+      return col_blocks(p.batch) == 2 ? launch_split_nc<FMT, 2>(p, sp, pdl, stream)
+                                      : launch_split_nc<FMT, 1>(p, sp, pdl, stream);
+  }
   if (ru <= 0) return QD_ERR_UNSUPPORTED;
   for (int u0 = 0; u0 < units; u0 += ru) {
     p.u0 = u0;
@@ -887,9 +1084,22 @@ qd_status launch(Params p, bool pdl, cudaStream_t stream) {
 
 namespace mma_gemv {
 
-// Whether one launch sequence (a single launch, or column ranges) takes these arguments:
-// x of every batch row beside a ring of two stages, or (store and accumulate without the
-// fused norm) column ranges that fit.
+// Whether x too wide for one CTA splits over a cluster (store and accumulate without the
+// fused norm).
+bool split_fits(const GemvArgs& a) {
+  const int units = (int)(a.W.cols / 32);
+  if (a.norm_g || (a.mode != kGemvStore && a.mode != kGemvAccumulate)) return false;
+  if (stages_for(a.fmt, 8, units, a.batch, false) >= 2) return false;
+  switch (a.fmt) {
+    case QD_Q4_0: return split_plan<QD_Q4_0>(a.W.rows, units, a.batch).c > 0;
+    case QD_Q8_0: return split_plan<QD_Q8_0>(a.W.rows, units, a.batch).c > 0;
+    default: return split_plan<QD_I8_ROW>(a.W.rows, units, a.batch).c > 0;
+  }
+}
+
+// Whether one launch sequence (a single launch, a split launch or column ranges) takes
+// these arguments: x of every batch row beside a ring of two stages, or (store and
+// accumulate without the fused norm) a split over a cluster or column ranges that fit.
 bool one_pass_fits(const GemvArgs& a) {
   const int units = (int)(a.W.cols / 32);
   if (stages_for(a.fmt, 8, units, a.batch, a.norm_g != nullptr) >= 2) return true;
@@ -938,6 +1148,7 @@ qd_status launch_args(const GemvArgs& a, cudaStream_t stream) {
   p.units = (int)(a.W.cols / 32);
   p.stages = 0;
   p.ks = 1;
+  p.ksplit = 1;
   p.accumulate = false;
   switch (a.fmt) {
     case QD_Q4_0: return launch<QD_Q4_0>(p, a.pdl, stream);
@@ -951,10 +1162,10 @@ qd_status launch_args(const GemvArgs& a, cudaStream_t stream) {
 // Batch 3-16, Q4_0 / Q8_0 / INT8 rows, even unit counts for the block formats (4-byte scale
 // copies), x and norm_g on 16-byte boundaries (bulk copies).  One pass over the weights when
 // x of every batch row fits beside a ring of two stages (or, store and accumulate without
-// RMSNorm, in column ranges that fit).  At batch 9-16 otherwise two passes of up to 8 rows
-// for Q4_0 and Q8_0 (measured faster than column ranges: the second pass finds much of
-// the weights in L2); INT8 rows then go to the batch-16 tcgen05 kernel, which measured
-// faster there.
+// RMSNorm, split over a cluster's CTAs or in column ranges that fit).  At batch 9-16
+// otherwise a split launch, or two passes of up to 8 rows for Q4_0 and Q8_0 (measured
+// faster than column ranges: the second pass finds much of the weights in L2); INT8 rows
+// then go to the batch-16 tcgen05 kernel, which measured faster there.
 bool gemv_mma_supported(const GemvArgs& a) {
   using namespace mma_gemv;
   if (!fmt_taken(a.fmt) || a.batch < 3 || a.batch > kMaxCols || a.W.cols % 32 || a.W.cols > (1 << 22)) return false;
@@ -967,7 +1178,7 @@ bool gemv_mma_supported(const GemvArgs& a) {
   }
   if (a.batch <= 8) return one_pass_fits(a);
   const int units_ok = stages_for(a.fmt, 8, units, a.batch, a.norm_g != nullptr) >= 2;
-  if (units_ok) return true;
+  if (units_ok || split_fits(a)) return true;
   if (a.fmt == QD_I8_ROW) return false;
   return one_pass_fits(row_slice(a, 0, 8)) && one_pass_fits(row_slice(a, 8, a.batch - 8));
 }
@@ -976,7 +1187,8 @@ qd_status launch_q_gemv_mma(const GemvArgs& a, cudaStream_t stream) {
   using namespace mma_gemv;
   if (!gemv_mma_supported(a)) return QD_ERR_UNSUPPORTED;
   const int units = (int)(a.W.cols / 32);
-  if (a.batch <= 8 || stages_for(a.fmt, 8, units, a.batch, a.norm_g != nullptr) >= 2) return launch_args(a, stream);
+  if (a.batch <= 8 || stages_for(a.fmt, 8, units, a.batch, a.norm_g != nullptr) >= 2 || split_fits(a))
+    return launch_args(a, stream);
   // two passes of up to 8 batch rows, the second a programmatic dependent of the first
   const qd_status st = launch_args(row_slice(a, 0, 8), stream);
   if (st != QD_OK) return st;

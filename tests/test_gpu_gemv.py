@@ -242,14 +242,34 @@ def test_q_gemv_tensor_core_partial_stage(qd, fmt, cols, batch):
     assert_close(got, oracle.gemv(fmt, src, rows, cols, x), tol=2e-5, what=f"{fmt} {cols} b{batch}")
 
 
-@pytest.mark.parametrize("fmt,cols", [("q4_0", 11008), ("q8_0", 11008), ("i8", 11040)])
-@pytest.mark.parametrize("batch", [5, 8, 16])
-def test_q_gemv_tensor_core_column_ranges(qd, fmt, cols, batch):
+@pytest.mark.parametrize("fmt,cols,batch", [(f, c, b) for f, c in [("q4_0", 11008), ("q8_0", 11008), ("i8", 11040)]
+                                            for b in (5, 8, 16)]
+                         + [("q4_0", 8192, 16), ("i8", 8192, 9), ("q8_0", 8192, 12)])
+def test_q_gemv_tensor_core_column_split(qd, fmt, cols, batch):
     """x rows too wide for the shared memory beside the weight ring (11008 columns at batch
-    5 or 8: over 220 KB of x) run as consecutive launches over column ranges, the first
-    storing and the rest adding; INT8 11040 = 345 units leaves an odd, partial last range.
-    Every output row against the oracle, and two runs give the same bits."""
+    5 or 8: over 220 KB of x) and few enough tiles for one per warp group: the columns
+    split over a cluster's CTAs (whole 256-column x groups; INT8 11040 = 345 units leaves
+    the last CTA a partial group), the first CTA adding the others' tile sums in CTA
+    order.  8192 columns at batch 9-16: one split launch with two blocks of 8 columns.
+    Batch 16 at 11008 columns runs two passes of 8 rows, each split (INT8: the tcgen05
+    kernel).  Every output row against the oracle, and two runs give the same bits."""
     rows = 300
+    src, p = weights(qd, fmt, 15, f"tcs.{fmt}", rows, cols)
+    x = qdsynth.activations(15, "tcs.x", batch, cols)
+    got = _gemv(qd, fmt, p, rows, cols, x)
+    assert_close(got, oracle.gemv(fmt, src, rows, cols, x), tol=2e-5, what=f"{fmt} {cols} b{batch}")
+    again = _gemv(qd, fmt, p, rows, cols, x)
+    assert np.array_equal(got.view(np.uint32), again.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt,cols,batch", [("q4_0", 11008, 5), ("q4_0", 11008, 8), ("q8_0", 8192, 8),
+                                            ("i8", 11040, 8)])
+def test_q_gemv_tensor_core_column_ranges(qd, fmt, cols, batch):
+    """x rows too wide for the shared memory and more tiles than a split grid gives its
+    warp groups (12288 rows = 768 tiles) run as consecutive launches over column ranges,
+    the first storing and the rest adding; INT8 11040 = 345 units leaves an odd, partial
+    last range.  Every output row against the oracle, and two runs give the same bits."""
+    rows = 12288
     src, p = weights(qd, fmt, 14, f"tcr.{fmt}", rows, cols)
     x = qdsynth.activations(14, "tcr.x", batch, cols)
     got = _gemv(qd, fmt, p, rows, cols, x)
