@@ -100,8 +100,11 @@ constexpr int slot_bytes() {
 // batch columns: one or two blocks of 8 (the MMA's N); scale and norm arrays keep 16 a stage
 constexpr int kMaxCols = 16;
 __host__ __device__ constexpr int col_blocks(int batch) { return batch > 8 ? 2 : 1; }
-// per-warp partial accumulators for the column split, two tiles deep
-__host__ __device__ constexpr size_t partial_bytes(int nc, int warps) { return (size_t)2 * warps * 32 * 4 * nc * 4; }
+// per-warp partial accumulators for the warps sharing a tile, two tiles deep (one in split
+// launches, whose warp groups take one tile each)
+__host__ __device__ constexpr size_t partial_bytes(int nc, int warps, int depth) {
+  return (size_t)depth * warps * 32 * 4 * nc * 4;
+}
 
 // Shared-memory layout of one launch (byte offsets; every part 16-byte aligned).
 struct Layout {
@@ -110,6 +113,7 @@ struct Layout {
 };
 template <int FMT, int W>
 __host__ __device__ inline Layout layout(int units, int batch, bool norm, int stages, size_t split_bytes = 0) {
+  const int depth = split_bytes > 0 ? 1 : 2;  // partial-sum buffers
   Layout L;
   const int nxg = (units + kXUnits - 1) / kXUnits;
   L.x_row = (int64_t)units * 128 + kXPad;
@@ -119,7 +123,7 @@ __host__ __device__ inline Layout layout(int units, int batch, bool norm, int st
   L.sx = L.gs + (norm ? (size_t)units * 128 : 0);
   L.ssq = L.sx + (size_t)nxg * kMaxCols * 4;
   L.partial = L.ssq + (size_t)nxg * kMaxCols * 4;
-  L.bar = L.partial + partial_bytes(col_blocks(batch), W);
+  L.bar = L.partial + partial_bytes(col_blocks(batch), W, depth);
   L.spl = L.bar + 16;
   L.total = L.spl + split_bytes;
   return L;
@@ -740,7 +744,7 @@ __global__ void __launch_bounds__(W * 32, 1) k_gemv_mma(const Params p) {
     }
     if (KS > 1) {
       // the group's column parts, summed in part order by its first warp
-      float* pt = partial + (size_t)(it & 1) * W * 32 * 4 * NC;
+      float* pt = partial + (size_t)(SPLIT ? 0 : (it & 1)) * W * 32 * 4 * NC;
 #pragma unroll
       for (int c = 0; c < NC; ++c)
         *reinterpret_cast<float4*>(pt + ((warp * 32 + lane) * NC + c) * 4) =

@@ -244,13 +244,14 @@ def test_q_gemv_tensor_core_partial_stage(qd, fmt, cols, batch):
 
 @pytest.mark.parametrize("fmt,cols,batch", [(f, c, b) for f, c in [("q4_0", 11008), ("q8_0", 11008), ("i8", 11040)]
                                             for b in (5, 8, 16)]
-                         + [("q4_0", 8192, 16), ("i8", 8192, 9), ("q8_0", 8192, 12)])
+                         + [("q4_0", 8192, 16), ("i8", 8192, 9), ("q8_0", 8192, 12), ("i8", 8192, 16)])
 def test_q_gemv_tensor_core_column_split(qd, fmt, cols, batch):
     """x rows too wide for the shared memory beside the weight ring (11008 columns at batch
     5 or 8: over 220 KB of x) and few enough tiles for one per warp group: the columns
     split over a cluster's CTAs (whole 256-column x groups; INT8 11040 = 345 units leaves
     the last CTA a partial group), the first CTA adding the others' tile sums in CTA
-    order.  8192 columns at batch 9-16: one split launch with two blocks of 8 columns.
+    order.  8192 columns at batch 9-16: one split launch with two blocks of 8 columns
+    (one buffer of per-warp partial sums: each warp group takes a single tile).
     Batch 16 at 11008 columns runs two passes of 8 rows, each split (INT8: the tcgen05
     kernel).  Every output row against the oracle, and two runs give the same bits."""
     rows = 300
