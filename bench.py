@@ -571,6 +571,7 @@ def bench_1p7b(qd, torch, stream, args, hbm, batches=(1, 16), layers=None, kv_f1
         gbs = (wbytes + kv) / t / 1e9
         roof = batch / ((wbytes + kv) / (hbm * 1e9))
         out[f"batch{batch}" + ("_kv_f16" if kv_f16 else "")] = {"ms_per_step": round(t * 1e3, 3), "ms_per_step_best": round(min(ts) * 1e3, 3),
+                                "launches_per_step": m.launches_per_step(),
                                 "tokens/s": round(batch / t, 1), "bytes_per_step": int(wbytes + kv),
                                 "GB/s": round(gbs, 1), "roofline_tokens/s": round(roof, 1),
                                 "frac": round(gbs / hbm, 4), "frac_nominal_8tbs": round(gbs / 8000, 4)}

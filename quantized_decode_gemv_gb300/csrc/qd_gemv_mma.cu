@@ -76,6 +76,8 @@ struct Params {
   int stages;        // ring depth (slots per warp), sized to the shared memory left
   int ks;            // warps that share one tile, each over a contiguous part of its columns
   int ksplit;        // CTAs per cluster splitting the columns (split launches; 1 otherwise)
+  int pdepth;        // buffers of warp partial sums: 0 (ks = 1), 1 (every warp group takes
+                     // one tile at most) or 2
   bool accumulate;   // a later column range: y += partial product (store mode's chunks)
 };
 
@@ -100,8 +102,8 @@ constexpr int slot_bytes() {
 // batch columns: one or two blocks of 8 (the MMA's N); scale and norm arrays keep 16 a stage
 constexpr int kMaxCols = 16;
 __host__ __device__ constexpr int col_blocks(int batch) { return batch > 8 ? 2 : 1; }
-// per-warp partial accumulators for the warps sharing a tile, two tiles deep (one in split
-// launches, whose warp groups take one tile each)
+// per-warp partial accumulators for the warps sharing a tile: `depth` tiles deep (two; one
+// where every warp group takes one tile at most; none where warps do not share tiles)
 __host__ __device__ constexpr size_t partial_bytes(int nc, int warps, int depth) {
   return (size_t)depth * warps * 32 * 4 * nc * 4;
 }
@@ -112,8 +114,8 @@ struct Layout {
   int64_t x_row;  // bytes between staged batch rows
 };
 template <int FMT, int W>
-__host__ __device__ inline Layout layout(int units, int batch, bool norm, int stages, size_t split_bytes = 0) {
-  const int depth = split_bytes > 0 ? 1 : 2;  // partial-sum buffers
+__host__ __device__ inline Layout layout(int units, int batch, bool norm, int stages, size_t split_bytes = 0,
+                                         int depth = 2) {
   Layout L;
   const int nxg = (units + kXUnits - 1) / kXUnits;
   L.x_row = (int64_t)units * 128 + kXPad;
@@ -527,7 +529,7 @@ __global__ void __launch_bounds__(W * 32, 1) k_gemv_mma(const Params p) {
   const bool norm = p.norm_g != nullptr;
   const int KS = p.ks, grp = warp / KS, ks = warp % KS;
   const Layout L = layout<FMT, W>(SPLIT ? split_units_cap(p.units, C) : units, p.batch, norm, kStages,
-                                  SPLIT ? split_slot_bytes(C, W / KS, NC) : 0);
+                                  SPLIT ? split_slot_bytes(C, W / KS, NC) : 0, p.pdepth);
   const int64_t tiles = (Wm.rows + kTileRows - 1) / kTileRows;
   // the KS warps of a group share each of the group's tiles; warp ks of the group takes
   // the tile's stages [st0, st1); groups take tiles round-robin over the grid (a split
@@ -744,7 +746,7 @@ __global__ void __launch_bounds__(W * 32, 1) k_gemv_mma(const Params p) {
     }
     if (KS > 1) {
       // the group's column parts, summed in part order by its first warp
-      float* pt = partial + (size_t)(SPLIT ? 0 : (it & 1)) * W * 32 * 4 * NC;
+      float* pt = partial + (size_t)(p.pdepth == 2 ? (it & 1) : 0) * W * 32 * 4 * NC;
 #pragma unroll
       for (int c = 0; c < NC; ++c)
         *reinterpret_cast<float4*>(pt + ((warp * 32 + lane) * NC + c) * 4) =
@@ -861,28 +863,51 @@ bool smem_attr_set() {
 bool fmt_taken(int fmt) { return fmt == QD_Q4_0 || fmt == QD_Q8_0 || fmt == QD_I8_ROW; }
 
 template <int W>
-size_t smem_for_w(int fmt, int units, int batch, bool norm, int stages, size_t split_bytes = 0) {
+size_t smem_for_w(int fmt, int units, int batch, bool norm, int stages, int depth) {
   switch (fmt) {
-    case QD_Q4_0: return layout<QD_Q4_0, W>(units, batch, norm, stages, split_bytes).total;
-    case QD_Q8_0: return layout<QD_Q8_0, W>(units, batch, norm, stages, split_bytes).total;
-    default: return layout<QD_I8_ROW, W>(units, batch, norm, stages, split_bytes).total;
+    case QD_Q4_0: return layout<QD_Q4_0, W>(units, batch, norm, stages, 0, depth).total;
+    case QD_Q8_0: return layout<QD_Q8_0, W>(units, batch, norm, stages, 0, depth).total;
+    default: return layout<QD_I8_ROW, W>(units, batch, norm, stages, 0, depth).total;
   }
 }
-size_t smem_for(int fmt, int warps, int units, int batch, bool norm, int stages) {
-  return warps == 16 ? smem_for_w<16>(fmt, units, batch, norm, stages) : smem_for_w<8>(fmt, units, batch, norm, stages);
+size_t smem_for(int fmt, int warps, int units, int batch, bool norm, int stages, int depth) {
+  return warps == 16 ? smem_for_w<16>(fmt, units, batch, norm, stages, depth)
+                     : smem_for_w<8>(fmt, units, batch, norm, stages, depth);
 }
 
-// Ring depth: the deepest (up to 8 slots a warp) that fits the shared memory; 0: none does.
-int stages_for(int fmt, int warps, int units, int batch, bool norm) {
-  for (int s = 8; s >= 2; --s)
-    if (smem_for(fmt, warps, units, batch, norm, s) <= kSmemCap) return s;
-  return 0;
+int ks_for(int64_t tiles, int nst, int sms, int warps);
+
+// One launch over `units` columns with CTAs of `warps` warps: warps per tile, grid,
+// partial-sum buffers and ring depth (the deepest, up to 8 slots a warp, that fits the
+// shared memory; 0: none does).
+struct RangePlan {
+  int ks = 1;
+  int64_t ctas = 0;
+  int depth = 2;
+  int stages = 0;
+};
+RangePlan range_plan(int fmt, int warps, int64_t rows, int units, int batch, bool norm) {
+  RangePlan r;
+  const int64_t tiles = (rows + kTileRows - 1) / kTileRows;
+  const int su = warps == 16 ? stage_units<16>() : stage_units<8>();
+  const int sms = sm_count();
+  r.ks = ks_for(tiles, (units + su - 1) / su, sms, warps);
+  const int64_t groups_per_cta = warps / r.ks;
+  r.ctas = (tiles + groups_per_cta - 1) / groups_per_cta;
+  if (r.ctas > sms) r.ctas = sms;
+  r.depth = r.ks == 1 ? 0 : tiles <= r.ctas * groups_per_cta ? 1 : 2;
+  for (int s = 8; s >= 2 && !r.stages; --s)
+    if (smem_for(fmt, warps, units, batch, norm, s, r.depth) <= kSmemCap) r.stages = s;
+  return r;
+}
+int stages_for(int fmt, int warps, int64_t rows, int units, int batch, bool norm) {
+  return range_plan(fmt, warps, rows, units, batch, norm).stages;
 }
 
 // Warps per CTA for a launch over `units` columns: 16 (4-unit stages) where their ring
 // can be three stages deep, otherwise 8 (8-unit stages).
-int warps_for(int fmt, int units, int batch, bool norm) {
-  return stages_for(fmt, 16, units, batch, norm) >= 3 ? 16 : 8;
+int warps_for(int fmt, int64_t rows, int units, int batch, bool norm) {
+  return stages_for(fmt, 16, rows, units, batch, norm) >= 3 ? 16 : 8;
 }
 
 // Ring stages a column range is sized for: about 64 KB of weights in flight per SM (8 warps).
@@ -894,12 +919,12 @@ int ring_floor(int fmt) {
 // Units per column range: all of them when x fits beside a ring of two stages or more;
 // otherwise the widest multiple of an x scale group that leaves room for ring_floor stages
 // of the 8-warp CTA.
-int range_units(int fmt, int units, int batch, bool norm) {
-  if (stages_for(fmt, 8, units, batch, norm) >= 2) return units;
+int range_units(int fmt, int64_t rows, int units, int batch, bool norm) {
+  if (stages_for(fmt, 8, rows, units, batch, norm) >= 2) return units;
   const int floor_st = ring_floor(fmt);
   int ru = (units / kXUnits) * kXUnits;
-  while (ru > kXUnits && smem_for(fmt, 8, ru, batch, norm, floor_st) > kSmemCap) ru -= kXUnits;
-  return smem_for(fmt, 8, ru, batch, norm, floor_st) <= kSmemCap ? ru : 0;
+  while (ru > kXUnits && smem_for(fmt, 8, ru, batch, norm, floor_st, 2) > kSmemCap) ru -= kXUnits;
+  return smem_for(fmt, 8, ru, batch, norm, floor_st, 2) <= kSmemCap ? ru : 0;
 }
 
 // Warps per tile (1, 2, 4, or 8 in a 16-warp CTA): the fewest rounds of stages on the
@@ -927,20 +952,16 @@ int ks_for(int64_t tiles, int nst, int sms, int warps) {
 template <int FMT, int W>
 qd_status launch_range(Params p, bool pdl, cudaStream_t stream) {
   if (!(col_blocks(p.batch) == 2 ? smem_attr_set<FMT, 2, W>() : smem_attr_set<FMT, 1, W>())) return QD_ERR_CUDA;
-  const int64_t tiles = (p.W.rows + kTileRows - 1) / kTileRows;
-  const int nst = (p.units + stage_units<W>() - 1) / stage_units<W>();
-  const int sms = sm_count();
   const bool norm = p.norm_g != nullptr;
-  p.stages = stages_for(FMT, W, p.units, p.batch, norm);
-  if (p.stages < 2) return QD_ERR_UNSUPPORTED;
-  p.ks = ks_for(tiles, nst, sms, W);
-  const int64_t groups_per_cta = W / p.ks;
-  int64_t ctas = (tiles + groups_per_cta - 1) / groups_per_cta;
-  if (ctas > sms) ctas = sms;
+  const RangePlan rp = range_plan(FMT, W, p.W.rows, p.units, p.batch, norm);
+  if (rp.stages < 2) return QD_ERR_UNSUPPORTED;
+  p.stages = rp.stages;
+  p.ks = rp.ks;
+  p.pdepth = rp.depth;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.gridDim = dim3((unsigned)rp.ctas);
   cfg.blockDim = dim3(W * 32);
-  cfg.dynamicSmemBytes = layout<FMT, W>(p.units, p.batch, norm, p.stages).total;
+  cfg.dynamicSmemBytes = layout<FMT, W>(p.units, p.batch, norm, p.stages, 0, p.pdepth).total;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1014,11 +1035,11 @@ SplitPlan split_plan(int64_t rows, int units, int batch) {
       const size_t sb = split_slot_bytes(c, 8 / ks, nc);
       int st = 0;
       for (int s2 = 8; s2 >= 2 && !st; --s2)
-        if (layout<FMT, 8>(cap, batch, false, s2, sb).total <= kSmemCap) st = s2;
+        if (layout<FMT, 8>(cap, batch, false, s2, sb, 1).total <= kSmemCap) st = s2;
       if (st < 2) continue;
       const int64_t need = (tiles + 8 / ks - 1) / (8 / ks);  // clusters for one tile per group
-      const int64_t fit = nc == 2 ? max_active_clusters<FMT, 2>(c, layout<FMT, 8>(cap, batch, false, st, sb).total)
-                                  : max_active_clusters<FMT, 1>(c, layout<FMT, 8>(cap, batch, false, st, sb).total);
+      const size_t smem = layout<FMT, 8>(cap, batch, false, st, sb, 1).total;
+      const int64_t fit = nc == 2 ? max_active_clusters<FMT, 2>(c, smem) : max_active_clusters<FMT, 1>(c, smem);
       if (need > fit) continue;
       const double cost = (double)((nst + ks - 1) / ks) * (1.0 + 0.05 * (ks - 1)) * (st >= 3 ? 1.0 : 1.25);
       if (cost < best_cost) {
@@ -1039,11 +1060,13 @@ qd_status launch_split_nc(Params p, const SplitPlan& sp, bool pdl, cudaStream_t 
   p.ks = sp.ks;
   p.stages = sp.stages;
   p.ksplit = sp.c;
+  p.pdepth = 1;  // one tile per warp group
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(sp.clusters * sp.c));
   cfg.blockDim = dim3(8 * 32);
   cfg.dynamicSmemBytes =
-      layout<FMT, 8>(split_units_cap(p.units, sp.c), p.batch, false, sp.stages, split_slot_bytes(sp.c, 8 / sp.ks, NC)).total;
+      layout<FMT, 8>(split_units_cap(p.units, sp.c), p.batch, false, sp.stages, split_slot_bytes(sp.c, 8 / sp.ks, NC), 1)
+          .total;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1064,8 +1087,8 @@ template <int FMT>
 qd_status launch(Params p, bool pdl, cudaStream_t stream) {
   const int units = (int)(p.W.cols / 32);
   const bool norm = p.norm_g != nullptr;
-  if (warps_for(FMT, units, p.batch, norm) == 16) return launch_range<FMT, 16>(p, pdl, stream);
-  const int ru = range_units(FMT, units, p.batch, norm);
+  if (warps_for(FMT, p.W.rows, units, p.batch, norm) == 16) return launch_range<FMT, 16>(p, pdl, stream);
+  const int ru = range_units(FMT, p.W.rows, units, p.batch, norm);
   if (ru < units && !norm && (p.mode == kGemvStore || p.mode == kGemvAccumulate)) {
     // x too wide for one CTA: split the columns over a cluster where that fits
     const SplitPlan sp = split_plan<FMT>(p.W.rows, units, p.batch);
@@ -1093,7 +1116,7 @@ namespace mma_gemv {
 bool split_fits(const GemvArgs& a) {
   const int units = (int)(a.W.cols / 32);
   if (a.norm_g || (a.mode != kGemvStore && a.mode != kGemvAccumulate)) return false;
-  if (stages_for(a.fmt, 8, units, a.batch, false) >= 2) return false;
+  if (stages_for(a.fmt, 8, a.W.rows, units, a.batch, false) >= 2) return false;
   switch (a.fmt) {
     case QD_Q4_0: return split_plan<QD_Q4_0>(a.W.rows, units, a.batch).c > 0;
     case QD_Q8_0: return split_plan<QD_Q8_0>(a.W.rows, units, a.batch).c > 0;
@@ -1106,9 +1129,9 @@ bool split_fits(const GemvArgs& a) {
 // accumulate without the fused norm) a split over a cluster or column ranges that fit.
 bool one_pass_fits(const GemvArgs& a) {
   const int units = (int)(a.W.cols / 32);
-  if (stages_for(a.fmt, 8, units, a.batch, a.norm_g != nullptr) >= 2) return true;
+  if (stages_for(a.fmt, 8, a.W.rows, units, a.batch, a.norm_g != nullptr) >= 2) return true;
   const bool splits = (a.mode == kGemvStore || a.mode == kGemvAccumulate) && !a.norm_g;
-  return splits && range_units(a.fmt, units, a.batch, false) > 0;
+  return splits && range_units(a.fmt, a.W.rows, units, a.batch, false) > 0;
 }
 
 // Batch rows [b0, b0 + nb) of `a` as arguments of their own: x, y and every epilogue
@@ -1153,6 +1176,7 @@ qd_status launch_args(const GemvArgs& a, cudaStream_t stream) {
   p.stages = 0;
   p.ks = 1;
   p.ksplit = 1;
+  p.pdepth = 2;
   p.accumulate = false;
   switch (a.fmt) {
     case QD_Q4_0: return launch<QD_Q4_0>(p, a.pdl, stream);
@@ -1181,7 +1205,7 @@ bool gemv_mma_supported(const GemvArgs& a) {
     if (a.W.rows & 1) return false;
   }
   if (a.batch <= 8) return one_pass_fits(a);
-  const int units_ok = stages_for(a.fmt, 8, units, a.batch, a.norm_g != nullptr) >= 2;
+  const int units_ok = stages_for(a.fmt, 8, a.W.rows, units, a.batch, a.norm_g != nullptr) >= 2;
   if (units_ok || split_fits(a)) return true;
   if (a.fmt == QD_I8_ROW) return false;
   return one_pass_fits(row_slice(a, 0, 8)) && one_pass_fits(row_slice(a, 8, a.batch - 8));
@@ -1191,7 +1215,7 @@ qd_status launch_q_gemv_mma(const GemvArgs& a, cudaStream_t stream) {
   using namespace mma_gemv;
   if (!gemv_mma_supported(a)) return QD_ERR_UNSUPPORTED;
   const int units = (int)(a.W.cols / 32);
-  if (a.batch <= 8 || stages_for(a.fmt, 8, units, a.batch, a.norm_g != nullptr) >= 2 || split_fits(a))
+  if (a.batch <= 8 || stages_for(a.fmt, 8, a.W.rows, units, a.batch, a.norm_g != nullptr) >= 2 || split_fits(a))
     return launch_args(a, stream);
   // two passes of up to 8 batch rows, the second a programmatic dependent of the first
   const qd_status st = launch_args(row_slice(a, 0, 8), stream);
