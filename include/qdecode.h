@@ -209,11 +209,13 @@ qd_status qd_quantize_i4_rows(const uint16_t* w_bf16, int64_t rows, int64_t cols
 /* or INT8 rows runs on the tensor cores instead: codes exact in binary16, x   */
 /* per 256-element stage scaled by a power of two and split into two binary16 */
 /* parts (at most 2^-22 of the stage's largest |x| per element), products     */
-/* summed in f32; x rows wider than the shared memory holds run as several    */
-/* launches over column ranges, added in a fixed order, or (batch 9-16) as two */
-/* passes of up to 8 batch rows.  Batch 9-16 INT8 rows whose x does not fit   */
-/* run on the 5th-generation tensor cores (the same split of x).  A non-finite */
-/* x gives NaN in its batch row.                                               */
+/* summed in f32; x rows wider than one CTA's shared memory holds split their */
+/* columns over a thread-block cluster (partial sums added in a fixed order), */
+/* or run as several launches over column ranges (added in a fixed order), or */
+/* (batch 9-16) as two passes of up to 8 batch rows.  Batch 9-16 INT8 rows    */
+/* that fit none of these run on the 5th-generation tensor cores (the same    */
+/* split of x).  Results are the same bits on every run.  A non-finite x      */
+/* gives NaN in its batch row.                                                 */
 /* ------------------------------------------------------------------------- */
 size_t qd_q_gemv_workspace(qd_fmt fmt, int64_t rows, int64_t cols, int batch);
 qd_status qd_q_gemv(qd_fmt fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch,
