@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(W * 32, 1) k_gemv_mma(const Params p) {
   const float* gs = reinterpret_cast<const float*>(smem + L.gs);
   float* sxs = reinterpret_cast<float*>(smem + L.sx);   // [x group][16] x scales
   float* ssq = reinterpret_cast<float*>(smem + L.ssq);  // [x group][16] sums of squares
-  float* partial = reinterpret_cast<float*>(smem + L.partial);  // [2][warps][32][4]
+  float* partial = reinterpret_cast<float*>(smem + L.partial);  // [pdepth][warps][32][NC][4]
   const uint32_t bar = tc::smem_u32(smem + L.bar);
 
   if (threadIdx.x == 0) {
